@@ -1,0 +1,159 @@
+"""Iteration-level FCFS scheduling (Orca Algorithm 1) with n_workers = 1.
+
+Algorithm 1 ("ORCA scheduling algorithm", Orca walk-through, section
+"两个约束：max batch size 与 GPU 显存"): Select drops RUNNING requests, sorts
+the rest by arrival, takes at most max_bs of them, and reserves max_tokens
+K/V slots for each INITIATION request; when a reservation would exceed
+n_slots it stops selecting (break, never skip: skipping would break FCFS).
+The main loop marks the batch RUNNING, runs one iteration, marks the
+returned requests INCREMENT and releases max_tokens for finished ones.
+
+Readings where the extracted text is garbled:
+* the per-request batch insertion applies to every non-RUNNING request,
+  INCREMENT included (the notes' select_batch sketch appends every request;
+  the walk-through's indentation puts it inside the INITIATION branch);
+* with one worker each batch returns before the next Select;
+* ties in arrival are broken by request id;
+* a request is finished when it has generated out_len tokens (no EOS, per
+  the evaluation setup) or prompt + generated >= max_tokens;
+* the slot pool gives each request one contiguous segment, first fit at the
+  lowest base; a reservation that passes the count rule but finds no hole
+  fails like a count failure (break).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional, Tuple
+
+INITIATION, INCREMENT, RUNNING, FINISHED = 0, 1, 2, 3
+
+
+class SlotPool:
+    """Contiguous K/V slot reservations over [0, n_slots)."""
+
+    def __init__(self, n_slots: int):
+        self.n_slots = n_slots
+        self.n_rsrv = 0
+        self.free: List[Tuple[int, int]] = [(0, n_slots)] if n_slots > 0 else []  # (base, length)
+        self.owned: Dict[int, Tuple[int, int]] = {}
+        self.frag_blocks = 0
+
+    def reserve(self, req_id: int, n: int) -> Optional[int]:
+        if n <= 0 or req_id in self.owned:
+            raise ValueError("invalid reservation")
+        if self.n_rsrv + n > self.n_slots:
+            return None
+        for i, (base, length) in enumerate(self.free):
+            if length >= n:
+                if length == n:
+                    del self.free[i]
+                else:
+                    self.free[i] = (base + n, length - n)
+                self.owned[req_id] = (base, n)
+                self.n_rsrv += n
+                return base
+        self.frag_blocks += 1
+        return None
+
+    def release(self, req_id: int) -> None:
+        if req_id not in self.owned:
+            raise KeyError(req_id)
+        base, n = self.owned.pop(req_id)
+        self.n_rsrv -= n
+        self.free.append((base, n))
+        self.free.sort()
+        merged: List[Tuple[int, int]] = []
+        for b, l in self.free:
+            if merged and merged[-1][0] + merged[-1][1] == b:
+                merged[-1] = (merged[-1][0], merged[-1][1] + l)
+            else:
+                merged.append((b, l))
+        self.free = merged
+
+
+@dataclasses.dataclass
+class ReqState:
+    req_id: int
+    arrival: int
+    n_prompt: int
+    out_len: int
+    max_tokens: int
+    state: int = INITIATION
+    n_cached: int = 0
+    n_generated: int = 0
+    slot_base: int = -1
+
+
+def select(pool: List[ReqState], slots: SlotPool, max_bs: int) -> List[ReqState]:
+    """Algorithm 1 Select over the arrived, unfinished requests."""
+    cands = sorted((r for r in pool if r.state in (INITIATION, INCREMENT)),
+                   key=lambda r: (r.arrival, r.req_id))
+    batch: List[ReqState] = []
+    for r in cands:
+        if len(batch) == max_bs:
+            break
+        if r.state == INITIATION:
+            base = slots.reserve(r.req_id, r.max_tokens)
+            if base is None:
+                break
+            r.slot_base = base
+        batch.append(r)
+    return batch
+
+
+def finished(r: ReqState) -> bool:
+    return r.n_generated >= r.out_len or r.n_prompt + r.n_generated >= r.max_tokens
+
+
+@dataclasses.dataclass
+class IterRecord:
+    it: int
+    req_ids: List[int]
+    n_new: List[int]        # L_i: prompt length for a prefill, 1 for a decode
+    n_ctx: List[int]        # c_i: tokens cached before this iteration
+    slot_base: List[int]
+    released: List[int]
+
+
+def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000) -> List[IterRecord]:
+    """Drive Algorithm 1 over a trace whose arrivals are iteration indices.
+
+    A request whose arrival is t can be selected at iteration t.  When no
+    request is in the pool the clock jumps to the next arrival (no iteration
+    is run).  Raises RuntimeError if the pool is non-empty but nothing can
+    ever be selected (a head request larger than n_slots)."""
+    order = sorted(trace, key=lambda r: (r.arrival, r.req_id))
+    states = [ReqState(r.req_id, r.arrival, r.n_prompt, r.out_len, r.max_tokens) for r in order]
+    slots = SlotPool(n_slots)
+    pool: List[ReqState] = []
+    nxt = 0
+    it = 0
+    records: List[IterRecord] = []
+    while nxt < len(states) or pool:
+        if not pool and states[nxt].arrival > it:
+            it = states[nxt].arrival
+        while nxt < len(states) and states[nxt].arrival <= it:
+            pool.append(states[nxt])
+            nxt += 1
+        batch = select(pool, slots, max_bs)
+        if not batch:
+            raise RuntimeError(f"no request can be scheduled at iteration {it}")
+        rec = IterRecord(it, [r.req_id for r in batch],
+                         [r.n_prompt if r.state == INITIATION else 1 for r in batch],
+                         [r.n_cached for r in batch], [r.slot_base for r in batch], [])
+        for r in batch:
+            r.state = RUNNING
+        for r, n_new in zip(batch, rec.n_new):
+            r.state = INCREMENT
+            r.n_cached += n_new
+            r.n_generated += 1
+            if finished(r):
+                r.state = FINISHED
+                slots.release(r.req_id)
+                rec.released.append(r.req_id)
+        pool = [r for r in pool if r.state != FINISHED]
+        records.append(rec)
+        it += 1
+        if len(records) > max_iters:
+            raise RuntimeError("iteration limit")
+    return records
