@@ -1,0 +1,373 @@
+#!/usr/bin/env python3
+"""Throughput of selectively batched iterations on one GB300 (or N replicas).
+
+Workload (default): a GPT-2-small-shaped bf16 decoder (12 layers, H=768,
+12 heads, vocab 50257, random-init N(0, 0.02) weights) serving a synthetic
+trace of 64 requests - prompts U{32..512}, outputs U{1..256}, max_tokens =
+prompt + 256, Poisson arrivals (0.5 per iteration), no EOS - with
+iteration-level scheduling (max_bs 64, K/V slots sized to 40 GB).  One step
+is one selectively batched iteration: Select, the ragged descriptor, the
+whole forward over the [sum L_i, H] rows, the LM head on each request's last
+row, greedy argmax and the post-iteration update.  When the trace completes
+it restarts (every request fresh, all slots released).
+
+value  = processed tokens (sum L_i) per second over the K timed iterations,
+         CUDA events on the iteration stream around the timed region;
+e2e    = the same through the C ABI with host request buffers, wall clock
+         (host scheduling, descriptor H2D and token D2H included).
+The roofline object describes the dominant kernel, timed per launch with CUDA
+events in a second, profiled pass over the same iterations.
+
+--impl reference times the CPU oracle (per-request, token-at-a-time
+generation in float64) on the same trace and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "tokens/s per selective-batched iteration at 1 GB300; % of HBM/tensor roofline"
+UNIT = "tokens/s"
+WORKLOAD = "gpt2-small bf16, 64-request Poisson trace (prompt U32-512, out U1-256, max_tokens=prompt+256), max_bs 64"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def trace_for(rank: int, gen: int = 0):
+    shape = synth.GPT2_SMALL
+    return synth.make_trace(64, (32, 512), (1, 256), vocab=shape.vocab, seed=1000 * rank + gen,
+                            rate_per_iter=0.5, max_extra=256)
+
+
+def n_slots_for(shape) -> int:
+    return int(40e9 // (shape.n_layers * 2 * shape.hidden * 2))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "iteration_level_selective_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+def cpu_oracle_sample(budget_s: float, rank: int = 0):
+    """The oracle as it stands, on the benchmark trace: requests in arrival
+    order, each generated alone token by token, until the time budget is
+    spent.  Returns (tokens processed, seconds, description)."""
+    from oracle import model as omodel
+    shape = synth.GPT2_SMALL
+    w = synth.make_weights(shape, seed=0)
+    orc = omodel.GPTOracle(shape, w)
+    trace = sorted(trace_for(rank), key=lambda r: (r.arrival, r.req_id))
+    n_tok, n_req = 0, 0
+    t0 = time.perf_counter()
+    for req in trace:
+        cache = orc.new_cache(req.n_prompt + req.out_len)
+        last = None
+        for t, tok in enumerate(req.prompt):
+            last = orc.step(cache, int(tok), t, want_logits=(t == req.n_prompt - 1))
+            n_tok += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        else:
+            for k in range(1, req.out_len):
+                tok = int(np.argmax(last))
+                last = orc.step(cache, tok, req.n_prompt + k - 1)
+                n_tok += 1
+                if time.perf_counter() - t0 > budget_s:
+                    break
+        n_req += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n_tok, dt, (f"oracle (float64 numpy, token-at-a-time) on the first {n_req} request(s) of the trace: "
+                       f"{n_tok} tokens in {dt:.1f} s")
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return 0
+    # each step: the oracle processes a bounded sample of 4 token rows of the trace
+    from oracle import model as omodel
+    shape = synth.GPT2_SMALL
+    w = synth.make_weights(shape, seed=0)
+    orc = omodel.GPTOracle(shape, w)
+    trace = sorted(trace_for(0), key=lambda r: (r.arrival, r.req_id))
+    state = {"req": 0, "t": 0, "cache": None, "last": None}
+
+    def one_row():
+        req = trace[state["req"] % len(trace)]
+        if state["cache"] is None:
+            state["cache"] = orc.new_cache(req.n_prompt + req.out_len)
+            state["t"] = 0
+        t = state["t"]
+        tok = int(req.prompt[t]) if t < req.n_prompt else int(np.argmax(state["last"]))
+        state["last"] = orc.step(state["cache"], tok, t, want_logits=(t >= req.n_prompt - 1))
+        state["t"] += 1
+        if state["t"] >= req.n_prompt + req.out_len - 1:
+            state["req"] += 1
+            state["cache"] = None
+
+    rows_per_step = 4
+    for _ in range(args.warmup):
+        for _ in range(rows_per_step):
+            one_row()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for _ in range(rows_per_step):
+            one_row()
+    dt = time.perf_counter() - t0
+    value = rows_per_step * args.steps / dt
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "step": f"{rows_per_step} token rows"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{rows_per_step * args.steps} token rows of the trace, token-at-a-time"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+    from iteration_level_selective_gb300 import _orca as C
+    from iteration_level_selective_gb300 import build as B
+    from iteration_level_selective_gb300 import runtime as rt
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    shape = synth.GPT2_SMALL
+    host_w = synth.make_weights(shape, seed=0)
+    weights = rt.DeviceWeights(shape, dev, host=host_w)
+    del host_w
+    n_slots = n_slots_for(shape)
+    eng = rt.Engine(shape, weights, max_bs=64, n_slots=n_slots, max_rows=64 * 512, device=dev)
+    stream = torch.cuda.Stream(dev)
+    gen = [0]
+
+    def new_loop():
+        gen[0] += 1
+        return rt.ServingLoop(eng, rt.RequestPool(trace_for(rank, gen[0])), stream=stream)
+
+    loop = new_loop()
+
+    def step():
+        nonlocal loop
+        if loop.done():
+            loop = new_loop()
+        rec = loop.step()
+        h2d, d2h, _ = C.orca_last_transfer(eng.handle)
+        return rec, h2d, d2h
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(local)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rows = gen_tok = done = h2d = d2h = 0
+    torch.cuda.synchronize(dev)
+    w0 = time.perf_counter()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        rec, hb, db = step()
+        rows += sum(rec.n_new)
+        gen_tok += len(rec.req_ids)
+        done += len(rec.released)
+        h2d += hb
+        d2h += db
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - w0
+    clocks = sampler.stop()
+    dev_s = ev0.elapsed_time(ev1) / 1000.0
+    if world > 1:
+        t = torch.tensor([dev_s, wall], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_s, wall = t.tolist()
+        c = torch.tensor([rows, gen_tok, done, h2d, d2h], device=dev, dtype=torch.float64)
+        dist.all_reduce(c, op=dist.ReduceOp.SUM)
+        rows, gen_tok, done, h2d, d2h = c.tolist()
+
+    # profiled pass: per-launch CUDA events around every kernel, same workload
+    C.orca_profile_enable(eng.handle, True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    stats = {C.KERNEL_NAMES[k]: C.orca_profile_read(eng.handle, k) for k in range(C.ORCA_K_COUNT)}
+    C.orca_profile_enable(eng.handle, False)
+    kernels = {
+        "gemm_tc_bf16": [stats[n] for n in ("gemm_qkv", "gemm_o", "gemm_fc1", "gemm_fc2", "lm_head")],
+        "attention": [stats["attention"]],
+        "layernorm": [stats["layernorm"]],
+        "embed": [stats["embed"]],
+        "argmax": [stats["argmax"]],
+    }
+    agg = {}
+    for k, lst in kernels.items():
+        agg[k] = {"launches": sum(s["launches"] for s in lst), "ms": sum(s["total_ms"] for s in lst),
+                  "flops": sum(s["flops"] for s in lst), "bytes": sum(s["bytes"] for s in lst)}
+    total_ms = sum(a["ms"] for a in agg.values()) or 1.0
+    dom = max(agg, key=lambda k: agg[k]["ms"])
+    a = agg[dom]
+    peaks, peak_src = load_peaks()
+    balance = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if a["bytes"] > 0 and a["flops"] / a["bytes"] > balance:
+        achieved = a["flops"] / (a["ms"] / 1000.0) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    else:
+        achieved = a["bytes"] / (a["ms"] / 1000.0) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    tr = measured_traffic(dom)
+    roof["traffic"] = tr
+    roof["kernel"] = dom
+    roof["peak_source"] = peak_src + (" sustained bf16" if roof["bound"] == "tensor" else " copy bandwidth")
+    roof["launches"] = a["launches"]
+    roof["algorithmic_per_launch"] = (a["flops"] if roof["bound"] == "tensor" else a["bytes"]) / max(1, a["launches"])
+    launches_per_iter = 4 + 7 * shape.n_layers
+    value = rows / dev_s
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": 1000.0 * dev_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "model": "gpt2-small-shaped (12L, H768, 12 heads, V50257), random init",
+                   "max_bs": 64, "n_slots": n_slots, "arrivals": "Poisson 0.5 per iteration",
+                   "l2": "inputs larger than L2 (0.25 GB weights + K/V pool), no flush",
+                   "parallelism": f"replicas x{world}"},
+        "generated_tokens_per_s": gen_tok / dev_s,
+        "completed_requests_per_s": done / dev_s,
+        "e2e": {"value": rows / wall, "unit": UNIT, "h2d_bytes_per_step": h2d / args.steps / max(1, world),
+                "d2h_bytes_per_step": d2h / args.steps / max(1, world)},
+        "gpu_launches": launches_per_iter * args.steps * world,
+        "roofline": roof,
+        "kernel_time_share": {k: round(v["ms"] / total_ms, 4) for k, v in agg.items()},
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_tok, dt, desc = cpu_oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": n_tok / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    eng.close()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        rc = run_reference(args, rank, world)
+    else:
+        rc = run_ours(args, rank, world)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

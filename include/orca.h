@@ -1,0 +1,251 @@
+/*
+ * orca.h - C ABI of liborca: one selectively batched Transformer iteration
+ * (Orca-style iteration-level scheduling + selective batching) on one GPU.
+ *
+ * Passages this interface follows (page title, section):
+ *   - "连续批处理完全拆解：Orca 的迭代级调度与选择性批处理" (Orca walk-through):
+ *       Algorithm 1 "ORCA scheduling algorithm" (Select, max_bs, n_slots,
+ *       max_tokens reservation, break on overflow); Figure 5 (flatten the
+ *       batch to [sum L_i, H], Split before attention, per-request attention
+ *       against the Attention K/V manager, Merge after it).
+ *   - CS349D Lecture 2 "批处理与调度", section 4.3 (reservation rule) and
+ *       section 5.1 (try_admit / free memory-manager interface).
+ *   - "Orca: The beginning of Morden LLM serving." notes, section "Scheduling
+ *       Algorithm" (select_batch sketch).
+ *
+ * Conventions for every call:
+ *   - Return 0 (ORCA_OK) or a negative ORCA_E* code.  No exception, abort or
+ *     exit crosses this boundary.  orca_last_error() gives a message.
+ *   - Device pointers are owned by the caller (the library never frees or
+ *     allocates device memory; it allocates only pinned host staging buffers
+ *     and CUDA events).  Host pointers are borrowed for the duration of a call,
+ *     except orca_request.tokens, which must stay valid while the request is
+ *     in a pool passed to orca_select_batch / orca_iteration.
+ *   - An engine is not thread-safe; one host thread drives one engine.
+ *   - Streams are passed as a cudaStream_t cast to void* (NULL = legacy
+ *     default stream).
+ */
+#ifndef ORCA_H_
+#define ORCA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- codes */
+#define ORCA_OK 0
+#define ORCA_EINVAL (-1)          /* bad argument, shape or state            */
+#define ORCA_ENOSLOTS (-2)        /* reservation exceeds n_slots or no hole  */
+#define ORCA_EBATCH (-3)          /* n_batch > max_bs or sum L_i > max_rows  */
+#define ORCA_EUNKNOWN_REQ (-4)    /* release of an id that never reserved    */
+#define ORCA_EDOUBLE_RELEASE (-5) /* release of an id already released       */
+#define ORCA_EDEVICE (-6)         /* a kernel raised its device status word  */
+#define ORCA_ECUDA (-7)           /* a CUDA runtime call failed              */
+#define ORCA_ESTATE (-8)          /* engine has no device side (host-only)   */
+
+#define ORCA_DTYPE_F32 0
+#define ORCA_DTYPE_BF16 1
+
+/* request states (Algorithm 1) */
+#define ORCA_INITIATION 0
+#define ORCA_INCREMENT 1
+#define ORCA_RUNNING 2
+#define ORCA_FINISHED 3
+
+/* orca_iteration flags */
+#define ORCA_ITER_TEACHER_FORCE 1 /* read every input token from req.tokens;
+                                     never write generated tokens into it   */
+
+/* ---------------------------------------------------------------- types */
+typedef struct orca_engine orca_engine;
+
+/* Model shape and scheduler parameters.
+ *   GPT decoder: n_layers blocks of hidden size `hidden`, n_heads heads
+ *   (head_dim = hidden / n_heads), MLP width `ffn`, vocabulary `vocab`,
+ *   learned positions 0..max_pos-1.
+ *   dtype: ORCA_DTYPE_F32 (all fp32) or ORCA_DTYPE_BF16 (matrices,
+ *   embeddings, K/V slots and stored activations bf16; residual stream,
+ *   LayerNorm statistics, accumulation and logits fp32).
+ *   max_bs, n_slots: Algorithm 1 parameters.  n_slots < 2^31.
+ *   max_rows: capacity for sum L_i of one iteration.
+ *   bf16 requires hidden % 64 == 0 and ffn % 64 == 0; every dtype requires
+ *   head_dim in {16, 32, 64, 128}. */
+typedef struct {
+  int32_t n_layers, hidden, n_heads, ffn, vocab, max_pos;
+  int32_t dtype;
+  int32_t max_bs;
+  int64_t n_slots;
+  int32_t max_rows;
+  int32_t reserved0;
+} orca_config;
+
+/* One request of the pool (host memory, owned by the caller).
+ *   arrival, req_id: Select sorts by (arrival, req_id) ascending.
+ *   state: ORCA_INITIATION until first scheduled; Select sets RUNNING,
+ *   orca_iteration sets INCREMENT or FINISHED.
+ *   n_prompt: prompt tokens; out_len: tokens to generate (no EOS);
+ *   max_tokens: K/V slots reserved at first schedule (>= n_prompt).
+ *   n_cached: tokens whose K/V are stored; n_generated: tokens produced.
+ *   slot_base: first reserved slot (-1 before reservation).
+ *   tokens: host int32 buffer of capacity n_prompt + out_len holding the
+ *   prompt followed by the generated (or teacher-forced) tokens.
+ * A request finishes when n_generated == out_len or
+ * n_prompt + n_generated >= max_tokens; its slots are then released. */
+typedef struct {
+  int64_t req_id;
+  int64_t arrival;
+  int32_t state;
+  int32_t n_prompt;
+  int32_t max_tokens;
+  int32_t out_len;
+  int32_t n_cached;
+  int32_t n_generated;
+  int64_t slot_base;
+  int32_t *tokens;
+} orca_request;
+
+/* Per-kernel-class timing gathered when profiling is enabled. */
+typedef struct {
+  int64_t launches;
+  double total_ms;     /* sum of CUDA-event durations of the launches      */
+  double flops;        /* algorithmic FLOPs of those launches              */
+  double bytes;        /* algorithmic HBM bytes of those launches          */
+} orca_kernel_stats;
+
+#define ORCA_K_EMBED 0
+#define ORCA_K_LAYERNORM 1
+#define ORCA_K_GEMM_QKV 2
+#define ORCA_K_ATTENTION 3
+#define ORCA_K_GEMM_O 4
+#define ORCA_K_GEMM_FC1 5
+#define ORCA_K_GEMM_FC2 6
+#define ORCA_K_LM_HEAD 7
+#define ORCA_K_ARGMAX 8
+#define ORCA_K_COUNT 9
+
+/* ---------------------------------------------------------------- sizing */
+/* Bytes of the K/V slot pool: n_layers * 2 * n_slots * hidden * elem.
+ * Layout (row-major): [n_layers][2 (K,V)][n_heads][n_slots][head_dim];
+ * slot s of a request holds the K/V of its token at position s - slot_base. */
+int orca_kv_pool_bytes(const orca_config *cfg, size_t *bytes);
+
+/* Bytes of device workspace orca_engine_create needs (activations, the
+ * device batch descriptor, attention scratch, logits). */
+int orca_workspace_bytes(const orca_config *cfg, size_t *bytes);
+
+/* Number of weight pointers orca_engine_create expects: 4 + 12 * n_layers.
+ * Order: tok_emb [vocab, hidden], pos_emb [max_pos, hidden], lnf_g [hidden],
+ * lnf_b [hidden], then per layer: ln1_g, ln1_b, w_qkv [3H, H], b_qkv [3H],
+ * w_o [H, H], b_o [H], ln2_g, ln2_b, w_fc1 [ffn, H], b_fc1 [ffn],
+ * w_fc2 [H, ffn], b_fc2 [H].  Matrices are [out, in] row-major; y = W x + b.
+ * Matrices and embeddings are in cfg.dtype; LayerNorm parameters and biases
+ * are fp32.  Every pointer must be 16-byte aligned. */
+int orca_weight_count(const orca_config *cfg, int32_t *count);
+
+/* ---------------------------------------------------------------- engine */
+/* Create an engine.  weights: n_weights device pointers (see
+ * orca_weight_count); kv_pool: device memory of kv_bytes >=
+ * orca_kv_pool_bytes; workspace: device memory of ws_bytes >=
+ * orca_workspace_bytes, 256-byte aligned.  All three stay owned by the
+ * caller and must outlive the engine.  Passing weights = kv_pool =
+ * workspace = NULL creates a host-only engine (scheduler and slot pool
+ * only; orca_iteration then returns ORCA_ESTATE) that makes no CUDA call.
+ * The current CUDA device at creation is the engine's device. */
+int orca_engine_create(const orca_config *cfg, const void *const *weights, int32_t n_weights,
+                       void *kv_pool, size_t kv_bytes, void *workspace, size_t ws_bytes,
+                       orca_engine **out);
+int orca_engine_destroy(orca_engine *eng);
+
+/* ---------------------------------------------------------------- K/V slots */
+/* Reserve n_tokens contiguous slots for req_id (Algorithm 1: max_tokens per
+ * request, kept until the request finishes).  First fit at the lowest free
+ * base.  ORCA_ENOSLOTS if n_rsrv + n_tokens > n_slots or no contiguous hole
+ * is large enough; ORCA_EINVAL if n_tokens <= 0 or req_id already holds a
+ * reservation. */
+int orca_kv_reserve(orca_engine *eng, int64_t req_id, int32_t n_tokens, int64_t *slot_base);
+/* Release req_id's slots.  ORCA_EDOUBLE_RELEASE if already released,
+ * ORCA_EUNKNOWN_REQ if it never reserved. */
+int orca_kv_release(orca_engine *eng, int64_t req_id);
+/* n_rsrv: reserved slots; n_free_blocks: holes in the free list;
+ * frag_blocks: reservations that passed the count rule but found no hole. */
+int orca_kv_stats(const orca_engine *eng, int64_t *n_rsrv, int64_t *n_free_blocks,
+                  int64_t *frag_blocks);
+
+/* ---------------------------------------------------------------- scheduling */
+/* Algorithm 1 Select over pool[0..n_pool): skip RUNNING and FINISHED
+ * requests, sort the rest by (arrival, req_id), take at most max_bs; an
+ * INITIATION request first reserves max_tokens slots (slot_base is set),
+ * and a failed reservation ends the selection (no skipping).  Selected
+ * requests become RUNNING.  batch_idx (capacity max_bs) receives pool
+ * indices in batch order; *n_batch their count (0 is valid). */
+int orca_select_batch(orca_engine *eng, orca_request *pool, int32_t n_pool, int32_t *batch_idx,
+                      int32_t *n_batch);
+
+/* Run one selectively batched iteration for pool[batch_idx[0..n_batch)]
+ * (all RUNNING) on `stream`, then wait for it.  Request i contributes
+ * L_i = n_prompt - n_cached rows when n_cached < n_prompt (prefill) and
+ * one row otherwise (decode); its rows carry tokens[n_cached + j] at
+ * positions n_cached + j.  Rows are flattened in batch order (Figure 5).
+ * next_tokens (host, capacity n_batch) receives each request's greedy
+ * token (argmax of the last row's logits, lowest index on ties).
+ * logits_dev, if not NULL, receives fp32 [n_batch, vocab] logits.
+ * Afterwards each request is INCREMENT (or FINISHED, slots released),
+ * n_cached += L_i, n_generated += 1, and, unless ORCA_ITER_TEACHER_FORCE,
+ * the token is appended to tokens[].  On error no request is modified. */
+int orca_iteration(orca_engine *eng, orca_request *pool, const int32_t *batch_idx, int32_t n_batch,
+                   int32_t flags, int32_t *next_tokens, float *logits_dev, void *stream);
+
+/* Host copy of the last iteration's ragged descriptor: row_off[n_batch+1],
+ * per-row position row_pos[n_rows] and K/V slot row_slot[n_rows], and
+ * last_row[n_batch].  Any output may be NULL. */
+int orca_last_descriptor(const orca_engine *eng, int32_t *n_batch, int32_t *n_rows,
+                         int32_t *row_off, int32_t *row_pos, int32_t *row_slot,
+                         int32_t *last_row, int32_t capacity);
+
+/* Bytes the last orca_iteration copied host->device (ragged descriptor:
+ * request, row and attention work records) and device->host (status word
+ * and greedy tokens), and its attention work-item count. */
+int orca_last_transfer(const orca_engine *eng, int64_t *h2d_bytes, int64_t *d2h_bytes, int32_t *n_work);
+
+/* ---------------------------------------------------------------- kernels */
+/* Greedy choice over forced logits: out_dev[r] = argmax_c logits_dev[r, c]
+ * (lowest index among equal maxima; NaN never wins).  Device pointers;
+ * enqueued on `stream`, not synchronised. */
+int orca_argmax_rows(const float *logits_dev, int32_t n_rows, int32_t vocab, int32_t *out_dev,
+                     void *stream);
+
+/* The token-wise Linear of Figure 5 on its own - the kernel orca_iteration
+ * runs for the QKV, Attn-Out and MLP Linears - exposed for tests and
+ * benchmarks:  out[m, n] = f(sum_k A[m, k] W[n, k] + bias[n]),
+ *   A [M, K], W [N, K] row-major in `dtype` (device pointers),
+ *   bias [N] fp32 device pointer or NULL,
+ *   mode ORCA_LINEAR_STORE: out[M, N] in dtype;  ORCA_LINEAR_GELU: out[M, N]
+ *   = gelu_tanh(.) in dtype;  ORCA_LINEAR_RESID: out[M, N] fp32 += (.);
+ *   ORCA_LINEAR_F32OUT: out[M, N] fp32.
+ * bf16 runs on tcgen05 tensor cores and needs K % 64 == 0 and 16-byte
+ * aligned A and W; fp32 runs CUDA-core FMA.  status_dev: device int32 that
+ * kernels OR error bits into (1 wait timeout, 2 bad index).  Enqueued on
+ * `stream`, not synchronised. */
+#define ORCA_LINEAR_STORE 0
+#define ORCA_LINEAR_GELU 1
+#define ORCA_LINEAR_RESID 2
+#define ORCA_LINEAR_F32OUT 3
+int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const float *bias, void *out,
+                int32_t M, int32_t N, int32_t K, int32_t *status_dev, void *stream);
+
+/* ---------------------------------------------------------------- profiling */
+/* enable != 0: time every launch of every kernel class with CUDA events on
+ * the iteration stream (adds event overhead); 0 disables.  Resets stats. */
+int orca_profile_enable(orca_engine *eng, int32_t enable);
+int orca_profile_read(const orca_engine *eng, int32_t kernel_class, orca_kernel_stats *out);
+
+/* Copy the last error message (NUL-terminated, truncated to n). */
+int orca_last_error(const orca_engine *eng, char *buf, size_t n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ORCA_H_ */

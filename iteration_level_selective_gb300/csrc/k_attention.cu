@@ -1,0 +1,358 @@
+// Ragged attention: every request attends only to its own K/V slots.
+//
+// Selective batching splits the flattened rows by request before attention
+// and merges them back afterwards (Orca walk-through, Figure 5: Split,
+// per-request Attention against the Attention K/V manager, Merge).  Here the
+// split and the merge are index math: one launch covers all requests, each
+// CTA takes one work item of one head and writes its rows of the [sum L_i, H]
+// output in place.  Orca stitches the thread blocks of different requests
+// into one kernel (CS349D Lecture 2, section 4.2); this launch does the same
+// for two kinds of work:
+//
+//   kind 0, query tile : up to 16 rows of one request (a prefill), causal,
+//                        K/V tiles of 32 keys staged in shared memory, online
+//                        softmax per row;
+//   kind 1, key split  : one row (a decode) over a range of at most `split`
+//                        keys, streamed from HBM with 16-byte loads, a group
+//                        of lanes per key; when a row has several splits the
+//                        partial (max, sum, acc) of each goes to scratch and
+//                        the last CTA to finish (atomic counter, no waiting)
+//                        merges them and resets the counter.
+//
+// Row r of request i sits at position c_i + (r - row_off_i) and reads keys
+// 0 .. that position (its own K/V was written by the QKV epilogue).  Scores
+// are scaled by log2(e)/sqrt(d) so the softmax uses exp2.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "orca_internal.h"
+
+namespace orca {
+namespace {
+
+template <typename T> struct Vec16;
+template <> struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const float *p, float *o) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(p));
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+};
+template <> struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void load(const __nv_bfloat16 *p, float *o) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+      o[2 * i] = f.x;
+      o[2 * i + 1] = f.y;
+    }
+  }
+};
+
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+constexpr int kThreads = 128;
+constexpr int kKeyTile = 32;
+
+template <int D>
+struct TileSmem {
+  float q[kQTile][D];
+  float k[kKeyTile][D + 1];
+  float v[kKeyTile][D];
+};
+template <int D>
+struct SplitSmem {
+  float m[kThreads / 32];
+  float l[kThreads / 32];
+  float acc[kThreads / 32][D];
+  int last;
+};
+
+// kind 0: rows r0 .. r0+cnt-1 of one request, keys 0 .. last row's position.
+template <typename T, int D>
+__device__ __forceinline__ void query_tile(const AttnArgs &a, const AttnWork &w, int head, TileSmem<D> &sm) {
+  const ReqInfo rq = a.reqs[w.req];
+  const int r0 = w.a, cnt = w.b;
+  const int pos0 = rq.ctx + (r0 - rq.row_off);
+  const int kv_len = pos0 + cnt;
+  if (rq.slot_base < 0 || (int64_t)rq.slot_base + kv_len > a.n_slots || cnt > kQTile || r0 + cnt > a.n_rows) {
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBadIndex);
+    return;
+  }
+  const T *Kp = static_cast<const T *>(a.k_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D;
+  const T *Vp = static_cast<const T *>(a.v_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D;
+  const T *Q = static_cast<const T *>(a.q);
+  for (int e = threadIdx.x; e < kQTile * D; e += kThreads) {
+    const int i = e / D, d = e - i * D;
+    sm.q[i][d] = i < cnt ? to_f(Q[(int64_t)(r0 + i) * a.hidden + head * D + d]) * a.scale_log2 : 0.f;
+  }
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int NDL = (D + 31) / 32;
+  constexpr int RPW = kQTile / (kThreads / 32);  // rows per warp
+  float m_run[RPW], l_run[RPW], acc[RPW][NDL];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    m_run[i] = -INFINITY;
+    l_run[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < NDL; ++j) acc[i][j] = 0.f;
+  }
+  constexpr int VN = Vec16<T>::N;
+  for (int t0 = 0; t0 < kv_len; t0 += kKeyTile) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kKeyTile * (D / VN); e += kThreads) {
+      const int kk = e / (D / VN), c = (e - kk * (D / VN)) * VN;
+      float kv[VN], vv[VN];
+      if (t0 + kk < kv_len) {
+        Vec16<T>::load(Kp + (int64_t)(t0 + kk) * D + c, kv);
+        Vec16<T>::load(Vp + (int64_t)(t0 + kk) * D + c, vv);
+      } else {
+#pragma unroll
+        for (int j = 0; j < VN; ++j) kv[j] = vv[j] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < VN; ++j) {
+        sm.k[kk][c + j] = kv[j];
+        sm.v[kk][c + j] = vv[j];
+      }
+    }
+    __syncthreads();
+    const int key = t0 + lane;
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      const int li = wid * RPW + i;
+      if (li >= cnt) continue;  // warp-uniform
+      const int pos = pos0 + li;
+      if (t0 > pos) continue;   // warp-uniform: whole tile is in this row's future
+      float s = -INFINITY;
+      if (key <= pos) {
+        float dot = 0.f;
+#pragma unroll 16
+        for (int d = 0; d < D; ++d) dot = fmaf(sm.q[li][d], sm.k[lane][d], dot);
+        s = dot;
+      }
+      const float mn = fmaxf(m_run[i], warp_max(s));
+      const float p = key <= pos ? exp2f(s - mn) : 0.f;
+      const float corr = exp2f(m_run[i] - mn);
+      l_run[i] = l_run[i] * corr + warp_sum(p);
+      float sum[NDL];
+#pragma unroll
+      for (int j = 0; j < NDL; ++j) sum[j] = 0.f;
+#pragma unroll 8
+      for (int kk = 0; kk < kKeyTile; ++kk) {
+        const float pk = __shfl_sync(0xffffffffu, p, kk);
+#pragma unroll
+        for (int j = 0; j < NDL; ++j) {
+          const int dim = lane + 32 * j;
+          if (dim < D) sum[j] = fmaf(pk, sm.v[kk][dim], sum[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NDL; ++j) acc[i][j] = acc[i][j] * corr + sum[j];
+      m_run[i] = mn;
+    }
+  }
+  T *O = static_cast<T *>(a.out);
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    const int li = wid * RPW + i;
+    if (li >= cnt) continue;
+    const float inv = 1.f / l_run[i];
+#pragma unroll
+    for (int j = 0; j < NDL; ++j) {
+      const int dim = lane + 32 * j;
+      if (dim < D) O[(int64_t)(r0 + li) * a.hidden + head * D + dim] = from_f<T>(acc[i][j] * inv);
+    }
+  }
+}
+
+// Merge (m2, l2, acc2) into (m, l, acc); states with m = -inf are empty.
+template <int VN>
+__device__ __forceinline__ void merge_state(float &m, float &l, float *acc, float m2, float l2, const float *acc2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;
+  const float c1 = exp2f(m - mn), c2 = exp2f(m2 - mn);
+  l = l * c1 + l2 * c2;
+#pragma unroll
+  for (int j = 0; j < VN; ++j) acc[j] = acc[j] * c1 + acc2[j] * c2;
+  m = mn;
+}
+
+// kind 1: one row over keys [split_idx * split, min(+split, pos + 1)).
+template <typename T, int D>
+__device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, int head, SplitSmem<D> &sm) {
+  constexpr int VN = Vec16<T>::N;
+  constexpr int LPK = D / VN;          // lanes per key (16 bytes each)
+  constexpr int KPW = 32 / LPK;        // keys per warp step
+  constexpr int NW = kThreads / 32;
+  const ReqInfo rq = a.reqs[w.req];
+  const int r = w.a;
+  const int pos = rq.ctx + (r - rq.row_off);
+  const int n_keys = pos + 1;
+  const int n_splits = (n_keys + a.split - 1) / a.split;
+  const int kb = w.b * a.split;
+  const int ke = min(kb + a.split, n_keys);
+  if (rq.slot_base < 0 || (int64_t)rq.slot_base + n_keys > a.n_slots || r >= a.n_rows || kb >= n_keys) {
+    if (threadIdx.x == 0) atomicOr(a.status, kStatusBadIndex);
+    return;
+  }
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane % LPK, grp = lane / LPK;
+  const T *Kp = static_cast<const T *>(a.k_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D + sub * VN;
+  const T *Vp = static_cast<const T *>(a.v_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D + sub * VN;
+  float q[VN];
+  Vec16<T>::load(static_cast<const T *>(a.q) + (int64_t)r * a.hidden + head * D + sub * VN, q);
+#pragma unroll
+  for (int j = 0; j < VN; ++j) q[j] *= a.scale_log2;
+
+  float m = -INFINITY, l = 0.f, acc[VN];
+#pragma unroll
+  for (int j = 0; j < VN; ++j) acc[j] = 0.f;
+  // Warp-uniform trip count so every lane joins the shuffles.
+#pragma unroll 2
+  for (int base = kb + wid * KPW; base < ke; base += NW * KPW) {
+    const int k = base + grp;
+    const bool valid = k < ke;
+    float kv[VN], vv[VN];
+    if (valid) {
+      Vec16<T>::load(Kp + (int64_t)k * D, kv);
+      Vec16<T>::load(Vp + (int64_t)k * D, vv);
+    } else {
+#pragma unroll
+      for (int j = 0; j < VN; ++j) kv[j] = vv[j] = 0.f;
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < VN; ++j) s = fmaf(q[j], kv[j], s);
+#pragma unroll
+    for (int o = LPK / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (valid) {
+      const float mn = fmaxf(m, s);
+      const float corr = exp2f(m - mn), p = exp2f(s - mn);
+      l = l * corr + p;
+#pragma unroll
+      for (int j = 0; j < VN; ++j) acc[j] = acc[j] * corr + p * vv[j];
+      m = mn;
+    }
+  }
+  // merge the KPW key groups of the warp
+#pragma unroll
+  for (int o = LPK; o < 32; o <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+    float acc2[VN];
+#pragma unroll
+    for (int j = 0; j < VN; ++j) acc2[j] = __shfl_xor_sync(0xffffffffu, acc[j], o);
+    merge_state<VN>(m, l, acc, m2, l2, acc2);
+  }
+  if (grp == 0) {
+#pragma unroll
+    for (int j = 0; j < VN; ++j) sm.acc[wid][sub * VN + j] = acc[j];
+    if (sub == 0) {
+      sm.m[wid] = m;
+      sm.l[wid] = l;
+    }
+  }
+  __syncthreads();
+  // merge the warps: thread `dim` owns one output dimension
+  const int dim = threadIdx.x;
+  float M = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) M = fmaxf(M, sm.m[i]);
+  float L = 0.f, A = 0.f;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    const float c = sm.m[i] == -INFINITY ? 0.f : exp2f(sm.m[i] - M);
+    L += sm.l[i] * c;
+    if (dim < D) A += sm.acc[i][dim] * c;
+  }
+  T *O = static_cast<T *>(a.out) + (int64_t)r * a.hidden + head * D;
+  if (n_splits == 1) {
+    if (dim < D) O[dim] = from_f<T>(A / L);
+    return;
+  }
+  float *part = a.part + ((int64_t)blockIdx.x * a.n_heads + head) * (D + 2);
+  if (dim < D) part[dim] = A;
+  if (dim == 0) {
+    part[D] = M;
+    part[D + 1] = L;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(a.counters + (int64_t)w.req * a.n_heads + head, 1);
+    sm.last = prev == n_splits - 1;
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+  const int w0 = blockIdx.x - w.b;  // the row's splits are consecutive work items
+  if (dim < D) {
+    float Mx = -INFINITY;
+    for (int j = 0; j < n_splits; ++j)
+      Mx = fmaxf(Mx, __ldcg(a.part + ((int64_t)(w0 + j) * a.n_heads + head) * (D + 2) + D));
+    float Lx = 0.f, Ax = 0.f;
+    for (int j = 0; j < n_splits; ++j) {
+      const float *pj = a.part + ((int64_t)(w0 + j) * a.n_heads + head) * (D + 2);
+      const float mj = __ldcg(pj + D);
+      const float c = mj == -INFINITY ? 0.f : exp2f(mj - Mx);
+      Lx += __ldcg(pj + D + 1) * c;
+      Ax += __ldcg(pj + dim) * c;
+    }
+    O[dim] = from_f<T>(Ax / Lx);
+  }
+  if (threadIdx.x == 0) a.counters[(int64_t)w.req * a.n_heads + head] = 0;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) attention_kernel(AttnArgs a) {
+  __shared__ __align__(16) unsigned char smem_raw[sizeof(TileSmem<D>) > sizeof(SplitSmem<D>) ? sizeof(TileSmem<D>)
+                                                                                             : sizeof(SplitSmem<D>)];
+  const AttnWork w = a.work[blockIdx.x];
+  const int head = blockIdx.y;
+  if (w.kind == 0)
+    query_tile<T, D>(a, w, head, *reinterpret_cast<TileSmem<D> *>(smem_raw));
+  else
+    key_split<T, D>(a, w, head, *reinterpret_cast<SplitSmem<D> *>(smem_raw));
+}
+
+template <typename T>
+cudaError_t launch_t(int head_dim, const AttnArgs &a, int n_work, cudaStream_t st) {
+  dim3 grid(n_work, a.n_heads);
+  switch (head_dim) {
+    case 16: attention_kernel<T, 16><<<grid, kThreads, 0, st>>>(a); break;
+    case 32: attention_kernel<T, 32><<<grid, kThreads, 0, st>>>(a); break;
+    case 64: attention_kernel<T, 64><<<grid, kThreads, 0, st>>>(a); break;
+    case 128: attention_kernel<T, 128><<<grid, kThreads, 0, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &a, int n_work, cudaStream_t st) {
+  if (n_work <= 0) return cudaSuccess;
+  return dtype == 1 ? launch_t<__nv_bfloat16>(head_dim, a, n_work, st) : launch_t<float>(head_dim, a, n_work, st);
+}
+
+}  // namespace orca

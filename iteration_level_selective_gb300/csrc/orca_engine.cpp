@@ -1,0 +1,780 @@
+// Host side of liborca: Algorithm 1 scheduling, the K/V slot pool, the
+// ragged batch descriptor, and the launch sequence of one selectively
+// batched iteration.  Declarations and contracts: include/orca.h.
+//
+// Passages followed (page title, section):
+//   Orca walk-through "连续批处理完全拆解", Algorithm 1 (Select with max_bs and
+//   max_tokens reservation, break on overflow; main loop state updates and
+//   release of finished requests) and Figure 5 (flatten to [sum L_i, H],
+//   per-request attention, Merge);
+//   CS349D Lecture 2, section 4.3 (reservation of max_tokens slots at the
+//   first schedule, kept until the request finishes) and section 5.1
+//   (prefill rows and decode rows of running requests in one step).
+#include "../../include/orca.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "orca_internal.h"
+
+using namespace orca;
+
+namespace {
+
+constexpr int kMinSplit = 256;   // keys per decode split, at least
+constexpr int kMaxSplits = 16;   // splits per decode row, at most
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct SlotPool {
+  int64_t n_slots = 0;
+  int64_t n_rsrv = 0;
+  int64_t frag_blocks = 0;
+  std::map<int64_t, int64_t> free_;                                   // base -> length
+  std::unordered_map<int64_t, std::pair<int64_t, int64_t>> owned;     // id -> (base, n)
+  std::unordered_set<int64_t> released;
+
+  void init(int64_t n) {
+    n_slots = n;
+    free_.clear();
+    if (n > 0) free_[0] = n;
+  }
+  int reserve(int64_t id, int64_t n, int64_t *base) {
+    if (n <= 0 || owned.count(id)) return ORCA_EINVAL;
+    if (n_rsrv + n > n_slots) return ORCA_ENOSLOTS;
+    for (auto it = free_.begin(); it != free_.end(); ++it) {
+      if (it->second >= n) {
+        const int64_t b = it->first, len = it->second;
+        free_.erase(it);
+        if (len > n) free_[b + n] = len - n;
+        owned[id] = {b, n};
+        released.erase(id);
+        n_rsrv += n;
+        *base = b;
+        return ORCA_OK;
+      }
+    }
+    ++frag_blocks;
+    return ORCA_ENOSLOTS;
+  }
+  int release(int64_t id) {
+    auto it = owned.find(id);
+    if (it == owned.end()) return released.count(id) ? ORCA_EDOUBLE_RELEASE : ORCA_EUNKNOWN_REQ;
+    int64_t b = it->second.first, n = it->second.second;
+    owned.erase(it);
+    released.insert(id);
+    n_rsrv -= n;
+    auto nx = free_.lower_bound(b);
+    if (nx != free_.end() && nx->first == b + n) {  // merge with the next hole
+      n += nx->second;
+      free_.erase(nx);
+    }
+    auto pv = free_.lower_bound(b);
+    if (pv != free_.begin()) {
+      --pv;
+      if (pv->first + pv->second == b) {  // merge with the previous hole
+        pv->second += n;
+        return ORCA_OK;
+      }
+    }
+    free_[b] = n;
+    return ORCA_OK;
+  }
+};
+
+struct Layout {  // byte offsets into the device workspace
+  size_t x, h, q, u, hf, logits, out, req, row, work, part, counters, total;
+  int max_work;
+};
+
+int elem_bytes(int dtype) { return dtype == ORCA_DTYPE_BF16 ? 2 : 4; }
+
+int check_config(const orca_config *c, std::string *why) {
+  if (!c) { *why = "config is NULL"; return ORCA_EINVAL; }
+  if (c->n_layers <= 0 || c->hidden <= 0 || c->n_heads <= 0 || c->ffn <= 0 || c->vocab <= 0 ||
+      c->max_pos <= 0 || c->max_bs <= 0 || c->max_rows <= 0 || c->n_slots <= 0) {
+    *why = "all sizes must be positive";
+    return ORCA_EINVAL;
+  }
+  if (c->dtype != ORCA_DTYPE_F32 && c->dtype != ORCA_DTYPE_BF16) { *why = "unknown dtype"; return ORCA_EINVAL; }
+  if (c->hidden % c->n_heads) { *why = "hidden must be a multiple of n_heads"; return ORCA_EINVAL; }
+  const int d = c->hidden / c->n_heads;
+  if (d != 16 && d != 32 && d != 64 && d != 128) { *why = "head_dim must be 16, 32, 64 or 128"; return ORCA_EINVAL; }
+  if (c->hidden % 4 || c->ffn % 4) { *why = "hidden and ffn must be multiples of 4"; return ORCA_EINVAL; }
+  if (c->dtype == ORCA_DTYPE_BF16 && (c->hidden % 64 || c->ffn % 64)) {
+    *why = "bf16 needs hidden and ffn multiples of 64";
+    return ORCA_EINVAL;
+  }
+  if (c->n_slots >= (int64_t)INT32_MAX) { *why = "n_slots must be < 2^31"; return ORCA_EINVAL; }
+  if (c->max_rows < c->max_bs) { *why = "max_rows must be >= max_bs"; return ORCA_EINVAL; }
+  return ORCA_OK;
+}
+
+Layout make_layout(const orca_config *c) {
+  Layout L{};
+  const size_t e = elem_bytes(c->dtype);
+  const size_t H = c->hidden, F = c->ffn, R = c->max_rows, B = c->max_bs, V = c->vocab;
+  const int d = c->hidden / c->n_heads;
+  L.max_work = (c->max_rows + kQTile - 1) / kQTile + c->max_bs + kMaxSplits * c->max_bs;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.x = take(R * H * 4);
+  L.h = take(R * H * e);
+  L.q = take(R * H * e);
+  L.u = take(R * F * e);
+  L.hf = take(B * H * e);
+  L.logits = take(B * V * 4);
+  L.out = take((B + 1) * 4);
+  L.req = take(B * sizeof(ReqInfo));
+  L.row = take(R * sizeof(RowInfo));
+  L.work = take((size_t)L.max_work * sizeof(AttnWork));
+  L.part = take((size_t)L.max_work * c->n_heads * (d + 2) * 4);
+  L.counters = take(B * c->n_heads * 4);
+  L.total = o;
+  return L;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+}  // namespace
+
+struct orca_engine {
+  orca_config cfg{};
+  bool host_only = true;
+  int device = 0;
+  int head_dim = 0;
+  std::string err;
+  SlotPool slots;
+  Layout lay{};
+  // device side (caller-owned memory)
+  std::vector<const void *> w;
+  char *kv = nullptr;
+  char *ws = nullptr;
+  // pinned host staging
+  ReqInfo *h_req = nullptr;
+  RowInfo *h_row = nullptr;
+  AttnWork *h_work = nullptr;
+  int32_t *h_out = nullptr;  // [0] status, [1..] tokens
+  // tensor maps (bf16)
+  CUtensorMap tm_h{}, tm_u{}, tm_hf{}, tm_emb{};
+  std::vector<CUtensorMap> tm_layer;  // 4 per layer: qkv, o, fc1, fc2
+  // last descriptor (host copy)
+  int32_t last_B = 0, last_N = 0, last_work = 0;
+  int64_t last_h2d = 0, last_d2h = 0;
+  std::vector<int32_t> last_row_off, last_row_pos, last_row_slot, last_last_row;
+  // profiling
+  bool prof = false;
+  orca_kernel_stats stats[ORCA_K_COUNT]{};
+  struct Pending { int cls; cudaEvent_t a, b; double flops, bytes; };
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  std::vector<Pending> pending;
+};
+
+namespace {
+
+int fail(orca_engine *e, int code, const char *fmt, ...) {
+  if (e) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    e->err = buf;
+  }
+  return code;
+}
+
+#define CUDA_TRY(eng, call)                                                                 \
+  do {                                                                                      \
+    cudaError_t _e = (call);                                                                \
+    if (_e != cudaSuccess)                                                                  \
+      return fail(eng, ORCA_ECUDA, "%s failed: %s", #call, cudaGetErrorString(_e));         \
+  } while (0)
+
+template <typename T> T *ws_ptr(orca_engine *e, size_t off) { return reinterpret_cast<T *>(e->ws + off); }
+
+int make_tmap(orca_engine *e, CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols) {
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    cudaError_t r = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (r != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(e, ORCA_ECUDA, "cuTensorMapEncodeTiled is not available");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (reinterpret_cast<uintptr_t>(base) & 15) return fail(e, ORCA_EINVAL, "TMA base must be 16-byte aligned");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)kTcBM};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(e, ORCA_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return ORCA_OK;
+}
+
+// Weight pointer index helpers (order documented in orca.h).
+enum { W_TOK = 0, W_POS = 1, W_LNF_G = 2, W_LNF_B = 3 };
+enum { L_LN1_G = 0, L_LN1_B, L_WQKV, L_BQKV, L_WO, L_BO, L_LN2_G, L_LN2_B, L_W1, L_B1, L_W2, L_B2, L_COUNT };
+inline const void *lw(const orca_engine *e, int layer, int which) { return e->w[4 + layer * L_COUNT + which]; }
+
+// ---- profiling helpers
+void prof_begin(orca_engine *e, cudaStream_t st, cudaEvent_t *a) {
+  *a = nullptr;
+  if (!e->prof) return;
+  if (e->ev_used + 2 > e->ev_pool.size()) {
+    for (int i = 0; i < 64; ++i) {
+      cudaEvent_t ev;
+      if (cudaEventCreate(&ev) != cudaSuccess) return;
+      e->ev_pool.push_back(ev);
+    }
+  }
+  *a = e->ev_pool[e->ev_used++];
+  cudaEventRecord(*a, st);
+}
+void prof_end(orca_engine *e, cudaStream_t st, cudaEvent_t a, int cls, double flops, double bytes) {
+  if (!e->prof || !a) return;
+  cudaEvent_t b = e->ev_pool[e->ev_used++];
+  cudaEventRecord(b, st);
+  e->pending.push_back({cls, a, b, flops, bytes});
+}
+void prof_collect(orca_engine *e) {
+  for (auto &p : e->pending) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+      auto &s = e->stats[p.cls];
+      s.launches += 1;
+      s.total_ms += ms;
+      s.flops += p.flops;
+      s.bytes += p.bytes;
+    }
+  }
+  e->pending.clear();
+  e->ev_used = 0;
+}
+
+}  // namespace
+
+// ======================================================================= API
+
+extern "C" {
+
+int orca_kv_pool_bytes(const orca_config *cfg, size_t *bytes) {
+  std::string why;
+  int rc = check_config(cfg, &why);
+  if (rc) return rc;
+  if (!bytes) return ORCA_EINVAL;
+  *bytes = (size_t)cfg->n_layers * 2 * (size_t)cfg->n_slots * cfg->hidden * elem_bytes(cfg->dtype);
+  return ORCA_OK;
+}
+
+int orca_workspace_bytes(const orca_config *cfg, size_t *bytes) {
+  std::string why;
+  int rc = check_config(cfg, &why);
+  if (rc) return rc;
+  if (!bytes) return ORCA_EINVAL;
+  *bytes = make_layout(cfg).total;
+  return ORCA_OK;
+}
+
+int orca_weight_count(const orca_config *cfg, int32_t *count) {
+  std::string why;
+  int rc = check_config(cfg, &why);
+  if (rc) return rc;
+  if (!count) return ORCA_EINVAL;
+  *count = 4 + L_COUNT * cfg->n_layers;
+  return ORCA_OK;
+}
+
+int orca_engine_create(const orca_config *cfg, const void *const *weights, int32_t n_weights, void *kv_pool,
+                       size_t kv_bytes, void *workspace, size_t ws_bytes, orca_engine **out) {
+  if (!out) return ORCA_EINVAL;
+  *out = nullptr;
+  std::string why;
+  int rc = check_config(cfg, &why);
+  if (rc) return rc;
+  orca_engine *e = new (std::nothrow) orca_engine();
+  if (!e) return ORCA_EINVAL;
+  e->cfg = *cfg;
+  e->head_dim = cfg->hidden / cfg->n_heads;
+  e->slots.init(cfg->n_slots);
+  e->lay = make_layout(cfg);
+  const bool any = weights || kv_pool || workspace;
+  if (!any) {  // host-only engine: scheduler and slot pool, no CUDA call
+    e->host_only = true;
+    *out = e;
+    return ORCA_OK;
+  }
+  e->host_only = false;
+  size_t need_kv = 0;
+  orca_kv_pool_bytes(cfg, &need_kv);
+  const int nw = 4 + L_COUNT * cfg->n_layers;
+  if (!weights || n_weights != nw || !kv_pool || kv_bytes < need_kv || !workspace || ws_bytes < e->lay.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) || (reinterpret_cast<uintptr_t>(kv_pool) & 15)) {
+    delete e;
+    return ORCA_EINVAL;
+  }
+  for (int i = 0; i < nw; ++i) {
+    if (!weights[i] || (reinterpret_cast<uintptr_t>(weights[i]) & 15)) {
+      delete e;
+      return ORCA_EINVAL;
+    }
+    e->w.push_back(weights[i]);
+  }
+  e->kv = static_cast<char *>(kv_pool);
+  e->ws = static_cast<char *>(workspace);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { delete e; return ORCA_ECUDA; }
+  e->device = dev;
+  const auto &L = e->lay;
+  bool ok = cudaHostAlloc(&e->h_req, sizeof(ReqInfo) * cfg->max_bs, cudaHostAllocDefault) == cudaSuccess &&
+            cudaHostAlloc(&e->h_row, sizeof(RowInfo) * cfg->max_rows, cudaHostAllocDefault) == cudaSuccess &&
+            cudaHostAlloc(&e->h_work, sizeof(AttnWork) * L.max_work, cudaHostAllocDefault) == cudaSuccess &&
+            cudaHostAlloc(&e->h_out, sizeof(int32_t) * (cfg->max_bs + 1), cudaHostAllocDefault) == cudaSuccess;
+  ok = ok && cudaMemset(e->ws + L.counters, 0, (size_t)cfg->max_bs * cfg->n_heads * 4) == cudaSuccess &&
+       cudaMemset(e->ws + L.out, 0, 4) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    orca_engine_destroy(e);
+    return ORCA_ECUDA;
+  }
+  if (cfg->dtype == ORCA_DTYPE_BF16) {
+    const uint64_t H = cfg->hidden, F = cfg->ffn;
+    e->tm_layer.resize(4 * cfg->n_layers);
+    rc = make_tmap(e, &e->tm_h, e->ws + L.h, cfg->max_rows, H);
+    if (!rc) rc = make_tmap(e, &e->tm_u, e->ws + L.u, cfg->max_rows, F);
+    if (!rc) rc = make_tmap(e, &e->tm_hf, e->ws + L.hf, cfg->max_bs, H);
+    if (!rc) rc = make_tmap(e, &e->tm_emb, e->w[W_TOK], cfg->vocab, H);
+    for (int l = 0; l < cfg->n_layers && !rc; ++l) {
+      rc = make_tmap(e, &e->tm_layer[4 * l + 0], lw(e, l, L_WQKV), 3 * H, H);
+      if (!rc) rc = make_tmap(e, &e->tm_layer[4 * l + 1], lw(e, l, L_WO), H, H);
+      if (!rc) rc = make_tmap(e, &e->tm_layer[4 * l + 2], lw(e, l, L_W1), F, H);
+      if (!rc) rc = make_tmap(e, &e->tm_layer[4 * l + 3], lw(e, l, L_W2), H, F);
+    }
+    if (rc) {
+      orca_engine_destroy(e);
+      return rc;
+    }
+  }
+  *out = e;
+  return ORCA_OK;
+}
+
+int orca_engine_destroy(orca_engine *e) {
+  if (!e) return ORCA_EINVAL;
+  if (!e->host_only) {
+    cudaFreeHost(e->h_req);
+    cudaFreeHost(e->h_row);
+    cudaFreeHost(e->h_work);
+    cudaFreeHost(e->h_out);
+    for (auto ev : e->ev_pool) cudaEventDestroy(ev);
+  }
+  delete e;
+  return ORCA_OK;
+}
+
+int orca_kv_reserve(orca_engine *e, int64_t req_id, int32_t n_tokens, int64_t *slot_base) {
+  if (!e || !slot_base) return ORCA_EINVAL;
+  int rc = e->slots.reserve(req_id, n_tokens, slot_base);
+  if (rc == ORCA_ENOSLOTS) return fail(e, rc, "cannot reserve %d slots (n_rsrv %lld of %lld)", n_tokens,
+                                       (long long)e->slots.n_rsrv, (long long)e->slots.n_slots);
+  if (rc) return fail(e, rc, "invalid reservation for request %lld", (long long)req_id);
+  return ORCA_OK;
+}
+
+int orca_kv_release(orca_engine *e, int64_t req_id) {
+  if (!e) return ORCA_EINVAL;
+  int rc = e->slots.release(req_id);
+  if (rc) return fail(e, rc, "release of request %lld: %s", (long long)req_id,
+                      rc == ORCA_EDOUBLE_RELEASE ? "already released" : "unknown request");
+  return ORCA_OK;
+}
+
+int orca_kv_stats(const orca_engine *e, int64_t *n_rsrv, int64_t *n_free_blocks, int64_t *frag_blocks) {
+  if (!e) return ORCA_EINVAL;
+  if (n_rsrv) *n_rsrv = e->slots.n_rsrv;
+  if (n_free_blocks) *n_free_blocks = (int64_t)e->slots.free_.size();
+  if (frag_blocks) *frag_blocks = e->slots.frag_blocks;
+  return ORCA_OK;
+}
+
+int orca_select_batch(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t *batch_idx, int32_t *n_batch) {
+  if (!e || !n_batch || (n_pool > 0 && (!pool || !batch_idx)) || n_pool < 0) return ORCA_EINVAL;
+  *n_batch = 0;
+  std::vector<int32_t> cand;
+  cand.reserve(n_pool);
+  for (int32_t i = 0; i < n_pool; ++i) {
+    const int s = pool[i].state;
+    if (s == ORCA_INITIATION || s == ORCA_INCREMENT) cand.push_back(i);
+    else if (s != ORCA_RUNNING && s != ORCA_FINISHED)
+      return fail(e, ORCA_EINVAL, "request %lld has unknown state %d", (long long)pool[i].req_id, s);
+  }
+  std::stable_sort(cand.begin(), cand.end(), [&](int32_t a, int32_t b) {
+    if (pool[a].arrival != pool[b].arrival) return pool[a].arrival < pool[b].arrival;
+    return pool[a].req_id < pool[b].req_id;
+  });
+  int32_t nb = 0;
+  for (int32_t idx : cand) {
+    if (nb == e->cfg.max_bs) break;
+    orca_request &r = pool[idx];
+    if (r.state == ORCA_INITIATION) {
+      if (r.max_tokens < r.n_prompt || r.n_prompt <= 0 || r.out_len <= 0)
+        return fail(e, ORCA_EINVAL, "request %lld: need 0 < n_prompt <= max_tokens and out_len > 0",
+                    (long long)r.req_id);
+      int64_t base = -1;
+      const int rc = e->slots.reserve(r.req_id, r.max_tokens, &base);
+      if (rc == ORCA_ENOSLOTS) break;  // Algorithm 1: stop selecting, never skip
+      if (rc) return fail(e, rc, "request %lld already holds a reservation", (long long)r.req_id);
+      r.slot_base = base;
+    }
+    batch_idx[nb++] = idx;
+  }
+  for (int32_t i = 0; i < nb; ++i) pool[batch_idx[i]].state = ORCA_RUNNING;
+  *n_batch = nb;
+  return ORCA_OK;
+}
+
+int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx, int32_t n_batch, int32_t flags,
+                   int32_t *next_tokens, float *logits_dev, void *stream) {
+  if (!e) return ORCA_EINVAL;
+  if (e->host_only) return fail(e, ORCA_ESTATE, "host-only engine has no device side");
+  const orca_config &c = e->cfg;
+  if (n_batch <= 0) return fail(e, ORCA_EINVAL, "empty batch");
+  if (n_batch > c.max_bs) return fail(e, ORCA_EBATCH, "n_batch %d > max_bs %d", n_batch, c.max_bs);
+  if (!pool || !batch_idx || !next_tokens) return fail(e, ORCA_EINVAL, "NULL argument");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int H = c.hidden, F = c.ffn, V = c.vocab, nh = c.n_heads, D = e->head_dim;
+  const bool bf16 = c.dtype == ORCA_DTYPE_BF16;
+  const size_t eb = elem_bytes(c.dtype);
+
+  // ---- ragged descriptor (host): rows in batch order, Figure 5
+  std::vector<int32_t> L(n_batch);
+  int32_t N = 0, max_keys = 0;
+  for (int32_t i = 0; i < n_batch; ++i) {
+    const orca_request &r = pool[batch_idx[i]];
+    if (r.state != ORCA_RUNNING) return fail(e, ORCA_EINVAL, "request %lld is not RUNNING", (long long)r.req_id);
+    if (!r.tokens || r.slot_base < 0) return fail(e, ORCA_EINVAL, "request %lld has no tokens or slots", (long long)r.req_id);
+    L[i] = r.n_cached < r.n_prompt ? r.n_prompt - r.n_cached : 1;
+    const int64_t end = (int64_t)r.n_cached + L[i];
+    if (end > r.max_tokens || end > c.max_pos || end > (int64_t)r.n_prompt + r.out_len || r.n_cached < 0)
+      return fail(e, ORCA_EINVAL, "request %lld: position %lld beyond max_tokens, max_pos or its buffer",
+                  (long long)r.req_id, (long long)end);
+    if (r.slot_base + r.max_tokens > c.n_slots)
+      return fail(e, ORCA_EINVAL, "request %lld: slots beyond n_slots", (long long)r.req_id);
+    N += L[i];
+    if (N > c.max_rows) return fail(e, ORCA_EBATCH, "sum L_i > max_rows %d", c.max_rows);
+    if (L[i] == 1) max_keys = std::max<int32_t>(max_keys, r.n_cached + 1);
+  }
+  const int split = std::max(kMinSplit, (max_keys + kMaxSplits - 1) / kMaxSplits);
+  int32_t n_work = 0;
+  int32_t row = 0;
+  for (int32_t i = 0; i < n_batch; ++i) {
+    const orca_request &r = pool[batch_idx[i]];
+    e->h_req[i] = {row, L[i], r.n_cached, (int32_t)r.slot_base};
+    for (int32_t j = 0; j < L[i]; ++j) {
+      const int32_t pos = r.n_cached + j;
+      const int32_t tok = r.tokens[pos];
+      if (tok < 0 || tok >= V) return fail(e, ORCA_EINVAL, "token id %d out of range", tok);
+      e->h_row[row + j] = {tok, pos, i, (int32_t)(r.slot_base + pos)};
+    }
+    if (L[i] == 1) {
+      const int n_keys = r.n_cached + 1;
+      const int ns = (n_keys + split - 1) / split;
+      for (int s = 0; s < ns; ++s) e->h_work[n_work++] = {1, i, row, s};
+    } else {
+      for (int t = 0; t < L[i]; t += kQTile) e->h_work[n_work++] = {0, i, row + t, std::min(kQTile, L[i] - t)};
+    }
+    row += L[i];
+  }
+  // host copy for orca_last_descriptor / orca_last_transfer
+  e->last_B = n_batch;
+  e->last_N = N;
+  e->last_work = n_work;
+  e->last_h2d = (int64_t)sizeof(ReqInfo) * n_batch + (int64_t)sizeof(RowInfo) * N + (int64_t)sizeof(AttnWork) * n_work;
+  e->last_d2h = (int64_t)sizeof(int32_t) * (n_batch + 1);
+  e->last_row_off.assign(n_batch + 1, 0);
+  e->last_last_row.resize(n_batch);
+  for (int32_t i = 0; i < n_batch; ++i) {
+    e->last_row_off[i + 1] = e->last_row_off[i] + L[i];
+    e->last_last_row[i] = e->last_row_off[i + 1] - 1;
+  }
+  e->last_row_pos.resize(N);
+  e->last_row_slot.resize(N);
+  for (int32_t r = 0; r < N; ++r) {
+    e->last_row_pos[r] = e->h_row[r].pos;
+    e->last_row_slot[r] = e->h_row[r].slot;
+  }
+
+  // ---- device work, all on `st`
+  CUDA_TRY(e, cudaSetDevice(e->device));
+  const Layout &Ly = e->lay;
+  ReqInfo *d_req = ws_ptr<ReqInfo>(e, Ly.req);
+  RowInfo *d_row = ws_ptr<RowInfo>(e, Ly.row);
+  AttnWork *d_work = ws_ptr<AttnWork>(e, Ly.work);
+  int32_t *d_out = ws_ptr<int32_t>(e, Ly.out);
+  int32_t *status = d_out;
+  float *x = ws_ptr<float>(e, Ly.x);
+  void *h = e->ws + Ly.h;
+  void *q = e->ws + Ly.q;
+  void *u = e->ws + Ly.u;
+  void *hf = e->ws + Ly.hf;
+  float *logits = logits_dev ? logits_dev : ws_ptr<float>(e, Ly.logits);
+  CUDA_TRY(e, cudaMemcpyAsync(d_req, e->h_req, sizeof(ReqInfo) * n_batch, cudaMemcpyHostToDevice, st));
+  CUDA_TRY(e, cudaMemcpyAsync(d_row, e->h_row, sizeof(RowInfo) * N, cudaMemcpyHostToDevice, st));
+  CUDA_TRY(e, cudaMemcpyAsync(d_work, e->h_work, sizeof(AttnWork) * n_work, cudaMemcpyHostToDevice, st));
+
+  cudaEvent_t ev;
+  prof_begin(e, st, &ev);
+  CUDA_TRY(e, launch_embed(c.dtype, d_row, N, e->w[W_TOK], e->w[W_POS], x, H, V, c.max_pos, status, st));
+  prof_end(e, st, ev, ORCA_K_EMBED, 0.0, (double)N * H * (2 * eb + 4));
+
+  const size_t layer_kv = (size_t)2 * nh * c.n_slots * D * eb;
+  // attention algorithmic work: unique K/V bytes, q/out bytes, QK and PV flops
+  double attn_pairs = 0.0, attn_kv_tokens = 0.0;
+  for (int32_t i = 0; i < n_batch; ++i) {
+    const double cc = pool[batch_idx[i]].n_cached, l = L[i];
+    attn_pairs += l * cc + l * (l + 1) / 2;
+    attn_kv_tokens += cc + l;
+  }
+  const double attn_flops = 4.0 * D * attn_pairs * nh;
+  const double attn_bytes = attn_kv_tokens * 2 * H * eb + 2.0 * N * H * eb;
+  auto gemm_bytes = [&](double M, double Nn, double K, double out_b) { return (M * K + Nn * K) * eb + M * Nn * out_b; };
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    char *kl = e->kv + (size_t)l * layer_kv;
+    char *vl = kl + layer_kv / 2;
+    // h = LN1(x)
+    prof_begin(e, st, &ev);
+    CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN1_G), (const float *)lw(e, l, L_LN1_B), h, N,
+                                 H, nullptr, st));
+    prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
+    // QKV Linear; K/V scattered to the requests' slots (Split)
+    EpiParams ep{};
+    ep.mode = kEpiQKV;
+    ep.ldo = H;
+    ep.bias = (const float *)lw(e, l, L_BQKV);
+    ep.out = q;
+    ep.k_layer = kl;
+    ep.v_layer = vl;
+    ep.rows = d_row;
+    ep.hidden = H;
+    ep.head_dim = D;
+    ep.n_slots = c.n_slots;
+    ep.status = status;
+    prof_begin(e, st, &ev);
+    if (bf16)
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 0], N, 3 * H, H, ep, status, st));
+    else
+      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WQKV), N, 3 * H, H, ep, st));
+    prof_end(e, st, ev, ORCA_K_GEMM_QKV, 2.0 * N * 3 * H * H, gemm_bytes(N, 3.0 * H, H, eb));
+    // ragged attention -> h (rows in place: Merge)
+    AttnArgs aa{};
+    aa.q = q;
+    aa.k_layer = kl;
+    aa.v_layer = vl;
+    aa.out = h;
+    aa.reqs = d_req;
+    aa.rows = d_row;
+    aa.work = d_work;
+    aa.part = ws_ptr<float>(e, Ly.part);
+    aa.counters = ws_ptr<int32_t>(e, Ly.counters);
+    aa.status = status;
+    aa.hidden = H;
+    aa.n_heads = nh;
+    aa.n_rows = N;
+    aa.split = split;
+    aa.n_slots = c.n_slots;
+    aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    prof_begin(e, st, &ev);
+    CUDA_TRY(e, launch_attention(c.dtype, D, aa, n_work, st));
+    prof_end(e, st, ev, ORCA_K_ATTENTION, attn_flops, attn_bytes);
+    // x += a Wo + bo
+    EpiParams eo{};
+    eo.mode = kEpiResid;
+    eo.ldo = H;
+    eo.bias = (const float *)lw(e, l, L_BO);
+    eo.out = x;
+    eo.status = status;
+    prof_begin(e, st, &ev);
+    if (bf16)
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 1], N, H, H, eo, status, st));
+    else
+      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WO), N, H, H, eo, st));
+    prof_end(e, st, ev, ORCA_K_GEMM_O, 2.0 * N * H * H, gemm_bytes(N, H, H, 8));
+    // h = LN2(x)
+    prof_begin(e, st, &ev);
+    CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN2_G), (const float *)lw(e, l, L_LN2_B), h, N,
+                                 H, nullptr, st));
+    prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
+    // u = GeLU(h W1 + b1)
+    EpiParams e1{};
+    e1.mode = kEpiGelu;
+    e1.ldo = F;
+    e1.bias = (const float *)lw(e, l, L_B1);
+    e1.out = u;
+    e1.status = status;
+    prof_begin(e, st, &ev);
+    if (bf16)
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 2], N, F, H, e1, status, st));
+    else
+      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_W1), N, F, H, e1, st));
+    prof_end(e, st, ev, ORCA_K_GEMM_FC1, 2.0 * N * F * H, gemm_bytes(N, F, H, eb));
+    // x += u W2 + b2
+    EpiParams e2{};
+    e2.mode = kEpiResid;
+    e2.ldo = H;
+    e2.bias = (const float *)lw(e, l, L_B2);
+    e2.out = x;
+    e2.status = status;
+    prof_begin(e, st, &ev);
+    if (bf16)
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_u, &e->tm_layer[4 * l + 3], N, H, F, e2, status, st));
+    else
+      CUDA_TRY(e, launch_gemm_simt_f32((const float *)u, (const float *)lw(e, l, L_W2), N, H, F, e2, st));
+    prof_end(e, st, ev, ORCA_K_GEMM_FC2, 2.0 * N * H * F, gemm_bytes(N, H, F, 8));
+  }
+  // final LayerNorm on each request's last row, LM head (tied), greedy argmax
+  prof_begin(e, st, &ev);
+  CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)e->w[W_LNF_G], (const float *)e->w[W_LNF_B], hf, n_batch, H,
+                               d_req, st));
+  prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)n_batch * H * (4 + eb));
+  EpiParams el{};
+  el.mode = kEpiLogits;
+  el.ldo = V;
+  el.bias = nullptr;
+  el.out = logits;
+  el.status = status;
+  prof_begin(e, st, &ev);
+  if (bf16)
+    CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_hf, &e->tm_emb, n_batch, V, H, el, status, st));
+  else
+    CUDA_TRY(e, launch_gemm_simt_f32((const float *)hf, (const float *)e->w[W_TOK], n_batch, V, H, el, st));
+  prof_end(e, st, ev, ORCA_K_LM_HEAD, 2.0 * n_batch * V * H, gemm_bytes(n_batch, V, H, 4));
+  prof_begin(e, st, &ev);
+  CUDA_TRY(e, launch_argmax(logits, n_batch, V, d_out + 1, st));
+  prof_end(e, st, ev, ORCA_K_ARGMAX, 0.0, (double)n_batch * V * 4);
+  CUDA_TRY(e, cudaMemcpyAsync(e->h_out, d_out, sizeof(int32_t) * (n_batch + 1), cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(e, cudaStreamSynchronize(st));
+  if (e->prof) prof_collect(e);
+  if (e->h_out[0] != 0) {
+    const int code = e->h_out[0];
+    cudaMemsetAsync(status, 0, 4, st);
+    cudaStreamSynchronize(st);
+    return fail(e, ORCA_EDEVICE, "device status word 0x%x (1 wait timeout, 2 bad index, 4 bad shape)", code);
+  }
+  // ---- Algorithm 1 main loop: returned requests become INCREMENT; finished ones release their slots
+  for (int32_t i = 0; i < n_batch; ++i) {
+    const int32_t tok = e->h_out[1 + i];
+    if (tok < 0 || tok >= V) return fail(e, ORCA_EDEVICE, "argmax produced no token (NaN logits?)");
+  }
+  for (int32_t i = 0; i < n_batch; ++i) {
+    orca_request &r = pool[batch_idx[i]];
+    const int32_t tok = e->h_out[1 + i];
+    next_tokens[i] = tok;
+    r.state = ORCA_INCREMENT;
+    r.n_cached += L[i];
+    r.n_generated += 1;
+    if (!(flags & ORCA_ITER_TEACHER_FORCE)) r.tokens[r.n_prompt + r.n_generated - 1] = tok;
+    if (r.n_generated >= r.out_len || r.n_prompt + r.n_generated >= r.max_tokens) {
+      r.state = ORCA_FINISHED;
+      e->slots.release(r.req_id);
+    }
+  }
+  return ORCA_OK;
+}
+
+int orca_last_descriptor(const orca_engine *e, int32_t *n_batch, int32_t *n_rows, int32_t *row_off, int32_t *row_pos,
+                         int32_t *row_slot, int32_t *last_row, int32_t capacity) {
+  if (!e) return ORCA_EINVAL;
+  if (n_batch) *n_batch = e->last_B;
+  if (n_rows) *n_rows = e->last_N;
+  if (capacity < e->last_N + 1 && (row_off || row_pos || row_slot || last_row)) return ORCA_EINVAL;
+  if (row_off) std::copy(e->last_row_off.begin(), e->last_row_off.end(), row_off);
+  if (row_pos) std::copy(e->last_row_pos.begin(), e->last_row_pos.end(), row_pos);
+  if (row_slot) std::copy(e->last_row_slot.begin(), e->last_row_slot.end(), row_slot);
+  if (last_row) std::copy(e->last_last_row.begin(), e->last_last_row.end(), last_row);
+  return ORCA_OK;
+}
+
+int orca_last_transfer(const orca_engine *e, int64_t *h2d_bytes, int64_t *d2h_bytes, int32_t *n_work) {
+  if (!e) return ORCA_EINVAL;
+  if (h2d_bytes) *h2d_bytes = e->last_h2d;
+  if (d2h_bytes) *d2h_bytes = e->last_d2h;
+  if (n_work) *n_work = e->last_work;
+  return ORCA_OK;
+}
+
+int orca_argmax_rows(const float *logits_dev, int32_t n_rows, int32_t vocab, int32_t *out_dev, void *stream) {
+  if (n_rows < 0 || vocab <= 0 || (n_rows > 0 && (!logits_dev || !out_dev))) return ORCA_EINVAL;
+  return launch_argmax(logits_dev, n_rows, vocab, out_dev, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ORCA_OK
+             : ORCA_ECUDA;
+}
+
+int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const float *bias, void *out, int32_t M,
+                int32_t N, int32_t K, int32_t *status_dev, void *stream) {
+  if (M < 0 || N <= 0 || K <= 0 || (M > 0 && (!A || !W || !out || !status_dev))) return ORCA_EINVAL;
+  if (dtype != ORCA_DTYPE_F32 && dtype != ORCA_DTYPE_BF16) return ORCA_EINVAL;
+  if (M == 0) return ORCA_OK;
+  EpiParams ep{};
+  switch (mode) {
+    case ORCA_LINEAR_STORE: ep.mode = kEpiStore; break;
+    case ORCA_LINEAR_GELU: ep.mode = kEpiGelu; break;
+    case ORCA_LINEAR_RESID: ep.mode = kEpiResid; break;
+    case ORCA_LINEAR_F32OUT: ep.mode = kEpiLogits; break;
+    default: return ORCA_EINVAL;
+  }
+  ep.ldo = N;
+  ep.bias = bias;
+  ep.out = out;
+  ep.status = status_dev;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == ORCA_DTYPE_F32) {
+    if (mode == ORCA_LINEAR_STORE) ep.mode = kEpiLogits;  // fp32 store
+    return launch_gemm_simt_f32(static_cast<const float *>(A), static_cast<const float *>(W), M, N, K, ep, st) ==
+                   cudaSuccess
+               ? ORCA_OK
+               : ORCA_ECUDA;
+  }
+  if (K % kTcBK) return ORCA_EINVAL;
+  CUtensorMap ta, tw;
+  if (make_tmap(nullptr, &ta, A, M, K) || make_tmap(nullptr, &tw, W, N, K)) return ORCA_EINVAL;
+  return launch_gemm_tc_bf16(&ta, &tw, M, N, K, ep, status_dev, st) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
+}
+
+int orca_profile_enable(orca_engine *e, int32_t enable) {
+  if (!e) return ORCA_EINVAL;
+  if (e->host_only && enable) return ORCA_ESTATE;
+  e->prof = enable != 0;
+  for (auto &s : e->stats) s = orca_kernel_stats{};
+  e->pending.clear();
+  e->ev_used = 0;
+  return ORCA_OK;
+}
+
+int orca_profile_read(const orca_engine *e, int32_t cls, orca_kernel_stats *out) {
+  if (!e || !out || cls < 0 || cls >= ORCA_K_COUNT) return ORCA_EINVAL;
+  *out = e->stats[cls];
+  return ORCA_OK;
+}
+
+int orca_last_error(const orca_engine *e, char *buf, size_t n) {
+  if (!e || !buf || n == 0) return ORCA_EINVAL;
+  snprintf(buf, n, "%s", e->err.c_str());
+  return ORCA_OK;
+}
+
+}  // extern "C"

@@ -10,3 +10,11 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+@pytest.fixture(scope="session")
+def liborca():
+    """Build (if stale) and load liborca.so."""
+    from iteration_level_selective_gb300 import build, _orca
+    build.build()
+    return _orca.lib()

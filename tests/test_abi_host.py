@@ -1,0 +1,170 @@
+"""C-ABI checks that need no GPU: exported symbols, host-only engine,
+Algorithm 1 Select and the slot pool, bit-exact against the oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from iteration_level_selective_gb300 import _orca as C
+from oracle import scheduler as osched
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "orca.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^int\s+(orca_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(liborca):
+    names = _declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(liborca, n), n
+    assert set(names) <= set(C.EXPORTS) | set(names)
+    assert set(C.EXPORTS) <= set(names)
+
+
+def _cfg(max_bs=4, n_slots=64, dtype=C.ORCA_DTYPE_F32):
+    return C.orca_config(n_layers=2, hidden=64, n_heads=4, ffn=256, vocab=256, max_pos=64, dtype=dtype,
+                         max_bs=max_bs, n_slots=n_slots, max_rows=64)
+
+
+def test_sizes_and_config_validation(liborca):
+    cfg = _cfg()
+    assert C.orca_kv_pool_bytes(cfg) == 2 * 2 * 64 * 64 * 4
+    assert C.orca_weight_count(cfg) == 4 + 12 * 2
+    assert C.orca_workspace_bytes(cfg) > 0
+    bad = _cfg()
+    bad.n_heads = 3
+    with pytest.raises(C.OrcaError):
+        C.orca_workspace_bytes(bad)
+    bad = _cfg(dtype=C.ORCA_DTYPE_BF16)   # hidden 64 ok, ffn 256 ok
+    C.orca_workspace_bytes(bad)
+    bad.hidden, bad.n_heads = 96, 6        # bf16 needs hidden % 64 == 0
+    with pytest.raises(C.OrcaError):
+        C.orca_workspace_bytes(bad)
+
+
+def test_host_only_engine_reserve_release_errors(liborca):
+    eng = C.orca_engine_create(_cfg(n_slots=20))
+    try:
+        assert [C.orca_kv_reserve(eng, i, 5) for i in range(3)] == [0, 5, 10]
+        C.orca_kv_release(eng, 1)
+        with pytest.raises(C.OrcaError) as ei:
+            C.orca_kv_reserve(eng, 3, 6)        # 16 <= 20 but no hole of 6
+        assert ei.value.code == C.ORCA_ENOSLOTS
+        assert C.orca_kv_stats(eng) == (10, 2, 1)
+        assert C.orca_kv_reserve(eng, 4, 5) == 5
+        with pytest.raises(C.OrcaError) as ei:
+            C.orca_kv_release(eng, 1)
+        assert ei.value.code == C.ORCA_EDOUBLE_RELEASE
+        with pytest.raises(C.OrcaError) as ei:
+            C.orca_kv_release(eng, 99)
+        assert ei.value.code == C.ORCA_EUNKNOWN_REQ
+        with pytest.raises(C.OrcaError) as ei:
+            C.orca_kv_reserve(eng, 0, 1)        # already holds a reservation
+        assert ei.value.code == C.ORCA_EINVAL
+        with pytest.raises(C.OrcaError) as ei:
+            C.orca_kv_reserve(eng, 7, 0)
+        assert ei.value.code == C.ORCA_EINVAL
+        # orca_iteration needs a device side
+        pool = (C.orca_request * 1)()
+        bi = (ctypes.c_int32 * 4)()
+        nt = (ctypes.c_int32 * 4)()
+        with pytest.raises(C.OrcaError) as ei:
+            C.orca_iteration(eng, pool, bi, 1, 0, nt)
+        assert ei.value.code == C.ORCA_ESTATE
+    finally:
+        C.orca_engine_destroy(eng)
+
+
+class _Sim:
+    """Drives the C Select and the oracle Select side by side; the test
+    applies the same post-iteration update to both."""
+
+    def __init__(self, trace, max_bs, n_slots):
+        self.trace = sorted(trace, key=lambda t: (t[1], t[0]))
+        self.eng = C.orca_engine_create(_cfg(max_bs=max_bs, n_slots=n_slots))
+        self.max_bs = max_bs
+        n = len(self.trace)
+        self.arr = (C.orca_request * n)()
+        self.bufs = []
+        for i, (rid, arrival, lp, lo, mt) in enumerate(self.trace):
+            b = np.zeros(lp + lo, dtype=np.int32)
+            self.bufs.append(b)
+            self.arr[i] = C.orca_request(req_id=rid, arrival=arrival, state=C.ORCA_INITIATION, n_prompt=lp,
+                                         max_tokens=mt, out_len=lo, n_cached=0, n_generated=0, slot_base=-1,
+                                         tokens=b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+        self.ostates = [osched.ReqState(rid, a, lp, lo, mt) for rid, a, lp, lo, mt in self.trace]
+        self.oslots = osched.SlotPool(n_slots)
+        self.bi = (ctypes.c_int32 * max_bs)()
+
+    def run(self):
+        it, n_arr, done = 0, 0, 0
+        n = len(self.trace)
+        while done < n:
+            if n_arr == done and self.trace[n_arr][1] > it:
+                it = self.trace[n_arr][1]
+            while n_arr < n and self.trace[n_arr][1] <= it:
+                n_arr += 1
+            nb = C.orca_select_batch(self.eng, self.arr, n_arr, self.bi)
+            opool = [s for s in self.ostates[:n_arr] if s.state != osched.FINISHED]
+            obatch = osched.select(opool, self.oslots, self.max_bs)
+            got = [(self.arr[self.bi[i]].req_id, self.arr[self.bi[i]].slot_base) for i in range(nb)]
+            want = [(r.req_id, r.slot_base) for r in obatch]
+            assert got == want, (it, got, want)
+            assert C.orca_kv_stats(self.eng)[0] == self.oslots.n_rsrv
+            for i in range(nb):
+                a = self.arr[self.bi[i]]
+                assert a.state == C.ORCA_RUNNING
+                L = a.n_prompt - a.n_cached if a.n_cached < a.n_prompt else 1
+                a.state, a.n_cached, a.n_generated = C.ORCA_INCREMENT, a.n_cached + L, a.n_generated + 1
+                if a.n_generated >= a.out_len or a.n_prompt + a.n_generated >= a.max_tokens:
+                    a.state = C.ORCA_FINISHED
+                    C.orca_kv_release(self.eng, a.req_id)
+                    done += 1
+            for r in obatch:
+                L = r.n_prompt if r.state == osched.INITIATION else 1
+                r.state, r.n_cached, r.n_generated = osched.INCREMENT, r.n_cached + L, r.n_generated + 1
+                if osched.finished(r):
+                    r.state = osched.FINISHED
+                    self.oslots.release(r.req_id)
+            it += 1
+        C.orca_engine_destroy(self.eng)
+        return it
+
+
+def test_select_bit_exact_vs_oracle_random_traces(liborca):
+    rng = np.random.default_rng(21)
+    for trial in range(40):
+        n = int(rng.integers(3, 60))
+        trace = []
+        for i in range(n):
+            lp, lo = int(rng.integers(1, 20)), int(rng.integers(1, 25))
+            trace.append((int(rng.permutation(1000)[i] if trial % 2 else i), int(rng.integers(0, 30)), lp, lo,
+                          lp + lo + int(rng.integers(0, 8))))
+        max_t = max(t[4] for t in trace)
+        _Sim(trace, max_bs=int(rng.integers(1, 12)), n_slots=int(rng.integers(max_t, 4 * max_t))).run()
+
+
+def test_select_break_no_skip_via_abi(liborca):
+    # head does not fit: later smaller requests are not admitted
+    sim = _Sim([(0, 0, 2, 5, 8), (1, 1, 2, 2, 4), (2, 2, 1, 1, 2)], max_bs=8, n_slots=10)
+    n_iters = sim.run()
+    assert n_iters == 5 + 2   # request 0 alone for 5 iterations, then 1 and 2 together
+
+
+def test_select_rejects_bad_request(liborca):
+    eng = C.orca_engine_create(_cfg())
+    arr = (C.orca_request * 1)()
+    b = np.zeros(4, dtype=np.int32)
+    arr[0] = C.orca_request(req_id=1, arrival=0, state=C.ORCA_INITIATION, n_prompt=3, max_tokens=2, out_len=1,
+                            n_cached=0, n_generated=0, slot_base=-1,
+                            tokens=b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+    bi = (ctypes.c_int32 * 4)()
+    with pytest.raises(C.OrcaError):
+        C.orca_select_batch(eng, arr, 1, bi)
+    C.orca_engine_destroy(eng)

@@ -1,0 +1,233 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bars (from the method's tolerance): integer work bit-exact (schedule,
+reservations, releases, ragged descriptor, greedy tokens on forced logits);
+logits within max relative error 1e-4 per row in fp32 models and 2e-2 in
+bf16 models, under teacher forcing where the CUDA path's own greedy choice
+could otherwise diverge from the oracle's.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import ragged as oragged
+
+from . import _harness as hz
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+FP32_TOL = 1e-4
+BF16_TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def cuda(liborca):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+# ------------------------------------------------------------------ kernels
+
+def test_argmax_forced_logits_bit_exact(cuda):
+    from iteration_level_selective_gb300 import _orca as C
+    rng = np.random.default_rng(0)
+    V = 50257
+    lg = rng.standard_normal((37, V)).astype(np.float32)
+    lg[3, [10, 500, 40000]] = 100.0                 # tie: lowest index wins
+    lg[4, :] = 1.0                                  # all equal -> 0
+    lg[5, 7] = np.nan                               # NaN never wins
+    lg[5, 9] = 50.0
+    lg[6, :] = -np.inf
+    lg[6, V - 1] = -1e30
+    want = np.argmax(np.where(np.isnan(lg), -np.inf, lg), axis=1)
+    d = torch.from_numpy(lg).to(cuda)
+    out = torch.full((37,), -7, dtype=torch.int32, device=cuda)
+    C.orca_argmax_rows(d.data_ptr(), 37, V, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    got = out.cpu().numpy()
+    np.testing.assert_array_equal(got, want)
+    assert got[3] == 10 and got[4] == 0 and got[5] == 9 and got[6] == V - 1
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (300, 1000, 768), (257, 2304, 768), (2048, 3072, 768),
+                                   (64, 50257, 768)])
+@pytest.mark.parametrize("mode", ["store", "gelu", "resid", "f32out"])
+def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode):
+    from iteration_level_selective_gb300 import _orca as C
+    if mode != "f32out" and N == 50257:
+        pytest.skip("vocab-wide output only in fp32")
+    rng = np.random.default_rng(M * 7 + N)
+    A = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16)
+    W = torch.from_numpy((rng.standard_normal((N, K)) * 0.05).astype(np.float32)).to(torch.bfloat16)
+    bias = torch.from_numpy(rng.standard_normal(N).astype(np.float32))
+    ref = A.double() @ W.double().T + bias.double()
+    x0 = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32))
+    if mode == "gelu":
+        ref = torch.nn.functional.gelu(ref, approximate="tanh")
+    if mode == "resid":
+        ref = ref + x0.double()
+    Ad, Wd, bd = A.to(cuda), W.to(cuda), bias.to(cuda)
+    if mode in ("store", "gelu"):
+        out = torch.zeros((M, N), dtype=torch.bfloat16, device=cuda)
+    else:
+        out = (x0.clone() if mode == "resid" else torch.zeros((M, N))).to(cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    m = {"store": C.ORCA_LINEAR_STORE, "gelu": C.ORCA_LINEAR_GELU, "resid": C.ORCA_LINEAR_RESID,
+         "f32out": C.ORCA_LINEAR_F32OUT}[mode]
+    C.orca_linear(C.ORCA_DTYPE_BF16, m, Ad.data_ptr(), Wd.data_ptr(), bd.data_ptr(), out.data_ptr(), M, N, K,
+                  status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out.double().cpu()
+    scale = ref.abs().max().item()
+    # fp32 accumulation of exact bf16 products; bf16 output rounding (2^-8) for store/gelu
+    tol = 2 ** -7 if mode in ("store", "gelu") else 1e-5
+    err = (got - ref).abs().max().item() / scale
+    assert err < tol, err
+
+
+# ------------------------------------------------------------------ toy fp32: Figure 5
+
+def _toy_weights(seed=0):
+    return synth.make_weights(synth.TOY, seed=seed, w_std=0.08, bias_std=0.02, ln_std=0.1)
+
+
+def test_toy_fp32_figure5_greedy(cuda):
+    """Toy GPT (2 layers, H=64, 4 heads, vocab 256), the four Figure 5
+    requests; iteration 1 is the 7-row Figure 5 batch; greedy to iteration 8."""
+    shape = synth.TOY
+    w = _toy_weights()
+    trace = synth.figure5_trace(vocab=shape.vocab, seed=0, out_len=8, extra=10)
+    from iteration_level_selective_gb300 import runtime as rt
+    from iteration_level_selective_gb300 import _orca as C
+    dev = cuda
+    dw = rt.DeviceWeights(shape, dev, host=w)
+    eng = rt.Engine(shape, dw, max_bs=4, n_slots=64, max_rows=64, device=dev)
+    pool = rt.RequestPool(trace)
+    loop = rt.ServingLoop(eng, pool, keep_logits=True)
+    recs = [loop.step()]
+    recs.append(loop.step())
+    desc = C.orca_last_descriptor(eng.handle, 64)
+    # Figure 5: x1 decode (3 cached), x2 decode (1 cached), x3 prefill 2, x4 prefill 3 -> 7 rows
+    lay = oragged.layout([(1, 3), (1, 1), (2, 0), (3, 0)])
+    assert recs[1].req_ids == [0, 1, 2, 3]
+    assert recs[1].n_new == [1, 1, 2, 3] and recs[1].n_ctx == [3, 1, 0, 0]
+    assert desc["n_rows"] == 7 and desc["row_off"] == lay["row_off"] == [0, 1, 2, 4, 7]
+    assert desc["row_pos"] == lay["row_pos"] and desc["last_row"] == lay["last_row"]
+    bases = recs[1].slot_base
+    assert desc["row_slot"] == [bases[lay["row_req"][r]] + lay["row_pos"][r] for r in range(7)]
+    recs += loop.run()
+    assert recs[-1].it == 8
+    hz.compare_schedule(recs, trace, max_bs=4, n_slots=64)
+    got_tok = hz.gpu_tokens_by_request(recs)
+    got_lg = hz.gpu_logits_by_request(recs)
+    for req in trace:
+        greedy, logits = hz.oracle_generate(shape, w, req, teacher_force=False)
+        assert got_tok[req.req_id] == greedy, (req.req_id, got_tok[req.req_id], greedy)
+        assert pool.tokens[[r.req_id for r in pool.reqs].index(req.req_id)][req.n_prompt:].tolist() == greedy
+        for k, (g, o) in enumerate(zip(got_lg[req.req_id], logits)):
+            assert hz.max_rel_err(g, o) < FP32_TOL, (req.req_id, k, hz.max_rel_err(g, o))
+
+
+def test_toy_fp32_teacher_forced_poisson_trace(cuda):
+    """12 requests, Poisson arrivals, max_bs 4 so requests wait and join
+    mid-flight; slots tight enough that reservations break."""
+    shape = synth.TOY
+    w = _toy_weights(seed=3)
+    trace = synth.make_trace(12, (1, 20), (1, 12), vocab=shape.vocab, seed=5, rate_per_iter=0.7, forced=True)
+    n_slots = 60
+    recs, eng, pool = hz.run_gpu(shape, w, trace, max_bs=4, n_slots=n_slots, max_rows=64, teacher_force=True,
+                                 keep_all=True)
+    hz.compare_schedule(recs, trace, max_bs=4, n_slots=n_slots)
+    got_lg = hz.gpu_logits_by_request(recs)
+    got_tok = hz.gpu_tokens_by_request(recs)
+    for req in trace:
+        greedy, logits = hz.oracle_generate(shape, w, req, teacher_force=True)
+        assert len(got_lg[req.req_id]) == len(logits) == hz.n_generated(req)
+        for g, o in zip(got_lg[req.req_id], logits):
+            assert hz.max_rel_err(g, o) < FP32_TOL
+        assert got_tok[req.req_id] == greedy
+
+
+# ------------------------------------------------------------------ bf16, multi-tile
+
+SMALL_BF16 = synth.ModelShape(n_layers=2, hidden=256, n_heads=4, ffn=1024, vocab=1000, max_pos=1024,
+                              dtype=synth.DTYPE_BF16)
+
+
+def test_small_bf16_mixed_prefill_decode_multi_tile(cuda):
+    """bf16 model with several GEMM tiles and ragged tails (rows ~ 1.3k,
+    N = 768/256/1024/1000), prefills of up to 600 tokens (38 query tiles)
+    and decode rows with > 256 keys (several key splits merged)."""
+    shape = SMALL_BF16
+    w = synth.make_weights(shape, seed=11, w_std=0.05, bias_std=0.02, ln_std=0.1)
+    trace = synth.make_trace(6, (1, 600), (2, 9), vocab=shape.vocab, seed=12, rate_per_iter=0.5, forced=True)
+    recs, eng, pool = hz.run_gpu(shape, w, trace, max_bs=8, n_slots=8000, max_rows=2048, teacher_force=True,
+                                 keep_all=True)
+    hz.compare_schedule(recs, trace, max_bs=8, n_slots=8000)
+    got_lg = hz.gpu_logits_by_request(recs)
+    worst = 0.0
+    for req in trace:
+        _, logits = hz.oracle_generate(shape, w, req, teacher_force=True)
+        for g, o in zip(got_lg[req.req_id], logits):
+            worst = max(worst, hz.max_rel_err(g, o))
+    assert worst < BF16_TOL, worst
+
+
+# ------------------------------------------------------------------ GPT-2-small, full size, sampled
+
+def test_gpt2_small_trace_sampled_parity(cuda):
+    """GPT-2-small-shaped bf16 model (12 layers, H=768, 12 heads, vocab
+    50257), 64 requests, prompts U{32..512}, outputs U{1..256},
+    max_tokens = prompt + 256, max_bs 64 - the benchmark's workload and
+    launch configuration.  Teacher-forced; the integer schedule is checked
+    in full and the logits of the three shortest-prompt requests at up to 6
+    generated steps each against the oracle."""
+    shape = synth.GPT2_SMALL
+    w = synth.make_weights(shape, seed=0)
+    trace = synth.make_trace(64, (32, 512), (1, 256), vocab=shape.vocab, seed=0, rate_per_iter=0.5,
+                             max_extra=256, forced=True)
+    sample = sorted(trace, key=lambda r: r.n_prompt)[:3]
+    n_slots = 64 * (512 + 256)
+    recs, eng, pool = hz.run_gpu(shape, w, trace, max_bs=64, n_slots=n_slots, max_rows=64 * 512,
+                                 teacher_force=True, keep_ids={r.req_id for r in sample})
+    hz.compare_schedule(recs, trace, max_bs=64, n_slots=n_slots)
+    got_lg = hz.gpu_logits_by_request(recs)
+    for req in sample:
+        steps = min(6, hz.n_generated(req))
+        _, logits = hz.oracle_generate(shape, w, req, teacher_force=True, stop_after=steps)
+        for k in range(steps):
+            err = hz.max_rel_err(got_lg[req.req_id][k], logits[k])
+            assert err < BF16_TOL, (req.req_id, k, err)
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_iteration_errors_leave_requests_untouched(cuda):
+    from iteration_level_selective_gb300 import runtime as rt
+    from iteration_level_selective_gb300 import _orca as C
+    import ctypes
+    shape = synth.TOY
+    dw = rt.DeviceWeights(shape, cuda, host=_toy_weights())
+    eng = rt.Engine(shape, dw, max_bs=2, n_slots=64, max_rows=8, device=cuda)
+    trace = synth.make_trace(3, (5, 5), (2, 2), vocab=256, seed=1)
+    pool = rt.RequestPool(trace)
+    bi = (ctypes.c_int32 * 2)()
+    nt = (ctypes.c_int32 * 2)()
+    nb = C.orca_select_batch(eng.handle, pool.arr, 3, bi)
+    assert nb == 2
+    with pytest.raises(C.OrcaError) as ei:    # 5 + 5 rows > max_rows 8
+        C.orca_iteration(eng.handle, pool.arr, bi, nb, 0, nt)
+    assert ei.value.code == C.ORCA_EBATCH
+    assert pool.arr[bi[0]].state == C.ORCA_RUNNING and pool.arr[bi[0]].n_cached == 0
+    with pytest.raises(C.OrcaError) as ei:
+        C.orca_iteration(eng.handle, pool.arr, bi, 0, 0, nt)
+    assert ei.value.code == C.ORCA_EINVAL
+    pool.tokens[0][0] = 999                   # token id out of range
+    with pytest.raises(C.OrcaError) as ei:
+        C.orca_iteration(eng.handle, pool.arr, bi, 1, 0, nt)
+    assert ei.value.code == C.ORCA_EINVAL
+    pool.tokens[0][0] = 1
+    C.orca_iteration(eng.handle, pool.arr, bi, 1, 0, nt)   # one request fits
+    assert pool.arr[bi[0]].n_cached == 5 and pool.arr[bi[0]].state == C.ORCA_INCREMENT
