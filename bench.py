@@ -46,6 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 def trace_for(rank: int, gen: int = 0):
+    """The rank's request stream (replicas serve distinct streams)."""
     shape = synth.GPT2_SMALL
     return synth.make_trace(64, (32, 512), (1, 256), vocab=shape.vocab, seed=1000 * rank + gen,
                             rate_per_iter=0.5, max_extra=256)
@@ -219,6 +220,7 @@ def run_ours(args, rank: int, world: int):
     import torch.distributed as dist
     from iteration_level_selective_gb300 import _orca as C
     from iteration_level_selective_gb300 import build as B
+    from iteration_level_selective_gb300 import replicas
     from iteration_level_selective_gb300 import runtime as rt
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -271,13 +273,8 @@ def run_ours(args, rank: int, world: int):
     wall = time.perf_counter() - w0
     clocks = sampler.stop()
     dev_s = ev0.elapsed_time(ev1) / 1000.0
-    if world > 1:
-        t = torch.tensor([dev_s, wall], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dev_s, wall = t.tolist()
-        c = torch.tensor([rows, gen_tok, done, h2d, d2h], device=dev, dtype=torch.float64)
-        dist.all_reduce(c, op=dist.ReduceOp.SUM)
-        rows, gen_tok, done, h2d, d2h = c.tolist()
+    (dev_s, wall), (rows, gen_tok, done, h2d, d2h) = replicas.reduce_timing(
+        [dev_s, wall], [rows, gen_tok, done, h2d, d2h], device=dev)
 
     # profiled pass: per-launch CUDA events around every kernel, same workload
     C.orca_profile_enable(eng.handle, True)
@@ -332,6 +329,7 @@ def run_ours(args, rank: int, world: int):
         "gpu_launches": launches_per_iter * args.steps * world,
         "roofline": roof,
         "kernel_time_share": {k: round(v["ms"] / total_ms, 4) for k, v in agg.items()},
+        "kernel_ms_per_step": {k: round(v["ms"] / args.steps, 4) for k, v in agg.items()},
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

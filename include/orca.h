@@ -58,6 +58,8 @@ extern "C" {
 /* orca_iteration flags */
 #define ORCA_ITER_TEACHER_FORCE 1 /* read every input token from req.tokens;
                                      never write generated tokens into it   */
+#define ORCA_ITER_EAGER 2         /* launch the kernels one by one instead of
+                                     replaying the engine's CUDA graph      */
 
 /* ---------------------------------------------------------------- types */
 typedef struct orca_engine orca_engine;
@@ -194,7 +196,11 @@ int orca_select_batch(orca_engine *eng, orca_request *pool, int32_t n_pool, int3
  * logits_dev, if not NULL, receives fp32 [n_batch, vocab] logits.
  * Afterwards each request is INCREMENT (or FINISHED, slots released),
  * n_cached += L_i, n_generated += 1, and, unless ORCA_ITER_TEACHER_FORCE,
- * the token is appended to tokens[].  On error no request is modified. */
+ * the token is appended to tokens[].  On error no request is modified.
+ * bf16 engines replay a CUDA graph of the whole forward (captured on first
+ * use for each GEMM tile-shape choice and logits pointer, on an internal
+ * stream; every kernel reads the iteration's sizes from the device
+ * descriptor) unless ORCA_ITER_EAGER is set or profiling is enabled. */
 int orca_iteration(orca_engine *eng, orca_request *pool, const int32_t *batch_idx, int32_t n_batch,
                    int32_t flags, int32_t *next_tokens, float *logits_dev, void *stream);
 
@@ -218,23 +224,51 @@ int orca_argmax_rows(const float *logits_dev, int32_t n_rows, int32_t vocab, int
                      void *stream);
 
 /* The token-wise Linear of Figure 5 on its own - the kernel orca_iteration
- * runs for the QKV, Attn-Out and MLP Linears - exposed for tests and
- * benchmarks:  out[m, n] = f(sum_k A[m, k] W[n, k] + bias[n]),
+ * runs for the QKV, Attn-Out and MLP Linears and the LM head - exposed for
+ * tests and benchmarks:  out[m, n] = f(sum_k A[m, k] W[n, k] + bias[n]),
  *   A [M, K], W [N, K] row-major in `dtype` (device pointers),
  *   bias [N] fp32 device pointer or NULL,
  *   mode ORCA_LINEAR_STORE: out[M, N] in dtype;  ORCA_LINEAR_GELU: out[M, N]
  *   = gelu_tanh(.) in dtype;  ORCA_LINEAR_RESID: out[M, N] fp32 += (.);
- *   ORCA_LINEAR_F32OUT: out[M, N] fp32.
+ *   ORCA_LINEAR_F32OUT: out[M, N] fp32 (out may be NULL when argmax_keys_dev
+ *   is given).
  * bf16 runs on tcgen05 tensor cores and needs K % 64 == 0 and 16-byte
- * aligned A and W; fp32 runs CUDA-core FMA.  status_dev: device int32 that
- * kernels OR error bits into (1 wait timeout, 2 bad index).  Enqueued on
- * `stream`, not synchronised. */
+ * aligned A and W; fp32 runs CUDA-core FMA.
+ * scratch / scratch_bytes: optional 256-byte aligned device scratch; with
+ *   enough of it (counters, then fp32 partial tiles) a bf16 product with few
+ *   output tiles is split along K over more SMs; NULL disables that.
+ * argmax_keys_dev: optional device uint64 [M] (bf16, F32OUT only), zeroed by
+ *   the call, receiving each row's greedy choice packed as key = (ordered
+ *   value bits << 32) | (0xFFFFFFFF - column); key 0 means no column.
+ * status_dev: device int32 that kernels OR error bits into (1 wait timeout,
+ * 2 bad index).  Enqueued on `stream`, not synchronised. */
 #define ORCA_LINEAR_STORE 0
 #define ORCA_LINEAR_GELU 1
 #define ORCA_LINEAR_RESID 2
 #define ORCA_LINEAR_F32OUT 3
 int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const float *bias, void *out,
-                int32_t M, int32_t N, int32_t K, int32_t *status_dev, void *stream);
+                int32_t M, int32_t N, int32_t K, void *scratch, size_t scratch_bytes, void *argmax_keys_dev,
+                int32_t *status_dev, void *stream);
+
+/* Ragged attention of one layer on its own (Figure 5: each request's
+ * queries against its own K/V slots, rows split and merged in place).
+ * Batch on the host: request i owns rows row_off[i] .. row_off[i+1]-1
+ * (row_off[0] = 0, strictly increasing), whose positions are ctx[i] + j;
+ * row j reads keys 0 .. ctx[i] + j of slots slot_base[i] + key.  q and out
+ * are [row_off[n_batch], n_heads * head_dim] device arrays; k_layer and
+ * v_layer one layer of the K/V pool, [n_heads][n_slots][head_dim], already
+ * holding every key the rows read (their own included).  dtype is the
+ * element type of q, K/V and out.  workspace: device scratch of at least
+ * orca_attention_workspace_bytes(n_batch, rows, ...) bytes, 256-byte
+ * aligned, owned by the caller.  The host arrays are read before return;
+ * the call synchronises the stream before staging them (pageable copy) and
+ * enqueues the kernel without waiting for it. */
+int orca_attention_workspace_bytes(int32_t n_batch, int32_t n_rows, int32_t n_heads, int32_t head_dim,
+                                   size_t *bytes);
+int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_slots, const void *q,
+                   const void *k_layer, const void *v_layer, void *out, int32_t n_batch,
+                   const int32_t *row_off, const int32_t *ctx, const int64_t *slot_base, void *workspace,
+                   size_t ws_bytes, int32_t *status_dev, void *stream);
 
 /* ---------------------------------------------------------------- profiling */
 /* enable != 0: time every launch of every kernel class with CUDA events on

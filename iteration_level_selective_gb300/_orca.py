@@ -30,6 +30,7 @@ ORCA_DTYPE_F32 = 0
 ORCA_DTYPE_BF16 = 1
 ORCA_INITIATION, ORCA_INCREMENT, ORCA_RUNNING, ORCA_FINISHED = 0, 1, 2, 3
 ORCA_ITER_TEACHER_FORCE = 1
+ORCA_ITER_EAGER = 2
 (ORCA_K_EMBED, ORCA_K_LAYERNORM, ORCA_K_GEMM_QKV, ORCA_K_ATTENTION, ORCA_K_GEMM_O, ORCA_K_GEMM_FC1,
  ORCA_K_GEMM_FC2, ORCA_K_LM_HEAD, ORCA_K_ARGMAX, ORCA_K_COUNT) = range(10)
 KERNEL_NAMES = ["embed", "layernorm", "gemm_qkv", "attention", "gemm_o", "gemm_fc1", "gemm_fc2",
@@ -64,7 +65,8 @@ class orca_kernel_stats(ctypes.Structure):
 EXPORTS = ("orca_kv_pool_bytes", "orca_workspace_bytes", "orca_weight_count", "orca_engine_create",
            "orca_engine_destroy", "orca_kv_reserve", "orca_kv_release", "orca_kv_stats", "orca_select_batch",
            "orca_iteration", "orca_last_descriptor", "orca_argmax_rows", "orca_profile_enable",
-           "orca_profile_read", "orca_last_error", "orca_linear", "orca_last_transfer")
+           "orca_profile_read", "orca_last_error", "orca_linear", "orca_last_transfer",
+           "orca_attention_workspace_bytes", "orca_attention")
 
 _lib = None
 
@@ -97,8 +99,10 @@ def lib() -> ctypes.CDLL:
             "orca_profile_enable": [P, c_i32],
             "orca_profile_read": [P, c_i32, ctypes.POINTER(orca_kernel_stats)],
             "orca_last_error": [P, ctypes.c_char_p, c_sz],
-            "orca_linear": [c_i32, c_i32, P, P, P, P, c_i32, c_i32, c_i32, P, P],
+            "orca_linear": [c_i32, c_i32, P, P, P, P, c_i32, c_i32, c_i32, P, c_sz, P, P, P],
             "orca_last_transfer": [P, i64p, i64p, i32p],
+            "orca_attention_workspace_bytes": [c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)],
+            "orca_attention": [c_i32, c_i32, c_i32, c_i64, P, P, P, P, c_i32, i32p, i32p, i64p, P, c_sz, P, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -203,6 +207,30 @@ def orca_last_transfer(eng):
     return a.value, b.value, n.value
 
 
+def orca_attention_workspace_bytes(n_batch: int, n_rows: int, n_heads: int, head_dim: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().orca_attention_workspace_bytes(n_batch, n_rows, n_heads, head_dim, ctypes.byref(n)))
+    return n.value
+
+
+def _i32_arr(vals):
+    return (ctypes.c_int32 * len(vals))(*[int(v) for v in vals])
+
+
+def _i64_arr(vals):
+    return (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
+
+
+def orca_attention(dtype: int, n_heads: int, head_dim: int, n_slots: int, q_ptr: int, k_ptr: int, v_ptr: int,
+                   out_ptr: int, row_off, ctx, slot_base, ws_ptr: int, ws_bytes: int, status_ptr: int,
+                   stream=0) -> None:
+    nb = len(ctx)
+    _check(lib().orca_attention(dtype, n_heads, head_dim, n_slots, ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr),
+                                ctypes.c_void_p(v_ptr), ctypes.c_void_p(out_ptr), nb, _i32_arr(row_off),
+                                _i32_arr(ctx), _i64_arr(slot_base), ctypes.c_void_p(ws_ptr), ws_bytes,
+                                ctypes.c_void_p(status_ptr), ctypes.c_void_p(stream or None)))
+
+
 def orca_argmax_rows(logits_ptr: int, n_rows: int, vocab: int, out_ptr: int, stream=0) -> None:
     _check(lib().orca_argmax_rows(ctypes.c_void_p(logits_ptr), n_rows, vocab, ctypes.c_void_p(out_ptr),
                                   ctypes.c_void_p(stream or None)))
@@ -212,10 +240,17 @@ ORCA_LINEAR_STORE, ORCA_LINEAR_GELU, ORCA_LINEAR_RESID, ORCA_LINEAR_F32OUT = 0, 
 
 
 def orca_linear(dtype: int, mode: int, a_ptr: int, w_ptr: int, bias_ptr: int, out_ptr: int, M: int, N: int, K: int,
-                status_ptr: int, stream=0) -> None:
+                status_ptr: int, stream=0, scratch_ptr: int = 0, scratch_bytes: int = 0, argmax_ptr: int = 0) -> None:
     _check(lib().orca_linear(dtype, mode, ctypes.c_void_p(a_ptr), ctypes.c_void_p(w_ptr),
-                             ctypes.c_void_p(bias_ptr or None), ctypes.c_void_p(out_ptr), M, N, K,
+                             ctypes.c_void_p(bias_ptr or None), ctypes.c_void_p(out_ptr or None), M, N, K,
+                             ctypes.c_void_p(scratch_ptr or None), scratch_bytes, ctypes.c_void_p(argmax_ptr or None),
                              ctypes.c_void_p(status_ptr), ctypes.c_void_p(stream or None)))
+
+
+def argmax_key_column(key: int) -> int:
+    """Column of a packed greedy-choice key (see orca_linear), -1 for none."""
+    key = int(key) & 0xFFFFFFFFFFFFFFFF
+    return -1 if key == 0 else 0xFFFFFFFF - (key & 0xFFFFFFFF)
 
 
 def orca_profile_enable(eng, enable: bool) -> None:

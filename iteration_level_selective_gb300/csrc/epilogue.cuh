@@ -99,8 +99,8 @@ __device__ __forceinline__ void epi_apply(const EpiParams &e, int m, int n0, flo
       store_run<T, CNT>(static_cast<T *>(e.out) + (int64_t)m * e.ldo + n0, v, cnt);
       break;
     }
-    default: {  // kEpiLogits
-      store_run<float, CNT>(static_cast<float *>(e.out) + (int64_t)m * e.ldo + n0, v, cnt);
+    default: {  // kEpiLogits (out may be nullptr when only the fused argmax is wanted)
+      if (e.out != nullptr) store_run<float, CNT>(static_cast<float *>(e.out) + (int64_t)m * e.ldo + n0, v, cnt);
       break;
     }
   }

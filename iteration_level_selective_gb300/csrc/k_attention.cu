@@ -199,7 +199,8 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float *acc, floa
 
 // kind 1: one row over keys [split_idx * split, min(+split, pos + 1)).
 template <typename T, int D>
-__device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, int head, SplitSmem<D> &sm) {
+__device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, int w_idx, int head,
+                                          SplitSmem<D> &sm) {
   constexpr int VN = Vec16<T>::N;
   constexpr int LPK = D / VN;          // lanes per key (16 bytes each)
   constexpr int KPW = 32 / LPK;        // keys per warp step
@@ -290,7 +291,7 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
     if (dim < D) O[dim] = from_f<T>(A / L);
     return;
   }
-  float *part = a.part + ((int64_t)blockIdx.x * a.n_heads + head) * (D + 2);
+  float *part = a.part + ((int64_t)w_idx * a.n_heads + head) * (D + 2);
   if (dim < D) part[dim] = A;
   if (dim == 0) {
     part[D] = M;
@@ -305,7 +306,7 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   __syncthreads();
   if (!sm.last) return;
   __threadfence();
-  const int w0 = blockIdx.x - w.b;  // the row's splits are consecutive work items
+  const int w0 = w_idx - w.b;  // the row's splits are consecutive work items
   if (dim < D) {
     float Mx = -INFINITY;
     for (int j = 0; j < n_splits; ++j)
@@ -323,21 +324,34 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   if (threadIdx.x == 0) a.counters[(int64_t)w.req * a.n_heads + head] = 0;
 }
 
+// Persistent: CTA b takes (work item, head) pairs b, b + gridDim.x, ...
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) attention_kernel(AttnArgs a) {
   __shared__ __align__(16) unsigned char smem_raw[sizeof(TileSmem<D>) > sizeof(SplitSmem<D>) ? sizeof(TileSmem<D>)
                                                                                              : sizeof(SplitSmem<D>)];
-  const AttnWork w = a.work[blockIdx.x];
-  const int head = blockIdx.y;
-  if (w.kind == 0)
-    query_tile<T, D>(a, w, head, *reinterpret_cast<TileSmem<D> *>(smem_raw));
-  else
-    key_split<T, D>(a, w, head, *reinterpret_cast<SplitSmem<D> *>(smem_raw));
+  if (a.hdr != nullptr) {
+    a.n_rows = a.hdr->n_rows;
+    a.n_work = a.hdr->n_work;
+    a.split = a.hdr->split;
+  }
+  const int total = a.n_work * a.n_heads;
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    const int w_idx = item / a.n_heads;
+    const int head = item - w_idx * a.n_heads;
+    const AttnWork w = a.work[w_idx];
+    __syncthreads();  // the previous item's shared-memory reads are done
+    if (w.kind == 0)
+      query_tile<T, D>(a, w, head, *reinterpret_cast<TileSmem<D> *>(smem_raw));
+    else
+      key_split<T, D>(a, w, w_idx, head, *reinterpret_cast<SplitSmem<D> *>(smem_raw));
+  }
 }
 
 template <typename T>
 cudaError_t launch_t(int head_dim, const AttnArgs &a, int n_work, cudaStream_t st) {
-  dim3 grid(n_work, a.n_heads);
+  const long long total = (long long)n_work * a.n_heads;
+  const int cap = 8 * gemm_sm_count();
+  dim3 grid(a.hdr != nullptr ? cap : (int)(total < cap ? total : cap));
   switch (head_dim) {
     case 16: attention_kernel<T, 16><<<grid, kThreads, 0, st>>>(a); break;
     case 32: attention_kernel<T, 32><<<grid, kThreads, 0, st>>>(a); break;

@@ -42,55 +42,92 @@ __device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 v) {
 
 // x[r] = tok_emb[tok_r] + pos_emb[pos_r]  (fp32 residual stream)
 template <typename T>
-__global__ void embed_kernel(const RowInfo *__restrict__ rows, const T *__restrict__ tok_emb,
-                             const T *__restrict__ pos_emb, float *__restrict__ x, int H, int vocab,
-                             int max_pos, int32_t *status) {
-  const int r = blockIdx.x;
-  const RowInfo ri = rows[r];
-  if (ri.tok < 0 || ri.tok >= vocab || ri.pos < 0 || ri.pos >= max_pos) {
-    if (threadIdx.x == 0) atomicOr(status, kStatusBadIndex);
-    return;
-  }
-  const T *te = tok_emb + (int64_t)ri.tok * H;
-  const T *pe = pos_emb + (int64_t)ri.pos * H;
-  float *xr = x + (int64_t)r * H;
-  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
-    float4 a = load4(te + c), b = load4(pe + c);
-    store4(xr + c, make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
+__global__ void embed_kernel(const RowInfo *__restrict__ rows, int n_rows_arg, const int32_t *n_rows_dev,
+                             const T *__restrict__ tok_emb, const T *__restrict__ pos_emb, float *__restrict__ x,
+                             int H, int vocab, int max_pos, int32_t *status) {
+  const int n_rows = n_rows_dev ? *n_rows_dev : n_rows_arg;
+  for (int r = blockIdx.x; r < n_rows; r += gridDim.x) {
+    const RowInfo ri = rows[r];
+    if (ri.tok < 0 || ri.tok >= vocab || ri.pos < 0 || ri.pos >= max_pos) {
+      if (threadIdx.x == 0) atomicOr(status, kStatusBadIndex);
+      continue;
+    }
+    const T *te = tok_emb + (int64_t)ri.tok * H;
+    const T *pe = pos_emb + (int64_t)ri.pos * H;
+    float *xr = x + (int64_t)r * H;
+    for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+      float4 a = load4(te + c), b = load4(pe + c);
+      store4(xr + c, make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
+    }
   }
 }
 
-// out[i] = LayerNorm(x[src_i]) * g + b, one warp per output row; src_i = i,
-// or the last row of request i when `gather` is given (final LayerNorm on
-// the rows whose logits are sampled).  Statistics in fp32, biased variance.
-template <typename T>
-__global__ void layernorm_kernel(const float *__restrict__ x, const float *__restrict__ g,
-                                 const float *__restrict__ b, T *__restrict__ out, int n_rows, int H,
-                                 const ReqInfo *__restrict__ gather) {
-  const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  if (row >= n_rows) return;
-  const int src = gather ? gather[row].row_off + gather[row].n_new - 1 : row;
+// LayerNorm of one row by one warp: (x - mean) / sqrt(var + eps) * g + b,
+// statistics in fp32, biased variance.  NV4 > 0: the row (NV4 float4 per
+// lane) stays in registers, one read of x; NV4 == 0: three passes.
+template <typename T, int NV4>
+__device__ __forceinline__ void layernorm_row(const float *__restrict__ x, const float *__restrict__ g,
+                                              const float *__restrict__ b, T *__restrict__ out, int row, int src,
+                                              int H, int lane) {
   const float *xr = x + (int64_t)src * H;
-  float s = 0.f;
-  for (int c = lane * 4; c < H; c += 128) {
-    float4 v = load4(xr + c);
-    s += (v.x + v.y) + (v.z + v.w);
-  }
-  const float mean = warp_sum(s) / (float)H;
-  float q = 0.f;
-  for (int c = lane * 4; c < H; c += 128) {
-    float4 v = load4(xr + c);
-    float a = v.x - mean, bb = v.y - mean, cc = v.z - mean, d = v.w - mean;
-    q += (a * a + bb * bb) + (cc * cc + d * d);
-  }
-  const float rstd = rsqrtf(warp_sum(q) / (float)H + 1e-5f);
   T *orow = out + (int64_t)row * H;
-  for (int c = lane * 4; c < H; c += 128) {
-    float4 v = load4(xr + c), gg = load4(g + c), bv = load4(b + c);
-    store4(orow + c, make_float4((v.x - mean) * rstd * gg.x + bv.x, (v.y - mean) * rstd * gg.y + bv.y,
-                                 (v.z - mean) * rstd * gg.z + bv.z, (v.w - mean) * rstd * gg.w + bv.w));
+  if constexpr (NV4 > 0) {
+    float4 v[NV4];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV4; ++i) {
+      v[i] = load4(xr + lane * 4 + i * 128);
+      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    }
+    const float mean = warp_sum(s) / (float)H;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV4; ++i) {
+      const float a = v[i].x - mean, bb = v[i].y - mean, cc = v[i].z - mean, d = v[i].w - mean;
+      q += (a * a + bb * bb) + (cc * cc + d * d);
+    }
+    const float rstd = rsqrtf(warp_sum(q) / (float)H + 1e-5f);
+#pragma unroll
+    for (int i = 0; i < NV4; ++i) {
+      const int c = lane * 4 + i * 128;
+      const float4 gg = load4(g + c), bv = load4(b + c);
+      store4(orow + c, make_float4((v[i].x - mean) * rstd * gg.x + bv.x, (v[i].y - mean) * rstd * gg.y + bv.y,
+                                   (v[i].z - mean) * rstd * gg.z + bv.z, (v[i].w - mean) * rstd * gg.w + bv.w));
+    }
+  } else {
+    float s = 0.f;
+    for (int c = lane * 4; c < H; c += 128) {
+      float4 v = load4(xr + c);
+      s += (v.x + v.y) + (v.z + v.w);
+    }
+    const float mean = warp_sum(s) / (float)H;
+    float q = 0.f;
+    for (int c = lane * 4; c < H; c += 128) {
+      float4 v = load4(xr + c);
+      float a = v.x - mean, bb = v.y - mean, cc = v.z - mean, d = v.w - mean;
+      q += (a * a + bb * bb) + (cc * cc + d * d);
+    }
+    const float rstd = rsqrtf(warp_sum(q) / (float)H + 1e-5f);
+    for (int c = lane * 4; c < H; c += 128) {
+      float4 v = load4(xr + c), gg = load4(g + c), bv = load4(b + c);
+      store4(orow + c, make_float4((v.x - mean) * rstd * gg.x + bv.x, (v.y - mean) * rstd * gg.y + bv.y,
+                                   (v.z - mean) * rstd * gg.z + bv.z, (v.w - mean) * rstd * gg.w + bv.w));
+    }
   }
+}
+
+// out[i] = LayerNorm(x[src_i]), one warp per output row, rows grid-strided;
+// src_i = i, or the last row of request i when `gather` is given (final
+// LayerNorm on the rows whose logits are sampled).
+template <typename T, int NV4>
+__global__ void layernorm_kernel(const float *__restrict__ x, const float *__restrict__ g,
+                                 const float *__restrict__ b, T *__restrict__ out, int n_rows_arg,
+                                 const int32_t *n_rows_dev, int H, const ReqInfo *__restrict__ gather) {
+  const int n_rows = n_rows_dev ? *n_rows_dev : n_rows_arg;
+  const int lane = threadIdx.x & 31;
+  const int wpc = blockDim.x / 32;
+  for (int row = blockIdx.x * wpc + threadIdx.x / 32; row < n_rows; row += gridDim.x * wpc)
+    layernorm_row<T, NV4>(x, g, b, out, row, gather ? gather[row].row_off + gather[row].n_new - 1 : row, H, lane);
 }
 
 // (value, index) order of the greedy choice: larger value wins, equal values
@@ -101,7 +138,8 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
-__global__ void argmax_kernel(const float *__restrict__ logits, int V, int32_t *__restrict__ out) {
+__global__ void argmax_kernel(const float *__restrict__ logits, int V, int32_t *__restrict__ out,
+                              unsigned long long *__restrict__ keys) {
   const int r = blockIdx.x;
   const float *lr = logits + (int64_t)r * V;
   float bv = -INFINITY;
@@ -131,45 +169,59 @@ __global__ void argmax_kernel(const float *__restrict__ logits, int V, int32_t *
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
-    if (lane == 0) out[r] = bi;
+    if (lane == 0) {
+      if (keys != nullptr)
+        keys[r] = bi < 0 ? 0ull : argmax_key(bv, bi);
+      else
+        out[r] = bi;
+    }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows, const void *tok_emb,
+cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows, const int32_t *n_rows_dev, const void *tok_emb,
                          const void *pos_emb, float *x, int H, int vocab, int max_pos, int32_t *status,
                          cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
   const int threads = H >= 512 ? 128 : 32;
+  const int grid = n_rows < 1184 ? n_rows : 1184;
   if (dtype == 1)
-    embed_kernel<__nv_bfloat16><<<n_rows, threads, 0, st>>>(
-        rows, static_cast<const __nv_bfloat16 *>(tok_emb), static_cast<const __nv_bfloat16 *>(pos_emb), x, H,
-        vocab, max_pos, status);
+    embed_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
+        rows, n_rows, n_rows_dev, static_cast<const __nv_bfloat16 *>(tok_emb),
+        static_cast<const __nv_bfloat16 *>(pos_emb), x, H, vocab, max_pos, status);
   else
-    embed_kernel<float><<<n_rows, threads, 0, st>>>(rows, static_cast<const float *>(tok_emb),
-                                                     static_cast<const float *>(pos_emb), x, H, vocab,
-                                                     max_pos, status);
+    embed_kernel<float><<<grid, threads, 0, st>>>(rows, n_rows, n_rows_dev, static_cast<const float *>(tok_emb),
+                                                   static_cast<const float *>(pos_emb), x, H, vocab, max_pos, status);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t layernorm_t(const float *x, const float *g, const float *b, T *out, int n_rows,
+                               const int32_t *n_rows_dev, int H, const ReqInfo *gather, cudaStream_t st) {
+  const int rows_per_cta = 8;
+  int grid = (n_rows + rows_per_cta - 1) / rows_per_cta;
+  if (grid > 1184) grid = 1184;
+  switch (H) {
+    case 768: layernorm_kernel<T, 6><<<grid, 32 * rows_per_cta, 0, st>>>(x, g, b, out, n_rows, n_rows_dev, H, gather); break;
+    case 1024: layernorm_kernel<T, 8><<<grid, 32 * rows_per_cta, 0, st>>>(x, g, b, out, n_rows, n_rows_dev, H, gather); break;
+    case 2048: layernorm_kernel<T, 16><<<grid, 32 * rows_per_cta, 0, st>>>(x, g, b, out, n_rows, n_rows_dev, H, gather); break;
+    default: layernorm_kernel<T, 0><<<grid, 32 * rows_per_cta, 0, st>>>(x, g, b, out, n_rows, n_rows_dev, H, gather); break;
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_layernorm(int dtype, const float *x, const float *g, const float *b, void *out, int n_rows,
-                             int H, const ReqInfo *gather, cudaStream_t st) {
+                             const int32_t *n_rows_dev, int H, const ReqInfo *gather, cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
-  const int rows_per_cta = 4;
-  const int grid = (n_rows + rows_per_cta - 1) / rows_per_cta;
-  if (dtype == 1)
-    layernorm_kernel<__nv_bfloat16><<<grid, 32 * rows_per_cta, 0, st>>>(
-        x, g, b, static_cast<__nv_bfloat16 *>(out), n_rows, H, gather);
-  else
-    layernorm_kernel<float><<<grid, 32 * rows_per_cta, 0, st>>>(x, g, b, static_cast<float *>(out), n_rows,
-                                                                 H, gather);
-  return cudaGetLastError();
+  if (dtype == 1) return layernorm_t(x, g, b, static_cast<__nv_bfloat16 *>(out), n_rows, n_rows_dev, H, gather, st);
+  return layernorm_t(x, g, b, static_cast<float *>(out), n_rows, n_rows_dev, H, gather, st);
 }
 
-cudaError_t launch_argmax(const float *logits, int n_rows, int vocab, int32_t *out, cudaStream_t st) {
+cudaError_t launch_argmax(const float *logits, int n_rows, int vocab, int32_t *out, unsigned long long *keys,
+                          cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
-  argmax_kernel<<<n_rows, 512, 0, st>>>(logits, vocab, out);
+  argmax_kernel<<<n_rows, 512, 0, st>>>(logits, vocab, out, keys);
   return cudaGetLastError();
 }
 

@@ -7,18 +7,28 @@
 //   C[m, n] = sum_k A[m, k] * W[n, k]     A: [M, K] bf16, W: [N, K] bf16
 // with fp32 accumulation in tensor memory, then the fused epilogue.
 //
-// Structure (one 128 x 128 output tile per CTA, 6 warps):
-//   warp 0      one lane issues TMA loads of 128x64 A and W tiles (128-byte
-//               swizzle) into a 4-stage shared-memory ring;
-//   warp 1      allocates 128 TMEM columns; one lane issues tcgen05.mma
-//               (kind::f16, M=128, N=128, K=16) and commits each stage back to
-//               the producer and the finished tile to the epilogue;
-//   warps 2..5  tcgen05.ld the accumulator (one TMEM lane quarter each) and
-//               run the epilogue.
-// Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
-// kernel sets kStatusWaitTimeout, skips the remaining work and still frees
-// its tensor memory.  Ragged M and N are handled by TMA zero fill on load
-// and masked epilogue stores.
+// Persistent CTAs (one per SM) walk a list of work units; a unit is one
+// 128 x BN output tile, or one K-range of it when the output has too few
+// tiles to fill the GPU (split-K, used for decode-sized M).  Tiles are
+// visited in groups of 8 M-tiles so the CTAs running at the same time share
+// their W tiles and A rows in L2.  Six warps:
+//   warp 0      one lane issues TMA loads of 128x64 A and BNx64 W tiles
+//               (128-byte swizzle) into a shared-memory ring;
+//   warp 1      allocates 2*BN TMEM columns (two accumulators); one lane
+//               issues tcgen05.mma (kind::f16, M=128, N=BN, K=16), releases
+//               each ring stage with tcgen05.commit and hands a finished
+//               accumulator to the epilogue;
+//   warps 2..5  tcgen05.ld the accumulator (one TMEM lane quarter each),
+//               free it for the next tile at once, and run the epilogue:
+//               bias, then QKV scatter to K/V slots, GeLU, residual add,
+//               logits store and/or a fused greedy argmax.  A split unit
+//               stores an fp32 partial; the last unit of a tile to arrive
+//               (atomic counter, no waiting) sums the partials and runs the
+//               epilogue.
+// Every mbarrier wait is bounded (about 2 s of %globaltimer).  On expiry the
+// CTA sets kStatusWaitTimeout and an abort flag that ends every other wait at
+// once; the roles then skip their work but keep their barrier sequence, and
+// the tensor memory is still freed.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -29,16 +39,67 @@
 namespace orca {
 namespace {
 
-constexpr int BM = kTcBM, BN = kTcBN, BK = kTcBK, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
-constexpr uint32_t TMEM_COLS = BN;
+constexpr int BM = kTcBM, BK = kTcBK;
+constexpr int kStageBudget = 200 * 1024;
+constexpr int kGroupM = 8;
 
-// Instruction descriptor, kind::f16: D fp32 (bit 4), A bf16 (bits 7-9),
-// B bf16 (bits 10-12), both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
+template <int BN>
+struct Cfg {
+  // W tiles arrive as BN/128 TMA boxes of 128 rows (the tensor maps' box).
+  static_assert(BN % kTcBM == 0 && BN <= 256, "BN must be 128 or 256");
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (kStageBudget / STAGE) > 8 ? 8 : (kStageBudget / STAGE);
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  // Instruction descriptor, kind::f16: D fp32 (bit 4), A bf16 (bits 7-9),
+  // B bf16 (bits 10-12), both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28.
+  static constexpr uint32_t IDESC =
+      (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+};
+
+// Work decomposition, computed identically on the host (grid size) and by
+// every thread of the kernel.
+struct Sched {
+  int nM, nN, KB, S, kbs, tiles, units;
+  __host__ __device__ void init(int M, int N, int K, int BN, int sm, const GemmScratch &scr) {
+    nM = (M + BM - 1) / BM;
+    nN = (N + BN - 1) / BN;
+    KB = K / BK;
+    tiles = nM * nN;
+    S = 1;
+    kbs = KB;
+    // The last unit of a tile reads all S partials through one SM, so split
+    // only long K (>= 16 k-blocks) and at most 4 ways.
+    if (scr.partials != nullptr && tiles > 0 && tiles * 2 <= sm && KB >= 16 && tiles <= scr.n_counters) {
+      int s = sm / tiles;
+      if (s > KB / 8) s = KB / 8;
+      if (s > 4) s = 4;
+      if (s > 1) {
+        const int k = (KB + s - 1) / s;
+        const int S2 = (KB + k - 1) / k;
+        if ((size_t)tiles * S2 * BM * BN * sizeof(float) <= scr.partial_bytes) {
+          S = S2;
+          kbs = k;
+        }
+      }
+    }
+    units = tiles * S;
+  }
+  __device__ __forceinline__ void unit(int u, int &m, int &n, int &kb0, int &kb1, int &tile, int &split) const {
+    split = u % S;
+    tile = u / S;
+    const int group = tile / (kGroupM * nN);
+    const int first_m = group * kGroupM;
+    const int gm = min(kGroupM, nM - first_m);
+    const int r = tile - group * kGroupM * nN;
+    m = first_m + r % gm;
+    n = r / gm;
+    kb0 = split * kbs;
+    kb1 = min(KB, kb0 + kbs);
+  }
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -51,6 +112,10 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
@@ -71,8 +136,10 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for the phase of `bar` with the given parity to complete; false after ~2 s.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Wait for the phase of `bar` with the given parity; false after ~2 s or
+// once another role of the CTA has aborted (then it also returns false).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_try_wait(addr, parity)) return true;
   const uint64_t t0 = global_ns();
@@ -80,7 +147,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(addr, parity)) return true;
-    if (global_ns() - t0 > 2000000000ull) return false;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > 2000000000ull) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusWaitTimeout);
+      return false;
+    }
   }
 }
 
@@ -112,12 +184,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accum) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accum)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
       : "memory");
 }
 
@@ -145,115 +218,272 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Bias + epilogue store (+ fused argmax candidate) of one 32-column run.
+__device__ __forceinline__ void finish_run(const EpiParams &epi, int row, int col, float *v, int cnt,
+                                           unsigned long long &best) {
+  epi_apply<__nv_bfloat16, 32>(epi, row, col, v, cnt);
+  if (epi.argmax_keys != nullptr) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < cnt && v[i] == v[i]) {
+        const unsigned long long k = argmax_key(v[i], col + i);
+        best = k > best ? k : best;
+      }
+  }
+}
+
+template <int BN>
 __global__ void __launch_bounds__(192, 1)
-    gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, int M,
-                        int N, int K, EpiParams epi, int32_t *status) {
+    gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, int M_arg,
+                        const int32_t *M_dev, int N, int K, int sm, EpiParams epi, GemmScratch scr,
+                        int32_t *status) {
+  using C = Cfg<BN>;
+  constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *sA = smem_raw + pad;
-  uint8_t *sB = sA + STAGES * A_BYTES;
-  uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
-  uint64_t *empty = full + STAGES;
-  uint64_t *done = empty + STAGES;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  uint8_t *sB = sA + ST * C::A_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sB + ST * C::B_BYTES);
+  uint64_t *empty = full + ST;
+  uint64_t *tfull = empty + ST;
+  uint64_t *tempty = tfull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-  const int KB = K / BK;
+  const int M = M_dev != nullptr ? *M_dev : M_arg;
+  Sched sc;
+  sc.init(M, N, K, BN, sm, scr);
 
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < ST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(done, 1);
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 4);
+    mbar_init(&tempty[1], 4);
+    *abort_flag = 0;
+    *last_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
   }
-  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u)) {
-          atomicOr(status, kStatusWaitTimeout);
-          break;
+    if (lane == 0) {  // TMA producer
+      int it = 0;
+      for (int u = blockIdx.x; u < sc.units; u += gridDim.x) {
+        int m, n, kb0, kb1, tile, split;
+        sc.unit(u, m, n, kb0, kb1, tile, split);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % ST;
+          const uint32_t ph = (uint32_t)(it / ST) & 1u;
+          // once the CTA has aborted no further copy is issued
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status) || *abort_flag) continue;
+          mbar_expect_tx(&full[s], C::STAGE);
+          tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * BK, m * BM, &full[s]);
+#pragma unroll
+          for (int h = 0; h < BN / kTcBM; ++h)
+            tma_load_2d(sB + s * C::B_BYTES + h * (kTcBM * BK * 2), &tmW, kb * BK, n * BN + h * kTcBM, &full[s]);
         }
-        mbar_expect_tx(&full[s], A_BYTES + B_BYTES);
-        tma_load_2d(sA + s * A_BYTES, &tmA, kb * BK, m0, &full[s]);
-        tma_load_2d(sB + s * B_BYTES, &tmW, kb * BK, n0, &full[s]);
+      }
+      if (*abort_flag) {  // let copies issued before the abort land before the CTA exits
+        const uint64_t t0 = global_ns();
+        while (global_ns() - t0 < 100000ull) {
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-        if (!mbar_wait(&full[s], ph)) {
-          atomicOr(status, kStatusWaitTimeout);
-          break;
-        }
+    if (lane == 0) {  // MMA issuer
+      int it = 0, i = 0;
+      for (int u = blockIdx.x; u < sc.units; u += gridDim.x, ++i) {
+        int m, n, kb0, kb1, tile, split;
+        sc.unit(u, m, n, kb0, kb1, tile, split);
+        const int acc = i & 1;
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+        mbar_wait(&tempty[acc], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, status);
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + s * A_BYTES);
-        const uint32_t b0 = smem_u32(sB + s * B_BYTES);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % ST;
+          const uint32_t ph = (uint32_t)(it / ST) & 1u;
+          if (mbar_wait(&full[s], ph, abort_flag, status)) {
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
+            const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          tc_mma(tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), (kb > 0 || k > 0) ? 1u : 0u);
-        tc_commit(&empty[s]);
+            for (int k = 0; k < BK / 16; ++k)
+              tc_mma(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), C::IDESC,
+                     (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+        }
+        tc_commit(&tfull[acc]);
       }
-      tc_commit(done);
     }
-  } else {
-    // warp-uniform decision: tcgen05.ld below is .sync.aligned
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0));
-    if (!ok && lane == 0) atomicOr(status, kStatusWaitTimeout);
-    tc_fence_after();
-    const int quarter = warp & 3;
-    const int row = m0 + quarter * 32 + lane;
-    if (ok) {
+  } else {  // epilogue warps 2..5: TMEM lane quarter = warp % 4
+    const int q = warp & 3;
+    int i = 0;
+    for (int u = blockIdx.x; u < sc.units; u += gridDim.x, ++i) {
+      int m, n, kb0, kb1, tile, split;
+      sc.unit(u, m, n, kb0, kb1, tile, split);
+      const int acc = i & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], (uint32_t)(i >> 1) & 1u, abort_flag, status));
+      tc_fence_after();
+      const int row = m * BM + q * 32 + lane;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      unsigned long long best = 0ull;
+      if (sc.S == 1) {
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
-        const int col = n0 + c;
-        if (row < M && col < N) epi_apply<__nv_bfloat16, 32>(epi, row, col, v, min(32, N - col));
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          if (ok) tmem_ld32(tbase + (uint32_t)c, v);
+          if (c + 32 == BN) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          const int col = n * BN + c;
+          if (ok && row < M && col < N) finish_run(epi, row, col, v, min(32, N - col), best);
+        }
+      } else {
+        float *part = scr.partials + ((size_t)(tile * sc.S + split) * BM + q * 32 + lane) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          if (ok) tmem_ld32(tbase + (uint32_t)c, v);
+          if (c + 32 == BN) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          if (ok && row < M) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4 *>(part + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          }
+        }
+        __threadfence();
+        epi_barrier();
+        if (threadIdx.x == 64) *last_flag = atomicAdd(scr.counters + tile, 1) == sc.S - 1;
+        epi_barrier();
+        if (*last_flag) {
+          __threadfence();
+          if (threadIdx.x == 64) scr.counters[tile] = 0;
+          if (ok && row < M) {
+            const float *p0 = scr.partials + ((size_t)tile * sc.S * BM + q * 32 + lane) * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+              const int col = n * BN + c;
+              if (col >= N) break;
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0.f;
+#pragma unroll 1
+              for (int s = 0; s < sc.S; ++s) {
+                const float4 *ps = reinterpret_cast<const float4 *>(p0 + (size_t)s * BM * BN + c);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 t = __ldcg(ps + j);
+                  v[4 * j] += t.x;
+                  v[4 * j + 1] += t.y;
+                  v[4 * j + 2] += t.z;
+                  v[4 * j + 3] += t.w;
+                }
+              }
+              finish_run(epi, row, col, v, min(32, N - col), best);
+            }
+          }
+        }
       }
+      if (epi.argmax_keys != nullptr && best != 0ull) atomicMax(epi.argmax_keys + row, best);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+template <int BN>
+cudaError_t set_smem_limit(int dev) {
+  static uint64_t attr_mask = 0;  // one bit per device ordinal
+  if (dev >= 64 || !(attr_mask & (1ull << dev))) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_mask |= 1ull << dev;
+  }
+  return cudaSuccess;
+}
+
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, const int32_t *M_dev, int N, int K,
+                      const EpiParams &epi, const GemmScratch &scr, int32_t *status, cudaStream_t st, int sm,
+                      int dev) {
+  cudaError_t e = set_smem_limit<BN>(dev);
+  if (e != cudaSuccess) return e;
+  Sched sc;
+  sc.init(M, N, K, BN, sm, scr);
+  const int grid = M_dev != nullptr ? sm : (sc.units < sm ? sc.units : sm);
+  if (grid <= 0) return cudaSuccess;
+  gemm_tc_bf16_kernel<BN><<<grid, 192, Cfg<BN>::SMEM, st>>>(*tmA, *tmW, M, M_dev, N, K, sm, epi, scr, status);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, int N, int K,
-                                const EpiParams &epi, int32_t *status, cudaStream_t st) {
-  if (M <= 0) return cudaSuccess;
+int gemm_sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 64 && cache[dev]) return cache[dev];
+  int n = 1;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+// 128 x 256 tiles when there are enough of them to fill the GPU, else 128 x 128.
+int gemm_tile_n(int M, int N) {
+  const long long tiles256 = (long long)((M + BM - 1) / BM) * ((N + 255) / 256);
+  return tiles256 >= gemm_sm_count() ? 256 : 128;
+}
+
+cudaError_t gemm_prepare() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = set_smem_limit<128>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<256>(dev);
+  gemm_sm_count();
+  return e;
+}
+
+// M selects the tile width; with M_dev the kernel reads the row count from
+// the device (the tile width chosen from M must then stay valid for it).
+cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, const int32_t *M_dev, int N,
+                                int K, const EpiParams &epi, const GemmScratch &scr, int32_t *status,
+                                cudaStream_t st) {
+  if (M <= 0 && M_dev == nullptr) return cudaSuccess;
   if (K % BK != 0 || K <= 0) return cudaErrorInvalidValue;
-  static uint64_t attr_set_mask = 0;  // one bit per device ordinal
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(attr_set_mask & (1ull << dev))) {
-    e = cudaFuncSetAttribute(gemm_tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set_mask |= 1ull << dev;
-  }
-  dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
-  gemm_tc_bf16_kernel<<<grid, 192, SMEM_BYTES, st>>>(*tmA, *tmW, M, N, K, epi, status);
-  return cudaGetLastError();
+  const int sm = gemm_sm_count();
+  if (gemm_tile_n(M, N) == 256) return launch_bn<256>(tmA, tmW, M, M_dev, N, K, epi, scr, status, st, sm, dev);
+  return launch_bn<128>(tmA, tmW, M, M_dev, N, K, epi, scr, status, st, sm, dev);
 }
 
 }  // namespace orca

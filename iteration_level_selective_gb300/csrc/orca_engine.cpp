@@ -35,6 +35,8 @@ namespace {
 
 constexpr int kMinSplit = 256;   // keys per decode split, at least
 constexpr int kMaxSplits = 16;   // splits per decode row, at most
+constexpr int kGemmMaxSms = 192;  // split-K GEMM: counters (and partial tiles up to one per SM)
+constexpr size_t kGemmPartialBytes = (size_t)kGemmMaxSms * 128 * 256 * 4;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -94,8 +96,10 @@ struct SlotPool {
   }
 };
 
+int32_t max_attn_work(int32_t n_batch, int32_t n_rows);
+
 struct Layout {  // byte offsets into the device workspace
-  size_t x, h, q, u, hf, logits, out, req, row, work, part, counters, total;
+  size_t x, h, q, u, hf, logits, out, req, row, work, part, counters, gemm_cnt, gemm_part, total;
   int max_work;
 };
 
@@ -127,7 +131,7 @@ Layout make_layout(const orca_config *c) {
   const size_t e = elem_bytes(c->dtype);
   const size_t H = c->hidden, F = c->ffn, R = c->max_rows, B = c->max_bs, V = c->vocab;
   const int d = c->hidden / c->n_heads;
-  L.max_work = (c->max_rows + kQTile - 1) / kQTile + c->max_bs + kMaxSplits * c->max_bs;
+  L.max_work = max_attn_work(c->max_bs, c->max_rows);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.x = take(R * H * 4);
@@ -136,17 +140,40 @@ Layout make_layout(const orca_config *c) {
   L.u = take(R * F * e);
   L.hf = take(B * H * e);
   L.logits = take(B * V * 4);
-  L.out = take((B + 1) * 4);
-  L.req = take(B * sizeof(ReqInfo));
+  L.out = take((B + 1) * 8);  // [0] status word, [1..B] packed argmax keys
+  L.req = take(sizeof(DevHeader) + B * sizeof(ReqInfo));  // header, then request records
   L.row = take(R * sizeof(RowInfo));
   L.work = take((size_t)L.max_work * sizeof(AttnWork));
   L.part = take((size_t)L.max_work * c->n_heads * (d + 2) * 4);
   L.counters = take(B * c->n_heads * 4);
+  L.gemm_cnt = take(kGemmMaxSms * 4);
+  L.gemm_part = take(kGemmPartialBytes);
   L.total = o;
   return L;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Keys per decode split for a batch whose longest single-row request reads
+// max_keys keys: at least kMinSplit, and at most kMaxSplits splits per row.
+int attn_split(int max_keys) { return std::max(kMinSplit, (max_keys + kMaxSplits - 1) / kMaxSplits); }
+
+// Work items of request i (rows row .. row+L-1 at positions ctx .. ctx+L-1):
+// query tiles of up to kQTile rows for a multi-row request, key splits for
+// a single-row one.  Returns the new item count.
+int32_t append_attn_work(AttnWork *w, int32_t n, int32_t i, int32_t row, int32_t L, int32_t ctx, int split) {
+  if (L == 1) {
+    const int ns = (ctx + 1 + split - 1) / split;
+    for (int s = 0; s < ns; ++s) w[n++] = {1, i, row, s};
+  } else {
+    for (int t = 0; t < L; t += kQTile) w[n++] = {0, i, row + t, std::min(kQTile, L - t)};
+  }
+  return n;
+}
+
+int32_t max_attn_work(int32_t n_batch, int32_t n_rows) {
+  return (n_rows + kQTile - 1) / kQTile + n_batch + kMaxSplits * n_batch;
+}
 
 }  // namespace
 
@@ -163,10 +190,11 @@ struct orca_engine {
   char *kv = nullptr;
   char *ws = nullptr;
   // pinned host staging
+  DevHeader *h_hdr = nullptr;  // pinned: header followed by the request records
   ReqInfo *h_req = nullptr;
   RowInfo *h_row = nullptr;
   AttnWork *h_work = nullptr;
-  int32_t *h_out = nullptr;  // [0] status, [1..] tokens
+  unsigned long long *h_out = nullptr;  // [0] status word, [1..] packed argmax keys
   // tensor maps (bf16)
   CUtensorMap tm_h{}, tm_u{}, tm_hf{}, tm_emb{};
   std::vector<CUtensorMap> tm_layer;  // 4 per layer: qkv, o, fc1, fc2
@@ -181,6 +209,9 @@ struct orca_engine {
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
   std::vector<Pending> pending;
+  // CUDA graphs of the forward, keyed by GEMM tile choices and logits pointer
+  cudaStream_t cap_stream = nullptr;
+  std::map<std::pair<uint32_t, uintptr_t>, cudaGraphExec_t> graphs;
 };
 
 namespace {
@@ -267,6 +298,178 @@ void prof_collect(orca_engine *e) {
   e->ev_used = 0;
 }
 
+
+// Per-iteration sizes and algorithmic attention work of one iteration.
+struct FwdSizes {
+  int32_t N, B, n_work, split;
+  double attn_pairs, attn_kv_tokens;
+};
+
+// Enqueue the forward of one iteration on `st`: embedding, the layers
+// (LN1, QKV + K/V Split, ragged attention, Attn-Out + residual, LN2, FC1 +
+// GeLU, FC2 + residual), final LN on the last rows, LM head + greedy choice.
+// graph = true: every kernel reads its sizes from the device header and
+// grids are fixed (the sequence is being captured into a CUDA graph);
+// otherwise sizes are passed by value.  Profiling events only when eager.
+int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *logits, bool graph) {
+  const orca_config &c = e->cfg;
+  const int H = c.hidden, F = c.ffn, V = c.vocab, nh = c.n_heads, D = e->head_dim;
+  const bool bf16 = c.dtype == ORCA_DTYPE_BF16;
+  const size_t eb = elem_bytes(c.dtype);
+  const Layout &Ly = e->lay;
+  DevHeader *d_hdr = ws_ptr<DevHeader>(e, Ly.req);
+  ReqInfo *d_req = reinterpret_cast<ReqInfo *>(d_hdr + 1);
+  RowInfo *d_row = ws_ptr<RowInfo>(e, Ly.row);
+  AttnWork *d_work = ws_ptr<AttnWork>(e, Ly.work);
+  unsigned long long *d_out = ws_ptr<unsigned long long>(e, Ly.out);
+  int32_t *status = reinterpret_cast<int32_t *>(d_out);
+  unsigned long long *d_keys = d_out + 1;
+  GemmScratch scr{ws_ptr<float>(e, Ly.gemm_part), kGemmPartialBytes, ws_ptr<int32_t>(e, Ly.gemm_cnt),
+                  std::min(kGemmMaxSms, gemm_sm_count())};
+  float *x = ws_ptr<float>(e, Ly.x);
+  void *h = e->ws + Ly.h;
+  void *q = e->ws + Ly.q;
+  void *u = e->ws + Ly.u;
+  void *hf = e->ws + Ly.hf;
+  const int N = z.N, B = z.B;
+  // graph mode: capacities for grid sizing, device pointers for the sizes
+  const int32_t *N_dev = graph ? &d_hdr->n_rows : nullptr;
+  const int32_t *B_dev = graph ? &d_hdr->n_batch : nullptr;
+  const int N_grid = graph ? c.max_rows : N;
+  const int B_grid = graph ? c.max_bs : B;
+
+  cudaEvent_t ev;
+  prof_begin(e, st, &ev);
+  CUDA_TRY(e, launch_embed(c.dtype, d_row, N_grid, N_dev, e->w[W_TOK], e->w[W_POS], x, H, V, c.max_pos, status, st));
+  prof_end(e, st, ev, ORCA_K_EMBED, 0.0, (double)N * H * (2 * eb + 4));
+
+  const size_t layer_kv = (size_t)2 * nh * c.n_slots * D * eb;
+  const double attn_flops = 4.0 * D * z.attn_pairs * nh;
+  const double attn_bytes = z.attn_kv_tokens * 2 * H * eb + 2.0 * N * H * eb;
+  auto gemm_bytes = [&](double M, double Nn, double K, double out_b) { return (M * K + Nn * K) * eb + M * Nn * out_b; };
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    char *kl = e->kv + (size_t)l * layer_kv;
+    char *vl = kl + layer_kv / 2;
+    // h = LN1(x)
+    prof_begin(e, st, &ev);
+    CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN1_G), (const float *)lw(e, l, L_LN1_B), h,
+                                 N_grid, N_dev, H, nullptr, st));
+    prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
+    // QKV Linear; K/V scattered to the requests' slots (Split)
+    EpiParams ep{};
+    ep.mode = kEpiQKV;
+    ep.ldo = H;
+    ep.bias = (const float *)lw(e, l, L_BQKV);
+    ep.out = q;
+    ep.k_layer = kl;
+    ep.v_layer = vl;
+    ep.rows = d_row;
+    ep.hidden = H;
+    ep.head_dim = D;
+    ep.n_slots = c.n_slots;
+    ep.status = status;
+    prof_begin(e, st, &ev);
+    if (bf16)
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 0], N, N_dev, 3 * H, H, ep, scr, status, st));
+    else
+      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WQKV), N, 3 * H, H, ep, st));
+    prof_end(e, st, ev, ORCA_K_GEMM_QKV, 2.0 * N * 3 * H * H, gemm_bytes(N, 3.0 * H, H, eb));
+    // ragged attention -> h (rows in place: Merge)
+    AttnArgs aa{};
+    aa.q = q;
+    aa.k_layer = kl;
+    aa.v_layer = vl;
+    aa.out = h;
+    aa.reqs = d_req;
+    aa.rows = d_row;
+    aa.work = d_work;
+    aa.part = ws_ptr<float>(e, Ly.part);
+    aa.counters = ws_ptr<int32_t>(e, Ly.counters);
+    aa.status = status;
+    aa.hidden = H;
+    aa.n_heads = nh;
+    aa.n_rows = N;
+    aa.split = z.split;
+    aa.n_work = z.n_work;
+    aa.n_slots = c.n_slots;
+    aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    aa.hdr = graph ? d_hdr : nullptr;
+    prof_begin(e, st, &ev);
+    CUDA_TRY(e, launch_attention(c.dtype, D, aa, graph ? Ly.max_work : z.n_work, st));
+    prof_end(e, st, ev, ORCA_K_ATTENTION, attn_flops, attn_bytes);
+    // x += a Wo + bo
+    EpiParams eo{};
+    eo.mode = kEpiResid;
+    eo.ldo = H;
+    eo.bias = (const float *)lw(e, l, L_BO);
+    eo.out = x;
+    eo.status = status;
+    prof_begin(e, st, &ev);
+    if (bf16)
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 1], N, N_dev, H, H, eo, scr, status, st));
+    else
+      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WO), N, H, H, eo, st));
+    prof_end(e, st, ev, ORCA_K_GEMM_O, 2.0 * N * H * H, gemm_bytes(N, H, H, 8));
+    // h = LN2(x)
+    prof_begin(e, st, &ev);
+    CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN2_G), (const float *)lw(e, l, L_LN2_B), h,
+                                 N_grid, N_dev, H, nullptr, st));
+    prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
+    // u = GeLU(h W1 + b1)
+    EpiParams e1{};
+    e1.mode = kEpiGelu;
+    e1.ldo = F;
+    e1.bias = (const float *)lw(e, l, L_B1);
+    e1.out = u;
+    e1.status = status;
+    prof_begin(e, st, &ev);
+    if (bf16)
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 2], N, N_dev, F, H, e1, scr, status, st));
+    else
+      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_W1), N, F, H, e1, st));
+    prof_end(e, st, ev, ORCA_K_GEMM_FC1, 2.0 * N * F * H, gemm_bytes(N, F, H, eb));
+    // x += u W2 + b2
+    EpiParams e2{};
+    e2.mode = kEpiResid;
+    e2.ldo = H;
+    e2.bias = (const float *)lw(e, l, L_B2);
+    e2.out = x;
+    e2.status = status;
+    prof_begin(e, st, &ev);
+    if (bf16)
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_u, &e->tm_layer[4 * l + 3], N, N_dev, H, F, e2, scr, status, st));
+    else
+      CUDA_TRY(e, launch_gemm_simt_f32((const float *)u, (const float *)lw(e, l, L_W2), N, H, F, e2, st));
+    prof_end(e, st, ev, ORCA_K_GEMM_FC2, 2.0 * N * H * F, gemm_bytes(N, H, F, 8));
+  }
+  // final LayerNorm on each request's last row, LM head (tied), greedy choice
+  prof_begin(e, st, &ev);
+  CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)e->w[W_LNF_G], (const float *)e->w[W_LNF_B], hf, B_grid,
+                               B_dev, H, d_req, st));
+  prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)B * H * (4 + eb));
+  EpiParams el{};
+  el.mode = kEpiLogits;
+  el.ldo = V;
+  el.bias = nullptr;
+  el.out = logits;
+  el.status = status;
+  el.argmax_keys = bf16 ? d_keys : nullptr;
+  CUDA_TRY(e, cudaMemsetAsync(d_keys, 0, sizeof(unsigned long long) * (graph ? c.max_bs : B), st));
+  prof_begin(e, st, &ev);
+  if (bf16)
+    CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_hf, &e->tm_emb, B, B_dev, V, H, el, scr, status, st));
+  else
+    CUDA_TRY(e, launch_gemm_simt_f32((const float *)hf, (const float *)e->w[W_TOK], B, V, H, el, st));
+  prof_end(e, st, ev, ORCA_K_LM_HEAD, 2.0 * B * V * H, gemm_bytes(B, V, H, logits ? 4 : 0));
+  if (!bf16) {
+    prof_begin(e, st, &ev);
+    CUDA_TRY(e, launch_argmax(logits, B, V, nullptr, d_keys, st));
+    prof_end(e, st, ev, ORCA_K_ARGMAX, 0.0, (double)B * V * 4);
+  }
+  return ORCA_OK;
+}
+
 }  // namespace
 
 // ======================================================================= API
@@ -341,12 +544,19 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
   if (cudaGetDevice(&dev) != cudaSuccess) { delete e; return ORCA_ECUDA; }
   e->device = dev;
   const auto &L = e->lay;
-  bool ok = cudaHostAlloc(&e->h_req, sizeof(ReqInfo) * cfg->max_bs, cudaHostAllocDefault) == cudaSuccess &&
+  bool ok = cudaHostAlloc(&e->h_hdr, sizeof(DevHeader) + sizeof(ReqInfo) * cfg->max_bs, cudaHostAllocDefault) ==
+                cudaSuccess &&
+            cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking) == cudaSuccess &&
             cudaHostAlloc(&e->h_row, sizeof(RowInfo) * cfg->max_rows, cudaHostAllocDefault) == cudaSuccess &&
             cudaHostAlloc(&e->h_work, sizeof(AttnWork) * L.max_work, cudaHostAllocDefault) == cudaSuccess &&
-            cudaHostAlloc(&e->h_out, sizeof(int32_t) * (cfg->max_bs + 1), cudaHostAllocDefault) == cudaSuccess;
+            cudaHostAlloc(&e->h_out, sizeof(unsigned long long) * (cfg->max_bs + 1), cudaHostAllocDefault) == cudaSuccess;
   ok = ok && cudaMemset(e->ws + L.counters, 0, (size_t)cfg->max_bs * cfg->n_heads * 4) == cudaSuccess &&
-       cudaMemset(e->ws + L.out, 0, 4) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
+       cudaMemset(e->ws + L.out, 0, 8) == cudaSuccess && cudaMemset(e->ws + L.gemm_cnt, 0, kGemmMaxSms * 4) == cudaSuccess &&
+       cudaDeviceSynchronize() == cudaSuccess;
+  if (ok) {
+    e->h_req = reinterpret_cast<ReqInfo *>(e->h_hdr + 1);
+    ok = gemm_prepare() == cudaSuccess;
+  }
   if (!ok) {
     orca_engine_destroy(e);
     return ORCA_ECUDA;
@@ -376,7 +586,9 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
 int orca_engine_destroy(orca_engine *e) {
   if (!e) return ORCA_EINVAL;
   if (!e->host_only) {
-    cudaFreeHost(e->h_req);
+    for (auto &g : e->graphs) cudaGraphExecDestroy(g.second);
+    if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
+    cudaFreeHost(e->h_hdr);
     cudaFreeHost(e->h_row);
     cudaFreeHost(e->h_work);
     cudaFreeHost(e->h_out);
@@ -478,7 +690,7 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
     if (N > c.max_rows) return fail(e, ORCA_EBATCH, "sum L_i > max_rows %d", c.max_rows);
     if (L[i] == 1) max_keys = std::max<int32_t>(max_keys, r.n_cached + 1);
   }
-  const int split = std::max(kMinSplit, (max_keys + kMaxSplits - 1) / kMaxSplits);
+  const int split = attn_split(max_keys);
   int32_t n_work = 0;
   int32_t row = 0;
   for (int32_t i = 0; i < n_batch; ++i) {
@@ -490,13 +702,7 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
       if (tok < 0 || tok >= V) return fail(e, ORCA_EINVAL, "token id %d out of range", tok);
       e->h_row[row + j] = {tok, pos, i, (int32_t)(r.slot_base + pos)};
     }
-    if (L[i] == 1) {
-      const int n_keys = r.n_cached + 1;
-      const int ns = (n_keys + split - 1) / split;
-      for (int s = 0; s < ns; ++s) e->h_work[n_work++] = {1, i, row, s};
-    } else {
-      for (int t = 0; t < L[i]; t += kQTile) e->h_work[n_work++] = {0, i, row + t, std::min(kQTile, L[i] - t)};
-    }
+    n_work = append_attn_work(e->h_work, n_work, i, row, L[i], r.n_cached, split);
     row += L[i];
   }
   // host copy for orca_last_descriptor / orca_last_transfer
@@ -504,7 +710,7 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
   e->last_N = N;
   e->last_work = n_work;
   e->last_h2d = (int64_t)sizeof(ReqInfo) * n_batch + (int64_t)sizeof(RowInfo) * N + (int64_t)sizeof(AttnWork) * n_work;
-  e->last_d2h = (int64_t)sizeof(int32_t) * (n_batch + 1);
+  e->last_d2h = (int64_t)sizeof(unsigned long long) * (n_batch + 1);
   e->last_row_off.assign(n_batch + 1, 0);
   e->last_last_row.resize(n_batch);
   for (int32_t i = 0; i < n_batch; ++i) {
@@ -521,168 +727,70 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
   // ---- device work, all on `st`
   CUDA_TRY(e, cudaSetDevice(e->device));
   const Layout &Ly = e->lay;
-  ReqInfo *d_req = ws_ptr<ReqInfo>(e, Ly.req);
+  DevHeader *d_hdr = ws_ptr<DevHeader>(e, Ly.req);
   RowInfo *d_row = ws_ptr<RowInfo>(e, Ly.row);
   AttnWork *d_work = ws_ptr<AttnWork>(e, Ly.work);
-  int32_t *d_out = ws_ptr<int32_t>(e, Ly.out);
-  int32_t *status = d_out;
-  float *x = ws_ptr<float>(e, Ly.x);
-  void *h = e->ws + Ly.h;
-  void *q = e->ws + Ly.q;
-  void *u = e->ws + Ly.u;
-  void *hf = e->ws + Ly.hf;
-  float *logits = logits_dev ? logits_dev : ws_ptr<float>(e, Ly.logits);
-  CUDA_TRY(e, cudaMemcpyAsync(d_req, e->h_req, sizeof(ReqInfo) * n_batch, cudaMemcpyHostToDevice, st));
+  unsigned long long *d_out = ws_ptr<unsigned long long>(e, Ly.out);
+  int32_t *status = reinterpret_cast<int32_t *>(d_out);
+  *e->h_hdr = DevHeader{N, n_batch, n_work, split};
+  CUDA_TRY(e, cudaMemcpyAsync(d_hdr, e->h_hdr, sizeof(DevHeader) + sizeof(ReqInfo) * n_batch, cudaMemcpyHostToDevice, st));
   CUDA_TRY(e, cudaMemcpyAsync(d_row, e->h_row, sizeof(RowInfo) * N, cudaMemcpyHostToDevice, st));
   CUDA_TRY(e, cudaMemcpyAsync(d_work, e->h_work, sizeof(AttnWork) * n_work, cudaMemcpyHostToDevice, st));
 
-  cudaEvent_t ev;
-  prof_begin(e, st, &ev);
-  CUDA_TRY(e, launch_embed(c.dtype, d_row, N, e->w[W_TOK], e->w[W_POS], x, H, V, c.max_pos, status, st));
-  prof_end(e, st, ev, ORCA_K_EMBED, 0.0, (double)N * H * (2 * eb + 4));
-
-  const size_t layer_kv = (size_t)2 * nh * c.n_slots * D * eb;
-  // attention algorithmic work: unique K/V bytes, q/out bytes, QK and PV flops
-  double attn_pairs = 0.0, attn_kv_tokens = 0.0;
-  for (int32_t i = 0; i < n_batch; ++i) {
+  FwdSizes z{N, n_batch, n_work, split, 0.0, 0.0};
+  for (int32_t i = 0; i < n_batch; ++i) {  // attention algorithmic work: pairs and unique K/V tokens
     const double cc = pool[batch_idx[i]].n_cached, l = L[i];
-    attn_pairs += l * cc + l * (l + 1) / 2;
-    attn_kv_tokens += cc + l;
+    z.attn_pairs += l * cc + l * (l + 1) / 2;
+    z.attn_kv_tokens += cc + l;
   }
-  const double attn_flops = 4.0 * D * attn_pairs * nh;
-  const double attn_bytes = attn_kv_tokens * 2 * H * eb + 2.0 * N * H * eb;
-  auto gemm_bytes = [&](double M, double Nn, double K, double out_b) { return (M * K + Nn * K) * eb + M * Nn * out_b; };
-
-  for (int l = 0; l < c.n_layers; ++l) {
-    char *kl = e->kv + (size_t)l * layer_kv;
-    char *vl = kl + layer_kv / 2;
-    // h = LN1(x)
-    prof_begin(e, st, &ev);
-    CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN1_G), (const float *)lw(e, l, L_LN1_B), h, N,
-                                 H, nullptr, st));
-    prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
-    // QKV Linear; K/V scattered to the requests' slots (Split)
-    EpiParams ep{};
-    ep.mode = kEpiQKV;
-    ep.ldo = H;
-    ep.bias = (const float *)lw(e, l, L_BQKV);
-    ep.out = q;
-    ep.k_layer = kl;
-    ep.v_layer = vl;
-    ep.rows = d_row;
-    ep.hidden = H;
-    ep.head_dim = D;
-    ep.n_slots = c.n_slots;
-    ep.status = status;
-    prof_begin(e, st, &ev);
-    if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 0], N, 3 * H, H, ep, status, st));
-    else
-      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WQKV), N, 3 * H, H, ep, st));
-    prof_end(e, st, ev, ORCA_K_GEMM_QKV, 2.0 * N * 3 * H * H, gemm_bytes(N, 3.0 * H, H, eb));
-    // ragged attention -> h (rows in place: Merge)
-    AttnArgs aa{};
-    aa.q = q;
-    aa.k_layer = kl;
-    aa.v_layer = vl;
-    aa.out = h;
-    aa.reqs = d_req;
-    aa.rows = d_row;
-    aa.work = d_work;
-    aa.part = ws_ptr<float>(e, Ly.part);
-    aa.counters = ws_ptr<int32_t>(e, Ly.counters);
-    aa.status = status;
-    aa.hidden = H;
-    aa.n_heads = nh;
-    aa.n_rows = N;
-    aa.split = split;
-    aa.n_slots = c.n_slots;
-    aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-    prof_begin(e, st, &ev);
-    CUDA_TRY(e, launch_attention(c.dtype, D, aa, n_work, st));
-    prof_end(e, st, ev, ORCA_K_ATTENTION, attn_flops, attn_bytes);
-    // x += a Wo + bo
-    EpiParams eo{};
-    eo.mode = kEpiResid;
-    eo.ldo = H;
-    eo.bias = (const float *)lw(e, l, L_BO);
-    eo.out = x;
-    eo.status = status;
-    prof_begin(e, st, &ev);
-    if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 1], N, H, H, eo, status, st));
-    else
-      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WO), N, H, H, eo, st));
-    prof_end(e, st, ev, ORCA_K_GEMM_O, 2.0 * N * H * H, gemm_bytes(N, H, H, 8));
-    // h = LN2(x)
-    prof_begin(e, st, &ev);
-    CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN2_G), (const float *)lw(e, l, L_LN2_B), h, N,
-                                 H, nullptr, st));
-    prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
-    // u = GeLU(h W1 + b1)
-    EpiParams e1{};
-    e1.mode = kEpiGelu;
-    e1.ldo = F;
-    e1.bias = (const float *)lw(e, l, L_B1);
-    e1.out = u;
-    e1.status = status;
-    prof_begin(e, st, &ev);
-    if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 2], N, F, H, e1, status, st));
-    else
-      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_W1), N, F, H, e1, st));
-    prof_end(e, st, ev, ORCA_K_GEMM_FC1, 2.0 * N * F * H, gemm_bytes(N, F, H, eb));
-    // x += u W2 + b2
-    EpiParams e2{};
-    e2.mode = kEpiResid;
-    e2.ldo = H;
-    e2.bias = (const float *)lw(e, l, L_B2);
-    e2.out = x;
-    e2.status = status;
-    prof_begin(e, st, &ev);
-    if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_u, &e->tm_layer[4 * l + 3], N, H, F, e2, status, st));
-    else
-      CUDA_TRY(e, launch_gemm_simt_f32((const float *)u, (const float *)lw(e, l, L_W2), N, H, F, e2, st));
-    prof_end(e, st, ev, ORCA_K_GEMM_FC2, 2.0 * N * H * F, gemm_bytes(N, H, F, 8));
+  // bf16: the LM head's epilogue takes the greedy choice itself and writes
+  // logits only when the caller asks for them; fp32: logits, then argmax.
+  float *logits = logits_dev ? logits_dev : (bf16 ? nullptr : ws_ptr<float>(e, Ly.logits));
+  const bool use_graph = bf16 && !e->prof && !(flags & ORCA_ITER_EAGER);
+  if (use_graph) {
+    const uint32_t key = (uint32_t)(gemm_tile_n(N, 3 * H) == 256) | ((uint32_t)(gemm_tile_n(N, H) == 256) << 1) |
+                         ((uint32_t)(gemm_tile_n(N, F) == 256) << 2) | ((uint32_t)(gemm_tile_n(n_batch, V) == 256) << 3);
+    const auto gk = std::make_pair(key, reinterpret_cast<uintptr_t>(logits));
+    auto it = e->graphs.find(gk);
+    if (it == e->graphs.end()) {
+      CUDA_TRY(e, cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal));
+      const int rc = enqueue_forward(e, e->cap_stream, z, logits, true);
+      cudaGraph_t g = nullptr;
+      const cudaError_t ce = cudaStreamEndCapture(e->cap_stream, &g);
+      if (rc) {
+        if (g) cudaGraphDestroy(g);
+        return rc;
+      }
+      if (ce != cudaSuccess) return fail(e, ORCA_ECUDA, "graph capture failed: %s", cudaGetErrorString(ce));
+      cudaGraphExec_t ex = nullptr;
+      const cudaError_t ie = cudaGraphInstantiate(&ex, g, 0);
+      cudaGraphDestroy(g);
+      if (ie != cudaSuccess) return fail(e, ORCA_ECUDA, "graph instantiate failed: %s", cudaGetErrorString(ie));
+      it = e->graphs.emplace(gk, ex).first;
+    }
+    CUDA_TRY(e, cudaGraphLaunch(it->second, st));
+  } else {
+    const int rc = enqueue_forward(e, st, z, logits, false);
+    if (rc) return rc;
   }
-  // final LayerNorm on each request's last row, LM head (tied), greedy argmax
-  prof_begin(e, st, &ev);
-  CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)e->w[W_LNF_G], (const float *)e->w[W_LNF_B], hf, n_batch, H,
-                               d_req, st));
-  prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)n_batch * H * (4 + eb));
-  EpiParams el{};
-  el.mode = kEpiLogits;
-  el.ldo = V;
-  el.bias = nullptr;
-  el.out = logits;
-  el.status = status;
-  prof_begin(e, st, &ev);
-  if (bf16)
-    CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_hf, &e->tm_emb, n_batch, V, H, el, status, st));
-  else
-    CUDA_TRY(e, launch_gemm_simt_f32((const float *)hf, (const float *)e->w[W_TOK], n_batch, V, H, el, st));
-  prof_end(e, st, ev, ORCA_K_LM_HEAD, 2.0 * n_batch * V * H, gemm_bytes(n_batch, V, H, 4));
-  prof_begin(e, st, &ev);
-  CUDA_TRY(e, launch_argmax(logits, n_batch, V, d_out + 1, st));
-  prof_end(e, st, ev, ORCA_K_ARGMAX, 0.0, (double)n_batch * V * 4);
-  CUDA_TRY(e, cudaMemcpyAsync(e->h_out, d_out, sizeof(int32_t) * (n_batch + 1), cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(e, cudaMemcpyAsync(e->h_out, d_out, sizeof(unsigned long long) * (n_batch + 1), cudaMemcpyDeviceToHost, st));
   CUDA_TRY(e, cudaStreamSynchronize(st));
   if (e->prof) prof_collect(e);
-  if (e->h_out[0] != 0) {
-    const int code = e->h_out[0];
+  const int32_t dev_status = (int32_t)(e->h_out[0] & 0xFFFFFFFFull);
+  if (dev_status != 0) {
+    const int code = dev_status;
     cudaMemsetAsync(status, 0, 4, st);
     cudaStreamSynchronize(st);
     return fail(e, ORCA_EDEVICE, "device status word 0x%x (1 wait timeout, 2 bad index, 4 bad shape)", code);
   }
   // ---- Algorithm 1 main loop: returned requests become INCREMENT; finished ones release their slots
   for (int32_t i = 0; i < n_batch; ++i) {
-    const int32_t tok = e->h_out[1 + i];
+    const int32_t tok = argmax_key_col(e->h_out[1 + i]);
     if (tok < 0 || tok >= V) return fail(e, ORCA_EDEVICE, "argmax produced no token (NaN logits?)");
   }
   for (int32_t i = 0; i < n_batch; ++i) {
     orca_request &r = pool[batch_idx[i]];
-    const int32_t tok = e->h_out[1 + i];
+    const int32_t tok = argmax_key_col(e->h_out[1 + i]);
     next_tokens[i] = tok;
     r.state = ORCA_INCREMENT;
     r.n_cached += L[i];
@@ -717,16 +825,87 @@ int orca_last_transfer(const orca_engine *e, int64_t *h2d_bytes, int64_t *d2h_by
   return ORCA_OK;
 }
 
+int orca_attention_workspace_bytes(int32_t n_batch, int32_t n_rows, int32_t n_heads, int32_t head_dim,
+                                   size_t *bytes) {
+  if (!bytes || n_batch <= 0 || n_rows < n_batch || n_heads <= 0 || head_dim <= 0) return ORCA_EINVAL;
+  const size_t mw = max_attn_work(n_batch, n_rows);
+  *bytes = align_up(sizeof(ReqInfo) * n_batch, 256) + align_up(sizeof(AttnWork) * mw, 256) +
+           align_up(mw * n_heads * (head_dim + 2) * 4, 256) + align_up((size_t)n_batch * n_heads * 4, 256);
+  return ORCA_OK;
+}
+
+int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_slots, const void *q,
+                   const void *k_layer, const void *v_layer, void *out, int32_t n_batch, const int32_t *row_off,
+                   const int32_t *ctx, const int64_t *slot_base, void *workspace, size_t ws_bytes,
+                   int32_t *status_dev, void *stream) {
+  if ((dtype != ORCA_DTYPE_F32 && dtype != ORCA_DTYPE_BF16) || n_heads <= 0 || n_batch <= 0 || !row_off || !ctx ||
+      !slot_base || !q || !k_layer || !v_layer || !out || !workspace || !status_dev || n_slots <= 0 ||
+      n_slots >= INT32_MAX)
+    return ORCA_EINVAL;
+  if (head_dim != 16 && head_dim != 32 && head_dim != 64 && head_dim != 128) return ORCA_EINVAL;
+  const int32_t N = row_off[n_batch];
+  if (row_off[0] != 0 || N <= 0) return ORCA_EINVAL;
+  size_t need = 0;
+  if (orca_attention_workspace_bytes(n_batch, N, n_heads, head_dim, &need) || ws_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return ORCA_EINVAL;
+  std::vector<ReqInfo> req(n_batch);
+  std::vector<AttnWork> work(max_attn_work(n_batch, N));
+  int max_keys = 0;
+  for (int32_t i = 0; i < n_batch; ++i) {
+    const int32_t L = row_off[i + 1] - row_off[i];
+    if (L <= 0 || ctx[i] < 0 || slot_base[i] < 0 || slot_base[i] + ctx[i] + L > n_slots) return ORCA_EINVAL;
+    req[i] = {row_off[i], L, ctx[i], (int32_t)slot_base[i]};
+    if (L == 1) max_keys = std::max(max_keys, ctx[i] + 1);
+  }
+  const int split = attn_split(max_keys);
+  int32_t n_work = 0;
+  for (int32_t i = 0; i < n_batch; ++i) n_work = append_attn_work(work.data(), n_work, i, req[i].row_off, req[i].n_new,
+                                                                  req[i].ctx, split);
+  const size_t mw = work.size();
+  char *ws = static_cast<char *>(workspace);
+  ReqInfo *d_req = reinterpret_cast<ReqInfo *>(ws);
+  AttnWork *d_work = reinterpret_cast<AttnWork *>(ws + align_up(sizeof(ReqInfo) * n_batch, 256));
+  float *d_part = reinterpret_cast<float *>(reinterpret_cast<char *>(d_work) + align_up(sizeof(AttnWork) * mw, 256));
+  int32_t *d_cnt = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(d_part) +
+                                               align_up(mw * n_heads * (head_dim + 2) * 4, 256));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(d_cnt, 0, (size_t)n_batch * n_heads * 4, st) != cudaSuccess ||
+      cudaMemcpyAsync(d_req, req.data(), sizeof(ReqInfo) * n_batch, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(d_work, work.data(), sizeof(AttnWork) * n_work, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return ORCA_ECUDA;
+  AttnArgs aa{};
+  aa.q = q;
+  aa.k_layer = k_layer;
+  aa.v_layer = v_layer;
+  aa.out = out;
+  aa.reqs = d_req;
+  aa.rows = nullptr;
+  aa.work = d_work;
+  aa.part = d_part;
+  aa.counters = d_cnt;
+  aa.status = status_dev;
+  aa.hidden = n_heads * head_dim;
+  aa.n_heads = n_heads;
+  aa.n_rows = N;
+  aa.split = split;
+  aa.n_work = n_work;
+  aa.n_slots = n_slots;
+  aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+  return launch_attention(dtype, head_dim, aa, n_work, st) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
+}
+
 int orca_argmax_rows(const float *logits_dev, int32_t n_rows, int32_t vocab, int32_t *out_dev, void *stream) {
   if (n_rows < 0 || vocab <= 0 || (n_rows > 0 && (!logits_dev || !out_dev))) return ORCA_EINVAL;
-  return launch_argmax(logits_dev, n_rows, vocab, out_dev, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return launch_argmax(logits_dev, n_rows, vocab, out_dev, nullptr, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? ORCA_OK
              : ORCA_ECUDA;
 }
 
 int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const float *bias, void *out, int32_t M,
-                int32_t N, int32_t K, int32_t *status_dev, void *stream) {
-  if (M < 0 || N <= 0 || K <= 0 || (M > 0 && (!A || !W || !out || !status_dev))) return ORCA_EINVAL;
+                int32_t N, int32_t K, void *scratch, size_t scratch_bytes, void *argmax_keys_dev, int32_t *status_dev,
+                void *stream) {
+  if (M < 0 || N <= 0 || K <= 0 || (M > 0 && (!A || !W || !status_dev))) return ORCA_EINVAL;
   if (dtype != ORCA_DTYPE_F32 && dtype != ORCA_DTYPE_BF16) return ORCA_EINVAL;
   if (M == 0) return ORCA_OK;
   EpiParams ep{};
@@ -737,10 +916,13 @@ int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const
     case ORCA_LINEAR_F32OUT: ep.mode = kEpiLogits; break;
     default: return ORCA_EINVAL;
   }
+  if (!out && !(mode == ORCA_LINEAR_F32OUT && argmax_keys_dev)) return ORCA_EINVAL;
+  if (argmax_keys_dev && (mode != ORCA_LINEAR_F32OUT || dtype != ORCA_DTYPE_BF16)) return ORCA_EINVAL;
   ep.ldo = N;
   ep.bias = bias;
   ep.out = out;
   ep.status = status_dev;
+  ep.argmax_keys = static_cast<unsigned long long *>(argmax_keys_dev);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == ORCA_DTYPE_F32) {
     if (mode == ORCA_LINEAR_STORE) ep.mode = kEpiLogits;  // fp32 store
@@ -750,9 +932,19 @@ int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const
                : ORCA_ECUDA;
   }
   if (K % kTcBK) return ORCA_EINVAL;
+  GemmScratch scr{nullptr, 0, nullptr, 0};
+  const size_t cnt_bytes = align_up(kGemmMaxSms * 4, 256);
+  if (scratch && scratch_bytes > cnt_bytes && !(reinterpret_cast<uintptr_t>(scratch) & 255)) {
+    scr.counters = static_cast<int32_t *>(scratch);
+    scr.n_counters = std::min(kGemmMaxSms, gemm_sm_count());
+    scr.partials = reinterpret_cast<float *>(static_cast<char *>(scratch) + cnt_bytes);
+    scr.partial_bytes = scratch_bytes - cnt_bytes;
+    if (cudaMemsetAsync(scratch, 0, kGemmMaxSms * 4, st) != cudaSuccess) return ORCA_ECUDA;
+  }
+  if (argmax_keys_dev && cudaMemsetAsync(argmax_keys_dev, 0, (size_t)M * 8, st) != cudaSuccess) return ORCA_ECUDA;
   CUtensorMap ta, tw;
   if (make_tmap(nullptr, &ta, A, M, K) || make_tmap(nullptr, &tw, W, N, K)) return ORCA_EINVAL;
-  return launch_gemm_tc_bf16(&ta, &tw, M, N, K, ep, status_dev, st) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
+  return launch_gemm_tc_bf16(&ta, &tw, M, nullptr, N, K, ep, scr, status_dev, st) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
 }
 
 int orca_profile_enable(orca_engine *e, int32_t enable) {

@@ -8,6 +8,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 namespace orca {
 
@@ -40,6 +41,15 @@ struct AttnWork {
 
 constexpr int kQTile = 16;
 
+// Per-iteration sizes on the device, read by every kernel of a replayed
+// CUDA graph (the host writes them with the request records).
+struct DevHeader {
+  int32_t n_rows;   // sum L_i
+  int32_t n_batch;  // B
+  int32_t n_work;   // attention work items
+  int32_t split;    // keys per decode split
+};
+
 // Device status word bits (set by kernels, read by the host after the sync).
 enum : int32_t {
   kStatusWaitTimeout = 1,   // an mbarrier wait gave up
@@ -67,6 +77,32 @@ struct EpiParams {
   int32_t hidden, head_dim;
   int64_t n_slots;
   int32_t *status;        // device status word
+  unsigned long long *argmax_keys;  // Logits mode: per-row packed (value, index) max, or nullptr
+};
+
+// Greedy-choice key of (value, column): larger value first, then lower
+// column; NaN never wins.  0 is below every key.
+__host__ __device__ __forceinline__ unsigned long long argmax_key(float v, int col) {
+  unsigned int u;
+#ifdef __CUDA_ARCH__
+  u = __float_as_uint(v);
+#else
+  memcpy(&u, &v, 4);
+#endif
+  const unsigned int ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned int)col);
+}
+__host__ __device__ __forceinline__ int argmax_key_col(unsigned long long key) {
+  return key == 0ull ? -1 : (int)(0xFFFFFFFFu - (unsigned int)(key & 0xFFFFFFFFull));
+}
+
+// Scratch of the split-K tcgen05 GEMM: fp32 partial tiles and one arrival
+// counter per output tile (zero between launches).
+struct GemmScratch {
+  float *partials;
+  size_t partial_bytes;
+  int32_t *counters;
+  int32_t n_counters;
 };
 
 struct AttnArgs {
@@ -80,22 +116,40 @@ struct AttnArgs {
   float *part;            // key-split partials [n_work][n_heads][D + 2]
   int32_t *counters;      // [max_bs][n_heads], zero between launches
   int32_t *status;
-  int32_t hidden, n_heads, n_rows, split;
+  int32_t hidden, n_heads, n_rows, split, n_work;
   int64_t n_slots;
   float scale_log2;       // log2(e) / sqrt(D)
+  const DevHeader *hdr;   // when set, n_rows / n_work / split come from it
 };
 
 // ---- launch wrappers (defined in the .cu files); all return cudaError_t.
-cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows,
+// Row counts: `n_rows` on the host, or *n_rows_dev when given (then n_rows
+// is only the capacity the fixed grid is sized for).
+cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows, const int32_t *n_rows_dev,
                          const void *tok_emb, const void *pos_emb, float *x, int H,
                          int vocab, int max_pos, int32_t *status, cudaStream_t st);
 cudaError_t launch_layernorm(int dtype, const float *x, const float *g, const float *b, void *out,
-                             int n_rows, int H, const ReqInfo *gather_last_row, cudaStream_t st);
-cudaError_t launch_argmax(const float *logits, int n_rows, int vocab, int32_t *out, cudaStream_t st);
+                             int n_rows, const int32_t *n_rows_dev, int H, const ReqInfo *gather_last_row,
+                             cudaStream_t st);
+// Greedy choice per row: column index to `out`, or its packed argmax_key to `keys` when given.
+cudaError_t launch_argmax(const float *logits, int n_rows, int vocab, int32_t *out, unsigned long long *keys,
+                          cudaStream_t st);
 cudaError_t launch_gemm_simt_f32(const float *A, const float *W, int M, int N, int K,
                                  const EpiParams &epi, cudaStream_t st);
-cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, int N, int K,
-                                const EpiParams &epi, int32_t *status, cudaStream_t st);
+// C = A W^T on tcgen05.  M rows (or *M_dev when M_dev is given: the grid is
+// then sized for max_M rows and idle CTAs exit).  Split-K is used when the
+// output has few tiles and `scratch` is large enough.
+cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, const int32_t *M_dev, int N,
+                                int K, const EpiParams &epi, const GemmScratch &scratch, int32_t *status,
+                                cudaStream_t st);
+int gemm_sm_count();
+// Output-tile width (128 or 256) the tcgen05 GEMM uses for an M x N product.
+int gemm_tile_n(int M, int N);
+// Per-device one-time set-up of the GEMM kernels (shared-memory limits);
+// call before any stream capture.
+cudaError_t gemm_prepare();
+// Persistent over (work item, head) pairs; n_work is the host count, or
+// the capacity when args.hdr is set.
 cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &args, int n_work, cudaStream_t st);
 
 // GEMM tile shape of the tcgen05 kernel (used by the host to build TMA maps).

@@ -158,9 +158,9 @@ class ServingLoop:
     next arrival.  step() runs one iteration and returns its record."""
 
     def __init__(self, engine: Engine, pool: RequestPool, teacher_force: bool = False, keep_logits: bool = False,
-                 stream: Optional[torch.cuda.Stream] = None, keep_ids: Optional[set] = None):
+                 stream: Optional[torch.cuda.Stream] = None, keep_ids: Optional[set] = None, eager: bool = False):
         self.eng, self.pool = engine, pool
-        self.flags = C.ORCA_ITER_TEACHER_FORCE if teacher_force else 0
+        self.flags = (C.ORCA_ITER_TEACHER_FORCE if teacher_force else 0) | (C.ORCA_ITER_EAGER if eager else 0)
         keep_logits = keep_logits or keep_ids is not None
         self.keep_logits = keep_logits
         self.keep_ids = keep_ids

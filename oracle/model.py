@@ -22,6 +22,22 @@ from .numerics import gelu_tanh, layer_norm, round_bf16, softmax
 _BF16 = 1
 
 
+def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, n_heads: int) -> np.ndarray:
+    """Multi-head attention of one query row over keys K[0..T), values V[0..T).
+
+    Per head h: softmax(q_h . K_h^T / sqrt(d)) . V_h; heads concatenated
+    (Figure 5: one request's query against its own cached K/V)."""
+    H = q.shape[-1]
+    d = H // n_heads
+    out = np.empty(H)
+    scale = 1.0 / np.sqrt(d)
+    for h in range(n_heads):
+        sl = slice(h * d, (h + 1) * d)
+        p = softmax(K[:, sl] @ q[sl] * scale)
+        out[sl] = p @ V[:, sl]
+    return out
+
+
 class GPTOracle:
     def __init__(self, shape, weights: Dict[str, np.ndarray], layers: Optional[Sequence[int]] = None):
         self.shape = shape
@@ -52,16 +68,7 @@ class GPTOracle:
                 "v": [np.zeros((capacity, self.H)) for _ in self.layers]}
 
     def attend(self, q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
-        """Multi-head attention of one query row over keys K[0..T), values V[0..T).
-
-        Per head h: softmax(q_h . K_h^T / sqrt(d)) . V_h; heads concatenated."""
-        out = np.empty(self.H)
-        scale = 1.0 / np.sqrt(self.d)
-        for h in range(self.nh):
-            sl = slice(h * self.d, (h + 1) * self.d)
-            p = softmax(K[:, sl] @ q[sl] * scale)
-            out[sl] = p @ V[:, sl]
-        return out
+        return attend(q, K, V, self.nh)
 
     def step(self, cache: dict, token: int, pos: int, want_logits: bool = True) -> Optional[np.ndarray]:
         """Feed one token at position `pos`; append its K/V to the cache;

@@ -15,14 +15,15 @@ def max_rel_err(got, want):
 
 
 def run_gpu(shape, host_weights, trace, max_bs, n_slots, max_rows, teacher_force=False, keep_ids=None,
-            keep_all=False):
+            keep_all=False, eager=False):
     import torch
     from iteration_level_selective_gb300 import runtime as rt
     dev = torch.device("cuda:0")
     w = rt.DeviceWeights(shape, dev, host=host_weights)
     eng = rt.Engine(shape, w, max_bs=max_bs, n_slots=n_slots, max_rows=max_rows, device=dev)
     pool = rt.RequestPool(trace, teacher_force=teacher_force)
-    loop = rt.ServingLoop(eng, pool, teacher_force=teacher_force, keep_logits=keep_all, keep_ids=keep_ids)
+    loop = rt.ServingLoop(eng, pool, teacher_force=teacher_force, keep_logits=keep_all, keep_ids=keep_ids,
+                          eager=eager)
     recs = loop.run()
     return recs, eng, pool
 

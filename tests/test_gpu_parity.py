@@ -51,9 +51,10 @@ def test_argmax_forced_logits_bit_exact(cuda):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (300, 1000, 768), (257, 2304, 768), (2048, 3072, 768),
-                                   (64, 50257, 768)])
+                                   (64, 50257, 768), (64, 768, 3072), (130, 2304, 768), (3000, 5120, 1024)])
 @pytest.mark.parametrize("mode", ["store", "gelu", "resid", "f32out"])
-def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode):
+@pytest.mark.parametrize("split", [False, True])
+def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode, split):
     from iteration_level_selective_gb300 import _orca as C
     if mode != "f32out" and N == 50257:
         pytest.skip("vocab-wide output only in fp32")
@@ -75,8 +76,10 @@ def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode):
     status = torch.zeros(1, dtype=torch.int32, device=cuda)
     m = {"store": C.ORCA_LINEAR_STORE, "gelu": C.ORCA_LINEAR_GELU, "resid": C.ORCA_LINEAR_RESID,
          "f32out": C.ORCA_LINEAR_F32OUT}[mode]
+    scratch = torch.empty(64 << 20, dtype=torch.uint8, device=cuda) if split else None
     C.orca_linear(C.ORCA_DTYPE_BF16, m, Ad.data_ptr(), Wd.data_ptr(), bd.data_ptr(), out.data_ptr(), M, N, K,
-                  status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+                  status.data_ptr(), torch.cuda.current_stream().cuda_stream,
+                  scratch_ptr=scratch.data_ptr() if split else 0, scratch_bytes=(64 << 20) if split else 0)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     got = out.double().cpu()
@@ -85,6 +88,31 @@ def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode):
     tol = 2 ** -7 if mode in ("store", "gelu") else 1e-5
     err = (got - ref).abs().max().item() / scale
     assert err < tol, err
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 50257, 768), (64, 50257, 768), (200, 1000, 256), (7, 300, 64)])
+def test_fused_argmax_matches_argmax_of_stored_logits(cuda, M, N, K):
+    """The LM head's fused greedy choice equals the argmax of the same
+    call's fp32 logits, bit for bit (lowest index on ties)."""
+    from iteration_level_selective_gb300 import _orca as C
+    rng = np.random.default_rng(M + N)
+    A = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16).to(cuda)
+    # a few duplicated weight rows create exact ties between columns
+    Wn = (rng.standard_normal((N, K)) * 0.05).astype(np.float32)
+    Wn[N // 2] = Wn[N // 3]
+    W = torch.from_numpy(Wn).to(torch.bfloat16).to(cuda)
+    out = torch.empty((M, N), dtype=torch.float32, device=cuda)
+    keys = torch.full((M,), -1, dtype=torch.int64, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    scratch = torch.empty(64 << 20, dtype=torch.uint8, device=cuda)
+    C.orca_linear(C.ORCA_DTYPE_BF16, C.ORCA_LINEAR_F32OUT, A.data_ptr(), W.data_ptr(), 0, out.data_ptr(), M, N, K,
+                  status.data_ptr(), torch.cuda.current_stream().cuda_stream, scratch_ptr=scratch.data_ptr(),
+                  scratch_bytes=64 << 20, argmax_ptr=keys.data_ptr())
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = [C.argmax_key_column(k) for k in keys.cpu().numpy().tolist()]
+    want = np.argmax(out.cpu().numpy(), axis=1).tolist()
+    assert got == want
 
 
 # ------------------------------------------------------------------ toy fp32: Figure 5
@@ -173,6 +201,26 @@ def test_small_bf16_mixed_prefill_decode_multi_tile(cuda):
         for g, o in zip(got_lg[req.req_id], logits):
             worst = max(worst, hz.max_rel_err(g, o))
     assert worst < BF16_TOL, worst
+
+
+def test_graph_replay_equals_eager_launches(cuda):
+    """The CUDA-graph replay (sizes read from the device descriptor, fixed
+    grids) and eager launches run the same decompositions: identical logits
+    and tokens, iteration by iteration, over a trace whose batches change
+    shape every iteration."""
+    shape = SMALL_BF16
+    w = synth.make_weights(shape, seed=21, w_std=0.05, bias_std=0.02, ln_std=0.1)
+    trace = synth.make_trace(10, (1, 300), (1, 12), vocab=shape.vocab, seed=22, rate_per_iter=0.6, forced=True)
+    out = []
+    for eager in (False, True):
+        recs, eng, pool = hz.run_gpu(shape, w, trace, max_bs=8, n_slots=8000, max_rows=2048, teacher_force=True,
+                                     keep_all=True, eager=eager)
+        out.append(recs)
+        eng.close()
+    assert len(out[0]) == len(out[1])
+    for g, e in zip(*out):
+        assert g.req_ids == e.req_ids and g.next_tokens == e.next_tokens
+        np.testing.assert_array_equal(g.logits, e.logits)
 
 
 # ------------------------------------------------------------------ GPT-2-small, full size, sampled
