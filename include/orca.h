@@ -270,6 +270,28 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
                    const int32_t *row_off, const int32_t *ctx, const int64_t *slot_base, void *workspace,
                    size_t ws_bytes, int32_t *status_dev, void *stream);
 
+/* orca_attention without a workspace, for callers that cannot allocate
+ * device memory.  The Orca pages have no counterpart to this call: it
+ * exists for callers such as a host runtime that owns every device
+ * allocation itself, or code running under a fixed memory budget, which must
+ * not call cudaMalloc (or anything that allocates device memory) where they
+ * run attention.  Arguments are those of orca_attention minus workspace and
+ * ws_bytes; the caller still owns q, the K/V slots and out.  The scratch
+ * (request and work records, key-split partials, counters) is one 8 MiB
+ * array compiled into the library, held on every device that loads it until
+ * the process exits.  A batch whose scratch need (what
+ * orca_attention_workspace_bytes reports) exceeds 8 MiB returns ORCA_EBATCH
+ * before any launch.  The first call on a device, with that device current,
+ * looks up the array's device address once; make that first call before any
+ * stream capture.  All calls share the array and it keeps the last call's
+ * contents; each call clears the counters it uses, and calls that overlap on
+ * the GPU (unordered streams) race on it.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called. */
+int orca_attention_noalloc(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_slots, const void *q,
+                           const void *k_layer, const void *v_layer, void *out, int32_t n_batch,
+                           const int32_t *row_off, const int32_t *ctx, const int64_t *slot_base,
+                           int32_t *status_dev, void *stream);
+
 /* ---------------------------------------------------------------- profiling */
 /* enable != 0: time every launch of every kernel class with CUDA events on
  * the iteration stream (adds event overhead); 0 disables.  Resets stats. */

@@ -66,7 +66,7 @@ EXPORTS = ("orca_kv_pool_bytes", "orca_workspace_bytes", "orca_weight_count", "o
            "orca_engine_destroy", "orca_kv_reserve", "orca_kv_release", "orca_kv_stats", "orca_select_batch",
            "orca_iteration", "orca_last_descriptor", "orca_argmax_rows", "orca_profile_enable",
            "orca_profile_read", "orca_last_error", "orca_linear", "orca_last_transfer",
-           "orca_attention_workspace_bytes", "orca_attention")
+           "orca_attention_workspace_bytes", "orca_attention", "orca_attention_noalloc")
 
 _lib = None
 
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
             "orca_last_transfer": [P, i64p, i64p, i32p],
             "orca_attention_workspace_bytes": [c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)],
             "orca_attention": [c_i32, c_i32, c_i32, c_i64, P, P, P, P, c_i32, i32p, i32p, i64p, P, c_sz, P, P],
+            "orca_attention_noalloc": [c_i32, c_i32, c_i32, c_i64, P, P, P, P, c_i32, i32p, i32p, i64p, P, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -229,6 +230,18 @@ def orca_attention(dtype: int, n_heads: int, head_dim: int, n_slots: int, q_ptr:
                                 ctypes.c_void_p(v_ptr), ctypes.c_void_p(out_ptr), nb, _i32_arr(row_off),
                                 _i32_arr(ctx), _i64_arr(slot_base), ctypes.c_void_p(ws_ptr), ws_bytes,
                                 ctypes.c_void_p(status_ptr), ctypes.c_void_p(stream or None)))
+
+
+def orca_attention_noalloc(dtype: int, n_heads: int, head_dim: int, n_slots: int, q_ptr: int, k_ptr: int,
+                           v_ptr: int, out_ptr: int, row_off, ctx, slot_base, status_ptr: int, stream=0) -> None:
+    """orca_attention with the library's fixed 8 MiB device scratch, for
+    callers that cannot allocate device memory; ORCA_EBATCH if the batch
+    needs more scratch than that."""
+    nb = len(ctx)
+    _check(lib().orca_attention_noalloc(dtype, n_heads, head_dim, n_slots, ctypes.c_void_p(q_ptr),
+                                        ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr), ctypes.c_void_p(out_ptr), nb,
+                                        _i32_arr(row_off), _i32_arr(ctx), _i64_arr(slot_base),
+                                        ctypes.c_void_p(status_ptr), ctypes.c_void_p(stream or None)))
 
 
 def orca_argmax_rows(logits_ptr: int, n_rows: int, vocab: int, out_ptr: int, stream=0) -> None:
