@@ -252,6 +252,7 @@ def run_ours(args, rank: int, world: int):
 
     for _ in range(max(3, args.warmup)):
         step()
+    prev_loop = [loop]
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -261,8 +262,15 @@ def run_ours(args, rank: int, world: int):
     torch.cuda.synchronize(dev)
     w0 = time.perf_counter()
     ev0.record(stream)
+    loop_stats = {"pre": 0.0, "call": 0.0, "post": 0.0}
     for _ in range(args.steps):
+        before = (loop.t_pre, loop.t_call, loop.t_post)
         rec, hb, db = step()
+        cur = loop
+        loop_stats["pre"] += cur.t_pre - (before[0] if cur is prev_loop[0] else 0.0)
+        loop_stats["call"] += cur.t_call - (before[1] if cur is prev_loop[0] else 0.0)
+        loop_stats["post"] += cur.t_post - (before[2] if cur is prev_loop[0] else 0.0)
+        prev_loop[0] = cur
         rows += sum(rec.n_new)
         gen_tok += len(rec.req_ids)
         done += len(rec.released)
@@ -271,6 +279,8 @@ def run_ours(args, rank: int, world: int):
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - w0
+    host = {"pre_ms": loop_stats["pre"] / args.steps * 1e3, "call_ms": loop_stats["call"] / args.steps * 1e3,
+            "post_ms": loop_stats["post"] / args.steps * 1e3}
     clocks = sampler.stop()
     dev_s = ev0.elapsed_time(ev1) / 1000.0
     (dev_s, wall), (rows, gen_tok, done, h2d, d2h) = replicas.reduce_timing(
@@ -331,6 +341,7 @@ def run_ours(args, rank: int, world: int):
         "kernel_time_share": {k: round(v["ms"] / total_ms, 4) for k, v in agg.items()},
         "kernel_ms_per_step": {k: round(v["ms"] / args.steps, 4) for k, v in agg.items()},
         "clocks": clocks,
+        "host_ms_per_step": host,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n_tok, dt, desc = cpu_oracle_sample(args.cpu_seconds)

@@ -41,18 +41,16 @@ __device__ __forceinline__ void store_run(T *dst, const float *v, int cnt) {
       return;
     }
   }
-  for (int i = 0; i < cnt; ++i) dst[i] = cvt_out<T>(v[i]);
+#pragma unroll
+  for (int i = 0; i < CNT; ++i)  // predicated, fully unrolled: v stays in registers
+    if (i < cnt) dst[i] = cvt_out<T>(v[i]);
 }
 
-// Columns n0 .. n0+cnt-1 of row m; v holds the raw accumulators.  CNT must
-// divide head_dim (a run never crosses a head) and hidden.
+// Columns n0 .. n0+cnt-1 of row m; v holds accumulators with the bias
+// already added.  CNT must divide head_dim (a run never crosses a head) and
+// hidden.
 template <typename T, int CNT>
-__device__ __forceinline__ void epi_apply(const EpiParams &e, int m, int n0, float *v, int cnt) {
-  if (e.bias != nullptr) {
-#pragma unroll
-    for (int i = 0; i < CNT; ++i)
-      if (i < cnt) v[i] += __ldg(e.bias + n0 + i);
-  }
+__device__ __forceinline__ void epi_store(const EpiParams &e, int m, int n0, float *v, int cnt) {
   switch (e.mode) {
     case kEpiQKV: {
       const int H = e.hidden;
@@ -85,7 +83,9 @@ __device__ __forceinline__ void epi_apply(const EpiParams &e, int m, int n0, flo
           *reinterpret_cast<float4 *>(xp + i) = o;
         }
       } else {
-        for (int i = 0; i < cnt; ++i) xp[i] += v[i];
+#pragma unroll
+        for (int i = 0; i < CNT; ++i)
+          if (i < cnt) xp[i] += v[i];
       }
       break;
     }
@@ -104,6 +104,17 @@ __device__ __forceinline__ void epi_apply(const EpiParams &e, int m, int n0, flo
       break;
     }
   }
+}
+
+// Bias (per column) then the epilogue store.
+template <typename T, int CNT>
+__device__ __forceinline__ void epi_apply(const EpiParams &e, int m, int n0, float *v, int cnt) {
+  if (e.bias != nullptr) {
+#pragma unroll
+    for (int i = 0; i < CNT; ++i)
+      if (i < cnt) v[i] += __ldg(e.bias + n0 + i);
+  }
+  epi_store<T, CNT>(e, m, n0, v, cnt);
 }
 
 }  // namespace orca

@@ -329,11 +329,13 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) attention_kernel(AttnArgs a) {
   __shared__ __align__(16) unsigned char smem_raw[sizeof(TileSmem<D>) > sizeof(SplitSmem<D>) ? sizeof(TileSmem<D>)
                                                                                              : sizeof(SplitSmem<D>)];
-  if (a.hdr != nullptr) {
+  pdl_trigger();
+  if (a.hdr != nullptr) {  // written before the forward, not by an earlier kernel
     a.n_rows = a.hdr->n_rows;
     a.n_work = a.hdr->n_work;
     a.split = a.hdr->split;
   }
+  pdl_wait();  // q and the K/V slots come from the QKV Linear
   const int total = a.n_work * a.n_heads;
   for (int item = blockIdx.x; item < total; item += gridDim.x) {
     const int w_idx = item / a.n_heads;
@@ -353,13 +355,12 @@ cudaError_t launch_t(int head_dim, const AttnArgs &a, int n_work, cudaStream_t s
   const int cap = 8 * gemm_sm_count();
   dim3 grid(a.hdr != nullptr ? cap : (int)(total < cap ? total : cap));
   switch (head_dim) {
-    case 16: attention_kernel<T, 16><<<grid, kThreads, 0, st>>>(a); break;
-    case 32: attention_kernel<T, 32><<<grid, kThreads, 0, st>>>(a); break;
-    case 64: attention_kernel<T, 64><<<grid, kThreads, 0, st>>>(a); break;
-    case 128: attention_kernel<T, 128><<<grid, kThreads, 0, st>>>(a); break;
+    case 16: return launch_pdl(attention_kernel<T, 16>, grid, kThreads, 0, st, a);
+    case 32: return launch_pdl(attention_kernel<T, 32>, grid, kThreads, 0, st, a);
+    case 64: return launch_pdl(attention_kernel<T, 64>, grid, kThreads, 0, st, a);
+    case 128: return launch_pdl(attention_kernel<T, 128>, grid, kThreads, 0, st, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace

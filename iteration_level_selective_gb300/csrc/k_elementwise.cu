@@ -45,7 +45,9 @@ template <typename T>
 __global__ void embed_kernel(const RowInfo *__restrict__ rows, int n_rows_arg, const int32_t *n_rows_dev,
                              const T *__restrict__ tok_emb, const T *__restrict__ pos_emb, float *__restrict__ x,
                              int H, int vocab, int max_pos, int32_t *status) {
+  pdl_trigger();
   const int n_rows = n_rows_dev ? *n_rows_dev : n_rows_arg;
+  pdl_wait();
   for (int r = blockIdx.x; r < n_rows; r += gridDim.x) {
     const RowInfo ri = rows[r];
     if (ri.tok < 0 || ri.tok >= vocab || ri.pos < 0 || ri.pos >= max_pos) {
@@ -122,12 +124,17 @@ __device__ __forceinline__ void layernorm_row(const float *__restrict__ x, const
 template <typename T, int NV4>
 __global__ void layernorm_kernel(const float *__restrict__ x, const float *__restrict__ g,
                                  const float *__restrict__ b, T *__restrict__ out, int n_rows_arg,
-                                 const int32_t *n_rows_dev, int H, const ReqInfo *__restrict__ gather) {
+                                 const int32_t *n_rows_dev, int H, const ReqInfo *__restrict__ gather,
+                                 unsigned long long *zero_keys) {
+  pdl_trigger();
   const int n_rows = n_rows_dev ? *n_rows_dev : n_rows_arg;
   const int lane = threadIdx.x & 31;
   const int wpc = blockDim.x / 32;
-  for (int row = blockIdx.x * wpc + threadIdx.x / 32; row < n_rows; row += gridDim.x * wpc)
+  pdl_wait();
+  for (int row = blockIdx.x * wpc + threadIdx.x / 32; row < n_rows; row += gridDim.x * wpc) {
     layernorm_row<T, NV4>(x, g, b, out, row, gather ? gather[row].row_off + gather[row].n_new - 1 : row, H, lane);
+    if (zero_keys != nullptr && lane == 0) zero_keys[row] = 0ull;
+  }
 }
 
 // (value, index) order of the greedy choice: larger value wins, equal values
@@ -140,6 +147,8 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 
 __global__ void argmax_kernel(const float *__restrict__ logits, int V, int32_t *__restrict__ out,
                               unsigned long long *__restrict__ keys) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const float *lr = logits + (int64_t)r * V;
   float bv = -INFINITY;
@@ -187,42 +196,43 @@ cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows, const int32
   const int threads = H >= 512 ? 128 : 32;
   const int grid = n_rows < 1184 ? n_rows : 1184;
   if (dtype == 1)
-    embed_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
-        rows, n_rows, n_rows_dev, static_cast<const __nv_bfloat16 *>(tok_emb),
-        static_cast<const __nv_bfloat16 *>(pos_emb), x, H, vocab, max_pos, status);
-  else
-    embed_kernel<float><<<grid, threads, 0, st>>>(rows, n_rows, n_rows_dev, static_cast<const float *>(tok_emb),
-                                                   static_cast<const float *>(pos_emb), x, H, vocab, max_pos, status);
-  return cudaGetLastError();
+    return launch_pdl(embed_kernel<__nv_bfloat16>, grid, threads, 0, st, rows, n_rows, n_rows_dev,
+                      static_cast<const __nv_bfloat16 *>(tok_emb), static_cast<const __nv_bfloat16 *>(pos_emb), x, H,
+                      vocab, max_pos, status);
+  return launch_pdl(embed_kernel<float>, grid, threads, 0, st, rows, n_rows, n_rows_dev,
+                    static_cast<const float *>(tok_emb), static_cast<const float *>(pos_emb), x, H, vocab, max_pos,
+                    status);
 }
 
 template <typename T>
 static cudaError_t layernorm_t(const float *x, const float *g, const float *b, T *out, int n_rows,
-                               const int32_t *n_rows_dev, int H, const ReqInfo *gather, cudaStream_t st) {
+                               const int32_t *n_rows_dev, int H, const ReqInfo *gather, unsigned long long *zk,
+                               cudaStream_t st) {
   const int rows_per_cta = 8;
   int grid = (n_rows + rows_per_cta - 1) / rows_per_cta;
   if (grid > 1184) grid = 1184;
+  const dim3 block(32 * rows_per_cta);
   switch (H) {
-    case 768: layernorm_kernel<T, 6><<<grid, 32 * rows_per_cta, 0, st>>>(x, g, b, out, n_rows, n_rows_dev, H, gather); break;
-    case 1024: layernorm_kernel<T, 8><<<grid, 32 * rows_per_cta, 0, st>>>(x, g, b, out, n_rows, n_rows_dev, H, gather); break;
-    case 2048: layernorm_kernel<T, 16><<<grid, 32 * rows_per_cta, 0, st>>>(x, g, b, out, n_rows, n_rows_dev, H, gather); break;
-    default: layernorm_kernel<T, 0><<<grid, 32 * rows_per_cta, 0, st>>>(x, g, b, out, n_rows, n_rows_dev, H, gather); break;
+    case 768: return launch_pdl(layernorm_kernel<T, 6>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk);
+    case 1024: return launch_pdl(layernorm_kernel<T, 8>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk);
+    case 2048: return launch_pdl(layernorm_kernel<T, 16>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk);
+    default: return launch_pdl(layernorm_kernel<T, 0>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_layernorm(int dtype, const float *x, const float *g, const float *b, void *out, int n_rows,
-                             const int32_t *n_rows_dev, int H, const ReqInfo *gather, cudaStream_t st) {
+                             const int32_t *n_rows_dev, int H, const ReqInfo *gather, unsigned long long *zero_keys,
+                             cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
-  if (dtype == 1) return layernorm_t(x, g, b, static_cast<__nv_bfloat16 *>(out), n_rows, n_rows_dev, H, gather, st);
-  return layernorm_t(x, g, b, static_cast<float *>(out), n_rows, n_rows_dev, H, gather, st);
+  if (dtype == 1)
+    return layernorm_t(x, g, b, static_cast<__nv_bfloat16 *>(out), n_rows, n_rows_dev, H, gather, zero_keys, st);
+  return layernorm_t(x, g, b, static_cast<float *>(out), n_rows, n_rows_dev, H, gather, zero_keys, st);
 }
 
 cudaError_t launch_argmax(const float *logits, int n_rows, int vocab, int32_t *out, unsigned long long *keys,
                           cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
-  argmax_kernel<<<n_rows, 512, 0, st>>>(logits, vocab, out, keys);
-  return cudaGetLastError();
+  return launch_pdl(argmax_kernel, n_rows, 512, 0, st, logits, vocab, out, keys);
 }
 
 }  // namespace orca

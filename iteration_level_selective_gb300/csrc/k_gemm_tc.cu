@@ -45,12 +45,14 @@ constexpr int kGroupM = 8;
 
 template <int BN>
 struct Cfg {
-  // W tiles arrive as BN/128 TMA boxes of 128 rows (the tensor maps' box).
-  static_assert(BN % kTcBM == 0 && BN <= 256, "BN must be 128 or 256");
+  // W tiles arrive as boxes of min(BN, 128) rows: one box for BN <= 128
+  // (tensor map with that box height), two 128-row boxes for BN = 256.
+  static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN must be 32, 64, 128 or 256");
+  static constexpr int BOX = BN < kTcBM ? BN : kTcBM;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (kStageBudget / STAGE) > 8 ? 8 : (kStageBudget / STAGE);
+  static constexpr int STAGES = (kStageBudget / STAGE) > 12 ? 12 : (kStageBudget / STAGE);
   static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   // Instruction descriptor, kind::f16: D fp32 (bit 4), A bf16 (bits 7-9),
@@ -220,10 +222,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
 
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Bias + epilogue store (+ fused argmax candidate) of one 32-column run.
-__device__ __forceinline__ void finish_run(const EpiParams &epi, int row, int col, float *v, int cnt,
+// Bias + epilogue store (+ fused argmax candidate) of one 32-column run of
+// this thread's row.  Every lane of the warp calls it (the bias of the 32
+// columns is one coalesced load, broadcast by shuffles); `active` masks rows
+// beyond M.
+__device__ __forceinline__ void finish_run(const EpiParams &epi, int row, int col, float *v, int cnt, bool active,
                                            unsigned long long &best) {
-  epi_apply<__nv_bfloat16, 32>(epi, row, col, v, cnt);
+  if (epi.bias != nullptr) {
+    const int lane = threadIdx.x & 31;
+    const float bl = col + lane < col + cnt ? __ldg(epi.bias + col + lane) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] += __shfl_sync(0xffffffffu, bl, i);
+  }
+  if (!active) return;
+  epi_store<__nv_bfloat16, 32>(epi, row, col, v, cnt);
   if (epi.argmax_keys != nullptr) {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
@@ -253,7 +265,9 @@ __global__ void __launch_bounds__(192, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *last_flag = abort_flag + 1;
 
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // M_dev is the descriptor header, written before the forward (not by an earlier kernel)
   const int M = M_dev != nullptr ? *M_dev : M_arg;
   Sched sc;
   sc.init(M, N, K, BN, sm, scr);
@@ -282,20 +296,41 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
+      // The weights do not depend on earlier kernels: the first stages' W
+      // tiles are requested before waiting for them, so their latency
+      // overlaps the previous kernel's tail.
+      int pre = 0;
+      if ((int)blockIdx.x < sc.units) {
+        int m, n, kb0, kb1, tile, split;
+        sc.unit(blockIdx.x, m, n, kb0, kb1, tile, split);
+        pre = min(ST, kb1 - kb0);
+        for (int j = 0; j < pre; ++j) {  // ring round 0: the stages are free
+          mbar_expect_tx(&full[j], C::STAGE);
+#pragma unroll
+          for (int h = 0; h < BN / C::BOX; ++h)
+            tma_load_2d(sB + j * C::B_BYTES + h * (C::BOX * BK * 2), &tmW, (kb0 + j) * BK, n * BN + h * C::BOX,
+                        &full[j]);
+        }
+      }
+      pdl_wait();  // A (activations) comes from earlier kernels
       int it = 0;
       for (int u = blockIdx.x; u < sc.units; u += gridDim.x) {
         int m, n, kb0, kb1, tile, split;
         sc.unit(u, m, n, kb0, kb1, tile, split);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % ST;
+          if (it < pre) {  // W already requested
+            tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * BK, m * BM, &full[s]);
+            continue;
+          }
           const uint32_t ph = (uint32_t)(it / ST) & 1u;
           // once the CTA has aborted no further copy is issued
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status) || *abort_flag) continue;
           mbar_expect_tx(&full[s], C::STAGE);
           tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * BK, m * BM, &full[s]);
 #pragma unroll
-          for (int h = 0; h < BN / kTcBM; ++h)
-            tma_load_2d(sB + s * C::B_BYTES + h * (kTcBM * BK * 2), &tmW, kb * BK, n * BN + h * kTcBM, &full[s]);
+          for (int h = 0; h < BN / C::BOX; ++h)
+            tma_load_2d(sB + s * C::B_BYTES + h * (C::BOX * BK * 2), &tmW, kb * BK, n * BN + h * C::BOX, &full[s]);
         }
       }
       if (*abort_flag) {  // let copies issued before the abort land before the CTA exits
@@ -332,6 +367,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {  // epilogue warps 2..5: TMEM lane quarter = warp % 4
+    pdl_wait();  // the epilogue reads / writes buffers of earlier kernels (x, K/V slots)
     const int q = warp & 3;
     int i = 0;
     for (int u = blockIdx.x; u < sc.units; u += gridDim.x, ++i) {
@@ -354,7 +390,7 @@ __global__ void __launch_bounds__(192, 1)
             if (lane == 0) mbar_arrive(&tempty[acc]);
           }
           const int col = n * BN + c;
-          if (ok && row < M && col < N) finish_run(epi, row, col, v, min(32, N - col), best);
+          if (ok && col < N) finish_run(epi, row, col, v, min(32, N - col), row < M, best);
         }
       } else {
         float *part = scr.partials + ((size_t)(tile * sc.S + split) * BM + q * 32 + lane) * BN;
@@ -380,7 +416,7 @@ __global__ void __launch_bounds__(192, 1)
         if (*last_flag) {
           __threadfence();
           if (threadIdx.x == 64) scr.counters[tile] = 0;
-          if (ok && row < M) {
+          if (ok) {
             const float *p0 = scr.partials + ((size_t)tile * sc.S * BM + q * 32 + lane) * BN;
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
@@ -390,7 +426,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = 0.f;
 #pragma unroll 1
-              for (int s = 0; s < sc.S; ++s) {
+              for (int s = 0; s < sc.S && row < M; ++s) {
                 const float4 *ps = reinterpret_cast<const float4 *>(p0 + (size_t)s * BM * BN + c);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -401,7 +437,7 @@ __global__ void __launch_bounds__(192, 1)
                   v[4 * j + 3] += t.w;
                 }
               }
-              finish_run(epi, row, col, v, min(32, N - col), best);
+              finish_run(epi, row, col, v, min(32, N - col), row < M, best);
             }
           }
         }
@@ -439,8 +475,8 @@ cudaError_t launch_bn(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, con
   sc.init(M, N, K, BN, sm, scr);
   const int grid = M_dev != nullptr ? sm : (sc.units < sm ? sc.units : sm);
   if (grid <= 0) return cudaSuccess;
-  gemm_tc_bf16_kernel<BN><<<grid, 192, Cfg<BN>::SMEM, st>>>(*tmA, *tmW, M, M_dev, N, K, sm, epi, scr, status);
-  return cudaGetLastError();
+  return launch_pdl(gemm_tc_bf16_kernel<BN>, grid, 192, Cfg<BN>::SMEM, st, *tmA, *tmW, M, M_dev, N, K, sm, epi, scr,
+                    status);
 }
 
 }  // namespace
@@ -456,15 +492,23 @@ int gemm_sm_count() {
   return n;
 }
 
-// 128 x 256 tiles when there are enough of them to fill the GPU, else 128 x 128.
+// Output-tile width: 256 when those tiles fill the GPU, else the widest of
+// 128 / 64 / 32 whose tiles occupy at least half the SMs (narrower tiles
+// spread a small-M product's weight stream over more SMs).
 int gemm_tile_n(int M, int N) {
-  const long long tiles256 = (long long)((M + BM - 1) / BM) * ((N + 255) / 256);
-  return tiles256 >= gemm_sm_count() ? 256 : 128;
+  const long long nM = (M + BM - 1) / BM;
+  const int sm = gemm_sm_count();
+  if (nM * ((N + 255) / 256) >= sm) return 256;
+  if (nM * ((N + 127) / 128) * 2 >= sm) return 128;
+  if (nM * ((N + 63) / 64) * 2 >= sm) return 64;
+  return 32;
 }
 
 cudaError_t gemm_prepare() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = set_smem_limit<32>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<64>(dev);
   if (e == cudaSuccess) e = set_smem_limit<128>(dev);
   if (e == cudaSuccess) e = set_smem_limit<256>(dev);
   gemm_sm_count();
@@ -473,7 +517,7 @@ cudaError_t gemm_prepare() {
 
 // M selects the tile width; with M_dev the kernel reads the row count from
 // the device (the tile width chosen from M must then stay valid for it).
-cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, const int32_t *M_dev, int N,
+cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const WeightMaps &W, int M, const int32_t *M_dev, int N,
                                 int K, const EpiParams &epi, const GemmScratch &scr, int32_t *status,
                                 cudaStream_t st) {
   if (M <= 0 && M_dev == nullptr) return cudaSuccess;
@@ -482,8 +526,12 @@ cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const CUtensorMap *tmW, 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const int sm = gemm_sm_count();
-  if (gemm_tile_n(M, N) == 256) return launch_bn<256>(tmA, tmW, M, M_dev, N, K, epi, scr, status, st, sm, dev);
-  return launch_bn<128>(tmA, tmW, M, M_dev, N, K, epi, scr, status, st, sm, dev);
+  switch (gemm_tile_n(M, N)) {
+    case 256: return launch_bn<256>(tmA, &W.box128, M, M_dev, N, K, epi, scr, status, st, sm, dev);
+    case 128: return launch_bn<128>(tmA, &W.box128, M, M_dev, N, K, epi, scr, status, st, sm, dev);
+    case 64: return launch_bn<64>(tmA, &W.box64, M, M_dev, N, K, epi, scr, status, st, sm, dev);
+    default: return launch_bn<32>(tmA, &W.box32, M, M_dev, N, K, epi, scr, status, st, sm, dev);
+  }
 }
 
 }  // namespace orca

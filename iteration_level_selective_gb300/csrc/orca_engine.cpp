@@ -196,8 +196,9 @@ struct orca_engine {
   AttnWork *h_work = nullptr;
   unsigned long long *h_out = nullptr;  // [0] status word, [1..] packed argmax keys
   // tensor maps (bf16)
-  CUtensorMap tm_h{}, tm_u{}, tm_hf{}, tm_emb{};
-  std::vector<CUtensorMap> tm_layer;  // 4 per layer: qkv, o, fc1, fc2
+  CUtensorMap tm_h{}, tm_u{}, tm_hf{};
+  WeightMaps tm_emb{};
+  std::vector<WeightMaps> tm_layer;  // 4 per layer: qkv, o, fc1, fc2
   // last descriptor (host copy)
   int32_t last_B = 0, last_N = 0, last_work = 0;
   int64_t last_h2d = 0, last_d2h = 0;
@@ -237,7 +238,8 @@ int fail(orca_engine *e, int code, const char *fmt, ...) {
 
 template <typename T> T *ws_ptr(orca_engine *e, size_t off) { return reinterpret_cast<T *>(e->ws + off); }
 
-int make_tmap(orca_engine *e, CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols) {
+int make_tmap(orca_engine *e, CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols,
+              uint32_t box_rows) {
   if (!g_encode) {
     cudaDriverEntryPointQueryResult q;
     void *fn = nullptr;
@@ -249,13 +251,20 @@ int make_tmap(orca_engine *e, CUtensorMap *tm, const void *base, uint64_t rows, 
   if (reinterpret_cast<uintptr_t>(base) & 15) return fail(e, ORCA_EINVAL, "TMA base must be 16-byte aligned");
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)kTcBM};
+  cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(e, ORCA_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return ORCA_OK;
+}
+
+int make_weight_maps(orca_engine *e, WeightMaps *w, const void *base, uint64_t rows, uint64_t cols) {
+  int rc = make_tmap(e, &w->box128, base, rows, cols, 128);
+  if (!rc) rc = make_tmap(e, &w->box64, base, rows, cols, 64);
+  if (!rc) rc = make_tmap(e, &w->box32, base, rows, cols, 32);
+  return rc;
 }
 
 // Weight pointer index helpers (order documented in orca.h).
@@ -354,7 +363,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     // h = LN1(x)
     prof_begin(e, st, &ev);
     CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN1_G), (const float *)lw(e, l, L_LN1_B), h,
-                                 N_grid, N_dev, H, nullptr, st));
+                                 N_grid, N_dev, H, nullptr, nullptr, st));
     prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
     // QKV Linear; K/V scattered to the requests' slots (Split)
     EpiParams ep{};
@@ -371,7 +380,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     ep.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 0], N, N_dev, 3 * H, H, ep, scr, status, st));
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 0], N, N_dev, 3 * H, H, ep, scr, status, st));
     else
       CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WQKV), N, 3 * H, H, ep, st));
     prof_end(e, st, ev, ORCA_K_GEMM_QKV, 2.0 * N * 3 * H * H, gemm_bytes(N, 3.0 * H, H, eb));
@@ -407,14 +416,14 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     eo.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 1], N, N_dev, H, H, eo, scr, status, st));
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 1], N, N_dev, H, H, eo, scr, status, st));
     else
       CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WO), N, H, H, eo, st));
     prof_end(e, st, ev, ORCA_K_GEMM_O, 2.0 * N * H * H, gemm_bytes(N, H, H, 8));
     // h = LN2(x)
     prof_begin(e, st, &ev);
     CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN2_G), (const float *)lw(e, l, L_LN2_B), h,
-                                 N_grid, N_dev, H, nullptr, st));
+                                 N_grid, N_dev, H, nullptr, nullptr, st));
     prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
     // u = GeLU(h W1 + b1)
     EpiParams e1{};
@@ -425,7 +434,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     e1.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, &e->tm_layer[4 * l + 2], N, N_dev, F, H, e1, scr, status, st));
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 2], N, N_dev, F, H, e1, scr, status, st));
     else
       CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_W1), N, F, H, e1, st));
     prof_end(e, st, ev, ORCA_K_GEMM_FC1, 2.0 * N * F * H, gemm_bytes(N, F, H, eb));
@@ -438,15 +447,16 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     e2.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_u, &e->tm_layer[4 * l + 3], N, N_dev, H, F, e2, scr, status, st));
+      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_u, e->tm_layer[4 * l + 3], N, N_dev, H, F, e2, scr, status, st));
     else
       CUDA_TRY(e, launch_gemm_simt_f32((const float *)u, (const float *)lw(e, l, L_W2), N, H, F, e2, st));
     prof_end(e, st, ev, ORCA_K_GEMM_FC2, 2.0 * N * H * F, gemm_bytes(N, H, F, 8));
   }
   // final LayerNorm on each request's last row, LM head (tied), greedy choice
   prof_begin(e, st, &ev);
+  // (also zeroes the argmax keys the LM head's epilogue max-reduces into)
   CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)e->w[W_LNF_G], (const float *)e->w[W_LNF_B], hf, B_grid,
-                               B_dev, H, d_req, st));
+                               B_dev, H, d_req, d_keys, st));
   prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)B * H * (4 + eb));
   EpiParams el{};
   el.mode = kEpiLogits;
@@ -455,10 +465,9 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
   el.out = logits;
   el.status = status;
   el.argmax_keys = bf16 ? d_keys : nullptr;
-  CUDA_TRY(e, cudaMemsetAsync(d_keys, 0, sizeof(unsigned long long) * (graph ? c.max_bs : B), st));
   prof_begin(e, st, &ev);
   if (bf16)
-    CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_hf, &e->tm_emb, B, B_dev, V, H, el, scr, status, st));
+    CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_hf, e->tm_emb, B, B_dev, V, H, el, scr, status, st));
   else
     CUDA_TRY(e, launch_gemm_simt_f32((const float *)hf, (const float *)e->w[W_TOK], B, V, H, el, st));
   prof_end(e, st, ev, ORCA_K_LM_HEAD, 2.0 * B * V * H, gemm_bytes(B, V, H, logits ? 4 : 0));
@@ -564,15 +573,15 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
   if (cfg->dtype == ORCA_DTYPE_BF16) {
     const uint64_t H = cfg->hidden, F = cfg->ffn;
     e->tm_layer.resize(4 * cfg->n_layers);
-    rc = make_tmap(e, &e->tm_h, e->ws + L.h, cfg->max_rows, H);
-    if (!rc) rc = make_tmap(e, &e->tm_u, e->ws + L.u, cfg->max_rows, F);
-    if (!rc) rc = make_tmap(e, &e->tm_hf, e->ws + L.hf, cfg->max_bs, H);
-    if (!rc) rc = make_tmap(e, &e->tm_emb, e->w[W_TOK], cfg->vocab, H);
+    rc = make_tmap(e, &e->tm_h, e->ws + L.h, cfg->max_rows, H, kTcBM);
+    if (!rc) rc = make_tmap(e, &e->tm_u, e->ws + L.u, cfg->max_rows, F, kTcBM);
+    if (!rc) rc = make_tmap(e, &e->tm_hf, e->ws + L.hf, cfg->max_bs, H, kTcBM);
+    if (!rc) rc = make_weight_maps(e, &e->tm_emb, e->w[W_TOK], cfg->vocab, H);
     for (int l = 0; l < cfg->n_layers && !rc; ++l) {
-      rc = make_tmap(e, &e->tm_layer[4 * l + 0], lw(e, l, L_WQKV), 3 * H, H);
-      if (!rc) rc = make_tmap(e, &e->tm_layer[4 * l + 1], lw(e, l, L_WO), H, H);
-      if (!rc) rc = make_tmap(e, &e->tm_layer[4 * l + 2], lw(e, l, L_W1), F, H);
-      if (!rc) rc = make_tmap(e, &e->tm_layer[4 * l + 3], lw(e, l, L_W2), H, F);
+      rc = make_weight_maps(e, &e->tm_layer[4 * l + 0], lw(e, l, L_WQKV), 3 * H, H);
+      if (!rc) rc = make_weight_maps(e, &e->tm_layer[4 * l + 1], lw(e, l, L_WO), H, H);
+      if (!rc) rc = make_weight_maps(e, &e->tm_layer[4 * l + 2], lw(e, l, L_W1), F, H);
+      if (!rc) rc = make_weight_maps(e, &e->tm_layer[4 * l + 3], lw(e, l, L_W2), H, F);
     }
     if (rc) {
       orca_engine_destroy(e);
@@ -748,8 +757,9 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
   float *logits = logits_dev ? logits_dev : (bf16 ? nullptr : ws_ptr<float>(e, Ly.logits));
   const bool use_graph = bf16 && !e->prof && !(flags & ORCA_ITER_EAGER);
   if (use_graph) {
-    const uint32_t key = (uint32_t)(gemm_tile_n(N, 3 * H) == 256) | ((uint32_t)(gemm_tile_n(N, H) == 256) << 1) |
-                         ((uint32_t)(gemm_tile_n(N, F) == 256) << 2) | ((uint32_t)(gemm_tile_n(n_batch, V) == 256) << 3);
+    auto code = [](int bn) { return (uint32_t)(bn == 256 ? 3 : bn == 128 ? 2 : bn == 64 ? 1 : 0); };
+    const uint32_t key = code(gemm_tile_n(N, 3 * H)) | (code(gemm_tile_n(N, H)) << 2) |
+                         (code(gemm_tile_n(N, F)) << 4) | (code(gemm_tile_n(n_batch, V)) << 6);
     const auto gk = std::make_pair(key, reinterpret_cast<uintptr_t>(logits));
     auto it = e->graphs.find(gk);
     if (it == e->graphs.end()) {
@@ -942,9 +952,10 @@ int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const
     if (cudaMemsetAsync(scratch, 0, kGemmMaxSms * 4, st) != cudaSuccess) return ORCA_ECUDA;
   }
   if (argmax_keys_dev && cudaMemsetAsync(argmax_keys_dev, 0, (size_t)M * 8, st) != cudaSuccess) return ORCA_ECUDA;
-  CUtensorMap ta, tw;
-  if (make_tmap(nullptr, &ta, A, M, K) || make_tmap(nullptr, &tw, W, N, K)) return ORCA_EINVAL;
-  return launch_gemm_tc_bf16(&ta, &tw, M, nullptr, N, K, ep, scr, status_dev, st) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
+  CUtensorMap ta;
+  WeightMaps tw;
+  if (make_tmap(nullptr, &ta, A, M, K, kTcBM) || make_weight_maps(nullptr, &tw, W, N, K)) return ORCA_EINVAL;
+  return launch_gemm_tc_bf16(&ta, tw, M, nullptr, N, K, ep, scr, status_dev, st) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
 }
 
 int orca_profile_enable(orca_engine *e, int32_t enable) {

@@ -10,6 +10,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <utility>
+
 namespace orca {
 
 // One request of the batch.
@@ -128,18 +130,26 @@ struct AttnArgs {
 cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows, const int32_t *n_rows_dev,
                          const void *tok_emb, const void *pos_emb, float *x, int H,
                          int vocab, int max_pos, int32_t *status, cudaStream_t st);
+// zero_keys (optional): per-row argmax keys set to 0 (final LayerNorm, ahead
+// of the LM head's fused greedy choice).
 cudaError_t launch_layernorm(int dtype, const float *x, const float *g, const float *b, void *out,
                              int n_rows, const int32_t *n_rows_dev, int H, const ReqInfo *gather_last_row,
-                             cudaStream_t st);
+                             unsigned long long *zero_keys, cudaStream_t st);
 // Greedy choice per row: column index to `out`, or its packed argmax_key to `keys` when given.
 cudaError_t launch_argmax(const float *logits, int n_rows, int vocab, int32_t *out, unsigned long long *keys,
                           cudaStream_t st);
 cudaError_t launch_gemm_simt_f32(const float *A, const float *W, int M, int N, int K,
                                  const EpiParams &epi, cudaStream_t st);
+// TMA maps of one weight matrix [N, K] with 128-, 64- and 32-row boxes
+// (the GEMM picks its output-tile width per product).
+struct WeightMaps {
+  CUtensorMap box128, box64, box32;
+};
+
 // C = A W^T on tcgen05.  M rows (or *M_dev when M_dev is given: the grid is
 // then sized for max_M rows and idle CTAs exit).  Split-K is used when the
 // output has few tiles and `scratch` is large enough.
-cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, const int32_t *M_dev, int N,
+cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const WeightMaps &W, int M, const int32_t *M_dev, int N,
                                 int K, const EpiParams &epi, const GemmScratch &scratch, int32_t *status,
                                 cudaStream_t st);
 int gemm_sm_count();
@@ -156,5 +166,32 @@ cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &args, int 
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 128;
 constexpr int kTcBK = 64;
+
+// ---- programmatic dependent launch (PDL)
+// Every kernel of the iteration is launched with programmatic stream
+// serialisation: it calls pdl_trigger() on entry so the next kernel may
+// start launching, and pdl_wait() before it touches anything an earlier
+// kernel wrote (work before that point may only read weights, the descriptor
+// header copied before the forward, or set up shared / tensor memory).
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace orca

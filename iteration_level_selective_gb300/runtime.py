@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import ctypes
 import dataclasses
+import time
 from typing import Dict, List, Optional, Sequence
 
 import numpy as np
@@ -110,6 +111,13 @@ class Engine:
             pass
 
 
+# numpy view of orca_request (same layout as the C struct)
+REQUEST_DTYPE = np.dtype([("req_id", "<i8"), ("arrival", "<i8"), ("state", "<i4"), ("n_prompt", "<i4"),
+                          ("max_tokens", "<i4"), ("out_len", "<i4"), ("n_cached", "<i4"), ("n_generated", "<i4"),
+                          ("slot_base", "<i8"), ("tokens", "<u8")])
+assert REQUEST_DTYPE.itemsize == ctypes.sizeof(C.orca_request)
+
+
 class RequestPool:
     """ctypes array of orca_request with numpy token buffers, in arrival order."""
 
@@ -131,6 +139,8 @@ class RequestPool:
                                          n_prompt=r.n_prompt, max_tokens=r.max_tokens, out_len=r.out_len,
                                          n_cached=0, n_generated=0, slot_base=-1,
                                          tokens=buf.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+        self.view = np.frombuffer(self.arr, dtype=REQUEST_DTYPE)   # shares memory with arr
+        self.arrivals = np.array([r.arrival for r in reqs], dtype=np.int64)
 
     def reset(self):
         for i, r in enumerate(self.reqs):
@@ -167,47 +177,58 @@ class ServingLoop:
         self.stream = stream if stream is not None else torch.cuda.current_stream(engine.device)
         self.batch_idx = (ctypes.c_int32 * engine.max_bs)()
         self.next_tok = (ctypes.c_int32 * engine.max_bs)()
+        self._bi = np.frombuffer(self.batch_idx, dtype=np.int32)
+        self._nt = np.frombuffer(self.next_tok, dtype=np.int32)
         self.logits = (torch.empty((engine.max_bs, engine.shape.vocab), dtype=torch.float32, device=engine.device)
                        if keep_logits else None)
         self.it = 0
         self.n_arrived = 0
         self.n_done = 0
+        # host seconds spent before / inside / after orca_iteration (diagnostics)
+        self.t_pre = self.t_call = self.t_post = 0.0
 
     def done(self) -> bool:
         return self.n_done >= self.pool.n
 
     def step(self) -> Optional[IterRecord]:
+        t0 = time.perf_counter()
         P = self.pool
         unfinished_arrived = self.n_arrived - self.n_done
-        if unfinished_arrived == 0 and self.n_arrived < P.n and P.reqs[self.n_arrived].arrival > self.it:
-            self.it = P.reqs[self.n_arrived].arrival
-        while self.n_arrived < P.n and P.reqs[self.n_arrived].arrival <= self.it:
-            self.n_arrived += 1
+        if unfinished_arrived == 0 and self.n_arrived < P.n and P.arrivals[self.n_arrived] > self.it:
+            self.it = int(P.arrivals[self.n_arrived])
+        if self.n_arrived < P.n and P.arrivals[self.n_arrived] <= self.it:
+            self.n_arrived = int(np.searchsorted(P.arrivals, self.it, side="right"))
         nb = C.orca_select_batch(self.eng.handle, P.arr, self.n_arrived, self.batch_idx)
         if nb == 0:
             raise RuntimeError(f"no request can be scheduled at iteration {self.it}")
-        idx = [self.batch_idx[i] for i in range(nb)]
-        rec = IterRecord(self.it, [P.arr[i].req_id for i in idx],
-                         [(P.arr[i].n_prompt - P.arr[i].n_cached) if P.arr[i].n_cached < P.arr[i].n_prompt else 1
-                          for i in idx],
-                         [P.arr[i].n_cached for i in idx], [P.arr[i].slot_base for i in idx], [], [])
+        idx = self._bi[:nb].copy()
+        sel = P.view[idx]
+        n_new = np.where(sel["n_cached"] < sel["n_prompt"], sel["n_prompt"] - sel["n_cached"], 1)
+        rec = IterRecord(self.it, sel["req_id"].tolist(), n_new.tolist(), sel["n_cached"].tolist(),
+                         sel["slot_base"].tolist(), [], [])
         lp = self.logits.data_ptr() if self.logits is not None else 0
+        t1 = time.perf_counter()
         C.orca_iteration(self.eng.handle, P.arr, self.batch_idx, nb, self.flags, self.next_tok, lp,
                          self.stream.cuda_stream)
-        rec.next_tokens = [self.next_tok[i] for i in range(nb)]
-        for i in idx:
-            if P.arr[i].state == C.ORCA_FINISHED:
-                rec.released.append(P.arr[i].req_id)
-                self.n_done += 1
+        t2 = time.perf_counter()
+        rec.next_tokens = self._nt[:nb].tolist()
+        done = P.view["state"][idx] == C.ORCA_FINISHED
+        if done.any():
+            rec.released = sel["req_id"][done].tolist()
+            self.n_done += int(done.sum())
         if self.logits is not None:
             if self.keep_ids is None:
                 rec.logits = self.logits[:nb].cpu().numpy()
             else:
                 rows = [k for k, rid in enumerate(rec.req_ids) if rid in self.keep_ids]
                 if rows:
-                    sel = self.logits[torch.tensor(rows, device=self.logits.device)].cpu().numpy()
-                    rec.logits = {rec.req_ids[k]: sel[j] for j, k in enumerate(rows)}
+                    sel_l = self.logits[torch.tensor(rows, device=self.logits.device)].cpu().numpy()
+                    rec.logits = {rec.req_ids[k]: sel_l[j] for j, k in enumerate(rows)}
         self.it += 1
+        t3 = time.perf_counter()
+        self.t_pre += t1 - t0
+        self.t_call += t2 - t1
+        self.t_post += t3 - t2
         return rec
 
     def run(self, max_iters: int = 10_000_000) -> List[IterRecord]:

@@ -51,7 +51,8 @@ def test_argmax_forced_logits_bit_exact(cuda):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (300, 1000, 768), (257, 2304, 768), (2048, 3072, 768),
-                                   (64, 50257, 768), (64, 768, 3072), (130, 2304, 768), (3000, 5120, 1024)])
+                                   (64, 50257, 768), (64, 768, 3072), (130, 2304, 768), (3000, 5120, 1024),
+                                   (600, 2304, 768)])
 @pytest.mark.parametrize("mode", ["store", "gelu", "resid", "f32out"])
 @pytest.mark.parametrize("split", [False, True])
 def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode, split):
