@@ -229,7 +229,7 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
 #pragma unroll
   for (int j = 0; j < VN; ++j) acc[j] = 0.f;
   // Warp-uniform trip count so every lane joins the shuffles.
-#pragma unroll 2
+#pragma unroll 4
   for (int base = kb + wid * KPW; base < ke; base += NW * KPW) {
     const int k = base + grp;
     const bool valid = k < ke;
@@ -291,7 +291,8 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
     if (dim < D) O[dim] = from_f<T>(A / L);
     return;
   }
-  float *part = a.part + ((int64_t)w_idx * a.n_heads + head) * (D + 2);
+  // partial slot of (request, split): independent of the work-list order
+  float *part = a.part + ((int64_t)(w.req * kMaxSplits + w.b) * a.n_heads + head) * (D + 2);
   if (dim < D) part[dim] = A;
   if (dim == 0) {
     part[D] = M;
@@ -306,14 +307,14 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   __syncthreads();
   if (!sm.last) return;
   __threadfence();
-  const int w0 = w_idx - w.b;  // the row's splits are consecutive work items
+  const int64_t s0 = (int64_t)w.req * kMaxSplits;  // the row's split partials
   if (dim < D) {
     float Mx = -INFINITY;
     for (int j = 0; j < n_splits; ++j)
-      Mx = fmaxf(Mx, __ldcg(a.part + ((int64_t)(w0 + j) * a.n_heads + head) * (D + 2) + D));
+      Mx = fmaxf(Mx, __ldcg(a.part + ((s0 + j) * a.n_heads + head) * (D + 2) + D));
     float Lx = 0.f, Ax = 0.f;
     for (int j = 0; j < n_splits; ++j) {
-      const float *pj = a.part + ((int64_t)(w0 + j) * a.n_heads + head) * (D + 2);
+      const float *pj = a.part + ((s0 + j) * a.n_heads + head) * (D + 2);
       const float mj = __ldcg(pj + D);
       const float c = mj == -INFINITY ? 0.f : exp2f(mj - Mx);
       Lx += __ldcg(pj + D + 1) * c;
@@ -324,11 +325,14 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   if (threadIdx.x == 0) a.counters[(int64_t)w.req * a.n_heads + head] = 0;
 }
 
-// Persistent: CTA b takes (work item, head) pairs b, b + gridDim.x, ...
+// Persistent: each CTA takes (work item, head) pairs from an atomic ticket
+// (the host orders the work list longest first) until none is left; the
+// last CTA to finish resets the ticket for the next launch.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) attention_kernel(AttnArgs a) {
   __shared__ __align__(16) unsigned char smem_raw[sizeof(TileSmem<D>) > sizeof(SplitSmem<D>) ? sizeof(TileSmem<D>)
                                                                                              : sizeof(SplitSmem<D>)];
+  __shared__ int s_item;
   pdl_trigger();
   if (a.hdr != nullptr) {  // written before the forward, not by an earlier kernel
     a.n_rows = a.hdr->n_rows;
@@ -337,28 +341,58 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(AttnArgs a) {
   }
   pdl_wait();  // q and the K/V slots come from the QKV Linear
   const int total = a.n_work * a.n_heads;
-  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+  while (true) {
+    __syncthreads();  // the previous item's shared-memory reads are done
+    if (threadIdx.x == 0) s_item = atomicAdd(a.ticket, 1);
+    __syncthreads();
+    const int item = s_item;
+    if (item >= total) break;
     const int w_idx = item / a.n_heads;
     const int head = item - w_idx * a.n_heads;
     const AttnWork w = a.work[w_idx];
-    __syncthreads();  // the previous item's shared-memory reads are done
     if (w.kind == 0)
       query_tile<T, D>(a, w, head, *reinterpret_cast<TileSmem<D> *>(smem_raw));
     else
       key_split<T, D>(a, w, w_idx, head, *reinterpret_cast<SplitSmem<D> *>(smem_raw));
   }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.ticket + 1, 1) == (int)gridDim.x - 1) {  // every CTA has left the loop
+      a.ticket[0] = 0;
+      a.ticket[1] = 0;
+    }
+  }
+}
+
+// CTAs that fit on the GPU at once (one wave) for this instantiation.
+template <typename T, int D>
+int resident_ctas() {
+  static int cache[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && cache[dev]) return cache[dev];
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_kernel<T, D>, kThreads, 0);
+  const int n = (per_sm > 0 ? per_sm : 1) * gemm_sm_count();
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+template <typename T, int D>
+cudaError_t launch_d(const AttnArgs &a, int n_work, cudaStream_t st) {
+  const long long total = (long long)n_work * a.n_heads;
+  const int cap = resident_ctas<T, D>();
+  const dim3 grid(a.hdr != nullptr ? cap : (int)(total < cap ? total : cap));
+  return launch_pdl(attention_kernel<T, D>, grid, kThreads, 0, st, a);
 }
 
 template <typename T>
 cudaError_t launch_t(int head_dim, const AttnArgs &a, int n_work, cudaStream_t st) {
-  const long long total = (long long)n_work * a.n_heads;
-  const int cap = 8 * gemm_sm_count();
-  dim3 grid(a.hdr != nullptr ? cap : (int)(total < cap ? total : cap));
   switch (head_dim) {
-    case 16: return launch_pdl(attention_kernel<T, 16>, grid, kThreads, 0, st, a);
-    case 32: return launch_pdl(attention_kernel<T, 32>, grid, kThreads, 0, st, a);
-    case 64: return launch_pdl(attention_kernel<T, 64>, grid, kThreads, 0, st, a);
-    case 128: return launch_pdl(attention_kernel<T, 128>, grid, kThreads, 0, st, a);
+    case 16: return launch_d<T, 16>(a, n_work, st);
+    case 32: return launch_d<T, 32>(a, n_work, st);
+    case 64: return launch_d<T, 64>(a, n_work, st);
+    case 128: return launch_d<T, 128>(a, n_work, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -34,7 +34,6 @@ using namespace orca;
 namespace {
 
 constexpr int kMinSplit = 256;   // keys per decode split, at least
-constexpr int kMaxSplits = 16;   // splits per decode row, at most
 constexpr int kGemmMaxSms = 192;  // split-K GEMM: counters (and partial tiles up to one per SM)
 constexpr size_t kGemmPartialBytes = (size_t)kGemmMaxSms * 128 * 256 * 4;
 
@@ -144,8 +143,8 @@ Layout make_layout(const orca_config *c) {
   L.req = take(sizeof(DevHeader) + B * sizeof(ReqInfo));  // header, then request records
   L.row = take(R * sizeof(RowInfo));
   L.work = take((size_t)L.max_work * sizeof(AttnWork));
-  L.part = take((size_t)L.max_work * c->n_heads * (d + 2) * 4);
-  L.counters = take(B * c->n_heads * 4);
+  L.part = take((size_t)B * kMaxSplits * c->n_heads * (d + 2) * 4);
+  L.counters = take((B * c->n_heads + 2) * 4);  // split arrivals, then the work ticket
   L.gemm_cnt = take(kGemmMaxSms * 4);
   L.gemm_part = take(kGemmPartialBytes);
   L.total = o;
@@ -154,9 +153,18 @@ Layout make_layout(const orca_config *c) {
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// Keys per decode split for a batch whose longest single-row request reads
-// max_keys keys: at least kMinSplit, and at most kMaxSplits splits per row.
-int attn_split(int max_keys) { return std::max(kMinSplit, (max_keys + kMaxSplits - 1) / kMaxSplits); }
+// Keys per decode split.  Rows are split only when the batch's (row, head)
+// pairs cannot fill the persistent attention grid: the split then aims at
+// about one item per CTA (sum_keys * n_heads / grid), at least kMinSplit
+// keys, and at most kMaxSplits splits for the longest row (max_keys).
+int attn_split(int max_keys, double sum_keys, int n_heads) {
+  const double grid = 8.0 * gemm_sm_count();
+  int split = (int)std::min<double>(std::max(1.0, sum_keys * n_heads / grid), 1 << 30);
+  split = (split + 63) / 64 * 64;
+  split = std::max(split, kMinSplit);
+  split = std::max(split, (max_keys + kMaxSplits - 1) / kMaxSplits);
+  return split;
+}
 
 // Work items of request i (rows row .. row+L-1 at positions ctx .. ctx+L-1):
 // query tiles of up to kQTile rows for a multi-row request, key splits for
@@ -169,6 +177,19 @@ int32_t append_attn_work(AttnWork *w, int32_t n, int32_t i, int32_t row, int32_t
     for (int t = 0; t < L; t += kQTile) w[n++] = {0, i, row + t, std::min(kQTile, L - t)};
   }
   return n;
+}
+
+// Order work items longest first (query tiles: rows x keys; key splits:
+// keys) so the attention CTAs, which take items from a ticket, finish
+// together.
+void order_attn_work(AttnWork *w, int32_t n, const ReqInfo *req, int split) {
+  auto cost = [&](const AttnWork &x) -> int64_t {
+    const ReqInfo &r = req[x.req];
+    if (x.kind == 0) return (int64_t)x.b * (r.ctx + (x.a - r.row_off) + x.b);
+    const int n_keys = r.ctx + 1;
+    return std::min<int64_t>(split, n_keys - (int64_t)x.b * split);
+  };
+  std::stable_sort(w, w + n, [&](const AttnWork &x, const AttnWork &y) { return cost(x) > cost(y); });
 }
 
 int32_t max_attn_work(int32_t n_batch, int32_t n_rows) {
@@ -395,6 +416,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     aa.work = d_work;
     aa.part = ws_ptr<float>(e, Ly.part);
     aa.counters = ws_ptr<int32_t>(e, Ly.counters);
+    aa.ticket = aa.counters + (size_t)c.max_bs * nh;
     aa.status = status;
     aa.hidden = H;
     aa.n_heads = nh;
@@ -559,7 +581,7 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
             cudaHostAlloc(&e->h_row, sizeof(RowInfo) * cfg->max_rows, cudaHostAllocDefault) == cudaSuccess &&
             cudaHostAlloc(&e->h_work, sizeof(AttnWork) * L.max_work, cudaHostAllocDefault) == cudaSuccess &&
             cudaHostAlloc(&e->h_out, sizeof(unsigned long long) * (cfg->max_bs + 1), cudaHostAllocDefault) == cudaSuccess;
-  ok = ok && cudaMemset(e->ws + L.counters, 0, (size_t)cfg->max_bs * cfg->n_heads * 4) == cudaSuccess &&
+  ok = ok && cudaMemset(e->ws + L.counters, 0, ((size_t)cfg->max_bs * cfg->n_heads + 2) * 4) == cudaSuccess &&
        cudaMemset(e->ws + L.out, 0, 8) == cudaSuccess && cudaMemset(e->ws + L.gemm_cnt, 0, kGemmMaxSms * 4) == cudaSuccess &&
        cudaDeviceSynchronize() == cudaSuccess;
   if (ok) {
@@ -684,6 +706,7 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
   // ---- ragged descriptor (host): rows in batch order, Figure 5
   std::vector<int32_t> L(n_batch);
   int32_t N = 0, max_keys = 0;
+  double sum_keys = 0.0;
   for (int32_t i = 0; i < n_batch; ++i) {
     const orca_request &r = pool[batch_idx[i]];
     if (r.state != ORCA_RUNNING) return fail(e, ORCA_EINVAL, "request %lld is not RUNNING", (long long)r.req_id);
@@ -697,9 +720,12 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
       return fail(e, ORCA_EINVAL, "request %lld: slots beyond n_slots", (long long)r.req_id);
     N += L[i];
     if (N > c.max_rows) return fail(e, ORCA_EBATCH, "sum L_i > max_rows %d", c.max_rows);
-    if (L[i] == 1) max_keys = std::max<int32_t>(max_keys, r.n_cached + 1);
+    if (L[i] == 1) {
+      max_keys = std::max<int32_t>(max_keys, r.n_cached + 1);
+      sum_keys += r.n_cached + 1;
+    }
   }
-  const int split = attn_split(max_keys);
+  const int split = attn_split(max_keys, sum_keys, nh);
   int32_t n_work = 0;
   int32_t row = 0;
   for (int32_t i = 0; i < n_batch; ++i) {
@@ -714,6 +740,7 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
     n_work = append_attn_work(e->h_work, n_work, i, row, L[i], r.n_cached, split);
     row += L[i];
   }
+  order_attn_work(e->h_work, n_work, e->h_req, split);
   // host copy for orca_last_descriptor / orca_last_transfer
   e->last_B = n_batch;
   e->last_N = N;
@@ -840,7 +867,8 @@ int orca_attention_workspace_bytes(int32_t n_batch, int32_t n_rows, int32_t n_he
   if (!bytes || n_batch <= 0 || n_rows < n_batch || n_heads <= 0 || head_dim <= 0) return ORCA_EINVAL;
   const size_t mw = max_attn_work(n_batch, n_rows);
   *bytes = align_up(sizeof(ReqInfo) * n_batch, 256) + align_up(sizeof(AttnWork) * mw, 256) +
-           align_up(mw * n_heads * (head_dim + 2) * 4, 256) + align_up((size_t)n_batch * n_heads * 4, 256);
+           align_up((size_t)n_batch * kMaxSplits * n_heads * (head_dim + 2) * 4, 256) +
+           align_up(((size_t)n_batch * n_heads + 2) * 4, 256);
   return ORCA_OK;
 }
 
@@ -862,25 +890,30 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
   std::vector<ReqInfo> req(n_batch);
   std::vector<AttnWork> work(max_attn_work(n_batch, N));
   int max_keys = 0;
+  double sum_keys = 0.0;
   for (int32_t i = 0; i < n_batch; ++i) {
     const int32_t L = row_off[i + 1] - row_off[i];
     if (L <= 0 || ctx[i] < 0 || slot_base[i] < 0 || slot_base[i] + ctx[i] + L > n_slots) return ORCA_EINVAL;
     req[i] = {row_off[i], L, ctx[i], (int32_t)slot_base[i]};
-    if (L == 1) max_keys = std::max(max_keys, ctx[i] + 1);
+    if (L == 1) {
+      max_keys = std::max(max_keys, ctx[i] + 1);
+      sum_keys += ctx[i] + 1;
+    }
   }
-  const int split = attn_split(max_keys);
+  const int split = attn_split(max_keys, sum_keys, n_heads);
   int32_t n_work = 0;
   for (int32_t i = 0; i < n_batch; ++i) n_work = append_attn_work(work.data(), n_work, i, req[i].row_off, req[i].n_new,
                                                                   req[i].ctx, split);
+  order_attn_work(work.data(), n_work, req.data(), split);
   const size_t mw = work.size();
   char *ws = static_cast<char *>(workspace);
   ReqInfo *d_req = reinterpret_cast<ReqInfo *>(ws);
   AttnWork *d_work = reinterpret_cast<AttnWork *>(ws + align_up(sizeof(ReqInfo) * n_batch, 256));
   float *d_part = reinterpret_cast<float *>(reinterpret_cast<char *>(d_work) + align_up(sizeof(AttnWork) * mw, 256));
   int32_t *d_cnt = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(d_part) +
-                                               align_up(mw * n_heads * (head_dim + 2) * 4, 256));
+                                               align_up((size_t)n_batch * kMaxSplits * n_heads * (head_dim + 2) * 4, 256));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(d_cnt, 0, (size_t)n_batch * n_heads * 4, st) != cudaSuccess ||
+  if (cudaMemsetAsync(d_cnt, 0, ((size_t)n_batch * n_heads + 2) * 4, st) != cudaSuccess ||
       cudaMemcpyAsync(d_req, req.data(), sizeof(ReqInfo) * n_batch, cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaMemcpyAsync(d_work, work.data(), sizeof(AttnWork) * n_work, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return ORCA_ECUDA;
@@ -894,6 +927,7 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
   aa.work = d_work;
   aa.part = d_part;
   aa.counters = d_cnt;
+  aa.ticket = d_cnt + (size_t)n_batch * n_heads;
   aa.status = status_dev;
   aa.hidden = n_heads * head_dim;
   aa.n_heads = n_heads;

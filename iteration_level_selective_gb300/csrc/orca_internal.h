@@ -42,6 +42,7 @@ struct AttnWork {
 };
 
 constexpr int kQTile = 16;
+constexpr int kMaxSplits = 16;  // key splits per decode row, at most
 
 // Per-iteration sizes on the device, read by every kernel of a replayed
 // CUDA graph (the host writes them with the request records).
@@ -115,8 +116,9 @@ struct AttnArgs {
   const ReqInfo *reqs;
   const RowInfo *rows;
   const AttnWork *work;
-  float *part;            // key-split partials [n_work][n_heads][D + 2]
-  int32_t *counters;      // [max_bs][n_heads], zero between launches
+  float *part;            // key-split partials [max_bs * kMaxSplits][n_heads][D + 2]
+  int32_t *counters;      // [max_bs][n_heads] split arrivals, zero between launches
+  int32_t *ticket;        // [2]: next work item, CTAs done; zero between launches
   int32_t *status;
   int32_t hidden, n_heads, n_rows, split, n_work;
   int64_t n_slots;

@@ -51,6 +51,65 @@ def time_linear(M: int, N: int, K: int, reps: int = 20, warmup: int = 3, mode: i
     return {"M": M, "N": N, "K": K, "ms": ms, "tflops": flops / ms / 1e9, "gbs": byts / ms / 1e6}
 
 
+def time_attention(batch, n_heads: int, head_dim: int, reps: int = 5, warmup: int = 2, seed: int = 0):
+    """Time orca_attention on a batch [(L_i, c_i)] with random bf16 K/V slots
+    laid out back to back; returns achieved algorithmic GB/s and TFLOP/s."""
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    row_off, slot_base, s = [0], [], 0
+    for L, c in batch:
+        row_off.append(row_off[-1] + L)
+        slot_base.append(s)
+        s += c + L
+    n_slots, N, H = s, row_off[-1], n_heads * head_dim
+    K = torch.randn((n_heads, n_slots, head_dim), device=dev, generator=g, dtype=torch.bfloat16)
+    V = torch.randn((n_heads, n_slots, head_dim), device=dev, generator=g, dtype=torch.bfloat16)
+    Q = (torch.randn((N, H), device=dev, generator=g) * 0.2).to(torch.bfloat16)
+    out = torch.empty((N, H), device=dev, dtype=torch.bfloat16)
+    ws_bytes = C.orca_attention_workspace_bytes(len(batch), N, n_heads, head_dim)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream()
+    ctx = [c for _, c in batch]
+
+    def run():
+        C.orca_attention(C.ORCA_DTYPE_BF16, n_heads, head_dim, n_slots, Q.data_ptr(), K.data_ptr(), V.data_ptr(),
+                         out.data_ptr(), row_off, ctx, slot_base, ws.data_ptr(), ws_bytes, status.data_ptr(),
+                         st.cuda_stream)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        run()
+        e1.record(st)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = sorted(times)[len(times) // 2]
+    pairs = sum(L * c + L * (L + 1) // 2 for L, c in batch)
+    kv_bytes = sum(c + L for L, c in batch) * 2 * H * 2
+    byts = kv_bytes + 2 * N * H * 2
+    flops = 4.0 * head_dim * pairs * n_heads
+    return {"rows": N, "kv_gb": kv_bytes / 1e9, "ms": ms, "gbs": byts / ms / 1e6, "tflops": flops / ms / 1e9}
+
+
+ATTN_CASES = {
+    # 256 decoding requests, cached contexts U{1024..4096}, 13B-shaped heads (one layer)
+    "c4": lambda rng: ([(1, int(c)) for c in rng.integers(1024, 4097, 256)], 40, 128),
+    # 16 prompts U{1024..2048} + 240 decodes with contexts U{128..2048}, 13B-shaped heads
+    "c5": lambda rng: ([(int(L), 0) for L in rng.integers(1024, 2049, 16)] +
+                       [(1, int(c)) for c in rng.integers(128, 2049, 240)], 40, 128),
+    # one GPT-2-small prefill of 512 tokens plus 63 decodes with contexts U{32..768}
+    "gpt2_mixed": lambda rng: ([(512, 0)] + [(1, int(c)) for c in rng.integers(32, 769, 63)], 12, 64),
+}
+
+
 def main():
     ap = argparse.ArgumentParser()
     sub = ap.add_subparsers(dest="cmd", required=True)
@@ -61,9 +120,18 @@ def main():
     p.add_argument("--reps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
     sub.add_parser("sweep")
+    pa = sub.add_parser("attention")
+    pa.add_argument("--case", choices=sorted(ATTN_CASES), required=True)
+    pa.add_argument("--reps", type=int, default=5)
     a = ap.parse_args()
     B.build()
-    if a.cmd == "linear":
+    if a.cmd == "attention":
+        import numpy as np
+        batch, nh, d = ATTN_CASES[a.case](np.random.default_rng(0))
+        r = time_attention(batch, nh, d, reps=a.reps)
+        r["case"] = a.case
+        print(json.dumps(r))
+    elif a.cmd == "linear":
         print(json.dumps(time_linear(a.M, a.N, a.K, a.reps, a.warmup)))
     else:
         for (N, K) in ((2304, 768), (768, 768), (3072, 768), (768, 3072), (15360, 5120), (5120, 5120),
