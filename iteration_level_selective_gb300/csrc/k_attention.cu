@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "async_copy.cuh"
 #include "orca_internal.h"
 
 namespace orca {
@@ -33,15 +34,16 @@ namespace {
 template <typename T> struct Vec16;
 template <> struct Vec16<float> {
   static constexpr int N = 4;
+  __device__ __forceinline__ static void unpack(const uint4 v, float *o) {
+    o[0] = __uint_as_float(v.x); o[1] = __uint_as_float(v.y); o[2] = __uint_as_float(v.z); o[3] = __uint_as_float(v.w);
+  }
   __device__ __forceinline__ static void load(const float *p, float *o) {
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(p));
-    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+    unpack(__ldg(reinterpret_cast<const uint4 *>(p)), o);
   }
 };
 template <> struct Vec16<__nv_bfloat16> {
   static constexpr int N = 8;
-  __device__ __forceinline__ static void load(const __nv_bfloat16 *p, float *o) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+  __device__ __forceinline__ static void unpack(const uint4 v, float *o) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -49,6 +51,9 @@ template <> struct Vec16<__nv_bfloat16> {
       o[2 * i] = f.x;
       o[2 * i + 1] = f.y;
     }
+  }
+  __device__ __forceinline__ static void load(const __nv_bfloat16 *p, float *o) {
+    unpack(__ldg(reinterpret_cast<const uint4 *>(p)), o);
   }
 };
 
@@ -79,12 +84,28 @@ struct TileSmem {
   float k[kKeyTile][D + 1];
   float v[kKeyTile][D];
 };
-template <int D>
+// Key-split streaming: K and V chunks of kChunkKeys keys flow through a
+// kRing-stage shared-memory ring, filled by 1-D bulk copies (the keys of a
+// request and head are contiguous in the slot pool) issued by thread 0.
+constexpr int kChunkKeys = 32;
+constexpr int kRing = 4;
+
+template <typename T, int D>
 struct SplitSmem {
+  static constexpr int CHUNK = kChunkKeys * D * (int)sizeof(T);  // bytes of one K (or V) chunk
+  alignas(128) unsigned char k[kRing][CHUNK];
+  alignas(128) unsigned char v[kRing][CHUNK];
   float m[kThreads / 32];
   float l[kThreads / 32];
   float acc[kThreads / 32][D];
   int last;
+};
+
+// Ring barriers and flags (static shared memory, set up once per CTA).
+struct Ring {
+  uint64_t full[kRing];   // one arrival (with the copy bytes) per fill
+  uint64_t empty[kRing];  // one arrival per warp per chunk consumed
+  int abort;
 };
 
 // kind 0: rows r0 .. r0+cnt-1 of one request, keys 0 .. last row's position.
@@ -198,9 +219,10 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float *acc, floa
 }
 
 // kind 1: one row over keys [split_idx * split, min(+split, pos + 1)).
+// `g` counts the ring chunks this CTA has consumed (identical in every thread).
 template <typename T, int D>
 __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, int w_idx, int head,
-                                          SplitSmem<D> &sm) {
+                                          SplitSmem<T, D> &sm, Ring &rg, uint32_t &g) {
   constexpr int VN = Vec16<T>::N;
   constexpr int LPK = D / VN;          // lanes per key (16 bytes each)
   constexpr int KPW = 32 / LPK;        // keys per warp step
@@ -212,14 +234,29 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   const int n_splits = (n_keys + a.split - 1) / a.split;
   const int kb = w.b * a.split;
   const int ke = min(kb + a.split, n_keys);
-  if (rq.slot_base < 0 || (int64_t)rq.slot_base + n_keys > a.n_slots || r >= a.n_rows || kb >= n_keys) {
+  if (rq.slot_base < 0 || (int64_t)rq.slot_base + n_keys > a.n_slots || r >= a.n_rows || kb >= n_keys ||
+      w.b >= kMaxSplits) {
     if (threadIdx.x == 0) atomicOr(a.status, kStatusBadIndex);
     return;
   }
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane % LPK, grp = lane / LPK;
-  const T *Kp = static_cast<const T *>(a.k_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D + sub * VN;
-  const T *Vp = static_cast<const T *>(a.v_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D + sub * VN;
+  const T *Kbase = static_cast<const T *>(a.k_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D;
+  const T *Vbase = static_cast<const T *>(a.v_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D;
+  const int n_chunks = (ke - kb + kChunkKeys - 1) / kChunkKeys;
+  auto issue = [&](int c) {  // thread 0: fill the ring stage of chunk c
+    const uint32_t idx = g + (uint32_t)c;
+    const int st = (int)(idx % kRing);
+    if (!mbar_wait(&rg.empty[st], ((idx / kRing) & 1u) ^ 1u, &rg.abort, a.status) || rg.abort) return;
+    const int k0 = kb + c * kChunkKeys;
+    const uint32_t bytes = (uint32_t)(min(kChunkKeys, ke - k0) * D * (int)sizeof(T));
+    mbar_expect_tx(&rg.full[st], 2 * bytes);
+    bulk_load(sm.k[st], Kbase + (int64_t)k0 * D, bytes, &rg.full[st]);
+    bulk_load(sm.v[st], Vbase + (int64_t)k0 * D, bytes, &rg.full[st]);
+  };
+  if (threadIdx.x == 0)
+    for (int c = 0; c < min(kRing - 1, n_chunks); ++c) issue(c);
+
   float q[VN];
   Vec16<T>::load(static_cast<const T *>(a.q) + (int64_t)r * a.hidden + head * D + sub * VN, q);
 #pragma unroll
@@ -228,33 +265,51 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   float m = -INFINITY, l = 0.f, acc[VN];
 #pragma unroll
   for (int j = 0; j < VN; ++j) acc[j] = 0.f;
-  // Warp-uniform trip count so every lane joins the shuffles.
-#pragma unroll 4
-  for (int base = kb + wid * KPW; base < ke; base += NW * KPW) {
-    const int k = base + grp;
-    const bool valid = k < ke;
-    float kv[VN], vv[VN];
-    if (valid) {
-      Vec16<T>::load(Kp + (int64_t)k * D, kv);
-      Vec16<T>::load(Vp + (int64_t)k * D, vv);
-    } else {
+  for (int c = 0; c < n_chunks; ++c) {
+    if (threadIdx.x == 0 && c + kRing - 1 < n_chunks) issue(c + kRing - 1);
+    const uint32_t idx = g + (uint32_t)c;
+    const int st = (int)(idx % kRing);
+    const bool ok = mbar_wait(&rg.full[st], (idx / kRing) & 1u, &rg.abort, a.status);
+    const int nk = min(kChunkKeys, ke - (kb + c * kChunkKeys));
+    const T *ks = reinterpret_cast<const T *>(sm.k[st]);
+    const T *vs = reinterpret_cast<const T *>(sm.v[st]);
+    // warp `wid` takes key groups wid, wid + NW, ... of the chunk (KPW keys
+    // each); warp-uniform trip count so every lane joins the shuffles
 #pragma unroll
-      for (int j = 0; j < VN; ++j) kv[j] = vv[j] = 0.f;
+    for (int j = wid * KPW; j < kChunkKeys; j += NW * KPW) {
+      const int kk = j + grp;
+      const bool valid = ok && kk < nk;
+      float kv[VN], vv[VN];
+      if (valid) {
+        Vec16<T>::unpack(*reinterpret_cast<const uint4 *>(ks + kk * D + sub * VN), kv);
+        Vec16<T>::unpack(*reinterpret_cast<const uint4 *>(vs + kk * D + sub * VN), vv);
+      } else {
+#pragma unroll
+        for (int t = 0; t < VN; ++t) kv[t] = vv[t] = 0.f;
+      }
+      float sc = 0.f;
+#pragma unroll
+      for (int t = 0; t < VN; ++t) sc = fmaf(q[t], kv[t], sc);
+#pragma unroll
+      for (int o = LPK / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
+      if (valid) {
+        if (sc > m) {  // rescale only when the running max grows
+          const float corr = exp2f(m - sc);
+          l *= corr;
+#pragma unroll
+          for (int t = 0; t < VN; ++t) acc[t] *= corr;
+          m = sc;
+        }
+        const float p = exp2f(sc - m);
+        l += p;
+#pragma unroll
+        for (int t = 0; t < VN; ++t) acc[t] = fmaf(p, vv[t], acc[t]);
+      }
     }
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < VN; ++j) s = fmaf(q[j], kv[j], s);
-#pragma unroll
-    for (int o = LPK / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (valid) {
-      const float mn = fmaxf(m, s);
-      const float corr = exp2f(m - mn), p = exp2f(s - mn);
-      l = l * corr + p;
-#pragma unroll
-      for (int j = 0; j < VN; ++j) acc[j] = acc[j] * corr + p * vv[j];
-      m = mn;
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rg.empty[st]);  // this warp is done reading the stage
   }
+  g += (uint32_t)n_chunks;
   // merge the KPW key groups of the warp
 #pragma unroll
   for (int o = LPK; o < 32; o <<= 1) {
@@ -329,10 +384,24 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
 // (the host orders the work list longest first) until none is left; the
 // last CTA to finish resets the ticket for the next launch.
 template <typename T, int D>
+constexpr int attn_smem_bytes() {
+  return (int)(sizeof(TileSmem<D>) > sizeof(SplitSmem<T, D>) ? sizeof(TileSmem<D>) : sizeof(SplitSmem<T, D>));
+}
+
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) attention_kernel(AttnArgs a) {
-  __shared__ __align__(16) unsigned char smem_raw[sizeof(TileSmem<D>) > sizeof(SplitSmem<D>) ? sizeof(TileSmem<D>)
-                                                                                             : sizeof(SplitSmem<D>)];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ Ring rg;
   __shared__ int s_item;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&rg.full[i], 1);
+      mbar_init(&rg.empty[i], kThreads / 32);
+    }
+    rg.abort = 0;
+    mbar_fence_init();
+  }
+  uint32_t g = 0;  // ring chunks consumed
   pdl_trigger();
   if (a.hdr != nullptr) {  // written before the forward, not by an earlier kernel
     a.n_rows = a.hdr->n_rows;
@@ -353,8 +422,9 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(AttnArgs a) {
     if (w.kind == 0)
       query_tile<T, D>(a, w, head, *reinterpret_cast<TileSmem<D> *>(smem_raw));
     else
-      key_split<T, D>(a, w, w_idx, head, *reinterpret_cast<SplitSmem<D> *>(smem_raw));
+      key_split<T, D>(a, w, w_idx, head, *reinterpret_cast<SplitSmem<T, D> *>(smem_raw), rg, g);
   }
+  if (rg.abort) drain_after_abort();
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(a.ticket + 1, 1) == (int)gridDim.x - 1) {  // every CTA has left the loop
@@ -364,15 +434,17 @@ __global__ void __launch_bounds__(kThreads) attention_kernel(AttnArgs a) {
   }
 }
 
-// CTAs that fit on the GPU at once (one wave) for this instantiation.
+// CTAs that fit on the GPU at once (one wave) for this instantiation; the
+// first call on a device also raises the kernel's shared-memory limit.
 template <typename T, int D>
 int resident_ctas() {
   static int cache[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && cache[dev]) return cache[dev];
+  cudaFuncSetAttribute(attention_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem_bytes<T, D>());
   int per_sm = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_kernel<T, D>, kThreads, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_kernel<T, D>, kThreads, attn_smem_bytes<T, D>());
   const int n = (per_sm > 0 ? per_sm : 1) * gemm_sm_count();
   if (dev < 64) cache[dev] = n;
   return n;
@@ -383,7 +455,7 @@ cudaError_t launch_d(const AttnArgs &a, int n_work, cudaStream_t st) {
   const long long total = (long long)n_work * a.n_heads;
   const int cap = resident_ctas<T, D>();
   const dim3 grid(a.hdr != nullptr ? cap : (int)(total < cap ? total : cap));
-  return launch_pdl(attention_kernel<T, D>, grid, kThreads, 0, st, a);
+  return launch_pdl(attention_kernel<T, D>, grid, kThreads, attn_smem_bytes<T, D>(), st, a);
 }
 
 template <typename T>
@@ -402,6 +474,20 @@ cudaError_t launch_t(int head_dim, const AttnArgs &a, int n_work, cudaStream_t s
 cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &a, int n_work, cudaStream_t st) {
   if (n_work <= 0) return cudaSuccess;
   return dtype == 1 ? launch_t<__nv_bfloat16>(head_dim, a, n_work, st) : launch_t<float>(head_dim, a, n_work, st);
+}
+
+// One-time per-device set-up of the attention kernels (shared-memory limits,
+// occupancy); call before any stream capture.
+cudaError_t attention_prepare() {
+  resident_ctas<float, 16>();
+  resident_ctas<float, 32>();
+  resident_ctas<float, 64>();
+  resident_ctas<float, 128>();
+  resident_ctas<__nv_bfloat16, 16>();
+  resident_ctas<__nv_bfloat16, 32>();
+  resident_ctas<__nv_bfloat16, 64>();
+  resident_ctas<__nv_bfloat16, 128>();
+  return cudaGetLastError();
 }
 
 }  // namespace orca

@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "async_copy.cuh"
 #include "epilogue.cuh"
 #include "orca_internal.h"
 
@@ -102,69 +103,6 @@ struct Sched {
     kb1 = min(KB, kb0 + kbs);
   }
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Wait for the phase of `bar` with the given parity; false after ~2 s or
-// once another role of the CTA has aborted (then it also returns false).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status) {
-  const uint32_t addr = smem_u32(bar);
-  if (mbar_try_wait(addr, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(addr, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > 2000000000ull) {
-      *abort_flag = 1;
-      atomicOr(status, kStatusWaitTimeout);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int x, int y, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -284,7 +222,7 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(&tempty[1], 4);
     *abort_flag = 0;
     *last_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
   }
@@ -333,11 +271,7 @@ __global__ void __launch_bounds__(192, 1)
             tma_load_2d(sB + s * C::B_BYTES + h * (C::BOX * BK * 2), &tmW, kb * BK, n * BN + h * C::BOX, &full[s]);
         }
       }
-      if (*abort_flag) {  // let copies issued before the abort land before the CTA exits
-        const uint64_t t0 = global_ns();
-        while (global_ns() - t0 < 100000ull) {
-        }
-      }
+      if (*abort_flag) drain_after_abort();  // copies issued before the abort land first
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer

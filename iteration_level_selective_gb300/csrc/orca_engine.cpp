@@ -586,7 +586,7 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
        cudaDeviceSynchronize() == cudaSuccess;
   if (ok) {
     e->h_req = reinterpret_cast<ReqInfo *>(e->h_hdr + 1);
-    ok = gemm_prepare() == cudaSuccess;
+    ok = gemm_prepare() == cudaSuccess && attention_prepare() == cudaSuccess;
   }
   if (!ok) {
     orca_engine_destroy(e);

@@ -160,6 +160,8 @@ int gemm_tile_n(int M, int N);
 // Per-device one-time set-up of the GEMM kernels (shared-memory limits);
 // call before any stream capture.
 cudaError_t gemm_prepare();
+// Same for the attention kernels.
+cudaError_t attention_prepare();
 // Persistent over (work item, head) pairs; n_work is the host count, or
 // the capacity when args.hdr is set.
 cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &args, int n_work, cudaStream_t st);
