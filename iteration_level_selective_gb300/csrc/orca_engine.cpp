@@ -96,9 +96,10 @@ struct SlotPool {
 };
 
 int32_t max_attn_work(int32_t n_batch, int32_t n_rows);
+int32_t max_tc_work(int32_t n_batch, int32_t n_rows);
 
 struct Layout {  // byte offsets into the device workspace
-  size_t x, h, q, u, hf, logits, out, req, row, work, part, counters, gemm_cnt, gemm_part, total;
+  size_t x, h, q, u, hf, logits, out, req, row, work, work_tc, part, counters, gemm_cnt, gemm_part, total;
   int max_work;
 };
 
@@ -143,8 +144,9 @@ Layout make_layout(const orca_config *c) {
   L.req = take(sizeof(DevHeader) + B * sizeof(ReqInfo));  // header, then request records
   L.row = take(R * sizeof(RowInfo));
   L.work = take((size_t)L.max_work * sizeof(AttnWork));
+  L.work_tc = take((size_t)max_tc_work(c->max_bs, c->max_rows) * sizeof(AttnWork));
   L.part = take((size_t)B * kMaxSplits * c->n_heads * (d + 2) * 4);
-  L.counters = take((B * c->n_heads + 2) * 4);  // split arrivals, then the work ticket
+  L.counters = take((B * c->n_heads + 4) * 4);  // split arrivals, then two work tickets
   L.gemm_cnt = take(kGemmMaxSms * 4);
   L.gemm_part = take(kGemmPartialBytes);
   L.total = o;
@@ -185,12 +187,21 @@ int32_t append_attn_work(AttnWork *w, int32_t n, int32_t i, int32_t row, int32_t
 void order_attn_work(AttnWork *w, int32_t n, const ReqInfo *req, int split) {
   auto cost = [&](const AttnWork &x) -> int64_t {
     const ReqInfo &r = req[x.req];
-    if (x.kind == 0) return (int64_t)x.b * (r.ctx + (x.a - r.row_off) + x.b);
+    if (x.kind != 1) return (int64_t)x.b * (r.ctx + (x.a - r.row_off) + x.b);
     const int n_keys = r.ctx + 1;
     return std::min<int64_t>(split, n_keys - (int64_t)x.b * split);
   };
   std::stable_sort(w, w + n, [&](const AttnWork &x, const AttnWork &y) { return cost(x) > cost(y); });
 }
+
+// Work items of the tensor-core prefill kernel (kind 2): request i's rows in
+// query tiles of up to kTcRows.
+int32_t append_tc_work(AttnWork *w, int32_t n, int32_t i, int32_t row, int32_t L) {
+  for (int t = 0; t < L; t += kTcRows) w[n++] = {2, i, row + t, std::min(kTcRows, L - t)};
+  return n;
+}
+
+int32_t max_tc_work(int32_t n_batch, int32_t n_rows) { return n_rows / kTcMinRows + n_batch; }
 
 int32_t max_attn_work(int32_t n_batch, int32_t n_rows) {
   return (n_rows + kQTile - 1) / kQTile + n_batch + kMaxSplits * n_batch;
@@ -215,9 +226,12 @@ struct orca_engine {
   ReqInfo *h_req = nullptr;
   RowInfo *h_row = nullptr;
   AttnWork *h_work = nullptr;
+  AttnWork *h_work_tc = nullptr;
   unsigned long long *h_out = nullptr;  // [0] status word, [1..] packed argmax keys
   // tensor maps (bf16)
-  CUtensorMap tm_h{}, tm_u{}, tm_hf{};
+  CUtensorMap tm_h{}, tm_u{}, tm_hf{}, tm_q{};
+  std::vector<CUtensorMap> tm_k;      // per layer: K slots as [n_heads * n_slots, head_dim]
+  bool attn_tc = false;               // prompts take the tensor-core prefill kernel
   WeightMaps tm_emb{};
   std::vector<WeightMaps> tm_layer;  // 4 per layer: qkv, o, fc1, fc2
   // last descriptor (host copy)
@@ -331,7 +345,7 @@ void prof_collect(orca_engine *e) {
 
 // Per-iteration sizes and algorithmic attention work of one iteration.
 struct FwdSizes {
-  int32_t N, B, n_work, split;
+  int32_t N, B, n_work, split, n_work_tc;
   double attn_pairs, attn_kv_tokens;
 };
 
@@ -427,6 +441,22 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     aa.hdr = graph ? d_hdr : nullptr;
     prof_begin(e, st, &ev);
+    if (e->attn_tc) {  // prompts: tensor-core tiles; then decodes and short prompts
+      TcAttnArgs ta{};
+      ta.out = h;
+      ta.v_layer = vl;
+      ta.reqs = d_req;
+      ta.work = ws_ptr<AttnWork>(e, Ly.work_tc);
+      ta.ticket = aa.ticket + 2;
+      ta.status = status;
+      ta.hidden = H;
+      ta.n_heads = nh;
+      ta.n_work = z.n_work_tc;
+      ta.n_work_dev = graph ? &d_hdr->n_work_tc : nullptr;
+      ta.n_slots = c.n_slots;
+      ta.scale_log2 = aa.scale_log2;
+      CUDA_TRY(e, launch_attention_tc(D, &e->tm_q, &e->tm_k[l], ta, z.n_work_tc, st));
+    }
     CUDA_TRY(e, launch_attention(c.dtype, D, aa, graph ? Ly.max_work : z.n_work, st));
     prof_end(e, st, ev, ORCA_K_ATTENTION, attn_flops, attn_bytes);
     // x += a Wo + bo
@@ -580,13 +610,15 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
             cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking) == cudaSuccess &&
             cudaHostAlloc(&e->h_row, sizeof(RowInfo) * cfg->max_rows, cudaHostAllocDefault) == cudaSuccess &&
             cudaHostAlloc(&e->h_work, sizeof(AttnWork) * L.max_work, cudaHostAllocDefault) == cudaSuccess &&
+            cudaHostAlloc(&e->h_work_tc, sizeof(AttnWork) * max_tc_work(cfg->max_bs, cfg->max_rows),
+                          cudaHostAllocDefault) == cudaSuccess &&
             cudaHostAlloc(&e->h_out, sizeof(unsigned long long) * (cfg->max_bs + 1), cudaHostAllocDefault) == cudaSuccess;
-  ok = ok && cudaMemset(e->ws + L.counters, 0, ((size_t)cfg->max_bs * cfg->n_heads + 2) * 4) == cudaSuccess &&
+  ok = ok && cudaMemset(e->ws + L.counters, 0, ((size_t)cfg->max_bs * cfg->n_heads + 4) * 4) == cudaSuccess &&
        cudaMemset(e->ws + L.out, 0, 8) == cudaSuccess && cudaMemset(e->ws + L.gemm_cnt, 0, kGemmMaxSms * 4) == cudaSuccess &&
        cudaDeviceSynchronize() == cudaSuccess;
   if (ok) {
     e->h_req = reinterpret_cast<ReqInfo *>(e->h_hdr + 1);
-    ok = gemm_prepare() == cudaSuccess && attention_prepare() == cudaSuccess;
+    ok = gemm_prepare() == cudaSuccess && attention_prepare() == cudaSuccess && attention_tc_prepare() == cudaSuccess;
   }
   if (!ok) {
     orca_engine_destroy(e);
@@ -599,6 +631,15 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
     if (!rc) rc = make_tmap(e, &e->tm_u, e->ws + L.u, cfg->max_rows, F, kTcBM);
     if (!rc) rc = make_tmap(e, &e->tm_hf, e->ws + L.hf, cfg->max_bs, H, kTcBM);
     if (!rc) rc = make_weight_maps(e, &e->tm_emb, e->w[W_TOK], cfg->vocab, H);
+    e->attn_tc = attention_tc_supported(cfg->dtype, e->head_dim);
+    if (!rc && e->attn_tc) {
+      rc = make_tmap(e, &e->tm_q, e->ws + L.q, cfg->max_rows, H, kTcBM);
+      const size_t layer_kv = (size_t)2 * cfg->n_heads * cfg->n_slots * e->head_dim * 2;
+      e->tm_k.resize(cfg->n_layers);
+      for (int l = 0; l < cfg->n_layers && !rc; ++l)
+        rc = make_tmap(e, &e->tm_k[l], e->kv + (size_t)l * layer_kv, (uint64_t)cfg->n_heads * cfg->n_slots,
+                       e->head_dim, kTcBM);
+    }
     for (int l = 0; l < cfg->n_layers && !rc; ++l) {
       rc = make_weight_maps(e, &e->tm_layer[4 * l + 0], lw(e, l, L_WQKV), 3 * H, H);
       if (!rc) rc = make_weight_maps(e, &e->tm_layer[4 * l + 1], lw(e, l, L_WO), H, H);
@@ -622,6 +663,7 @@ int orca_engine_destroy(orca_engine *e) {
     cudaFreeHost(e->h_hdr);
     cudaFreeHost(e->h_row);
     cudaFreeHost(e->h_work);
+    cudaFreeHost(e->h_work_tc);
     cudaFreeHost(e->h_out);
     for (auto ev : e->ev_pool) cudaEventDestroy(ev);
   }
@@ -726,7 +768,7 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
     }
   }
   const int split = attn_split(max_keys, sum_keys, nh);
-  int32_t n_work = 0;
+  int32_t n_work = 0, n_work_tc = 0;
   int32_t row = 0;
   for (int32_t i = 0; i < n_batch; ++i) {
     const orca_request &r = pool[batch_idx[i]];
@@ -737,15 +779,20 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
       if (tok < 0 || tok >= V) return fail(e, ORCA_EINVAL, "token id %d out of range", tok);
       e->h_row[row + j] = {tok, pos, i, (int32_t)(r.slot_base + pos)};
     }
-    n_work = append_attn_work(e->h_work, n_work, i, row, L[i], r.n_cached, split);
+    if (e->attn_tc && L[i] >= kTcMinRows)
+      n_work_tc = append_tc_work(e->h_work_tc, n_work_tc, i, row, L[i]);
+    else
+      n_work = append_attn_work(e->h_work, n_work, i, row, L[i], r.n_cached, split);
     row += L[i];
   }
   order_attn_work(e->h_work, n_work, e->h_req, split);
+  order_attn_work(e->h_work_tc, n_work_tc, e->h_req, split);
   // host copy for orca_last_descriptor / orca_last_transfer
   e->last_B = n_batch;
   e->last_N = N;
   e->last_work = n_work;
-  e->last_h2d = (int64_t)sizeof(ReqInfo) * n_batch + (int64_t)sizeof(RowInfo) * N + (int64_t)sizeof(AttnWork) * n_work;
+  e->last_h2d = (int64_t)sizeof(DevHeader) + (int64_t)sizeof(ReqInfo) * n_batch + (int64_t)sizeof(RowInfo) * N +
+                (int64_t)sizeof(AttnWork) * (n_work + n_work_tc);
   e->last_d2h = (int64_t)sizeof(unsigned long long) * (n_batch + 1);
   e->last_row_off.assign(n_batch + 1, 0);
   e->last_last_row.resize(n_batch);
@@ -768,12 +815,16 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
   AttnWork *d_work = ws_ptr<AttnWork>(e, Ly.work);
   unsigned long long *d_out = ws_ptr<unsigned long long>(e, Ly.out);
   int32_t *status = reinterpret_cast<int32_t *>(d_out);
-  *e->h_hdr = DevHeader{N, n_batch, n_work, split};
+  *e->h_hdr = DevHeader{N, n_batch, n_work, split, n_work_tc, {0, 0, 0}};
   CUDA_TRY(e, cudaMemcpyAsync(d_hdr, e->h_hdr, sizeof(DevHeader) + sizeof(ReqInfo) * n_batch, cudaMemcpyHostToDevice, st));
   CUDA_TRY(e, cudaMemcpyAsync(d_row, e->h_row, sizeof(RowInfo) * N, cudaMemcpyHostToDevice, st));
-  CUDA_TRY(e, cudaMemcpyAsync(d_work, e->h_work, sizeof(AttnWork) * n_work, cudaMemcpyHostToDevice, st));
+  if (n_work > 0)
+    CUDA_TRY(e, cudaMemcpyAsync(d_work, e->h_work, sizeof(AttnWork) * n_work, cudaMemcpyHostToDevice, st));
+  if (n_work_tc > 0)
+    CUDA_TRY(e, cudaMemcpyAsync(ws_ptr<AttnWork>(e, Ly.work_tc), e->h_work_tc, sizeof(AttnWork) * n_work_tc,
+                                cudaMemcpyHostToDevice, st));
 
-  FwdSizes z{N, n_batch, n_work, split, 0.0, 0.0};
+  FwdSizes z{N, n_batch, n_work, split, n_work_tc, 0.0, 0.0};
   for (int32_t i = 0; i < n_batch; ++i) {  // attention algorithmic work: pairs and unique K/V tokens
     const double cc = pool[batch_idx[i]].n_cached, l = L[i];
     z.attn_pairs += l * cc + l * (l + 1) / 2;
@@ -862,13 +913,30 @@ int orca_last_transfer(const orca_engine *e, int64_t *h2d_bytes, int64_t *d2h_by
   return ORCA_OK;
 }
 
+// Workspace of orca_attention: request records | CUDA-core work items |
+// tensor-core work items | split partials | counters (split arrivals, then
+// two work tickets).
+struct AttnWsLayout {
+  size_t req, work, work_tc, part, cnt, total;
+};
+
+AttnWsLayout attn_ws_layout(int32_t n_batch, int32_t n_rows, int32_t n_heads, int32_t head_dim) {
+  AttnWsLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t b) { size_t at = o; o = align_up(o + b, 256); return at; };
+  L.req = take(sizeof(ReqInfo) * n_batch);
+  L.work = take(sizeof(AttnWork) * (size_t)max_attn_work(n_batch, n_rows));
+  L.work_tc = take(sizeof(AttnWork) * (size_t)max_tc_work(n_batch, n_rows));
+  L.part = take((size_t)n_batch * kMaxSplits * n_heads * (head_dim + 2) * 4);
+  L.cnt = take(((size_t)n_batch * n_heads + 4) * 4);
+  L.total = o;
+  return L;
+}
+
 int orca_attention_workspace_bytes(int32_t n_batch, int32_t n_rows, int32_t n_heads, int32_t head_dim,
                                    size_t *bytes) {
   if (!bytes || n_batch <= 0 || n_rows < n_batch || n_heads <= 0 || head_dim <= 0) return ORCA_EINVAL;
-  const size_t mw = max_attn_work(n_batch, n_rows);
-  *bytes = align_up(sizeof(ReqInfo) * n_batch, 256) + align_up(sizeof(AttnWork) * mw, 256) +
-           align_up((size_t)n_batch * kMaxSplits * n_heads * (head_dim + 2) * 4, 256) +
-           align_up(((size_t)n_batch * n_heads + 2) * 4, 256);
+  *bytes = attn_ws_layout(n_batch, n_rows, n_heads, head_dim).total;
   return ORCA_OK;
 }
 
@@ -887,8 +955,9 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
   if (orca_attention_workspace_bytes(n_batch, N, n_heads, head_dim, &need) || ws_bytes < need ||
       (reinterpret_cast<uintptr_t>(workspace) & 255))
     return ORCA_EINVAL;
+  const AttnWsLayout Lw = attn_ws_layout(n_batch, N, n_heads, head_dim);
   std::vector<ReqInfo> req(n_batch);
-  std::vector<AttnWork> work(max_attn_work(n_batch, N));
+  std::vector<AttnWork> work(max_attn_work(n_batch, N)), work_tc(max_tc_work(n_batch, N));
   int max_keys = 0;
   double sum_keys = 0.0;
   for (int32_t i = 0; i < n_batch; ++i) {
@@ -901,22 +970,54 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
     }
   }
   const int split = attn_split(max_keys, sum_keys, n_heads);
-  int32_t n_work = 0;
-  for (int32_t i = 0; i < n_batch; ++i) n_work = append_attn_work(work.data(), n_work, i, req[i].row_off, req[i].n_new,
-                                                                  req[i].ctx, split);
+  const bool tc = attention_tc_supported(dtype, head_dim);
+  int32_t n_work = 0, n_work_tc = 0;
+  for (int32_t i = 0; i < n_batch; ++i) {
+    if (tc && req[i].n_new >= kTcMinRows)
+      n_work_tc = append_tc_work(work_tc.data(), n_work_tc, i, req[i].row_off, req[i].n_new);
+    else
+      n_work = append_attn_work(work.data(), n_work, i, req[i].row_off, req[i].n_new, req[i].ctx, split);
+  }
   order_attn_work(work.data(), n_work, req.data(), split);
-  const size_t mw = work.size();
+  order_attn_work(work_tc.data(), n_work_tc, req.data(), split);
   char *ws = static_cast<char *>(workspace);
-  ReqInfo *d_req = reinterpret_cast<ReqInfo *>(ws);
-  AttnWork *d_work = reinterpret_cast<AttnWork *>(ws + align_up(sizeof(ReqInfo) * n_batch, 256));
-  float *d_part = reinterpret_cast<float *>(reinterpret_cast<char *>(d_work) + align_up(sizeof(AttnWork) * mw, 256));
-  int32_t *d_cnt = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(d_part) +
-                                               align_up((size_t)n_batch * kMaxSplits * n_heads * (head_dim + 2) * 4, 256));
+  ReqInfo *d_req = reinterpret_cast<ReqInfo *>(ws + Lw.req);
+  AttnWork *d_work = reinterpret_cast<AttnWork *>(ws + Lw.work);
+  AttnWork *d_work_tc = reinterpret_cast<AttnWork *>(ws + Lw.work_tc);
+  float *d_part = reinterpret_cast<float *>(ws + Lw.part);
+  int32_t *d_cnt = reinterpret_cast<int32_t *>(ws + Lw.cnt);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(d_cnt, 0, ((size_t)n_batch * n_heads + 2) * 4, st) != cudaSuccess ||
-      cudaMemcpyAsync(d_req, req.data(), sizeof(ReqInfo) * n_batch, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+  if (cudaMemsetAsync(d_cnt, 0, ((size_t)n_batch * n_heads + 4) * 4, st) != cudaSuccess ||
+      cudaMemcpyAsync(d_req, req.data(), sizeof(ReqInfo) * n_batch, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return ORCA_ECUDA;
+  if (n_work > 0 &&
       cudaMemcpyAsync(d_work, work.data(), sizeof(AttnWork) * n_work, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return ORCA_ECUDA;
+  if (n_work_tc > 0 &&
+      cudaMemcpyAsync(d_work_tc, work_tc.data(), sizeof(AttnWork) * n_work_tc, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess)
+    return ORCA_ECUDA;
+  const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+  if (n_work_tc > 0) {
+    CUtensorMap tq, tk;
+    if (make_tmap(nullptr, &tq, q, N, (uint64_t)n_heads * head_dim, kTcBM) ||
+        make_tmap(nullptr, &tk, k_layer, (uint64_t)n_heads * n_slots, head_dim, kTcBM))
+      return ORCA_EINVAL;
+    TcAttnArgs ta{};
+    ta.out = out;
+    ta.v_layer = v_layer;
+    ta.reqs = d_req;
+    ta.work = d_work_tc;
+    ta.ticket = d_cnt + (size_t)n_batch * n_heads + 2;
+    ta.status = status_dev;
+    ta.hidden = n_heads * head_dim;
+    ta.n_heads = n_heads;
+    ta.n_work = n_work_tc;
+    ta.n_work_dev = nullptr;
+    ta.n_slots = n_slots;
+    ta.scale_log2 = scale_log2;
+    if (launch_attention_tc(head_dim, &tq, &tk, ta, n_work_tc, st) != cudaSuccess) return ORCA_ECUDA;
+  }
   AttnArgs aa{};
   aa.q = q;
   aa.k_layer = k_layer;
@@ -935,7 +1036,7 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
   aa.split = split;
   aa.n_work = n_work;
   aa.n_slots = n_slots;
-  aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+  aa.scale_log2 = scale_log2;
   return launch_attention(dtype, head_dim, aa, n_work, st) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
 }
 

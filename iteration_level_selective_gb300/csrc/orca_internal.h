@@ -47,11 +47,18 @@ constexpr int kMaxSplits = 16;  // key splits per decode row, at most
 // Per-iteration sizes on the device, read by every kernel of a replayed
 // CUDA graph (the host writes them with the request records).
 struct DevHeader {
-  int32_t n_rows;   // sum L_i
-  int32_t n_batch;  // B
-  int32_t n_work;   // attention work items
-  int32_t split;    // keys per decode split
+  int32_t n_rows;     // sum L_i
+  int32_t n_batch;    // B
+  int32_t n_work;     // attention work items of the CUDA-core kernel
+  int32_t split;      // keys per decode split
+  int32_t n_work_tc;  // attention work items of the tensor-core prefill kernel
+  int32_t pad[3];
 };
+
+// Prompts of at least this many rows (bf16, head_dim 64 or 128) take the
+// tensor-core prefill path, in 128-row query tiles.
+constexpr int kTcMinRows = 32;
+constexpr int kTcRows = 128;
 
 // Device status word bits (set by kernels, read by the host after the sync).
 enum : int32_t {
@@ -126,6 +133,21 @@ struct AttnArgs {
   const DevHeader *hdr;   // when set, n_rows / n_work / split come from it
 };
 
+// Arguments of the tensor-core prefill attention (work items: kind 2,
+// req, a = first row, b = rows, at most kTcRows).
+struct TcAttnArgs {
+  void *out;              // [n_rows, H] bf16
+  const void *v_layer;    // [n_heads][n_slots][D] bf16
+  const ReqInfo *reqs;
+  const AttnWork *work;
+  int32_t *ticket;        // [2], zero between launches
+  int32_t *status;
+  int32_t hidden, n_heads, n_work;
+  const int32_t *n_work_dev;  // when set, the item count comes from it
+  int64_t n_slots;
+  float scale_log2;
+};
+
 // ---- launch wrappers (defined in the .cu files); all return cudaError_t.
 // Row counts: `n_rows` on the host, or *n_rows_dev when given (then n_rows
 // is only the capacity the fixed grid is sized for).
@@ -162,6 +184,12 @@ int gemm_tile_n(int M, int N);
 cudaError_t gemm_prepare();
 // Same for the attention kernels.
 cudaError_t attention_prepare();
+cudaError_t attention_tc_prepare();
+bool attention_tc_supported(int dtype, int head_dim);
+// tmQ: q buffer [rows, H] (box 64 x 128); tmK: one layer's K slots viewed as
+// [n_heads * n_slots, D] (box 64 x 128).
+cudaError_t launch_attention_tc(int head_dim, const CUtensorMap *tmQ, const CUtensorMap *tmK, const TcAttnArgs &a,
+                                int n_work, cudaStream_t st);
 // Persistent over (work item, head) pairs; n_work is the host count, or
 // the capacity when args.hdr is set.
 cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &args, int n_work, cudaStream_t st);
