@@ -121,15 +121,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(kernel: str):
+def measured_traffic(kernel: str, config: str = "gpt2-trace"):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current kernel sources and this workload (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    ent = d.get(kernel)
+    ent = d.get(config, {}).get(kernel)
     if not ent or ent.get("source_hash") != kernel_source_hash():
         return None
     return ent.get("bytes_per_launch")
@@ -172,6 +172,7 @@ def cpu_oracle_sample(budget_s: float, rank: int = 0):
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return 0
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS["gpt2-trace"]
     # each step: the oracle processes a bounded sample of 4 token rows of the trace
     from oracle import model as omodel
     shape = synth.GPT2_SMALL
@@ -198,21 +199,100 @@ def run_reference(args, rank: int, world: int):
         for _ in range(rows_per_step):
             one_row()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(steps):
         for _ in range(rows_per_step):
             one_row()
     dt = time.perf_counter() - t0
-    value = rows_per_step * args.steps / dt
+    value = rows_per_step * steps / dt
     cores = os.cpu_count()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": WORKLOAD, "step": f"{rows_per_step} token rows"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{rows_per_step * args.steps} token rows of the trace, token-at-a-time"},
+                             "sample": f"{rows_per_step * steps} token rows of the trace, token-at-a-time"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+CONFIGS = ("gpt2-trace", "13b-mixed", "13b-decode")
+DEFAULT_STEPS = {"gpt2-trace": 200, "13b-mixed": 10, "13b-decode": 50}
+
+
+def fixed_batch_spec(name: str):
+    """The two fixed 13B-shaped iterations: (shape, prompt lengths, decode
+    contexts, workload description)."""
+    if name == "13b-mixed":
+        prompts, ctx = synth.mixed_batch_lengths(16, (1024, 2048), 240, (128, 2048), seed=0)
+        return (synth.GPT_13B, prompts, ctx,
+                "13B-shaped bf16 (40L, H5120, 40 heads, FFN 4H, V50257), one prefill-heavy mixed iteration repeated: "
+                "16 prompts U1024-2048 + 240 decodes with contexts U128-2048, max_bs 256")
+    if name == "13b-decode":
+        _, ctx = synth.mixed_batch_lengths(0, (1, 1), 256, (1024, 4096), seed=0)
+        shape = synth.with_layers(synth.GPT_13B, 16)
+        return (shape, np.zeros(0, np.int64), ctx,
+                "13B-shaped bf16 with 16 of its 40 layers (the K/V of 40 layers does not fit in HBM), one "
+                "decode-only iteration repeated: 256 decodes with contexts U1024-4096, max_bs 256")
+    raise ValueError(name)
+
+
+class TraceWorkload:
+    """The GPT-2-small serving trace, restarted whenever it completes."""
+
+    def __init__(self, eng, rank, stream):
+        from iteration_level_selective_gb300 import runtime as rt
+        self.rt, self.eng, self.rank, self.stream, self.gen = rt, eng, rank, stream, 0
+        self.loop = self._new()
+
+    def _new(self):
+        self.gen += 1
+        return self.rt.ServingLoop(self.eng, self.rt.RequestPool(trace_for(self.rank, self.gen)), stream=self.stream)
+
+    def step(self):
+        if self.loop.done():
+            self.loop = self._new()
+        return self.loop.step()
+
+
+class FixedBatchWorkload:
+    """One selectively batched iteration, repeated.  Every request holds its
+    max_tokens reservation from the start and is in the increment state:
+    prompts have nothing cached (L_i = prompt length), decodes have c_i cached
+    tokens (L_i = 1).  After each iteration the request counters are put
+    back, so every step runs the same batch and rewrites the same K/V slots."""
+
+    def __init__(self, eng, prompts, ctx, vocab, stream):
+        from iteration_level_selective_gb300 import _orca as C
+        from iteration_level_selective_gb300 import runtime as rt
+        reqs = []
+        for i, L in enumerate(prompts):
+            reqs.append(synth.Request(req_id=i, arrival=0, prompt=synth.token_ids(int(L), vocab, stream=i),
+                                      out_len=4, max_tokens=int(L) + 3))
+        for j, c in enumerate(ctx):
+            k = len(prompts) + j
+            reqs.append(synth.Request(req_id=k, arrival=0, prompt=synth.token_ids(int(c), vocab, stream=k),
+                                      out_len=4, max_tokens=int(c) + 3))
+        self.pool = rt.RequestPool(reqs)
+        v = self.pool.view
+        for k in range(self.pool.n):
+            v["slot_base"][k] = C.orca_kv_reserve(eng.handle, int(v["req_id"][k]), int(v["max_tokens"][k]))
+        v["state"] = C.ORCA_INCREMENT
+        v["n_cached"][len(prompts):] = ctx
+        v["n_generated"][len(prompts):] = 1
+        self.saved = {f: v[f].copy() for f in ("state", "n_cached", "n_generated")}
+        self.loop = rt.ServingLoop(eng, self.pool, stream=stream)
+
+    @staticmethod
+    def slots_needed(prompts, ctx) -> int:
+        return int(np.sum(prompts + 3) + np.sum(ctx + 3))
+
+    def step(self):
+        rec = self.loop.step()
+        v = self.pool.view
+        for f, a in self.saved.items():
+            v[f] = a
+        return rec
 
 
 def run_ours(args, rank: int, world: int):
@@ -227,68 +307,74 @@ def run_ours(args, rank: int, world: int):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     B.build()
-    shape = synth.GPT2_SMALL
-    host_w = synth.make_weights(shape, seed=0)
-    weights = rt.DeviceWeights(shape, dev, host=host_w)
-    del host_w
-    n_slots = n_slots_for(shape)
-    eng = rt.Engine(shape, weights, max_bs=64, n_slots=n_slots, max_rows=64 * 512, device=dev)
     stream = torch.cuda.Stream(dev)
-    gen = [0]
-
-    def new_loop():
-        gen[0] += 1
-        return rt.ServingLoop(eng, rt.RequestPool(trace_for(rank, gen[0])), stream=stream)
-
-    loop = new_loop()
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.config]
+    if args.config == "gpt2-trace":
+        shape = synth.GPT2_SMALL
+        host_w = synth.make_weights(shape, seed=0)
+        weights = rt.DeviceWeights(shape, dev, host=host_w)
+        del host_w
+        n_slots = args.kv_slots if args.kv_slots else n_slots_for(shape)
+        eng = rt.Engine(shape, weights, max_bs=64, n_slots=n_slots, max_rows=64 * 512, device=dev)
+        work = TraceWorkload(eng, rank, stream)
+        workload = WORKLOAD
+        cfg_extra = {"model": "gpt2-small-shaped (12L, H768, 12 heads, V50257), random init", "max_bs": 64,
+                     "n_slots": n_slots, "arrivals": "Poisson 0.5 per iteration",
+                     "l2": "inputs larger than L2 (0.25 GB weights + K/V pool), no flush"}
+    else:
+        shape, prompts, ctx, workload = fixed_batch_spec(args.config)
+        n_slots = FixedBatchWorkload.slots_needed(prompts, ctx)
+        n_rows = int(np.sum(prompts) + len(ctx))
+        weights = rt.DeviceWeights(shape, dev, host=None, seed=0)
+        free, _ = torch.cuda.mem_get_info(dev)
+        cfg = rt.make_config(shape, 256, n_slots, n_rows)
+        need = C.orca_kv_pool_bytes(cfg) + C.orca_workspace_bytes(cfg)
+        if need > free:
+            raise SystemExit(f"{args.config}: K/V pool + workspace need {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free")
+        eng = rt.Engine(shape, weights, max_bs=256, n_slots=n_slots, max_rows=n_rows, device=dev)
+        eng.kv.zero_()   # no stale bits in the cached contexts
+        work = FixedBatchWorkload(eng, prompts, ctx, shape.vocab, stream)
+        cfg_extra = {"model": f"13B-shaped, {shape.n_layers} layers, random init N(0, 0.02)", "max_bs": 256,
+                     "n_rows": n_rows, "n_slots": n_slots, "kv_pool_gb": round(eng.kv_bytes / 1e9, 1),
+                     "weights_gb": round(weights.nbytes / 1e9, 1),
+                     "l2": "inputs larger than L2 (weights and K/V many times L2), no flush"}
 
     def step():
-        nonlocal loop
-        if loop.done():
-            loop = new_loop()
-        rec = loop.step()
+        rec = work.step()
         h2d, d2h, _ = C.orca_last_transfer(eng.handle)
         return rec, h2d, d2h
 
-    for _ in range(max(3, args.warmup)):
+    warmup = max(3, args.warmup)
+    for _ in range(warmup):
         step()
-    prev_loop = [loop]
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
     sampler = ClockSampler(local)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    rows = gen_tok = done = h2d = d2h = 0
+    rows = gen_tok = done = h2d = d2h = launches = 0
     torch.cuda.synchronize(dev)
     w0 = time.perf_counter()
     ev0.record(stream)
-    loop_stats = {"pre": 0.0, "call": 0.0, "post": 0.0}
-    for _ in range(args.steps):
-        before = (loop.t_pre, loop.t_call, loop.t_post)
+    for _ in range(steps):
         rec, hb, db = step()
-        cur = loop
-        loop_stats["pre"] += cur.t_pre - (before[0] if cur is prev_loop[0] else 0.0)
-        loop_stats["call"] += cur.t_call - (before[1] if cur is prev_loop[0] else 0.0)
-        loop_stats["post"] += cur.t_post - (before[2] if cur is prev_loop[0] else 0.0)
-        prev_loop[0] = cur
         rows += sum(rec.n_new)
         gen_tok += len(rec.req_ids)
         done += len(rec.released)
         h2d += hb
         d2h += db
+        launches += rec.launches
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - w0
-    host = {"pre_ms": loop_stats["pre"] / args.steps * 1e3, "call_ms": loop_stats["call"] / args.steps * 1e3,
-            "post_ms": loop_stats["post"] / args.steps * 1e3}
     clocks = sampler.stop()
     dev_s = ev0.elapsed_time(ev1) / 1000.0
-    (dev_s, wall), (rows, gen_tok, done, h2d, d2h) = replicas.reduce_timing(
-        [dev_s, wall], [rows, gen_tok, done, h2d, d2h], device=dev)
+    (dev_s, wall), (rows, gen_tok, done, h2d, d2h, launches) = replicas.reduce_timing(
+        [dev_s, wall], [rows, gen_tok, done, h2d, d2h, launches], device=dev)
 
     # profiled pass: per-launch CUDA events around every kernel, same workload
     C.orca_profile_enable(eng.handle, True)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     torch.cuda.synchronize(dev)
     stats = {C.KERNEL_NAMES[k]: C.orca_profile_read(eng.handle, k) for k in range(C.ORCA_K_COUNT)}
@@ -316,37 +402,51 @@ def run_ours(args, rank: int, world: int):
         achieved = a["bytes"] / (a["ms"] / 1000.0) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    tr = measured_traffic(dom)
-    roof["traffic"] = tr
+    roof["traffic"] = measured_traffic(dom, args.config)
     roof["kernel"] = dom
     roof["peak_source"] = peak_src + (" sustained bf16" if roof["bound"] == "tensor" else " copy bandwidth")
     roof["launches"] = a["launches"]
     roof["algorithmic_per_launch"] = (a["flops"] if roof["bound"] == "tensor" else a["bytes"]) / max(1, a["launches"])
-    launches_per_iter = 4 + 7 * shape.n_layers
+    # the other kernel classes against their own bound
+    per_kernel = {}
+    for k, v in agg.items():
+        if v["ms"] <= 0:
+            continue
+        if v["bytes"] > 0 and v["flops"] / v["bytes"] > balance:
+            per_kernel[k] = {"TFLOP/s": round(v["flops"] / v["ms"] / 1e9, 1),
+                             "frac_tensor": round(v["flops"] / v["ms"] / 1e9 / peaks["bf16_tflops_sustained"], 3)}
+        else:
+            per_kernel[k] = {"GB/s": round(v["bytes"] / v["ms"] / 1e6, 1),
+                             "frac_hbm": round(v["bytes"] / v["ms"] / 1e6 / peaks["hbm_gbs"], 3)}
     value = rows / dev_s
+    config = {"workload": workload}
+    config.update(cfg_extra)
+    config["parallelism"] = f"replicas x{world}"
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(3, args.warmup), "ms_per_step": 1000.0 * dev_s / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": 1000.0 * dev_s / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "model": "gpt2-small-shaped (12L, H768, 12 heads, V50257), random init",
-                   "max_bs": 64, "n_slots": n_slots, "arrivals": "Poisson 0.5 per iteration",
-                   "l2": "inputs larger than L2 (0.25 GB weights + K/V pool), no flush",
-                   "parallelism": f"replicas x{world}"},
+        "config": config,
         "generated_tokens_per_s": gen_tok / dev_s,
         "completed_requests_per_s": done / dev_s,
-        "e2e": {"value": rows / wall, "unit": UNIT, "h2d_bytes_per_step": h2d / args.steps / max(1, world),
-                "d2h_bytes_per_step": d2h / args.steps / max(1, world)},
-        "gpu_launches": launches_per_iter * args.steps * world,
+        "e2e": {"value": rows / wall, "unit": UNIT, "h2d_bytes_per_step": h2d / steps / max(1, world),
+                "d2h_bytes_per_step": d2h / steps / max(1, world)},
+        "gpu_launches": launches,
         "roofline": roof,
+        "kernel_roofline": per_kernel,
         "kernel_time_share": {k: round(v["ms"] / total_ms, 4) for k, v in agg.items()},
-        "kernel_ms_per_step": {k: round(v["ms"] / args.steps, 4) for k, v in agg.items()},
+        "kernel_ms_per_step": {k: round(v["ms"] / steps, 4) for k, v in agg.items()},
         "clocks": clocks,
-        "host_ms_per_step": host,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_tok, dt, desc = cpu_oracle_sample(args.cpu_seconds)
-        line["cpu_baseline"] = {"value": n_tok / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": desc}
+        if args.config == "gpt2-trace":
+            n_tok, dt, desc = cpu_oracle_sample(args.cpu_seconds)
+            line["cpu_baseline"] = {"value": n_tok / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                                    "sample": desc}
+        else:
+            line["cpu_baseline"] = None
+            line["cpu_baseline_note"] = ("the float64 oracle needs the 13B weights on the host (50 GB in float64 "
+                                         "per 40 layers); it is timed on the GPT-2-small trace only")
     if rank == 0:
         print(json.dumps(line), flush=True)
     eng.close()
@@ -356,9 +456,16 @@ def run_ours(args, rank: int, world: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed iterations (default: 200 for gpt2-trace, 10 for 13b-mixed, 50 for 13b-decode)")
+    ap.add_argument("--config", choices=CONFIGS, default="gpt2-trace",
+                    help="gpt2-trace (the serving trace, default), 13b-mixed (one prefill-heavy 13B iteration), "
+                         "13b-decode (one decode-only 13B iteration)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--kv-slots", type=int, default=0,
+                    help="gpt2-trace only: K/V pool slots (default: 40 GB worth); the trace needs at most "
+                         "64 x 768, so profiler captures use a small pool")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()

@@ -216,6 +216,11 @@ int orca_last_descriptor(const orca_engine *eng, int32_t *n_batch, int32_t *n_ro
  * and greedy tokens), and its attention work-item count. */
 int orca_last_transfer(const orca_engine *eng, int64_t *h2d_bytes, int64_t *d2h_bytes, int32_t *n_work);
 
+/* Number of kernels the last orca_iteration launched on the device (the
+ * kernel nodes of its CUDA graph when it replayed one, else the kernels it
+ * enqueued eagerly).  Host call; ORCA_EINVAL on a NULL argument. */
+int orca_last_launches(const orca_engine *eng, int32_t *n_kernels);
+
 /* ---------------------------------------------------------------- kernels */
 /* Greedy choice over forced logits: out_dev[r] = argmax_c logits_dev[r, c]
  * (lowest index among equal maxima; NaN never wins).  Device pointers;

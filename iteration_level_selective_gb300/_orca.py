@@ -101,6 +101,7 @@ def lib() -> ctypes.CDLL:
             "orca_last_error": [P, ctypes.c_char_p, c_sz],
             "orca_linear": [c_i32, c_i32, P, P, P, P, c_i32, c_i32, c_i32, P, c_sz, P, P, P],
             "orca_last_transfer": [P, i64p, i64p, i32p],
+            "orca_last_launches": [P, i32p],
             "orca_attention_workspace_bytes": [c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)],
             "orca_attention": [c_i32, c_i32, c_i32, c_i64, P, P, P, P, c_i32, i32p, i32p, i64p, P, c_sz, P, P],
             "orca_attention_noalloc": [c_i32, c_i32, c_i32, c_i64, P, P, P, P, c_i32, i32p, i32p, i64p, P, P],
@@ -206,6 +207,12 @@ def orca_last_transfer(eng):
     a, b, n = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
     _check(lib().orca_last_transfer(eng, ctypes.byref(a), ctypes.byref(b), ctypes.byref(n)), eng)
     return a.value, b.value, n.value
+
+
+def orca_last_launches(eng) -> int:
+    n = ctypes.c_int32()
+    _check(lib().orca_last_launches(eng, ctypes.byref(n)), eng)
+    return n.value
 
 
 def orca_attention_workspace_bytes(n_batch: int, n_rows: int, n_heads: int, head_dim: int) -> int:

@@ -235,7 +235,8 @@ struct orca_engine {
   WeightMaps tm_emb{};
   std::vector<WeightMaps> tm_layer;  // 4 per layer: qkv, o, fc1, fc2
   // last descriptor (host copy)
-  int32_t last_B = 0, last_N = 0, last_work = 0;
+  int32_t last_B = 0, last_N = 0, last_work = 0, last_launches = 0;
+  int32_t n_launch = 0;               // kernels enqueued by the current eager forward
   int64_t last_h2d = 0, last_d2h = 0;
   std::vector<int32_t> last_row_off, last_row_pos, last_row_slot, last_last_row;
   // profiling
@@ -247,7 +248,11 @@ struct orca_engine {
   std::vector<Pending> pending;
   // CUDA graphs of the forward, keyed by GEMM tile choices and logits pointer
   cudaStream_t cap_stream = nullptr;
-  std::map<std::pair<uint32_t, uintptr_t>, cudaGraphExec_t> graphs;
+  struct Graph {
+    cudaGraphExec_t exec;
+    int32_t n_kernels;  // kernel nodes in the captured forward
+  };
+  std::map<std::pair<uint32_t, uintptr_t>, Graph> graphs;
 };
 
 namespace {
@@ -269,6 +274,13 @@ int fail(orca_engine *e, int code, const char *fmt, ...) {
     cudaError_t _e = (call);                                                                \
     if (_e != cudaSuccess)                                                                  \
       return fail(eng, ORCA_ECUDA, "%s failed: %s", #call, cudaGetErrorString(_e));         \
+  } while (0)
+
+// A kernel launch of the forward: checked, and counted for orca_last_launches.
+#define LAUNCH(eng, call)   \
+  do {                      \
+    CUDA_TRY(eng, call);    \
+    ++(eng)->n_launch;      \
   } while (0)
 
 template <typename T> T *ws_ptr(orca_engine *e, size_t off) { return reinterpret_cast<T *>(e->ws + off); }
@@ -384,7 +396,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
 
   cudaEvent_t ev;
   prof_begin(e, st, &ev);
-  CUDA_TRY(e, launch_embed(c.dtype, d_row, N_grid, N_dev, e->w[W_TOK], e->w[W_POS], x, H, V, c.max_pos, status, st));
+  LAUNCH(e, launch_embed(c.dtype, d_row, N_grid, N_dev, e->w[W_TOK], e->w[W_POS], x, H, V, c.max_pos, status, st));
   prof_end(e, st, ev, ORCA_K_EMBED, 0.0, (double)N * H * (2 * eb + 4));
 
   const size_t layer_kv = (size_t)2 * nh * c.n_slots * D * eb;
@@ -397,7 +409,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     char *vl = kl + layer_kv / 2;
     // h = LN1(x)
     prof_begin(e, st, &ev);
-    CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN1_G), (const float *)lw(e, l, L_LN1_B), h,
+    LAUNCH(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN1_G), (const float *)lw(e, l, L_LN1_B), h,
                                  N_grid, N_dev, H, nullptr, nullptr, st));
     prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
     // QKV Linear; K/V scattered to the requests' slots (Split)
@@ -415,9 +427,9 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     ep.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 0], N, N_dev, 3 * H, H, ep, scr, status, st));
+      LAUNCH(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 0], N, N_dev, 3 * H, H, ep, scr, status, st));
     else
-      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WQKV), N, 3 * H, H, ep, st));
+      LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WQKV), N, 3 * H, H, ep, st));
     prof_end(e, st, ev, ORCA_K_GEMM_QKV, 2.0 * N * 3 * H * H, gemm_bytes(N, 3.0 * H, H, eb));
     // ragged attention -> h (rows in place: Merge)
     AttnArgs aa{};
@@ -456,8 +468,9 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
       ta.n_slots = c.n_slots;
       ta.scale_log2 = aa.scale_log2;
       CUDA_TRY(e, launch_attention_tc(D, &e->tm_q, &e->tm_k[l], ta, z.n_work_tc, st));
+      if (graph || z.n_work_tc > 0) ++e->n_launch;
     }
-    CUDA_TRY(e, launch_attention(c.dtype, D, aa, graph ? Ly.max_work : z.n_work, st));
+    LAUNCH(e, launch_attention(c.dtype, D, aa, graph ? Ly.max_work : z.n_work, st));
     prof_end(e, st, ev, ORCA_K_ATTENTION, attn_flops, attn_bytes);
     // x += a Wo + bo
     EpiParams eo{};
@@ -468,13 +481,13 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     eo.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 1], N, N_dev, H, H, eo, scr, status, st));
+      LAUNCH(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 1], N, N_dev, H, H, eo, scr, status, st));
     else
-      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WO), N, H, H, eo, st));
+      LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WO), N, H, H, eo, st));
     prof_end(e, st, ev, ORCA_K_GEMM_O, 2.0 * N * H * H, gemm_bytes(N, H, H, 8));
     // h = LN2(x)
     prof_begin(e, st, &ev);
-    CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN2_G), (const float *)lw(e, l, L_LN2_B), h,
+    LAUNCH(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN2_G), (const float *)lw(e, l, L_LN2_B), h,
                                  N_grid, N_dev, H, nullptr, nullptr, st));
     prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
     // u = GeLU(h W1 + b1)
@@ -486,9 +499,9 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     e1.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 2], N, N_dev, F, H, e1, scr, status, st));
+      LAUNCH(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 2], N, N_dev, F, H, e1, scr, status, st));
     else
-      CUDA_TRY(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_W1), N, F, H, e1, st));
+      LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_W1), N, F, H, e1, st));
     prof_end(e, st, ev, ORCA_K_GEMM_FC1, 2.0 * N * F * H, gemm_bytes(N, F, H, eb));
     // x += u W2 + b2
     EpiParams e2{};
@@ -499,15 +512,15 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     e2.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_u, e->tm_layer[4 * l + 3], N, N_dev, H, F, e2, scr, status, st));
+      LAUNCH(e, launch_gemm_tc_bf16(&e->tm_u, e->tm_layer[4 * l + 3], N, N_dev, H, F, e2, scr, status, st));
     else
-      CUDA_TRY(e, launch_gemm_simt_f32((const float *)u, (const float *)lw(e, l, L_W2), N, H, F, e2, st));
+      LAUNCH(e, launch_gemm_simt_f32((const float *)u, (const float *)lw(e, l, L_W2), N, H, F, e2, st));
     prof_end(e, st, ev, ORCA_K_GEMM_FC2, 2.0 * N * H * F, gemm_bytes(N, H, F, 8));
   }
   // final LayerNorm on each request's last row, LM head (tied), greedy choice
   prof_begin(e, st, &ev);
   // (also zeroes the argmax keys the LM head's epilogue max-reduces into)
-  CUDA_TRY(e, launch_layernorm(c.dtype, x, (const float *)e->w[W_LNF_G], (const float *)e->w[W_LNF_B], hf, B_grid,
+  LAUNCH(e, launch_layernorm(c.dtype, x, (const float *)e->w[W_LNF_G], (const float *)e->w[W_LNF_B], hf, B_grid,
                                B_dev, H, d_req, d_keys, st));
   prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)B * H * (4 + eb));
   EpiParams el{};
@@ -519,13 +532,13 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
   el.argmax_keys = bf16 ? d_keys : nullptr;
   prof_begin(e, st, &ev);
   if (bf16)
-    CUDA_TRY(e, launch_gemm_tc_bf16(&e->tm_hf, e->tm_emb, B, B_dev, V, H, el, scr, status, st));
+    LAUNCH(e, launch_gemm_tc_bf16(&e->tm_hf, e->tm_emb, B, B_dev, V, H, el, scr, status, st));
   else
-    CUDA_TRY(e, launch_gemm_simt_f32((const float *)hf, (const float *)e->w[W_TOK], B, V, H, el, st));
+    LAUNCH(e, launch_gemm_simt_f32((const float *)hf, (const float *)e->w[W_TOK], B, V, H, el, st));
   prof_end(e, st, ev, ORCA_K_LM_HEAD, 2.0 * B * V * H, gemm_bytes(B, V, H, logits ? 4 : 0));
   if (!bf16) {
     prof_begin(e, st, &ev);
-    CUDA_TRY(e, launch_argmax(logits, B, V, nullptr, d_keys, st));
+    LAUNCH(e, launch_argmax(logits, B, V, nullptr, d_keys, st));
     prof_end(e, st, ev, ORCA_K_ARGMAX, 0.0, (double)B * V * 4);
   }
   return ORCA_OK;
@@ -658,7 +671,7 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
 int orca_engine_destroy(orca_engine *e) {
   if (!e) return ORCA_EINVAL;
   if (!e->host_only) {
-    for (auto &g : e->graphs) cudaGraphExecDestroy(g.second);
+    for (auto &g : e->graphs) cudaGraphExecDestroy(g.second.exec);
     if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
     cudaFreeHost(e->h_hdr);
     cudaFreeHost(e->h_row);
@@ -850,16 +863,29 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
         return rc;
       }
       if (ce != cudaSuccess) return fail(e, ORCA_ECUDA, "graph capture failed: %s", cudaGetErrorString(ce));
+      int32_t n_kernels = 0;
+      size_t n_nodes = 0;
+      if (cudaGraphGetNodes(g, nullptr, &n_nodes) == cudaSuccess && n_nodes > 0) {
+        std::vector<cudaGraphNode_t> nodes(n_nodes);
+        if (cudaGraphGetNodes(g, nodes.data(), &n_nodes) == cudaSuccess)
+          for (size_t k = 0; k < n_nodes; ++k) {
+            cudaGraphNodeType t;
+            if (cudaGraphNodeGetType(nodes[k], &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++n_kernels;
+          }
+      }
       cudaGraphExec_t ex = nullptr;
       const cudaError_t ie = cudaGraphInstantiate(&ex, g, 0);
       cudaGraphDestroy(g);
       if (ie != cudaSuccess) return fail(e, ORCA_ECUDA, "graph instantiate failed: %s", cudaGetErrorString(ie));
-      it = e->graphs.emplace(gk, ex).first;
+      it = e->graphs.emplace(gk, orca_engine::Graph{ex, n_kernels}).first;
     }
-    CUDA_TRY(e, cudaGraphLaunch(it->second, st));
+    CUDA_TRY(e, cudaGraphLaunch(it->second.exec, st));
+    e->last_launches = it->second.n_kernels;
   } else {
+    e->n_launch = 0;
     const int rc = enqueue_forward(e, st, z, logits, false);
     if (rc) return rc;
+    e->last_launches = e->n_launch;
   }
   CUDA_TRY(e, cudaMemcpyAsync(e->h_out, d_out, sizeof(unsigned long long) * (n_batch + 1), cudaMemcpyDeviceToHost, st));
   CUDA_TRY(e, cudaStreamSynchronize(st));
@@ -902,6 +928,12 @@ int orca_last_descriptor(const orca_engine *e, int32_t *n_batch, int32_t *n_rows
   if (row_pos) std::copy(e->last_row_pos.begin(), e->last_row_pos.end(), row_pos);
   if (row_slot) std::copy(e->last_row_slot.begin(), e->last_row_slot.end(), row_slot);
   if (last_row) std::copy(e->last_last_row.begin(), e->last_last_row.end(), last_row);
+  return ORCA_OK;
+}
+
+int orca_last_launches(const orca_engine *e, int32_t *n_kernels) {
+  if (!e || !n_kernels) return ORCA_EINVAL;
+  *n_kernels = e->last_launches;
   return ORCA_OK;
 }
 

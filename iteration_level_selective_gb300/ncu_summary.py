@@ -1,0 +1,145 @@
+"""Summarise an Nsight Compute launch list (``ncu --csv --log-file``) per kernel.
+
+    python -m iteration_level_selective_gb300.ncu_summary launches.csv \
+        [--traffic profiles/traffic.json --workload gpt2-trace --scale S]
+
+prints one markdown row per kernel (launches, total device time, share,
+average time, DRAM bytes per launch when the capture has the
+``dram__bytes_read.sum`` / ``dram__bytes_write.sum`` counters) and, with
+``--traffic``, records the measured DRAM bytes per launch of each kernel class
+the benchmark reports (``gemm_tc_bf16``, ``attention``, ``layernorm``,
+``embed``) under the workload's name, together with a hash of the kernel
+sources so that a stale figure is never reported after the kernels change.
+``--scale`` multiplies the bytes (a capture of a smaller case scaled to the
+full launch by the units processed).  The attention class counts one launch
+per layer, so its bytes are those of both attention kernels over the number
+of launches of the ragged (CUDA-core) kernel.
+"""
+from __future__ import annotations
+
+import argparse
+import collections
+import csv
+import hashlib
+import io
+import json
+import os
+import re
+import sys
+
+CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc")
+
+_TIME = {"ns": 1e-6, "nsecond": 1e-6, "us": 1e-3, "usecond": 1e-3, "ms": 1.0, "msecond": 1.0, "s": 1e3,
+         "second": 1e3}
+_BYTES = {"byte": 1.0, "b": 1.0, "kbyte": 1e3, "kb": 1e3, "mbyte": 1e6, "mb": 1e6, "gbyte": 1e9, "gb": 1e9}
+
+CLASSES = {
+    "gemm_tc_bf16": ("gemm_tc_bf16_kernel",),
+    "attention": ("attention_kernel", "prefill_attention_tc_kernel"),
+    "layernorm": ("layernorm_kernel",),
+    "embed": ("embed_kernel",),
+}
+
+
+def source_hash() -> str:
+    """Hash of the CUDA/C++ sources (the benchmark computes the same)."""
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(CSRC, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def short_name(full: str) -> str:
+    """'void orca::(anonymous namespace)::gemm_tc_bf16_kernel<128>(...)' -> 'gemm_tc_bf16_kernel'."""
+    head = re.split(r"[<(]", full.replace("(anonymous namespace)", ""), maxsplit=1)[0]
+    return head.split("::")[-1].split()[-1]
+
+
+def read_launches(path: str):
+    """{launch id: {"kernel": name, metric: value in ms or bytes}}."""
+    with open(path, newline="") as f:
+        text = f.read()
+    start = text.find('"ID"')
+    if start < 0:
+        raise ValueError(f"{path}: no ncu CSV header")
+    launches = collections.OrderedDict()
+    for row in csv.DictReader(io.StringIO(text[start:])):
+        lid = row["ID"]
+        ent = launches.setdefault(lid, {"kernel": short_name(row["Kernel Name"])})
+        name, unit = row["Metric Name"], row["Metric Unit"].strip().lower()
+        try:
+            val = float(row["Metric Value"].replace(",", ""))
+        except ValueError:
+            continue
+        if name == "gpu__time_duration.sum":
+            ent["ms"] = val * _TIME.get(unit, 1e-6)
+        elif name in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            ent[name] = val * _BYTES.get(unit, 1.0)
+    return launches
+
+
+def summarise(launches):
+    per = collections.OrderedDict()
+    for ent in launches.values():
+        k = per.setdefault(ent["kernel"], {"launches": 0, "ms": 0.0, "dram": 0.0, "has_dram": False})
+        k["launches"] += 1
+        k["ms"] += ent.get("ms", 0.0)
+        if "dram__bytes_read.sum" in ent or "dram__bytes_write.sum" in ent:
+            k["has_dram"] = True
+            k["dram"] += ent.get("dram__bytes_read.sum", 0.0) + ent.get("dram__bytes_write.sum", 0.0)
+    return per
+
+
+def markdown(per) -> str:
+    total = sum(v["ms"] for v in per.values()) or 1.0
+    n = sum(v["launches"] for v in per.values())
+    out = [f"Launches: {n}; total kernel time {total:.2f} ms.", "",
+           "| kernel | launches | total ms | share | avg us/launch | DRAM MB/launch |",
+           "|---|---|---|---|---|---|"]
+    for k, v in sorted(per.items(), key=lambda kv: -kv[1]["ms"]):
+        dram = f"{v['dram'] / v['launches'] / 1e6:.3f}" if v["has_dram"] else "-"
+        out.append(f"| {k} | {v['launches']} | {v['ms']:.3f} | {v['ms'] / total:.3f} | "
+                   f"{1000 * v['ms'] / v['launches']:.2f} | {dram} |")
+    return "\n".join(out)
+
+
+def traffic_by_class(per, scale: float = 1.0):
+    res = {}
+    for cls, names in CLASSES.items():
+        present = [n for n in names if n in per and per[n]["has_dram"]]
+        if not present:
+            continue
+        n_launch = per[present[0]]["launches"]   # the first name present counts the class's launches
+        res[cls] = scale * sum(per[n]["dram"] for n in present) / n_launch
+    return res
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("csv")
+    ap.add_argument("--traffic", help="JSON file to record per-launch DRAM bytes in")
+    ap.add_argument("--workload", default="gpt2-trace")
+    ap.add_argument("--scale", type=float, default=1.0)
+    ap.add_argument("--note", default="")
+    args = ap.parse_args(argv)
+    per = summarise(read_launches(args.csv))
+    print(markdown(per))
+    if args.traffic:
+        d = {}
+        if os.path.exists(args.traffic):
+            with open(args.traffic) as f:
+                d = json.load(f)
+        h = source_hash()
+        ent = d.setdefault(args.workload, {})
+        for cls, b in traffic_by_class(per, args.scale).items():
+            ent[cls] = {"bytes_per_launch": b, "source_hash": h, "scale": args.scale, "note": args.note}
+        with open(args.traffic, "w") as f:
+            json.dump(d, f, indent=1)
+            f.write("\n")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

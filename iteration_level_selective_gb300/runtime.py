@@ -158,6 +158,7 @@ class IterRecord:
     released: List[int]
     next_tokens: List[int]
     logits: Optional[np.ndarray] = None
+    launches: int = 0          # kernels the iteration launched on the device
 
 
 class ServingLoop:
@@ -212,6 +213,7 @@ class ServingLoop:
                          self.stream.cuda_stream)
         t2 = time.perf_counter()
         rec.next_tokens = self._nt[:nb].tolist()
+        rec.launches = C.orca_last_launches(self.eng.handle)
         done = P.view["state"][idx] == C.ORCA_FINISHED
         if done.any():
             rec.released = sel["req_id"][done].tolist()

@@ -205,6 +205,20 @@ def figure5_trace(vocab: int = 256, seed: int = 0, out_len: int = 8, extra: int 
     return reqs
 
 
+def mixed_batch_lengths(n_prefill: int, prompt_range, n_decode: int, ctx_range, seed: int = 0):
+    """Lengths of one fixed mixed iteration: n_prefill prompt lengths and
+    n_decode cached-context lengths, each uniform over its inclusive range."""
+    rng = _rng(seed, 5_000_000)
+    prompts = rng.integers(prompt_range[0], prompt_range[1] + 1, size=n_prefill).astype(np.int64)
+    ctx = rng.integers(ctx_range[0], ctx_range[1] + 1, size=n_decode).astype(np.int64)
+    return prompts, ctx
+
+
+def token_ids(n: int, vocab: int, seed: int = 0, stream: int = 0) -> np.ndarray:
+    """n token ids uniform in [0, vocab) (int32)."""
+    return _rng(seed, 6_000_000, stream).integers(0, vocab, size=n, dtype=np.int64).astype(np.int32)
+
+
 def random_kv(n_tokens: int, hidden: int, seed: int, dtype: int) -> np.ndarray:
     """[n_tokens, hidden] random values (N(0,1)) in storage precision, used to
     fill K/V slots directly when an attention case needs long cached contexts."""

@@ -219,9 +219,15 @@ def test_graph_replay_equals_eager_launches(cuda):
         out.append(recs)
         eng.close()
     assert len(out[0]) == len(out[1])
+    nl = shape.n_layers
     for g, e in zip(*out):
         assert g.req_ids == e.req_ids and g.next_tokens == e.next_tokens
         np.testing.assert_array_equal(g.logits, e.logits)
+        # embed, final LN, LM head + per layer LN1, QKV, attention, Attn-Out,
+        # LN2, FC1, FC2, and the tensor-core prompt attention (always in the
+        # graph; eagerly only when a prompt of >= 32 rows is in the batch)
+        assert g.launches == 3 + 8 * nl
+        assert e.launches == 3 + nl * (7 + int(max(e.n_new) >= 32))
 
 
 # ------------------------------------------------------------------ GPT-2-small, full size, sampled

@@ -1,0 +1,36 @@
+"""The ncu launch-list summariser on a small hand-written CSV."""
+import json
+
+from iteration_level_selective_gb300 import ncu_summary as ns
+
+CSV = '''==PROF== Connected to process 1
+"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"
+"0","1","python","h","void orca::(anonymous namespace)::gemm_tc_bf16_kernel<128>(CUtensorMap, int)","1","7","(192, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","Mbyte","2.50"
+"0","1","python","h","void orca::(anonymous namespace)::gemm_tc_bf16_kernel<128>(CUtensorMap, int)","1","7","(192, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_write.sum","Kbyte","500"
+"0","1","python","h","void orca::(anonymous namespace)::gemm_tc_bf16_kernel<128>(CUtensorMap, int)","1","7","(192, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","gpu__time_duration.sum","usecond","10.00"
+"1","1","python","h","void orca::attention_kernel<__nv_bfloat16, 64>(orca::AttnArgs)","1","7","(256, 1, 1)","(304, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","byte","1,000,000"
+"1","1","python","h","void orca::attention_kernel<__nv_bfloat16, 64>(orca::AttnArgs)","1","7","(256, 1, 1)","(304, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_write.sum","byte","0"
+"1","1","python","h","void orca::attention_kernel<__nv_bfloat16, 64>(orca::AttnArgs)","1","7","(256, 1, 1)","(304, 1, 1)","0","10.3","Command line profiler metrics","gpu__time_duration.sum","nsecond","30000"
+"2","1","python","h","void orca::prefill_attention_tc_kernel<64>(CUtensorMap, CUtensorMap, orca::TcAttnArgs)","1","7","(128, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","byte","500000"
+"2","1","python","h","void orca::prefill_attention_tc_kernel<64>(CUtensorMap, CUtensorMap, orca::TcAttnArgs)","1","7","(128, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_write.sum","byte","0"
+"2","1","python","h","void orca::prefill_attention_tc_kernel<64>(CUtensorMap, CUtensorMap, orca::TcAttnArgs)","1","7","(128, 1, 1)","(152, 1, 1)","0","10.3","Command line profiler metrics","gpu__time_duration.sum","usecond","60"
+'''
+
+
+def test_summary_and_traffic(tmp_path):
+    p = tmp_path / "l.csv"
+    p.write_text(CSV)
+    per = ns.summarise(ns.read_launches(str(p)))
+    assert set(per) == {"gemm_tc_bf16_kernel", "attention_kernel", "prefill_attention_tc_kernel"}
+    g = per["gemm_tc_bf16_kernel"]
+    assert g["launches"] == 1 and abs(g["ms"] - 0.010) < 1e-12 and abs(g["dram"] - 3.0e6) < 1e-6
+    assert abs(per["attention_kernel"]["ms"] - 0.030) < 1e-12
+    md = ns.markdown(per)
+    assert "| prefill_attention_tc_kernel | 1 | 0.060 | 0.600 |" in md
+    t = ns.traffic_by_class(per, scale=2.0)
+    assert abs(t["gemm_tc_bf16"] - 6.0e6) < 1e-6
+    assert abs(t["attention"] - 3.0e6) < 1e-6       # both attention kernels over one ragged-kernel launch
+    out = tmp_path / "traffic.json"
+    ns.main([str(p), "--traffic", str(out), "--workload", "w"])
+    d = json.loads(out.read_text())
+    assert d["w"]["gemm_tc_bf16"]["source_hash"] == ns.source_hash()
