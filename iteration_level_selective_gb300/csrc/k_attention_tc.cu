@@ -5,20 +5,23 @@
 // keys, softmax, O = P V.  One work item is up to 128 query rows of one
 // request and one head; persistent CTAs take items from an atomic ticket.
 //
-// Per item (two passes over the key tiles of 128 keys up to the last row's
-// position, so the output accumulator never needs rescaling):
-//   pass 1  S = Q K^T on tcgen05 into TMEM; each thread (one query row =
-//           one TMEM lane) reads its row of S and keeps the running max of
-//           the keys it may see (key position <= its own position);
-//   pass 2  S again; p = exp2((s - max) * log2(e)/sqrt(d)) in fp32, the row
-//           sum in registers, P rounded to bf16 into shared memory (K-major,
-//           128-byte swizzle); O += P V on tcgen05 with V transposed by the
-//           threads into a K-major tile (keys past the causal range are
-//           zero, so stale slot contents never reach O);
-//   end     O / sum -> bf16 rows of the output.
-// Q and K tiles arrive by TMA (tensor maps over the q buffer and the
-// layer's K slots).  Rows beyond the item's rows and keys beyond a row's
-// position are masked by selection.  Every mbarrier wait is bounded.
+// One pass over the key tiles (128 keys each) with an online softmax, the
+// roles of a CTA running as a pipeline:
+//   warp 0     claims items and loads Q, then K and V tiles by TMA into a
+//              ring of stages;
+//   warp 1     issues the MMAs: S = Q K^T into one of two TMEM buffers, and
+//              O += P V into a TMEM accumulator (V is the B operand as it
+//              lies in the K/V pool, head dim contiguous: MN-major);
+//   warps 2-5  one query row per thread (one TMEM lane): read the row of S,
+//              mask the keys past the row's position, keep the running max
+//              m and sum l, write P = exp2((S - m) * log2(e)/sqrt(d)) as
+//              bf16 into shared memory; O is rescaled only when m grows by
+//              more than a factor 2^8 (until then P may exceed 1, which fp32
+//              and bf16 hold as well); at the end O / l -> bf16 rows.
+// While the softmax warps work on tile t the tensor core computes S of tile
+// t+1 and P V of tile t-1.  Keys beyond the item's causal range are masked by
+// selection; their V rows are zeroed in shared memory before P V, so stale
+// slot contents never reach O.  Every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -29,32 +32,45 @@
 namespace orca {
 namespace {
 
-constexpr int kRows = 128;  // query rows per item = TMEM lanes
-constexpr int kKeys = 128;  // keys per tile
-constexpr int kThreadsTc = 128;
+constexpr int kRows = 128;       // query rows per item = TMEM lanes
+constexpr int kKeys = 128;       // keys per tile
+constexpr int kThreadsTc = 192;  // warp 0 loads, warp 1 issues MMAs, warps 2-5 softmax
+constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
 struct TcCfg {
-  static constexpr int KB = D / 64;              // 64-element K-blocks of the head dim
+  static constexpr int KB = D / 64;                // 64-element blocks of the head dim
+  static constexpr int NS = D == 128 ? 2 : 4;      // K/V stages
   static constexpr int Q_BYTES = KB * kRows * 128;
-  static constexpr int K_BYTES = KB * kKeys * 128;
-  static constexpr int VT_BYTES = 2 * D * 128;   // D rows x 128 keys (two 64-key K-blocks)
-  static constexpr int P_BYTES = 2 * kRows * 128;
-  static constexpr int SMEM = Q_BYTES + K_BYTES + VT_BYTES + P_BYTES + 1024;
-  static constexpr uint32_t TMEM_COLS = 256;     // S: [0, 128), O: [128, 128 + D)
+  static constexpr int K_BYTES = KB * kKeys * 128;  // K-major: key rows of 128 B per block
+  static constexpr int V_BYTES = KB * kKeys * 128;  // same bytes, read as an MN-major operand
+  static constexpr int P_BYTES = 2 * kRows * 128;   // 128 rows x 128 keys, K-major
+  static constexpr int SMEM = Q_BYTES + NS * (K_BYTES + V_BYTES) + P_BYTES + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;        // S0 [0,128), S1 [128,256), O [256, 256+D)
+  static constexpr uint32_t O_COL = 256;
+  // kind::f16: D fp32 (bit 4), A bf16 (bits 7-9), B bf16 (bits 10-12),
+  // B MN-major (bit 16) for P V, N >> 3 (bits 17-22), M >> 4 (bits 24-28)
   static constexpr uint32_t IDESC_S =
       (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kKeys >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
-  static constexpr uint32_t IDESC_O =
-      (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+  static constexpr uint32_t IDESC_O = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                      ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 };
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Shared-memory matrix descriptors, 128-byte swizzle (layout 2), version 1.
+// K-major: 8-row groups 1024 B apart (SBO), leading offset unused.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// MN-major: rows of 64 MN-elements (128 B) along K; 8-row groups along K are
+// `sbo` apart, 64-element column blocks along MN are `lbo` apart.
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -72,6 +88,7 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
                : "memory");
 }
 
+// 32 consecutive TMEM columns of this thread's lane (warp-collective).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   uint32_t r[32];
   asm volatile(
@@ -89,6 +106,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+// Hardware base-2 exponential (PTX ex2.approx; ftz).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Byte offset of element (row, k) in a K-major, 128-byte-swizzled operand
 // tile of `rows` rows (64-element K-blocks stacked, 8-row atoms of 1024 B).
 __device__ __forceinline__ uint32_t sw128_offset(int row, int k, int rows) {
@@ -96,206 +140,338 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int k, int rows) {
   return (uint32_t)(kb * rows * 128 + row * 128 + ((((kk >> 3) ^ (row & 7)) << 4) | ((kk & 7) << 1)));
 }
 
+// One claimed work item, decoded by the loader for the other roles.
+struct TcItem {
+  int head, r0, nq, p0;  // query rows r0 .. r0+nq-1 at positions p0 ..
+  int kv_len, n_tiles;   // keys 0 .. kv_len-1; n_tiles < 0 ends the CTA
+  long long krow0;       // row of key 0 in the [n_heads * n_slots, D] view
+};
+
+template <int NS>
 struct TcShared {
-  uint64_t kbar, sbar, obar;
+  uint64_t q_full, q_empty;
+  uint64_t k_full[NS], v_full[NS], kv_empty[NS];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full, o_done;
+  uint64_t it_full[2], it_empty[2];
+  TcItem it[2];
   uint32_t tmem;
-  int item;
   int abort;
 };
+
+// All lanes of the warp wait; the warp continues only if every lane saw the
+// phase (so the warp-collective TMEM accesses that follow stay converged).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *status) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     prefill_attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                                TcAttnArgs a) {
+                                const __grid_constant__ CUtensorMap tmV, TcAttnArgs a) {
   using C = TcCfg<D>;
+  constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ TcShared sh;
+  __shared__ TcShared<NS> sh;
   pdl_trigger();
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *sQ = smem_raw + pad;
-  uint8_t *sK = sQ + C::Q_BYTES;
-  uint8_t *sVt = sK + C::K_BYTES;
-  uint8_t *sP = sVt + C::VT_BYTES;
+  uint8_t *sK = sQ + C::Q_BYTES;       // NS stages of K
+  uint8_t *sV = sK + NS * C::K_BYTES;  // NS stages of V
+  uint8_t *sP = sV + NS * C::V_BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = warp * 32 + lane;  // query row of this thread = TMEM lane
   if (threadIdx.x == 0) {
-    mbar_init(&sh.kbar, 1);
-    mbar_init(&sh.sbar, 1);
-    mbar_init(&sh.obar, 1);
+    mbar_init(&sh.q_full, 1);
+    mbar_init(&sh.q_empty, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&sh.k_full[s], 1);
+      mbar_init(&sh.v_full[s], 1);
+      mbar_init(&sh.kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.s_full[b], 1);
+      mbar_init(&sh.s_empty[b], 128);
+      mbar_init(&sh.it_full[b], 1);
+      mbar_init(&sh.it_empty[b], 1 + 4);  // the MMA warp and the four softmax warps
+    }
+    mbar_init(&sh.p_full, 128);
+    mbar_init(&sh.o_done, 1);
     sh.abort = 0;
     mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
   }
-  if (warp == 0) {
+  if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sh.tmem)),
                  "r"(C::TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  const int n_work = a.n_work_dev ? *a.n_work_dev : a.n_work;  // header written before the forward
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem;
-  const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
-  const uint32_t tS = tmem + t_lane, tO = tmem + t_lane + 128;
   volatile int *abort_flag = &sh.abort;
-  uint32_t kph = 0, sph = 0, oph = 0;  // phases of the three barriers
-  const __nv_bfloat16 *Vl = static_cast<const __nv_bfloat16 *>(a.v_layer);
-  pdl_wait();  // q and the K/V slots come from the QKV Linear
+  pdl_wait();  // q and the K/V slots come from the QKV Linear; the output rows are its input
 
-  while (true) {
-    __syncthreads();
-    if (threadIdx.x == 0) sh.item = atomicAdd(a.ticket, 1);
-    __syncthreads();
-    const int item = sh.item;
-    if (item >= n_work * a.n_heads) break;
-    const int w_idx = item / a.n_heads, head = item - w_idx * a.n_heads;
-    const AttnWork w = a.work[w_idx];
-    const ReqInfo rq = a.reqs[w.req];
-    const int r0 = w.a, nq = w.b;
-    const int p0 = rq.ctx + (r0 - rq.row_off);
-    const int kv_len = p0 + nq;                 // keys 0 .. p0 + nq - 1
-    const bool bad = rq.slot_base < 0 || (int64_t)rq.slot_base + kv_len > a.n_slots || nq > kRows || nq <= 0;
-    if (bad) {
-      if (threadIdx.x == 0) atomicOr(a.status, kStatusBadIndex);
-      continue;
-    }
-    const int my_pos = row < nq ? p0 + row : -1;  // -1: no key is visible to this row
-    const int n_tiles = (kv_len + kKeys - 1) / kKeys;
-    const int64_t krow0 = (int64_t)head * a.n_slots + rq.slot_base;  // K / V row of key 0
-    // ---- Q tile (TMA) with the first K tile
-    auto load_k = [&](int t, bool with_q) {
-      if (threadIdx.x != 0 || *abort_flag) return;
-      mbar_expect_tx(&sh.kbar, C::K_BYTES + (with_q ? C::Q_BYTES : 0));
-      for (int kb = 0; kb < C::KB; ++kb) {
-        if (with_q) tma_load_2d(sQ + kb * kRows * 128, &tmQ, head * D + kb * 64, r0, &sh.kbar);
-        tma_load_2d(sK + kb * kKeys * 128, &tmK, kb * 64, (int)(krow0 + (int64_t)t * kKeys), &sh.kbar);
+  if (warp == 0) {
+    // ------------------------------------------------------------ loader
+    if (lane == 0) {
+      const int n_work = a.n_work_dev ? *a.n_work_dev : a.n_work;
+      const int total = n_work * a.n_heads;
+      uint32_t n_item = 0, g = 0;  // items enqueued, K/V tiles loaded
+      while (!*abort_flag) {
+        const int t = atomicAdd(a.ticket, 1);
+        TcItem it{};
+        it.n_tiles = -1;
+        if (t < total) {
+          // ticket -> (request group, head, query tile): a group is one
+          // request's query tiles (work[G .. G+T-1]); its tickets run over
+          // the heads, the tiles of one head consecutive (shared K/V in L2)
+          const int g0 = a.work[t / a.n_heads].kind;
+          const int G = g0 >> 10, T = g0 & 1023;
+          const int local = t - G * a.n_heads;
+          const int head = T > 0 ? local / T : a.n_heads;
+          const int wi = T > 0 ? G + local % T : 0;
+          const AttnWork w = a.work[wi < n_work ? wi : 0];
+          const ReqInfo rq = a.reqs[w.req];
+          it.head = head;
+          it.r0 = w.a;
+          it.nq = w.b;
+          it.p0 = rq.ctx + (w.a - rq.row_off);
+          it.kv_len = it.p0 + w.b;
+          it.krow0 = (long long)head * a.n_slots + rq.slot_base;
+          it.n_tiles = (it.kv_len + kKeys - 1) / kKeys;
+          if (T <= 0 || wi >= n_work || local < 0 || head >= a.n_heads || rq.slot_base < 0 ||
+              (int64_t)rq.slot_base + it.kv_len > a.n_slots || w.b > kRows || w.b <= 0 || it.p0 < 0) {
+            atomicOr(a.status, kStatusBadIndex);
+            continue;
+          }
+        }
+        const uint32_t slot = n_item & 1;
+        if (n_item >= 2 && !mbar_wait(&sh.it_empty[slot], ((n_item - 2) >> 1) & 1, abort_flag, a.status)) break;
+        sh.it[slot] = it;
+        mbar_arrive(&sh.it_full[slot]);
+        ++n_item;
+        if (it.n_tiles < 0) break;
+        // Q of this item once the previous item's S products are done
+        if (n_item >= 2 && !mbar_wait(&sh.q_empty, (n_item - 2) & 1, abort_flag, a.status)) break;
+        mbar_expect_tx(&sh.q_full, C::Q_BYTES);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_2d(sQ + kb * kRows * 128, &tmQ, it.head * D + kb * 64, it.r0, &sh.q_full);
+        bool ok = true;
+        for (int tile = 0; tile < it.n_tiles; ++tile, ++g) {
+          const uint32_t s = g % NS, use = g / NS;
+          if (use >= 1 && !mbar_wait(&sh.kv_empty[s], (use - 1) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const int krow = (int)(it.krow0 + (long long)tile * kKeys);
+          mbar_expect_tx(&sh.k_full[s], C::K_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_2d(sK + s * C::K_BYTES + kb * kKeys * 128, &tmK, kb * 64, krow, &sh.k_full[s]);
+          mbar_expect_tx(&sh.v_full[s], C::V_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_2d(sV + s * C::V_BYTES + kb * kKeys * 128, &tmV, kb * 64, krow, &sh.v_full[s]);
+        }
+        if (!ok) break;
       }
-    };
-    auto mma_s = [&]() {  // S = Q K^T
-      if (threadIdx.x != 0) return;
-      tc_fence_after();
-      for (int kb = 0; kb < C::KB; ++kb)
-        for (int k = 0; k < 4; ++k)
-          tc_mma(tmem, sw128_desc(smem_u32(sQ + kb * kRows * 128) + k * 32),
-                 sw128_desc(smem_u32(sK + kb * kKeys * 128) + k * 32), C::IDESC_S, (kb | k) ? 1u : 0u);
-      tc_commit(&sh.sbar);
-    };
-    // ---- pass 1: row max of the visible scores (raw dot products)
-    float mx = -INFINITY;
-    for (int t = 0; t < n_tiles; ++t) {
-      load_k(t, t == 0);
-      mbar_wait(&sh.kbar, kph, abort_flag, a.status);
-      kph ^= 1u;
-      mma_s();
-      mbar_wait(&sh.sbar, sph, abort_flag, a.status);
-      sph ^= 1u;
-      tc_fence_after();
-      for (int c = 0; c < kKeys; c += 32) {
-        float v[32];
-        tmem_ld32(tS + (uint32_t)c, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = t * kKeys + c + i;
-          if (key <= my_pos) mx = fmaxf(mx, v[i]);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t n_item = 0, g = 0;
+    const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV), pa = smem_u32(sP);
+    while (true) {
+      const uint32_t slot = n_item & 1;
+      if (!warp_wait(&sh.it_full[slot], (n_item >> 1) & 1, abort_flag, a.status)) break;
+      const TcItem it = sh.it[slot];
+      if (it.n_tiles < 0) break;
+      if (!warp_wait(&sh.q_full, n_item & 1, abort_flag, a.status)) break;
+      bool ok = true;
+      for (int tile = 0; tile <= it.n_tiles; ++tile) {
+        if (tile < it.n_tiles) {  // S(tile) = Q K^T into buffer (g + tile) & 1
+          const uint32_t gt = g + tile, s = gt % NS, b = gt & 1, use_b = gt >> 1;
+          if ((use_b >= 1 && !warp_wait(&sh.s_empty[b], (use_b - 1) & 1, abort_flag, a.status)) ||
+              !warp_wait(&sh.k_full[s], (gt / NS) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            tc_fence_after();
+            for (int kb = 0; kb < C::KB; ++kb)
+              for (int k = 0; k < 4; ++k)
+                tc_mma(tmem + b * 128, sw128_desc(qa + kb * kRows * 128 + k * 32),
+                       sw128_desc(ka + s * C::K_BYTES + kb * kKeys * 128 + k * 32), C::IDESC_S,
+                       (kb | k) ? 1u : 0u);
+            tc_commit(&sh.s_full[b]);
+            if (tile == it.n_tiles - 1) tc_commit(&sh.q_empty);
+          }
+          __syncwarp();
+        }
+        if (tile >= 1) {  // O += P(tile-1) V(tile-1)
+          const int tp = tile - 1;
+          const uint32_t gp = g + tp, s = gp % NS;
+          if (!warp_wait(&sh.p_full, gp & 1, abort_flag, a.status) ||
+              !warp_wait(&sh.v_full[s], (gp / NS) & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const int valid = it.kv_len - tp * kKeys;  // V rows holding keys of this item
+          if (valid < kKeys) {
+            uint8_t *vt = sV + s * C::V_BYTES;
+            const int n_chunks = (kKeys - valid) * C::KB * 8;
+            for (int c = lane; c < n_chunks; c += 32) {
+              const int r = valid + c / (C::KB * 8), rem = c % (C::KB * 8);
+              *reinterpret_cast<uint4 *>(vt + (rem >> 3) * kKeys * 128 + r * 128 + (rem & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async();
+          }
+          __syncwarp();
+          if (lane == 0) {
+            tc_fence_after();
+            for (int kk = 0; kk < kKeys / 16; ++kk)
+              tc_mma(tmem + C::O_COL, sw128_desc(pa + (kk >> 2) * kRows * 128 + (kk & 3) * 32),
+                     sw128_mn_desc(va + s * C::V_BYTES + kk * 2048, kKeys * 128, 1024), C::IDESC_O,
+                     (tp | kk) ? 1u : 0u);
+            tc_commit(&sh.kv_empty[s]);
+            tc_commit(&sh.o_done);
+          }
+          __syncwarp();
         }
       }
-      tc_fence_before();
-      __syncthreads();  // S and the K tile are free again
+      if (!ok) break;
+      g += it.n_tiles;
+      if (lane == 0) mbar_arrive(&sh.it_empty[slot]);
+      ++n_item;
     }
-    // ---- pass 2: P = exp2((S - max) * scale), O += P V
-    float sum = 0.f;
-    for (int t = 0; t < n_tiles; ++t) {
-      load_k(t, false);
-      // V tile transposed into sVt (K-major: row = head dim, 128 keys per row);
-      // keys beyond kv_len are written as zero
-      for (int e = threadIdx.x; e < (kKeys / 2) * (D / 8); e += kThreadsTc) {
-        const int kp = e % (kKeys / 2), dc = e / (kKeys / 2);
-        const int key = t * kKeys + 2 * kp;
-        uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-        if (key < kv_len) v0 = __ldg(reinterpret_cast<const uint4 *>(Vl + (krow0 + key) * D + dc * 8));
-        if (key + 1 < kv_len) v1 = __ldg(reinterpret_cast<const uint4 *>(Vl + (krow0 + key + 1) * D + dc * 8));
-        const uint16_t *h0 = reinterpret_cast<const uint16_t *>(&v0);
-        const uint16_t *h1 = reinterpret_cast<const uint16_t *>(&v1);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t pk = (uint32_t)h0[j] | ((uint32_t)h1[j] << 16);
-          *reinterpret_cast<uint32_t *>(sVt + sw128_offset(dc * 8 + j, 2 * kp, D)) = pk;
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quad = warp & 3;         // TMEM lane quarter this warp may access
+    const int row = quad * 32 + lane;  // query row of this thread
+    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+    uint32_t n_item = 0, g = 0, o_cnt = 0;
+    while (true) {
+      const uint32_t slot = n_item & 1;
+      if (!warp_wait(&sh.it_full[slot], (n_item >> 1) & 1, abort_flag, a.status)) break;
+      const TcItem it = sh.it[slot];
+      if (it.n_tiles < 0) break;
+      const int my_pos = row < it.nq ? it.p0 + row : -1;  // -1: no key is visible to this row
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int tile = 0; tile < it.n_tiles; ++tile) {
+        const uint32_t gt = g + tile, b = gt & 1;
+        if (!warp_wait(&sh.s_full[b], (gt >> 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
         }
-      }
-      mbar_wait(&sh.kbar, kph, abort_flag, a.status);
-      kph ^= 1u;
-      mma_s();
-      mbar_wait(&sh.sbar, sph, abort_flag, a.status);
-      sph ^= 1u;
-      tc_fence_after();
-      for (int c = 0; c < kKeys; c += 32) {
-        float v[32];
-        tmem_ld32(tS + (uint32_t)c, v);
-        uint32_t pk[16];
+        tc_fence_after();
+        float v[kKeys];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int key = t * kKeys + c + i;
-          const float pa = key <= my_pos ? exp2f((v[i] - mx) * a.scale_log2) : 0.f;
-          const float pb = key + 1 <= my_pos ? exp2f((v[i + 1] - mx) * a.scale_log2) : 0.f;
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(pa, pb);
-          sum += __low2float(b2) + __high2float(b2);  // the sum of the P that reaches the MMA
+        for (int c = 0; c < kKeys; c += 32) tmem_ld32(tl + b * 128 + c, v + c);
+        tc_fence_before();
+        mbar_arrive(&sh.s_empty[b]);
+        const int k0 = tile * kKeys;
+        if (k0 + kKeys - 1 > my_pos) {
+#pragma unroll
+          for (int i = 0; i < kKeys; ++i)
+            if (k0 + i > my_pos) v[i] = -INFINITY;
+        }
+        float tmax = v[0];
+#pragma unroll
+        for (int i = 1; i < kKeys; ++i) tmax = fmaxf(tmax, v[i]);
+        const float m_new = fmaxf(m, tmax);
+        const bool need = (m_new - m) * a.scale_log2 > kRescaleLog2;  // false while both are -inf
+        float alpha = 1.f;
+        if (need) {
+          alpha = m == -INFINITY ? 0.f : ex2((m - m_new) * a.scale_log2);
+          l *= alpha;
+          m = m_new;
+        }
+        const float ms = m == -INFINITY ? 0.f : m * a.scale_log2;
+        uint32_t pk[kKeys / 2];
+        float lsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < kKeys; i += 2) {
+          const float p0 = ex2(fmaf(v[i], a.scale_log2, -ms));
+          const float p1 = ex2(fmaf(v[i + 1], a.scale_log2, -ms));
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          lsum += __low2float(b2) + __high2float(b2);  // the P that reaches the MMA
           pk[i / 2] = *reinterpret_cast<const uint32_t *>(&b2);
         }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<uint4 *>(sP + sw128_offset(row, c + q4 * 8, kRows)) =
-              make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-      }
-      tc_fence_before();
-      fence_proxy_async();  // P and V^T (generic stores) become visible to the tensor core
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        tc_fence_after();
-        for (int kb = 0; kb < 2; ++kb)
-          for (int k = 0; k < 4; ++k)
-            tc_mma(tmem + 128, sw128_desc(smem_u32(sP + kb * kRows * 128) + k * 32),
-                   sw128_desc(smem_u32(sVt + kb * D * 128) + k * 32), C::IDESC_O, (t | kb | k) ? 1u : 0u);
-        tc_commit(&sh.obar);
-      }
-      mbar_wait(&sh.obar, oph, abort_flag, a.status);  // P, V^T, S free for the next tile
-      oph ^= 1u;
-    }
-    // ---- O / sum -> output rows
-    tc_fence_after();
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) + (int64_t)(r0 + row) * a.hidden + head * D;
-    for (int c = 0; c < D; c += 32) {
-      float v[32];
-      tmem_ld32(tO + (uint32_t)c, v);
-      if (row < nq && !*abort_flag) {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[q4 * 8 + 2 * j] * inv, v[q4 * 8 + 2 * j + 1] * inv);
-            pk[j] = *reinterpret_cast<const uint32_t *>(&b2);
+        l += lsum;
+        if (tile > 0) {  // P buffer and O are free once P V of the previous tile is done
+          if (!warp_wait(&sh.o_done, o_cnt & 1, abort_flag, a.status)) {
+            ok = false;
+            break;
           }
-          *reinterpret_cast<uint4 *>(orow + c + q4 * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          ++o_cnt;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              float o[32];
+              tmem_ld32(tl + C::O_COL + c, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= alpha;
+              tmem_st32(tl + C::O_COL + c, o);
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kKeys / 8; ++q)
+          *reinterpret_cast<uint4 *>(sP + sw128_offset(row, q * 8, kRows)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        fence_proxy_async();  // P (generic stores) becomes visible to the tensor core
+        tc_fence_before();
+        mbar_arrive(&sh.p_full);
+      }
+      if (!ok) break;
+      // ---- O / l -> output rows
+      if (!warp_wait(&sh.o_done, o_cnt & 1, abort_flag, a.status)) break;
+      ++o_cnt;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) + (int64_t)(it.r0 + row) * a.hidden + it.head * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        float o[32];
+        tmem_ld32(tl + C::O_COL + c, o);
+        if (row < it.nq) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[q4 * 8 + 2 * j] * inv, o[q4 * 8 + 2 * j + 1] * inv);
+              pk[j] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            *reinterpret_cast<uint4 *>(orow + c + q4 * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
         }
       }
+      tc_fence_before();
+      if (lane == 0) mbar_arrive(&sh.it_empty[slot]);
+      g += it.n_tiles;
+      ++n_item;
     }
-    tc_fence_before();
   }
+
   // teardown: the last CTA out resets the ticket; free tensor memory
+  __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(a.ticket + 1, 1) == (int)gridDim.x - 1) {
       a.ticket[0] = 0;
       a.ticket[1] = 0;
     }
+    if (*abort_flag) drain_after_abort();
   }
-  if (*abort_flag && threadIdx.x == 0) drain_after_abort();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
   }
@@ -325,8 +501,8 @@ cudaError_t attention_tc_prepare() {
 
 bool attention_tc_supported(int dtype, int head_dim) { return dtype == 1 && (head_dim == 64 || head_dim == 128); }
 
-cudaError_t launch_attention_tc(int head_dim, const CUtensorMap *tmQ, const CUtensorMap *tmK, const TcAttnArgs &a,
-                                int n_work, cudaStream_t st) {
+cudaError_t launch_attention_tc(int head_dim, const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                const TcAttnArgs &a, int n_work, cudaStream_t st) {
   if (n_work <= 0 && a.n_work_dev == nullptr) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -337,12 +513,13 @@ cudaError_t launch_attention_tc(int head_dim, const CUtensorMap *tmQ, const CUte
   if (head_dim == 64) {
     e = set_limit<64>(dev);
     if (e != cudaSuccess) return e;
-    return launch_pdl(prefill_attention_tc_kernel<64>, grid, kThreadsTc, TcCfg<64>::SMEM, st, *tmQ, *tmK, a);
+    return launch_pdl(prefill_attention_tc_kernel<64>, grid, kThreadsTc, TcCfg<64>::SMEM, st, *tmQ, *tmK, *tmV, a);
   }
   if (head_dim == 128) {
     e = set_limit<128>(dev);
     if (e != cudaSuccess) return e;
-    return launch_pdl(prefill_attention_tc_kernel<128>, grid, kThreadsTc, TcCfg<128>::SMEM, st, *tmQ, *tmK, a);
+    return launch_pdl(prefill_attention_tc_kernel<128>, grid, kThreadsTc, TcCfg<128>::SMEM, st, *tmQ, *tmK, *tmV,
+                      a);
   }
   return cudaErrorInvalidValue;
 }

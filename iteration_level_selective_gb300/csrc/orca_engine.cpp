@@ -97,6 +97,7 @@ struct SlotPool {
 
 int32_t max_attn_work(int32_t n_batch, int32_t n_rows);
 int32_t max_tc_work(int32_t n_batch, int32_t n_rows);
+int order_tc_work(AttnWork *w, int32_t n, const ReqInfo *req);
 
 struct Layout {  // byte offsets into the device workspace
   size_t x, h, q, u, hf, logits, out, req, row, work, work_tc, part, counters, gemm_cnt, gemm_part, total;
@@ -201,6 +202,36 @@ int32_t append_tc_work(AttnWork *w, int32_t n, int32_t i, int32_t row, int32_t L
   return n;
 }
 
+// Tensor-core items grouped by request (groups with the most work first,
+// within a group the query tiles with the most keys first).  Each item's kind
+// records its group as (first index << 10) | size: the kernel walks a group's
+// tiles head by head, so the CTAs working at one time share K/V in L2.
+int order_tc_work(AttnWork *w, int32_t n, const ReqInfo *req) {
+  auto cost = [&](const AttnWork &x) -> int64_t {
+    const ReqInfo &r = req[x.req];
+    return (int64_t)x.b * (r.ctx + (x.a - r.row_off) + x.b);
+  };
+  int32_t max_req = 0;
+  for (int32_t k = 0; k < n; ++k) max_req = std::max(max_req, w[k].req);
+  std::vector<int64_t> group_cost(max_req + 1, 0);  // indexed by request
+  for (int32_t k = 0; k < n; ++k) group_cost[w[k].req] += cost(w[k]);
+  std::stable_sort(w, w + n, [&](const AttnWork &x, const AttnWork &y) {
+    if (x.req != y.req) {
+      if (group_cost[x.req] != group_cost[y.req]) return group_cost[x.req] > group_cost[y.req];
+      return x.req < y.req;
+    }
+    return cost(x) > cost(y);
+  });
+  for (int32_t k = 0; k < n;) {
+    int32_t e = k;
+    while (e < n && w[e].req == w[k].req) ++e;
+    if (e - k > 1023 || k >= (1 << 21)) return ORCA_EBATCH;
+    for (int32_t j = k; j < e; ++j) w[j].kind = (k << 10) | (e - k);
+    k = e;
+  }
+  return ORCA_OK;
+}
+
 int32_t max_tc_work(int32_t n_batch, int32_t n_rows) { return n_rows / kTcMinRows + n_batch; }
 
 int32_t max_attn_work(int32_t n_batch, int32_t n_rows) {
@@ -231,6 +262,7 @@ struct orca_engine {
   // tensor maps (bf16)
   CUtensorMap tm_h{}, tm_u{}, tm_hf{}, tm_q{};
   std::vector<CUtensorMap> tm_k;      // per layer: K slots as [n_heads * n_slots, head_dim]
+  std::vector<CUtensorMap> tm_v;      // per layer: V slots, same view
   bool attn_tc = false;               // prompts take the tensor-core prefill kernel
   WeightMaps tm_emb{};
   std::vector<WeightMaps> tm_layer;  // 4 per layer: qkv, o, fc1, fc2
@@ -456,7 +488,6 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     if (e->attn_tc) {  // prompts: tensor-core tiles; then decodes and short prompts
       TcAttnArgs ta{};
       ta.out = h;
-      ta.v_layer = vl;
       ta.reqs = d_req;
       ta.work = ws_ptr<AttnWork>(e, Ly.work_tc);
       ta.ticket = aa.ticket + 2;
@@ -467,7 +498,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
       ta.n_work_dev = graph ? &d_hdr->n_work_tc : nullptr;
       ta.n_slots = c.n_slots;
       ta.scale_log2 = aa.scale_log2;
-      CUDA_TRY(e, launch_attention_tc(D, &e->tm_q, &e->tm_k[l], ta, z.n_work_tc, st));
+      CUDA_TRY(e, launch_attention_tc(D, &e->tm_q, &e->tm_k[l], &e->tm_v[l], ta, z.n_work_tc, st));
       if (graph || z.n_work_tc > 0) ++e->n_launch;
     }
     LAUNCH(e, launch_attention(c.dtype, D, aa, graph ? Ly.max_work : z.n_work, st));
@@ -649,9 +680,14 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
       rc = make_tmap(e, &e->tm_q, e->ws + L.q, cfg->max_rows, H, kTcBM);
       const size_t layer_kv = (size_t)2 * cfg->n_heads * cfg->n_slots * e->head_dim * 2;
       e->tm_k.resize(cfg->n_layers);
-      for (int l = 0; l < cfg->n_layers && !rc; ++l)
+      e->tm_v.resize(cfg->n_layers);
+      for (int l = 0; l < cfg->n_layers && !rc; ++l) {
         rc = make_tmap(e, &e->tm_k[l], e->kv + (size_t)l * layer_kv, (uint64_t)cfg->n_heads * cfg->n_slots,
                        e->head_dim, kTcBM);
+        if (!rc)
+          rc = make_tmap(e, &e->tm_v[l], e->kv + (size_t)l * layer_kv + layer_kv / 2,
+                         (uint64_t)cfg->n_heads * cfg->n_slots, e->head_dim, kTcBM);
+      }
     }
     for (int l = 0; l < cfg->n_layers && !rc; ++l) {
       rc = make_weight_maps(e, &e->tm_layer[4 * l + 0], lw(e, l, L_WQKV), 3 * H, H);
@@ -799,7 +835,8 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
     row += L[i];
   }
   order_attn_work(e->h_work, n_work, e->h_req, split);
-  order_attn_work(e->h_work_tc, n_work_tc, e->h_req, split);
+  if (order_tc_work(e->h_work_tc, n_work_tc, e->h_req))
+    return fail(e, ORCA_EBATCH, "a prompt has more than 1023 query tiles");
   // host copy for orca_last_descriptor / orca_last_transfer
   e->last_B = n_batch;
   e->last_N = N;
@@ -1011,7 +1048,7 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
       n_work = append_attn_work(work.data(), n_work, i, req[i].row_off, req[i].n_new, req[i].ctx, split);
   }
   order_attn_work(work.data(), n_work, req.data(), split);
-  order_attn_work(work_tc.data(), n_work_tc, req.data(), split);
+  if (order_tc_work(work_tc.data(), n_work_tc, req.data())) return ORCA_EBATCH;
   char *ws = static_cast<char *>(workspace);
   ReqInfo *d_req = reinterpret_cast<ReqInfo *>(ws + Lw.req);
   AttnWork *d_work = reinterpret_cast<AttnWork *>(ws + Lw.work);
@@ -1031,13 +1068,13 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
     return ORCA_ECUDA;
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
   if (n_work_tc > 0) {
-    CUtensorMap tq, tk;
+    CUtensorMap tq, tk, tv;
     if (make_tmap(nullptr, &tq, q, N, (uint64_t)n_heads * head_dim, kTcBM) ||
-        make_tmap(nullptr, &tk, k_layer, (uint64_t)n_heads * n_slots, head_dim, kTcBM))
+        make_tmap(nullptr, &tk, k_layer, (uint64_t)n_heads * n_slots, head_dim, kTcBM) ||
+        make_tmap(nullptr, &tv, v_layer, (uint64_t)n_heads * n_slots, head_dim, kTcBM))
       return ORCA_EINVAL;
     TcAttnArgs ta{};
     ta.out = out;
-    ta.v_layer = v_layer;
     ta.reqs = d_req;
     ta.work = d_work_tc;
     ta.ticket = d_cnt + (size_t)n_batch * n_heads + 2;
@@ -1048,7 +1085,7 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
     ta.n_work_dev = nullptr;
     ta.n_slots = n_slots;
     ta.scale_log2 = scale_log2;
-    if (launch_attention_tc(head_dim, &tq, &tk, ta, n_work_tc, st) != cudaSuccess) return ORCA_ECUDA;
+    if (launch_attention_tc(head_dim, &tq, &tk, &tv, ta, n_work_tc, st) != cudaSuccess) return ORCA_ECUDA;
   }
   AttnArgs aa{};
   aa.q = q;

@@ -137,9 +137,8 @@ struct AttnArgs {
 // req, a = first row, b = rows, at most kTcRows).
 struct TcAttnArgs {
   void *out;              // [n_rows, H] bf16
-  const void *v_layer;    // [n_heads][n_slots][D] bf16
   const ReqInfo *reqs;
-  const AttnWork *work;
+  const AttnWork *work;   // query tiles grouped by request, kind = (group start << 10) | group size
   int32_t *ticket;        // [2], zero between launches
   int32_t *status;
   int32_t hidden, n_heads, n_work;
@@ -186,10 +185,10 @@ cudaError_t gemm_prepare();
 cudaError_t attention_prepare();
 cudaError_t attention_tc_prepare();
 bool attention_tc_supported(int dtype, int head_dim);
-// tmQ: q buffer [rows, H] (box 64 x 128); tmK: one layer's K slots viewed as
-// [n_heads * n_slots, D] (box 64 x 128).
-cudaError_t launch_attention_tc(int head_dim, const CUtensorMap *tmQ, const CUtensorMap *tmK, const TcAttnArgs &a,
-                                int n_work, cudaStream_t st);
+// tmQ: q buffer [rows, H] (box 64 x 128); tmK / tmV: one layer's K / V slots
+// viewed as [n_heads * n_slots, D] (box 64 x 128).
+cudaError_t launch_attention_tc(int head_dim, const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                const TcAttnArgs &a, int n_work, cudaStream_t st);
 // Persistent over (work item, head) pairs; n_work is the host count, or
 // the capacity when args.hdr is set.
 cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &args, int n_work, cudaStream_t st);

@@ -105,6 +105,8 @@ ATTN_CASES = {
     # 16 prompts U{1024..2048} + 240 decodes with contexts U{128..2048}, 13B-shaped heads
     "c5": lambda rng: ([(int(L), 0) for L in rng.integers(1024, 2049, 16)] +
                        [(1, int(c)) for c in rng.integers(128, 2049, 240)], 40, 128),
+    # the 16 prompts of c5 alone (tensor-core prefill kernel only)
+    "c5_prefill": lambda rng: ([(int(L), 0) for L in rng.integers(1024, 2049, 16)], 40, 128),
     # one GPT-2-small prefill of 512 tokens plus 63 decodes with contexts U{32..768}
     "gpt2_mixed": lambda rng: ([(512, 0)] + [(1, int(c)) for c in rng.integers(32, 769, 63)], 12, 64),
 }
