@@ -238,16 +238,19 @@ def fixed_batch_spec(name: str):
 
 
 class TraceWorkload:
-    """The GPT-2-small serving trace, restarted whenever it completes."""
+    """The GPT-2-small serving trace, restarted whenever it completes
+    (optionally with chunked prefill under a per-iteration token budget)."""
 
-    def __init__(self, eng, rank, stream):
+    def __init__(self, eng, rank, stream, token_budget=None, chunk=None):
         from iteration_level_selective_gb300 import runtime as rt
         self.rt, self.eng, self.rank, self.stream, self.gen = rt, eng, rank, stream, 0
+        self.budget = (token_budget, chunk)
         self.loop = self._new()
 
     def _new(self):
         self.gen += 1
-        return self.rt.ServingLoop(self.eng, self.rt.RequestPool(trace_for(self.rank, self.gen)), stream=self.stream)
+        return self.rt.ServingLoop(self.eng, self.rt.RequestPool(trace_for(self.rank, self.gen)), stream=self.stream,
+                                   token_budget=self.budget[0], chunk=self.budget[1])
 
     def step(self):
         if self.loop.done():
@@ -316,11 +319,16 @@ def run_ours(args, rank: int, world: int):
         del host_w
         n_slots = args.kv_slots if args.kv_slots else n_slots_for(shape)
         eng = rt.Engine(shape, weights, max_bs=64, n_slots=n_slots, max_rows=64 * 512, device=dev)
-        work = TraceWorkload(eng, rank, stream)
+        work = TraceWorkload(eng, rank, stream, args.token_budget, args.chunk)
         workload = WORKLOAD
+        if args.token_budget or args.chunk:
+            workload += f", chunked prefill (token budget {args.token_budget or 'none'}, chunk {args.chunk or 'none'})"
         cfg_extra = {"model": "gpt2-small-shaped (12L, H768, 12 heads, V50257), random init", "max_bs": 64,
                      "n_slots": n_slots, "arrivals": "Poisson 0.5 per iteration",
                      "l2": "inputs larger than L2 (0.25 GB weights + K/V pool), no flush"}
+        if args.token_budget or args.chunk:
+            cfg_extra["token_budget"] = args.token_budget or None
+            cfg_extra["chunk"] = args.chunk or None
     else:
         shape, prompts, ctx, workload = fixed_batch_spec(args.config)
         n_slots = FixedBatchWorkload.slots_needed(prompts, ctx)
@@ -353,13 +361,16 @@ def run_ours(args, rank: int, world: int):
     sampler = ClockSampler(local)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     rows = gen_tok = done = h2d = d2h = launches = 0
+    step_ms = []
     torch.cuda.synchronize(dev)
     w0 = time.perf_counter()
     ev0.record(stream)
     for _ in range(steps):
+        t0 = time.perf_counter()
         rec, hb, db = step()
+        step_ms.append(1000.0 * (time.perf_counter() - t0))
         rows += sum(rec.n_new)
-        gen_tok += len(rec.req_ids)
+        gen_tok += sum(1 for t in rec.next_tokens if t >= 0)
         done += len(rec.released)
         h2d += hb
         d2h += db
@@ -432,6 +443,9 @@ def run_ours(args, rank: int, world: int):
         "e2e": {"value": rows / wall, "unit": UNIT, "h2d_bytes_per_step": h2d / steps / max(1, world),
                 "d2h_bytes_per_step": d2h / steps / max(1, world)},
         "gpu_launches": launches,
+        "iteration_ms": {"p50": round(float(np.percentile(step_ms, 50)), 4),
+                         "p99": round(float(np.percentile(step_ms, 99)), 4), "max": round(max(step_ms), 4),
+                         "clock": "host wall clock per iteration (the call waits for the tokens)"},
         "roofline": roof,
         "kernel_roofline": per_kernel,
         "kernel_time_share": {k: round(v["ms"] / total_ms, 4) for k, v in agg.items()},
@@ -463,6 +477,10 @@ def main():
                          "13b-decode (one decode-only 13B iteration)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--token-budget", type=int, default=0,
+                    help="gpt2-trace only: chunked prefill with this many rows per iteration at most")
+    ap.add_argument("--chunk", type=int, default=0,
+                    help="gpt2-trace only: prompt chunk size for chunked prefill")
     ap.add_argument("--kv-slots", type=int, default=0,
                     help="gpt2-trace only: K/V pool slots (default: 40 GB worth); the trace needs at most "
                          "64 x 768, so profiler captures use a small pool")

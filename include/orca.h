@@ -89,11 +89,16 @@ typedef struct {
  *   state: ORCA_INITIATION until first scheduled; Select sets RUNNING,
  *   orca_iteration sets INCREMENT or FINISHED.
  *   n_prompt: prompt tokens; out_len: tokens to generate (no EOS);
- *   max_tokens: K/V slots reserved at first schedule (>= n_prompt).
+ *   max_tokens: the request's length limit, prompt included (>= n_prompt).
  *   n_cached: tokens whose K/V are stored; n_generated: tokens produced.
- *   slot_base: first reserved slot (-1 before reservation).
+ *   n_sched: rows of this request in the selected batch, set by the Select
+ *   calls (0 = the default: the rest of the prompt while n_cached <
+ *   n_prompt, else one row); orca_iteration resets it to 0.
+ *   n_reserved: K/V slots reserved at first schedule (0 before; set by
+ *   Select); slot_base: first reserved slot (-1 before reservation).
  *   tokens: host int32 buffer of capacity n_prompt + out_len holding the
  *   prompt followed by the generated (or teacher-forced) tokens.
+ * Callers initialise n_sched = n_reserved = 0 and slot_base = -1.
  * A request finishes when n_generated == out_len or
  * n_prompt + n_generated >= max_tokens; its slots are then released. */
 typedef struct {
@@ -105,6 +110,8 @@ typedef struct {
   int32_t out_len;
   int32_t n_cached;
   int32_t n_generated;
+  int32_t n_sched;
+  int32_t n_reserved;
   int64_t slot_base;
   int32_t *tokens;
 } orca_request;
@@ -186,17 +193,37 @@ int orca_kv_stats(const orca_engine *eng, int64_t *n_rsrv, int64_t *n_free_block
 int orca_select_batch(orca_engine *eng, orca_request *pool, int32_t n_pool, int32_t *batch_idx,
                       int32_t *n_batch);
 
+/* Select with chunked prefill under a per-iteration token budget (CS349D
+ * Lecture 2, Exercise 9: prompts cut into chunks, SeqWork(n_new = chunk,
+ * n_past = tokens already processed), a cap on the tokens of one
+ * iteration; static-to-continuous article, chunked prefill: decode first).
+ * First Algorithm 1 Select exactly as orca_select_batch (FCFS, max_bs,
+ * reservation, break); then, over the selected requests, every decoding
+ * request (n_cached >= n_prompt) takes one row while the budget lasts, in
+ * batch order, and then every prompting request takes
+ * min(n_prompt - n_cached, chunk, budget left) rows, in batch order.
+ * Requests left with no row are dropped from batch_idx and become
+ * INCREMENT (a reservation made for them is kept); the rest are RUNNING
+ * with n_sched set.  token_budget >= 1 and chunk >= 1 (INT32_MAX for no
+ * limit: then the result equals orca_select_batch). */
+int orca_select_batch_budget(orca_engine *eng, orca_request *pool, int32_t n_pool, int32_t token_budget,
+                             int32_t chunk, int32_t *batch_idx, int32_t *n_batch);
+
 /* Run one selectively batched iteration for pool[batch_idx[0..n_batch)]
  * (all RUNNING) on `stream`, then wait for it.  Request i contributes
- * L_i = n_prompt - n_cached rows when n_cached < n_prompt (prefill) and
- * one row otherwise (decode); its rows carry tokens[n_cached + j] at
+ * L_i = n_sched rows when n_sched > 0, else n_prompt - n_cached rows when
+ * n_cached < n_prompt (prefill) and one row otherwise (decode); n_sched
+ * may not exceed that default.  Its rows carry tokens[n_cached + j] at
  * positions n_cached + j.  Rows are flattened in batch order (Figure 5).
  * next_tokens (host, capacity n_batch) receives each request's greedy
- * token (argmax of the last row's logits, lowest index on ties).
+ * token (argmax of the last row's logits, lowest index on ties; -1 for a
+ * request whose prompt is not complete after this iteration).
  * logits_dev, if not NULL, receives fp32 [n_batch, vocab] logits.
- * Afterwards each request is INCREMENT (or FINISHED, slots released),
- * n_cached += L_i, n_generated += 1, and, unless ORCA_ITER_TEACHER_FORCE,
- * the token is appended to tokens[].  On error no request is modified.
+ * Afterwards each request is INCREMENT (or FINISHED, slots released) with
+ * n_cached += L_i and n_sched = 0; once its prompt is complete it also
+ * gets n_generated += 1 and, unless ORCA_ITER_TEACHER_FORCE, the token is
+ * appended to tokens[] (a prompt chunk that leaves part of the prompt
+ * unprocessed generates nothing).  On error no request is modified.
  * bf16 engines replay a CUDA graph of the whole forward (captured on first
  * use for each GEMM tile-shape choice and logits pointer, on an internal
  * stream; every kernel reads the iteration's sizes from the device

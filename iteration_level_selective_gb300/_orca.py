@@ -53,7 +53,8 @@ class orca_config(ctypes.Structure):
 class orca_request(ctypes.Structure):
     _fields_ = [("req_id", ctypes.c_int64), ("arrival", ctypes.c_int64), ("state", ctypes.c_int32),
                 ("n_prompt", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("out_len", ctypes.c_int32),
-                ("n_cached", ctypes.c_int32), ("n_generated", ctypes.c_int32), ("slot_base", ctypes.c_int64),
+                ("n_cached", ctypes.c_int32), ("n_generated", ctypes.c_int32), ("n_sched", ctypes.c_int32),
+                ("n_reserved", ctypes.c_int32), ("slot_base", ctypes.c_int64),
                 ("tokens", ctypes.POINTER(ctypes.c_int32))]
 
 
@@ -66,7 +67,8 @@ EXPORTS = ("orca_kv_pool_bytes", "orca_workspace_bytes", "orca_weight_count", "o
            "orca_engine_destroy", "orca_kv_reserve", "orca_kv_release", "orca_kv_stats", "orca_select_batch",
            "orca_iteration", "orca_last_descriptor", "orca_argmax_rows", "orca_profile_enable",
            "orca_profile_read", "orca_last_error", "orca_linear", "orca_last_transfer",
-           "orca_attention_workspace_bytes", "orca_attention", "orca_attention_noalloc")
+           "orca_attention_workspace_bytes", "orca_attention", "orca_attention_noalloc", "orca_last_launches",
+           "orca_select_batch_budget")
 
 _lib = None
 
@@ -93,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "orca_kv_release": [P, c_i64],
             "orca_kv_stats": [P, i64p, i64p, i64p],
             "orca_select_batch": [P, reqp, c_i32, i32p, i32p],
+            "orca_select_batch_budget": [P, reqp, c_i32, c_i32, c_i32, i32p, i32p],
             "orca_iteration": [P, reqp, i32p, c_i32, c_i32, i32p, P, P],
             "orca_last_descriptor": [P, i32p, i32p, i32p, i32p, i32p, i32p, c_i32],
             "orca_argmax_rows": [P, c_i32, c_i32, P, P],
@@ -182,6 +185,12 @@ def orca_select_batch(eng, pool, n_pool: int, batch_idx) -> int:
     nb = ctypes.c_int32()
     _check(lib().orca_select_batch(eng, pool, n_pool, batch_idx, ctypes.byref(nb)), eng)
     return nb.value
+
+
+def orca_select_batch_budget(eng, pool, n_pool: int, token_budget: int, chunk: int, batch_idx) -> int:
+    n = ctypes.c_int32()
+    _check(lib().orca_select_batch_budget(eng, pool, n_pool, token_budget, chunk, batch_idx, ctypes.byref(n)), eng)
+    return n.value
 
 
 def orca_iteration(eng, pool, batch_idx, n_batch: int, flags: int, next_tokens, logits_ptr=0, stream=0) -> None:

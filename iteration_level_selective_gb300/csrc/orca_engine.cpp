@@ -485,7 +485,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     aa.hdr = graph ? d_hdr : nullptr;
     prof_begin(e, st, &ev);
-    if (e->attn_tc) {  // prompts: tensor-core tiles; then decodes and short prompts
+    if (e->attn_tc && z.n_work_tc > 0) {  // prompts: tensor-core tiles; then decodes and short prompts
       TcAttnArgs ta{};
       ta.out = h;
       ta.reqs = d_req;
@@ -499,7 +499,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
       ta.n_slots = c.n_slots;
       ta.scale_log2 = aa.scale_log2;
       CUDA_TRY(e, launch_attention_tc(D, &e->tm_q, &e->tm_k[l], &e->tm_v[l], ta, z.n_work_tc, st));
-      if (graph || z.n_work_tc > 0) ++e->n_launch;
+      ++e->n_launch;
     }
     LAUNCH(e, launch_attention(c.dtype, D, aa, graph ? Ly.max_work : z.n_work, st));
     prof_end(e, st, ev, ORCA_K_ATTENTION, attn_flops, attn_bytes);
@@ -745,9 +745,18 @@ int orca_kv_stats(const orca_engine *e, int64_t *n_rsrv, int64_t *n_free_blocks,
   return ORCA_OK;
 }
 
-int orca_select_batch(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t *batch_idx, int32_t *n_batch) {
-  if (!e || !n_batch || (n_pool > 0 && (!pool || !batch_idx)) || n_pool < 0) return ORCA_EINVAL;
-  *n_batch = 0;
+namespace {
+
+// Rows a selected request contributes when nothing narrower was scheduled:
+// the rest of its prompt, or one row once the prompt is processed.
+int32_t default_rows(const orca_request &r) { return r.n_cached < r.n_prompt ? r.n_prompt - r.n_cached : 1; }
+
+// Algorithm 1 Select (Orca walk-through, Algorithm 1): candidates are the
+// non-RUNNING, unfinished requests in (arrival, req_id) order; at most max_bs;
+// an INITIATION request first reserves max_tokens slots and a failed
+// reservation ends the selection.  Fills batch_idx; states are not changed.
+int select_fcfs(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t *batch_idx, int32_t *nb_out) {
+  *nb_out = 0;
   std::vector<int32_t> cand;
   cand.reserve(n_pool);
   for (int32_t i = 0; i < n_pool; ++i) {
@@ -769,15 +778,71 @@ int orca_select_batch(orca_engine *e, orca_request *pool, int32_t n_pool, int32_
         return fail(e, ORCA_EINVAL, "request %lld: need 0 < n_prompt <= max_tokens and out_len > 0",
                     (long long)r.req_id);
       int64_t base = -1;
-      const int rc = e->slots.reserve(r.req_id, r.max_tokens, &base);
+      const int32_t want = r.max_tokens;
+      const int rc = e->slots.reserve(r.req_id, want, &base);
       if (rc == ORCA_ENOSLOTS) break;  // Algorithm 1: stop selecting, never skip
       if (rc) return fail(e, rc, "request %lld already holds a reservation", (long long)r.req_id);
       r.slot_base = base;
+      r.n_reserved = want;
+      r.state = ORCA_INCREMENT;  // admitted: holds its slots from now on
     }
     batch_idx[nb++] = idx;
   }
-  for (int32_t i = 0; i < nb; ++i) pool[batch_idx[i]].state = ORCA_RUNNING;
+  *nb_out = nb;
+  return ORCA_OK;
+}
+
+}  // namespace
+
+int orca_select_batch(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t *batch_idx, int32_t *n_batch) {
+  if (!e || !n_batch || (n_pool > 0 && (!pool || !batch_idx)) || n_pool < 0) return ORCA_EINVAL;
+  *n_batch = 0;
+  int32_t nb = 0;
+  const int rc = select_fcfs(e, pool, n_pool, batch_idx, &nb);
+  if (rc) return rc;
+  for (int32_t i = 0; i < nb; ++i) {
+    orca_request &r = pool[batch_idx[i]];
+    r.n_sched = default_rows(r);
+    r.state = ORCA_RUNNING;
+  }
   *n_batch = nb;
+  return ORCA_OK;
+}
+
+int orca_select_batch_budget(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t token_budget,
+                             int32_t chunk, int32_t *batch_idx, int32_t *n_batch) {
+  if (!e || !n_batch || (n_pool > 0 && (!pool || !batch_idx)) || n_pool < 0) return ORCA_EINVAL;
+  *n_batch = 0;
+  if (token_budget < 1 || chunk < 1) return fail(e, ORCA_EINVAL, "token_budget and chunk must be >= 1");
+  int32_t nb = 0;
+  const int rc = select_fcfs(e, pool, n_pool, batch_idx, &nb);
+  if (rc) return rc;
+  int64_t left = token_budget;
+  std::vector<int32_t> rows(nb, 0);
+  for (int32_t i = 0; i < nb; ++i) {  // decodes first: one row each
+    const orca_request &r = pool[batch_idx[i]];
+    if (r.n_cached >= r.n_prompt && left >= 1) {
+      rows[i] = 1;
+      left -= 1;
+    }
+  }
+  for (int32_t i = 0; i < nb; ++i) {  // then prompt chunks, in batch order
+    const orca_request &r = pool[batch_idx[i]];
+    if (r.n_cached < r.n_prompt) {
+      const int64_t n = std::min<int64_t>(std::min<int64_t>(r.n_prompt - r.n_cached, chunk), left);
+      rows[i] = (int32_t)n;
+      left -= n;
+    }
+  }
+  int32_t out = 0;
+  for (int32_t i = 0; i < nb; ++i) {
+    orca_request &r = pool[batch_idx[i]];
+    if (rows[i] == 0) continue;  // admitted or waiting, but no row this iteration (state stays INCREMENT)
+    r.n_sched = rows[i];
+    r.state = ORCA_RUNNING;
+    batch_idx[out++] = batch_idx[i];
+  }
+  *n_batch = out;
   return ORCA_OK;
 }
 
@@ -802,12 +867,17 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
     const orca_request &r = pool[batch_idx[i]];
     if (r.state != ORCA_RUNNING) return fail(e, ORCA_EINVAL, "request %lld is not RUNNING", (long long)r.req_id);
     if (!r.tokens || r.slot_base < 0) return fail(e, ORCA_EINVAL, "request %lld has no tokens or slots", (long long)r.req_id);
-    L[i] = r.n_cached < r.n_prompt ? r.n_prompt - r.n_cached : 1;
+    if (r.n_cached < 0) return fail(e, ORCA_EINVAL, "request %lld: negative n_cached", (long long)r.req_id);
+    const int32_t dflt = default_rows(r);
+    if (r.n_sched < 0 || r.n_sched > dflt)
+      return fail(e, ORCA_EINVAL, "request %lld: n_sched %d outside 0..%d", (long long)r.req_id, r.n_sched, dflt);
+    L[i] = r.n_sched > 0 ? r.n_sched : dflt;
+    const int64_t cap = r.n_reserved > 0 ? r.n_reserved : r.max_tokens;  // slots the request holds
     const int64_t end = (int64_t)r.n_cached + L[i];
-    if (end > r.max_tokens || end > c.max_pos || end > (int64_t)r.n_prompt + r.out_len || r.n_cached < 0)
-      return fail(e, ORCA_EINVAL, "request %lld: position %lld beyond max_tokens, max_pos or its buffer",
+    if (end > cap || end > r.max_tokens || end > c.max_pos || end > (int64_t)r.n_prompt + r.out_len)
+      return fail(e, ORCA_EINVAL, "request %lld: position %lld beyond its slots, max_pos or its buffer",
                   (long long)r.req_id, (long long)end);
-    if (r.slot_base + r.max_tokens > c.n_slots)
+    if (r.slot_base + cap > c.n_slots)
       return fail(e, ORCA_EINVAL, "request %lld: slots beyond n_slots", (long long)r.req_id);
     N += L[i];
     if (N > c.max_rows) return fail(e, ORCA_EBATCH, "sum L_i > max_rows %d", c.max_rows);
@@ -886,8 +956,11 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
   const bool use_graph = bf16 && !e->prof && !(flags & ORCA_ITER_EAGER);
   if (use_graph) {
     auto code = [](int bn) { return (uint32_t)(bn == 256 ? 3 : bn == 128 ? 2 : bn == 64 ? 1 : 0); };
+    // graphs differ in their GEMM tile choices and in whether the tensor-core
+    // prompt attention runs at all
     const uint32_t key = code(gemm_tile_n(N, 3 * H)) | (code(gemm_tile_n(N, H)) << 2) |
-                         (code(gemm_tile_n(N, F)) << 4) | (code(gemm_tile_n(n_batch, V)) << 6);
+                         (code(gemm_tile_n(N, F)) << 4) | (code(gemm_tile_n(n_batch, V)) << 6) |
+                         ((uint32_t)(n_work_tc > 0) << 8);
     const auto gk = std::make_pair(key, reinterpret_cast<uintptr_t>(logits));
     auto it = e->graphs.find(gk);
     if (it == e->graphs.end()) {
@@ -942,9 +1015,14 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
   for (int32_t i = 0; i < n_batch; ++i) {
     orca_request &r = pool[batch_idx[i]];
     const int32_t tok = argmax_key_col(e->h_out[1 + i]);
-    next_tokens[i] = tok;
     r.state = ORCA_INCREMENT;
+    r.n_sched = 0;
     r.n_cached += L[i];
+    if (r.n_cached < r.n_prompt) {  // a prompt chunk: the prompt is not complete yet, nothing generated
+      next_tokens[i] = -1;
+      continue;
+    }
+    next_tokens[i] = tok;
     r.n_generated += 1;
     if (!(flags & ORCA_ITER_TEACHER_FORCE)) r.tokens[r.n_prompt + r.n_generated - 1] = tok;
     if (r.n_generated >= r.out_len || r.n_prompt + r.n_generated >= r.max_tokens) {

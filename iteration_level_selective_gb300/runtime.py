@@ -114,7 +114,7 @@ class Engine:
 # numpy view of orca_request (same layout as the C struct)
 REQUEST_DTYPE = np.dtype([("req_id", "<i8"), ("arrival", "<i8"), ("state", "<i4"), ("n_prompt", "<i4"),
                           ("max_tokens", "<i4"), ("out_len", "<i4"), ("n_cached", "<i4"), ("n_generated", "<i4"),
-                          ("slot_base", "<i8"), ("tokens", "<u8")])
+                          ("n_sched", "<i4"), ("n_reserved", "<i4"), ("slot_base", "<i8"), ("tokens", "<u8")])
 assert REQUEST_DTYPE.itemsize == ctypes.sizeof(C.orca_request)
 
 
@@ -146,6 +146,7 @@ class RequestPool:
         for i, r in enumerate(self.reqs):
             a = self.arr[i]
             a.state, a.n_cached, a.n_generated, a.slot_base = C.ORCA_INITIATION, 0, 0, -1
+            a.n_sched, a.n_reserved = 0, 0
 
 
 @dataclasses.dataclass
@@ -169,7 +170,8 @@ class ServingLoop:
     next arrival.  step() runs one iteration and returns its record."""
 
     def __init__(self, engine: Engine, pool: RequestPool, teacher_force: bool = False, keep_logits: bool = False,
-                 stream: Optional[torch.cuda.Stream] = None, keep_ids: Optional[set] = None, eager: bool = False):
+                 stream: Optional[torch.cuda.Stream] = None, keep_ids: Optional[set] = None, eager: bool = False,
+                 token_budget: Optional[int] = None, chunk: Optional[int] = None):
         self.eng, self.pool = engine, pool
         self.flags = (C.ORCA_ITER_TEACHER_FORCE if teacher_force else 0) | (C.ORCA_ITER_EAGER if eager else 0)
         keep_logits = keep_logits or keep_ids is not None
@@ -182,6 +184,11 @@ class ServingLoop:
         self._nt = np.frombuffer(self.next_tok, dtype=np.int32)
         self.logits = (torch.empty((engine.max_bs, engine.shape.vocab), dtype=torch.float32, device=engine.device)
                        if keep_logits else None)
+        # chunked prefill under a per-iteration token budget (None: plain Algorithm 1)
+        self.budget = None
+        if token_budget is not None or chunk is not None:
+            big = 2 ** 31 - 1
+            self.budget = (token_budget or big, chunk or big)
         self.it = 0
         self.n_arrived = 0
         self.n_done = 0
@@ -199,13 +206,16 @@ class ServingLoop:
             self.it = int(P.arrivals[self.n_arrived])
         if self.n_arrived < P.n and P.arrivals[self.n_arrived] <= self.it:
             self.n_arrived = int(np.searchsorted(P.arrivals, self.it, side="right"))
-        nb = C.orca_select_batch(self.eng.handle, P.arr, self.n_arrived, self.batch_idx)
+        if self.budget is None:
+            nb = C.orca_select_batch(self.eng.handle, P.arr, self.n_arrived, self.batch_idx)
+        else:
+            nb = C.orca_select_batch_budget(self.eng.handle, P.arr, self.n_arrived, self.budget[0], self.budget[1],
+                                            self.batch_idx)
         if nb == 0:
             raise RuntimeError(f"no request can be scheduled at iteration {self.it}")
         idx = self._bi[:nb].copy()
         sel = P.view[idx]
-        n_new = np.where(sel["n_cached"] < sel["n_prompt"], sel["n_prompt"] - sel["n_cached"], 1)
-        rec = IterRecord(self.it, sel["req_id"].tolist(), n_new.tolist(), sel["n_cached"].tolist(),
+        rec = IterRecord(self.it, sel["req_id"].tolist(), sel["n_sched"].tolist(), sel["n_cached"].tolist(),
                          sel["slot_base"].tolist(), [], [])
         lp = self.logits.data_ptr() if self.logits is not None else 0
         t1 = time.perf_counter()

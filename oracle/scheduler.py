@@ -101,6 +101,42 @@ def select(pool: List[ReqState], slots: SlotPool, max_bs: int) -> List[ReqState]
     return batch
 
 
+def default_rows(r: ReqState) -> int:
+    """Rows of a selected request in plain Algorithm 1: the rest of its
+    prompt (all of it at first schedule), else one decode row."""
+    return r.n_prompt - r.n_cached if r.n_cached < r.n_prompt else 1
+
+
+def select_budget(pool: List[ReqState], slots: SlotPool, max_bs: int, token_budget: int,
+                  chunk: int) -> List[Tuple[ReqState, int]]:
+    """Chunked prefill under a per-iteration token budget, on top of
+    Algorithm 1.
+
+    CS349D Lecture 2, Exercise 9: cut long prompts into chunks, mix chunks
+    into the iterations and cap the tokens of one iteration; the engine then
+    runs SeqWork(n_new = chunk, n_past = prompt tokens already processed).
+    Static-to-continuous article, chunked prefill: decode first, the rest of
+    the budget goes to prompt chunks.  Reading: Algorithm 1 Select is kept
+    as it is (FCFS, max_bs, reservation at first schedule, break); over the
+    selected requests, in batch order, every decoding request takes one row
+    while the budget lasts, then every prompting request takes
+    min(remaining prompt, chunk, budget left) rows.  Returns (request, rows)
+    in batch order; rows may be 0 (admitted but idle this iteration)."""
+    batch = select(pool, slots, max_bs)
+    left = token_budget
+    rows: Dict[int, int] = {}
+    for r in batch:
+        if r.n_cached >= r.n_prompt and left >= 1:
+            rows[r.req_id] = 1
+            left -= 1
+    for r in batch:
+        if r.n_cached < r.n_prompt:
+            n = min(r.n_prompt - r.n_cached, chunk, left)
+            rows[r.req_id] = n
+            left -= n
+    return [(r, rows.get(r.req_id, 0)) for r in batch]
+
+
 def finished(r: ReqState) -> bool:
     return r.n_generated >= r.out_len or r.n_prompt + r.n_generated >= r.max_tokens
 
@@ -115,13 +151,16 @@ class IterRecord:
     released: List[int]
 
 
-def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000) -> List[IterRecord]:
+def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
+                 token_budget: Optional[int] = None, chunk: Optional[int] = None) -> List[IterRecord]:
     """Drive Algorithm 1 over a trace whose arrivals are iteration indices.
 
     A request whose arrival is t can be selected at iteration t.  When no
     request is in the pool the clock jumps to the next arrival (no iteration
     is run).  Raises RuntimeError if the pool is non-empty but nothing can
-    ever be selected (a head request larger than n_slots)."""
+    ever be selected (a head request larger than n_slots).  With a token
+    budget or a chunk size the batch comes from select_budget: a prompt
+    chunk that leaves part of the prompt unprocessed generates no token."""
     order = sorted(trace, key=lambda r: (r.arrival, r.req_id))
     states = [ReqState(r.req_id, r.arrival, r.n_prompt, r.out_len, r.max_tokens) for r in order]
     slots = SlotPool(n_slots)
@@ -129,23 +168,33 @@ def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000) 
     nxt = 0
     it = 0
     records: List[IterRecord] = []
+    budgeted = token_budget is not None or chunk is not None
+    big = 2 ** 31 - 1
     while nxt < len(states) or pool:
         if not pool and states[nxt].arrival > it:
             it = states[nxt].arrival
         while nxt < len(states) and states[nxt].arrival <= it:
             pool.append(states[nxt])
             nxt += 1
-        batch = select(pool, slots, max_bs)
-        if not batch:
+        if budgeted:
+            sel = select_budget(pool, slots, max_bs, token_budget or big, chunk or big)
+        else:
+            sel = [(r, default_rows(r)) for r in select(pool, slots, max_bs)]
+        run = [(r, n) for r, n in sel if n > 0]
+        if not run:
             raise RuntimeError(f"no request can be scheduled at iteration {it}")
-        rec = IterRecord(it, [r.req_id for r in batch],
-                         [r.n_prompt if r.state == INITIATION else 1 for r in batch],
-                         [r.n_cached for r in batch], [r.slot_base for r in batch], [])
-        for r in batch:
+        for r, n in sel:
+            if n == 0:
+                r.state = INCREMENT  # admitted (slots reserved) but idle this iteration
+        rec = IterRecord(it, [r.req_id for r, _ in run], [n for _, n in run], [r.n_cached for r, _ in run],
+                         [r.slot_base for r, _ in run], [])
+        for r, _ in run:
             r.state = RUNNING
-        for r, n_new in zip(batch, rec.n_new):
+        for r, n in run:
             r.state = INCREMENT
-            r.n_cached += n_new
+            r.n_cached += n
+            if r.n_cached < r.n_prompt:
+                continue  # a prompt chunk: nothing generated yet
             r.n_generated += 1
             if finished(r):
                 r.state = FINISHED

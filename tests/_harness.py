@@ -15,7 +15,7 @@ def max_rel_err(got, want):
 
 
 def run_gpu(shape, host_weights, trace, max_bs, n_slots, max_rows, teacher_force=False, keep_ids=None,
-            keep_all=False, eager=False):
+            keep_all=False, eager=False, token_budget=None, chunk=None):
     import torch
     from iteration_level_selective_gb300 import runtime as rt
     dev = torch.device("cuda:0")
@@ -23,14 +23,14 @@ def run_gpu(shape, host_weights, trace, max_bs, n_slots, max_rows, teacher_force
     eng = rt.Engine(shape, w, max_bs=max_bs, n_slots=n_slots, max_rows=max_rows, device=dev)
     pool = rt.RequestPool(trace, teacher_force=teacher_force)
     loop = rt.ServingLoop(eng, pool, teacher_force=teacher_force, keep_logits=keep_all, keep_ids=keep_ids,
-                          eager=eager)
+                          eager=eager, token_budget=token_budget, chunk=chunk)
     recs = loop.run()
     return recs, eng, pool
 
 
-def compare_schedule(gpu_recs, trace, max_bs, n_slots):
+def compare_schedule(gpu_recs, trace, max_bs, n_slots, token_budget=None, chunk=None):
     """Integer record of every iteration, bit-exact against the oracle scheduler."""
-    orecs = osched.run_schedule(trace, max_bs=max_bs, n_slots=n_slots)
+    orecs = osched.run_schedule(trace, max_bs=max_bs, n_slots=n_slots, token_budget=token_budget, chunk=chunk)
     assert len(gpu_recs) == len(orecs)
     for g, o in zip(gpu_recs, orecs):
         assert (g.it, g.req_ids, g.n_new, g.n_ctx, g.slot_base, sorted(g.released)) == \
@@ -39,17 +39,22 @@ def compare_schedule(gpu_recs, trace, max_bs, n_slots):
 
 
 def gpu_logits_by_request(recs):
-    """request id -> list of logits rows in generation order."""
+    """request id -> list of logits rows in generation order (iterations
+    that ran a prompt chunk without completing the prompt generate nothing
+    and are skipped)."""
     out = {}
     for rec in recs:
         if rec.logits is None:
             continue
+        emitted = {rid for rid, t in zip(rec.req_ids, rec.next_tokens) if t >= 0}
         if isinstance(rec.logits, dict):
             for rid, row in rec.logits.items():
-                out.setdefault(rid, []).append(row)
+                if rid in emitted:
+                    out.setdefault(rid, []).append(row)
         else:
             for k, rid in enumerate(rec.req_ids):
-                out.setdefault(rid, []).append(rec.logits[k])
+                if rid in emitted:
+                    out.setdefault(rid, []).append(rec.logits[k])
     return out
 
 
@@ -57,7 +62,8 @@ def gpu_tokens_by_request(recs):
     out = {}
     for rec in recs:
         for rid, t in zip(rec.req_ids, rec.next_tokens):
-            out.setdefault(rid, []).append(t)
+            if t >= 0:
+                out.setdefault(rid, []).append(t)
     return out
 
 

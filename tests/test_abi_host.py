@@ -85,7 +85,8 @@ class _Sim:
     """Drives the C Select and the oracle Select side by side; the test
     applies the same post-iteration update to both."""
 
-    def __init__(self, trace, max_bs, n_slots):
+    def __init__(self, trace, max_bs, n_slots, budget=None):
+        self.budget = budget  # (token_budget, chunk) for the chunked-prefill Select, or None
         self.trace = sorted(trace, key=lambda t: (t[1], t[0]))
         self.eng = C.orca_engine_create(_cfg(max_bs=max_bs, n_slots=n_slots))
         self.max_bs = max_bs
@@ -110,28 +111,46 @@ class _Sim:
                 it = self.trace[n_arr][1]
             while n_arr < n and self.trace[n_arr][1] <= it:
                 n_arr += 1
-            nb = C.orca_select_batch(self.eng, self.arr, n_arr, self.bi)
             opool = [s for s in self.ostates[:n_arr] if s.state != osched.FINISHED]
-            obatch = osched.select(opool, self.oslots, self.max_bs)
-            got = [(self.arr[self.bi[i]].req_id, self.arr[self.bi[i]].slot_base) for i in range(nb)]
-            want = [(r.req_id, r.slot_base) for r in obatch]
+            if self.budget is None:
+                nb = C.orca_select_batch(self.eng, self.arr, n_arr, self.bi)
+                osel = [(r, osched.default_rows(r)) for r in osched.select(opool, self.oslots, self.max_bs)]
+            else:
+                nb = C.orca_select_batch_budget(self.eng, self.arr, n_arr, self.budget[0], self.budget[1], self.bi)
+                osel = osched.select_budget(opool, self.oslots, self.max_bs, *self.budget)
+            orun = [(r, k) for r, k in osel if k > 0]
+            got = [(self.arr[self.bi[i]].req_id, self.arr[self.bi[i]].slot_base, self.arr[self.bi[i]].n_sched)
+                   for i in range(nb)]
+            want = [(r.req_id, r.slot_base, k) for r, k in orun]
             assert got == want, (it, got, want)
             assert C.orca_kv_stats(self.eng)[0] == self.oslots.n_rsrv
             for i in range(nb):
                 a = self.arr[self.bi[i]]
                 assert a.state == C.ORCA_RUNNING
-                L = a.n_prompt - a.n_cached if a.n_cached < a.n_prompt else 1
-                a.state, a.n_cached, a.n_generated = C.ORCA_INCREMENT, a.n_cached + L, a.n_generated + 1
+                L = a.n_sched
+                a.state, a.n_sched, a.n_cached = C.ORCA_INCREMENT, 0, a.n_cached + L
+                if a.n_cached < a.n_prompt:
+                    continue
+                a.n_generated += 1
                 if a.n_generated >= a.out_len or a.n_prompt + a.n_generated >= a.max_tokens:
                     a.state = C.ORCA_FINISHED
                     C.orca_kv_release(self.eng, a.req_id)
                     done += 1
-            for r in obatch:
-                L = r.n_prompt if r.state == osched.INITIATION else 1
-                r.state, r.n_cached, r.n_generated = osched.INCREMENT, r.n_cached + L, r.n_generated + 1
+            for r, k in osel:
+                r.state = osched.INCREMENT
+                if k == 0:
+                    continue
+                r.n_cached += k
+                if r.n_cached < r.n_prompt:
+                    continue
+                r.n_generated += 1
                 if osched.finished(r):
                     r.state = osched.FINISHED
                     self.oslots.release(r.req_id)
+            # requests admitted without a row wait in INCREMENT on both sides
+            for j in range(n_arr):
+                if self.arr[j].state == C.ORCA_INCREMENT:
+                    assert self.ostates[j].state == osched.INCREMENT
             it += 1
         C.orca_engine_destroy(self.eng)
         return it
@@ -148,6 +167,32 @@ def test_select_bit_exact_vs_oracle_random_traces(liborca):
                           lp + lo + int(rng.integers(0, 8))))
         max_t = max(t[4] for t in trace)
         _Sim(trace, max_bs=int(rng.integers(1, 12)), n_slots=int(rng.integers(max_t, 4 * max_t))).run()
+
+
+def test_budget_select_bit_exact_vs_oracle_random_traces(liborca):
+    rng = np.random.default_rng(22)
+    for trial in range(40):
+        n = int(rng.integers(3, 40))
+        trace = []
+        for i in range(n):
+            lp, lo = int(rng.integers(1, 40)), int(rng.integers(1, 12))
+            trace.append((i, int(rng.integers(0, 30)), lp, lo, lp + lo + int(rng.integers(0, 8))))
+        max_t = max(t[4] for t in trace)
+        budget = (int(rng.integers(1, 48)), int(rng.integers(1, 32)))
+        _Sim(trace, max_bs=int(rng.integers(1, 12)), n_slots=int(rng.integers(max_t, 4 * max_t)), budget=budget).run()
+
+
+def test_budget_select_rejects_bad_budget(liborca):
+    eng = C.orca_engine_create(_cfg(max_bs=4, n_slots=100))
+    try:
+        pool = (C.orca_request * 1)()
+        bi = (ctypes.c_int32 * 4)()
+        for tb, ch in ((0, 4), (4, 0), (-1, 4)):
+            with pytest.raises(C.OrcaError) as ei:
+                C.orca_select_batch_budget(eng, pool, 0, tb, ch, bi)
+            assert ei.value.code == C.ORCA_EINVAL
+    finally:
+        C.orca_engine_destroy(eng)
 
 
 def test_select_break_no_skip_via_abi(liborca):

@@ -336,3 +336,99 @@ def test_fcfs_invariant_and_reservation_bound_random_traces():
                     if arrival[a] < arrival[b]:
                         assert iters[a] >= iters[b], (trial, rec.it, a, b)
         assert all(iters[t.req_id] == t.out_len for t in trace)
+
+
+# ---------------------------------------------------------------- chunked prefill under a token budget
+# CS349D Lecture 2, Exercise 9 (prompt chunks, SeqWork(n_new, n_past), a cap
+# on the tokens of one iteration); static-to-continuous article, chunked
+# prefill (decode first, the rest of the budget to prompt chunks).
+
+def _records(recs):
+    return [(r.it, r.req_ids, r.n_new, r.n_ctx, sorted(r.released)) for r in recs]
+
+
+def test_budget_worked_example_by_hand():
+    # A: prompt 5, B: prompt 3, both arrive at 0, 2 tokens each; budget 4,
+    # chunk 3.
+    #   it 0: no decodes; A takes min(5, 3, 4) = 3, B min(3, 3, 1) = 1
+    #   it 1: no decodes; A takes min(2, 3, 4) = 2 (prompt done -> token 1),
+    #         B min(2, 3, 2) = 2 (prompt done -> token 1)
+    #   it 2: A and B decode one row each -> second token, both finish
+    trace = [_R(0, 0, 5, 2, 7), _R(1, 0, 3, 2, 5)]
+    recs = scheduler.run_schedule(trace, max_bs=4, n_slots=100, token_budget=4, chunk=3)
+    assert _records(recs) == [(0, [0, 1], [3, 1], [0, 0], []),
+                              (1, [0, 1], [2, 2], [3, 1], []),
+                              (2, [0, 1], [1, 1], [5, 3], [0, 1])]
+
+
+def test_budget_decodes_go_first():
+    # A (prompt 2, 3 tokens) decodes from iteration 1; B (prompt 6) arrives
+    # at 1.  Budget 3: each iteration A's decode row is served first and B
+    # gets the 2 rows left (it 1: 2, it 2: 2); A finishes after it 2, so at
+    # it 3 B takes its last 2 prompt rows alone.
+    trace = [_R(0, 0, 2, 3, 5), _R(1, 1, 6, 1, 7)]
+    recs = scheduler.run_schedule(trace, max_bs=4, n_slots=100, token_budget=3, chunk=8)
+    assert _records(recs) == [(0, [0], [2], [0], []),
+                              (1, [0, 1], [1, 2], [2, 0], []),
+                              (2, [0, 1], [1, 2], [3, 2], [0]),
+                              (3, [1], [2], [4], [1])]
+
+
+def test_budget_admitted_request_keeps_reservation_while_idle():
+    # budget 2 with two new prompts of 4: B is admitted (slots reserved by
+    # Algorithm 1) but gets no row until A's prompt is done
+    trace = [_R(0, 0, 4, 1, 5), _R(1, 0, 4, 1, 5)]
+    order = sorted(trace, key=lambda r: (r.arrival, r.req_id))
+    states = [scheduler.ReqState(r.req_id, r.arrival, r.n_prompt, r.out_len, r.max_tokens) for r in order]
+    slots = scheduler.SlotPool(10)
+    sel = scheduler.select_budget(states, slots, max_bs=4, token_budget=2, chunk=8)
+    assert [(r.req_id, n) for r, n in sel] == [(0, 2), (1, 0)]
+    assert slots.n_rsrv == 10 and states[1].slot_base == 5
+    recs = scheduler.run_schedule(trace, max_bs=4, n_slots=10, token_budget=2, chunk=8)
+    assert _records(recs) == [(0, [0], [2], [0], []), (1, [0], [2], [2], [0]),
+                              (2, [1], [2], [0], []), (3, [1], [2], [2], [1])]
+
+
+def test_unlimited_budget_is_algorithm_1():
+    rng = np.random.default_rng(41)
+    for trial in range(20):
+        n = int(rng.integers(3, 30))
+        trace = []
+        for i in range(n):
+            lp, lo = int(rng.integers(1, 12)), int(rng.integers(1, 10))
+            trace.append(_R(i, int(rng.integers(0, 20)), lp, lo, lp + lo + int(rng.integers(0, 4))))
+        kw = dict(max_bs=int(rng.integers(1, 9)), n_slots=int(rng.integers(30, 120)))
+        plain = scheduler.run_schedule(trace, **kw)
+        big = scheduler.run_schedule(trace, token_budget=2 ** 31 - 1, chunk=2 ** 31 - 1, **kw)
+        assert _records(plain) == _records(big)
+        assert [r.slot_base for r in plain] == [r.slot_base for r in big]
+
+
+def test_budget_invariants_random_traces():
+    rng = np.random.default_rng(42)
+    for trial in range(30):
+        n = int(rng.integers(3, 30))
+        budget, chunk = int(rng.integers(1, 24)), int(rng.integers(1, 16))
+        trace = []
+        for i in range(n):
+            lp, lo = int(rng.integers(1, 30)), int(rng.integers(1, 10))
+            trace.append(_R(i, int(rng.integers(0, 20)), lp, lo, lp + lo + int(rng.integers(0, 4))))
+        recs = scheduler.run_schedule(trace, max_bs=int(rng.integers(1, 9)), n_slots=400, token_budget=budget,
+                                      chunk=chunk)
+        n_prompt = {t.req_id: t.n_prompt for t in trace}
+        done_prompt = {t.req_id: 0 for t in trace}
+        generated = {t.req_id: 0 for t in trace}
+        for rec in recs:
+            assert 1 <= sum(rec.n_new) <= budget
+            decoding = [c >= n_prompt[r] for r, c in zip(rec.req_ids, rec.n_ctx)]
+            for rid, L, c, dec in zip(rec.req_ids, rec.n_new, rec.n_ctx, decoding):
+                assert c == (done_prompt[rid] if not dec else n_prompt[rid] + generated[rid] - 1)
+                if dec:
+                    assert L == 1
+                else:
+                    assert 1 <= L <= min(chunk, n_prompt[rid] - c)
+                    done_prompt[rid] += L
+                if c + L >= n_prompt[rid]:
+                    generated[rid] += 1
+        assert done_prompt == n_prompt
+        assert all(generated[t.req_id] == t.out_len for t in trace)
