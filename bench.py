@@ -318,7 +318,8 @@ def run_ours(args, rank: int, world: int):
         weights = rt.DeviceWeights(shape, dev, host=host_w)
         del host_w
         n_slots = args.kv_slots if args.kv_slots else n_slots_for(shape)
-        eng = rt.Engine(shape, weights, max_bs=64, n_slots=n_slots, max_rows=64 * 512, device=dev)
+        eng = rt.Engine(shape, weights, max_bs=64, n_slots=n_slots, max_rows=64 * 512, device=dev,
+                        reserve_policy=rt.RESERVE_POLICIES[args.reserve])
         work = TraceWorkload(eng, rank, stream, args.token_budget, args.chunk)
         workload = WORKLOAD
         if args.token_budget or args.chunk:
@@ -329,6 +330,9 @@ def run_ours(args, rank: int, world: int):
         if args.token_budget or args.chunk:
             cfg_extra["token_budget"] = args.token_budget or None
             cfg_extra["chunk"] = args.chunk or None
+        if args.reserve != "max":
+            cfg_extra["reserve_policy"] = args.reserve
+            workload += f", {args.reserve} K/V reservation"
     else:
         shape, prompts, ctx, workload = fixed_batch_spec(args.config)
         n_slots = FixedBatchWorkload.slots_needed(prompts, ctx)
@@ -352,6 +356,10 @@ def run_ours(args, rank: int, world: int):
         h2d, d2h, _ = C.orca_last_transfer(eng.handle)
         return rec, h2d, d2h
 
+    def kv_usage():
+        pool = work.loop.pool if hasattr(work, "loop") else work.pool
+        return C.orca_kv_usage(eng.handle, pool.arr, pool.n)
+
     warmup = max(3, args.warmup)
     for _ in range(warmup):
         step()
@@ -361,7 +369,7 @@ def run_ours(args, rank: int, world: int):
     sampler = ClockSampler(local)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     rows = gen_tok = done = h2d = d2h = launches = 0
-    step_ms = []
+    step_ms, usage = [], []
     torch.cuda.synchronize(dev)
     w0 = time.perf_counter()
     ev0.record(stream)
@@ -369,6 +377,7 @@ def run_ours(args, rank: int, world: int):
         t0 = time.perf_counter()
         rec, hb, db = step()
         step_ms.append(1000.0 * (time.perf_counter() - t0))
+        usage.append(kv_usage())
         rows += sum(rec.n_new)
         gen_tok += sum(1 for t in rec.next_tokens if t >= 0)
         done += len(rec.released)
@@ -443,6 +452,12 @@ def run_ours(args, rank: int, world: int):
         "e2e": {"value": rows / wall, "unit": UNIT, "h2d_bytes_per_step": h2d / steps / max(1, world),
                 "d2h_bytes_per_step": d2h / steps / max(1, world)},
         "gpu_launches": launches,
+        "kv_usage": {"reserved_frac": round(float(np.mean([u[0] for u in usage])) / n_slots, 5),
+                     "stored_frac": round(float(np.mean([u[1] for u in usage])) / n_slots, 5),
+                     "stored_over_reserved": round(float(np.sum([u[1] for u in usage]) /
+                                                         max(1, np.sum([u[0] for u in usage]))), 4),
+                     "weighting": "per iteration, after each timed iteration"},
+        "generated_per_iteration": round(gen_tok / steps / max(1, world), 2),
         "iteration_ms": {"p50": round(float(np.percentile(step_ms, 50)), 4),
                          "p99": round(float(np.percentile(step_ms, 99)), 4), "max": round(max(step_ms), 4),
                          "clock": "host wall clock per iteration (the call waits for the tokens)"},
@@ -481,6 +496,8 @@ def main():
                     help="gpt2-trace only: chunked prefill with this many rows per iteration at most")
     ap.add_argument("--chunk", type=int, default=0,
                     help="gpt2-trace only: prompt chunk size for chunked prefill")
+    ap.add_argument("--reserve", choices=["max", "pow2", "oracle"], default="max",
+                    help="gpt2-trace only: K/V reservation policy (max_tokens, power of two, true length)")
     ap.add_argument("--kv-slots", type=int, default=0,
                     help="gpt2-trace only: K/V pool slots (default: 40 GB worth); the trace needs at most "
                          "64 x 768, so profiler captures use a small pool")

@@ -64,6 +64,10 @@ extern "C" {
 /* ---------------------------------------------------------------- types */
 typedef struct orca_engine orca_engine;
 
+#define ORCA_RESERVE_MAX 0
+#define ORCA_RESERVE_POW2 1
+#define ORCA_RESERVE_ORACLE 2
+
 /* Model shape and scheduler parameters.
  *   GPT decoder: n_layers blocks of hidden size `hidden`, n_heads heads
  *   (head_dim = hidden / n_heads), MLP width `ffn`, vocabulary `vocab`,
@@ -73,6 +77,11 @@ typedef struct orca_engine orca_engine;
  *   LayerNorm statistics, accumulation and logits fp32).
  *   max_bs, n_slots: Algorithm 1 parameters.  n_slots < 2^31.
  *   max_rows: capacity for sum L_i of one iteration.
+ *   reserve_policy: K/V slots a request reserves at first schedule (CS349D
+ *   Lecture 2, section 6.1): ORCA_RESERVE_MAX max_tokens (Orca's rule);
+ *   ORCA_RESERVE_POW2 its true final length n_prompt + out_len rounded up to
+ *   a power of two (a rough length prediction); ORCA_RESERVE_ORACLE the true
+ *   final length; both capped at max_tokens.
  *   bf16 requires hidden % 64 == 0 and ffn % 64 == 0; every dtype requires
  *   head_dim in {16, 32, 64, 128}. */
 typedef struct {
@@ -81,7 +90,7 @@ typedef struct {
   int32_t max_bs;
   int64_t n_slots;
   int32_t max_rows;
-  int32_t reserved0;
+  int32_t reserve_policy;
 } orca_config;
 
 /* One request of the pool (host memory, owned by the caller).
@@ -183,10 +192,18 @@ int orca_kv_release(orca_engine *eng, int64_t req_id);
 int orca_kv_stats(const orca_engine *eng, int64_t *n_rsrv, int64_t *n_free_blocks,
                   int64_t *frag_blocks);
 
+/* K/V memory use over a pool (CS349D Lecture 2, section 6.1: reserved is
+ * not the same as used): *reserved = slots currently reserved by the
+ * engine; *stored = sum of n_cached over the pool's requests that hold a
+ * reservation (not INITIATION, not FINISHED), the slots that hold K/V. */
+int orca_kv_usage(const orca_engine *eng, const orca_request *pool, int32_t n_pool, int64_t *reserved,
+                  int64_t *stored);
+
 /* ---------------------------------------------------------------- scheduling */
 /* Algorithm 1 Select over pool[0..n_pool): skip RUNNING and FINISHED
  * requests, sort the rest by (arrival, req_id), take at most max_bs; an
- * INITIATION request first reserves max_tokens slots (slot_base is set),
+ * INITIATION request first reserves slots by reserve_policy (slot_base and
+ * n_reserved are set),
  * and a failed reservation ends the selection (no skipping).  Selected
  * requests become RUNNING.  batch_idx (capacity max_bs) receives pool
  * indices in batch order; *n_batch their count (0 is valid). */

@@ -29,6 +29,7 @@ ERROR_NAMES = {ORCA_EINVAL: "EINVAL", ORCA_ENOSLOTS: "ENOSLOTS", ORCA_EBATCH: "E
 ORCA_DTYPE_F32 = 0
 ORCA_DTYPE_BF16 = 1
 ORCA_INITIATION, ORCA_INCREMENT, ORCA_RUNNING, ORCA_FINISHED = 0, 1, 2, 3
+ORCA_RESERVE_MAX, ORCA_RESERVE_POW2, ORCA_RESERVE_ORACLE = 0, 1, 2
 ORCA_ITER_TEACHER_FORCE = 1
 ORCA_ITER_EAGER = 2
 (ORCA_K_EMBED, ORCA_K_LAYERNORM, ORCA_K_GEMM_QKV, ORCA_K_ATTENTION, ORCA_K_GEMM_O, ORCA_K_GEMM_FC1,
@@ -47,7 +48,7 @@ class orca_config(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("ffn", ctypes.c_int32), ("vocab", ctypes.c_int32), ("max_pos", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("max_bs", ctypes.c_int32), ("n_slots", ctypes.c_int64),
-                ("max_rows", ctypes.c_int32), ("reserved0", ctypes.c_int32)]
+                ("max_rows", ctypes.c_int32), ("reserve_policy", ctypes.c_int32)]
 
 
 class orca_request(ctypes.Structure):
@@ -68,7 +69,7 @@ EXPORTS = ("orca_kv_pool_bytes", "orca_workspace_bytes", "orca_weight_count", "o
            "orca_iteration", "orca_last_descriptor", "orca_argmax_rows", "orca_profile_enable",
            "orca_profile_read", "orca_last_error", "orca_linear", "orca_last_transfer",
            "orca_attention_workspace_bytes", "orca_attention", "orca_attention_noalloc", "orca_last_launches",
-           "orca_select_batch_budget")
+           "orca_select_batch_budget", "orca_kv_usage")
 
 _lib = None
 
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "orca_kv_reserve": [P, c_i64, c_i32, i64p],
             "orca_kv_release": [P, c_i64],
             "orca_kv_stats": [P, i64p, i64p, i64p],
+            "orca_kv_usage": [P, reqp, c_i32, i64p, i64p],
             "orca_select_batch": [P, reqp, c_i32, i32p, i32p],
             "orca_select_batch_budget": [P, reqp, c_i32, c_i32, c_i32, i32p, i32p],
             "orca_iteration": [P, reqp, i32p, c_i32, c_i32, i32p, P, P],
@@ -177,6 +179,13 @@ def orca_kv_stats(eng):
     a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
     _check(lib().orca_kv_stats(eng, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), eng)
     return a.value, b.value, c.value
+
+
+def orca_kv_usage(eng, pool, n_pool: int):
+    """(reserved slots, slots holding K/V) over the pool."""
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().orca_kv_usage(eng, pool, n_pool, ctypes.byref(a), ctypes.byref(b)), eng)
+    return a.value, b.value
 
 
 def orca_select_batch(eng, pool, n_pool: int, batch_idx) -> int:

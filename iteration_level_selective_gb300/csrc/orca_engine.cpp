@@ -124,6 +124,10 @@ int check_config(const orca_config *c, std::string *why) {
   }
   if (c->n_slots >= (int64_t)INT32_MAX) { *why = "n_slots must be < 2^31"; return ORCA_EINVAL; }
   if (c->max_rows < c->max_bs) { *why = "max_rows must be >= max_bs"; return ORCA_EINVAL; }
+  if (c->reserve_policy < ORCA_RESERVE_MAX || c->reserve_policy > ORCA_RESERVE_ORACLE) {
+    *why = "unknown reserve_policy";
+    return ORCA_EINVAL;
+  }
   return ORCA_OK;
 }
 
@@ -751,6 +755,21 @@ namespace {
 // the rest of its prompt, or one row once the prompt is processed.
 int32_t default_rows(const orca_request &r) { return r.n_cached < r.n_prompt ? r.n_prompt - r.n_cached : 1; }
 
+// Slots a request reserves at first schedule (CS349D Lecture 2, section
+// 6.1): max_tokens (Orca), or its true final length n_prompt + out_len
+// rounded up to a power of two, or that length itself; never above
+// max_tokens, the most a request can hold.
+int32_t reserve_size(int policy, const orca_request &r) {
+  const int64_t len = std::min<int64_t>((int64_t)r.n_prompt + r.out_len, r.max_tokens);
+  if (policy == ORCA_RESERVE_ORACLE) return (int32_t)len;
+  if (policy == ORCA_RESERVE_POW2) {
+    int64_t p = 1;
+    while (p < len) p <<= 1;
+    return (int32_t)std::min<int64_t>(p, r.max_tokens);
+  }
+  return r.max_tokens;
+}
+
 // Algorithm 1 Select (Orca walk-through, Algorithm 1): candidates are the
 // non-RUNNING, unfinished requests in (arrival, req_id) order; at most max_bs;
 // an INITIATION request first reserves max_tokens slots and a failed
@@ -778,7 +797,7 @@ int select_fcfs(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t *bat
         return fail(e, ORCA_EINVAL, "request %lld: need 0 < n_prompt <= max_tokens and out_len > 0",
                     (long long)r.req_id);
       int64_t base = -1;
-      const int32_t want = r.max_tokens;
+      const int32_t want = reserve_size(e->cfg.reserve_policy, r);
       const int rc = e->slots.reserve(r.req_id, want, &base);
       if (rc == ORCA_ENOSLOTS) break;  // Algorithm 1: stop selecting, never skip
       if (rc) return fail(e, rc, "request %lld already holds a reservation", (long long)r.req_id);
@@ -793,6 +812,19 @@ int select_fcfs(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t *bat
 }
 
 }  // namespace
+
+int orca_kv_usage(const orca_engine *e, const orca_request *pool, int32_t n_pool, int64_t *reserved,
+                  int64_t *stored) {
+  if (!e || n_pool < 0 || (n_pool > 0 && !pool)) return ORCA_EINVAL;
+  int64_t st = 0;
+  for (int32_t i = 0; i < n_pool; ++i) {
+    const orca_request &r = pool[i];
+    if (r.state != ORCA_INITIATION && r.state != ORCA_FINISHED && r.slot_base >= 0) st += r.n_cached;
+  }
+  if (reserved) *reserved = e->slots.n_rsrv;
+  if (stored) *stored = st;
+  return ORCA_OK;
+}
 
 int orca_select_batch(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t *batch_idx, int32_t *n_batch) {
   if (!e || !n_batch || (n_pool > 0 && (!pool || !batch_idx)) || n_pool < 0) return ORCA_EINVAL;

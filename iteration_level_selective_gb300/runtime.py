@@ -29,10 +29,14 @@ def _is_matrix(name: str) -> bool:
     return name.startswith("w_") or name.endswith("_emb")
 
 
-def make_config(shape, max_bs: int, n_slots: int, max_rows: int) -> C.orca_config:
+RESERVE_POLICIES = {"max": C.ORCA_RESERVE_MAX, "pow2": C.ORCA_RESERVE_POW2, "oracle": C.ORCA_RESERVE_ORACLE}
+
+
+def make_config(shape, max_bs: int, n_slots: int, max_rows: int, reserve_policy: int = C.ORCA_RESERVE_MAX
+                ) -> C.orca_config:
     return C.orca_config(n_layers=shape.n_layers, hidden=shape.hidden, n_heads=shape.n_heads, ffn=shape.ffn,
                          vocab=shape.vocab, max_pos=shape.max_pos, dtype=shape.dtype, max_bs=max_bs,
-                         n_slots=n_slots, max_rows=max_rows)
+                         n_slots=n_slots, max_rows=max_rows, reserve_policy=reserve_policy)
 
 
 class DeviceWeights:
@@ -79,10 +83,11 @@ class DeviceWeights:
 class Engine:
     """liborca engine with torch-allocated K/V pool and workspace."""
 
-    def __init__(self, shape, weights: DeviceWeights, max_bs: int, n_slots: int, max_rows: int, device=None):
+    def __init__(self, shape, weights: DeviceWeights, max_bs: int, n_slots: int, max_rows: int, device=None,
+                 reserve_policy: int = C.ORCA_RESERVE_MAX):
         self.shape = shape
         self.device = torch.device(device if device is not None else "cuda")
-        self.cfg = make_config(shape, max_bs, n_slots, max_rows)
+        self.cfg = make_config(shape, max_bs, n_slots, max_rows, reserve_policy)
         self.kv_bytes = C.orca_kv_pool_bytes(self.cfg)
         self.ws_bytes = C.orca_workspace_bytes(self.cfg)
         self.kv = torch.empty(self.kv_bytes, dtype=torch.uint8, device=self.device)

@@ -84,7 +84,30 @@ class ReqState:
     slot_base: int = -1
 
 
-def select(pool: List[ReqState], slots: SlotPool, max_bs: int) -> List[ReqState]:
+RESERVE_MAX, RESERVE_POW2, RESERVE_ORACLE = 0, 1, 2
+
+
+def reserve_size(policy: int, r: ReqState) -> int:
+    """Slots a request reserves at first schedule (CS349D Lecture 2, section
+    6.1, the three ways Orca is re-implemented there): Max reserves
+    max_tokens, the most the request may reach; Pow2 reserves its true
+    final length (prompt + output) rounded up to a power of two, as with an
+    imprecise length prediction; Oracle reserves exactly the true final
+    length.  Reading: "true final length" is n_prompt + out_len, capped at
+    max_tokens (a request never grows past max_tokens), and so are the other
+    two."""
+    true_len = min(r.n_prompt + r.out_len, r.max_tokens)
+    if policy == RESERVE_ORACLE:
+        return true_len
+    if policy == RESERVE_POW2:
+        p = 1
+        while p < true_len:
+            p *= 2
+        return min(p, r.max_tokens)
+    return r.max_tokens
+
+
+def select(pool: List[ReqState], slots: SlotPool, max_bs: int, policy: int = RESERVE_MAX) -> List[ReqState]:
     """Algorithm 1 Select over the arrived, unfinished requests."""
     cands = sorted((r for r in pool if r.state in (INITIATION, INCREMENT)),
                    key=lambda r: (r.arrival, r.req_id))
@@ -93,12 +116,19 @@ def select(pool: List[ReqState], slots: SlotPool, max_bs: int) -> List[ReqState]
         if len(batch) == max_bs:
             break
         if r.state == INITIATION:
-            base = slots.reserve(r.req_id, r.max_tokens)
+            base = slots.reserve(r.req_id, reserve_size(policy, r))
             if base is None:
                 break
             r.slot_base = base
         batch.append(r)
     return batch
+
+
+def kv_usage(pool: List[ReqState], slots: SlotPool) -> Tuple[int, int]:
+    """(reserved slots, slots holding K/V): CS349D Lecture 2, section 6.1
+    contrasts the memory a reservation occupies with what is written."""
+    stored = sum(r.n_cached for r in pool if r.state not in (INITIATION, FINISHED) and r.slot_base >= 0)
+    return slots.n_rsrv, stored
 
 
 def default_rows(r: ReqState) -> int:
@@ -108,7 +138,7 @@ def default_rows(r: ReqState) -> int:
 
 
 def select_budget(pool: List[ReqState], slots: SlotPool, max_bs: int, token_budget: int,
-                  chunk: int) -> List[Tuple[ReqState, int]]:
+                  chunk: int, policy: int = RESERVE_MAX) -> List[Tuple[ReqState, int]]:
     """Chunked prefill under a per-iteration token budget, on top of
     Algorithm 1.
 
@@ -122,7 +152,7 @@ def select_budget(pool: List[ReqState], slots: SlotPool, max_bs: int, token_budg
     while the budget lasts, then every prompting request takes
     min(remaining prompt, chunk, budget left) rows.  Returns (request, rows)
     in batch order; rows may be 0 (admitted but idle this iteration)."""
-    batch = select(pool, slots, max_bs)
+    batch = select(pool, slots, max_bs, policy)
     left = token_budget
     rows: Dict[int, int] = {}
     for r in batch:
@@ -152,7 +182,8 @@ class IterRecord:
 
 
 def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
-                 token_budget: Optional[int] = None, chunk: Optional[int] = None) -> List[IterRecord]:
+                 token_budget: Optional[int] = None, chunk: Optional[int] = None,
+                 policy: int = RESERVE_MAX) -> List[IterRecord]:
     """Drive Algorithm 1 over a trace whose arrivals are iteration indices.
 
     A request whose arrival is t can be selected at iteration t.  When no
@@ -177,9 +208,9 @@ def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
             pool.append(states[nxt])
             nxt += 1
         if budgeted:
-            sel = select_budget(pool, slots, max_bs, token_budget or big, chunk or big)
+            sel = select_budget(pool, slots, max_bs, token_budget or big, chunk or big, policy)
         else:
-            sel = [(r, default_rows(r)) for r in select(pool, slots, max_bs)]
+            sel = [(r, default_rows(r)) for r in select(pool, slots, max_bs, policy)]
         run = [(r, n) for r, n in sel if n > 0]
         if not run:
             raise RuntimeError(f"no request can be scheduled at iteration {it}")

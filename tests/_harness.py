@@ -15,12 +15,13 @@ def max_rel_err(got, want):
 
 
 def run_gpu(shape, host_weights, trace, max_bs, n_slots, max_rows, teacher_force=False, keep_ids=None,
-            keep_all=False, eager=False, token_budget=None, chunk=None):
+            keep_all=False, eager=False, token_budget=None, chunk=None, reserve_policy=0):
     import torch
     from iteration_level_selective_gb300 import runtime as rt
     dev = torch.device("cuda:0")
     w = rt.DeviceWeights(shape, dev, host=host_weights)
-    eng = rt.Engine(shape, w, max_bs=max_bs, n_slots=n_slots, max_rows=max_rows, device=dev)
+    eng = rt.Engine(shape, w, max_bs=max_bs, n_slots=n_slots, max_rows=max_rows, device=dev,
+                    reserve_policy=reserve_policy)
     pool = rt.RequestPool(trace, teacher_force=teacher_force)
     loop = rt.ServingLoop(eng, pool, teacher_force=teacher_force, keep_logits=keep_all, keep_ids=keep_ids,
                           eager=eager, token_budget=token_budget, chunk=chunk)
@@ -28,9 +29,10 @@ def run_gpu(shape, host_weights, trace, max_bs, n_slots, max_rows, teacher_force
     return recs, eng, pool
 
 
-def compare_schedule(gpu_recs, trace, max_bs, n_slots, token_budget=None, chunk=None):
+def compare_schedule(gpu_recs, trace, max_bs, n_slots, token_budget=None, chunk=None, reserve_policy=0):
     """Integer record of every iteration, bit-exact against the oracle scheduler."""
-    orecs = osched.run_schedule(trace, max_bs=max_bs, n_slots=n_slots, token_budget=token_budget, chunk=chunk)
+    orecs = osched.run_schedule(trace, max_bs=max_bs, n_slots=n_slots, token_budget=token_budget, chunk=chunk,
+                                policy=reserve_policy)
     assert len(gpu_recs) == len(orecs)
     for g, o in zip(gpu_recs, orecs):
         assert (g.it, g.req_ids, g.n_new, g.n_ctx, g.slot_base, sorted(g.released)) == \

@@ -27,9 +27,9 @@ def test_every_declared_symbol_is_exported(liborca):
     assert set(C.EXPORTS) <= set(names)
 
 
-def _cfg(max_bs=4, n_slots=64, dtype=C.ORCA_DTYPE_F32):
+def _cfg(max_bs=4, n_slots=64, dtype=C.ORCA_DTYPE_F32, policy=C.ORCA_RESERVE_MAX):
     return C.orca_config(n_layers=2, hidden=64, n_heads=4, ffn=256, vocab=256, max_pos=64, dtype=dtype,
-                         max_bs=max_bs, n_slots=n_slots, max_rows=64)
+                         max_bs=max_bs, n_slots=n_slots, max_rows=64, reserve_policy=policy)
 
 
 def test_sizes_and_config_validation(liborca):
@@ -85,10 +85,11 @@ class _Sim:
     """Drives the C Select and the oracle Select side by side; the test
     applies the same post-iteration update to both."""
 
-    def __init__(self, trace, max_bs, n_slots, budget=None):
+    def __init__(self, trace, max_bs, n_slots, budget=None, policy=C.ORCA_RESERVE_MAX):
         self.budget = budget  # (token_budget, chunk) for the chunked-prefill Select, or None
+        self.policy = policy
         self.trace = sorted(trace, key=lambda t: (t[1], t[0]))
-        self.eng = C.orca_engine_create(_cfg(max_bs=max_bs, n_slots=n_slots))
+        self.eng = C.orca_engine_create(_cfg(max_bs=max_bs, n_slots=n_slots, policy=policy))
         self.max_bs = max_bs
         n = len(self.trace)
         self.arr = (C.orca_request * n)()
@@ -114,16 +115,18 @@ class _Sim:
             opool = [s for s in self.ostates[:n_arr] if s.state != osched.FINISHED]
             if self.budget is None:
                 nb = C.orca_select_batch(self.eng, self.arr, n_arr, self.bi)
-                osel = [(r, osched.default_rows(r)) for r in osched.select(opool, self.oslots, self.max_bs)]
+                osel = [(r, osched.default_rows(r))
+                        for r in osched.select(opool, self.oslots, self.max_bs, self.policy)]
             else:
                 nb = C.orca_select_batch_budget(self.eng, self.arr, n_arr, self.budget[0], self.budget[1], self.bi)
-                osel = osched.select_budget(opool, self.oslots, self.max_bs, *self.budget)
+                osel = osched.select_budget(opool, self.oslots, self.max_bs, *self.budget, policy=self.policy)
             orun = [(r, k) for r, k in osel if k > 0]
             got = [(self.arr[self.bi[i]].req_id, self.arr[self.bi[i]].slot_base, self.arr[self.bi[i]].n_sched)
                    for i in range(nb)]
             want = [(r.req_id, r.slot_base, k) for r, k in orun]
             assert got == want, (it, got, want)
             assert C.orca_kv_stats(self.eng)[0] == self.oslots.n_rsrv
+            assert C.orca_kv_usage(self.eng, self.arr, n_arr) == osched.kv_usage(self.ostates[:n_arr], self.oslots)
             for i in range(nb):
                 a = self.arr[self.bi[i]]
                 assert a.state == C.ORCA_RUNNING
@@ -180,6 +183,27 @@ def test_budget_select_bit_exact_vs_oracle_random_traces(liborca):
         max_t = max(t[4] for t in trace)
         budget = (int(rng.integers(1, 48)), int(rng.integers(1, 32)))
         _Sim(trace, max_bs=int(rng.integers(1, 12)), n_slots=int(rng.integers(max_t, 4 * max_t)), budget=budget).run()
+
+
+@pytest.mark.parametrize("policy", [C.ORCA_RESERVE_POW2, C.ORCA_RESERVE_ORACLE])
+def test_reserve_policy_select_bit_exact_vs_oracle(liborca, policy):
+    rng = np.random.default_rng(23 + policy)
+    for trial in range(30):
+        n = int(rng.integers(3, 40))
+        trace = []
+        for i in range(n):
+            lp, lo = int(rng.integers(1, 30)), int(rng.integers(1, 20))
+            trace.append((i, int(rng.integers(0, 30)), lp, lo, lp + lo + int(rng.integers(0, 30))))
+        max_t = max(t[4] for t in trace)
+        budget = (int(rng.integers(1, 48)), int(rng.integers(1, 32))) if trial % 2 else None
+        _Sim(trace, max_bs=int(rng.integers(1, 12)), n_slots=int(rng.integers(max_t, 3 * max_t)), budget=budget,
+             policy=policy).run()
+
+
+def test_bad_reserve_policy_rejected(liborca):
+    with pytest.raises(C.OrcaError) as ei:
+        C.orca_kv_pool_bytes(_cfg(policy=3))
+    assert ei.value.code == C.ORCA_EINVAL
 
 
 def test_budget_select_rejects_bad_budget(liborca):

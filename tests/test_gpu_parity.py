@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import synth
+from oracle import scheduler as osched
 from oracle import ragged as oragged
 
 from . import _harness as hz
@@ -177,6 +178,32 @@ def test_toy_fp32_teacher_forced_poisson_trace(cuda):
         for g, o in zip(got_lg[req.req_id], logits):
             assert hz.max_rel_err(g, o) < FP32_TOL
         assert got_tok[req.req_id] == greedy
+
+
+@pytest.mark.parametrize("policy", [1, 2])
+def test_toy_fp32_reservation_policies_tight_memory(cuda, policy):
+    """Pow2 and Oracle reservations (CS349D Lecture 2, section 6.1) on a
+    trace whose slots bind: the schedule, the slot bases and the K/V usage
+    match the oracle scheduler; every request writes only inside the slots
+    it reserved, and its logits equal its own generation."""
+    from iteration_level_selective_gb300 import _orca as C
+    shape = synth.TOY
+    w = _toy_weights(seed=9)
+    trace = synth.make_trace(12, (1, 20), (1, 12), vocab=shape.vocab, seed=10, rate_per_iter=1.0, forced=True,
+                             max_extra=30)
+    n_slots = 64
+    recs, eng, pool = hz.run_gpu(shape, w, trace, max_bs=6, n_slots=n_slots, max_rows=64, teacher_force=True,
+                                 keep_all=True, reserve_policy=policy)
+    hz.compare_schedule(recs, trace, max_bs=6, n_slots=n_slots, reserve_policy=policy)
+    mx = osched.run_schedule(trace, max_bs=6, n_slots=n_slots, policy=osched.RESERVE_MAX)
+    assert len(recs) < len(mx)  # smaller reservations admit more requests at once
+    assert C.orca_kv_usage(eng.handle, pool.arr, pool.n) == (0, 0)  # all finished, all released
+    got_lg = hz.gpu_logits_by_request(recs)
+    for req in trace:
+        _, logits = hz.oracle_generate(shape, w, req, teacher_force=True)
+        assert len(got_lg[req.req_id]) == len(logits)
+        for g, o in zip(got_lg[req.req_id], logits):
+            assert hz.max_rel_err(g, o) < FP32_TOL
 
 
 # ------------------------------------------------------------------ bf16, multi-tile

@@ -432,3 +432,69 @@ def test_budget_invariants_random_traces():
                     generated[rid] += 1
         assert done_prompt == n_prompt
         assert all(generated[t.req_id] == t.out_len for t in trace)
+
+
+# ---------------------------------------------------------------- reservation variants (CS349D Lecture 2, 6.1)
+
+def test_reserve_sizes_by_hand():
+    R = scheduler.ReqState
+    M, P2, O = scheduler.RESERVE_MAX, scheduler.RESERVE_POW2, scheduler.RESERVE_ORACLE
+    size = scheduler.reserve_size
+    r = R(0, 0, 300, 100, 556)          # true length 400
+    assert (size(M, r), size(P2, r), size(O, r)) == (556, 512, 400)
+    r = R(0, 0, 300, 300, 556)          # true length 600 > max_tokens: all capped
+    assert (size(M, r), size(P2, r), size(O, r)) == (556, 556, 556)
+    r = R(0, 0, 3, 2, 9)                # 5 -> 8
+    assert (size(M, r), size(P2, r), size(O, r)) == (9, 8, 5)
+    r = R(0, 0, 1, 1, 5)                # 2 is already a power of two
+    assert (size(P2, r), size(O, r)) == (2, 2)
+
+
+def test_tight_memory_policies_by_hand():
+    # n_slots 10, A and B: prompt 2, 2 tokens, max_tokens 8 (true length 4).
+    # Max: A takes 8 slots, B (8 more) does not fit and waits for A;
+    # Pow2 and Oracle: 4 + 4 slots, both run together.
+    trace = [_R(0, 0, 2, 2, 8), _R(1, 0, 2, 2, 8)]
+    mx = scheduler.run_schedule(trace, max_bs=4, n_slots=10, policy=scheduler.RESERVE_MAX)
+    assert _records(mx) == [(0, [0], [2], [0], []), (1, [0], [1], [2], [0]),
+                            (2, [1], [2], [0], []), (3, [1], [1], [2], [1])]
+    for pol in (scheduler.RESERVE_POW2, scheduler.RESERVE_ORACLE):
+        recs = scheduler.run_schedule(trace, max_bs=4, n_slots=10, policy=pol)
+        assert _records(recs) == [(0, [0, 1], [2, 2], [0, 0], []), (1, [0, 1], [1, 1], [2, 2], [0, 1])]
+        assert recs[0].slot_base == [0, 4]
+
+
+def test_policies_agree_when_memory_is_ample_and_stored_never_exceeds_reserved():
+    rng = np.random.default_rng(43)
+    for trial in range(20):
+        n = int(rng.integers(3, 30))
+        trace = []
+        for i in range(n):
+            lp, lo = int(rng.integers(1, 20)), int(rng.integers(1, 12))
+            trace.append(_R(i, int(rng.integers(0, 20)), lp, lo, lp + lo + int(rng.integers(0, 20))))
+        base = None
+        for pol in (scheduler.RESERVE_MAX, scheduler.RESERVE_POW2, scheduler.RESERVE_ORACLE):
+            recs = scheduler.run_schedule(trace, max_bs=int(trial % 7) + 1, n_slots=10_000, policy=pol)
+            if base is None:
+                base = _records(recs)
+            assert _records(recs) == base
+        # tight memory: at every step the written slots fit in the reservations
+        for pol in (scheduler.RESERVE_MAX, scheduler.RESERVE_POW2, scheduler.RESERVE_ORACLE):
+            order = sorted(trace, key=lambda r: (r.arrival, r.req_id))
+            states = [scheduler.ReqState(r.req_id, r.arrival, r.n_prompt, r.out_len, r.max_tokens) for r in order]
+            slots = scheduler.SlotPool(max(t.max_tokens for t in trace) * 2)
+            for step in range(200):
+                live = [r for r in states if r.arrival <= step and r.state != scheduler.FINISHED]
+                if not live:
+                    continue
+                for r in scheduler.select(live, slots, 4, pol):
+                    r.n_cached += scheduler.default_rows(r)
+                    r.n_generated += 1
+                    r.state = scheduler.INCREMENT
+                    assert r.n_cached <= slots.owned[r.req_id][1]
+                    if scheduler.finished(r):
+                        r.state = scheduler.FINISHED
+                        slots.release(r.req_id)
+                reserved, stored = scheduler.kv_usage(states, slots)
+                assert stored <= reserved <= slots.n_slots
+            assert all(r.state == scheduler.FINISHED for r in states)
