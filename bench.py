@@ -241,16 +241,17 @@ class TraceWorkload:
     """The GPT-2-small serving trace, restarted whenever it completes
     (optionally with chunked prefill under a per-iteration token budget)."""
 
-    def __init__(self, eng, rank, stream, token_budget=None, chunk=None):
+    def __init__(self, eng, rank, stream, token_budget=None, chunk=None, n_workers=1):
         from iteration_level_selective_gb300 import runtime as rt
         self.rt, self.eng, self.rank, self.stream, self.gen = rt, eng, rank, stream, 0
         self.budget = (token_budget, chunk)
+        self.n_workers = n_workers
         self.loop = self._new()
 
     def _new(self):
         self.gen += 1
         return self.rt.ServingLoop(self.eng, self.rt.RequestPool(trace_for(self.rank, self.gen)), stream=self.stream,
-                                   token_budget=self.budget[0], chunk=self.budget[1])
+                                   token_budget=self.budget[0], chunk=self.budget[1], n_workers=self.n_workers)
 
     def step(self):
         if self.loop.done():
@@ -320,7 +321,7 @@ def run_ours(args, rank: int, world: int):
         n_slots = args.kv_slots if args.kv_slots else n_slots_for(shape)
         eng = rt.Engine(shape, weights, max_bs=64, n_slots=n_slots, max_rows=64 * 512, device=dev,
                         reserve_policy=rt.RESERVE_POLICIES[args.reserve])
-        work = TraceWorkload(eng, rank, stream, args.token_budget, args.chunk)
+        work = TraceWorkload(eng, rank, stream, args.token_budget, args.chunk, args.workers)
         workload = WORKLOAD
         if args.token_budget or args.chunk:
             workload += f", chunked prefill (token budget {args.token_budget or 'none'}, chunk {args.chunk or 'none'})"
@@ -330,6 +331,9 @@ def run_ours(args, rank: int, world: int):
         if args.token_budget or args.chunk:
             cfg_extra["token_budget"] = args.token_budget or None
             cfg_extra["chunk"] = args.chunk or None
+        if args.workers != 1:
+            cfg_extra["n_workers"] = args.workers
+            workload += f", {args.workers} batches in flight"
         if args.reserve != "max":
             cfg_extra["reserve_policy"] = args.reserve
             workload += f", {args.reserve} K/V reservation"
@@ -496,6 +500,8 @@ def main():
                     help="gpt2-trace only: chunked prefill with this many rows per iteration at most")
     ap.add_argument("--chunk", type=int, default=0,
                     help="gpt2-trace only: prompt chunk size for chunked prefill")
+    ap.add_argument("--workers", type=int, choices=[1, 2], default=1,
+                    help="gpt2-trace only: batches in flight at once (Algorithm 1's n_workers)")
     ap.add_argument("--reserve", choices=["max", "pow2", "oracle"], default="max",
                     help="gpt2-trace only: K/V reservation policy (max_tokens, power of two, true length)")
     ap.add_argument("--kv-slots", type=int, default=0,

@@ -248,6 +248,25 @@ int orca_select_batch_budget(orca_engine *eng, orca_request *pool, int32_t n_poo
 int orca_iteration(orca_engine *eng, orca_request *pool, const int32_t *batch_idx, int32_t n_batch,
                    int32_t flags, int32_t *next_tokens, float *logits_dev, void *stream);
 
+/* orca_iteration in two halves, so that up to two iterations are in flight
+ * (Algorithm 1 with n_workers = 2: the scheduler selects and enqueues the
+ * next batch, from the requests not RUNNING, while the previous one runs;
+ * Orca walk-through, Algorithm 1 and pipelined workers).
+ * orca_iteration_submit validates the batch, stages its descriptor and
+ * enqueues the forward and the result copy on `stream`, without waiting;
+ * the requests stay RUNNING.  Iterations in flight together share one
+ * stream, run in submission order, never share a request, and use distinct
+ * logits_dev buffers (or NULL).  ORCA_ESTATE
+ * when two are already in flight.  `pool` must stay valid until the wait.
+ * orca_iteration_wait waits for the oldest iteration in flight and applies
+ * its updates as orca_iteration does; *n_batch and batch_idx (capacity
+ * max_bs; either may be NULL) receive its batch, next_tokens (capacity
+ * max_bs, may be NULL) its tokens.  ORCA_ESTATE when none is in flight.
+ * orca_iteration itself is submit + wait and needs none in flight. */
+int orca_iteration_submit(orca_engine *eng, orca_request *pool, const int32_t *batch_idx, int32_t n_batch,
+                          int32_t flags, float *logits_dev, void *stream);
+int orca_iteration_wait(orca_engine *eng, int32_t *n_batch, int32_t *batch_idx, int32_t *next_tokens);
+
 /* Host copy of the last iteration's ragged descriptor: row_off[n_batch+1],
  * per-row position row_pos[n_rows] and K/V slot row_slot[n_rows], and
  * last_row[n_batch].  Any output may be NULL. */

@@ -69,7 +69,7 @@ EXPORTS = ("orca_kv_pool_bytes", "orca_workspace_bytes", "orca_weight_count", "o
            "orca_iteration", "orca_last_descriptor", "orca_argmax_rows", "orca_profile_enable",
            "orca_profile_read", "orca_last_error", "orca_linear", "orca_last_transfer",
            "orca_attention_workspace_bytes", "orca_attention", "orca_attention_noalloc", "orca_last_launches",
-           "orca_select_batch_budget", "orca_kv_usage")
+           "orca_select_batch_budget", "orca_kv_usage", "orca_iteration_submit", "orca_iteration_wait")
 
 _lib = None
 
@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
             "orca_select_batch": [P, reqp, c_i32, i32p, i32p],
             "orca_select_batch_budget": [P, reqp, c_i32, c_i32, c_i32, i32p, i32p],
             "orca_iteration": [P, reqp, i32p, c_i32, c_i32, i32p, P, P],
+            "orca_iteration_submit": [P, reqp, i32p, c_i32, c_i32, P, P],
+            "orca_iteration_wait": [P, i32p, i32p, i32p],
             "orca_last_descriptor": [P, i32p, i32p, i32p, i32p, i32p, i32p, c_i32],
             "orca_argmax_rows": [P, c_i32, c_i32, P, P],
             "orca_profile_enable": [P, c_i32],
@@ -205,6 +207,18 @@ def orca_select_batch_budget(eng, pool, n_pool: int, token_budget: int, chunk: i
 def orca_iteration(eng, pool, batch_idx, n_batch: int, flags: int, next_tokens, logits_ptr=0, stream=0) -> None:
     _check(lib().orca_iteration(eng, pool, batch_idx, n_batch, flags, next_tokens,
                                 ctypes.c_void_p(logits_ptr or None), ctypes.c_void_p(stream or None)), eng)
+
+
+def orca_iteration_submit(eng, pool, batch_idx, n_batch: int, flags: int, logits_ptr=0, stream=0) -> None:
+    _check(lib().orca_iteration_submit(eng, pool, batch_idx, n_batch, flags, ctypes.c_void_p(logits_ptr or None),
+                                       ctypes.c_void_p(stream or None)), eng)
+
+
+def orca_iteration_wait(eng, batch_idx, next_tokens) -> int:
+    """Wait for the oldest iteration in flight; returns its batch size."""
+    n = ctypes.c_int32()
+    _check(lib().orca_iteration_wait(eng, ctypes.byref(n), batch_idx, next_tokens), eng)
+    return n.value
 
 
 def orca_last_descriptor(eng, capacity: int):

@@ -99,8 +99,14 @@ int32_t max_attn_work(int32_t n_batch, int32_t n_rows);
 int32_t max_tc_work(int32_t n_batch, int32_t n_rows);
 int order_tc_work(AttnWork *w, int32_t n, const ReqInfo *req);
 
+// Iterations one engine keeps in flight at once (Algorithm 1 with up to
+// two scheduled batches): each has its own descriptor and result buffers;
+// the activations are shared because the batches run in stream order.
+constexpr int kMaxInflight = 2;
+
 struct Layout {  // byte offsets into the device workspace
-  size_t x, h, q, u, hf, logits, out, req, row, work, work_tc, part, counters, gemm_cnt, gemm_part, total;
+  size_t x, h, q, u, hf, logits, part, counters, gemm_cnt, gemm_part, total;
+  size_t out[kMaxInflight], req[kMaxInflight], row[kMaxInflight], work[kMaxInflight], work_tc[kMaxInflight];
   int max_work;
 };
 
@@ -145,11 +151,13 @@ Layout make_layout(const orca_config *c) {
   L.u = take(R * F * e);
   L.hf = take(B * H * e);
   L.logits = take(B * V * 4);
-  L.out = take((B + 1) * 8);  // [0] status word, [1..B] packed argmax keys
-  L.req = take(sizeof(DevHeader) + B * sizeof(ReqInfo));  // header, then request records
-  L.row = take(R * sizeof(RowInfo));
-  L.work = take((size_t)L.max_work * sizeof(AttnWork));
-  L.work_tc = take((size_t)max_tc_work(c->max_bs, c->max_rows) * sizeof(AttnWork));
+  for (int k = 0; k < kMaxInflight; ++k) {
+    L.out[k] = take((B + 1) * 8);  // [0] status word, [1..B] packed argmax keys
+    L.req[k] = take(sizeof(DevHeader) + B * sizeof(ReqInfo));  // header, then request records
+    L.row[k] = take(R * sizeof(RowInfo));
+    L.work[k] = take((size_t)L.max_work * sizeof(AttnWork));
+    L.work_tc[k] = take((size_t)max_tc_work(c->max_bs, c->max_rows) * sizeof(AttnWork));
+  }
   L.part = take((size_t)B * kMaxSplits * c->n_heads * (d + 2) * 4);
   L.counters = take((B * c->n_heads + 4) * 4);  // split arrivals, then two work tickets
   L.gemm_cnt = take(kGemmMaxSms * 4);
@@ -256,13 +264,23 @@ struct orca_engine {
   std::vector<const void *> w;
   char *kv = nullptr;
   char *ws = nullptr;
-  // pinned host staging
-  DevHeader *h_hdr = nullptr;  // pinned: header followed by the request records
-  ReqInfo *h_req = nullptr;
-  RowInfo *h_row = nullptr;
-  AttnWork *h_work = nullptr;
-  AttnWork *h_work_tc = nullptr;
-  unsigned long long *h_out = nullptr;  // [0] status word, [1..] packed argmax keys
+  // one in-flight iteration: pinned host staging and what its wait needs
+  struct IterSlot {
+    DevHeader *h_hdr = nullptr;  // pinned: header followed by the request records
+    ReqInfo *h_req = nullptr;
+    RowInfo *h_row = nullptr;
+    AttnWork *h_work = nullptr;
+    AttnWork *h_work_tc = nullptr;
+    unsigned long long *h_out = nullptr;  // [0] status word, [1..] packed argmax keys
+    cudaEvent_t done = nullptr;           // recorded after the result copy
+    orca_request *pool = nullptr;
+    float *logits = nullptr;
+    cudaStream_t st = nullptr;
+    int32_t flags = 0, n_batch = 0;
+    std::vector<int32_t> idx, L;
+  };
+  IterSlot slot[kMaxInflight];
+  int q_head = 0, q_len = 0;  // submitted iterations, oldest first
   // tensor maps (bf16)
   CUtensorMap tm_h{}, tm_u{}, tm_hf{}, tm_q{};
   std::vector<CUtensorMap> tm_k;      // per layer: K slots as [n_heads * n_slots, head_dim]
@@ -278,10 +296,10 @@ struct orca_engine {
   // profiling
   bool prof = false;
   orca_kernel_stats stats[ORCA_K_COUNT]{};
-  struct Pending { int cls; cudaEvent_t a, b; double flops, bytes; };
-  std::vector<cudaEvent_t> ev_pool;
-  size_t ev_used = 0;
+  struct Pending { int slot, cls; cudaEvent_t a, b; double flops, bytes; };
+  std::vector<cudaEvent_t> ev_all, ev_free;  // every event created; those not recorded for a pending launch
   std::vector<Pending> pending;
+  int cur_slot = 0;                          // in-flight slot of the iteration being enqueued
   // CUDA graphs of the forward, keyed by GEMM tile choices and logits pointer
   cudaStream_t cap_stream = nullptr;
   struct Graph {
@@ -356,27 +374,41 @@ enum { L_LN1_G = 0, L_LN1_B, L_WQKV, L_BQKV, L_WO, L_BO, L_LN2_G, L_LN2_B, L_W1,
 inline const void *lw(const orca_engine *e, int layer, int which) { return e->w[4 + layer * L_COUNT + which]; }
 
 // ---- profiling helpers
+cudaEvent_t prof_event(orca_engine *e) {
+  if (e->ev_free.empty()) {
+    cudaEvent_t ev;
+    if (cudaEventCreate(&ev) != cudaSuccess) return nullptr;
+    e->ev_all.push_back(ev);
+    return ev;
+  }
+  cudaEvent_t ev = e->ev_free.back();
+  e->ev_free.pop_back();
+  return ev;
+}
 void prof_begin(orca_engine *e, cudaStream_t st, cudaEvent_t *a) {
   *a = nullptr;
   if (!e->prof) return;
-  if (e->ev_used + 2 > e->ev_pool.size()) {
-    for (int i = 0; i < 64; ++i) {
-      cudaEvent_t ev;
-      if (cudaEventCreate(&ev) != cudaSuccess) return;
-      e->ev_pool.push_back(ev);
-    }
-  }
-  *a = e->ev_pool[e->ev_used++];
-  cudaEventRecord(*a, st);
+  *a = prof_event(e);
+  if (*a) cudaEventRecord(*a, st);
 }
 void prof_end(orca_engine *e, cudaStream_t st, cudaEvent_t a, int cls, double flops, double bytes) {
   if (!e->prof || !a) return;
-  cudaEvent_t b = e->ev_pool[e->ev_used++];
+  cudaEvent_t b = prof_event(e);
+  if (!b) {
+    e->ev_free.push_back(a);
+    return;
+  }
   cudaEventRecord(b, st);
-  e->pending.push_back({cls, a, b, flops, bytes});
+  e->pending.push_back({e->cur_slot, cls, a, b, flops, bytes});
 }
-void prof_collect(orca_engine *e) {
+// Add the launches of in-flight slot k (now complete) to the statistics.
+void prof_collect(orca_engine *e, int k) {
+  std::vector<orca_engine::Pending> keep;
   for (auto &p : e->pending) {
+    if (p.slot != k) {
+      keep.push_back(p);
+      continue;
+    }
     float ms = 0.f;
     if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
       auto &s = e->stats[p.cls];
@@ -385,9 +417,10 @@ void prof_collect(orca_engine *e) {
       s.flops += p.flops;
       s.bytes += p.bytes;
     }
+    e->ev_free.push_back(p.a);
+    e->ev_free.push_back(p.b);
   }
-  e->pending.clear();
-  e->ev_used = 0;
+  e->pending.swap(keep);
 }
 
 
@@ -403,17 +436,17 @@ struct FwdSizes {
 // graph = true: every kernel reads its sizes from the device header and
 // grids are fixed (the sequence is being captured into a CUDA graph);
 // otherwise sizes are passed by value.  Profiling events only when eager.
-int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *logits, bool graph) {
+int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *logits, bool graph, int k) {
   const orca_config &c = e->cfg;
   const int H = c.hidden, F = c.ffn, V = c.vocab, nh = c.n_heads, D = e->head_dim;
   const bool bf16 = c.dtype == ORCA_DTYPE_BF16;
   const size_t eb = elem_bytes(c.dtype);
   const Layout &Ly = e->lay;
-  DevHeader *d_hdr = ws_ptr<DevHeader>(e, Ly.req);
+  DevHeader *d_hdr = ws_ptr<DevHeader>(e, Ly.req[k]);
   ReqInfo *d_req = reinterpret_cast<ReqInfo *>(d_hdr + 1);
-  RowInfo *d_row = ws_ptr<RowInfo>(e, Ly.row);
-  AttnWork *d_work = ws_ptr<AttnWork>(e, Ly.work);
-  unsigned long long *d_out = ws_ptr<unsigned long long>(e, Ly.out);
+  RowInfo *d_row = ws_ptr<RowInfo>(e, Ly.row[k]);
+  AttnWork *d_work = ws_ptr<AttnWork>(e, Ly.work[k]);
+  unsigned long long *d_out = ws_ptr<unsigned long long>(e, Ly.out[k]);
   int32_t *status = reinterpret_cast<int32_t *>(d_out);
   unsigned long long *d_keys = d_out + 1;
   GemmScratch scr{ws_ptr<float>(e, Ly.gemm_part), kGemmPartialBytes, ws_ptr<int32_t>(e, Ly.gemm_cnt),
@@ -493,7 +526,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
       TcAttnArgs ta{};
       ta.out = h;
       ta.reqs = d_req;
-      ta.work = ws_ptr<AttnWork>(e, Ly.work_tc);
+      ta.work = ws_ptr<AttnWork>(e, Ly.work_tc[k]);
       ta.ticket = aa.ticket + 2;
       ta.status = status;
       ta.hidden = H;
@@ -653,21 +686,25 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
   if (cudaGetDevice(&dev) != cudaSuccess) { delete e; return ORCA_ECUDA; }
   e->device = dev;
   const auto &L = e->lay;
-  bool ok = cudaHostAlloc(&e->h_hdr, sizeof(DevHeader) + sizeof(ReqInfo) * cfg->max_bs, cudaHostAllocDefault) ==
-                cudaSuccess &&
-            cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaHostAlloc(&e->h_row, sizeof(RowInfo) * cfg->max_rows, cudaHostAllocDefault) == cudaSuccess &&
-            cudaHostAlloc(&e->h_work, sizeof(AttnWork) * L.max_work, cudaHostAllocDefault) == cudaSuccess &&
-            cudaHostAlloc(&e->h_work_tc, sizeof(AttnWork) * max_tc_work(cfg->max_bs, cfg->max_rows),
-                          cudaHostAllocDefault) == cudaSuccess &&
-            cudaHostAlloc(&e->h_out, sizeof(unsigned long long) * (cfg->max_bs + 1), cudaHostAllocDefault) == cudaSuccess;
-  ok = ok && cudaMemset(e->ws + L.counters, 0, ((size_t)cfg->max_bs * cfg->n_heads + 4) * 4) == cudaSuccess &&
-       cudaMemset(e->ws + L.out, 0, 8) == cudaSuccess && cudaMemset(e->ws + L.gemm_cnt, 0, kGemmMaxSms * 4) == cudaSuccess &&
-       cudaDeviceSynchronize() == cudaSuccess;
-  if (ok) {
-    e->h_req = reinterpret_cast<ReqInfo *>(e->h_hdr + 1);
-    ok = gemm_prepare() == cudaSuccess && attention_prepare() == cudaSuccess && attention_tc_prepare() == cudaSuccess;
+  bool ok = cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
+  for (int k = 0; k < kMaxInflight && ok; ++k) {
+    orca_engine::IterSlot &S = e->slot[k];
+    ok = cudaHostAlloc(&S.h_hdr, sizeof(DevHeader) + sizeof(ReqInfo) * cfg->max_bs, cudaHostAllocDefault) ==
+             cudaSuccess &&
+         cudaHostAlloc(&S.h_row, sizeof(RowInfo) * cfg->max_rows, cudaHostAllocDefault) == cudaSuccess &&
+         cudaHostAlloc(&S.h_work, sizeof(AttnWork) * L.max_work, cudaHostAllocDefault) == cudaSuccess &&
+         cudaHostAlloc(&S.h_work_tc, sizeof(AttnWork) * max_tc_work(cfg->max_bs, cfg->max_rows),
+                       cudaHostAllocDefault) == cudaSuccess &&
+         cudaHostAlloc(&S.h_out, sizeof(unsigned long long) * (cfg->max_bs + 1), cudaHostAllocDefault) ==
+             cudaSuccess &&
+         cudaEventCreateWithFlags(&S.done, cudaEventDisableTiming) == cudaSuccess &&
+         cudaMemset(e->ws + L.out[k], 0, 8) == cudaSuccess;
+    if (ok) S.h_req = reinterpret_cast<ReqInfo *>(S.h_hdr + 1);
   }
+  ok = ok && cudaMemset(e->ws + L.counters, 0, ((size_t)cfg->max_bs * cfg->n_heads + 4) * 4) == cudaSuccess &&
+       cudaMemset(e->ws + L.gemm_cnt, 0, kGemmMaxSms * 4) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
+  if (ok)
+    ok = gemm_prepare() == cudaSuccess && attention_prepare() == cudaSuccess && attention_tc_prepare() == cudaSuccess;
   if (!ok) {
     orca_engine_destroy(e);
     return ORCA_ECUDA;
@@ -713,12 +750,16 @@ int orca_engine_destroy(orca_engine *e) {
   if (!e->host_only) {
     for (auto &g : e->graphs) cudaGraphExecDestroy(g.second.exec);
     if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
-    cudaFreeHost(e->h_hdr);
-    cudaFreeHost(e->h_row);
-    cudaFreeHost(e->h_work);
-    cudaFreeHost(e->h_work_tc);
-    cudaFreeHost(e->h_out);
-    for (auto ev : e->ev_pool) cudaEventDestroy(ev);
+    for (auto &S : e->slot) {
+      if (S.done) cudaEventSynchronize(S.done);
+      cudaFreeHost(S.h_hdr);
+      cudaFreeHost(S.h_row);
+      cudaFreeHost(S.h_work);
+      cudaFreeHost(S.h_work_tc);
+      cudaFreeHost(S.h_out);
+      if (S.done) cudaEventDestroy(S.done);
+    }
+    for (auto ev : e->ev_all) cudaEventDestroy(ev);
   }
   delete e;
   return ORCA_OK;
@@ -878,18 +919,26 @@ int orca_select_batch_budget(orca_engine *e, orca_request *pool, int32_t n_pool,
   return ORCA_OK;
 }
 
-int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx, int32_t n_batch, int32_t flags,
-                   int32_t *next_tokens, float *logits_dev, void *stream) {
+int orca_iteration_submit(orca_engine *e, orca_request *pool, const int32_t *batch_idx, int32_t n_batch,
+                          int32_t flags, float *logits_dev, void *stream) {
   if (!e) return ORCA_EINVAL;
   if (e->host_only) return fail(e, ORCA_ESTATE, "host-only engine has no device side");
   const orca_config &c = e->cfg;
   if (n_batch <= 0) return fail(e, ORCA_EINVAL, "empty batch");
   if (n_batch > c.max_bs) return fail(e, ORCA_EBATCH, "n_batch %d > max_bs %d", n_batch, c.max_bs);
-  if (!pool || !batch_idx || !next_tokens) return fail(e, ORCA_EINVAL, "NULL argument");
+  if (!pool || !batch_idx) return fail(e, ORCA_EINVAL, "NULL argument");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int H = c.hidden, F = c.ffn, V = c.vocab, nh = c.n_heads, D = e->head_dim;
+  if (e->q_len == kMaxInflight) return fail(e, ORCA_ESTATE, "%d iterations already in flight", kMaxInflight);
+  if (e->q_len > 0 && e->slot[e->q_head].st != st)
+    return fail(e, ORCA_EINVAL, "iterations in flight together must use one stream");
+  for (int j = 0; j < e->q_len && logits_dev; ++j)
+    if (e->slot[(e->q_head + j) % kMaxInflight].logits == logits_dev)
+      return fail(e, ORCA_EINVAL, "iterations in flight together need distinct logits buffers");
+  const int k = (e->q_head + e->q_len) % kMaxInflight;
+  orca_engine::IterSlot &S = e->slot[k];
+  e->cur_slot = k;
+  const int H = c.hidden, F = c.ffn, V = c.vocab, nh = c.n_heads;
   const bool bf16 = c.dtype == ORCA_DTYPE_BF16;
-  const size_t eb = elem_bytes(c.dtype);
 
   // ---- ragged descriptor (host): rows in batch order, Figure 5
   std::vector<int32_t> L(n_batch);
@@ -911,6 +960,12 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
                   (long long)r.req_id, (long long)end);
     if (r.slot_base + cap > c.n_slots)
       return fail(e, ORCA_EINVAL, "request %lld: slots beyond n_slots", (long long)r.req_id);
+    for (int j = 0; j < e->q_len; ++j) {  // a request is in at most one batch in flight
+      const orca_engine::IterSlot &O = e->slot[(e->q_head + j) % kMaxInflight];
+      for (int32_t x : O.idx)
+        if (O.pool == pool && x == batch_idx[i])
+          return fail(e, ORCA_EINVAL, "request %lld is already in an iteration in flight", (long long)r.req_id);
+    }
     N += L[i];
     if (N > c.max_rows) return fail(e, ORCA_EBATCH, "sum L_i > max_rows %d", c.max_rows);
     if (L[i] == 1) {
@@ -923,21 +978,21 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
   int32_t row = 0;
   for (int32_t i = 0; i < n_batch; ++i) {
     const orca_request &r = pool[batch_idx[i]];
-    e->h_req[i] = {row, L[i], r.n_cached, (int32_t)r.slot_base};
+    S.h_req[i] = {row, L[i], r.n_cached, (int32_t)r.slot_base};
     for (int32_t j = 0; j < L[i]; ++j) {
       const int32_t pos = r.n_cached + j;
       const int32_t tok = r.tokens[pos];
       if (tok < 0 || tok >= V) return fail(e, ORCA_EINVAL, "token id %d out of range", tok);
-      e->h_row[row + j] = {tok, pos, i, (int32_t)(r.slot_base + pos)};
+      S.h_row[row + j] = {tok, pos, i, (int32_t)(r.slot_base + pos)};
     }
     if (e->attn_tc && L[i] >= kTcMinRows)
-      n_work_tc = append_tc_work(e->h_work_tc, n_work_tc, i, row, L[i]);
+      n_work_tc = append_tc_work(S.h_work_tc, n_work_tc, i, row, L[i]);
     else
-      n_work = append_attn_work(e->h_work, n_work, i, row, L[i], r.n_cached, split);
+      n_work = append_attn_work(S.h_work, n_work, i, row, L[i], r.n_cached, split);
     row += L[i];
   }
-  order_attn_work(e->h_work, n_work, e->h_req, split);
-  if (order_tc_work(e->h_work_tc, n_work_tc, e->h_req))
+  order_attn_work(S.h_work, n_work, S.h_req, split);
+  if (order_tc_work(S.h_work_tc, n_work_tc, S.h_req))
     return fail(e, ORCA_EBATCH, "a prompt has more than 1023 query tiles");
   // host copy for orca_last_descriptor / orca_last_transfer
   e->last_B = n_batch;
@@ -955,25 +1010,24 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
   e->last_row_pos.resize(N);
   e->last_row_slot.resize(N);
   for (int32_t r = 0; r < N; ++r) {
-    e->last_row_pos[r] = e->h_row[r].pos;
-    e->last_row_slot[r] = e->h_row[r].slot;
+    e->last_row_pos[r] = S.h_row[r].pos;
+    e->last_row_slot[r] = S.h_row[r].slot;
   }
 
   // ---- device work, all on `st`
   CUDA_TRY(e, cudaSetDevice(e->device));
   const Layout &Ly = e->lay;
-  DevHeader *d_hdr = ws_ptr<DevHeader>(e, Ly.req);
-  RowInfo *d_row = ws_ptr<RowInfo>(e, Ly.row);
-  AttnWork *d_work = ws_ptr<AttnWork>(e, Ly.work);
-  unsigned long long *d_out = ws_ptr<unsigned long long>(e, Ly.out);
-  int32_t *status = reinterpret_cast<int32_t *>(d_out);
-  *e->h_hdr = DevHeader{N, n_batch, n_work, split, n_work_tc, {0, 0, 0}};
-  CUDA_TRY(e, cudaMemcpyAsync(d_hdr, e->h_hdr, sizeof(DevHeader) + sizeof(ReqInfo) * n_batch, cudaMemcpyHostToDevice, st));
-  CUDA_TRY(e, cudaMemcpyAsync(d_row, e->h_row, sizeof(RowInfo) * N, cudaMemcpyHostToDevice, st));
+  DevHeader *d_hdr = ws_ptr<DevHeader>(e, Ly.req[k]);
+  RowInfo *d_row = ws_ptr<RowInfo>(e, Ly.row[k]);
+  AttnWork *d_work = ws_ptr<AttnWork>(e, Ly.work[k]);
+  unsigned long long *d_out = ws_ptr<unsigned long long>(e, Ly.out[k]);
+  *S.h_hdr = DevHeader{N, n_batch, n_work, split, n_work_tc, {0, 0, 0}};
+  CUDA_TRY(e, cudaMemcpyAsync(d_hdr, S.h_hdr, sizeof(DevHeader) + sizeof(ReqInfo) * n_batch, cudaMemcpyHostToDevice, st));
+  CUDA_TRY(e, cudaMemcpyAsync(d_row, S.h_row, sizeof(RowInfo) * N, cudaMemcpyHostToDevice, st));
   if (n_work > 0)
-    CUDA_TRY(e, cudaMemcpyAsync(d_work, e->h_work, sizeof(AttnWork) * n_work, cudaMemcpyHostToDevice, st));
+    CUDA_TRY(e, cudaMemcpyAsync(d_work, S.h_work, sizeof(AttnWork) * n_work, cudaMemcpyHostToDevice, st));
   if (n_work_tc > 0)
-    CUDA_TRY(e, cudaMemcpyAsync(ws_ptr<AttnWork>(e, Ly.work_tc), e->h_work_tc, sizeof(AttnWork) * n_work_tc,
+    CUDA_TRY(e, cudaMemcpyAsync(ws_ptr<AttnWork>(e, Ly.work_tc[k]), S.h_work_tc, sizeof(AttnWork) * n_work_tc,
                                 cudaMemcpyHostToDevice, st));
 
   FwdSizes z{N, n_batch, n_work, split, n_work_tc, 0.0, 0.0};
@@ -988,16 +1042,16 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
   const bool use_graph = bf16 && !e->prof && !(flags & ORCA_ITER_EAGER);
   if (use_graph) {
     auto code = [](int bn) { return (uint32_t)(bn == 256 ? 3 : bn == 128 ? 2 : bn == 64 ? 1 : 0); };
-    // graphs differ in their GEMM tile choices and in whether the tensor-core
-    // prompt attention runs at all
+    // graphs differ in their GEMM tile choices, in whether the tensor-core
+    // prompt attention runs at all, and in the in-flight slot they read
     const uint32_t key = code(gemm_tile_n(N, 3 * H)) | (code(gemm_tile_n(N, H)) << 2) |
                          (code(gemm_tile_n(N, F)) << 4) | (code(gemm_tile_n(n_batch, V)) << 6) |
-                         ((uint32_t)(n_work_tc > 0) << 8);
+                         ((uint32_t)(n_work_tc > 0) << 8) | ((uint32_t)k << 9);
     const auto gk = std::make_pair(key, reinterpret_cast<uintptr_t>(logits));
     auto it = e->graphs.find(gk);
     if (it == e->graphs.end()) {
       CUDA_TRY(e, cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal));
-      const int rc = enqueue_forward(e, e->cap_stream, z, logits, true);
+      const int rc = enqueue_forward(e, e->cap_stream, z, logits, true, k);
       cudaGraph_t g = nullptr;
       const cudaError_t ce = cudaStreamEndCapture(e->cap_stream, &g);
       if (rc) {
@@ -1010,9 +1064,9 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
       if (cudaGraphGetNodes(g, nullptr, &n_nodes) == cudaSuccess && n_nodes > 0) {
         std::vector<cudaGraphNode_t> nodes(n_nodes);
         if (cudaGraphGetNodes(g, nodes.data(), &n_nodes) == cudaSuccess)
-          for (size_t k = 0; k < n_nodes; ++k) {
+          for (size_t q = 0; q < n_nodes; ++q) {
             cudaGraphNodeType t;
-            if (cudaGraphNodeGetType(nodes[k], &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++n_kernels;
+            if (cudaGraphNodeGetType(nodes[q], &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++n_kernels;
           }
       }
       cudaGraphExec_t ex = nullptr;
@@ -1025,44 +1079,77 @@ int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx,
     e->last_launches = it->second.n_kernels;
   } else {
     e->n_launch = 0;
-    const int rc = enqueue_forward(e, st, z, logits, false);
+    const int rc = enqueue_forward(e, st, z, logits, false, k);
     if (rc) return rc;
     e->last_launches = e->n_launch;
   }
-  CUDA_TRY(e, cudaMemcpyAsync(e->h_out, d_out, sizeof(unsigned long long) * (n_batch + 1), cudaMemcpyDeviceToHost, st));
-  CUDA_TRY(e, cudaStreamSynchronize(st));
-  if (e->prof) prof_collect(e);
-  const int32_t dev_status = (int32_t)(e->h_out[0] & 0xFFFFFFFFull);
+  CUDA_TRY(e, cudaMemcpyAsync(S.h_out, d_out, sizeof(unsigned long long) * (n_batch + 1), cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(e, cudaEventRecord(S.done, st));
+  S.pool = pool;
+  S.logits = logits_dev;
+  S.st = st;
+  S.flags = flags;
+  S.n_batch = n_batch;
+  S.idx.assign(batch_idx, batch_idx + n_batch);
+  S.L = std::move(L);
+  ++e->q_len;
+  return ORCA_OK;
+}
+
+int orca_iteration_wait(orca_engine *e, int32_t *n_batch, int32_t *batch_idx, int32_t *next_tokens) {
+  if (!e) return ORCA_EINVAL;
+  if (e->q_len == 0) return fail(e, ORCA_ESTATE, "no iteration in flight");
+  const int k = e->q_head;
+  orca_engine::IterSlot &S = e->slot[k];
+  const int V = e->cfg.vocab;
+  // the oldest iteration leaves the queue whatever its outcome
+  e->q_head = (e->q_head + 1) % kMaxInflight;
+  --e->q_len;
+  if (n_batch) *n_batch = S.n_batch;
+  if (batch_idx) std::copy(S.idx.begin(), S.idx.end(), batch_idx);
+  CUDA_TRY(e, cudaEventSynchronize(S.done));
+  if (e->prof) prof_collect(e, k);
+  const int32_t dev_status = (int32_t)(S.h_out[0] & 0xFFFFFFFFull);
   if (dev_status != 0) {
-    const int code = dev_status;
-    cudaMemsetAsync(status, 0, 4, st);
-    cudaStreamSynchronize(st);
-    return fail(e, ORCA_EDEVICE, "device status word 0x%x (1 wait timeout, 2 bad index, 4 bad shape)", code);
+    int32_t *status = ws_ptr<int32_t>(e, e->lay.out[k]);
+    cudaMemsetAsync(status, 0, 4, S.st);
+    cudaStreamSynchronize(S.st);
+    return fail(e, ORCA_EDEVICE, "device status word 0x%x (1 wait timeout, 2 bad index, 4 bad shape)", dev_status);
   }
-  // ---- Algorithm 1 main loop: returned requests become INCREMENT; finished ones release their slots
-  for (int32_t i = 0; i < n_batch; ++i) {
-    const int32_t tok = argmax_key_col(e->h_out[1 + i]);
+  for (int32_t i = 0; i < S.n_batch; ++i) {
+    const int32_t tok = argmax_key_col(S.h_out[1 + i]);
     if (tok < 0 || tok >= V) return fail(e, ORCA_EDEVICE, "argmax produced no token (NaN logits?)");
   }
-  for (int32_t i = 0; i < n_batch; ++i) {
-    orca_request &r = pool[batch_idx[i]];
-    const int32_t tok = argmax_key_col(e->h_out[1 + i]);
+  // ---- Algorithm 1 main loop: returned requests become INCREMENT; finished ones release their slots
+  for (int32_t i = 0; i < S.n_batch; ++i) {
+    orca_request &r = S.pool[S.idx[i]];
+    const int32_t tok = argmax_key_col(S.h_out[1 + i]);
     r.state = ORCA_INCREMENT;
     r.n_sched = 0;
-    r.n_cached += L[i];
+    r.n_cached += S.L[i];
     if (r.n_cached < r.n_prompt) {  // a prompt chunk: the prompt is not complete yet, nothing generated
-      next_tokens[i] = -1;
+      if (next_tokens) next_tokens[i] = -1;
       continue;
     }
-    next_tokens[i] = tok;
+    if (next_tokens) next_tokens[i] = tok;
     r.n_generated += 1;
-    if (!(flags & ORCA_ITER_TEACHER_FORCE)) r.tokens[r.n_prompt + r.n_generated - 1] = tok;
+    if (!(S.flags & ORCA_ITER_TEACHER_FORCE)) r.tokens[r.n_prompt + r.n_generated - 1] = tok;
     if (r.n_generated >= r.out_len || r.n_prompt + r.n_generated >= r.max_tokens) {
       r.state = ORCA_FINISHED;
       e->slots.release(r.req_id);
     }
   }
   return ORCA_OK;
+}
+
+int orca_iteration(orca_engine *e, orca_request *pool, const int32_t *batch_idx, int32_t n_batch, int32_t flags,
+                   int32_t *next_tokens, float *logits_dev, void *stream) {
+  if (!e) return ORCA_EINVAL;
+  if (!next_tokens) return fail(e, ORCA_EINVAL, "NULL argument");
+  if (e->q_len > 0) return fail(e, ORCA_ESTATE, "iterations in flight: use orca_iteration_wait");
+  const int rc = orca_iteration_submit(e, pool, batch_idx, n_batch, flags, logits_dev, stream);
+  if (rc) return rc;
+  return orca_iteration_wait(e, nullptr, nullptr, next_tokens);
 }
 
 int orca_last_descriptor(const orca_engine *e, int32_t *n_batch, int32_t *n_rows, int32_t *row_off, int32_t *row_pos,
@@ -1277,8 +1364,11 @@ int orca_profile_enable(orca_engine *e, int32_t enable) {
   if (e->host_only && enable) return ORCA_ESTATE;
   e->prof = enable != 0;
   for (auto &s : e->stats) s = orca_kernel_stats{};
+  for (auto &p : e->pending) {  // launches still in flight are not counted
+    e->ev_free.push_back(p.a);
+    e->ev_free.push_back(p.b);
+  }
   e->pending.clear();
-  e->ev_used = 0;
   return ORCA_OK;
 }
 

@@ -168,16 +168,25 @@ class IterRecord:
 
 
 class ServingLoop:
-    """Iteration-level scheduling over a RequestPool (Algorithm 1, one worker).
+    """Iteration-level scheduling over a RequestPool (Algorithm 1).
 
     Arrivals are iteration indices: a request whose arrival is t can be
-    selected at iteration t.  When nothing has arrived the clock jumps to the
-    next arrival.  step() runs one iteration and returns its record."""
+    selected at iteration t.  n_workers batches may be scheduled at once
+    (Algorithm 1's main loop; on one GPU the host selects and enqueues the
+    next batch while the previous one runs): the requests of a batch in
+    flight are RUNNING and the next Select skips them; once n_workers
+    batches are in flight, or when nothing else can be selected, the oldest
+    is waited for.  When nothing has arrived the clock jumps to the next
+    arrival.  step() returns the record of the next iteration to complete,
+    in scheduling order."""
 
     def __init__(self, engine: Engine, pool: RequestPool, teacher_force: bool = False, keep_logits: bool = False,
                  stream: Optional[torch.cuda.Stream] = None, keep_ids: Optional[set] = None, eager: bool = False,
-                 token_budget: Optional[int] = None, chunk: Optional[int] = None):
+                 token_budget: Optional[int] = None, chunk: Optional[int] = None, n_workers: int = 1):
+        if n_workers not in (1, 2):
+            raise ValueError("n_workers must be 1 or 2")
         self.eng, self.pool = engine, pool
+        self.n_workers = n_workers
         self.flags = (C.ORCA_ITER_TEACHER_FORCE if teacher_force else 0) | (C.ORCA_ITER_EAGER if eager else 0)
         keep_logits = keep_logits or keep_ids is not None
         self.keep_logits = keep_logits
@@ -187,8 +196,9 @@ class ServingLoop:
         self.next_tok = (ctypes.c_int32 * engine.max_bs)()
         self._bi = np.frombuffer(self.batch_idx, dtype=np.int32)
         self._nt = np.frombuffer(self.next_tok, dtype=np.int32)
-        self.logits = (torch.empty((engine.max_bs, engine.shape.vocab), dtype=torch.float32, device=engine.device)
-                       if keep_logits else None)
+        # one logits buffer per iteration that can be in flight
+        self.logits = ([torch.empty((engine.max_bs, engine.shape.vocab), dtype=torch.float32, device=engine.device)
+                        for _ in range(n_workers)] if keep_logits else None)
         # chunked prefill under a per-iteration token budget (None: plain Algorithm 1)
         self.budget = None
         if token_budget is not None or chunk is not None:
@@ -197,56 +207,70 @@ class ServingLoop:
         self.it = 0
         self.n_arrived = 0
         self.n_done = 0
-        # host seconds spent before / inside / after orca_iteration (diagnostics)
+        self.n_submitted = 0
+        self.inflight: List[tuple] = []   # (record, pool indices, logits buffer), oldest first
+        # host seconds spent selecting / submitting / completing (diagnostics)
         self.t_pre = self.t_call = self.t_post = 0.0
 
     def done(self) -> bool:
-        return self.n_done >= self.pool.n
+        return self.n_done >= self.pool.n and not self.inflight
 
-    def step(self) -> Optional[IterRecord]:
+    def _complete(self) -> IterRecord:
         t0 = time.perf_counter()
-        P = self.pool
-        unfinished_arrived = self.n_arrived - self.n_done
-        if unfinished_arrived == 0 and self.n_arrived < P.n and P.arrivals[self.n_arrived] > self.it:
-            self.it = int(P.arrivals[self.n_arrived])
-        if self.n_arrived < P.n and P.arrivals[self.n_arrived] <= self.it:
-            self.n_arrived = int(np.searchsorted(P.arrivals, self.it, side="right"))
-        if self.budget is None:
-            nb = C.orca_select_batch(self.eng.handle, P.arr, self.n_arrived, self.batch_idx)
-        else:
-            nb = C.orca_select_batch_budget(self.eng.handle, P.arr, self.n_arrived, self.budget[0], self.budget[1],
-                                            self.batch_idx)
-        if nb == 0:
-            raise RuntimeError(f"no request can be scheduled at iteration {self.it}")
-        idx = self._bi[:nb].copy()
-        sel = P.view[idx]
-        rec = IterRecord(self.it, sel["req_id"].tolist(), sel["n_sched"].tolist(), sel["n_cached"].tolist(),
-                         sel["slot_base"].tolist(), [], [])
-        lp = self.logits.data_ptr() if self.logits is not None else 0
+        rec, idx, lg = self.inflight.pop(0)
+        nb = C.orca_iteration_wait(self.eng.handle, self.batch_idx, self.next_tok)
         t1 = time.perf_counter()
-        C.orca_iteration(self.eng.handle, P.arr, self.batch_idx, nb, self.flags, self.next_tok, lp,
-                         self.stream.cuda_stream)
-        t2 = time.perf_counter()
         rec.next_tokens = self._nt[:nb].tolist()
-        rec.launches = C.orca_last_launches(self.eng.handle)
+        P = self.pool
         done = P.view["state"][idx] == C.ORCA_FINISHED
         if done.any():
-            rec.released = sel["req_id"][done].tolist()
+            rec.released = P.view["req_id"][idx][done].tolist()
             self.n_done += int(done.sum())
-        if self.logits is not None:
+        if lg is not None:
             if self.keep_ids is None:
-                rec.logits = self.logits[:nb].cpu().numpy()
+                rec.logits = lg[:nb].cpu().numpy()
             else:
                 rows = [k for k, rid in enumerate(rec.req_ids) if rid in self.keep_ids]
                 if rows:
-                    sel_l = self.logits[torch.tensor(rows, device=self.logits.device)].cpu().numpy()
+                    sel_l = lg[torch.tensor(rows, device=lg.device)].cpu().numpy()
                     rec.logits = {rec.req_ids[k]: sel_l[j] for j, k in enumerate(rows)}
-        self.it += 1
-        t3 = time.perf_counter()
-        self.t_pre += t1 - t0
-        self.t_call += t2 - t1
-        self.t_post += t3 - t2
+        self.t_call += t1 - t0
+        self.t_post += time.perf_counter() - t1
         return rec
+
+    def step(self) -> Optional[IterRecord]:
+        P = self.pool
+        while True:
+            t0 = time.perf_counter()
+            if self.n_arrived < P.n and P.arrivals[self.n_arrived] <= self.it:
+                self.n_arrived = int(np.searchsorted(P.arrivals, self.it, side="right"))
+            if self.budget is None:
+                nb = C.orca_select_batch(self.eng.handle, P.arr, self.n_arrived, self.batch_idx)
+            else:
+                nb = C.orca_select_batch_budget(self.eng.handle, P.arr, self.n_arrived, self.budget[0],
+                                                self.budget[1], self.batch_idx)
+            if nb > 0:
+                idx = self._bi[:nb].copy()
+                sel = P.view[idx]
+                rec = IterRecord(self.it, sel["req_id"].tolist(), sel["n_sched"].tolist(), sel["n_cached"].tolist(),
+                                 sel["slot_base"].tolist(), [], [])
+                lg = self.logits[self.n_submitted % self.n_workers] if self.logits is not None else None
+                t1 = time.perf_counter()
+                C.orca_iteration_submit(self.eng.handle, P.arr, self.batch_idx, nb, self.flags,
+                                        lg.data_ptr() if lg is not None else 0, self.stream.cuda_stream)
+                rec.launches = C.orca_last_launches(self.eng.handle)
+                self.inflight.append((rec, idx, lg))
+                self.n_submitted += 1
+                self.it += 1
+                self.t_pre += t1 - t0
+                self.t_call += time.perf_counter() - t1
+            if self.inflight and (len(self.inflight) == self.n_workers or nb == 0):
+                return self._complete()
+            if nb == 0:
+                if self.n_arrived - self.n_done == 0 and self.n_arrived < P.n:
+                    self.it = int(P.arrivals[self.n_arrived])   # idle: jump to the next arrival
+                    continue
+                raise RuntimeError(f"no request can be scheduled at iteration {self.it}")
 
     def run(self, max_iters: int = 10_000_000) -> List[IterRecord]:
         recs = []

@@ -183,7 +183,7 @@ class IterRecord:
 
 def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
                  token_budget: Optional[int] = None, chunk: Optional[int] = None,
-                 policy: int = RESERVE_MAX) -> List[IterRecord]:
+                 policy: int = RESERVE_MAX, n_workers: int = 1) -> List[IterRecord]:
     """Drive Algorithm 1 over a trace whose arrivals are iteration indices.
 
     A request whose arrival is t can be selected at iteration t.  When no
@@ -191,7 +191,16 @@ def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
     is run).  Raises RuntimeError if the pool is non-empty but nothing can
     ever be selected (a head request larger than n_slots).  With a token
     budget or a chunk size the batch comes from select_budget: a prompt
-    chunk that leaves part of the prompt unprocessed generates no token."""
+    chunk that leaves part of the prompt unprocessed generates no token.
+
+    n_workers: batches kept scheduled at once (Algorithm 1's main loop:
+    select and schedule a batch, count it, and once n_workers batches are
+    scheduled wait for the oldest to return before selecting again).  The
+    requests of a scheduled batch are RUNNING, so the next Select skips
+    them.  Readings: the clock counts scheduled batches; a Select that finds
+    nothing to run does not schedule an empty batch, it waits for the
+    oldest batch in flight instead (or, with none in flight, the clock jumps
+    to the next arrival).  Records are in scheduling order."""
     order = sorted(trace, key=lambda r: (r.arrival, r.req_id))
     states = [ReqState(r.req_id, r.arrival, r.n_prompt, r.out_len, r.max_tokens) for r in order]
     slots = SlotPool(n_slots)
@@ -199,11 +208,10 @@ def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
     nxt = 0
     it = 0
     records: List[IterRecord] = []
+    inflight: List[Tuple[IterRecord, List[Tuple[ReqState, int]]]] = []
     budgeted = token_budget is not None or chunk is not None
     big = 2 ** 31 - 1
     while nxt < len(states) or pool:
-        if not pool and states[nxt].arrival > it:
-            it = states[nxt].arrival
         while nxt < len(states) and states[nxt].arrival <= it:
             pool.append(states[nxt])
             nxt += 1
@@ -212,28 +220,34 @@ def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
         else:
             sel = [(r, default_rows(r)) for r in select(pool, slots, max_bs, policy)]
         run = [(r, n) for r, n in sel if n > 0]
-        if not run:
-            raise RuntimeError(f"no request can be scheduled at iteration {it}")
         for r, n in sel:
             if n == 0:
                 r.state = INCREMENT  # admitted (slots reserved) but idle this iteration
-        rec = IterRecord(it, [r.req_id for r, _ in run], [n for _, n in run], [r.n_cached for r, _ in run],
-                         [r.slot_base for r, _ in run], [])
-        for r, _ in run:
-            r.state = RUNNING
-        for r, n in run:
-            r.state = INCREMENT
-            r.n_cached += n
-            if r.n_cached < r.n_prompt:
-                continue  # a prompt chunk: nothing generated yet
-            r.n_generated += 1
-            if finished(r):
-                r.state = FINISHED
-                slots.release(r.req_id)
-                rec.released.append(r.req_id)
-        pool = [r for r in pool if r.state != FINISHED]
-        records.append(rec)
-        it += 1
-        if len(records) > max_iters:
-            raise RuntimeError("iteration limit")
+        if run:
+            rec = IterRecord(it, [r.req_id for r, _ in run], [n for _, n in run], [r.n_cached for r, _ in run],
+                             [r.slot_base for r, _ in run], [])
+            for r, _ in run:
+                r.state = RUNNING
+            inflight.append((rec, run))
+            records.append(rec)
+            it += 1
+            if len(records) > max_iters:
+                raise RuntimeError("iteration limit")
+        if inflight and (len(inflight) == n_workers or not run):
+            rec, done_run = inflight.pop(0)
+            for r, n in done_run:
+                r.state = INCREMENT
+                r.n_cached += n
+                if r.n_cached < r.n_prompt:
+                    continue  # a prompt chunk: nothing generated yet
+                r.n_generated += 1
+                if finished(r):
+                    r.state = FINISHED
+                    slots.release(r.req_id)
+                    rec.released.append(r.req_id)
+            pool = [r for r in pool if r.state != FINISHED]
+        elif not run:
+            if pool:
+                raise RuntimeError(f"no request can be scheduled at iteration {it}")
+            it = states[nxt].arrival  # idle: the clock jumps to the next arrival
     return records

@@ -15,7 +15,7 @@ def max_rel_err(got, want):
 
 
 def run_gpu(shape, host_weights, trace, max_bs, n_slots, max_rows, teacher_force=False, keep_ids=None,
-            keep_all=False, eager=False, token_budget=None, chunk=None, reserve_policy=0):
+            keep_all=False, eager=False, token_budget=None, chunk=None, reserve_policy=0, n_workers=1):
     import torch
     from iteration_level_selective_gb300 import runtime as rt
     dev = torch.device("cuda:0")
@@ -24,15 +24,16 @@ def run_gpu(shape, host_weights, trace, max_bs, n_slots, max_rows, teacher_force
                     reserve_policy=reserve_policy)
     pool = rt.RequestPool(trace, teacher_force=teacher_force)
     loop = rt.ServingLoop(eng, pool, teacher_force=teacher_force, keep_logits=keep_all, keep_ids=keep_ids,
-                          eager=eager, token_budget=token_budget, chunk=chunk)
+                          eager=eager, token_budget=token_budget, chunk=chunk, n_workers=n_workers)
     recs = loop.run()
     return recs, eng, pool
 
 
-def compare_schedule(gpu_recs, trace, max_bs, n_slots, token_budget=None, chunk=None, reserve_policy=0):
+def compare_schedule(gpu_recs, trace, max_bs, n_slots, token_budget=None, chunk=None, reserve_policy=0,
+                     n_workers=1):
     """Integer record of every iteration, bit-exact against the oracle scheduler."""
     orecs = osched.run_schedule(trace, max_bs=max_bs, n_slots=n_slots, token_budget=token_budget, chunk=chunk,
-                                policy=reserve_policy)
+                                policy=reserve_policy, n_workers=n_workers)
     assert len(gpu_recs) == len(orecs)
     for g, o in zip(gpu_recs, orecs):
         assert (g.it, g.req_ids, g.n_new, g.n_ctx, g.slot_base, sorted(g.released)) == \

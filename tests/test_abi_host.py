@@ -77,6 +77,12 @@ def test_host_only_engine_reserve_release_errors(liborca):
         with pytest.raises(C.OrcaError) as ei:
             C.orca_iteration(eng, pool, bi, 1, 0, nt)
         assert ei.value.code == C.ORCA_ESTATE
+        with pytest.raises(C.OrcaError) as ei:
+            C.orca_iteration_submit(eng, pool, bi, 1, 0)
+        assert ei.value.code == C.ORCA_ESTATE
+        with pytest.raises(C.OrcaError) as ei:
+            C.orca_iteration_wait(eng, bi, nt)
+        assert ei.value.code == C.ORCA_ESTATE
     finally:
         C.orca_engine_destroy(eng)
 

@@ -268,6 +268,68 @@ def test_chunked_prefill_token_budget(cuda, which):
     assert worst < tol, worst
 
 
+# ------------------------------------------------------------------ two batches in flight
+
+@pytest.mark.parametrize("which", ["toy_fp32", "small_bf16"])
+def test_two_batches_in_flight(cuda, which):
+    """Algorithm 1 with n_workers = 2: the next batch is selected from the
+    requests not RUNNING and enqueued while the previous one runs.  The
+    integer record matches the oracle's two-worker schedule and every
+    request's logits equal its own generation (teacher forcing)."""
+    if which == "toy_fp32":
+        shape, w, tol = synth.TOY, _toy_weights(seed=13), FP32_TOL
+        trace = synth.make_trace(12, (1, 20), (1, 12), vocab=shape.vocab, seed=14, rate_per_iter=0.8, forced=True)
+        kw = dict(max_bs=4, n_slots=300, max_rows=64)
+    else:
+        shape, tol = SMALL_BF16, BF16_TOL
+        w = synth.make_weights(shape, seed=15, w_std=0.05, bias_std=0.02, ln_std=0.1)
+        trace = synth.make_trace(12, (1, 300), (1, 10), vocab=shape.vocab, seed=16, rate_per_iter=0.8, forced=True)
+        kw = dict(max_bs=6, n_slots=8000, max_rows=2048)
+    recs, eng, pool = hz.run_gpu(shape, w, trace, teacher_force=True, keep_all=True, n_workers=2, **kw)
+    hz.compare_schedule(recs, trace, max_bs=kw["max_bs"], n_slots=kw["n_slots"], n_workers=2)
+    got_lg = hz.gpu_logits_by_request(recs)
+    worst = 0.0
+    for req in trace:
+        _, logits = hz.oracle_generate(shape, w, req, teacher_force=True)
+        assert len(got_lg[req.req_id]) == len(logits)
+        for g, o in zip(got_lg[req.req_id], logits):
+            worst = max(worst, hz.max_rel_err(g, o))
+    assert worst < tol, worst
+
+
+def test_in_flight_limits(cuda):
+    """At most two iterations in flight, never sharing a request."""
+    import ctypes
+    from iteration_level_selective_gb300 import _orca as C
+    from iteration_level_selective_gb300 import runtime as rt
+    shape = synth.TOY
+    dw = rt.DeviceWeights(shape, cuda, host=_toy_weights())
+    eng = rt.Engine(shape, dw, max_bs=4, n_slots=200, max_rows=64, device=cuda)
+    trace = synth.make_trace(3, (2, 4), (3, 3), vocab=shape.vocab, seed=1)
+    pool = rt.RequestPool(trace)
+    st = torch.cuda.current_stream().cuda_stream
+    bi = (ctypes.c_int32 * 4)()
+    nt = (ctypes.c_int32 * 4)()
+    one = (ctypes.c_int32 * 1)
+    nb = C.orca_select_batch(eng.handle, pool.arr, 1, bi)   # request 0
+    C.orca_iteration_submit(eng.handle, pool.arr, one(0), 1, 0, 0, st)
+    with pytest.raises(C.OrcaError) as ei:                  # request 0 again while in flight
+        C.orca_iteration_submit(eng.handle, pool.arr, one(0), 1, 0, 0, st)
+    assert ei.value.code == C.ORCA_EINVAL
+    assert C.orca_select_batch(eng.handle, pool.arr, 3, bi) == 2   # requests 1 and 2
+    C.orca_iteration_submit(eng.handle, pool.arr, one(1), 1, 0, 0, st)
+    with pytest.raises(C.OrcaError) as ei:                  # a third in flight
+        C.orca_iteration_submit(eng.handle, pool.arr, one(2), 1, 0, 0, st)
+    assert ei.value.code == C.ORCA_ESTATE
+    with pytest.raises(C.OrcaError) as ei:                  # synchronous call while two are in flight
+        C.orca_iteration(eng.handle, pool.arr, one(2), 1, 0, nt)
+    assert ei.value.code == C.ORCA_ESTATE
+    assert C.orca_iteration_wait(eng.handle, bi, nt) == 1 and bi[0] == 0
+    assert C.orca_iteration_wait(eng.handle, bi, nt) == 1 and bi[0] == 1
+    assert pool.view["n_generated"].tolist() == [1, 1, 0] and nb == 1
+    eng.close()
+
+
 def test_graph_replay_equals_eager_launches(cuda):
     """The CUDA-graph replay (sizes read from the device descriptor, fixed
     grids) and eager launches run the same decompositions: identical logits

@@ -498,3 +498,44 @@ def test_policies_agree_when_memory_is_ample_and_stored_never_exceeds_reserved()
                 reserved, stored = scheduler.kv_usage(states, slots)
                 assert stored <= reserved <= slots.n_slots
             assert all(r.state == scheduler.FINISHED for r in states)
+
+
+# ---------------------------------------------------------------- batches in flight (Algorithm 1, n_workers = 2)
+
+def test_two_workers_by_hand():
+    # A, B, C arrive at 0 (prompt 1, 2 tokens each), max_bs 2.  Iteration 0
+    # schedules A, B; with one batch in flight the next Select sees only C;
+    # then the oldest batch returns and A, B are selectable again, and so on.
+    trace = [_R(0, 0, 1, 2, 3), _R(1, 0, 1, 2, 3), _R(2, 0, 1, 2, 3)]
+    recs = scheduler.run_schedule(trace, max_bs=2, n_slots=100, n_workers=2)
+    assert _records(recs) == [(0, [0, 1], [1, 1], [0, 0], []), (1, [2], [1], [0], []),
+                              (2, [0, 1], [1, 1], [1, 1], [0, 1]), (3, [2], [1], [1], [2])]
+    one = scheduler.run_schedule(trace, max_bs=2, n_slots=100, n_workers=1)
+    assert _records(one) == [(0, [0, 1], [1, 1], [0, 0], []), (1, [0, 1], [1, 1], [1, 1], [0, 1]),
+                             (2, [2], [1], [0], []), (3, [2], [1], [1], [2])]
+
+
+def test_two_workers_invariants_random_traces():
+    rng = np.random.default_rng(44)
+    for trial in range(30):
+        n = int(rng.integers(2, 30))
+        trace = []
+        for i in range(n):
+            lp, lo = int(rng.integers(1, 12)), int(rng.integers(1, 10))
+            trace.append(_R(i, int(rng.integers(0, 25)), lp, lo, lp + lo + int(rng.integers(0, 4))))
+        kw = dict(max_bs=int(rng.integers(1, 9)), n_slots=int(rng.integers(30, 150)))
+        if trial % 3 == 0:
+            kw.update(token_budget=int(rng.integers(1, 20)), chunk=int(rng.integers(1, 10)))
+        recs = scheduler.run_schedule(trace, n_workers=2, **kw)
+        prompt_done = {t.req_id: 0 for t in trace}
+        gen = {t.req_id: 0 for t in trace}
+        n_prompt = {t.req_id: t.n_prompt for t in trace}
+        for rec in recs:
+            for rid, L, c in zip(rec.req_ids, rec.n_new, rec.n_ctx):
+                if c < n_prompt[rid]:
+                    assert c == prompt_done[rid]
+                    prompt_done[rid] += L
+                if c + L >= n_prompt[rid]:
+                    gen[rid] += 1
+        assert prompt_done == n_prompt
+        assert all(gen[t.req_id] == t.out_len for t in trace)
