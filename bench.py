@@ -319,6 +319,8 @@ def run_ours(args, rank: int, world: int):
         weights = rt.DeviceWeights(shape, dev, host=host_w)
         del host_w
         n_slots = args.kv_slots if args.kv_slots else n_slots_for(shape)
+        if args.reserve == "paged":
+            n_slots -= n_slots % 32   # whole K/V blocks
         eng = rt.Engine(shape, weights, max_bs=64, n_slots=n_slots, max_rows=64 * 512, device=dev,
                         reserve_policy=rt.RESERVE_POLICIES[args.reserve])
         work = TraceWorkload(eng, rank, stream, args.token_budget, args.chunk, args.workers)
@@ -502,8 +504,9 @@ def main():
                     help="gpt2-trace only: prompt chunk size for chunked prefill")
     ap.add_argument("--workers", type=int, choices=[1, 2], default=1,
                     help="gpt2-trace only: batches in flight at once (Algorithm 1's n_workers)")
-    ap.add_argument("--reserve", choices=["max", "pow2", "oracle"], default="max",
-                    help="gpt2-trace only: K/V reservation policy (max_tokens, power of two, true length)")
+    ap.add_argument("--reserve", choices=["max", "pow2", "oracle", "paged"], default="max",
+                    help="gpt2-trace only: K/V reservation policy (max_tokens, power of two, true length) or "
+                         "paged K/V (32-slot blocks on demand, preemption of the latest arrival)")
     ap.add_argument("--kv-slots", type=int, default=0,
                     help="gpt2-trace only: K/V pool slots (default: 40 GB worth); the trace needs at most "
                          "64 x 768, so profiler captures use a small pool")

@@ -67,6 +67,8 @@ typedef struct orca_engine orca_engine;
 #define ORCA_RESERVE_MAX 0
 #define ORCA_RESERVE_POW2 1
 #define ORCA_RESERVE_ORACLE 2
+#define ORCA_RESERVE_PAGED 3
+#define ORCA_KV_BLOCK 32
 
 /* Model shape and scheduler parameters.
  *   GPT decoder: n_layers blocks of hidden size `hidden`, n_heads heads
@@ -81,7 +83,9 @@ typedef struct orca_engine orca_engine;
  *   Lecture 2, section 6.1): ORCA_RESERVE_MAX max_tokens (Orca's rule);
  *   ORCA_RESERVE_POW2 its true final length n_prompt + out_len rounded up to
  *   a power of two (a rough length prediction); ORCA_RESERVE_ORACLE the true
- *   final length; both capped at max_tokens.
+ *   final length; both capped at max_tokens.  ORCA_RESERVE_PAGED reserves
+ *   nothing: slots come in blocks of ORCA_KV_BLOCK as a request grows
+ *   (n_slots must be a multiple of ORCA_KV_BLOCK); see orca_select_batch.
  *   bf16 requires hidden % 64 == 0 and ffn % 64 == 0; every dtype requires
  *   head_dim in {16, 32, 64, 128}. */
 typedef struct {
@@ -209,6 +213,17 @@ int orca_kv_usage(const orca_engine *eng, const orca_request *pool, int32_t n_po
  * indices in batch order; *n_batch their count (0 is valid). */
 int orca_select_batch(orca_engine *eng, orca_request *pool, int32_t n_pool, int32_t *batch_idx,
                       int32_t *n_batch);
+/* With ORCA_RESERVE_PAGED (CS349D Lecture 2, sections 5.1 and 6.1: blocks
+ * handed out on demand, preemption of the latest arrival when memory runs
+ * short) the same walk over the candidates grows each one's block table to
+ * cover the rows it runs this iteration (lowest free blocks first).  When
+ * the pool is short, the latest-arrived requests holding blocks that are not
+ * in the batch (and not RUNNING) are preempted: their blocks are freed and
+ * they return to INITIATION with n_cached = 0, to recompute their prompt and
+ * generated tokens when selected again.  If it still does not fit, a request
+ * that holds no blocks ends the selection (as a failed reservation does),
+ * and one that does is itself preempted and ends it.  n_reserved = slots
+ * held; slot_base stays -1. */
 
 /* Select with chunked prefill under a per-iteration token budget (CS349D
  * Lecture 2, Exercise 9: prompts cut into chunks, SeqWork(n_new = chunk,

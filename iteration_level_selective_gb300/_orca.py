@@ -29,7 +29,8 @@ ERROR_NAMES = {ORCA_EINVAL: "EINVAL", ORCA_ENOSLOTS: "ENOSLOTS", ORCA_EBATCH: "E
 ORCA_DTYPE_F32 = 0
 ORCA_DTYPE_BF16 = 1
 ORCA_INITIATION, ORCA_INCREMENT, ORCA_RUNNING, ORCA_FINISHED = 0, 1, 2, 3
-ORCA_RESERVE_MAX, ORCA_RESERVE_POW2, ORCA_RESERVE_ORACLE = 0, 1, 2
+ORCA_RESERVE_MAX, ORCA_RESERVE_POW2, ORCA_RESERVE_ORACLE, ORCA_RESERVE_PAGED = 0, 1, 2, 3
+ORCA_KV_BLOCK = 32
 ORCA_ITER_TEACHER_FORCE = 1
 ORCA_ITER_EAGER = 2
 (ORCA_K_EMBED, ORCA_K_LAYERNORM, ORCA_K_GEMM_QKV, ORCA_K_ATTENTION, ORCA_K_GEMM_O, ORCA_K_GEMM_FC1,

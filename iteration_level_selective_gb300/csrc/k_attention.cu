@@ -108,6 +108,29 @@ struct Ring {
   int abort;
 };
 
+// First slot of keys k0 .. k0 + kKvBlock - 1 of a request (k0 a multiple of
+// kKvBlock), in the per-head [n_slots] view: consecutive slots of a
+// contiguous reservation, or one block of a paged table.  -1 for a block
+// outside the request's table or the pool.
+__device__ __forceinline__ int64_t key_run_slot(const int32_t *blocks, int64_t n_slots, int slot_base, int block_off,
+                                                int n_blocks, int k0) {
+  if (block_off < 0) return (int64_t)slot_base + k0;
+  const int bi = k0 / kKvBlock;
+  if (bi >= n_blocks) return -1;
+  const int64_t blk = blocks[block_off + bi];
+  if (blk < 0 || (blk + 1) * kKvBlock > n_slots) return -1;
+  return blk * kKvBlock;
+}
+
+// The request may read keys 0 .. n_keys-1 (contiguous: inside its
+// reservation and the pool; paged: inside its block table).
+__device__ __forceinline__ bool keys_in_range(const AttnArgs &a, const ReqInfo &rq, int n_keys) {
+  if (rq.block_off < 0) return rq.slot_base >= 0 && (int64_t)rq.slot_base + n_keys <= a.n_slots;
+  return (int64_t)rq.n_blocks * kKvBlock >= n_keys;
+}
+
+static_assert(kKeyTile == kKvBlock && kChunkKeys == kKvBlock, "key tiles and decode chunks are one K/V block");
+
 // kind 0: rows r0 .. r0+cnt-1 of one request, keys 0 .. last row's position.
 template <typename T, int D>
 __device__ __forceinline__ void query_tile(const AttnArgs &a, const AttnWork &w, int head, TileSmem<D> &sm) {
@@ -115,12 +138,18 @@ __device__ __forceinline__ void query_tile(const AttnArgs &a, const AttnWork &w,
   const int r0 = w.a, cnt = w.b;
   const int pos0 = rq.ctx + (r0 - rq.row_off);
   const int kv_len = pos0 + cnt;
-  if (rq.slot_base < 0 || (int64_t)rq.slot_base + kv_len > a.n_slots || cnt > kQTile || r0 + cnt > a.n_rows) {
+  bool bad = !keys_in_range(a, rq, kv_len) || cnt > kQTile || r0 + cnt > a.n_rows;
+  for (int t0 = 0; t0 < kv_len && !bad && rq.block_off >= 0; t0 += kKeyTile)  // every block of a paged table
+    bad = key_run_slot(a.blocks, a.n_slots, rq.slot_base, rq.block_off, rq.n_blocks, t0) < 0;
+  if (bad) {
     if (threadIdx.x == 0) atomicOr(a.status, kStatusBadIndex);
     return;
   }
-  const T *Kp = static_cast<const T *>(a.k_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D;
-  const T *Vp = static_cast<const T *>(a.v_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D;
+  // contiguous: keys from the reservation's first slot; paged: one block per key tile
+  const int32_t *table = rq.block_off >= 0 ? a.blocks + rq.block_off : nullptr;
+  const int64_t first = table ? 0 : rq.slot_base;
+  const T *Kl = static_cast<const T *>(a.k_layer) + ((int64_t)head * a.n_slots + first) * D;
+  const T *Vl = static_cast<const T *>(a.v_layer) + ((int64_t)head * a.n_slots + first) * D;
   const T *Q = static_cast<const T *>(a.q);
   for (int e = threadIdx.x; e < kQTile * D; e += kThreads) {
     const int i = e / D, d = e - i * D;
@@ -140,12 +169,16 @@ __device__ __forceinline__ void query_tile(const AttnArgs &a, const AttnWork &w,
   constexpr int VN = Vec16<T>::N;
   for (int t0 = 0; t0 < kv_len; t0 += kKeyTile) {
     __syncthreads();
+    // the tile's keys are one run of slots (checked above)
+    const int64_t s0 = table ? (int64_t)table[t0 / kKvBlock] * kKvBlock : t0;
+    const T *Kp = Kl + s0 * D;
+    const T *Vp = Vl + s0 * D;
     for (int e = threadIdx.x; e < kKeyTile * (D / VN); e += kThreads) {
       const int kk = e / (D / VN), c = (e - kk * (D / VN)) * VN;
       float kv[VN], vv[VN];
       if (t0 + kk < kv_len) {
-        Vec16<T>::load(Kp + (int64_t)(t0 + kk) * D + c, kv);
-        Vec16<T>::load(Vp + (int64_t)(t0 + kk) * D + c, vv);
+        Vec16<T>::load(Kp + (int64_t)kk * D + c, kv);
+        Vec16<T>::load(Vp + (int64_t)kk * D + c, vv);
       } else {
 #pragma unroll
         for (int j = 0; j < VN; ++j) kv[j] = vv[j] = 0.f;
@@ -234,25 +267,32 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   const int n_splits = (n_keys + a.split - 1) / a.split;
   const int kb = w.b * a.split;
   const int ke = min(kb + a.split, n_keys);
-  if (rq.slot_base < 0 || (int64_t)rq.slot_base + n_keys > a.n_slots || r >= a.n_rows || kb >= n_keys ||
-      w.b >= kMaxSplits) {
+  bool bad = !keys_in_range(a, rq, n_keys) || r >= a.n_rows || kb >= n_keys || w.b >= kMaxSplits || kb % kKvBlock;
+  for (int k0 = kb; k0 < ke && !bad && rq.block_off >= 0; k0 += kKvBlock)  // every block of a paged table
+    bad = key_run_slot(a.blocks, a.n_slots, rq.slot_base, rq.block_off, rq.n_blocks, k0) < 0;
+  if (bad) {
     if (threadIdx.x == 0) atomicOr(a.status, kStatusBadIndex);
     return;
   }
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane % LPK, grp = lane / LPK;
-  const T *Kbase = static_cast<const T *>(a.k_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D;
-  const T *Vbase = static_cast<const T *>(a.v_layer) + ((int64_t)head * a.n_slots + rq.slot_base) * D;
+  // contiguous slots: keys from the reservation's first slot; paged: one
+  // block of kKvBlock slots per chunk (blocks checked above)
+  const bool paged = rq.block_off >= 0;
+  const int32_t *table = paged ? a.blocks + rq.block_off : nullptr;
+  const T *Kbase = static_cast<const T *>(a.k_layer) + ((int64_t)head * a.n_slots + (paged ? 0 : rq.slot_base)) * D;
+  const T *Vbase = static_cast<const T *>(a.v_layer) + ((int64_t)head * a.n_slots + (paged ? 0 : rq.slot_base)) * D;
   const int n_chunks = (ke - kb + kChunkKeys - 1) / kChunkKeys;
   auto issue = [&](int c) {  // thread 0: fill the ring stage of chunk c
     const uint32_t idx = g + (uint32_t)c;
     const int st = (int)(idx % kRing);
     if (!mbar_wait(&rg.empty[st], ((idx / kRing) & 1u) ^ 1u, &rg.abort, a.status) || rg.abort) return;
     const int k0 = kb + c * kChunkKeys;
+    const int64_t off = paged ? (int64_t)table[k0 / kKvBlock] * kKvBlock : k0;
     const uint32_t bytes = (uint32_t)(min(kChunkKeys, ke - k0) * D * (int)sizeof(T));
     mbar_expect_tx(&rg.full[st], 2 * bytes);
-    bulk_load(sm.k[st], Kbase + (int64_t)k0 * D, bytes, &rg.full[st]);
-    bulk_load(sm.v[st], Vbase + (int64_t)k0 * D, bytes, &rg.full[st]);
+    bulk_load(sm.k[st], Kbase + off * D, bytes, &rg.full[st]);
+    bulk_load(sm.v[st], Vbase + off * D, bytes, &rg.full[st]);
   };
   if (threadIdx.x == 0)
     for (int c = 0; c < min(kRing - 1, n_chunks); ++c) issue(c);
@@ -388,8 +428,17 @@ constexpr int attn_smem_bytes() {
   return (int)(sizeof(TileSmem<D>) > sizeof(SplitSmem<T, D>) ? sizeof(TileSmem<D>) : sizeof(SplitSmem<T, D>));
 }
 
+// CTAs per SM that shared memory allows (at most 8, i.e. at least 64
+// registers a thread): the register budget is sized to keep that many
+// resident, so registers never lower the occupancy.
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) attention_kernel(AttnArgs a) {
+constexpr int attn_min_ctas() {
+  const int by_smem = (227 * 1024) / (attn_smem_bytes<T, D>() + 1024);
+  return by_smem < 1 ? 1 : (by_smem > 8 ? 8 : by_smem);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, (attn_min_ctas<T, D>())) attention_kernel(AttnArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ Ring rg;
   __shared__ int s_item;

@@ -182,7 +182,9 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int k, int rows) {
 struct TcItem {
   int head, r0, nq, p0;  // query rows r0 .. r0+nq-1 at positions p0 ..
   int kv_len, n_tiles;   // keys 0 .. kv_len-1; n_tiles < 0 ends the CTA
-  long long krow0;       // row of key 0 in the [n_heads * n_slots, D] view
+  int block_off;         // paged K/V: the request's block table, else -1
+  long long krow0;       // contiguous: row of key 0 in the [n_heads * n_slots, D] view;
+                         // paged: row of the head's slot 0
 };
 
 template <int NS>
@@ -208,7 +210,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 template <int D>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     prefill_attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                                const __grid_constant__ CUtensorMap tmV, TcAttnArgs a) {
+                                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKb,
+                                const __grid_constant__ CUtensorMap tmVb, TcAttnArgs a) {
   using C = TcCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -241,6 +244,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmKb)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmVb)) : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sh.tmem)),
@@ -281,10 +286,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           it.nq = w.b;
           it.p0 = rq.ctx + (w.a - rq.row_off);
           it.kv_len = it.p0 + w.b;
-          it.krow0 = (long long)head * a.n_slots + rq.slot_base;
+          it.block_off = rq.block_off;
+          it.krow0 = (long long)head * a.n_slots + (rq.block_off < 0 ? rq.slot_base : 0);
           it.n_tiles = (it.kv_len + kKeys - 1) / kKeys;
-          if (T <= 0 || wi >= n_work || local < 0 || head >= a.n_heads || rq.slot_base < 0 ||
-              (int64_t)rq.slot_base + it.kv_len > a.n_slots || w.b > kRows || w.b <= 0 || it.p0 < 0) {
+          const bool keys_ok = rq.block_off < 0
+                                   ? rq.slot_base >= 0 && (int64_t)rq.slot_base + it.kv_len <= a.n_slots
+                                   : (int64_t)rq.n_blocks * kKvBlock >= it.kv_len;
+          if (T <= 0 || wi >= n_work || local < 0 || head >= a.n_heads || !keys_ok || w.b > kRows || w.b <= 0 ||
+              it.p0 < 0) {
             atomicOr(a.status, kStatusBadIndex);
             continue;
           }
@@ -307,13 +316,44 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             ok = false;
             break;
           }
-          const int krow = (int)(it.krow0 + (long long)tile * kKeys);
-          mbar_expect_tx(&sh.k_full[s], C::K_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_2d(sK + s * C::K_BYTES + kb * kKeys * 128, &tmK, kb * 64, krow, &sh.k_full[s]);
-          mbar_expect_tx(&sh.v_full[s], C::V_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_2d(sV + s * C::V_BYTES + kb * kKeys * 128, &tmV, kb * 64, krow, &sh.v_full[s]);
+          if (it.block_off < 0) {  // contiguous slots: one 128-row box per 64-column block
+            const int krow = (int)(it.krow0 + (long long)tile * kKeys);
+            mbar_expect_tx(&sh.k_full[s], C::K_BYTES);
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_2d(sK + s * C::K_BYTES + kb * kKeys * 128, &tmK, kb * 64, krow, &sh.k_full[s]);
+            mbar_expect_tx(&sh.v_full[s], C::V_BYTES);
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_2d(sV + s * C::V_BYTES + kb * kKeys * 128, &tmV, kb * 64, krow, &sh.v_full[s]);
+            continue;
+          }
+          // paged: the tile's keys in blocks of kKvBlock slots; blocks past the
+          // item's keys are not loaded (their rows are masked, and zeroed in V,
+          // before use)
+          int rows[kKeys / kKvBlock];
+          int n_runs = 0;
+          for (int j = 0; j < kKeys / kKvBlock; ++j) {
+            const int k0 = tile * kKeys + j * kKvBlock;
+            if (k0 >= it.kv_len) break;
+            const int blk = a.blocks[it.block_off + k0 / kKvBlock];
+            const long long run =
+                (blk >= 0 && (long long)(blk + 1) * kKvBlock <= a.n_slots) ? it.krow0 + (long long)blk * kKvBlock : -1;
+            if (run < 0) {
+              atomicOr(a.status, kStatusBadIndex);
+              break;
+            }
+            rows[n_runs++] = (int)run;
+          }
+          const uint32_t run_bytes = C::KB * kKvBlock * 128;
+          mbar_expect_tx(&sh.k_full[s], n_runs * run_bytes);
+          for (int j = 0; j < n_runs; ++j)
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_2d(sK + s * C::K_BYTES + kb * kKeys * 128 + j * kKvBlock * 128, &tmKb, kb * 64, rows[j],
+                          &sh.k_full[s]);
+          mbar_expect_tx(&sh.v_full[s], n_runs * run_bytes);
+          for (int j = 0; j < n_runs; ++j)
+            for (int kb = 0; kb < C::KB; ++kb)
+              tma_load_2d(sV + s * C::V_BYTES + kb * kKeys * 128 + j * kKvBlock * 128, &tmVb, kb * 64, rows[j],
+                          &sh.v_full[s]);
         }
         if (!ok) break;
       }
@@ -543,7 +583,8 @@ cudaError_t attention_tc_prepare() {
 bool attention_tc_supported(int dtype, int head_dim) { return dtype == 1 && (head_dim == 64 || head_dim == 128); }
 
 cudaError_t launch_attention_tc(int head_dim, const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
-                                const TcAttnArgs &a, int n_work, cudaStream_t st) {
+                                const CUtensorMap *tmKb, const CUtensorMap *tmVb, const TcAttnArgs &a, int n_work,
+                                cudaStream_t st) {
   if (n_work <= 0 && a.n_work_dev == nullptr) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -554,13 +595,14 @@ cudaError_t launch_attention_tc(int head_dim, const CUtensorMap *tmQ, const CUte
   if (head_dim == 64) {
     e = set_limit<64>(dev);
     if (e != cudaSuccess) return e;
-    return launch_pdl(prefill_attention_tc_kernel<64>, grid, kThreadsTc, TcCfg<64>::SMEM, st, *tmQ, *tmK, *tmV, a);
+    return launch_pdl(prefill_attention_tc_kernel<64>, grid, kThreadsTc, TcCfg<64>::SMEM, st, *tmQ, *tmK, *tmV, *tmKb,
+                      *tmVb, a);
   }
   if (head_dim == 128) {
     e = set_limit<128>(dev);
     if (e != cudaSuccess) return e;
     return launch_pdl(prefill_attention_tc_kernel<128>, grid, kThreadsTc, TcCfg<128>::SMEM, st, *tmQ, *tmK, *tmV,
-                      a);
+                      *tmKb, *tmVb, a);
   }
   return cudaErrorInvalidValue;
 }

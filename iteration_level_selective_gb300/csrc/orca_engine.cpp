@@ -22,6 +22,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <set>
 #include <string>
 #include <unordered_map>
 #include <unordered_set>
@@ -95,6 +96,49 @@ struct SlotPool {
   }
 };
 
+// Paged K/V (CS349D Lecture 2, sections 5.1 and 6.1: memory handed out in
+// blocks as requests grow, nothing reserved ahead): the pool's slots are
+// n_slots / kKvBlock blocks; a request holds a table of blocks in position
+// order; the lowest free block is handed out first.
+struct BlockPool {
+  int32_t n_blocks = 0;
+  std::set<int32_t> free_;
+  std::unordered_map<int64_t, std::vector<int32_t>> table;
+  std::unordered_set<int64_t> released;
+
+  void init(int32_t n) {
+    n_blocks = n;
+    free_.clear();
+    for (int32_t b = 0; b < n; ++b) free_.insert(b);
+  }
+  int32_t held(int64_t id) const {
+    auto it = table.find(id);
+    return it == table.end() ? 0 : (int32_t)it->second.size();
+  }
+  int64_t used_slots() const { return (int64_t)(n_blocks - (int32_t)free_.size()) * kKvBlock; }
+  // Grow the request's table to `total` blocks; false (nothing taken) if the pool is short.
+  bool grow(int64_t id, int32_t total) {
+    const int32_t need = total - held(id);
+    if (need <= 0) return true;
+    if ((int32_t)free_.size() < need) return false;
+    auto &t = table[id];
+    for (int32_t k = 0; k < need; ++k) {
+      t.push_back(*free_.begin());
+      free_.erase(free_.begin());
+    }
+    released.erase(id);
+    return true;
+  }
+  int release(int64_t id) {
+    auto it = table.find(id);
+    if (it == table.end()) return released.count(id) ? ORCA_EDOUBLE_RELEASE : ORCA_EUNKNOWN_REQ;
+    for (int32_t b : it->second) free_.insert(b);
+    table.erase(it);
+    released.insert(id);
+    return ORCA_OK;
+  }
+};
+
 int32_t max_attn_work(int32_t n_batch, int32_t n_rows);
 int32_t max_tc_work(int32_t n_batch, int32_t n_rows);
 int order_tc_work(AttnWork *w, int32_t n, const ReqInfo *req);
@@ -107,10 +151,17 @@ constexpr int kMaxInflight = 2;
 struct Layout {  // byte offsets into the device workspace
   size_t x, h, q, u, hf, logits, part, counters, gemm_cnt, gemm_part, total;
   size_t out[kMaxInflight], req[kMaxInflight], row[kMaxInflight], work[kMaxInflight], work_tc[kMaxInflight];
+  size_t blocks[kMaxInflight];  // paged K/V: the batch's block tables
   int max_work;
 };
 
 int elem_bytes(int dtype) { return dtype == ORCA_DTYPE_BF16 ? 2 : 4; }
+
+// Block-table entries one batch may need (paged K/V): each request's
+// positions stay below max_pos.
+size_t max_table_entries(const orca_config *c) {
+  return c->reserve_policy == ORCA_RESERVE_PAGED ? (size_t)c->max_bs * ((c->max_pos + kKvBlock - 1) / kKvBlock) : 1;
+}
 
 int check_config(const orca_config *c, std::string *why) {
   if (!c) { *why = "config is NULL"; return ORCA_EINVAL; }
@@ -130,8 +181,12 @@ int check_config(const orca_config *c, std::string *why) {
   }
   if (c->n_slots >= (int64_t)INT32_MAX) { *why = "n_slots must be < 2^31"; return ORCA_EINVAL; }
   if (c->max_rows < c->max_bs) { *why = "max_rows must be >= max_bs"; return ORCA_EINVAL; }
-  if (c->reserve_policy < ORCA_RESERVE_MAX || c->reserve_policy > ORCA_RESERVE_ORACLE) {
+  if (c->reserve_policy < ORCA_RESERVE_MAX || c->reserve_policy > ORCA_RESERVE_PAGED) {
     *why = "unknown reserve_policy";
+    return ORCA_EINVAL;
+  }
+  if (c->reserve_policy == ORCA_RESERVE_PAGED && c->n_slots % kKvBlock) {
+    *why = "paged K/V needs n_slots to be a multiple of ORCA_KV_BLOCK";
     return ORCA_EINVAL;
   }
   return ORCA_OK;
@@ -157,6 +212,7 @@ Layout make_layout(const orca_config *c) {
     L.row[k] = take(R * sizeof(RowInfo));
     L.work[k] = take((size_t)L.max_work * sizeof(AttnWork));
     L.work_tc[k] = take((size_t)max_tc_work(c->max_bs, c->max_rows) * sizeof(AttnWork));
+    L.blocks[k] = take((size_t)max_table_entries(c) * 4);
   }
   L.part = take((size_t)B * kMaxSplits * c->n_heads * (d + 2) * 4);
   L.counters = take((B * c->n_heads + 4) * 4);  // split arrivals, then two work tickets
@@ -259,6 +315,8 @@ struct orca_engine {
   int head_dim = 0;
   std::string err;
   SlotPool slots;
+  bool paged = false;  // ORCA_RESERVE_PAGED: K/V in blocks handed out on demand
+  BlockPool blocks;
   Layout lay{};
   // device side (caller-owned memory)
   std::vector<const void *> w;
@@ -272,6 +330,7 @@ struct orca_engine {
     AttnWork *h_work = nullptr;
     AttnWork *h_work_tc = nullptr;
     unsigned long long *h_out = nullptr;  // [0] status word, [1..] packed argmax keys
+    int32_t *h_blocks = nullptr;          // paged K/V: the batch's block tables
     cudaEvent_t done = nullptr;           // recorded after the result copy
     orca_request *pool = nullptr;
     float *logits = nullptr;
@@ -285,6 +344,7 @@ struct orca_engine {
   CUtensorMap tm_h{}, tm_u{}, tm_hf{}, tm_q{};
   std::vector<CUtensorMap> tm_k;      // per layer: K slots as [n_heads * n_slots, head_dim]
   std::vector<CUtensorMap> tm_v;      // per layer: V slots, same view
+  std::vector<CUtensorMap> tm_kb, tm_vb;  // per layer: the same views in kKvBlock-row boxes (paged)
   bool attn_tc = false;               // prompts take the tensor-core prefill kernel
   WeightMaps tm_emb{};
   std::vector<WeightMaps> tm_layer;  // 4 per layer: qkv, o, fc1, fc2
@@ -521,6 +581,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     aa.n_slots = c.n_slots;
     aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     aa.hdr = graph ? d_hdr : nullptr;
+    aa.blocks = ws_ptr<int32_t>(e, Ly.blocks[k]);
     prof_begin(e, st, &ev);
     if (e->attn_tc && z.n_work_tc > 0) {  // prompts: tensor-core tiles; then decodes and short prompts
       TcAttnArgs ta{};
@@ -533,9 +594,11 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
       ta.n_heads = nh;
       ta.n_work = z.n_work_tc;
       ta.n_work_dev = graph ? &d_hdr->n_work_tc : nullptr;
+      ta.blocks = aa.blocks;
       ta.n_slots = c.n_slots;
       ta.scale_log2 = aa.scale_log2;
-      CUDA_TRY(e, launch_attention_tc(D, &e->tm_q, &e->tm_k[l], &e->tm_v[l], ta, z.n_work_tc, st));
+      CUDA_TRY(e, launch_attention_tc(D, &e->tm_q, &e->tm_k[l], &e->tm_v[l], &e->tm_kb[l], &e->tm_vb[l], ta,
+                                      z.n_work_tc, st));
       ++e->n_launch;
     }
     LAUNCH(e, launch_attention(c.dtype, D, aa, graph ? Ly.max_work : z.n_work, st));
@@ -657,6 +720,8 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
   e->cfg = *cfg;
   e->head_dim = cfg->hidden / cfg->n_heads;
   e->slots.init(cfg->n_slots);
+  e->paged = cfg->reserve_policy == ORCA_RESERVE_PAGED;
+  if (e->paged) e->blocks.init((int32_t)(cfg->n_slots / kKvBlock));
   e->lay = make_layout(cfg);
   const bool any = weights || kv_pool || workspace;
   if (!any) {  // host-only engine: scheduler and slot pool, no CUDA call
@@ -697,6 +762,7 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
                        cudaHostAllocDefault) == cudaSuccess &&
          cudaHostAlloc(&S.h_out, sizeof(unsigned long long) * (cfg->max_bs + 1), cudaHostAllocDefault) ==
              cudaSuccess &&
+         cudaHostAlloc(&S.h_blocks, max_table_entries(cfg) * 4, cudaHostAllocDefault) == cudaSuccess &&
          cudaEventCreateWithFlags(&S.done, cudaEventDisableTiming) == cudaSuccess &&
          cudaMemset(e->ws + L.out[k], 0, 8) == cudaSuccess;
     if (ok) S.h_req = reinterpret_cast<ReqInfo *>(S.h_hdr + 1);
@@ -722,12 +788,15 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
       const size_t layer_kv = (size_t)2 * cfg->n_heads * cfg->n_slots * e->head_dim * 2;
       e->tm_k.resize(cfg->n_layers);
       e->tm_v.resize(cfg->n_layers);
+      e->tm_kb.resize(cfg->n_layers);
+      e->tm_vb.resize(cfg->n_layers);
+      const uint64_t kv_rows = (uint64_t)cfg->n_heads * cfg->n_slots;
       for (int l = 0; l < cfg->n_layers && !rc; ++l) {
-        rc = make_tmap(e, &e->tm_k[l], e->kv + (size_t)l * layer_kv, (uint64_t)cfg->n_heads * cfg->n_slots,
-                       e->head_dim, kTcBM);
-        if (!rc)
-          rc = make_tmap(e, &e->tm_v[l], e->kv + (size_t)l * layer_kv + layer_kv / 2,
-                         (uint64_t)cfg->n_heads * cfg->n_slots, e->head_dim, kTcBM);
+        char *kl = e->kv + (size_t)l * layer_kv, *vl = kl + layer_kv / 2;
+        rc = make_tmap(e, &e->tm_k[l], kl, kv_rows, e->head_dim, kTcBM);
+        if (!rc) rc = make_tmap(e, &e->tm_v[l], vl, kv_rows, e->head_dim, kTcBM);
+        if (!rc) rc = make_tmap(e, &e->tm_kb[l], kl, kv_rows, e->head_dim, kKvBlock);
+        if (!rc) rc = make_tmap(e, &e->tm_vb[l], vl, kv_rows, e->head_dim, kKvBlock);
       }
     }
     for (int l = 0; l < cfg->n_layers && !rc; ++l) {
@@ -757,6 +826,7 @@ int orca_engine_destroy(orca_engine *e) {
       cudaFreeHost(S.h_work);
       cudaFreeHost(S.h_work_tc);
       cudaFreeHost(S.h_out);
+      cudaFreeHost(S.h_blocks);
       if (S.done) cudaEventDestroy(S.done);
     }
     for (auto ev : e->ev_all) cudaEventDestroy(ev);
@@ -767,6 +837,7 @@ int orca_engine_destroy(orca_engine *e) {
 
 int orca_kv_reserve(orca_engine *e, int64_t req_id, int32_t n_tokens, int64_t *slot_base) {
   if (!e || !slot_base) return ORCA_EINVAL;
+  if (e->paged) return fail(e, ORCA_ESTATE, "paged K/V hands out blocks on demand; nothing to reserve");
   int rc = e->slots.reserve(req_id, n_tokens, slot_base);
   if (rc == ORCA_ENOSLOTS) return fail(e, rc, "cannot reserve %d slots (n_rsrv %lld of %lld)", n_tokens,
                                        (long long)e->slots.n_rsrv, (long long)e->slots.n_slots);
@@ -776,7 +847,7 @@ int orca_kv_reserve(orca_engine *e, int64_t req_id, int32_t n_tokens, int64_t *s
 
 int orca_kv_release(orca_engine *e, int64_t req_id) {
   if (!e) return ORCA_EINVAL;
-  int rc = e->slots.release(req_id);
+  int rc = e->paged ? e->blocks.release(req_id) : e->slots.release(req_id);
   if (rc) return fail(e, rc, "release of request %lld: %s", (long long)req_id,
                       rc == ORCA_EDOUBLE_RELEASE ? "already released" : "unknown request");
   return ORCA_OK;
@@ -784,17 +855,22 @@ int orca_kv_release(orca_engine *e, int64_t req_id) {
 
 int orca_kv_stats(const orca_engine *e, int64_t *n_rsrv, int64_t *n_free_blocks, int64_t *frag_blocks) {
   if (!e) return ORCA_EINVAL;
-  if (n_rsrv) *n_rsrv = e->slots.n_rsrv;
-  if (n_free_blocks) *n_free_blocks = (int64_t)e->slots.free_.size();
-  if (frag_blocks) *frag_blocks = e->slots.frag_blocks;
+  if (n_rsrv) *n_rsrv = e->paged ? e->blocks.used_slots() : e->slots.n_rsrv;
+  if (n_free_blocks) *n_free_blocks = e->paged ? (int64_t)e->blocks.free_.size() : (int64_t)e->slots.free_.size();
+  if (frag_blocks) *frag_blocks = e->paged ? 0 : e->slots.frag_blocks;
   return ORCA_OK;
 }
 
 namespace {
 
 // Rows a selected request contributes when nothing narrower was scheduled:
-// the rest of its prompt, or one row once the prompt is processed.
-int32_t default_rows(const orca_request &r) { return r.n_cached < r.n_prompt ? r.n_prompt - r.n_cached : 1; }
+// its known tokens (prompt + generated) not yet in the K/V slots - the rest
+// of the prompt, one decode row, or everything after a preemption.
+int32_t known_len(const orca_request &r) { return r.n_prompt + r.n_generated; }
+int32_t default_rows(const orca_request &r) { return std::max(1, known_len(r) - r.n_cached); }
+// A request that runs one decode row (its prompt and all but the last
+// generated token are in the slots).
+bool decoding(const orca_request &r) { return r.n_generated > 0 && r.n_cached == known_len(r) - 1; }
 
 // Slots a request reserves at first schedule (CS349D Lecture 2, section
 // 6.1): max_tokens (Orca), or its true final length n_prompt + out_len
@@ -815,7 +891,16 @@ int32_t reserve_size(int policy, const orca_request &r) {
 // non-RUNNING, unfinished requests in (arrival, req_id) order; at most max_bs;
 // an INITIATION request first reserves max_tokens slots and a failed
 // reservation ends the selection.  Fills batch_idx; states are not changed.
-int select_fcfs(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t *batch_idx, int32_t *nb_out) {
+void preempt(orca_engine *e, orca_request &v) {
+  e->blocks.release(v.req_id);
+  v.n_cached = 0;
+  v.n_reserved = 0;
+  v.n_sched = 0;
+  v.state = ORCA_INITIATION;
+}
+
+int select_fcfs(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t *batch_idx, int32_t *nb_out,
+                int64_t chunk_cap) {
   *nb_out = 0;
   std::vector<int32_t> cand;
   cand.reserve(n_pool);
@@ -830,13 +915,40 @@ int select_fcfs(orca_engine *e, orca_request *pool, int32_t n_pool, int32_t *bat
     return pool[a].req_id < pool[b].req_id;
   });
   int32_t nb = 0;
+  std::vector<char> in_batch(e->paged ? n_pool : 0, 0);
   for (int32_t idx : cand) {
     if (nb == e->cfg.max_bs) break;
     orca_request &r = pool[idx];
+    if (r.state == ORCA_INITIATION &&
+        (r.max_tokens < r.n_prompt || r.n_prompt <= 0 || r.out_len <= 0 || r.n_generated < 0))
+      return fail(e, ORCA_EINVAL, "request %lld: need 0 < n_prompt <= max_tokens and out_len > 0",
+                  (long long)r.req_id);
+    if (e->paged) {
+      const int64_t rows = std::min<int64_t>(default_rows(r), chunk_cap);
+      const int32_t total = (int32_t)((r.n_cached + rows + kKvBlock - 1) / kKvBlock);
+      while ((int32_t)e->blocks.free_.size() < total - e->blocks.held(r.req_id)) {
+        int32_t v = -1;  // the latest arrival that holds blocks and is neither batched nor running
+        for (int32_t i = 0; i < n_pool; ++i) {
+          const orca_request &q = pool[i];
+          if (i == idx || in_batch[i] || q.state != ORCA_INCREMENT || e->blocks.held(q.req_id) == 0) continue;
+          if (v < 0 || q.arrival > pool[v].arrival || (q.arrival == pool[v].arrival && q.req_id > pool[v].req_id))
+            v = i;
+        }
+        if (v < 0) break;
+        preempt(e, pool[v]);
+      }
+      if (!e->blocks.grow(r.req_id, total)) {
+        if (e->blocks.held(r.req_id) > 0) preempt(e, r);  // cannot grow even alone: recompute later
+        break;                                            // as a failed reservation: stop selecting
+      }
+      r.n_reserved = e->blocks.held(r.req_id) * kKvBlock;
+      r.slot_base = -1;
+      r.state = ORCA_INCREMENT;
+      in_batch[idx] = 1;
+      batch_idx[nb++] = idx;
+      continue;
+    }
     if (r.state == ORCA_INITIATION) {
-      if (r.max_tokens < r.n_prompt || r.n_prompt <= 0 || r.out_len <= 0)
-        return fail(e, ORCA_EINVAL, "request %lld: need 0 < n_prompt <= max_tokens and out_len > 0",
-                    (long long)r.req_id);
       int64_t base = -1;
       const int32_t want = reserve_size(e->cfg.reserve_policy, r);
       const int rc = e->slots.reserve(r.req_id, want, &base);
@@ -860,9 +972,10 @@ int orca_kv_usage(const orca_engine *e, const orca_request *pool, int32_t n_pool
   int64_t st = 0;
   for (int32_t i = 0; i < n_pool; ++i) {
     const orca_request &r = pool[i];
-    if (r.state != ORCA_INITIATION && r.state != ORCA_FINISHED && r.slot_base >= 0) st += r.n_cached;
+    if (r.state != ORCA_INITIATION && r.state != ORCA_FINISHED && (r.slot_base >= 0 || r.n_reserved > 0))
+      st += r.n_cached;
   }
-  if (reserved) *reserved = e->slots.n_rsrv;
+  if (reserved) *reserved = e->paged ? e->blocks.used_slots() : e->slots.n_rsrv;
   if (stored) *stored = st;
   return ORCA_OK;
 }
@@ -871,7 +984,7 @@ int orca_select_batch(orca_engine *e, orca_request *pool, int32_t n_pool, int32_
   if (!e || !n_batch || (n_pool > 0 && (!pool || !batch_idx)) || n_pool < 0) return ORCA_EINVAL;
   *n_batch = 0;
   int32_t nb = 0;
-  const int rc = select_fcfs(e, pool, n_pool, batch_idx, &nb);
+  const int rc = select_fcfs(e, pool, n_pool, batch_idx, &nb, INT32_MAX);
   if (rc) return rc;
   for (int32_t i = 0; i < nb; ++i) {
     orca_request &r = pool[batch_idx[i]];
@@ -888,21 +1001,21 @@ int orca_select_batch_budget(orca_engine *e, orca_request *pool, int32_t n_pool,
   *n_batch = 0;
   if (token_budget < 1 || chunk < 1) return fail(e, ORCA_EINVAL, "token_budget and chunk must be >= 1");
   int32_t nb = 0;
-  const int rc = select_fcfs(e, pool, n_pool, batch_idx, &nb);
+  const int rc = select_fcfs(e, pool, n_pool, batch_idx, &nb, chunk);
   if (rc) return rc;
   int64_t left = token_budget;
   std::vector<int32_t> rows(nb, 0);
   for (int32_t i = 0; i < nb; ++i) {  // decodes first: one row each
     const orca_request &r = pool[batch_idx[i]];
-    if (r.n_cached >= r.n_prompt && left >= 1) {
+    if (decoding(r) && left >= 1) {
       rows[i] = 1;
       left -= 1;
     }
   }
-  for (int32_t i = 0; i < nb; ++i) {  // then prompt chunks, in batch order
+  for (int32_t i = 0; i < nb; ++i) {  // then prompt chunks (and recomputations), in batch order
     const orca_request &r = pool[batch_idx[i]];
-    if (r.n_cached < r.n_prompt) {
-      const int64_t n = std::min<int64_t>(std::min<int64_t>(r.n_prompt - r.n_cached, chunk), left);
+    if (!decoding(r)) {
+      const int64_t n = std::min<int64_t>(std::min<int64_t>(default_rows(r), chunk), left);
       rows[i] = (int32_t)n;
       left -= n;
     }
@@ -947,18 +1060,21 @@ int orca_iteration_submit(orca_engine *e, orca_request *pool, const int32_t *bat
   for (int32_t i = 0; i < n_batch; ++i) {
     const orca_request &r = pool[batch_idx[i]];
     if (r.state != ORCA_RUNNING) return fail(e, ORCA_EINVAL, "request %lld is not RUNNING", (long long)r.req_id);
-    if (!r.tokens || r.slot_base < 0) return fail(e, ORCA_EINVAL, "request %lld has no tokens or slots", (long long)r.req_id);
+    if (!r.tokens || (!e->paged && r.slot_base < 0))
+      return fail(e, ORCA_EINVAL, "request %lld has no tokens or slots", (long long)r.req_id);
     if (r.n_cached < 0) return fail(e, ORCA_EINVAL, "request %lld: negative n_cached", (long long)r.req_id);
     const int32_t dflt = default_rows(r);
     if (r.n_sched < 0 || r.n_sched > dflt)
       return fail(e, ORCA_EINVAL, "request %lld: n_sched %d outside 0..%d", (long long)r.req_id, r.n_sched, dflt);
     L[i] = r.n_sched > 0 ? r.n_sched : dflt;
-    const int64_t cap = r.n_reserved > 0 ? r.n_reserved : r.max_tokens;  // slots the request holds
+    // slots the request holds
+    const int64_t cap = e->paged ? (int64_t)e->blocks.held(r.req_id) * kKvBlock
+                                 : (r.n_reserved > 0 ? r.n_reserved : r.max_tokens);
     const int64_t end = (int64_t)r.n_cached + L[i];
     if (end > cap || end > r.max_tokens || end > c.max_pos || end > (int64_t)r.n_prompt + r.out_len)
       return fail(e, ORCA_EINVAL, "request %lld: position %lld beyond its slots, max_pos or its buffer",
                   (long long)r.req_id, (long long)end);
-    if (r.slot_base + cap > c.n_slots)
+    if (!e->paged && r.slot_base + cap > c.n_slots)
       return fail(e, ORCA_EINVAL, "request %lld: slots beyond n_slots", (long long)r.req_id);
     for (int j = 0; j < e->q_len; ++j) {  // a request is in at most one batch in flight
       const orca_engine::IterSlot &O = e->slot[(e->q_head + j) % kMaxInflight];
@@ -975,15 +1091,24 @@ int orca_iteration_submit(orca_engine *e, orca_request *pool, const int32_t *bat
   }
   const int split = attn_split(max_keys, sum_keys, nh);
   int32_t n_work = 0, n_work_tc = 0;
-  int32_t row = 0;
+  int32_t row = 0, n_entries = 0;
   for (int32_t i = 0; i < n_batch; ++i) {
     const orca_request &r = pool[batch_idx[i]];
-    S.h_req[i] = {row, L[i], r.n_cached, (int32_t)r.slot_base};
+    const std::vector<int32_t> *table = nullptr;
+    if (e->paged) {  // the request's block table, for the kernels and the row slots
+      table = &e->blocks.table.at(r.req_id);
+      S.h_req[i] = {row, L[i], r.n_cached, -1, n_entries, (int32_t)table->size()};
+      std::copy(table->begin(), table->end(), S.h_blocks + n_entries);
+      n_entries += (int32_t)table->size();
+    } else {
+      S.h_req[i] = {row, L[i], r.n_cached, (int32_t)r.slot_base, -1, 0};
+    }
     for (int32_t j = 0; j < L[i]; ++j) {
       const int32_t pos = r.n_cached + j;
       const int32_t tok = r.tokens[pos];
       if (tok < 0 || tok >= V) return fail(e, ORCA_EINVAL, "token id %d out of range", tok);
-      S.h_row[row + j] = {tok, pos, i, (int32_t)(r.slot_base + pos)};
+      const int32_t slot = table ? (*table)[pos / kKvBlock] * kKvBlock + pos % kKvBlock : (int32_t)(r.slot_base + pos);
+      S.h_row[row + j] = {tok, pos, i, slot};
     }
     if (e->attn_tc && L[i] >= kTcMinRows)
       n_work_tc = append_tc_work(S.h_work_tc, n_work_tc, i, row, L[i]);
@@ -999,7 +1124,7 @@ int orca_iteration_submit(orca_engine *e, orca_request *pool, const int32_t *bat
   e->last_N = N;
   e->last_work = n_work;
   e->last_h2d = (int64_t)sizeof(DevHeader) + (int64_t)sizeof(ReqInfo) * n_batch + (int64_t)sizeof(RowInfo) * N +
-                (int64_t)sizeof(AttnWork) * (n_work + n_work_tc);
+                (int64_t)sizeof(AttnWork) * (n_work + n_work_tc) + (int64_t)sizeof(int32_t) * n_entries;
   e->last_d2h = (int64_t)sizeof(unsigned long long) * (n_batch + 1);
   e->last_row_off.assign(n_batch + 1, 0);
   e->last_last_row.resize(n_batch);
@@ -1028,6 +1153,9 @@ int orca_iteration_submit(orca_engine *e, orca_request *pool, const int32_t *bat
     CUDA_TRY(e, cudaMemcpyAsync(d_work, S.h_work, sizeof(AttnWork) * n_work, cudaMemcpyHostToDevice, st));
   if (n_work_tc > 0)
     CUDA_TRY(e, cudaMemcpyAsync(ws_ptr<AttnWork>(e, Ly.work_tc[k]), S.h_work_tc, sizeof(AttnWork) * n_work_tc,
+                                cudaMemcpyHostToDevice, st));
+  if (n_entries > 0)
+    CUDA_TRY(e, cudaMemcpyAsync(ws_ptr<int32_t>(e, Ly.blocks[k]), S.h_blocks, sizeof(int32_t) * n_entries,
                                 cudaMemcpyHostToDevice, st));
 
   FwdSizes z{N, n_batch, n_work, split, n_work_tc, 0.0, 0.0};
@@ -1127,7 +1255,7 @@ int orca_iteration_wait(orca_engine *e, int32_t *n_batch, int32_t *batch_idx, in
     r.state = ORCA_INCREMENT;
     r.n_sched = 0;
     r.n_cached += S.L[i];
-    if (r.n_cached < r.n_prompt) {  // a prompt chunk: the prompt is not complete yet, nothing generated
+    if (r.n_cached < known_len(r)) {  // a chunk: known tokens remain unprocessed, nothing generated
       if (next_tokens) next_tokens[i] = -1;
       continue;
     }
@@ -1136,7 +1264,10 @@ int orca_iteration_wait(orca_engine *e, int32_t *n_batch, int32_t *batch_idx, in
     if (!(S.flags & ORCA_ITER_TEACHER_FORCE)) r.tokens[r.n_prompt + r.n_generated - 1] = tok;
     if (r.n_generated >= r.out_len || r.n_prompt + r.n_generated >= r.max_tokens) {
       r.state = ORCA_FINISHED;
-      e->slots.release(r.req_id);
+      if (e->paged)
+        e->blocks.release(r.req_id);
+      else
+        e->slots.release(r.req_id);
     }
   }
   return ORCA_OK;
@@ -1229,7 +1360,7 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
   for (int32_t i = 0; i < n_batch; ++i) {
     const int32_t L = row_off[i + 1] - row_off[i];
     if (L <= 0 || ctx[i] < 0 || slot_base[i] < 0 || slot_base[i] + ctx[i] + L > n_slots) return ORCA_EINVAL;
-    req[i] = {row_off[i], L, ctx[i], (int32_t)slot_base[i]};
+    req[i] = {row_off[i], L, ctx[i], (int32_t)slot_base[i], -1, 0};
     if (L == 1) {
       max_keys = std::max(max_keys, ctx[i] + 1);
       sum_keys += ctx[i] + 1;
@@ -1282,7 +1413,7 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
     ta.n_work_dev = nullptr;
     ta.n_slots = n_slots;
     ta.scale_log2 = scale_log2;
-    if (launch_attention_tc(head_dim, &tq, &tk, &tv, ta, n_work_tc, st) != cudaSuccess) return ORCA_ECUDA;
+    if (launch_attention_tc(head_dim, &tq, &tk, &tv, &tk, &tv, ta, n_work_tc, st) != cudaSuccess) return ORCA_ECUDA;
   }
   AttnArgs aa{};
   aa.q = q;

@@ -14,12 +14,19 @@
 
 namespace orca {
 
+// Paged K/V: a request's slots are blocks of kKvBlock consecutive slots
+// (key k of the request lives in block table[k / kKvBlock] at offset
+// k % kKvBlock).  A multiple of the decode chunk and of 8 (TMA swizzle atom).
+constexpr int kKvBlock = 32;
+
 // One request of the batch.
 struct ReqInfo {
   int32_t row_off;    // first row of this request
   int32_t n_new;      // L_i: rows this iteration
   int32_t ctx;        // c_i: tokens cached before this iteration
-  int32_t slot_base;  // first K/V slot of the request's reservation
+  int32_t slot_base;  // first K/V slot of a contiguous reservation
+  int32_t block_off;  // paged K/V: first entry of the request's block table, else -1
+  int32_t n_blocks;   // paged K/V: entries of that table
 };
 
 // One row (token) of the flattened [sum L_i, H] tensor.
@@ -131,6 +138,7 @@ struct AttnArgs {
   int64_t n_slots;
   float scale_log2;       // log2(e) / sqrt(D)
   const DevHeader *hdr;   // when set, n_rows / n_work / split come from it
+  const int32_t *blocks;  // paged K/V block tables (ReqInfo::block_off >= 0)
 };
 
 // Arguments of the tensor-core prefill attention (work items: kind 2,
@@ -143,6 +151,7 @@ struct TcAttnArgs {
   int32_t *status;
   int32_t hidden, n_heads, n_work;
   const int32_t *n_work_dev;  // when set, the item count comes from it
+  const int32_t *blocks;      // paged K/V block tables (ReqInfo::block_off >= 0)
   int64_t n_slots;
   float scale_log2;
 };
@@ -186,9 +195,11 @@ cudaError_t attention_prepare();
 cudaError_t attention_tc_prepare();
 bool attention_tc_supported(int dtype, int head_dim);
 // tmQ: q buffer [rows, H] (box 64 x 128); tmK / tmV: one layer's K / V slots
-// viewed as [n_heads * n_slots, D] (box 64 x 128).
+// viewed as [n_heads * n_slots, D] (box 64 x 128); tmKb / tmVb: the same
+// views with box 64 x kKvBlock (paged block tables).
 cudaError_t launch_attention_tc(int head_dim, const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
-                                const TcAttnArgs &a, int n_work, cudaStream_t st);
+                                const CUtensorMap *tmKb, const CUtensorMap *tmVb, const TcAttnArgs &a, int n_work,
+                                cudaStream_t st);
 // Persistent over (work item, head) pairs; n_work is the host count, or
 // the capacity when args.hdr is set.
 cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &args, int n_work, cudaStream_t st);

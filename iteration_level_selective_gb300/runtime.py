@@ -29,7 +29,8 @@ def _is_matrix(name: str) -> bool:
     return name.startswith("w_") or name.endswith("_emb")
 
 
-RESERVE_POLICIES = {"max": C.ORCA_RESERVE_MAX, "pow2": C.ORCA_RESERVE_POW2, "oracle": C.ORCA_RESERVE_ORACLE}
+RESERVE_POLICIES = {"max": C.ORCA_RESERVE_MAX, "pow2": C.ORCA_RESERVE_POW2, "oracle": C.ORCA_RESERVE_ORACLE,
+                    "paged": C.ORCA_RESERVE_PAGED}
 
 
 def make_config(shape, max_bs: int, n_slots: int, max_rows: int, reserve_policy: int = C.ORCA_RESERVE_MAX
@@ -165,6 +166,7 @@ class IterRecord:
     next_tokens: List[int]
     logits: Optional[np.ndarray] = None
     launches: int = 0          # kernels the iteration launched on the device
+    preempted: List[int] = dataclasses.field(default_factory=list)  # paged K/V: requests sent back by this Select
 
 
 class ServingLoop:
@@ -209,6 +211,7 @@ class ServingLoop:
         self.n_done = 0
         self.n_submitted = 0
         self.inflight: List[tuple] = []   # (record, pool indices, logits buffer), oldest first
+        self.preempted: List[int] = []    # preemptions not yet attached to a record
         # host seconds spent selecting / submitting / completing (diagnostics)
         self.t_pre = self.t_call = self.t_post = 0.0
 
@@ -244,16 +247,21 @@ class ServingLoop:
             t0 = time.perf_counter()
             if self.n_arrived < P.n and P.arrivals[self.n_arrived] <= self.it:
                 self.n_arrived = int(np.searchsorted(P.arrivals, self.it, side="right"))
+            held = P.view["state"][:self.n_arrived] == C.ORCA_INCREMENT
             if self.budget is None:
                 nb = C.orca_select_batch(self.eng.handle, P.arr, self.n_arrived, self.batch_idx)
             else:
                 nb = C.orca_select_batch_budget(self.eng.handle, P.arr, self.n_arrived, self.budget[0],
                                                 self.budget[1], self.batch_idx)
+            gone = held & (P.view["state"][:self.n_arrived] == C.ORCA_INITIATION)   # preempted (paged K/V)
+            if gone.any():
+                self.preempted += sorted(P.view["req_id"][:self.n_arrived][gone].tolist())
             if nb > 0:
                 idx = self._bi[:nb].copy()
                 sel = P.view[idx]
                 rec = IterRecord(self.it, sel["req_id"].tolist(), sel["n_sched"].tolist(), sel["n_cached"].tolist(),
-                                 sel["slot_base"].tolist(), [], [])
+                                 sel["slot_base"].tolist(), [], [], preempted=sorted(self.preempted))
+                self.preempted = []
                 lg = self.logits[self.n_submitted % self.n_workers] if self.logits is not None else None
                 t1 = time.perf_counter()
                 C.orca_iteration_submit(self.eng.handle, P.arr, self.batch_idx, nb, self.flags,

@@ -82,9 +82,46 @@ class ReqState:
     n_cached: int = 0
     n_generated: int = 0
     slot_base: int = -1
+    preempted: int = 0
 
 
-RESERVE_MAX, RESERVE_POW2, RESERVE_ORACLE = 0, 1, 2
+RESERVE_MAX, RESERVE_POW2, RESERVE_ORACLE, RESERVE_PAGED = 0, 1, 2, 3
+KV_BLOCK = 32
+
+
+class BlockPool:
+    """Paged K/V (CS349D Lecture 2, sections 5.1 and 6.1: memory handed out
+    block by block as requests grow, nothing reserved ahead): n_slots //
+    KV_BLOCK blocks; each request holds a list of blocks in position order;
+    the lowest free block is handed out first."""
+
+    def __init__(self, n_slots: int):
+        self.n_slots = n_slots
+        self.n_blocks = n_slots // KV_BLOCK
+        self.free = list(range(self.n_blocks))   # kept sorted
+        self.table: Dict[int, List[int]] = {}
+
+    @property
+    def n_rsrv(self) -> int:   # slots held
+        return (self.n_blocks - len(self.free)) * KV_BLOCK
+
+    def held(self, req_id: int) -> int:
+        return len(self.table.get(req_id, []))
+
+    def grow(self, req_id: int, total: int) -> bool:
+        need = total - self.held(req_id)
+        if need <= 0:
+            return True
+        if len(self.free) < need:
+            return False
+        t = self.table.setdefault(req_id, [])
+        t.extend(self.free[:need])
+        del self.free[:need]
+        return True
+
+    def release(self, req_id: int) -> None:
+        blocks = self.table.pop(req_id)
+        self.free = sorted(self.free + blocks)
 
 
 def reserve_size(policy: int, r: ReqState) -> int:
@@ -107,14 +144,50 @@ def reserve_size(policy: int, r: ReqState) -> int:
     return r.max_tokens
 
 
-def select(pool: List[ReqState], slots: SlotPool, max_bs: int, policy: int = RESERVE_MAX) -> List[ReqState]:
-    """Algorithm 1 Select over the arrived, unfinished requests."""
+def preempt(r: ReqState, blocks: BlockPool) -> None:
+    """Free the request's blocks; it recomputes its known tokens when it is
+    selected again (CS349D Lecture 2, section 5.1: the latest arrival is
+    kicked out and recomputed later)."""
+    blocks.release(r.req_id)
+    r.n_cached = 0
+    r.state = INITIATION
+    r.preempted += 1
+
+
+def select(pool: List[ReqState], slots, max_bs: int, policy: int = RESERVE_MAX,
+           chunk: Optional[int] = None) -> List[ReqState]:
+    """Algorithm 1 Select over the arrived, unfinished requests.
+
+    Paged K/V (slots is a BlockPool): the same walk grows each candidate's
+    block table to cover the rows it runs this iteration (the rest of its
+    known tokens, at most `chunk`).  When the pool is short, the latest
+    arrivals holding blocks that are not in the batch (and not running) are
+    preempted; if that is not enough, a candidate holding no blocks ends the
+    selection (as a failed reservation does) and one holding blocks is
+    itself preempted and ends it.  Readings: "latest arrival" is the largest
+    (arrival, request id); preempted requests recompute from position 0."""
     cands = sorted((r for r in pool if r.state in (INITIATION, INCREMENT)),
                    key=lambda r: (r.arrival, r.req_id))
     batch: List[ReqState] = []
     for r in cands:
         if len(batch) == max_bs:
             break
+        if policy == RESERVE_PAGED:
+            rows = min(default_rows(r), chunk) if chunk else default_rows(r)
+            total = -(-(r.n_cached + rows) // KV_BLOCK)
+            while len(slots.free) < total - slots.held(r.req_id):
+                victims = [q for q in pool if q is not r and q not in batch and q.state == INCREMENT
+                           and slots.held(q.req_id) > 0]
+                if not victims:
+                    break
+                preempt(max(victims, key=lambda q: (q.arrival, q.req_id)), slots)
+            if not slots.grow(r.req_id, total):
+                if slots.held(r.req_id) > 0:
+                    preempt(r, slots)
+                break
+            r.state = INCREMENT
+            batch.append(r)
+            continue
         if r.state == INITIATION:
             base = slots.reserve(r.req_id, reserve_size(policy, r))
             if base is None:
@@ -127,14 +200,27 @@ def select(pool: List[ReqState], slots: SlotPool, max_bs: int, policy: int = RES
 def kv_usage(pool: List[ReqState], slots: SlotPool) -> Tuple[int, int]:
     """(reserved slots, slots holding K/V): CS349D Lecture 2, section 6.1
     contrasts the memory a reservation occupies with what is written."""
-    stored = sum(r.n_cached for r in pool if r.state not in (INITIATION, FINISHED) and r.slot_base >= 0)
+    if isinstance(slots, BlockPool):
+        stored = sum(r.n_cached for r in pool if r.state not in (INITIATION, FINISHED) and slots.held(r.req_id))
+    else:
+        stored = sum(r.n_cached for r in pool if r.state not in (INITIATION, FINISHED) and r.slot_base >= 0)
     return slots.n_rsrv, stored
 
 
+def known_len(r: ReqState) -> int:
+    """Tokens of the request known so far: prompt + generated."""
+    return r.n_prompt + r.n_generated
+
+
 def default_rows(r: ReqState) -> int:
-    """Rows of a selected request in plain Algorithm 1: the rest of its
-    prompt (all of it at first schedule), else one decode row."""
-    return r.n_prompt - r.n_cached if r.n_cached < r.n_prompt else 1
+    """Rows of a selected request: its known tokens not yet in the K/V
+    slots - the rest of its prompt (all of it at first schedule), one decode
+    row, or, after a preemption, the prompt and the generated tokens again."""
+    return max(1, known_len(r) - r.n_cached)
+
+
+def decoding(r: ReqState) -> bool:
+    return r.n_generated > 0 and r.n_cached == known_len(r) - 1
 
 
 def select_budget(pool: List[ReqState], slots: SlotPool, max_bs: int, token_budget: int,
@@ -152,16 +238,16 @@ def select_budget(pool: List[ReqState], slots: SlotPool, max_bs: int, token_budg
     while the budget lasts, then every prompting request takes
     min(remaining prompt, chunk, budget left) rows.  Returns (request, rows)
     in batch order; rows may be 0 (admitted but idle this iteration)."""
-    batch = select(pool, slots, max_bs, policy)
+    batch = select(pool, slots, max_bs, policy, chunk)
     left = token_budget
     rows: Dict[int, int] = {}
     for r in batch:
-        if r.n_cached >= r.n_prompt and left >= 1:
+        if decoding(r) and left >= 1:
             rows[r.req_id] = 1
             left -= 1
     for r in batch:
-        if r.n_cached < r.n_prompt:
-            n = min(r.n_prompt - r.n_cached, chunk, left)
+        if not decoding(r):
+            n = min(default_rows(r), chunk, left)
             rows[r.req_id] = n
             left -= n
     return [(r, rows.get(r.req_id, 0)) for r in batch]
@@ -179,6 +265,7 @@ class IterRecord:
     n_ctx: List[int]        # c_i: tokens cached before this iteration
     slot_base: List[int]
     released: List[int]
+    preempted: List[int] = dataclasses.field(default_factory=list)
 
 
 def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
@@ -203,7 +290,7 @@ def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
     to the next arrival).  Records are in scheduling order."""
     order = sorted(trace, key=lambda r: (r.arrival, r.req_id))
     states = [ReqState(r.req_id, r.arrival, r.n_prompt, r.out_len, r.max_tokens) for r in order]
-    slots = SlotPool(n_slots)
+    slots = BlockPool(n_slots) if policy == RESERVE_PAGED else SlotPool(n_slots)
     pool: List[ReqState] = []
     nxt = 0
     it = 0
@@ -215,17 +302,19 @@ def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
         while nxt < len(states) and states[nxt].arrival <= it:
             pool.append(states[nxt])
             nxt += 1
+        before = {r.req_id: r.preempted for r in pool}
         if budgeted:
             sel = select_budget(pool, slots, max_bs, token_budget or big, chunk or big, policy)
         else:
             sel = [(r, default_rows(r)) for r in select(pool, slots, max_bs, policy)]
+        preempted = sorted(r.req_id for r in pool if r.preempted != before[r.req_id])
         run = [(r, n) for r, n in sel if n > 0]
         for r, n in sel:
             if n == 0:
                 r.state = INCREMENT  # admitted (slots reserved) but idle this iteration
         if run:
             rec = IterRecord(it, [r.req_id for r, _ in run], [n for _, n in run], [r.n_cached for r, _ in run],
-                             [r.slot_base for r, _ in run], [])
+                             [r.slot_base for r, _ in run], [], preempted)
             for r, _ in run:
                 r.state = RUNNING
             inflight.append((rec, run))
@@ -238,8 +327,8 @@ def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
             for r, n in done_run:
                 r.state = INCREMENT
                 r.n_cached += n
-                if r.n_cached < r.n_prompt:
-                    continue  # a prompt chunk: nothing generated yet
+                if r.n_cached < known_len(r):
+                    continue  # a chunk: known tokens remain unprocessed, nothing generated yet
                 r.n_generated += 1
                 if finished(r):
                     r.state = FINISHED

@@ -36,8 +36,8 @@ def compare_schedule(gpu_recs, trace, max_bs, n_slots, token_budget=None, chunk=
                                 policy=reserve_policy, n_workers=n_workers)
     assert len(gpu_recs) == len(orecs)
     for g, o in zip(gpu_recs, orecs):
-        assert (g.it, g.req_ids, g.n_new, g.n_ctx, g.slot_base, sorted(g.released)) == \
-               (o.it, o.req_ids, o.n_new, o.n_ctx, o.slot_base, sorted(o.released)), (g, o)
+        assert (g.it, g.req_ids, g.n_new, g.n_ctx, g.slot_base, sorted(g.released), sorted(g.preempted)) == \
+               (o.it, o.req_ids, o.n_new, o.n_ctx, o.slot_base, sorted(o.released), sorted(o.preempted)), (g, o)
     return orecs
 
 

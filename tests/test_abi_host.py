@@ -107,7 +107,7 @@ class _Sim:
                                          max_tokens=mt, out_len=lo, n_cached=0, n_generated=0, slot_base=-1,
                                          tokens=b.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
         self.ostates = [osched.ReqState(rid, a, lp, lo, mt) for rid, a, lp, lo, mt in self.trace]
-        self.oslots = osched.SlotPool(n_slots)
+        self.oslots = osched.BlockPool(n_slots) if policy == C.ORCA_RESERVE_PAGED else osched.SlotPool(n_slots)
         self.bi = (ctypes.c_int32 * max_bs)()
 
     def run(self):
@@ -138,7 +138,7 @@ class _Sim:
                 assert a.state == C.ORCA_RUNNING
                 L = a.n_sched
                 a.state, a.n_sched, a.n_cached = C.ORCA_INCREMENT, 0, a.n_cached + L
-                if a.n_cached < a.n_prompt:
+                if a.n_cached < a.n_prompt + a.n_generated:
                     continue
                 a.n_generated += 1
                 if a.n_generated >= a.out_len or a.n_prompt + a.n_generated >= a.max_tokens:
@@ -150,16 +150,18 @@ class _Sim:
                 if k == 0:
                     continue
                 r.n_cached += k
-                if r.n_cached < r.n_prompt:
+                if r.n_cached < osched.known_len(r):
                     continue
                 r.n_generated += 1
                 if osched.finished(r):
                     r.state = osched.FINISHED
                     self.oslots.release(r.req_id)
-            # requests admitted without a row wait in INCREMENT on both sides
+            # requests admitted without a row wait in INCREMENT, preempted ones in
+            # INITIATION, on both sides
             for j in range(n_arr):
-                if self.arr[j].state == C.ORCA_INCREMENT:
-                    assert self.ostates[j].state == osched.INCREMENT
+                if self.arr[j].state in (C.ORCA_INCREMENT, C.ORCA_INITIATION):
+                    assert self.arr[j].state == self.ostates[j].state, (it, j)
+                    assert self.arr[j].n_cached == self.ostates[j].n_cached
             it += 1
         C.orca_engine_destroy(self.eng)
         return it
@@ -206,9 +208,36 @@ def test_reserve_policy_select_bit_exact_vs_oracle(liborca, policy):
              policy=policy).run()
 
 
+def test_paged_select_bit_exact_vs_oracle(liborca):
+    rng = np.random.default_rng(26)
+    for trial in range(30):
+        n = int(rng.integers(2, 25))
+        trace = []
+        for i in range(n):
+            lp, lo = int(rng.integers(1, 60)), int(rng.integers(1, 30))
+            trace.append((i, int(rng.integers(0, 20)), lp, lo, lp + lo + int(rng.integers(0, 4))))
+        need = max(-(-(t[2] + t[3]) // 32) for t in trace)
+        budget = (int(rng.integers(8, 64)), int(rng.integers(4, 40))) if trial % 2 else None
+        _Sim(trace, max_bs=int(rng.integers(1, 9)), n_slots=32 * int(rng.integers(need, 2 * need + 2)),
+             budget=budget, policy=C.ORCA_RESERVE_PAGED).run()
+
+
+def test_paged_engine_has_no_reservations(liborca):
+    eng = C.orca_engine_create(_cfg(n_slots=64, policy=C.ORCA_RESERVE_PAGED))
+    try:
+        with pytest.raises(C.OrcaError) as ei:
+            C.orca_kv_reserve(eng, 1, 4)
+        assert ei.value.code == C.ORCA_ESTATE
+    finally:
+        C.orca_engine_destroy(eng)
+
+
 def test_bad_reserve_policy_rejected(liborca):
     with pytest.raises(C.OrcaError) as ei:
-        C.orca_kv_pool_bytes(_cfg(policy=3))
+        C.orca_kv_pool_bytes(_cfg(policy=4))
+    assert ei.value.code == C.ORCA_EINVAL
+    with pytest.raises(C.OrcaError) as ei:   # paged K/V: whole blocks
+        C.orca_kv_pool_bytes(_cfg(n_slots=100, policy=C.ORCA_RESERVE_PAGED))
     assert ei.value.code == C.ORCA_EINVAL
 
 

@@ -268,6 +268,42 @@ def test_chunked_prefill_token_budget(cuda, which):
     assert worst < tol, worst
 
 
+# ------------------------------------------------------------------ paged K/V
+
+@pytest.mark.parametrize("which", ["toy_fp32", "small_bf16"])
+def test_paged_kv_with_preemption(cuda, which):
+    """Paged K/V (blocks of 32 slots handed out as requests grow) in a pool
+    small enough that requests are preempted and recomputed: the integer
+    record (batches, rows, preemptions, releases) matches the oracle, and
+    every request's logits equal its own generation - the recomputation
+    after a preemption changes no result.  The bf16 case runs prompts on the
+    tensor-core attention (K/V tiles gathered block by block) and decode
+    rows with key splits over block runs."""
+    from iteration_level_selective_gb300 import _orca as C
+    if which == "toy_fp32":
+        shape, w, tol = synth.TOY, _toy_weights(seed=17), FP32_TOL
+        trace = synth.make_trace(10, (1, 40), (1, 20), vocab=shape.vocab, seed=18, rate_per_iter=1.5, forced=True)
+        kw = dict(max_bs=4, n_slots=4 * 32, max_rows=256)
+    else:
+        shape, tol = SMALL_BF16, BF16_TOL
+        w = synth.make_weights(shape, seed=19, w_std=0.05, bias_std=0.02, ln_std=0.1)
+        trace = synth.make_trace(10, (1, 160), (10, 60), vocab=shape.vocab, seed=20, rate_per_iter=1.5, forced=True)
+        kw = dict(max_bs=6, n_slots=6 * 32, max_rows=2048)
+    pol = C.ORCA_RESERVE_PAGED
+    recs, eng, pool = hz.run_gpu(shape, w, trace, teacher_force=True, keep_all=True, reserve_policy=pol, **kw)
+    hz.compare_schedule(recs, trace, max_bs=kw["max_bs"], n_slots=kw["n_slots"], reserve_policy=pol)
+    assert any(r.preempted for r in recs)
+    got_lg = hz.gpu_logits_by_request(recs)
+    worst = 0.0
+    for req in trace:
+        _, logits = hz.oracle_generate(shape, w, req, teacher_force=True)
+        assert len(got_lg[req.req_id]) == len(logits)
+        for g, o in zip(got_lg[req.req_id], logits):
+            worst = max(worst, hz.max_rel_err(g, o))
+    assert worst < tol, worst
+    assert C.orca_kv_usage(eng.handle, pool.arr, pool.n) == (0, 0)
+
+
 # ------------------------------------------------------------------ two batches in flight
 
 @pytest.mark.parametrize("which", ["toy_fp32", "small_bf16"])

@@ -539,3 +539,84 @@ def test_two_workers_invariants_random_traces():
                     gen[rid] += 1
         assert prompt_done == n_prompt
         assert all(gen[t.req_id] == t.out_len for t in trace)
+
+
+# ---------------------------------------------------------------- paged K/V (CS349D Lecture 2, 5.1 and 6.1)
+
+def test_block_pool_lowest_first_and_release():
+    b = scheduler.BlockPool(5 * scheduler.KV_BLOCK)
+    assert b.grow(7, 2) and b.table[7] == [0, 1]
+    assert b.grow(8, 1) and b.table[8] == [2]
+    assert not b.grow(9, 3) and b.held(9) == 0          # all or nothing
+    b.release(7)
+    assert b.grow(9, 3) and b.table[9] == [0, 1, 3]      # lowest free blocks first
+    assert b.n_rsrv == 4 * scheduler.KV_BLOCK
+
+
+def test_paged_with_ample_memory_is_algorithm_1():
+    rng = np.random.default_rng(45)
+    for trial in range(15):
+        n = int(rng.integers(3, 25))
+        trace = []
+        for i in range(n):
+            lp, lo = int(rng.integers(1, 60)), int(rng.integers(1, 12))
+            trace.append(_R(i, int(rng.integers(0, 20)), lp, lo, lp + lo + int(rng.integers(0, 4))))
+        kw = dict(max_bs=int(rng.integers(1, 9)))
+        plain = scheduler.run_schedule(trace, n_slots=100_000, **kw)
+        paged = scheduler.run_schedule(trace, n_slots=100_000 // 32 * 32, policy=scheduler.RESERVE_PAGED, **kw)
+        assert _records(plain) == _records(paged)
+        assert all(not r.preempted for r in paged)
+
+
+def test_paged_preemption_by_hand():
+    # two blocks (64 slots); A and B: prompt 30, 10 tokens each, both at 0.
+    #  it 0-2: both fit in one block each (positions 0..31)
+    #  it 3:   A's position 32 needs a second block; none is free, so the
+    #          latest arrival holding blocks (B) is preempted; B then needs
+    #          two blocks to recompute 33 known tokens and does not fit
+    #  it 4-9: A alone; it finishes at it 9 and frees both blocks
+    #  it 10:  B recomputes its 33 known tokens (30 prompt + 3 generated)
+    trace = [_R(0, 0, 30, 10, 40), _R(1, 0, 30, 10, 40)]
+    recs = scheduler.run_schedule(trace, max_bs=4, n_slots=64, policy=scheduler.RESERVE_PAGED)
+    got = [(r.it, r.req_ids, r.n_new, r.n_ctx, sorted(r.released), r.preempted) for r in recs]
+    want = [(0, [0, 1], [30, 30], [0, 0], [], []), (1, [0, 1], [1, 1], [30, 30], [], []),
+            (2, [0, 1], [1, 1], [31, 31], [], []), (3, [0], [1], [32], [], [1])]
+    want += [(t, [0], [1], [29 + t], [0] if t == 9 else [], []) for t in range(4, 10)]
+    want += [(10, [1], [33], [0], [], [])]
+    want += [(t, [1], [1], [22 + t], [1] if t == 16 else [], []) for t in range(11, 17)]
+    assert got == want
+
+
+def test_paged_invariants_random_traces():
+    rng = np.random.default_rng(46)
+    n_preempted = 0
+    for trial in range(30):
+        n = int(rng.integers(2, 20))
+        trace = []
+        for i in range(n):
+            lp, lo = int(rng.integers(1, 70)), int(rng.integers(1, 40))
+            trace.append(_R(i, int(rng.integers(0, 20)), lp, lo, lp + lo + int(rng.integers(0, 4))))
+        need = max(-(-(t.n_prompt + t.out_len) // 32) for t in trace)
+        n_slots = 32 * int(rng.integers(need, 2 * need + 3))
+        kw = dict(max_bs=int(rng.integers(1, 9)), n_slots=n_slots, policy=scheduler.RESERVE_PAGED)
+        if trial % 3 == 0:
+            kw.update(token_budget=int(rng.integers(8, 64)), chunk=int(rng.integers(4, 40)))
+        recs = scheduler.run_schedule(trace, **kw)
+        gen = {t.req_id: 0 for t in trace}
+        known = {t.req_id: t.n_prompt for t in trace}
+        cached = {t.req_id: 0 for t in trace}
+        for rec in recs:
+            for rid in rec.preempted:
+                cached[rid] = 0
+                n_preempted += 1
+            held = 0
+            for rid, L, c in zip(rec.req_ids, rec.n_new, rec.n_ctx):
+                assert c == cached[rid] and 1 <= L <= known[rid] - c
+                cached[rid] += L
+                if cached[rid] == known[rid]:
+                    gen[rid] += 1
+                    known[rid] += 1
+                held += -(-cached[rid] // 32)
+            assert held * 32 <= n_slots
+        assert all(gen[t.req_id] == t.out_len for t in trace)
+    assert n_preempted > 0   # the traces do exercise preemption
