@@ -44,14 +44,18 @@ constexpr int BM = kTcBM, BK = kTcBK;
 constexpr int kStageBudget = 200 * 1024;
 constexpr int kGroupM = 8;
 
-template <int BN>
+template <int BN, int KS = 1>
 struct Cfg {
-  // W tiles arrive as boxes of min(BN, 128) rows: one box for BN <= 128
-  // (tensor map with that box height), two 128-row boxes for BN = 256.
+  // A stage holds KS k-blocks of 64 columns, each a K-major SW128 sub-tile:
+  // A as one box {64, a_box rows, KS} (sub-tiles a_box * 128 bytes apart;
+  // room is kept for 128 rows each), W as boxes of min(BN, 128) rows - one
+  // box {64, BN, KS} for BN <= 128, two 128-row boxes for BN = 256 (KS = 1).
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN must be 32, 64, 128 or 256");
+  static_assert(KS == 1 || KS == 2 || KS == 4, "KS must be 1, 2 or 4");
+  static_assert(BN <= 128 || KS == 1, "256-wide tiles take one k-block per stage");
   static constexpr int BOX = BN < kTcBM ? BN : kTcBM;
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int A_BYTES = KS * BM * BK * 2;
+  static constexpr int B_BYTES = KS * BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = (kStageBudget / STAGE) > 12 ? 12 : (kStageBudget / STAGE);
   static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
@@ -66,18 +70,20 @@ struct Cfg {
 // every thread of the kernel.
 struct Sched {
   int nM, nN, KB, S, kbs, tiles, units;
-  __host__ __device__ void init(int M, int N, int K, int BN, int sm, const GemmScratch &scr) {
+  // KB counts stages' worth of k-blocks (K / (64 * KS)).
+  __host__ __device__ void init(int M, int N, int K, int BN, int KSb, int sm, const GemmScratch &scr) {
     nM = (M + BM - 1) / BM;
     nN = (N + BN - 1) / BN;
-    KB = K / BK;
+    KB = K / (BK * KSb);
     tiles = nM * nN;
     S = 1;
     kbs = KB;
     // The last unit of a tile reads all S partials through one SM, so split
-    // only long K (>= 16 k-blocks) and at most 4 ways.
-    if (scr.partials != nullptr && tiles > 0 && tiles * 2 <= sm && KB >= 16 && tiles <= scr.n_counters) {
+    // only long K (>= 16 k-blocks of 64) and at most 4 ways.
+    if (scr.partials != nullptr && tiles > 0 && tiles * 2 <= sm && KB * KSb >= 16 && tiles <= scr.n_counters) {
       int s = sm / tiles;
-      if (s > KB / 8) s = KB / 8;
+      if (s > KB * KSb / 8) s = KB * KSb / 8;
+      if (s > KB) s = KB;
       if (s > 4) s = 4;
       if (s > 1) {
         const int k = (KB + s - 1) / s;
@@ -184,12 +190,12 @@ __device__ __forceinline__ void finish_run(const EpiParams &epi, int row, int co
   }
 }
 
-template <int BN>
+template <int BN, int KS>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, int M_arg,
-                        const int32_t *M_dev, int N, int K, int sm, EpiParams epi, GemmScratch scr,
+                        const int32_t *M_dev, int N, int K, int sm, int a_box, EpiParams epi, GemmScratch scr,
                         int32_t *status) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, KS>;
   constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -208,7 +214,11 @@ __global__ void __launch_bounds__(192, 1)
   // M_dev is the descriptor header, written before the forward (not by an earlier kernel)
   const int M = M_dev != nullptr ? *M_dev : M_arg;
   Sched sc;
-  sc.init(M, N, K, BN, sm, scr);
+  sc.init(M, N, K, BN, KS, sm, scr);
+  // bytes of one stage: the A box (a_box rows; 64 for products of <= 64 rows,
+  // whose MMA rows 64..127 read the next sub-tile and are never stored) + W
+  const uint32_t stage_tx = (uint32_t)KS * a_box * BK * 2 + C::B_BYTES;
+  const uint32_t a_sub = (uint32_t)a_box * BK * 2;  // bytes between A sub-tiles of a stage
 
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -243,10 +253,10 @@ __global__ void __launch_bounds__(192, 1)
         sc.unit(blockIdx.x, m, n, kb0, kb1, tile, split);
         pre = min(ST, kb1 - kb0);
         for (int j = 0; j < pre; ++j) {  // ring round 0: the stages are free
-          mbar_expect_tx(&full[j], C::STAGE);
+          mbar_expect_tx(&full[j], stage_tx);
 #pragma unroll
           for (int h = 0; h < BN / C::BOX; ++h)
-            tma_load_2d(sB + j * C::B_BYTES + h * (C::BOX * BK * 2), &tmW, (kb0 + j) * BK, n * BN + h * C::BOX,
+            tma_load_3d(sB + j * C::B_BYTES + h * (C::BOX * BK * 2), &tmW, 0, n * BN + h * C::BOX, (kb0 + j) * KS,
                         &full[j]);
         }
       }
@@ -258,17 +268,18 @@ __global__ void __launch_bounds__(192, 1)
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % ST;
           if (it < pre) {  // W already requested
-            tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * BK, m * BM, &full[s]);
+            tma_load_3d(sA + s * C::A_BYTES, &tmA, 0, m * BM, kb * KS, &full[s]);
             continue;
           }
           const uint32_t ph = (uint32_t)(it / ST) & 1u;
           // once the CTA has aborted no further copy is issued
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status) || *abort_flag) continue;
-          mbar_expect_tx(&full[s], C::STAGE);
-          tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * BK, m * BM, &full[s]);
+          mbar_expect_tx(&full[s], stage_tx);
+          tma_load_3d(sA + s * C::A_BYTES, &tmA, 0, m * BM, kb * KS, &full[s]);
 #pragma unroll
           for (int h = 0; h < BN / C::BOX; ++h)
-            tma_load_2d(sB + s * C::B_BYTES + h * (C::BOX * BK * 2), &tmW, kb * BK, n * BN + h * C::BOX, &full[s]);
+            tma_load_3d(sB + s * C::B_BYTES + h * (C::BOX * BK * 2), &tmW, 0, n * BN + h * C::BOX, kb * KS,
+                        &full[s]);
         }
       }
       if (*abort_flag) drain_after_abort();  // copies issued before the abort land first
@@ -291,9 +302,11 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
             const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-              tc_mma(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), C::IDESC,
-                     (kb > kb0 || k > 0) ? 1u : 0u);
+            for (int j = 0; j < KS; ++j)
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k)
+                tc_mma(d_tmem, sw128_desc(a0 + j * a_sub + k * 32), sw128_desc(b0 + j * (BN * BK * 2) + k * 32),
+                       C::IDESC, (kb > kb0 || j > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(&empty[s]);
         }
@@ -387,12 +400,188 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Small-M products (one 128-row output tile in M): split-K over a thread-block
+// cluster.  With few rows the cost of a Linear is moving its operands into
+// the SMs, and every CTA of a narrow-tile split re-reads the whole activation
+// block.  Here each output tile of BN columns is one cluster of S CTAs; CTA
+// r of the cluster multiplies the r-th K-range (all its k-blocks loaded at
+// once, one shared-memory stage each, so there is no ring to recycle), puts
+// its fp32 partial tile in shared memory, and after a cluster barrier sums
+// BN/S columns of all S partials through distributed shared memory and runs
+// the epilogue on them.  The CTAs of a cluster are resident together, so the
+// barrier always completes; every other wait is bounded.  With at most 64
+// rows the A tile is loaded as a 64-row box (the MMA's rows 64..127 hold
+// stale shared memory and are never stored).
 template <int BN>
+struct CCfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int MAX_KB = (kStageBudget / STAGE) > 10 ? 10 : (kStageBudget / STAGE);
+  static constexpr int PSTRIDE = BN + 4;  // floats per partial row (16-byte chunks spread over the banks)
+  static constexpr int P_BYTES = BM * PSTRIDE * 4;
+  static constexpr int BODY = MAX_KB * STAGE > P_BYTES ? MAX_KB * STAGE : P_BYTES;
+  static constexpr int SMEM = BODY + 1024 + 256;  // the most a launch asks for
+  static constexpr uint32_t TMEM_COLS = BN;
+  // bytes of the stage area for kbs k-blocks (also holds the partial tile)
+  __host__ __device__ static constexpr int body(int kbs) { return kbs * STAGE > P_BYTES ? kbs * STAGE : P_BYTES; }
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// grid = nN * S CTAs in clusters of S; a_box = rows of one A box (64 or 128);
+// kbs = k-blocks per CTA (<= MAX_KB); the last rank may have fewer.
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                           int M_arg, const int32_t *M_dev, int N, int K, int S, int kbs, int a_box, EpiParams epi,
+                           int32_t *status) {
+  using C = CCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t *body = smem_raw + pad;
+  uint64_t *full = reinterpret_cast<uint64_t *>(body + C::body(kbs));
+  uint64_t *done = full + C::MAX_KB;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = M_dev != nullptr ? *M_dev : M_arg;  // M_dev: the descriptor header, written before the forward
+  const int rank = (int)cluster_rank();
+  const int n = blockIdx.x / S;  // output tile = cluster
+  const int KB = K / BK;
+  const int kb0 = rank * kbs, kb1 = min(KB, kb0 + kbs), nkb = max(0, kb1 - kb0);
+  const uint32_t a_bytes = (uint32_t)a_box * BK * 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::MAX_KB; ++s) mbar_init(&full[s], 1);
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0 && nkb <= C::MAX_KB && M <= BM) {  // TMA producer: every k-block of this rank at once
+      for (int j = 0; j < nkb; ++j) {  // weights do not depend on earlier kernels
+        uint8_t *st = body + j * C::STAGE;
+        mbar_expect_tx(&full[j], a_bytes + C::B_BYTES);
+#pragma unroll
+        for (int h = 0; h < BN / Cfg<BN>::BOX; ++h)
+          tma_load_3d(st + C::A_BYTES + h * (Cfg<BN>::BOX * BK * 2), &tmW, 0, n * BN + h * Cfg<BN>::BOX, kb0 + j,
+                      &full[j]);
+      }
+      pdl_wait();  // A (activations) comes from earlier kernels
+      for (int j = 0; j < nkb; ++j) tma_load_3d(body + j * C::STAGE, &tmA, 0, 0, kb0 + j, &full[j]);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      for (int j = 0; j < nkb && nkb <= C::MAX_KB && M <= BM; ++j) {
+        if (mbar_wait(&full[j], 0, abort_flag, status)) {
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(body + j * C::STAGE);
+          const uint32_t b0 = a0 + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma(tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), Cfg<BN>::IDESC, (j > 0 || k > 0) ? 1u : 0u);
+        }
+      }
+      tc_commit(done);  // also when there was nothing to multiply: the epilogue then writes zeros
+    }
+  } else {  // epilogue warps 2..5: TMEM lane quarter = warp % 4; own partial into shared memory
+    pdl_wait();
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, status)) && nkb > 0 &&
+                    nkb <= C::MAX_KB && M <= BM;
+    tc_fence_after();
+    float *P = reinterpret_cast<float *>(body) + (size_t)row * C::PSTRIDE;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      float v[32];
+      if (ok) {
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4 *>(P + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    }
+    tc_fence_before();
+  }
+  __syncwarp();
+  cluster_sync_all();  // every partial of the cluster is in shared memory
+  if (warp >= 2) {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int cw = BN / S;  // columns this rank reduces
+    const int c0 = rank * cw;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    const uint32_t mine = smem_u32(body) + (uint32_t)((row * C::PSTRIDE + c0) * 4);
+    for (int j = 0; j < S; ++j) {
+      const uint32_t src = map_to_rank(mine, (uint32_t)j);
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        if (i < cw) {
+          const float4 t = ld_cluster_f4(src + i * 4);
+          v[i] += t.x;
+          v[i + 1] += t.y;
+          v[i + 2] += t.z;
+          v[i + 3] += t.w;
+        }
+      }
+    }
+    unsigned long long best = 0ull;
+    const int col = n * BN + c0;
+    if (col < N && !*abort_flag) finish_run(epi, row, col, v, min(cw, N - col), row < M, best);
+    if (epi.argmax_keys != nullptr && best != 0ull) atomicMax(epi.argmax_keys + row, best);
+  }
+  if (threadIdx.x == 0 && (nkb > C::MAX_KB || M > BM)) atomicOr(status, kStatusBadShape);
+  __syncwarp();
+  cluster_sync_all();  // no CTA leaves while another still reads its shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int BN, int KS>
 cudaError_t set_smem_limit(int dev) {
   static uint64_t attr_mask = 0;  // one bit per device ordinal
   if (dev >= 64 || !(attr_mask & (1ull << dev))) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_bf16_kernel<BN, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<BN, KS>::SMEM);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_mask |= 1ull << dev;
   }
@@ -400,17 +589,53 @@ cudaError_t set_smem_limit(int dev) {
 }
 
 template <int BN>
+cudaError_t set_cluster_smem_limit(int dev) {
+  static uint64_t attr_mask = 0;
+  if (dev >= 64 || !(attr_mask & (1ull << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_cluster_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         CCfg<BN>::SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_mask |= 1ull << dev;
+  }
+  return cudaSuccess;
+}
+
+template <int BN>
+cudaError_t launch_cluster(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, const int32_t *M_dev, int N, int K,
+                           int S, int kbs, int a_box, const EpiParams &epi, int32_t *status, cudaStream_t st, int dev) {
+  cudaError_t e = set_cluster_smem_limit<BN>(dev);
+  if (e != cudaSuccess) return e;
+  const int nN = (N + BN - 1) / BN;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(nN * S);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = CCfg<BN>::body(kbs) + 1024 + 256;  // only what this launch uses
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_cluster_kernel<BN>, *tmA, *tmW, M, M_dev, N, K, S, kbs, a_box, epi,
+                            status);
+}
+
+template <int BN, int KS>
 cudaError_t launch_bn(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, const int32_t *M_dev, int N, int K,
-                      const EpiParams &epi, const GemmScratch &scr, int32_t *status, cudaStream_t st, int sm,
-                      int dev) {
-  cudaError_t e = set_smem_limit<BN>(dev);
+                      int a_box, const EpiParams &epi, const GemmScratch &scr, int32_t *status, cudaStream_t st,
+                      int sm, int dev) {
+  cudaError_t e = set_smem_limit<BN, KS>(dev);
   if (e != cudaSuccess) return e;
   Sched sc;
-  sc.init(M, N, K, BN, sm, scr);
+  sc.init(M, N, K, BN, KS, sm, scr);
   const int grid = M_dev != nullptr ? sm : (sc.units < sm ? sc.units : sm);
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(gemm_tc_bf16_kernel<BN>, grid, 192, Cfg<BN>::SMEM, st, *tmA, *tmW, M, M_dev, N, K, sm, epi, scr,
-                    status);
+  return launch_pdl(gemm_tc_bf16_kernel<BN, KS>, grid, 192, Cfg<BN, KS>::SMEM, st, *tmA, *tmW, M, M_dev, N, K, sm,
+                    a_box, epi, scr, status);
 }
 
 }  // namespace
@@ -426,9 +651,9 @@ int gemm_sm_count() {
   return n;
 }
 
-// Output-tile width: 256 when those tiles fill the GPU, else the widest of
-// 128 / 64 / 32 whose tiles occupy at least half the SMs (narrower tiles
-// spread a small-M product's weight stream over more SMs).
+// Output-tile width of the persistent kernel: 256 when those tiles fill the
+// GPU, else the widest of 128 / 64 / 32 whose tiles occupy at least half the
+// SMs (narrower tiles spread a small-M product's weight stream over more SMs).
 int gemm_tile_n(int M, int N) {
   const long long nM = (M + BM - 1) / BM;
   const int sm = gemm_sm_count();
@@ -438,34 +663,136 @@ int gemm_tile_n(int M, int N) {
   return 32;
 }
 
+namespace {
+
+int bn_code(int bn) { return bn == 256 ? 3 : bn == 128 ? 2 : bn == 64 ? 1 : 0; }
+
+// k-blocks per stage of the persistent kernel: one TMA box then carries
+// KS * 64 columns, so narrow tiles (whose per-box issue cost would dominate)
+// take 4, 128-wide tiles 2, 256-wide tiles 1; fewer when K is no multiple.
+int gemm_ks(int bn, int K) {
+  int ks = bn == 256 ? 1 : bn == 128 ? 2 : 4;
+  while (ks > 1 && K % (BK * ks) != 0) ks /= 2;
+  return ks;
+}
+int max_kb_cluster(int bn) {
+  return bn == 256 ? CCfg<256>::MAX_KB : bn == 128 ? CCfg<128>::MAX_KB : bn == 64 ? CCfg<64>::MAX_KB : CCfg<32>::MAX_KB;
+}
+
+}  // namespace
+
+// How one Linear runs.  Rows of one 128-row tile (M <= 128): the cluster
+// split-K kernel when its estimated critical path beats the persistent
+// kernel's; else the persistent kernel with gemm_tile_n's width.  The
+// estimate counts 128-byte rows of operand brought into one SM: per wave of
+// CTAs, k-blocks per CTA times (A rows + W rows), plus a fixed cost for a
+// CTA's start-up and teardown (about one microsecond of loading, paid once
+// per wave by the cluster kernel and once by the persistent one) and, for
+// the cluster kernel, the partial tile a CTA gathers.
+constexpr double kCtaFixedRows = 400.0;
+// The cluster kernel's extra steps (partial tile to shared memory, two
+// cluster barriers, the gather through distributed shared memory) measured
+// as about three more microseconds per wave on GB300.
+constexpr double kClusterFixedRows = 1600.0;
+GemmPlan gemm_plan(int M, int N, int K) {
+  GemmPlan p{};
+  p.bn = gemm_tile_n(M, N);
+  p.ks = gemm_ks(p.bn, K);
+  const int KB = K / BK;
+  if (M > BM || M <= 0 || KB <= 0) return p;
+  const int a_box = M <= 64 ? 64 : 128;
+  p.a_box = a_box;
+  const int sm = gemm_sm_count();
+  const long long waves_p = ((N + p.bn - 1) / p.bn + sm - 1) / sm;
+  const double cost_p = (double)waves_p * KB * (a_box + p.bn) + kCtaFixedRows;
+  double best = cost_p;
+  for (int bn : {32, 64, 128, 256}) {
+    const int nN = (N + bn - 1) / bn;
+    for (int S : {2, 4, 8}) {
+      const int kbs = (KB + S - 1) / S;
+      if (kbs > max_kb_cluster(bn) || nN * S > 16 * sm) continue;
+      const long long waves = ((long long)nN * S + sm - 1) / sm;
+      const double cost = (double)waves * (kbs * (a_box + bn) + kClusterFixedRows) + 4.0 * bn;
+      if (cost < best * 0.95) {
+        best = cost;
+        p.cluster = true;
+        p.bn = bn;
+        p.S = S;
+        p.kbs = kbs;
+        p.a_box = a_box;
+        p.ks = 1;
+      }
+    }
+  }
+  return p;
+}
+
+int gemm_plan_code(int M, int N, int K) {
+  const GemmPlan p = gemm_plan(M, N, K);
+  if (!p.cluster) return bn_code(p.bn) * 2 + (p.a_box == 64 ? 1 : 0);
+  return 8 + bn_code(p.bn) * 8 + (p.S == 2 ? 0 : p.S == 4 ? 1 : 2) * 2 + (p.a_box == 64 ? 1 : 0);
+}
+
 cudaError_t gemm_prepare() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = set_smem_limit<32>(dev);
-  if (e == cudaSuccess) e = set_smem_limit<64>(dev);
-  if (e == cudaSuccess) e = set_smem_limit<128>(dev);
-  if (e == cudaSuccess) e = set_smem_limit<256>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<32, 1>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<32, 2>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<32, 4>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<64, 1>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<64, 2>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<64, 4>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<128, 1>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<128, 2>(dev);
+  if (e == cudaSuccess) e = set_smem_limit<256, 1>(dev);
+  if (e == cudaSuccess) e = set_cluster_smem_limit<32>(dev);
+  if (e == cudaSuccess) e = set_cluster_smem_limit<64>(dev);
+  if (e == cudaSuccess) e = set_cluster_smem_limit<128>(dev);
+  if (e == cudaSuccess) e = set_cluster_smem_limit<256>(dev);
   gemm_sm_count();
   return e;
 }
 
-// M selects the tile width; with M_dev the kernel reads the row count from
-// the device (the tile width chosen from M must then stay valid for it).
-cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const WeightMaps &W, int M, const int32_t *M_dev, int N,
-                                int K, const EpiParams &epi, const GemmScratch &scr, int32_t *status,
-                                cudaStream_t st) {
+// M selects the plan; with M_dev the kernel reads the row count from the
+// device (the plan chosen from M must then stay valid for it: callers key
+// their CUDA graphs on gemm_plan_code).  A and W come as 3-D views
+// {64 columns, rows, K / 64} with boxes of 32 / 64 / 128 rows by 1 / 2 / 4
+// k-blocks; the plan picks the ones it loads.
+cudaError_t launch_gemm_tc_bf16(const OperandMaps &A, const OperandMaps &W, int M, const int32_t *M_dev, int N, int K,
+                                const EpiParams &epi, const GemmScratch &scr, int32_t *status, cudaStream_t st) {
   if (M <= 0 && M_dev == nullptr) return cudaSuccess;
   if (K % BK != 0 || K <= 0) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const int sm = gemm_sm_count();
-  switch (gemm_tile_n(M, N)) {
-    case 256: return launch_bn<256>(tmA, &W.box128, M, M_dev, N, K, epi, scr, status, st, sm, dev);
-    case 128: return launch_bn<128>(tmA, &W.box128, M, M_dev, N, K, epi, scr, status, st, sm, dev);
-    case 64: return launch_bn<64>(tmA, &W.box64, M, M_dev, N, K, epi, scr, status, st, sm, dev);
-    default: return launch_bn<32>(tmA, &W.box32, M, M_dev, N, K, epi, scr, status, st, sm, dev);
+  const GemmPlan p = gemm_plan(M, N, K);
+  const CUtensorMap *a1 = A.get(p.a_box, 1);
+  if (p.cluster) {
+    switch (p.bn) {
+      case 256: return launch_cluster<256>(a1, W.get(128, 1), M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
+      case 128: return launch_cluster<128>(a1, W.get(128, 1), M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
+      case 64: return launch_cluster<64>(a1, W.get(64, 1), M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
+      default: return launch_cluster<32>(a1, W.get(32, 1), M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
+    }
   }
+  const int ks = p.ks;
+  const CUtensorMap *a = A.get(p.a_box, ks);
+#define ORCA_GEMM_CASE(BN_, KS_)                                                                          \
+  if (p.bn == BN_ && ks == KS_)                                                                           \
+    return launch_bn<BN_, KS_>(a, W.get(BN_ < 128 ? BN_ : 128, KS_), M, M_dev, N, K, p.a_box, epi, scr, status, st, \
+                               sm, dev);
+  ORCA_GEMM_CASE(256, 1)
+  ORCA_GEMM_CASE(128, 2)
+  ORCA_GEMM_CASE(128, 1)
+  ORCA_GEMM_CASE(64, 4)
+  ORCA_GEMM_CASE(64, 2)
+  ORCA_GEMM_CASE(64, 1)
+  ORCA_GEMM_CASE(32, 4)
+  ORCA_GEMM_CASE(32, 2)
+  ORCA_GEMM_CASE(32, 1)
+#undef ORCA_GEMM_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace orca

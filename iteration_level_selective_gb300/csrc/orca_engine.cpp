@@ -341,13 +341,14 @@ struct orca_engine {
   IterSlot slot[kMaxInflight];
   int q_head = 0, q_len = 0;  // submitted iterations, oldest first
   // tensor maps (bf16)
-  CUtensorMap tm_h{}, tm_u{}, tm_hf{}, tm_q{};
+  OperandMaps tm_h{}, tm_u{}, tm_hf{};  // GEMM activation operands
+  CUtensorMap tm_q{};
   std::vector<CUtensorMap> tm_k;      // per layer: K slots as [n_heads * n_slots, head_dim]
   std::vector<CUtensorMap> tm_v;      // per layer: V slots, same view
   std::vector<CUtensorMap> tm_kb, tm_vb;  // per layer: the same views in kKvBlock-row boxes (paged)
   bool attn_tc = false;               // prompts take the tensor-core prefill kernel
-  WeightMaps tm_emb{};
-  std::vector<WeightMaps> tm_layer;  // 4 per layer: qkv, o, fc1, fc2
+  OperandMaps tm_emb{};
+  std::vector<OperandMaps> tm_layer;  // 4 per layer: qkv, o, fc1, fc2
   // last descriptor (host copy)
   int32_t last_B = 0, last_N = 0, last_work = 0, last_launches = 0;
   int32_t n_launch = 0;               // kernels enqueued by the current eager forward
@@ -366,7 +367,7 @@ struct orca_engine {
     cudaGraphExec_t exec;
     int32_t n_kernels;  // kernel nodes in the captured forward
   };
-  std::map<std::pair<uint32_t, uintptr_t>, Graph> graphs;
+  std::map<std::pair<uint64_t, uintptr_t>, Graph> graphs;
 };
 
 namespace {
@@ -399,33 +400,63 @@ int fail(orca_engine *e, int code, const char *fmt, ...) {
 
 template <typename T> T *ws_ptr(orca_engine *e, size_t off) { return reinterpret_cast<T *>(e->ws + off); }
 
-int make_tmap(orca_engine *e, CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols,
-              uint32_t box_rows) {
+PFN_cuTensorMapEncodeTiled_v12000 encoder(orca_engine *e) {
   if (!g_encode) {
     cudaDriverEntryPointQueryResult q;
     void *fn = nullptr;
     cudaError_t r = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (r != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-      return fail(e, ORCA_ECUDA, "cuTensorMapEncodeTiled is not available");
+    if (r != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+      fail(e, ORCA_ECUDA, "cuTensorMapEncodeTiled is not available");
+      return nullptr;
+    }
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
+  return g_encode;
+}
+
+// Row-major bf16 [rows, cols] in boxes of 64 columns x box_rows rows (SW128).
+int make_tmap(orca_engine *e, CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols,
+              uint32_t box_rows) {
+  auto enc = encoder(e);
+  if (!enc) return ORCA_ECUDA;
   if (reinterpret_cast<uintptr_t>(base) & 15) return fail(e, ORCA_EINVAL, "TMA base must be 16-byte aligned");
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(e, ORCA_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return ORCA_OK;
 }
 
-int make_weight_maps(orca_engine *e, WeightMaps *w, const void *base, uint64_t rows, uint64_t cols) {
-  int rc = make_tmap(e, &w->box128, base, rows, cols, 128);
-  if (!rc) rc = make_tmap(e, &w->box64, base, rows, cols, 64);
-  if (!rc) rc = make_tmap(e, &w->box32, base, rows, cols, 32);
-  return rc;
+// GEMM operand views: the same row-major bf16 [rows, cols] seen as
+// {64 columns, rows, cols / 64 k-blocks}, so that one box of
+// {64, box_rows, ks} brings ks consecutive K-major SW128 sub-tiles.  Box
+// heights 32 / 64 / 128 by ks 1 / 2 / 4; a ks above cols / 64 is never
+// chosen and left unencoded.
+int make_operand_maps(orca_engine *e, OperandMaps *m, const void *base, uint64_t rows, uint64_t cols) {
+  auto enc = encoder(e);
+  if (!enc) return ORCA_ECUDA;
+  if (reinterpret_cast<uintptr_t>(base) & 15) return fail(e, ORCA_EINVAL, "TMA base must be 16-byte aligned");
+  if (cols % kTcBK) return fail(e, ORCA_EINVAL, "GEMM operand width %llu is no multiple of 64", (unsigned long long)cols);
+  *m = OperandMaps{};
+  const uint32_t heights[3] = {32, 64, 128};
+  const uint32_t kss[3] = {1, 2, 4};
+  for (int b = 0; b < 3; ++b)
+    for (int k = 0; k < 3; ++k) {
+      if (kss[k] > cols / kTcBK) continue;
+      cuuint64_t dims[3] = {(cuuint64_t)kTcBK, rows, cols / kTcBK};
+      cuuint64_t strides[2] = {cols * 2, (cuuint64_t)kTcBK * 2};
+      cuuint32_t box[3] = {(cuuint32_t)kTcBK, heights[b], kss[k]};
+      cuuint32_t es[3] = {1, 1, 1};
+      CUresult r = enc(&m->m[b][k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                       es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(e, ORCA_ECUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", (int)r);
+    }
+  return ORCA_OK;
 }
 
 // Weight pointer index helpers (order documented in orca.h).
@@ -556,7 +587,8 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     ep.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      LAUNCH(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 0], N, N_dev, 3 * H, H, ep, scr, status, st));
+      LAUNCH(e, launch_gemm_tc_bf16(e->tm_h, e->tm_layer[4 * l + 0], N, N_dev, 3 * H, H, ep, scr,
+                                    status, st));
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WQKV), N, 3 * H, H, ep, st));
     prof_end(e, st, ev, ORCA_K_GEMM_QKV, 2.0 * N * 3 * H * H, gemm_bytes(N, 3.0 * H, H, eb));
@@ -612,7 +644,8 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     eo.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      LAUNCH(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 1], N, N_dev, H, H, eo, scr, status, st));
+      LAUNCH(e, launch_gemm_tc_bf16(e->tm_h, e->tm_layer[4 * l + 1], N, N_dev, H, H, eo, scr, status,
+                                    st));
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WO), N, H, H, eo, st));
     prof_end(e, st, ev, ORCA_K_GEMM_O, 2.0 * N * H * H, gemm_bytes(N, H, H, 8));
@@ -630,7 +663,8 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     e1.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      LAUNCH(e, launch_gemm_tc_bf16(&e->tm_h, e->tm_layer[4 * l + 2], N, N_dev, F, H, e1, scr, status, st));
+      LAUNCH(e, launch_gemm_tc_bf16(e->tm_h, e->tm_layer[4 * l + 2], N, N_dev, F, H, e1, scr, status,
+                                    st));
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_W1), N, F, H, e1, st));
     prof_end(e, st, ev, ORCA_K_GEMM_FC1, 2.0 * N * F * H, gemm_bytes(N, F, H, eb));
@@ -643,7 +677,8 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     e2.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      LAUNCH(e, launch_gemm_tc_bf16(&e->tm_u, e->tm_layer[4 * l + 3], N, N_dev, H, F, e2, scr, status, st));
+      LAUNCH(e, launch_gemm_tc_bf16(e->tm_u, e->tm_layer[4 * l + 3], N, N_dev, H, F, e2, scr, status,
+                                    st));
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)u, (const float *)lw(e, l, L_W2), N, H, F, e2, st));
     prof_end(e, st, ev, ORCA_K_GEMM_FC2, 2.0 * N * H * F, gemm_bytes(N, H, F, 8));
@@ -663,7 +698,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
   el.argmax_keys = bf16 ? d_keys : nullptr;
   prof_begin(e, st, &ev);
   if (bf16)
-    LAUNCH(e, launch_gemm_tc_bf16(&e->tm_hf, e->tm_emb, B, B_dev, V, H, el, scr, status, st));
+    LAUNCH(e, launch_gemm_tc_bf16(e->tm_hf, e->tm_emb, B, B_dev, V, H, el, scr, status, st));
   else
     LAUNCH(e, launch_gemm_simt_f32((const float *)hf, (const float *)e->w[W_TOK], B, V, H, el, st));
   prof_end(e, st, ev, ORCA_K_LM_HEAD, 2.0 * B * V * H, gemm_bytes(B, V, H, logits ? 4 : 0));
@@ -778,10 +813,10 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
   if (cfg->dtype == ORCA_DTYPE_BF16) {
     const uint64_t H = cfg->hidden, F = cfg->ffn;
     e->tm_layer.resize(4 * cfg->n_layers);
-    rc = make_tmap(e, &e->tm_h, e->ws + L.h, cfg->max_rows, H, kTcBM);
-    if (!rc) rc = make_tmap(e, &e->tm_u, e->ws + L.u, cfg->max_rows, F, kTcBM);
-    if (!rc) rc = make_tmap(e, &e->tm_hf, e->ws + L.hf, cfg->max_bs, H, kTcBM);
-    if (!rc) rc = make_weight_maps(e, &e->tm_emb, e->w[W_TOK], cfg->vocab, H);
+    rc = make_operand_maps(e, &e->tm_h, e->ws + L.h, cfg->max_rows, H);
+    if (!rc) rc = make_operand_maps(e, &e->tm_u, e->ws + L.u, cfg->max_rows, F);
+    if (!rc) rc = make_operand_maps(e, &e->tm_hf, e->ws + L.hf, cfg->max_bs, H);
+    if (!rc) rc = make_operand_maps(e, &e->tm_emb, e->w[W_TOK], cfg->vocab, H);
     e->attn_tc = attention_tc_supported(cfg->dtype, e->head_dim);
     if (!rc && e->attn_tc) {
       rc = make_tmap(e, &e->tm_q, e->ws + L.q, cfg->max_rows, H, kTcBM);
@@ -800,10 +835,10 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
       }
     }
     for (int l = 0; l < cfg->n_layers && !rc; ++l) {
-      rc = make_weight_maps(e, &e->tm_layer[4 * l + 0], lw(e, l, L_WQKV), 3 * H, H);
-      if (!rc) rc = make_weight_maps(e, &e->tm_layer[4 * l + 1], lw(e, l, L_WO), H, H);
-      if (!rc) rc = make_weight_maps(e, &e->tm_layer[4 * l + 2], lw(e, l, L_W1), F, H);
-      if (!rc) rc = make_weight_maps(e, &e->tm_layer[4 * l + 3], lw(e, l, L_W2), H, F);
+      rc = make_operand_maps(e, &e->tm_layer[4 * l + 0], lw(e, l, L_WQKV), 3 * H, H);
+      if (!rc) rc = make_operand_maps(e, &e->tm_layer[4 * l + 1], lw(e, l, L_WO), H, H);
+      if (!rc) rc = make_operand_maps(e, &e->tm_layer[4 * l + 2], lw(e, l, L_W1), F, H);
+      if (!rc) rc = make_operand_maps(e, &e->tm_layer[4 * l + 3], lw(e, l, L_W2), H, F);
     }
     if (rc) {
       orca_engine_destroy(e);
@@ -1169,12 +1204,12 @@ int orca_iteration_submit(orca_engine *e, orca_request *pool, const int32_t *bat
   float *logits = logits_dev ? logits_dev : (bf16 ? nullptr : ws_ptr<float>(e, Ly.logits));
   const bool use_graph = bf16 && !e->prof && !(flags & ORCA_ITER_EAGER);
   if (use_graph) {
-    auto code = [](int bn) { return (uint32_t)(bn == 256 ? 3 : bn == 128 ? 2 : bn == 64 ? 1 : 0); };
-    // graphs differ in their GEMM tile choices, in whether the tensor-core
-    // prompt attention runs at all, and in the in-flight slot they read
-    const uint32_t key = code(gemm_tile_n(N, 3 * H)) | (code(gemm_tile_n(N, H)) << 2) |
-                         (code(gemm_tile_n(N, F)) << 4) | (code(gemm_tile_n(n_batch, V)) << 6) |
-                         ((uint32_t)(n_work_tc > 0) << 8) | ((uint32_t)k << 9);
+    // graphs differ in their GEMM plans, in whether the tensor-core prompt
+    // attention runs at all, and in the in-flight slot they read
+    const uint64_t key = (uint64_t)gemm_plan_code(N, 3 * H, H) | ((uint64_t)gemm_plan_code(N, H, H) << 6) |
+                         ((uint64_t)gemm_plan_code(N, F, H) << 12) | ((uint64_t)gemm_plan_code(N, H, F) << 18) |
+                         ((uint64_t)gemm_plan_code(n_batch, V, H) << 24) | ((uint64_t)(n_work_tc > 0) << 30) |
+                         ((uint64_t)k << 31);
     const auto gk = std::make_pair(key, reinterpret_cast<uintptr_t>(logits));
     auto it = e->graphs.find(gk);
     if (it == e->graphs.end()) {
@@ -1484,10 +1519,9 @@ int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const
     if (cudaMemsetAsync(scratch, 0, kGemmMaxSms * 4, st) != cudaSuccess) return ORCA_ECUDA;
   }
   if (argmax_keys_dev && cudaMemsetAsync(argmax_keys_dev, 0, (size_t)M * 8, st) != cudaSuccess) return ORCA_ECUDA;
-  CUtensorMap ta;
-  WeightMaps tw;
-  if (make_tmap(nullptr, &ta, A, M, K, kTcBM) || make_weight_maps(nullptr, &tw, W, N, K)) return ORCA_EINVAL;
-  return launch_gemm_tc_bf16(&ta, tw, M, nullptr, N, K, ep, scr, status_dev, st) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
+  OperandMaps ta, tw;
+  if (make_operand_maps(nullptr, &ta, A, M, K) || make_operand_maps(nullptr, &tw, W, N, K)) return ORCA_EINVAL;
+  return launch_gemm_tc_bf16(ta, tw, M, nullptr, N, K, ep, scr, status_dev, st) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
 }
 
 int orca_profile_enable(orca_engine *e, int32_t enable) {

@@ -174,14 +174,34 @@ cudaError_t launch_gemm_simt_f32(const float *A, const float *W, int M, int N, i
                                  const EpiParams &epi, cudaStream_t st);
 // TMA maps of one weight matrix [N, K] with 128-, 64- and 32-row boxes
 // (the GEMM picks its output-tile width per product).
-struct WeightMaps {
-  CUtensorMap box128, box64, box32;
+// TMA maps of one bf16 operand [rows, cols] (cols a multiple of 64) for the
+// tcgen05 GEMM, viewed in three dimensions {64, rows, cols / 64} with the
+// 64-column blocks as the outer dimension (strides: a row, 128 bytes), so one
+// box {64, box rows, ks} brings ks k-blocks of 64 columns, each a 128-byte-
+// swizzled K-major sub-tile of `box rows` rows.  m[b][k]: box rows 32 / 64 /
+// 128 (b = 0, 1, 2) and ks = 1 / 2 / 4 (k = 0, 1, 2).
+struct OperandMaps {
+  CUtensorMap m[3][3];
+  const CUtensorMap *get(int box_rows, int ks) const {
+    const int b = box_rows == 32 ? 0 : box_rows == 64 ? 1 : 2;
+    const int k = ks == 1 ? 0 : ks == 2 ? 1 : 2;
+    return &m[b][k];
+  }
 };
 
 // C = A W^T on tcgen05.  M rows (or *M_dev when M_dev is given: the grid is
 // then sized for max_M rows and idle CTAs exit).  Split-K is used when the
 // output has few tiles and `scratch` is large enough.
-cudaError_t launch_gemm_tc_bf16(const CUtensorMap *tmA, const WeightMaps &W, int M, const int32_t *M_dev, int N,
+// How one Linear runs (persistent kernel with tile width bn, or the cluster
+// split-K kernel with S CTAs per output tile, kbs k-blocks each, A boxes of
+// a_box rows); gemm_plan_code is a small integer unique per plan.
+struct GemmPlan {
+  bool cluster = false;
+  int bn = 128, S = 1, kbs = 0, a_box = 128, ks = 1;
+};
+GemmPlan gemm_plan(int M, int N, int K);
+int gemm_plan_code(int M, int N, int K);
+cudaError_t launch_gemm_tc_bf16(const OperandMaps &A, const OperandMaps &W, int M, const int32_t *M_dev, int N,
                                 int K, const EpiParams &epi, const GemmScratch &scratch, int32_t *status,
                                 cudaStream_t st);
 int gemm_sm_count();
