@@ -316,7 +316,11 @@ int orca_argmax_rows(const float *logits_dev, int32_t n_rows, int32_t vocab, int
  *   ORCA_LINEAR_F32OUT: out[M, N] fp32 (out may be NULL when argmax_keys_dev
  *   is given).
  * bf16 runs on tcgen05 tensor cores and needs K % 64 == 0 and 16-byte
- * aligned A and W; fp32 runs CUDA-core FMA.
+ * aligned A and W; fp32 runs CUDA-core FMA.  The bf16 kernel starts reading
+ * W and bias before the work enqueued ahead of it on `stream` has finished
+ * (programmatic dependent launch; A and out wait for it), so W and bias must
+ * not be written by the library call enqueued just before it on the same
+ * stream.
  * scratch / scratch_bytes: optional 256-byte aligned device scratch; with
  *   enough of it (counters, then fp32 partial tiles) a bf16 product with few
  *   output tiles is split along K over more SMs; NULL disables that.
@@ -324,7 +328,7 @@ int orca_argmax_rows(const float *logits_dev, int32_t n_rows, int32_t vocab, int
  *   the call, receiving each row's greedy choice packed as key = (ordered
  *   value bits << 32) | (0xFFFFFFFF - column); key 0 means no column.
  * status_dev: device int32 that kernels OR error bits into (1 wait timeout,
- * 2 bad index).  Enqueued on `stream`, not synchronised. */
+ * 2 bad index, 4 unsupported shape).  Enqueued on `stream`, not synchronised. */
 #define ORCA_LINEAR_STORE 0
 #define ORCA_LINEAR_GELU 1
 #define ORCA_LINEAR_RESID 2

@@ -216,7 +216,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   __shared__ TcShared<NS> sh;
-  pdl_trigger();
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *sQ = smem_raw + pad;
   uint8_t *sK = sQ + C::Q_BYTES;       // NS stages of K
@@ -258,6 +257,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   tc_fence_after();
   const uint32_t tmem = sh.tmem;
   volatile int *abort_flag = &sh.abort;
+  // The next kernel may start only once this CTA holds its tensor memory: a
+  // dependent CTA that allocated first and then waited for this kernel could
+  // otherwise leave it without columns.
+  pdl_trigger();
   pdl_wait();  // q and the K/V slots come from the QKV Linear; the output rows are its input
 
   if (warp == 0) {

@@ -47,18 +47,28 @@ constexpr int kGroupM = 8;
 template <int BN, int KS = 1>
 struct Cfg {
   // A stage holds KS k-blocks of 64 columns, each a K-major SW128 sub-tile:
-  // A as one box {64, a_box rows, KS} (sub-tiles a_box * 128 bytes apart;
-  // room is kept for 128 rows each), W as boxes of min(BN, 128) rows - one
-  // box {64, BN, KS} for BN <= 128, two 128-row boxes for BN = 256 (KS = 1).
+  // A as one box {64, a_box rows, KS} (sub-tiles a_box * 128 bytes apart),
+  // W as boxes of min(BN, 128) rows - one box {64, BN, KS} for BN <= 128,
+  // two 128-row boxes for BN = 256 (KS = 1).  The ring takes as many stages
+  // of this size as fit in the budget (up to 12): with 64-row A boxes twice
+  // as many A sub-tiles fit.
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "BN must be 32, 64, 128 or 256");
   static_assert(KS == 1 || KS == 2 || KS == 4, "KS must be 1, 2 or 4");
   static_assert(BN <= 128 || KS == 1, "256-wide tiles take one k-block per stage");
   static constexpr int BOX = BN < kTcBM ? BN : kTcBM;
-  static constexpr int A_BYTES = KS * BM * BK * 2;
   static constexpr int B_BYTES = KS * BN * BK * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (kStageBudget / STAGE) > 12 ? 12 : (kStageBudget / STAGE);
-  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+  static constexpr int MAX_STAGES = 12;
+  static constexpr int SMEM = kStageBudget + 1024 + 256;  // the most a launch asks for
+  // stage bytes of the A part for boxes of a_box rows
+  __host__ __device__ static constexpr int a_stage(int a_box) { return KS * a_box * BK * 2; }
+  __host__ __device__ static constexpr int stages(int a_box) {
+    return kStageBudget / (a_stage(a_box) + B_BYTES) > MAX_STAGES ? MAX_STAGES
+                                                                   : kStageBudget / (a_stage(a_box) + B_BYTES);
+  }
+  // dynamic shared memory of a launch: the ring, then its barriers
+  __host__ __device__ static constexpr int smem(int a_box) {
+    return stages(a_box) * (a_stage(a_box) + B_BYTES) + 1024 + 256;
+  }
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   // Instruction descriptor, kind::f16: D fp32 (bit 4), A bf16 (bits 7-9),
   // B bf16 (bits 10-12), both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28.
@@ -170,11 +180,16 @@ __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" 
 // this thread's row.  Every lane of the warp calls it (the bias of the 32
 // columns is one coalesced load, broadcast by shuffles); `active` masks rows
 // beyond M.
+// Bias of column col + lane (0 past the run or without bias).
+__device__ __forceinline__ float run_bias(const EpiParams &epi, int col, int cnt) {
+  const int lane = threadIdx.x & 31;
+  return epi.bias != nullptr && lane < cnt ? __ldg(epi.bias + col + lane) : 0.f;
+}
+
+// bl: this lane's bias value of the run (run_bias), loaded ahead.
 __device__ __forceinline__ void finish_run(const EpiParams &epi, int row, int col, float *v, int cnt, bool active,
-                                           unsigned long long &best) {
+                                           unsigned long long &best, float bl) {
   if (epi.bias != nullptr) {
-    const int lane = threadIdx.x & 31;
-    const float bl = col + lane < col + cnt ? __ldg(epi.bias + col + lane) : 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] += __shfl_sync(0xffffffffu, bl, i);
   }
@@ -196,28 +211,29 @@ __global__ void __launch_bounds__(192, 1)
                         const int32_t *M_dev, int N, int K, int sm, int a_box, EpiParams epi, GemmScratch scr,
                         int32_t *status) {
   using C = Cfg<BN, KS>;
-  constexpr int ST = C::STAGES;
+  const int ST = C::stages(a_box);
+  const int A_ST = C::a_stage(a_box);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *sA = smem_raw + pad;
-  uint8_t *sB = sA + ST * C::A_BYTES;
+  uint8_t *sB = sA + ST * A_ST;
   uint64_t *full = reinterpret_cast<uint64_t *>(sB + ST * C::B_BYTES);
-  uint64_t *empty = full + ST;
-  uint64_t *tfull = empty + ST;
+  uint64_t *empty = full + C::MAX_STAGES;
+  uint64_t *tfull = empty + C::MAX_STAGES;
   uint64_t *tempty = tfull + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *last_flag = abort_flag + 1;
 
-  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // M_dev is the descriptor header, written before the forward (not by an earlier kernel)
   const int M = M_dev != nullptr ? *M_dev : M_arg;
   Sched sc;
   sc.init(M, N, K, BN, KS, sm, scr);
   // bytes of one stage: the A box (a_box rows; 64 for products of <= 64 rows,
-  // whose MMA rows 64..127 read the next sub-tile and are never stored) + W
-  const uint32_t stage_tx = (uint32_t)KS * a_box * BK * 2 + C::B_BYTES;
+  // whose MMA rows 64..127 read the next 8 KB of shared memory - still inside
+  // the stage area - and are never stored) + W
+  const uint32_t stage_tx = (uint32_t)A_ST + C::B_BYTES;
   const uint32_t a_sub = (uint32_t)a_box * BK * 2;  // bytes between A sub-tiles of a stage
 
   if (threadIdx.x == 0) {
@@ -241,6 +257,10 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The next kernel may start only once this CTA holds its tensor memory: a
+  // dependent CTA that allocated first and then waited for this kernel could
+  // otherwise leave it without columns.
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
@@ -261,21 +281,21 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       pdl_wait();  // A (activations) comes from earlier kernels
-      int it = 0;
+      // ring position (stage s, its phase parity ph) of copy number it
+      int it = 0, s = 0;
+      uint32_t ph = 0;
       for (int u = blockIdx.x; u < sc.units; u += gridDim.x) {
         int m, n, kb0, kb1, tile, split;
         sc.unit(u, m, n, kb0, kb1, tile, split);
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % ST;
+        for (int kb = kb0; kb < kb1; ++kb, ++it, s = s + 1 == ST ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
           if (it < pre) {  // W already requested
-            tma_load_3d(sA + s * C::A_BYTES, &tmA, 0, m * BM, kb * KS, &full[s]);
+            tma_load_3d(sA + s * A_ST, &tmA, 0, m * BM, kb * KS, &full[s]);
             continue;
           }
-          const uint32_t ph = (uint32_t)(it / ST) & 1u;
           // once the CTA has aborted no further copy is issued
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status) || *abort_flag) continue;
           mbar_expect_tx(&full[s], stage_tx);
-          tma_load_3d(sA + s * C::A_BYTES, &tmA, 0, m * BM, kb * KS, &full[s]);
+          tma_load_3d(sA + s * A_ST, &tmA, 0, m * BM, kb * KS, &full[s]);
 #pragma unroll
           for (int h = 0; h < BN / C::BOX; ++h)
             tma_load_3d(sB + s * C::B_BYTES + h * (C::BOX * BK * 2), &tmW, 0, n * BN + h * C::BOX, kb * KS,
@@ -286,7 +306,8 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
-      int it = 0, i = 0;
+      int i = 0, s = 0;
+      uint32_t ph = 0;
       for (int u = blockIdx.x; u < sc.units; u += gridDim.x, ++i) {
         int m, n, kb0, kb1, tile, split;
         sc.unit(u, m, n, kb0, kb1, tile, split);
@@ -294,12 +315,10 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
         mbar_wait(&tempty[acc], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, status);
         tc_fence_after();
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % ST;
-          const uint32_t ph = (uint32_t)(it / ST) & 1u;
+        for (int kb = kb0; kb < kb1; ++kb, s = s + 1 == ST ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
           if (mbar_wait(&full[s], ph, abort_flag, status)) {
             tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + s * C::A_BYTES);
+            const uint32_t a0 = smem_u32(sA + s * A_ST);
             const uint32_t b0 = smem_u32(sB + s * C::B_BYTES);
 #pragma unroll
             for (int j = 0; j < KS; ++j)
@@ -314,13 +333,20 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {  // epilogue warps 2..5: TMEM lane quarter = warp % 4
-    pdl_wait();  // the epilogue reads / writes buffers of earlier kernels (x, K/V slots)
     const int q = warp & 3;
     int i = 0;
     for (int u = blockIdx.x; u < sc.units; u += gridDim.x, ++i) {
       int m, n, kb0, kb1, tile, split;
       sc.unit(u, m, n, kb0, kb1, tile, split);
       const int acc = i & 1;
+      // the bias (a weight, like W) is loaded while the tile is computed
+      float bias_r[BN / 32];
+#pragma unroll
+      for (int r = 0; r < BN / 32; ++r) {
+        const int col = n * BN + 32 * r;
+        bias_r[r] = col < N ? run_bias(epi, col, min(32, N - col)) : 0.f;
+      }
+      if (i == 0) pdl_wait();  // the epilogue reads / writes buffers of earlier kernels (x, K/V slots)
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], (uint32_t)(i >> 1) & 1u, abort_flag, status));
       tc_fence_after();
       const int row = m * BM + q * 32 + lane;
@@ -337,7 +363,11 @@ __global__ void __launch_bounds__(192, 1)
             if (lane == 0) mbar_arrive(&tempty[acc]);
           }
           const int col = n * BN + c;
-          if (ok && col < N) finish_run(epi, row, col, v, min(32, N - col), row < M, best);
+          float bl = 0.f;
+#pragma unroll
+          for (int r = 0; r < BN / 32; ++r)
+            if (r == c / 32) bl = bias_r[r];
+          if (ok && col < N) finish_run(epi, row, col, v, min(32, N - col), row < M, best, bl);
         }
       } else {
         float *part = scr.partials + ((size_t)(tile * sc.S + split) * BM + q * 32 + lane) * BN;
@@ -384,7 +414,11 @@ __global__ void __launch_bounds__(192, 1)
                   v[4 * j + 3] += t.w;
                 }
               }
-              finish_run(epi, row, col, v, min(32, N - col), row < M, best);
+              float bl = 0.f;
+#pragma unroll
+              for (int r = 0; r < BN / 32; ++r)
+                if (r == c / 32) bl = bias_r[r];
+              finish_run(epi, row, col, v, min(32, N - col), row < M, best, bl);
             }
           }
         }
@@ -403,127 +437,182 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------------------
 // Small-M products (one 128-row output tile in M): split-K over a thread-block
 // cluster.  With few rows the cost of a Linear is moving its operands into
-// the SMs, and every CTA of a narrow-tile split re-reads the whole activation
-// block.  Here each output tile of BN columns is one cluster of S CTAs; CTA
-// r of the cluster multiplies the r-th K-range (all its k-blocks loaded at
-// once, one shared-memory stage each, so there is no ring to recycle), puts
-// its fp32 partial tile in shared memory, and after a cluster barrier sums
-// BN/S columns of all S partials through distributed shared memory and runs
-// the epilogue on them.  The CTAs of a cluster are resident together, so the
-// barrier always completes; every other wait is bounded.  With at most 64
-// rows the A tile is loaded as a 64-row box (the MMA's rows 64..127 hold
-// stale shared memory and are never stored).
+// the SMs and issuing its MMAs (one tcgen05.mma of N <= 64 columns takes
+// about as long as one of 128), so the work is cut along K instead of into
+// narrow tiles.  Each output tile of BN columns is one cluster of S CTAs; CTA
+// r multiplies the r-th K-range (every k-block of it loaded at once onto one
+// barrier, so there is no ring to recycle).  Column group g (BN / S columns)
+// of the tile belongs to rank g: every rank stores its fp32 partial of group
+// g straight from TMEM into rank g's receive area through distributed shared
+// memory, and after a cluster barrier each rank sums the S partials of its
+// own group and runs the epilogue on them.  The CTAs of a cluster are
+// resident together, so the cluster barriers always complete; every other
+// wait is bounded.  With at most 64 rows the A tile is loaded as a 64-row box
+// (the MMA's rows 64..127 read the 8 KB after it and are never stored).
 template <int BN>
 struct CCfg {
-  static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int MAX_KB = (kStageBudget / STAGE) > 10 ? 10 : (kStageBudget / STAGE);
-  static constexpr int PSTRIDE = BN + 4;  // floats per partial row (16-byte chunks spread over the banks)
-  static constexpr int P_BYTES = BM * PSTRIDE * 4;
-  static constexpr int BODY = MAX_KB * STAGE > P_BYTES ? MAX_KB * STAGE : P_BYTES;
-  static constexpr int SMEM = BODY + 1024 + 256;  // the most a launch asks for
   static constexpr uint32_t TMEM_COLS = BN;
-  // bytes of the stage area for kbs k-blocks (also holds the partial tile)
-  __host__ __device__ static constexpr int body(int kbs) { return kbs * STAGE > P_BYTES ? kbs * STAGE : P_BYTES; }
+  // stage area for kbs k-blocks with A boxes of a_box rows (+ 8 KB read by the
+  // MMA past 64-row boxes)
+  __host__ __device__ static constexpr int stage_bytes(int kbs, int a_box) {
+    return kbs * (a_box * BK * 2 + B_BYTES) + (a_box < BM ? 8192 : 0);
+  }
+  // receive area: S partials of 128 rows x (BN / S + 4) floats (the padding
+  // spreads a warp's 16-byte stores over all banks)
+  __host__ __device__ static constexpr int recv_stride(int S) { return BN / S + 4; }
+  __host__ __device__ static constexpr int recv_bytes(int S) { return S * BM * recv_stride(S) * 4; }
+  __host__ __device__ static constexpr int smem(int kbs, int a_box, int S) {
+    return stage_bytes(kbs, a_box) + recv_bytes(S) + 1024 + 64;
+  }
 };
+constexpr int kClusterSmemMax = 227 * 1024;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
-  return v;
 }
 
-// grid = nN * S CTAs in clusters of S; a_box = rows of one A box (64 or 128);
-// kbs = k-blocks per CTA (<= MAX_KB); the last rank may have fewer.
+// k-blocks [kb0, kb0 + nk) of one operand (rows from y) into consecutive
+// sub-tiles `sub` bytes apart, in boxes of 4, 2 and 1 k-blocks (t4 / t2 /
+// t1), all completing on one barrier.  A box of ks k-blocks exists whenever
+// ks <= K / 64, which nk never exceeds.
+__device__ __forceinline__ void load_kblocks(uint8_t *dst, const CUtensorMap *t1, const CUtensorMap *t2,
+                                             const CUtensorMap *t4, int y, int kb0, int nk, uint32_t sub,
+                                             uint64_t *bar) {
+  int j = 0;
+  for (; j + 4 <= nk; j += 4) tma_load_3d(dst + j * sub, t4, 0, y, kb0 + j, bar);
+  if (j + 2 <= nk) {
+    tma_load_3d(dst + j * sub, t2, 0, y, kb0 + j, bar);
+    j += 2;
+  }
+  if (j < nk) tma_load_3d(dst + j * sub, t1, 0, y, kb0 + j, bar);
+}
+
+// grid = nN * S CTAs in clusters of S (S in {2, 4, 8}); a_box = rows of one A
+// box (64 or 128); rank r takes k-blocks [r * KB / S, (r + 1) * KB / S), at
+// most kbs.  Shared memory: A sub-tiles (a_box * 128 bytes apart), W
+// sub-tiles (BN * 128 bytes each), the receive area, then the barriers.
+// tmA1/2/4, tmW1/2/4: boxes of 1, 2 and 4 k-blocks.
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
-    gemm_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+    gemm_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmA2,
+                           const __grid_constant__ CUtensorMap tmA4, const __grid_constant__ CUtensorMap tmW1,
+                           const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmW4,
                            int M_arg, const int32_t *M_dev, int N, int K, int S, int kbs, int a_box, EpiParams epi,
                            int32_t *status) {
   using C = CCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *body = smem_raw + pad;
-  uint64_t *full = reinterpret_cast<uint64_t *>(body + C::body(kbs));
-  uint64_t *done = full + C::MAX_KB;
+  const uint32_t a_sub = (uint32_t)a_box * BK * 2;
+  uint8_t *sW = body + kbs * a_sub + (a_box < BM ? 8192 : 0);
+  float *recv = reinterpret_cast<float *>(body + C::stage_bytes(kbs, a_box));
+  uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(recv) + C::recv_bytes(S));
+  uint64_t *done = full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = M_dev != nullptr ? *M_dev : M_arg;  // M_dev: the descriptor header, written before the forward
   const int rank = (int)cluster_rank();
   const int n = blockIdx.x / S;  // output tile = cluster
   const int KB = K / BK;
-  const int kb0 = rank * kbs, kb1 = min(KB, kb0 + kbs), nkb = max(0, kb1 - kb0);
-  const uint32_t a_bytes = (uint32_t)a_box * BK * 2;
+  const int kb0 = rank * KB / S, kb1 = (rank + 1) * KB / S, nkb = kb1 - kb0;
+  const int cw = BN / S;  // columns of the group this rank owns
+  const int rs = C::recv_stride(S);
+  const bool shape_ok = nkb <= kbs && M <= BM && BN % (4 * S) == 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::MAX_KB; ++s) mbar_init(&full[s], 1);
+    mbar_init(full, 1);
     mbar_init(done, 1);
     *abort_flag = 0;
     mbar_fence_init();
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();  // only once this CTA holds its tensor memory (as in the persistent kernel)
+  // first cluster phase: this CTA runs (its receive area may be written once
+  // every CTA of the cluster has arrived here)
+  cluster_arrive_relaxed();
 
   if (warp == 0) {
-    if (lane == 0 && nkb <= C::MAX_KB && M <= BM) {  // TMA producer: every k-block of this rank at once
-      for (int j = 0; j < nkb; ++j) {  // weights do not depend on earlier kernels
-        uint8_t *st = body + j * C::STAGE;
-        mbar_expect_tx(&full[j], a_bytes + C::B_BYTES);
+    if (lane == 0 && shape_ok && nkb > 0) {  // TMA producer: every k-block of this rank at once
+      mbar_expect_tx(full, (uint32_t)nkb * (a_sub + C::B_BYTES));
+      // weights do not depend on earlier kernels
+      if (BN <= 128) {
+        load_kblocks(sW, &tmW1, &tmW2, &tmW4, n * BN, kb0, nkb, C::B_BYTES, full);
+      } else {
+        for (int j = 0; j < nkb; ++j)
 #pragma unroll
-        for (int h = 0; h < BN / Cfg<BN>::BOX; ++h)
-          tma_load_3d(st + C::A_BYTES + h * (Cfg<BN>::BOX * BK * 2), &tmW, 0, n * BN + h * Cfg<BN>::BOX, kb0 + j,
-                      &full[j]);
+          for (int h = 0; h < BN / Cfg<BN>::BOX; ++h)
+            tma_load_3d(sW + j * C::B_BYTES + h * (Cfg<BN>::BOX * BK * 2), &tmW1, 0, n * BN + h * Cfg<BN>::BOX,
+                        kb0 + j, full);
       }
       pdl_wait();  // A (activations) comes from earlier kernels
-      for (int j = 0; j < nkb; ++j) tma_load_3d(body + j * C::STAGE, &tmA, 0, 0, kb0 + j, &full[j]);
+      load_kblocks(body, &tmA1, &tmA2, &tmA4, 0, kb0, nkb, a_sub, full);
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
-      for (int j = 0; j < nkb && nkb <= C::MAX_KB && M <= BM; ++j) {
-        if (mbar_wait(&full[j], 0, abort_flag, status)) {
+      if (shape_ok && nkb > 0) {
+        if (mbar_wait(full, 0, abort_flag, status)) {
           tc_fence_after();
-          const uint32_t a0 = smem_u32(body + j * C::STAGE);
-          const uint32_t b0 = a0 + C::A_BYTES;
+          const uint32_t a0 = smem_u32(body), b0 = smem_u32(sW);
+          for (int j = 0; j < nkb; ++j)
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            tc_mma(tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), Cfg<BN>::IDESC, (j > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k)
+              tc_mma(tmem, sw128_desc(a0 + j * a_sub + k * 32), sw128_desc(b0 + j * C::B_BYTES + k * 32),
+                     Cfg<BN>::IDESC, (j > 0 || k > 0) ? 1u : 0u);
+        } else {
+          drain_after_abort();  // copies issued before the abort land first
         }
       }
-      tc_commit(done);  // also when there was nothing to multiply: the epilogue then writes zeros
+      tc_commit(done);  // also when there was nothing to multiply: the partial is then zero
     }
-  } else {  // epilogue warps 2..5: TMEM lane quarter = warp % 4; own partial into shared memory
+  }
+  __syncwarp();
+  const int q = warp & 3;  // TMEM lane quarter of an epilogue warp (rows q * 32 ...)
+  const int row = q * 32 + lane;
+  float bias_r[BN / 32 > 0 ? BN / 32 : 1];
+  if (warp >= 2) {
+    // the bias of the owned group (a weight, like W) is loaded during the MMAs
+#pragma unroll
+    for (int r = 0; r < (BN / 32 > 0 ? BN / 32 : 1); ++r) {
+      const int col = n * BN + rank * cw + 32 * r;
+      bias_r[r] = 32 * r < cw && col < N ? run_bias(epi, col, min(min(32, cw - 32 * r), N - col)) : 0.f;
+    }
     pdl_wait();
-    const int q = warp & 3;
-    const int row = q * 32 + lane;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, status)) && nkb > 0 &&
-                    nkb <= C::MAX_KB && M <= BM;
+  }
+  const bool ok = warp >= 2 && __all_sync(0xffffffffu, warp >= 2 ? mbar_wait(done, 0, abort_flag, status) : true) &&
+                  nkb > 0 && shape_ok;
+  cluster_wait_acquire();  // every CTA of the cluster runs
+  if (warp >= 2) {
     tc_fence_after();
-    float *P = reinterpret_cast<float *>(body) + (size_t)row * C::PSTRIDE;
+    // push: columns [g * cw, (g + 1) * cw) of this rank's partial go to rank
+    // g's receive area, slot `rank`; rows past M are not needed
+    const uint32_t recv_row = smem_u32(recv) + (uint32_t)(((rank * BM) + row) * rs * 4);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       float v[32];
@@ -533,43 +622,57 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
+      if (row < M) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4 *>(P + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        for (int i = 0; i < 32; i += 4) {
+          const int col = c + i, g = col / cw;
+          st_cluster_f4(map_to_rank(recv_row + (uint32_t)((col - g * cw) * 4), (uint32_t)g), v[i], v[i + 1], v[i + 2],
+                        v[i + 3]);
+        }
+      }
     }
     tc_fence_before();
   }
   __syncwarp();
-  cluster_sync_all();  // every partial of the cluster is in shared memory
-  if (warp >= 2) {
-    const int q = warp & 3;
-    const int row = q * 32 + lane;
-    const int cw = BN / S;  // columns this rank reduces
-    const int c0 = rank * cw;
-    float v[32];
+  cluster_arrive_release();  // second phase: every partial has been stored
+  cluster_wait_acquire();
+  if (warp >= 2) {  // every lane: finish_run shuffles the bias across the warp; rows past M store nothing
+    const bool alive = __all_sync(0xffffffffu, *abort_flag == 0);  // warp-uniform
+    unsigned long long best = 0ull;
+    const float *mine = recv + (size_t)row * rs;
+#pragma unroll 1
+    for (int r0 = 0; r0 < cw; r0 += 32) {
+      const int cnt = min(32, cw - r0);
+      float v[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0.f;
-    const uint32_t mine = smem_u32(body) + (uint32_t)((row * C::PSTRIDE + c0) * 4);
-    for (int j = 0; j < S; ++j) {
-      const uint32_t src = map_to_rank(mine, (uint32_t)j);
+      for (int i = 0; i < 32; ++i) v[i] = 0.f;
+#pragma unroll 1
+      for (int j = 0; j < S; ++j) {
+        const float4 *src = reinterpret_cast<const float4 *>(mine + (size_t)j * BM * rs + r0);
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        if (i < cw) {
-          const float4 t = ld_cluster_f4(src + i * 4);
-          v[i] += t.x;
-          v[i + 1] += t.y;
-          v[i + 2] += t.z;
-          v[i + 3] += t.w;
+        for (int i = 0; i < 8; ++i) {
+          if (4 * i < cnt) {
+            const float4 t = src[i];
+            v[4 * i] += t.x;
+            v[4 * i + 1] += t.y;
+            v[4 * i + 2] += t.z;
+            v[4 * i + 3] += t.w;
+          }
         }
       }
+      float bl = 0.f;
+#pragma unroll
+      for (int r = 0; r < (BN / 32 > 0 ? BN / 32 : 1); ++r)
+        if (r == r0 / 32) bl = bias_r[r];
+      const int col = n * BN + rank * cw + r0;
+      if (col < N && alive) finish_run(epi, row, col, v, min(cnt, N - col), row < M, best, bl);
     }
-    unsigned long long best = 0ull;
-    const int col = n * BN + c0;
-    if (col < N && !*abort_flag) finish_run(epi, row, col, v, min(cw, N - col), row < M, best);
     if (epi.argmax_keys != nullptr && best != 0ull) atomicMax(epi.argmax_keys + row, best);
   }
-  if (threadIdx.x == 0 && (nkb > C::MAX_KB || M > BM)) atomicOr(status, kStatusBadShape);
-  __syncwarp();
-  cluster_sync_all();  // no CTA leaves while another still reads its shared memory
+  if (threadIdx.x == 0 && !shape_ok) atomicOr(status, kStatusBadShape);
+  // no CTA reads another's shared memory after the second phase: leave freely
+  tc_fence_before();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -593,7 +696,7 @@ cudaError_t set_cluster_smem_limit(int dev) {
   static uint64_t attr_mask = 0;
   if (dev >= 64 || !(attr_mask & (1ull << dev))) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_cluster_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         CCfg<BN>::SMEM);
+                                         kClusterSmemMax);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_mask |= 1ull << dev;
   }
@@ -601,15 +704,17 @@ cudaError_t set_cluster_smem_limit(int dev) {
 }
 
 template <int BN>
-cudaError_t launch_cluster(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, const int32_t *M_dev, int N, int K,
+cudaError_t launch_cluster(const OperandMaps &A, const OperandMaps &W, int M, const int32_t *M_dev, int N, int K,
                            int S, int kbs, int a_box, const EpiParams &epi, int32_t *status, cudaStream_t st, int dev) {
   cudaError_t e = set_cluster_smem_limit<BN>(dev);
   if (e != cudaSuccess) return e;
+  const int smem = CCfg<BN>::smem(kbs, a_box, S);
+  if (smem > kClusterSmemMax || BN % (4 * S) != 0) return cudaErrorInvalidValue;
   const int nN = (N + BN - 1) / BN;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(nN * S);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = CCfg<BN>::body(kbs) + 1024 + 256;  // only what this launch uses
+  cfg.dynamicSmemBytes = smem;  // only what this launch uses
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -620,8 +725,9 @@ cudaError_t launch_cluster(const CUtensorMap *tmA, const CUtensorMap *tmW, int M
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_cluster_kernel<BN>, *tmA, *tmW, M, M_dev, N, K, S, kbs, a_box, epi,
-                            status);
+  const int wb = BN < 128 ? BN : 128;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_cluster_kernel<BN>, *A.get(a_box, 1), *A.get(a_box, 2), *A.get(a_box, 4),
+                            *W.get(wb, 1), *W.get(wb, 2), *W.get(wb, 4), M, M_dev, N, K, S, kbs, a_box, epi, status);
 }
 
 template <int BN, int KS>
@@ -634,8 +740,8 @@ cudaError_t launch_bn(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, con
   sc.init(M, N, K, BN, KS, sm, scr);
   const int grid = M_dev != nullptr ? sm : (sc.units < sm ? sc.units : sm);
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(gemm_tc_bf16_kernel<BN, KS>, grid, 192, Cfg<BN, KS>::SMEM, st, *tmA, *tmW, M, M_dev, N, K, sm,
-                    a_box, epi, scr, status);
+  return launch_pdl(gemm_tc_bf16_kernel<BN, KS>, grid, 192, Cfg<BN, KS>::smem(a_box), st, *tmA, *tmW, M, M_dev, N, K,
+                    sm, a_box, epi, scr, status);
 }
 
 }  // namespace
@@ -675,25 +781,31 @@ int gemm_ks(int bn, int K) {
   while (ks > 1 && K % (BK * ks) != 0) ks /= 2;
   return ks;
 }
-int max_kb_cluster(int bn) {
-  return bn == 256 ? CCfg<256>::MAX_KB : bn == 128 ? CCfg<128>::MAX_KB : bn == 64 ? CCfg<64>::MAX_KB : CCfg<32>::MAX_KB;
+int cluster_smem(int bn, int kbs, int a_box, int S) {
+  return bn == 256   ? CCfg<256>::smem(kbs, a_box, S)
+         : bn == 128 ? CCfg<128>::smem(kbs, a_box, S)
+         : bn == 64  ? CCfg<64>::smem(kbs, a_box, S)
+                     : CCfg<32>::smem(kbs, a_box, S);
 }
+
+// Issue time of one tcgen05.mma (M = 128, K = 16) by its N, in microseconds:
+// measured on GB300 at about 50 cycles for N <= 64, 65 for 128 and 127 for
+// 256 (where it is bound by the tensor core's throughput), at 1.9 GHz.
+double mma_us(int bn) { return (bn <= 64 ? 50.0 : bn == 128 ? 65.0 : 127.0) / 1900.0; }
+// Operand bytes one SM takes in: a few TMA boxes in flight land at about
+// 115 GB/s, the first about 0.45 us after it is issued.
+double load_us(double bytes) { return 0.45 + bytes / 115e3; }
 
 }  // namespace
 
 // How one Linear runs.  Rows of one 128-row tile (M <= 128): the cluster
-// split-K kernel when its estimated critical path beats the persistent
-// kernel's; else the persistent kernel with gemm_tile_n's width.  The
-// estimate counts 128-byte rows of operand brought into one SM: per wave of
-// CTAs, k-blocks per CTA times (A rows + W rows), plus a fixed cost for a
-// CTA's start-up and teardown (about one microsecond of loading, paid once
-// per wave by the cluster kernel and once by the persistent one) and, for
-// the cluster kernel, the partial tile a CTA gathers.
-constexpr double kCtaFixedRows = 400.0;
-// The cluster kernel's extra steps (partial tile to shared memory, two
-// cluster barriers, the gather through distributed shared memory) measured
-// as about three more microseconds per wave on GB300.
-constexpr double kClusterFixedRows = 1600.0;
+// split-K kernel when its estimated time beats the persistent kernel's; else
+// the persistent kernel with gemm_tile_n's width.  The estimates (per wave of
+// CTAs) add the operand loads and the MMA issue of one CTA - the persistent
+// kernel overlaps them through its ring - and, for the cluster kernel, the
+// exchange of the fp32 partial tile (pushed through distributed shared
+// memory, two cluster barriers) as a fixed cost measured on GB300.
+constexpr double kClusterExchangeUs = 0.6;
 GemmPlan gemm_plan(int M, int N, int K) {
   GemmPlan p{};
   p.bn = gemm_tile_n(M, N);
@@ -704,17 +816,19 @@ GemmPlan gemm_plan(int M, int N, int K) {
   p.a_box = a_box;
   const int sm = gemm_sm_count();
   const long long waves_p = ((N + p.bn - 1) / p.bn + sm - 1) / sm;
-  const double cost_p = (double)waves_p * KB * (a_box + p.bn) + kCtaFixedRows;
-  double best = cost_p;
+  const double t_load_p = load_us((double)KB * (a_box + p.bn) * 128.0);
+  const double t_mma_p = KB * 4 * mma_us(p.bn);
+  double best = (double)waves_p * (t_load_p > t_mma_p ? t_load_p : t_mma_p);
   for (int bn : {32, 64, 128, 256}) {
     const int nN = (N + bn - 1) / bn;
     for (int S : {2, 4, 8}) {
       const int kbs = (KB + S - 1) / S;
-      if (kbs > max_kb_cluster(bn) || nN * S > 16 * sm) continue;
+      if (bn % (4 * S) != 0 || cluster_smem(bn, kbs, a_box, S) > kClusterSmemMax || nN * S > 16 * sm) continue;
       const long long waves = ((long long)nN * S + sm - 1) / sm;
-      const double cost = (double)waves * (kbs * (a_box + bn) + kClusterFixedRows) + 4.0 * bn;
-      if (cost < best * 0.95) {
-        best = cost;
+      const double t = (double)waves * (load_us((double)kbs * (a_box + bn) * 128.0) + kbs * 4 * mma_us(bn)) +
+                       kClusterExchangeUs;
+      if (t < best * 0.95) {
+        best = t;
         p.cluster = true;
         p.bn = bn;
         p.S = S;
@@ -767,13 +881,12 @@ cudaError_t launch_gemm_tc_bf16(const OperandMaps &A, const OperandMaps &W, int 
   if (e != cudaSuccess) return e;
   const int sm = gemm_sm_count();
   const GemmPlan p = gemm_plan(M, N, K);
-  const CUtensorMap *a1 = A.get(p.a_box, 1);
   if (p.cluster) {
     switch (p.bn) {
-      case 256: return launch_cluster<256>(a1, W.get(128, 1), M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
-      case 128: return launch_cluster<128>(a1, W.get(128, 1), M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
-      case 64: return launch_cluster<64>(a1, W.get(64, 1), M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
-      default: return launch_cluster<32>(a1, W.get(32, 1), M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
+      case 256: return launch_cluster<256>(A, W, M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
+      case 128: return launch_cluster<128>(A, W, M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
+      case 64: return launch_cluster<64>(A, W, M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
+      default: return launch_cluster<32>(A, W, M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);
     }
   }
   const int ks = p.ks;
