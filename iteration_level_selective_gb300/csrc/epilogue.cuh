@@ -24,25 +24,32 @@ template <> __device__ __forceinline__ __nv_bfloat16 cvt_out<__nv_bfloat16>(floa
   return __float2bfloat16_rn(v);
 }
 
-// Store cnt <= CNT consecutive values; 16-byte stores when the run is full and aligned.
+// Store cnt <= CNT consecutive values: 16-byte stores for every whole 16-byte
+// group of the run when dst is 16-byte aligned, element stores for the rest.
 template <typename T, int CNT>
 __device__ __forceinline__ void store_run(T *dst, const float *v, int cnt) {
   constexpr int PER = 16 / sizeof(T);
   if constexpr ((CNT * sizeof(T)) % 16 == 0) {
-    if (cnt == CNT && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+    if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
-      for (int i = 0; i < CNT; i += PER) {
-        uint4 pk;
-        T *pt = reinterpret_cast<T *>(&pk);
+      for (int i = 0; i < CNT; i += PER) {  // predicated, fully unrolled: v stays in registers
+        if (i + PER <= cnt) {
+          uint4 pk;
+          T *pt = reinterpret_cast<T *>(&pk);
 #pragma unroll
-        for (int j = 0; j < PER; ++j) pt[j] = cvt_out<T>(v[i + j]);
-        *reinterpret_cast<uint4 *>(dst + i) = pk;
+          for (int j = 0; j < PER; ++j) pt[j] = cvt_out<T>(v[i + j]);
+          *reinterpret_cast<uint4 *>(dst + i) = pk;
+        } else {
+#pragma unroll
+          for (int j = 0; j < PER; ++j)
+            if (i + j < cnt) dst[i + j] = cvt_out<T>(v[i + j]);
+        }
       }
       return;
     }
   }
 #pragma unroll
-  for (int i = 0; i < CNT; ++i)  // predicated, fully unrolled: v stays in registers
+  for (int i = 0; i < CNT; ++i)
     if (i < cnt) dst[i] = cvt_out<T>(v[i]);
 }
 
@@ -75,12 +82,18 @@ __device__ __forceinline__ void epi_store(const EpiParams &e, int m, int n0, flo
     }
     case kEpiResid: {
       float *xp = static_cast<float *>(e.out) + (int64_t)m * e.ldo + n0;
-      if (cnt == CNT && (CNT % 4) == 0 && (reinterpret_cast<uintptr_t>(xp) & 15) == 0) {
+      if ((CNT % 4) == 0 && (reinterpret_cast<uintptr_t>(xp) & 15) == 0) {
 #pragma unroll
         for (int i = 0; i < CNT; i += 4) {
-          float4 o = *reinterpret_cast<float4 *>(xp + i);
-          o.x += v[i]; o.y += v[i + 1]; o.z += v[i + 2]; o.w += v[i + 3];
-          *reinterpret_cast<float4 *>(xp + i) = o;
+          if (i + 4 <= cnt) {
+            float4 o = *reinterpret_cast<float4 *>(xp + i);
+            o.x += v[i]; o.y += v[i + 1]; o.z += v[i + 2]; o.w += v[i + 3];
+            *reinterpret_cast<float4 *>(xp + i) = o;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (i + j < cnt) xp[i + j] += v[i + j];
+          }
         }
       } else {
 #pragma unroll

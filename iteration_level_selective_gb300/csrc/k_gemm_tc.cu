@@ -339,13 +339,9 @@ __global__ void __launch_bounds__(192, 1)
       int m, n, kb0, kb1, tile, split;
       sc.unit(u, m, n, kb0, kb1, tile, split);
       const int acc = i & 1;
-      // the bias (a weight, like W) is loaded while the tile is computed
-      float bias_r[BN / 32];
-#pragma unroll
-      for (int r = 0; r < BN / 32; ++r) {
-        const int col = n * BN + 32 * r;
-        bias_r[r] = col < N ? run_bias(epi, col, min(32, N - col)) : 0.f;
-      }
+      // the bias of the first run (a weight, like W) is loaded while the tile
+      // is computed; each run then loads the next run's
+      float bl_next = n * BN < N ? run_bias(epi, n * BN, min(32, N - n * BN)) : 0.f;
       if (i == 0) pdl_wait();  // the epilogue reads / writes buffers of earlier kernels (x, K/V slots)
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], (uint32_t)(i >> 1) & 1u, abort_flag, status));
       tc_fence_after();
@@ -363,10 +359,8 @@ __global__ void __launch_bounds__(192, 1)
             if (lane == 0) mbar_arrive(&tempty[acc]);
           }
           const int col = n * BN + c;
-          float bl = 0.f;
-#pragma unroll
-          for (int r = 0; r < BN / 32; ++r)
-            if (r == c / 32) bl = bias_r[r];
+          const float bl = bl_next;
+          if (c + 32 < BN && col + 32 < N) bl_next = run_bias(epi, col + 32, min(32, N - col - 32));
           if (ok && col < N) finish_run(epi, row, col, v, min(32, N - col), row < M, best, bl);
         }
       } else {
@@ -414,11 +408,7 @@ __global__ void __launch_bounds__(192, 1)
                   v[4 * j + 3] += t.w;
                 }
               }
-              float bl = 0.f;
-#pragma unroll
-              for (int r = 0; r < BN / 32; ++r)
-                if (r == c / 32) bl = bias_r[r];
-              finish_run(epi, row, col, v, min(32, N - col), row < M, best, bl);
+              finish_run(epi, row, col, v, min(32, N - col), row < M, best, run_bias(epi, col, min(32, N - col)));
             }
           }
         }
@@ -442,13 +432,15 @@ __global__ void __launch_bounds__(192, 1)
 // narrow tiles.  Each output tile of BN columns is one cluster of S CTAs; CTA
 // r multiplies the r-th K-range (every k-block of it loaded at once onto one
 // barrier, so there is no ring to recycle).  Column group g (BN / S columns)
-// of the tile belongs to rank g: every rank stores its fp32 partial of group
-// g straight from TMEM into rank g's receive area through distributed shared
-// memory, and after a cluster barrier each rank sums the S partials of its
-// own group and runs the epilogue on them.  The CTAs of a cluster are
-// resident together, so the cluster barriers always complete; every other
-// wait is bounded.  With at most 64 rows the A tile is loaded as a 64-row box
-// (the MMA's rows 64..127 read the 8 KB after it and are never stored).
+// of the tile belongs to rank g: every rank writes its fp32 partial tile to
+// its own shared memory grouped by owner, sends group g to rank g with one
+// bulk copy over distributed shared memory (completing on rank g's receive
+// barrier), and each rank then sums the S partials of its own group and runs
+// the epilogue on them.  The CTAs of a cluster are resident together, so its
+// two cluster barriers (all CTAs running; all copies landed before any CTA
+// leaves) always complete; every other wait is bounded.  With at most 64 rows
+// the A tile is loaded as a 64-row box (the MMA's rows 64..127 read the 8 KB
+// after it and are never stored).
 template <int BN>
 struct CCfg {
   static constexpr int B_BYTES = BN * BK * 2;
@@ -458,12 +450,15 @@ struct CCfg {
   __host__ __device__ static constexpr int stage_bytes(int kbs, int a_box) {
     return kbs * (a_box * BK * 2 + B_BYTES) + (a_box < BM ? 8192 : 0);
   }
-  // receive area: S partials of 128 rows x (BN / S + 4) floats (the padding
-  // spreads a warp's 16-byte stores over all banks)
-  __host__ __device__ static constexpr int recv_stride(int S) { return BN / S + 4; }
-  __host__ __device__ static constexpr int recv_bytes(int S) { return S * BM * recv_stride(S) * 4; }
-  __host__ __device__ static constexpr int smem(int kbs, int a_box, int S) {
-    return stage_bytes(kbs, a_box) + recv_bytes(S) + 1024 + 64;
+  // this rank's partial tile, [owner g][row][BN / S] floats, written once the
+  // MMAs are done (over the stage area); then the S received partials of the
+  // owned group, [source rank][row][BN / S]
+  static constexpr int TILE_BYTES = BM * BN * 4;
+  __host__ __device__ static constexpr int work_bytes(int kbs, int a_box) {
+    return stage_bytes(kbs, a_box) > TILE_BYTES ? stage_bytes(kbs, a_box) : TILE_BYTES;
+  }
+  __host__ __device__ static constexpr int smem(int kbs, int a_box) {
+    return work_bytes(kbs, a_box) + TILE_BYTES + 1024 + 64;
   }
 };
 constexpr int kClusterSmemMax = 227 * 1024;
@@ -487,10 +482,15 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// another CTA's (dst and bar are shared::cluster addresses from mapa),
+// completing on that CTA's barrier.
+__device__ __forceinline__ void bulk_copy_to_rank(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "r"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+__device__ __forceinline__ void fence_proxy_async_cta() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // k-blocks [kb0, kb0 + nk) of one operand (rows from y) into consecutive
 // sub-tiles `sub` bytes apart, in boxes of 4, 2 and 1 k-blocks (t4 / t2 /
@@ -510,9 +510,11 @@ __device__ __forceinline__ void load_kblocks(uint8_t *dst, const CUtensorMap *t1
 
 // grid = nN * S CTAs in clusters of S (S in {2, 4, 8}); a_box = rows of one A
 // box (64 or 128); rank r takes k-blocks [r * KB / S, (r + 1) * KB / S), at
-// most kbs.  Shared memory: A sub-tiles (a_box * 128 bytes apart), W
-// sub-tiles (BN * 128 bytes each), the receive area, then the barriers.
-// tmA1/2/4, tmW1/2/4: boxes of 1, 2 and 4 k-blocks.
+// most kbs.  Shared memory: the work area (A sub-tiles a_box * 128 bytes
+// apart, then W sub-tiles of BN * 128 bytes; later the partial tile), the
+// receive area, then the barriers.  In both tile areas the 16-byte chunks of
+// a row are XOR-swizzled by the row (spreading a warp's stores over the
+// banks).  tmA1/2/4, tmW1/2/4: boxes of 1, 2 and 4 k-blocks.
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmA2,
@@ -526,10 +528,12 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t *body = smem_raw + pad;
   const uint32_t a_sub = (uint32_t)a_box * BK * 2;
   uint8_t *sW = body + kbs * a_sub + (a_box < BM ? 8192 : 0);
-  float *recv = reinterpret_cast<float *>(body + C::stage_bytes(kbs, a_box));
-  uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(recv) + C::recv_bytes(S));
+  float *part = reinterpret_cast<float *>(body);  // over the stage area once the MMAs are done
+  float *recv = reinterpret_cast<float *>(body + C::work_bytes(kbs, a_box));
+  uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(recv) + C::TILE_BYTES);
   uint64_t *done = full + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  uint64_t *recv_bar = done + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(recv_bar + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -538,13 +542,14 @@ __global__ void __launch_bounds__(192, 1)
   const int n = blockIdx.x / S;  // output tile = cluster
   const int KB = K / BK;
   const int kb0 = rank * KB / S, kb1 = (rank + 1) * KB / S, nkb = kb1 - kb0;
-  const int cw = BN / S;  // columns of the group this rank owns
-  const int rs = C::recv_stride(S);
+  const int cw = BN / S;            // columns of the group this rank owns
+  const int swz = cw / 4 - 1;       // chunk swizzle mask (cw / 4 is a power of two)
   const bool shape_ok = nkb <= kbs && M <= BM && BN % (4 * S) == 0;
 
   if (threadIdx.x == 0) {
     mbar_init(full, 1);
     mbar_init(done, 1);
+    mbar_init(recv_bar, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -595,24 +600,23 @@ __global__ void __launch_bounds__(192, 1)
   __syncwarp();
   const int q = warp & 3;  // TMEM lane quarter of an epilogue warp (rows q * 32 ...)
   const int row = q * 32 + lane;
-  float bias_r[BN / 32 > 0 ? BN / 32 : 1];
+  float bl_next = 0.f;
   if (warp >= 2) {
-    // the bias of the owned group (a weight, like W) is loaded during the MMAs
-#pragma unroll
-    for (int r = 0; r < (BN / 32 > 0 ? BN / 32 : 1); ++r) {
-      const int col = n * BN + rank * cw + 32 * r;
-      bias_r[r] = 32 * r < cw && col < N ? run_bias(epi, col, min(min(32, cw - 32 * r), N - col)) : 0.f;
-    }
+    // the bias of the owned group's first run (a weight, like W) is loaded
+    // during the MMAs; each run then loads the next run's
+    const int col = n * BN + rank * cw;
+    bl_next = col < N ? run_bias(epi, col, min(min(32, cw), N - col)) : 0.f;
     pdl_wait();
   }
   const bool ok = warp >= 2 && __all_sync(0xffffffffu, warp >= 2 ? mbar_wait(done, 0, abort_flag, status) : true) &&
                   nkb > 0 && shape_ok;
-  cluster_wait_acquire();  // every CTA of the cluster runs
+  cluster_wait_acquire();  // every CTA of the cluster runs (its barriers are initialised)
+  const int rows = M < BM ? (M > 0 ? M : 0) : BM;  // rows sent and summed
   if (warp >= 2) {
     tc_fence_after();
-    // push: columns [g * cw, (g + 1) * cw) of this rank's partial go to rank
-    // g's receive area, slot `rank`; rows past M are not needed
-    const uint32_t recv_row = smem_u32(recv) + (uint32_t)(((rank * BM) + row) * rs * 4);
+    // partial tile (zeros without MMAs) into the work area, grouped by owner;
+    // the whole warp loads (tcgen05.ld is warp-collective), rows past M are
+    // not stored
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       float v[32];
@@ -622,55 +626,69 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
-      if (row < M) {
+      if (row < rows) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const int col = c + i, g = col / cw;
-          st_cluster_f4(map_to_rank(recv_row + (uint32_t)((col - g * cw) * 4), (uint32_t)g), v[i], v[i + 1], v[i + 2],
-                        v[i + 3]);
+          const int col = c + i, g = col / cw, ch = (col - g * cw) >> 2;
+          *reinterpret_cast<float4 *>(part + (size_t)(g * BM + row) * cw + ((ch ^ (row & swz)) << 2)) =
+              make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
         }
       }
     }
     tc_fence_before();
-  }
-  __syncwarp();
-  cluster_arrive_release();  // second phase: every partial has been stored
-  cluster_wait_acquire();
-  if (warp >= 2) {  // every lane: finish_run shuffles the bias across the warp; rows past M store nothing
-    const bool alive = __all_sync(0xffffffffu, *abort_flag == 0);  // warp-uniform
+    fence_proxy_async_cta();  // the bulk copies read what these threads wrote
+    epi_barrier();
+    if (warp == 2) {  // lane g sends group g (the S copies are issued side by side)
+      const uint32_t grp = (uint32_t)(rows * cw * 4);  // bytes of one group
+      if (lane == 0) mbar_expect_tx(recv_bar, (uint32_t)S * grp);
+      if (grp > 0 && lane < S) {
+        const uint32_t slot = smem_u32(recv) + (uint32_t)(rank * BM * cw * 4);
+        bulk_copy_to_rank(map_to_rank(slot, (uint32_t)lane), smem_u32(part + (size_t)lane * BM * cw), grp,
+                          map_to_rank(smem_u32(recv_bar), (uint32_t)lane));
+      }
+    }
+    // every lane: finish_run shuffles the bias across the warp; rows past M store nothing
+    const bool got = __all_sync(0xffffffffu, mbar_wait(recv_bar, 0, abort_flag, status));
+    const bool alive = got && __all_sync(0xffffffffu, *abort_flag == 0);
     unsigned long long best = 0ull;
-    const float *mine = recv + (size_t)row * rs;
+    const float *mine = recv + (size_t)row * cw;
 #pragma unroll 1
     for (int r0 = 0; r0 < cw; r0 += 32) {
       const int cnt = min(32, cw - r0);
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      if (alive && row < rows) {
 #pragma unroll 1
-      for (int j = 0; j < S; ++j) {
-        const float4 *src = reinterpret_cast<const float4 *>(mine + (size_t)j * BM * rs + r0);
+        for (int j = 0; j < S; ++j) {
+          const float *src = mine + (size_t)j * BM * cw;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (4 * i < cnt) {
-            const float4 t = src[i];
-            v[4 * i] += t.x;
-            v[4 * i + 1] += t.y;
-            v[4 * i + 2] += t.z;
-            v[4 * i + 3] += t.w;
+          for (int i = 0; i < 8; ++i) {
+            if (4 * i < cnt) {
+              const int ch = (r0 >> 2) + i;
+              const float4 t = *reinterpret_cast<const float4 *>(src + ((ch ^ (row & swz)) << 2));
+              v[4 * i] += t.x;
+              v[4 * i + 1] += t.y;
+              v[4 * i + 2] += t.z;
+              v[4 * i + 3] += t.w;
+            }
           }
         }
       }
-      float bl = 0.f;
-#pragma unroll
-      for (int r = 0; r < (BN / 32 > 0 ? BN / 32 : 1); ++r)
-        if (r == r0 / 32) bl = bias_r[r];
       const int col = n * BN + rank * cw + r0;
+      const float bl = bl_next;
+      if (r0 + 32 < cw && col + 32 < N) bl_next = run_bias(epi, col + 32, min(min(32, cw - r0 - 32), N - col - 32));
       if (col < N && alive) finish_run(epi, row, col, v, min(cnt, N - col), row < M, best, bl);
     }
     if (epi.argmax_keys != nullptr && best != 0ull) atomicMax(epi.argmax_keys + row, best);
+    if (!got) drain_after_abort();  // copies still on their way land before the CTA leaves
   }
   if (threadIdx.x == 0 && !shape_ok) atomicOr(status, kStatusBadShape);
-  // no CTA reads another's shared memory after the second phase: leave freely
+  // second phase: every CTA has received its copies, so no copy still reads
+  // the shared memory of a CTA that leaves
+  __syncwarp();
+  cluster_arrive_release();
+  cluster_wait_acquire();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -708,7 +726,7 @@ cudaError_t launch_cluster(const OperandMaps &A, const OperandMaps &W, int M, co
                            int S, int kbs, int a_box, const EpiParams &epi, int32_t *status, cudaStream_t st, int dev) {
   cudaError_t e = set_cluster_smem_limit<BN>(dev);
   if (e != cudaSuccess) return e;
-  const int smem = CCfg<BN>::smem(kbs, a_box, S);
+  const int smem = CCfg<BN>::smem(kbs, a_box);
   if (smem > kClusterSmemMax || BN % (4 * S) != 0) return cudaErrorInvalidValue;
   const int nN = (N + BN - 1) / BN;
   cudaLaunchConfig_t cfg{};
@@ -781,11 +799,11 @@ int gemm_ks(int bn, int K) {
   while (ks > 1 && K % (BK * ks) != 0) ks /= 2;
   return ks;
 }
-int cluster_smem(int bn, int kbs, int a_box, int S) {
-  return bn == 256   ? CCfg<256>::smem(kbs, a_box, S)
-         : bn == 128 ? CCfg<128>::smem(kbs, a_box, S)
-         : bn == 64  ? CCfg<64>::smem(kbs, a_box, S)
-                     : CCfg<32>::smem(kbs, a_box, S);
+int cluster_smem(int bn, int kbs, int a_box) {
+  return bn == 256   ? CCfg<256>::smem(kbs, a_box)
+         : bn == 128 ? CCfg<128>::smem(kbs, a_box)
+         : bn == 64  ? CCfg<64>::smem(kbs, a_box)
+                     : CCfg<32>::smem(kbs, a_box);
 }
 
 // Issue time of one tcgen05.mma (M = 128, K = 16) by its N, in microseconds:
@@ -798,36 +816,34 @@ double load_us(double bytes) { return 0.45 + bytes / 115e3; }
 
 }  // namespace
 
-// How one Linear runs.  Rows of one 128-row tile (M <= 128): the cluster
-// split-K kernel when its estimated time beats the persistent kernel's; else
-// the persistent kernel with gemm_tile_n's width.  The estimates (per wave of
-// CTAs) add the operand loads and the MMA issue of one CTA - the persistent
-// kernel overlaps them through its ring - and, for the cluster kernel, the
-// exchange of the fp32 partial tile (pushed through distributed shared
-// memory, two cluster barriers) as a fixed cost measured on GB300.
-constexpr double kClusterExchangeUs = 0.6;
+// How one Linear runs.  Rows of one 128-row tile (M <= 128) and a long K
+// (at least 32 k-blocks): the cluster split-K kernel, whose exchange of
+// partial tiles costs a few microseconds but which splits the many MMAs of a
+// long K over S SMs; its tile width and S are the ones with the least
+// estimated load and MMA-issue time per wave.  Otherwise the persistent
+// kernel with gemm_tile_n's width.  (Measured on GB300 for M <= 128: with
+// K = 768 the persistent kernel was faster for every N of GPT-2 small, with
+// K = 3072 the cluster kernel by 30-40%.)
+constexpr int kClusterMinKb = 32;
 GemmPlan gemm_plan(int M, int N, int K) {
   GemmPlan p{};
   p.bn = gemm_tile_n(M, N);
   p.ks = gemm_ks(p.bn, K);
   const int KB = K / BK;
-  if (M > BM || M <= 0 || KB <= 0) return p;
-  const int a_box = M <= 64 ? 64 : 128;
+  if (M > BM || M <= 0) return p;
+  const int a_box = M <= 64 ? 64 : 128;  // products of <= 64 rows load 64-row A boxes
   p.a_box = a_box;
+  if (KB < kClusterMinKb) return p;
   const int sm = gemm_sm_count();
-  const long long waves_p = ((N + p.bn - 1) / p.bn + sm - 1) / sm;
-  const double t_load_p = load_us((double)KB * (a_box + p.bn) * 128.0);
-  const double t_mma_p = KB * 4 * mma_us(p.bn);
-  double best = (double)waves_p * (t_load_p > t_mma_p ? t_load_p : t_mma_p);
-  for (int bn : {32, 64, 128, 256}) {
+  double best = 1e30;
+  for (int bn : {64, 128}) {
     const int nN = (N + bn - 1) / bn;
-    for (int S : {2, 4, 8}) {
+    for (int S : {4, 8}) {
       const int kbs = (KB + S - 1) / S;
-      if (bn % (4 * S) != 0 || cluster_smem(bn, kbs, a_box, S) > kClusterSmemMax || nN * S > 16 * sm) continue;
+      if (bn % (4 * S) != 0 || cluster_smem(bn, kbs, a_box) > kClusterSmemMax || nN * S > 16 * sm) continue;
       const long long waves = ((long long)nN * S + sm - 1) / sm;
-      const double t = (double)waves * (load_us((double)kbs * (a_box + bn) * 128.0) + kbs * 4 * mma_us(bn)) +
-                       kClusterExchangeUs;
-      if (t < best * 0.95) {
+      const double t = (double)waves * (load_us((double)kbs * (a_box + bn) * 128.0) + kbs * 4 * mma_us(bn));
+      if (t < best) {
         best = t;
         p.cluster = true;
         p.bn = bn;
@@ -837,6 +853,10 @@ GemmPlan gemm_plan(int M, int N, int K) {
         p.ks = 1;
       }
     }
+  }
+  if (!p.cluster) {
+    p.bn = gemm_tile_n(M, N);
+    p.ks = gemm_ks(p.bn, K);
   }
   return p;
 }
