@@ -84,15 +84,21 @@ struct TileSmem {
   float k[kKeyTile][D + 1];
   float v[kKeyTile][D];
 };
-// Key-split streaming: K and V chunks of kChunkKeys keys flow through a
-// kRing-stage shared-memory ring, filled by 1-D bulk copies (the keys of a
-// request and head are contiguous in the slot pool) issued by thread 0.
-constexpr int kChunkKeys = 32;
+// Key-split streaming: K and V chunks of chunk_keys<D>() keys flow through a
+// kRing-stage shared-memory ring, filled by 1-D bulk copies issued by thread
+// 0 (one per K/V block of the chunk: the keys of a request and head are
+// contiguous in the slot pool, or one run per block of a paged table).  One
+// block per chunk: larger chunks for 64-dim heads (fewer waits per key)
+// halved the CTAs resident per SM and measured slower on GPT-2-small decode.
+template <int D>
+__host__ __device__ constexpr int chunk_keys() {
+  return kKvBlock;
+}
 constexpr int kRing = 4;
 
 template <typename T, int D>
 struct SplitSmem {
-  static constexpr int CHUNK = kChunkKeys * D * (int)sizeof(T);  // bytes of one K (or V) chunk
+  static constexpr int CHUNK = chunk_keys<D>() * D * (int)sizeof(T);  // bytes of one K (or V) chunk
   alignas(128) unsigned char k[kRing][CHUNK];
   alignas(128) unsigned char v[kRing][CHUNK];
   float m[kThreads / 32];
@@ -129,7 +135,9 @@ __device__ __forceinline__ bool keys_in_range(const AttnArgs &a, const ReqInfo &
   return (int64_t)rq.n_blocks * kKvBlock >= n_keys;
 }
 
-static_assert(kKeyTile == kKvBlock && kChunkKeys == kKvBlock, "key tiles and decode chunks are one K/V block");
+static_assert(kKeyTile == kKvBlock, "key tiles are one K/V block");
+static_assert(chunk_keys<64>() % kKvBlock == 0 && chunk_keys<128>() % kKvBlock == 0,
+              "decode chunks are whole K/V blocks");
 
 // kind 0: rows r0 .. r0+cnt-1 of one request, keys 0 .. last row's position.
 template <typename T, int D>
@@ -253,9 +261,12 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float *acc, floa
 
 // kind 1: one row over keys [split_idx * split, min(+split, pos + 1)).
 // `g` counts the ring chunks this CTA has consumed (identical in every thread).
+// `waited`: whether this CTA has waited for the kernels it depends on (the
+// QKV Linear); until then only keys below the row's own position - written
+// by earlier iterations - are read.
 template <typename T, int D>
 __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, int w_idx, int head,
-                                          SplitSmem<T, D> &sm, Ring &rg, uint32_t &g) {
+                                          SplitSmem<T, D> &sm, Ring &rg, uint32_t &g, bool &waited) {
   constexpr int VN = Vec16<T>::N;
   constexpr int LPK = D / VN;          // lanes per key (16 bytes each)
   constexpr int KPW = 32 / LPK;        // keys per warp step
@@ -282,20 +293,41 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   const int32_t *table = paged ? a.blocks + rq.block_off : nullptr;
   const T *Kbase = static_cast<const T *>(a.k_layer) + ((int64_t)head * a.n_slots + (paged ? 0 : rq.slot_base)) * D;
   const T *Vbase = static_cast<const T *>(a.v_layer) + ((int64_t)head * a.n_slots + (paged ? 0 : rq.slot_base)) * D;
-  const int n_chunks = (ke - kb + kChunkKeys - 1) / kChunkKeys;
+  constexpr int CK = chunk_keys<D>();
+  const int n_chunks = (ke - kb + CK - 1) / CK;
   auto issue = [&](int c) {  // thread 0: fill the ring stage of chunk c
     const uint32_t idx = g + (uint32_t)c;
     const int st = (int)(idx % kRing);
     if (!mbar_wait(&rg.empty[st], ((idx / kRing) & 1u) ^ 1u, &rg.abort, a.status) || rg.abort) return;
-    const int k0 = kb + c * kChunkKeys;
-    const int64_t off = paged ? (int64_t)table[k0 / kKvBlock] * kKvBlock : k0;
-    const uint32_t bytes = (uint32_t)(min(kChunkKeys, ke - k0) * D * (int)sizeof(T));
-    mbar_expect_tx(&rg.full[st], 2 * bytes);
-    bulk_load(sm.k[st], Kbase + off * D, bytes, &rg.full[st]);
-    bulk_load(sm.v[st], Vbase + off * D, bytes, &rg.full[st]);
+    const int k0 = kb + c * CK;
+    const int nk = min(CK, ke - k0);
+    mbar_expect_tx(&rg.full[st], 2u * (uint32_t)(nk * D * (int)sizeof(T)));
+    if (!paged) {
+      const uint32_t bytes = (uint32_t)(nk * D * (int)sizeof(T));
+      bulk_load(sm.k[st], Kbase + (int64_t)k0 * D, bytes, &rg.full[st]);
+      bulk_load(sm.v[st], Vbase + (int64_t)k0 * D, bytes, &rg.full[st]);
+    } else {
+      for (int b0 = 0; b0 < nk; b0 += kKvBlock) {  // one run per block of the table
+        const int64_t off = (int64_t)table[(k0 + b0) / kKvBlock] * kKvBlock;
+        const uint32_t bytes = (uint32_t)(min(kKvBlock, nk - b0) * D * (int)sizeof(T));
+        bulk_load(sm.k[st] + b0 * D * (int)sizeof(T), Kbase + off * D, bytes, &rg.full[st]);
+        bulk_load(sm.v[st] + b0 * D * (int)sizeof(T), Vbase + off * D, bytes, &rg.full[st]);
+      }
+    }
   };
+  const int n_first = min(kRing - 1, n_chunks);
+  // chunks wholly below the row's position hold keys of earlier iterations:
+  // they are requested before waiting for the QKV Linear (which writes the
+  // row's own key and q)
+  const int n_old = waited ? n_first : min(n_first, max(0, (pos - kb) / CK));
   if (threadIdx.x == 0)
-    for (int c = 0; c < min(kRing - 1, n_chunks); ++c) issue(c);
+    for (int c = 0; c < n_old; ++c) issue(c);
+  if (!waited) {
+    pdl_wait();
+    waited = true;
+  }
+  if (threadIdx.x == 0)
+    for (int c = n_old; c < n_first; ++c) issue(c);
 
   float q[VN];
   Vec16<T>::load(static_cast<const T *>(a.q) + (int64_t)r * a.hidden + head * D + sub * VN, q);
@@ -310,13 +342,13 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
     const uint32_t idx = g + (uint32_t)c;
     const int st = (int)(idx % kRing);
     const bool ok = mbar_wait(&rg.full[st], (idx / kRing) & 1u, &rg.abort, a.status);
-    const int nk = min(kChunkKeys, ke - (kb + c * kChunkKeys));
+    const int nk = min(CK, ke - (kb + c * CK));
     const T *ks = reinterpret_cast<const T *>(sm.k[st]);
     const T *vs = reinterpret_cast<const T *>(sm.v[st]);
     // warp `wid` takes key groups wid, wid + NW, ... of the chunk (KPW keys
     // each); warp-uniform trip count so every lane joins the shuffles
 #pragma unroll
-    for (int j = wid * KPW; j < kChunkKeys; j += NW * KPW) {
+    for (int j = wid * KPW; j < CK; j += NW * KPW) {
       const int kk = j + grp;
       const bool valid = ok && kk < nk;
       float kv[VN], vv[VN];
@@ -420,8 +452,9 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   if (threadIdx.x == 0) a.counters[(int64_t)w.req * a.n_heads + head] = 0;
 }
 
-// Persistent: each CTA takes (work item, head) pairs from an atomic ticket
-// (the host orders the work list longest first) until none is left; the
+// Persistent: CTA i takes (work item, head) pair i of the list (the host
+// orders it longest first); when the pairs outnumber the CTAs, each CTA then
+// takes further pairs from an atomic ticket until none is left, and the
 // last CTA to finish resets the ticket for the next launch.
 template <typename T, int D>
 constexpr int attn_smem_bytes() {
@@ -457,24 +490,37 @@ __global__ void __launch_bounds__(kThreads, (attn_min_ctas<T, D>())) attention_k
     a.n_work = a.hdr->n_work;
     a.split = a.hdr->split;
   }
-  pdl_wait();  // q and the K/V slots come from the QKV Linear
+  // q and this step's K/V rows come from the QKV Linear: every item waits for
+  // it (griddepcontrol.wait) before reading them; the work list, request
+  // records and older K/V slots are read before
+  bool waited = false;
   const int total = a.n_work * a.n_heads;
-  while (true) {
-    __syncthreads();  // the previous item's shared-memory reads are done
-    if (threadIdx.x == 0) s_item = atomicAdd(a.ticket, 1);
-    __syncthreads();
-    const int item = s_item;
-    if (item >= total) break;
+  // CTA i takes item i first; only when there are more items than CTAs do
+  // the rest go out by ticket (so a small batch costs no atomics at all)
+  const bool ticketed = total > (int)gridDim.x;
+  int item = blockIdx.x;
+  __syncthreads();  // the ring barriers are initialised
+  while (item < total) {
     const int w_idx = item / a.n_heads;
     const int head = item - w_idx * a.n_heads;
     const AttnWork w = a.work[w_idx];
-    if (w.kind == 0)
+    if (w.kind == 0) {
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+      }
       query_tile<T, D>(a, w, head, *reinterpret_cast<TileSmem<D> *>(smem_raw));
-    else
-      key_split<T, D>(a, w, w_idx, head, *reinterpret_cast<SplitSmem<T, D> *>(smem_raw), rg, g);
+    } else {
+      key_split<T, D>(a, w, w_idx, head, *reinterpret_cast<SplitSmem<T, D> *>(smem_raw), rg, g, waited);
+    }
+    if (!ticketed) break;
+    __syncthreads();  // the item's shared-memory reads are done
+    if (threadIdx.x == 0) s_item = (int)gridDim.x + atomicAdd(a.ticket, 1);
+    __syncthreads();
+    item = s_item;
   }
   if (rg.abort) drain_after_abort();
-  if (threadIdx.x == 0) {
+  if (ticketed && threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(a.ticket + 1, 1) == (int)gridDim.x - 1) {  // every CTA has left the loop
       a.ticket[0] = 0;

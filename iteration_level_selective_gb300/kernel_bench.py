@@ -109,6 +109,8 @@ ATTN_CASES = {
     "c5_prefill": lambda rng: ([(int(L), 0) for L in rng.integers(1024, 2049, 16)], 40, 128),
     # one GPT-2-small prefill of 512 tokens plus 63 decodes with contexts U{32..768}
     "gpt2_mixed": lambda rng: ([(512, 0)] + [(1, int(c)) for c in rng.integers(32, 769, 63)], 12, 64),
+    # a decode-only GPT-2-small iteration: 30 decodes with contexts U{32..768}
+    "gpt2_decode": lambda rng: ([(1, int(c)) for c in rng.integers(32, 769, 30)], 12, 64),
 }
 
 
