@@ -85,22 +85,28 @@ struct TileSmem {
   float v[kKeyTile][D];
 };
 // Key-split streaming: K and V chunks of chunk_keys<D>() keys flow through a
-// kRing-stage shared-memory ring, filled by 1-D bulk copies issued by thread
-// 0 (one per K/V block of the chunk: the keys of a request and head are
-// contiguous in the slot pool, or one run per block of a paged table).  One
-// block per chunk: larger chunks for 64-dim heads (fewer waits per key)
-// halved the CTAs resident per SM and measured slower on GPT-2-small decode.
+// ring_stages<D>()-stage shared-memory ring, filled by 1-D bulk copies issued
+// by thread 0 (one per K/V block of the chunk: the keys of a request and head
+// are contiguous in the slot pool, or one run per block of a paged table).
+// One block per chunk and four stages: on GPT-2-small decode, larger chunks
+// or an 8-stage ring (fewer waits per key, more bytes in flight per CTA)
+// measured slower, as the bigger ring halves the CTAs resident per SM and
+// the batch's items then need two waves.
 template <int D>
 __host__ __device__ constexpr int chunk_keys() {
   return kKvBlock;
 }
-constexpr int kRing = 4;
+template <int D>
+__host__ __device__ constexpr int ring_stages() {
+  return 4;
+}
+constexpr int kRingMax = 4;
 
 template <typename T, int D>
 struct SplitSmem {
   static constexpr int CHUNK = chunk_keys<D>() * D * (int)sizeof(T);  // bytes of one K (or V) chunk
-  alignas(128) unsigned char k[kRing][CHUNK];
-  alignas(128) unsigned char v[kRing][CHUNK];
+  alignas(128) unsigned char k[ring_stages<D>()][CHUNK];
+  alignas(128) unsigned char v[ring_stages<D>()][CHUNK];
   float m[kThreads / 32];
   float l[kThreads / 32];
   float acc[kThreads / 32][D];
@@ -109,8 +115,8 @@ struct SplitSmem {
 
 // Ring barriers and flags (static shared memory, set up once per CTA).
 struct Ring {
-  uint64_t full[kRing];   // one arrival (with the copy bytes) per fill
-  uint64_t empty[kRing];  // one arrival per warp per chunk consumed
+  uint64_t full[kRingMax];   // one arrival (with the copy bytes) per fill
+  uint64_t empty[kRingMax];  // one arrival per warp per chunk consumed
   int abort;
 };
 
@@ -294,6 +300,7 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   const T *Kbase = static_cast<const T *>(a.k_layer) + ((int64_t)head * a.n_slots + (paged ? 0 : rq.slot_base)) * D;
   const T *Vbase = static_cast<const T *>(a.v_layer) + ((int64_t)head * a.n_slots + (paged ? 0 : rq.slot_base)) * D;
   constexpr int CK = chunk_keys<D>();
+  constexpr int kRing = ring_stages<D>();
   const int n_chunks = (ke - kb + CK - 1) / CK;
   auto issue = [&](int c) {  // thread 0: fill the ring stage of chunk c
     const uint32_t idx = g + (uint32_t)c;
@@ -476,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, (attn_min_ctas<T, D>())) attention_k
   __shared__ Ring rg;
   __shared__ int s_item;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < kRingMax; ++i) {
       mbar_init(&rg.full[i], 1);
       mbar_init(&rg.empty[i], kThreads / 32);
     }
