@@ -34,11 +34,14 @@ _TIME = {"ns": 1e-6, "nsecond": 1e-6, "us": 1e-3, "usecond": 1e-3, "ms": 1.0, "m
 _BYTES = {"byte": 1.0, "b": 1.0, "kbyte": 1e3, "kb": 1e3, "mbyte": 1e6, "mb": 1e6, "gbyte": 1e9, "gb": 1e9}
 
 CLASSES = {
-    "gemm_tc_bf16": ("gemm_tc_bf16_kernel",),
+    "gemm_tc_bf16": ("gemm_tc_bf16_kernel", "gemm_tc_cluster_kernel"),
     "attention": ("attention_kernel", "prefill_attention_tc_kernel"),
     "layernorm": ("layernorm_kernel",),
     "embed": ("embed_kernel",),
 }
+# classes whose kernels are alternatives (one launch each): bytes over all their launches;
+# the others count the launches of their first kernel (attention: one per layer)
+ALTERNATIVES = {"gemm_tc_bf16"}
 
 
 def source_hash() -> str:
@@ -111,7 +114,10 @@ def traffic_by_class(per, scale: float = 1.0):
         present = [n for n in names if n in per and per[n]["has_dram"]]
         if not present:
             continue
-        n_launch = per[present[0]]["launches"]   # the first name present counts the class's launches
+        if cls in ALTERNATIVES:
+            n_launch = sum(per[n]["launches"] for n in names if n in per)
+        else:
+            n_launch = per[present[0]]["launches"]   # the first name present counts the class's launches
         res[cls] = scale * sum(per[n]["dram"] for n in present) / n_launch
     return res
 
