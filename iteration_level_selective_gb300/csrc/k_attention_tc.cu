@@ -3,7 +3,8 @@
 // The per-request attention of Figure 5 (Orca walk-through) for the rows of
 // a prompt is a dense, causal contraction: S = Q K^T over the request's own
 // keys, softmax, O = P V.  One work item is up to 128 query rows of one
-// request and one head; persistent CTAs take items from an atomic ticket.
+// request and one head; persistent CTA i takes item i, and further items from
+// an atomic ticket when the items outnumber the CTAs.
 //
 // One pass over the key tiles (128 keys each) with an online softmax, the
 // roles of a CTA running as a pipeline:
@@ -262,15 +263,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   // otherwise leave it without columns.
   pdl_trigger();
   pdl_wait();  // q and the K/V slots come from the QKV Linear; the output rows are its input
+  const int n_work = a.n_work_dev ? *a.n_work_dev : a.n_work;  // descriptor header, written before the forward
+  const int total = n_work * a.n_heads;
+  // CTA i takes item i first; only when there are more items than CTAs do
+  // the rest go out by ticket (so a small batch costs no atomics at all)
+  const bool ticketed = total > (int)gridDim.x;
 
   if (warp == 0) {
     // ------------------------------------------------------------ loader
     if (lane == 0) {
-      const int n_work = a.n_work_dev ? *a.n_work_dev : a.n_work;
-      const int total = n_work * a.n_heads;
       uint32_t n_item = 0, g = 0;  // items enqueued, K/V tiles loaded
+      bool first = true;
       while (!*abort_flag) {
-        const int t = atomicAdd(a.ticket, 1);
+        const int t = first ? (int)blockIdx.x : ticketed ? (int)gridDim.x + atomicAdd(a.ticket, 1) : total;
+        first = false;
         TcItem it{};
         it.n_tiles = -1;
         if (t < total) {
@@ -544,13 +550,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
   }
 
-  // teardown: the last CTA out resets the ticket; free tensor memory
+  // teardown: the last CTA out resets the ticket (when it was used); free tensor memory
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(a.ticket + 1, 1) == (int)gridDim.x - 1) {
-      a.ticket[0] = 0;
-      a.ticket[1] = 0;
+    if (ticketed) {
+      __threadfence();
+      if (atomicAdd(a.ticket + 1, 1) == (int)gridDim.x - 1) {
+        a.ticket[0] = 0;
+        a.ticket[1] = 0;
+      }
     }
     if (*abort_flag) drain_after_abort();
   }
