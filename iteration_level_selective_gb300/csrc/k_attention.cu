@@ -432,27 +432,31 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
     part[D] = M;
     part[D + 1] = L;
   }
-  __threadfence();
-  __syncthreads();
+  __syncthreads();  // the CTA's partial is written ...
   if (threadIdx.x == 0) {
+    __threadfence();  // ... and visible GPU-wide before it is counted
     const int prev = atomicAdd(a.counters + (int64_t)w.req * a.n_heads + head, 1);
     sm.last = prev == n_splits - 1;
+    if (sm.last) __threadfence();  // the other splits' partials, counted before, are read below
   }
   __syncthreads();
   if (!sm.last) return;
-  __threadfence();
   const int64_t s0 = (int64_t)w.req * kMaxSplits;  // the row's split partials
   if (dim < D) {
-    float Mx = -INFINITY;
-    for (int j = 0; j < n_splits; ++j)
-      Mx = fmaxf(Mx, __ldcg(a.part + ((s0 + j) * a.n_heads + head) * (D + 2) + D));
-    float Lx = 0.f, Ax = 0.f;
+    // online merge of the other splits' (max, sum, value) with this CTA's own
+    // (its loads are independent of one another, so they overlap)
+    float Mx = M, Lx = L, Ax = A;
+#pragma unroll 4
     for (int j = 0; j < n_splits; ++j) {
+      if (j == w.b) continue;
       const float *pj = a.part + ((s0 + j) * a.n_heads + head) * (D + 2);
-      const float mj = __ldcg(pj + D);
-      const float c = mj == -INFINITY ? 0.f : exp2f(mj - Mx);
-      Lx += __ldcg(pj + D + 1) * c;
-      Ax += __ldcg(pj + dim) * c;
+      const float mj = __ldcg(pj + D), lj = __ldcg(pj + D + 1), aj = __ldcg(pj + dim);
+      const float mn = fmaxf(Mx, mj);
+      if (mn == -INFINITY) continue;
+      const float c1 = exp2f(Mx - mn), c2 = exp2f(mj - mn);
+      Lx = Lx * c1 + lj * c2;
+      Ax = Ax * c1 + aj * c2;
+      Mx = mn;
     }
     O[dim] = from_f<T>(Ax / Lx);
   }
