@@ -89,8 +89,12 @@ struct Sched {
     S = 1;
     kbs = KB;
     // The last unit of a tile reads all S partials through one SM, so split
-    // only long K (>= 16 k-blocks of 64) and at most 4 ways.
-    if (scr.partials != nullptr && tiles > 0 && tiles * 2 <= sm && KB * KSb >= 16 && tiles <= scr.n_counters) {
+    // only long K (>= 16 k-blocks of 64), at most 4 ways, and only tiles
+    // whose weight block is at least 1 MB (a weight stream that one SM would
+    // take microseconds to bring in; smaller ones - the MLP of GPT-2-small
+    // at a few hundred rows - measured slower split than whole).
+    if (scr.partials != nullptr && tiles > 0 && tiles * 2 <= sm && KB * KSb >= 16 && tiles <= scr.n_counters &&
+        (long long)BN * K * 2 >= (1ll << 20)) {
       int s = sm / tiles;
       if (s > KB * KSb / 8) s = KB * KSb / 8;
       if (s > KB) s = KB;

@@ -56,7 +56,10 @@ def test_argmax_forced_logits_bit_exact(cuda):
                                    (600, 2304, 768),
                                    # one row tile and a long K: split-K over a cluster (ragged N, 64- and
                                    # 128-row A boxes, uneven K ranges)
-                                   (37, 300, 2048), (100, 768, 3072), (1, 1000, 4096), (128, 520, 2112)])
+                                   (37, 300, 2048), (100, 768, 3072), (1, 1000, 4096), (128, 520, 2112),
+                                   # few narrow tiles with a 1 MB weight block each: split-K over the
+                                   # persistent kernel when a scratch buffer is given
+                                   (200, 520, 16384)])
 @pytest.mark.parametrize("mode", ["store", "gelu", "resid", "f32out"])
 @pytest.mark.parametrize("split", [False, True])
 def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode, split):
@@ -89,8 +92,9 @@ def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode, split):
     assert int(status.item()) == 0
     got = out.double().cpu()
     scale = ref.abs().max().item()
-    # fp32 accumulation of exact bf16 products; bf16 output rounding (2^-8) for store/gelu
-    tol = 2 ** -7 if mode in ("store", "gelu") else 1e-5
+    # fp32 accumulation of exact bf16 products (its rounding error grows with the K / 16 chained
+    # MMAs: 1e-5 up to K = 4096, in proportion beyond); bf16 output rounding (2^-8) for store/gelu
+    tol = 2 ** -7 if mode in ("store", "gelu") else 1e-5 * max(1.0, K / 4096)
     err = (got - ref).abs().max().item() / scale
     assert err < tol, err
 
