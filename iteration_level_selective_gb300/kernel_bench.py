@@ -2,10 +2,15 @@
 
     python -m iteration_level_selective_gb300.kernel_bench linear --M 2048 --N 20480 --K 5120
     python -m iteration_level_selective_gb300.kernel_bench sweep
+    python -m iteration_level_selective_gb300.kernel_bench linear-graph
 
 `linear` times orca_linear (the token-wise Linear of one iteration, bf16
 tcgen05) with CUDA events, after warm-up, and prints achieved TFLOP/s and
-algorithmic GB/s.  Inputs are random on the device.
+algorithmic GB/s.  `linear-graph` times the small-M Linears of GPT-2-small as
+they run in an iteration - 20 back-to-back launches captured in a CUDA graph,
+so that launch latency and programmatic dependent launch count as they do in
+the engine - next to cuBLAS (torch.nn.functional.linear) captured the same
+way.  Inputs are random on the device.
 """
 from __future__ import annotations
 
@@ -49,6 +54,58 @@ def time_linear(M: int, N: int, K: int, reps: int = 20, warmup: int = 3, mode: i
     flops = 2.0 * M * N * K
     byts = (M * K + N * K) * 2 + M * N * out.element_size()
     return {"M": M, "N": N, "K": K, "ms": ms, "tflops": flops / ms / 1e9, "gbs": byts / ms / 1e6}
+
+
+def graph_us(fn, n: int = 20, trials: int = 3) -> float:
+    """Microseconds per call of fn(stream) over n calls captured in one CUDA
+    graph (best of `trials` replays)."""
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(n):
+                fn(s)
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(trials):  # replay() launches on the current stream: the events go there too
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1000.0 / n)
+    return best
+
+
+def time_linear_graph(M: int, N: int, K: int):
+    """orca_linear (bf16 store epilogue with a bias) vs cuBLAS, both graph-captured."""
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    A = torch.randn((M, K), device=dev, generator=g).to(torch.bfloat16)
+    W = (torch.randn((N, K), device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    bias = torch.randn(N, device=dev, generator=g)
+    out = torch.empty((M, N), device=dev, dtype=torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def ours(s):
+        C.orca_linear(C.ORCA_DTYPE_BF16, C.ORCA_LINEAR_STORE, A.data_ptr(), W.data_ptr(), bias.data_ptr(),
+                      out.data_ptr(), M, N, K, status.data_ptr(), s.cuda_stream)
+
+    bias16 = bias.to(torch.bfloat16)
+
+    def cublas(s):
+        torch.nn.functional.linear(A, W, bias16, out=out)
+
+    t_ours = graph_us(ours)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    return {"M": M, "N": N, "K": K, "ours_us": round(t_ours, 2), "cublas_us": round(graph_us(cublas), 2)}
 
 
 def time_attention(batch, n_heads: int, head_dim: int, reps: int = 5, warmup: int = 2, seed: int = 0):
@@ -124,6 +181,7 @@ def main():
     p.add_argument("--reps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
     sub.add_parser("sweep")
+    sub.add_parser("linear-graph")
     pa = sub.add_parser("attention")
     pa.add_argument("--case", choices=sorted(ATTN_CASES), required=True)
     pa.add_argument("--reps", type=int, default=5)
@@ -137,6 +195,11 @@ def main():
         print(json.dumps(r))
     elif a.cmd == "linear":
         print(json.dumps(time_linear(a.M, a.N, a.K, a.reps, a.warmup)))
+    elif a.cmd == "linear-graph":
+        # GPT-2-small's Linears (QKV, Attn-Out, FC1, FC2, LM head) at decode and prefill row counts
+        for M in (8, 64, 128, 256):
+            for (N, K) in ((2304, 768), (768, 768), (3072, 768), (768, 3072), (50304, 768)):
+                print(json.dumps(time_linear_graph(M, N, K)))
     else:
         for (N, K) in ((2304, 768), (768, 768), (3072, 768), (768, 3072), (15360, 5120), (5120, 5120),
                        (20480, 5120), (5120, 20480)):
