@@ -24,7 +24,6 @@ generation in float64) on the same trace and metric.
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import os
 import statistics
@@ -112,13 +111,8 @@ class ClockSampler:
 
 
 def kernel_source_hash() -> str:
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "iteration_level_selective_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
-    return h.hexdigest()[:16]
+    from iteration_level_selective_gb300.ncu_summary import source_hash
+    return source_hash(os.path.join(ROOT, "iteration_level_selective_gb300", "csrc"))
 
 
 def measured_traffic(kernel: str, config: str = "gpt2-trace"):

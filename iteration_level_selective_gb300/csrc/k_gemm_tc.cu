@@ -7,13 +7,14 @@
 //   C[m, n] = sum_k A[m, k] * W[n, k]     A: [M, K] bf16, W: [N, K] bf16
 // with fp32 accumulation in tensor memory, then the fused epilogue.
 //
-// Persistent CTAs (one per SM) walk a list of work units; a unit is one
-// 128 x BN output tile, or one K-range of it when the output has too few
-// tiles to fill the GPU (split-K, used for decode-sized M).  Tiles are
-// visited in groups of 8 M-tiles so the CTAs running at the same time share
-// their W tiles and A rows in L2.  Six warps:
-//   warp 0      one lane issues TMA loads of 128x64 A and BNx64 W tiles
-//               (128-byte swizzle) into a shared-memory ring;
+// Two kernels.  The persistent one: CTAs (one per SM) walk a list of work
+// units; a unit is one 128 x BN output tile, or one K-range of it when the
+// output has too few tiles to fill the GPU and each tile's weight block is
+// large (split-K).  Tiles are visited in groups of 8 M-tiles so the CTAs
+// running at the same time share their W tiles and A rows in L2.  Six warps:
+//   warp 0      one lane issues TMA loads into a shared-memory ring, one A
+//               box and one W box per stage, each of KS k-blocks of 64
+//               columns (128-byte swizzle);
 //   warp 1      allocates 2*BN TMEM columns (two accumulators); one lane
 //               issues tcgen05.mma (kind::f16, M=128, N=BN, K=16), releases
 //               each ring stage with tcgen05.commit and hands a finished
@@ -25,6 +26,9 @@
 //               stores an fp32 partial; the last unit of a tile to arrive
 //               (atomic counter, no waiting) sums the partials and runs the
 //               epilogue.
+// The cluster split-K kernel (further down) serves one 128-row tile with a
+// long K: the K-ranges of an output tile go to the CTAs of one cluster, which
+// exchange their fp32 partials through distributed shared memory.
 // Every mbarrier wait is bounded (about 2 s of %globaltimer).  On expiry the
 // CTA sets kStatusWaitTimeout and an abort flag that ends every other wait at
 // once; the roles then skip their work but keep their barrier sequence, and

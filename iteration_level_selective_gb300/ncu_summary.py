@@ -44,13 +44,39 @@ CLASSES = {
 ALTERNATIVES = {"gemm_tc_bf16"}
 
 
-def source_hash() -> str:
-    """Hash of the CUDA/C++ sources (the benchmark computes the same)."""
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed
+    (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # literal: copy through its closing quote
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def source_hash(csrc: str = CSRC) -> str:
+    """Hash of the CUDA/C++ sources' code (comments and layout do not count:
+    a profile stays valid across comment edits); the benchmark uses the same."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
+    for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(CSRC, f), "rb") as fh:
-                h.update(fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                h.update(code_only(fh.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 
