@@ -34,3 +34,30 @@ def test_summary_and_traffic(tmp_path):
     ns.main([str(p), "--traffic", str(out), "--workload", "w"])
     d = json.loads(out.read_text())
     assert d["w"]["gemm_tc_bf16"]["source_hash"] == ns.source_hash()
+
+
+def test_gemm_class_sums_alternative_kernels(tmp_path):
+    """The GEMM class divides the bytes of the persistent and the cluster
+    split-K kernels by the launches of both (each Linear is one or the other)."""
+    extra = '''"3","1","python","h","void orca::(anonymous namespace)::gemm_tc_cluster_kernel<64>(CUtensorMap, int)","1","7","(192, 1, 1)","(96, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","Mbyte","1.00"
+"3","1","python","h","void orca::(anonymous namespace)::gemm_tc_cluster_kernel<64>(CUtensorMap, int)","1","7","(192, 1, 1)","(96, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_write.sum","byte","0"
+"3","1","python","h","void orca::(anonymous namespace)::gemm_tc_cluster_kernel<64>(CUtensorMap, int)","1","7","(192, 1, 1)","(96, 1, 1)","0","10.3","Command line profiler metrics","gpu__time_duration.sum","usecond","5"
+'''
+    p = tmp_path / "l.csv"
+    p.write_text(CSV + extra)
+    per = ns.summarise(ns.read_launches(str(p)))
+    t = ns.traffic_by_class(per)
+    assert abs(t["gemm_tc_bf16"] - (3.0e6 + 1.0e6) / 2) < 1e-6
+
+
+def test_source_hash_ignores_comments_and_layout(tmp_path):
+    a = tmp_path / "a"
+    b = tmp_path / "b"
+    a.mkdir()
+    b.mkdir()
+    (a / "k.cu").write_text('// header\n__global__ void k() { asm("mov.u32 %0, 1; // in a string"); }\n')
+    (b / "k.cu").write_text('/* another header */\n__global__ void k()\n{\n  asm("mov.u32 %0, 1; // in a string");  // note\n}\n')
+    assert ns.source_hash(str(a)) == ns.source_hash(str(b))
+    (b / "k.cu").write_text('__global__ void k() { asm("mov.u32 %0, 2; // in a string"); }\n')
+    assert ns.source_hash(str(a)) != ns.source_hash(str(b))
+    assert ns.code_only('x = "/*"; /* c */ y = \'"\'; // d\nz') == 'x = "/*"; y = \'"\'; z'
