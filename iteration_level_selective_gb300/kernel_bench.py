@@ -159,6 +159,8 @@ def time_attention(batch, n_heads: int, head_dim: int, reps: int = 5, warmup: in
 ATTN_CASES = {
     # 256 decoding requests, cached contexts U{1024..4096}, 13B-shaped heads (one layer)
     "c4": lambda rng: ([(1, int(c)) for c in rng.integers(1024, 4097, 256)], 40, 128),
+    # a quarter of c4 (64 requests, 3.4 GB of K/V): small enough for profiler captures
+    "c4_quarter": lambda rng: ([(1, int(c)) for c in rng.integers(1024, 4097, 64)], 40, 128),
     # 16 prompts U{1024..2048} + 240 decodes with contexts U{128..2048}, 13B-shaped heads
     "c5": lambda rng: ([(int(L), 0) for L in rng.integers(1024, 2049, 16)] +
                        [(1, int(c)) for c in rng.integers(128, 2049, 240)], 40, 128),
