@@ -869,6 +869,8 @@ GemmPlan gemm_plan(int M, int N, int K) {
   return p;
 }
 
+// A small integer naming the plan, below 64: callers pack one per Linear
+// into 6 bits of their CUDA-graph keys (persistent 0..7, cluster 8..39).
 int gemm_plan_code(int M, int N, int K) {
   const GemmPlan p = gemm_plan(M, N, K);
   if (!p.cluster) return bn_code(p.bn) * 2 + (p.a_box == 64 ? 1 : 0);

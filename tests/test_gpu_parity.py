@@ -54,6 +54,9 @@ def test_argmax_forced_logits_bit_exact(cuda):
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (300, 1000, 768), (257, 2304, 768), (2048, 3072, 768),
                                    (64, 50257, 768), (64, 768, 3072), (130, 2304, 768), (3000, 5120, 1024),
                                    (600, 2304, 768),
+                                   # one row tile with all of K in flight at once (64- and 128-row A
+                                   # boxes, a ragged last column tile, a single k stage)
+                                   (64, 768, 768), (100, 768, 512), (17, 1000, 1024), (5, 3072, 256),
                                    # one row tile and a long K: split-K over a cluster (ragged N, 64- and
                                    # 128-row A boxes, uneven K ranges)
                                    (37, 300, 2048), (100, 768, 3072), (1, 1000, 4096), (128, 520, 2112),
