@@ -155,7 +155,9 @@ typedef struct {
 int orca_kv_pool_bytes(const orca_config *cfg, size_t *bytes);
 
 /* Bytes of device workspace orca_engine_create needs (activations, the
- * device batch descriptor, attention scratch, logits). */
+ * device batch descriptor, attention scratch, logits; in bf16 also the
+ * row statistics and per-layer vectors of the LayerNorms folded into the
+ * Linears after them). */
 int orca_workspace_bytes(const orca_config *cfg, size_t *bytes);
 
 /* Number of weight pointers orca_engine_create expects: 4 + 12 * n_layers.
@@ -175,7 +177,10 @@ int orca_weight_count(const orca_config *cfg, int32_t *count);
  * caller and must outlive the engine.  Passing weights = kv_pool =
  * workspace = NULL creates a host-only engine (scheduler and slot pool
  * only; orca_iteration then returns ORCA_ESTATE) that makes no CUDA call.
- * The current CUDA device at creation is the engine's device. */
+ * The current CUDA device at creation is the engine's device.  A bf16
+ * engine reads the weights once here (after a device synchronisation) to
+ * derive the vectors of its folded LayerNorms: the weights must not change
+ * while the engine lives. */
 int orca_engine_create(const orca_config *cfg, const void *const *weights, int32_t n_weights,
                        void *kv_pool, size_t kv_bytes, void *workspace, size_t ws_bytes,
                        orca_engine **out);
