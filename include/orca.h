@@ -311,6 +311,14 @@ int orca_last_launches(const orca_engine *eng, int32_t *n_kernels);
 int orca_argmax_rows(const float *logits_dev, int32_t n_rows, int32_t vocab, int32_t *out_dev,
                      void *stream);
 
+/* Self-test of the kernels' failure path.  Every wait inside the library's
+ * kernels is bounded (about 2 s); on expiry the kernel ORs 1 into its device
+ * status word and returns, so the CUDA context stays usable.  This call
+ * enqueues one CTA on `stream` that waits on a barrier nothing completes:
+ * after the bound it ORs 1 into *status_dev (a device int32) and ends.
+ * Returns ORCA_ECUDA if the launch fails, else ORCA_OK (not synchronised). */
+int orca_selftest_wait_timeout(int32_t *status_dev, void *stream);
+
 /* The token-wise Linear of Figure 5 on its own - the kernel orca_iteration
  * runs for the QKV, Attn-Out and MLP Linears and the LM head - exposed for
  * tests and benchmarks:  out[m, n] = f(sum_k A[m, k] W[n, k] + bias[n]),

@@ -1551,6 +1551,11 @@ int orca_argmax_rows(const float *logits_dev, int32_t n_rows, int32_t vocab, int
              : ORCA_ECUDA;
 }
 
+int orca_selftest_wait_timeout(int32_t *status_dev, void *stream) {
+  if (!status_dev) return ORCA_EINVAL;
+  return launch_wait_selftest(status_dev, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
+}
+
 int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const float *bias, void *out, int32_t M,
                 int32_t N, int32_t K, void *scratch, size_t scratch_bytes, void *argmax_keys_dev, int32_t *status_dev,
                 void *stream) {

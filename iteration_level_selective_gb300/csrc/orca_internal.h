@@ -205,6 +205,10 @@ cudaError_t launch_ln_fold_vectors(const void *W, const float *gamma, const floa
 cudaError_t launch_layernorm(int dtype, const float *x, const float *g, const float *b, void *out,
                              int n_rows, const int32_t *n_rows_dev, int H, const ReqInfo *gather_last_row,
                              unsigned long long *zero_keys, cudaStream_t st);
+// One CTA that waits on an mbarrier nothing completes: the bounded wait
+// expires and raises kStatusWaitTimeout in *status (the failure path of
+// every kernel's waits, exercised without a fault).
+cudaError_t launch_wait_selftest(int32_t *status, cudaStream_t st);
 // Greedy choice per row: column index to `out`, or its packed argmax_key to `keys` when given.
 cudaError_t launch_argmax(const float *logits, int n_rows, int vocab, int32_t *out, unsigned long long *keys,
                           cudaStream_t st);
