@@ -234,7 +234,8 @@ Layout make_layout(const orca_config *c) {
 // Fold vectors of layer l: 0 = c of QKV, 1 = d of QKV, 2 = c of FC1, 3 = d of FC1.
 float *fold_vec(char *ws, const Layout &L, const orca_config &c, int l, int which) {
   const size_t H = c.hidden, F = c.ffn;
-  const size_t at = (size_t)l * 2 * (3 * H + F) + (which == 0 ? 0 : which == 1 ? 3 * H : which == 2 ? 6 * H : 6 * H + F);
+  const size_t within = which == 0 ? 0 : which == 1 ? 3 * H : which == 2 ? 6 * H : 6 * H + F;
+  const size_t at = (size_t)l * 2 * (3 * H + F) + within;
   return reinterpret_cast<float *>(ws + L.fold) + at;
 }
 
@@ -906,10 +907,12 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
       for (int l = 0; l < cfg->n_layers && okf; ++l)
         okf = launch_ln_fold_vectors(lw(e, l, L_WQKV), (const float *)lw(e, l, L_LN1_G),
                                      (const float *)lw(e, l, L_LN1_B), (const float *)lw(e, l, L_BQKV), 3 * H, H,
-                                     fold_vec(e->ws, L, *cfg, l, 0), fold_vec(e->ws, L, *cfg, l, 1), 0) == cudaSuccess &&
+                                     fold_vec(e->ws, L, *cfg, l, 0), fold_vec(e->ws, L, *cfg, l, 1),
+                                     0) == cudaSuccess &&
               launch_ln_fold_vectors(lw(e, l, L_W1), (const float *)lw(e, l, L_LN2_G),
                                      (const float *)lw(e, l, L_LN2_B), (const float *)lw(e, l, L_B1), F, H,
-                                     fold_vec(e->ws, L, *cfg, l, 2), fold_vec(e->ws, L, *cfg, l, 3), 0) == cudaSuccess;
+                                     fold_vec(e->ws, L, *cfg, l, 2), fold_vec(e->ws, L, *cfg, l, 3),
+                                     0) == cudaSuccess;
       if (!okf || cudaDeviceSynchronize() != cudaSuccess) rc = ORCA_ECUDA;
     }
     if (rc) {
@@ -1349,7 +1352,8 @@ int orca_iteration_wait(orca_engine *e, int32_t *n_batch, int32_t *batch_idx, in
     int32_t *status = ws_ptr<int32_t>(e, e->lay.out[k]);
     cudaMemsetAsync(status, 0, 4, S.st);
     cudaStreamSynchronize(S.st);
-    return fail(e, ORCA_EDEVICE, "device status word 0x%x (1 wait timeout, 2 bad index, 4 bad shape, 8 out of range)", dev_status);
+    return fail(e, ORCA_EDEVICE, "device status word 0x%x (1 wait timeout, 2 bad index, 4 bad shape, 8 out of range)",
+                dev_status);
   }
   for (int32_t i = 0; i < S.n_batch; ++i) {
     const int32_t tok = argmax_key_col(S.h_out[1 + i]);
