@@ -155,7 +155,9 @@ typedef struct {
 int orca_kv_pool_bytes(const orca_config *cfg, size_t *bytes);
 
 /* Bytes of device workspace orca_engine_create needs (activations, the
- * device batch descriptor, attention scratch, logits). */
+ * device batch descriptor, attention scratch, logits; in bf16 also the
+ * row statistics and per-layer vectors of the LayerNorms folded into the
+ * Linears after them). */
 int orca_workspace_bytes(const orca_config *cfg, size_t *bytes);
 
 /* Number of weight pointers orca_engine_create expects: 4 + 12 * n_layers.
@@ -175,7 +177,10 @@ int orca_weight_count(const orca_config *cfg, int32_t *count);
  * caller and must outlive the engine.  Passing weights = kv_pool =
  * workspace = NULL creates a host-only engine (scheduler and slot pool
  * only; orca_iteration then returns ORCA_ESTATE) that makes no CUDA call.
- * The current CUDA device at creation is the engine's device. */
+ * The current CUDA device at creation is the engine's device.  A bf16
+ * engine reads the weights once here (after a device synchronisation) to
+ * derive the vectors of its folded LayerNorms: the weights must not change
+ * while the engine lives. */
 int orca_engine_create(const orca_config *cfg, const void *const *weights, int32_t n_weights,
                        void *kv_pool, size_t kv_bytes, void *workspace, size_t ws_bytes,
                        orca_engine **out);
@@ -305,6 +310,14 @@ int orca_last_launches(const orca_engine *eng, int32_t *n_kernels);
  * enqueued on `stream`, not synchronised. */
 int orca_argmax_rows(const float *logits_dev, int32_t n_rows, int32_t vocab, int32_t *out_dev,
                      void *stream);
+
+/* Self-test of the kernels' failure path.  Every wait inside the library's
+ * kernels is bounded (about 2 s); on expiry the kernel ORs 1 into its device
+ * status word and returns, so the CUDA context stays usable.  This call
+ * enqueues one CTA on `stream` that waits on a barrier nothing completes:
+ * after the bound it ORs 1 into *status_dev (a device int32) and ends.
+ * Returns ORCA_ECUDA if the launch fails, else ORCA_OK (not synchronised). */
+int orca_selftest_wait_timeout(int32_t *status_dev, void *stream);
 
 /* The token-wise Linear of Figure 5 on its own - the kernel orca_iteration
  * runs for the QKV, Attn-Out and MLP Linears and the LM head - exposed for

@@ -70,7 +70,8 @@ EXPORTS = ("orca_kv_pool_bytes", "orca_workspace_bytes", "orca_weight_count", "o
            "orca_iteration", "orca_last_descriptor", "orca_argmax_rows", "orca_profile_enable",
            "orca_profile_read", "orca_last_error", "orca_linear", "orca_last_transfer",
            "orca_attention_workspace_bytes", "orca_attention", "orca_attention_noalloc", "orca_last_launches",
-           "orca_select_batch_budget", "orca_kv_usage", "orca_iteration_submit", "orca_iteration_wait")
+           "orca_select_batch_budget", "orca_kv_usage", "orca_iteration_submit", "orca_iteration_wait",
+           "orca_selftest_wait_timeout")
 
 _lib = None
 
@@ -113,6 +114,7 @@ def lib() -> ctypes.CDLL:
             "orca_attention_workspace_bytes": [c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_sz)],
             "orca_attention": [c_i32, c_i32, c_i32, c_i64, P, P, P, P, c_i32, i32p, i32p, i64p, P, c_sz, P, P],
             "orca_attention_noalloc": [c_i32, c_i32, c_i32, c_i64, P, P, P, P, c_i32, i32p, i32p, i64p, P, P],
+            "orca_selftest_wait_timeout": [P, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -287,6 +289,12 @@ def orca_attention_noalloc(dtype: int, n_heads: int, head_dim: int, n_slots: int
 def orca_argmax_rows(logits_ptr: int, n_rows: int, vocab: int, out_ptr: int, stream=0) -> None:
     _check(lib().orca_argmax_rows(ctypes.c_void_p(logits_ptr), n_rows, vocab, ctypes.c_void_p(out_ptr),
                                   ctypes.c_void_p(stream or None)))
+
+
+def orca_selftest_wait_timeout(status_ptr: int, stream=0) -> None:
+    """Enqueue one CTA whose bounded wait expires (about 2 s): it ORs 1
+    into the device status word and ends."""
+    _check(lib().orca_selftest_wait_timeout(ctypes.c_void_p(status_ptr), ctypes.c_void_p(stream or None)))
 
 
 ORCA_LINEAR_STORE, ORCA_LINEAR_GELU, ORCA_LINEAR_RESID, ORCA_LINEAR_F32OUT = 0, 1, 2, 3

@@ -1,5 +1,6 @@
 // Token-wise, HBM-bound kernels of one selectively batched iteration:
-// embedding gather, LayerNorm, greedy argmax.
+// embedding gather (with the first LayerNorm), LayerNorm, greedy argmax; and
+// the one-time vectors of a LayerNorm folded into the Linear after it.
 //
 // These operate on every row of the flattened [sum L_i, H] tensor without
 // knowing which request a row belongs to (Orca walk-through, section on
@@ -38,30 +39,6 @@ __device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 v) {
   u.x = *reinterpret_cast<uint32_t *>(&a);
   u.y = *reinterpret_cast<uint32_t *>(&b);
   *reinterpret_cast<uint2 *>(p) = u;
-}
-
-// x[r] = tok_emb[tok_r] + pos_emb[pos_r]  (fp32 residual stream)
-template <typename T>
-__global__ void embed_kernel(const RowInfo *__restrict__ rows, int n_rows_arg, const int32_t *n_rows_dev,
-                             const T *__restrict__ tok_emb, const T *__restrict__ pos_emb, float *__restrict__ x,
-                             int H, int vocab, int max_pos, int32_t *status) {
-  pdl_trigger();
-  const int n_rows = n_rows_dev ? *n_rows_dev : n_rows_arg;
-  pdl_wait();
-  for (int r = blockIdx.x; r < n_rows; r += gridDim.x) {
-    const RowInfo ri = rows[r];
-    if (ri.tok < 0 || ri.tok >= vocab || ri.pos < 0 || ri.pos >= max_pos) {
-      if (threadIdx.x == 0) atomicOr(status, kStatusBadIndex);
-      continue;
-    }
-    const T *te = tok_emb + (int64_t)ri.tok * H;
-    const T *pe = pos_emb + (int64_t)ri.pos * H;
-    float *xr = x + (int64_t)r * H;
-    for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
-      float4 a = load4(te + c), b = load4(pe + c);
-      store4(xr + c, make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
-    }
-  }
 }
 
 // LayerNorm of one row by one warp: (x - mean) / sqrt(var + eps) * g + b,
@@ -114,6 +91,37 @@ __device__ __forceinline__ void layernorm_row(const float *__restrict__ x, const
       float4 v = load4(xr + c), gg = load4(g + c), bv = load4(b + c);
       store4(orow + c, make_float4((v.x - mean) * rstd * gg.x + bv.x, (v.y - mean) * rstd * gg.y + bv.y,
                                    (v.z - mean) * rstd * gg.z + bv.z, (v.w - mean) * rstd * gg.w + bv.w));
+    }
+  }
+}
+
+// x[r] = tok_emb[tok_r] + pos_emb[pos_r]  (fp32 residual stream), one CTA
+// per row.  With ln_out, warp 0 then takes the row's LayerNorm (the first
+// block's LN1) from the x just written, so that no separate launch reads x.
+template <typename T>
+__global__ void embed_kernel(const RowInfo *__restrict__ rows, int n_rows_arg, const int32_t *n_rows_dev,
+                             const T *__restrict__ tok_emb, const T *__restrict__ pos_emb, float *__restrict__ x,
+                             int H, int vocab, int max_pos, int32_t *status, const float *__restrict__ ln_g,
+                             const float *__restrict__ ln_b, T *__restrict__ ln_out) {
+  pdl_trigger();
+  const int n_rows = n_rows_dev ? *n_rows_dev : n_rows_arg;
+  pdl_wait();
+  for (int r = blockIdx.x; r < n_rows; r += gridDim.x) {
+    const RowInfo ri = rows[r];
+    if (ri.tok < 0 || ri.tok >= vocab || ri.pos < 0 || ri.pos >= max_pos) {
+      if (threadIdx.x == 0) atomicOr(status, kStatusBadIndex);
+      continue;
+    }
+    const T *te = tok_emb + (int64_t)ri.tok * H;
+    const T *pe = pos_emb + (int64_t)ri.pos * H;
+    float *xr = x + (int64_t)r * H;
+    for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+      float4 a = load4(te + c), b = load4(pe + c);
+      store4(xr + c, make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
+    }
+    if (ln_out != nullptr) {
+      __syncthreads();  // the row of x is written
+      if (threadIdx.x < 32) layernorm_row<T, 0>(x, ln_g, ln_b, ln_out, r, r, H, threadIdx.x);
     }
   }
 }
@@ -187,21 +195,54 @@ __global__ void argmax_kernel(const float *__restrict__ logits, int V, int32_t *
   }
 }
 
+// c[n] = sum_k gamma_k W[n, k], d[n] = bias[n] + sum_k beta_k W[n, k]: one
+// warp per output column n, fp32 sums over the bf16 row W[n, :].
+__global__ void ln_fold_vectors_kernel(const __nv_bfloat16 *__restrict__ W, const float *__restrict__ gamma,
+                                       const float *__restrict__ beta, const float *__restrict__ bias, int N, int K,
+                                       float *__restrict__ c, float *__restrict__ d) {
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (n >= N) return;
+  const __nv_bfloat16 *wr = W + (int64_t)n * K;
+  float sc = 0.f, sd = 0.f;
+  for (int k = lane; k < K; k += 32) {
+    const float w = __bfloat162float(wr[k]);
+    sc += gamma[k] * w;
+    sd += beta[k] * w;
+  }
+  sc = warp_sum(sc);
+  sd = warp_sum(sd);
+  if (lane == 0) {
+    c[n] = sc;
+    d[n] = (bias != nullptr ? bias[n] : 0.f) + sd;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows, const int32_t *n_rows_dev, const void *tok_emb,
                          const void *pos_emb, float *x, int H, int vocab, int max_pos, int32_t *status,
-                         cudaStream_t st) {
+                         const float *ln_g, const float *ln_b, void *ln_out, cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
   const int threads = H >= 512 ? 128 : 32;
   const int grid = n_rows < 1184 ? n_rows : 1184;
+  if ((ln_out != nullptr) != (ln_g != nullptr && ln_b != nullptr)) return cudaErrorInvalidValue;
   if (dtype == 1)
     return launch_pdl(embed_kernel<__nv_bfloat16>, grid, threads, 0, st, rows, n_rows, n_rows_dev,
                       static_cast<const __nv_bfloat16 *>(tok_emb), static_cast<const __nv_bfloat16 *>(pos_emb), x, H,
-                      vocab, max_pos, status);
+                      vocab, max_pos, status, ln_g, ln_b, static_cast<__nv_bfloat16 *>(ln_out));
   return launch_pdl(embed_kernel<float>, grid, threads, 0, st, rows, n_rows, n_rows_dev,
                     static_cast<const float *>(tok_emb), static_cast<const float *>(pos_emb), x, H, vocab, max_pos,
-                    status);
+                    status, ln_g, ln_b, static_cast<float *>(ln_out));
+}
+
+cudaError_t launch_ln_fold_vectors(const void *W, const float *gamma, const float *beta, const float *bias, int N,
+                                   int K, float *c, float *d, cudaStream_t st) {
+  if (N <= 0 || K <= 0) return cudaErrorInvalidValue;
+  const int warps = 8;
+  ln_fold_vectors_kernel<<<(N + warps - 1) / warps, 32 * warps, 0, st>>>(
+      static_cast<const __nv_bfloat16 *>(W), gamma, beta, bias, N, K, c, d);
+  return cudaGetLastError();
 }
 
 template <typename T>

@@ -194,14 +194,90 @@ __device__ __forceinline__ float run_bias(const EpiParams &epi, int col, int cnt
   return epi.bias != nullptr && lane < cnt ? __ldg(epi.bias + col + lane) : 0.f;
 }
 
+// LayerNorm folded into this Linear: v = rstd * (v - mean * c), with the
+// row's mean and rstd from its fixed-point sums (biased variance, eps 1e-5,
+// as the LayerNorm kernel).  Every lane calls it (c is shuffled).
+__device__ __forceinline__ void fold_ln(const EpiParams &epi, int row, int col, float *v, int cnt, bool active) {
+  const int lane = threadIdx.x & 31;
+  const float cl = lane < cnt ? __ldg(epi.ln_c + col + lane) : 0.f;
+  float mean = 0.f, rstd = 0.f;
+  if (active) {
+    const LnStats st = epi.ln_in[row];
+    const float inv = 1.f / ((float)epi.ln_width * kLnStatScale);
+    mean = (float)(long long)st.sum * inv;
+    const float ex2 = (float)(long long)st.sumsq * inv;
+    rstd = rsqrtf(fmaxf(ex2 - mean * mean, 0.f) + 1e-5f);
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = rstd * (v[i] - mean * __shfl_sync(0xffffffffu, cl, i));
+}
+
+// Residual rows that feed the next LayerNorm: x += v, then bf16(gamma * x)
+// to ln_xb and the run's sums of x and x^2 into the row's statistics.  On
+// return v holds the new x and g gamma * x.
+__device__ __forceinline__ void resid_ln_run(const EpiParams &epi, int row, int col, float *v, float *g, int cnt) {
+  float *xp = static_cast<float *>(epi.out) + (int64_t)row * epi.ldo + col;
+  if ((reinterpret_cast<uintptr_t>(xp) & 15) == 0) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      if (i + 4 <= cnt) {
+        float4 o = *reinterpret_cast<float4 *>(xp + i);
+        o.x += v[i]; o.y += v[i + 1]; o.z += v[i + 2]; o.w += v[i + 3];
+        *reinterpret_cast<float4 *>(xp + i) = o;
+        v[i] = o.x; v[i + 1] = o.y; v[i + 2] = o.z; v[i + 3] = o.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (i + j < cnt) {
+            v[i + j] += xp[i + j];
+            xp[i + j] = v[i + j];
+          }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < cnt) {
+        v[i] += xp[i];
+        xp[i] = v[i];
+      }
+  }
+  float s = 0.f, ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i < cnt) {
+      s += v[i];
+      ss += v[i] * v[i];
+      g[i] *= v[i];
+    }
+  store_run<__nv_bfloat16, 32>(static_cast<__nv_bfloat16 *>(epi.ln_xb) + (int64_t)row * epi.ldo + col, g, cnt);
+  if (!(fabsf(s) < kLnStatMax && ss < kLnStatMax)) {  // also NaN
+    atomicOr(epi.status, kStatusRange);
+    return;
+  }
+  atomicAdd(&epi.ln_out[row].sum, (unsigned long long)__float2ll_rn(s * kLnStatScale));
+  atomicAdd(&epi.ln_out[row].sumsq, (unsigned long long)__float2ll_rn(ss * kLnStatScale));
+}
+
 // bl: this lane's bias value of the run (run_bias), loaded ahead.
 __device__ __forceinline__ void finish_run(const EpiParams &epi, int row, int col, float *v, int cnt, bool active,
                                            unsigned long long &best, float bl) {
+  if (epi.ln_in != nullptr) fold_ln(epi, row, col, v, cnt, active);
   if (epi.bias != nullptr) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] += __shfl_sync(0xffffffffu, bl, i);
   }
+  if (epi.ln_gamma != nullptr) {  // residual mode feeding the next LayerNorm
+    const int lane = threadIdx.x & 31;
+    const float gl = lane < cnt ? __ldg(epi.ln_gamma + col + lane) : 0.f;
+    float g[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) g[i] = __shfl_sync(0xffffffffu, gl, i);
+    if (active) resid_ln_run(epi, row, col, v, g, cnt);
+    return;
+  }
   if (!active) return;
+  if (epi.ln_zero != nullptr && col == 0) epi.ln_zero[row] = LnStats{0ull, 0ull};
   epi_store<__nv_bfloat16, 32>(epi, row, col, v, cnt);
   if (epi.argmax_keys != nullptr) {
 #pragma unroll

@@ -150,6 +150,10 @@ constexpr int kMaxInflight = 2;
 
 struct Layout {  // byte offsets into the device workspace
   size_t x, h, q, u, hf, logits, part, counters, gemm_cnt, gemm_part, total;
+  // LayerNorms folded into the Linears after them (bf16): the scaled rows
+  // bf16(gamma * x), two row-statistics buffers and per layer the vectors
+  // c, d of QKV (3H each) and of FC1 (F each)
+  size_t xb, ln_a, ln_b, fold;
   size_t out[kMaxInflight], req[kMaxInflight], row[kMaxInflight], work[kMaxInflight], work_tc[kMaxInflight];
   size_t blocks[kMaxInflight];  // paged K/V: the batch's block tables
   int max_work;
@@ -218,8 +222,21 @@ Layout make_layout(const orca_config *c) {
   L.counters = take((B * c->n_heads + 4) * 4);  // split arrivals, then two work tickets
   L.gemm_cnt = take(kGemmMaxSms * 4);
   L.gemm_part = take(kGemmPartialBytes);
+  const bool fold = c->dtype == ORCA_DTYPE_BF16;
+  L.xb = take(fold ? R * H * 2 : 0);
+  L.ln_a = take(fold ? R * sizeof(LnStats) : 0);
+  L.ln_b = take(fold ? R * sizeof(LnStats) : 0);
+  L.fold = take(fold ? (size_t)c->n_layers * 2 * (3 * H + F) * 4 : 0);
   L.total = o;
   return L;
+}
+
+// Fold vectors of layer l: 0 = c of QKV, 1 = d of QKV, 2 = c of FC1, 3 = d of FC1.
+float *fold_vec(char *ws, const Layout &L, const orca_config &c, int l, int which) {
+  const size_t H = c.hidden, F = c.ffn;
+  const size_t within = which == 0 ? 0 : which == 1 ? 3 * H : which == 2 ? 6 * H : 6 * H + F;
+  const size_t at = (size_t)l * 2 * (3 * H + F) + within;
+  return reinterpret_cast<float *>(ws + L.fold) + at;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -341,7 +358,7 @@ struct orca_engine {
   IterSlot slot[kMaxInflight];
   int q_head = 0, q_len = 0;  // submitted iterations, oldest first
   // tensor maps (bf16)
-  OperandMaps tm_h{}, tm_u{}, tm_hf{};  // GEMM activation operands
+  OperandMaps tm_h{}, tm_u{}, tm_hf{}, tm_xb{};  // GEMM activation operands
   CUtensorMap tm_q{};
   std::vector<CUtensorMap> tm_k;      // per layer: K slots as [n_heads * n_slots, head_dim]
   std::vector<CUtensorMap> tm_v;      // per layer: V slots, same view
@@ -524,6 +541,12 @@ struct FwdSizes {
 // Enqueue the forward of one iteration on `st`: embedding, the layers
 // (LN1, QKV + K/V Split, ragged attention, Attn-Out + residual, LN2, FC1 +
 // GeLU, FC2 + residual), final LN on the last rows, LM head + greedy choice.
+// In bf16 the LayerNorms inside the layers launch nothing of their own: the
+// first runs in the embedding kernel, the others are folded into QKV / FC1.
+// Two row-statistics buffers alternate; each is cleared by a Linear that runs
+// after its last reader and before its next writer in stream order (QKV
+// clears ln_a, which Attn-Out fills and FC1 reads; FC1 clears ln_b, which
+// FC2 fills and the next QKV reads).
 // graph = true: every kernel reads its sizes from the device header and
 // grids are fixed (the sequence is being captured into a CUDA graph);
 // otherwise sizes are passed by value.  Profiling events only when eager.
@@ -554,10 +577,20 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
   const int N_grid = graph ? c.max_rows : N;
   const int B_grid = graph ? c.max_bs : B;
 
+  // bf16: each LayerNorm inside the layers is folded into the Linear after it
+  // (the residual epilogue before it writes bf16(gamma * x) and the row sums);
+  // the first one runs in the embedding kernel
+  const bool fold = bf16;
+  void *xb = e->ws + Ly.xb;
+  LnStats *ln_a = ws_ptr<LnStats>(e, Ly.ln_a);  // LN2 of each layer
+  LnStats *ln_b = ws_ptr<LnStats>(e, Ly.ln_b);  // LN1 of layers 1 ..
+
   cudaEvent_t ev;
   prof_begin(e, st, &ev);
-  LAUNCH(e, launch_embed(c.dtype, d_row, N_grid, N_dev, e->w[W_TOK], e->w[W_POS], x, H, V, c.max_pos, status, st));
-  prof_end(e, st, ev, ORCA_K_EMBED, 0.0, (double)N * H * (2 * eb + 4));
+  LAUNCH(e, launch_embed(c.dtype, d_row, N_grid, N_dev, e->w[W_TOK], e->w[W_POS], x, H, V, c.max_pos, status,
+                         fold ? (const float *)lw(e, 0, L_LN1_G) : nullptr,
+                         fold ? (const float *)lw(e, 0, L_LN1_B) : nullptr, fold ? h : nullptr, st));
+  prof_end(e, st, ev, ORCA_K_EMBED, 0.0, (double)N * H * (2 * eb + 4 + (fold ? eb : 0)));
 
   const size_t layer_kv = (size_t)2 * nh * c.n_slots * D * eb;
   const double attn_flops = 4.0 * D * z.attn_pairs * nh;
@@ -567,16 +600,24 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
   for (int l = 0; l < c.n_layers; ++l) {
     char *kl = e->kv + (size_t)l * layer_kv;
     char *vl = kl + layer_kv / 2;
-    // h = LN1(x)
-    prof_begin(e, st, &ev);
-    LAUNCH(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN1_G), (const float *)lw(e, l, L_LN1_B), h,
-                                 N_grid, N_dev, H, nullptr, nullptr, st));
-    prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
+    const bool fold_in = fold && l > 0;  // LN1 folded into QKV (layer 0: the embedding kernel's LN)
+    if (!fold) {  // h = LN1(x)
+      prof_begin(e, st, &ev);
+      LAUNCH(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN1_G), (const float *)lw(e, l, L_LN1_B), h,
+                                   N_grid, N_dev, H, nullptr, nullptr, st));
+      prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
+    }
     // QKV Linear; K/V scattered to the requests' slots (Split)
     EpiParams ep{};
     ep.mode = kEpiQKV;
     ep.ldo = H;
-    ep.bias = (const float *)lw(e, l, L_BQKV);
+    ep.bias = fold_in ? fold_vec(e->ws, Ly, c, l, 1) : (const float *)lw(e, l, L_BQKV);
+    if (fold_in) {
+      ep.ln_in = ln_b;
+      ep.ln_c = fold_vec(e->ws, Ly, c, l, 0);
+      ep.ln_width = H;
+    }
+    if (fold) ep.ln_zero = ln_a;  // for this layer's Attn-Out epilogue
     ep.out = q;
     ep.k_layer = kl;
     ep.v_layer = vl;
@@ -587,8 +628,8 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     ep.status = status;
     prof_begin(e, st, &ev);
     if (bf16)
-      LAUNCH(e, launch_gemm_tc_bf16(e->tm_h, e->tm_layer[4 * l + 0], N, N_dev, 3 * H, H, ep, scr,
-                                    status, st));
+      LAUNCH(e, launch_gemm_tc_bf16(fold_in ? e->tm_xb : e->tm_h, e->tm_layer[4 * l + 0], N, N_dev, 3 * H, H, ep,
+                                    scr, status, st));
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WQKV), N, 3 * H, H, ep, st));
     prof_end(e, st, ev, ORCA_K_GEMM_QKV, 2.0 * N * 3 * H * H, gemm_bytes(N, 3.0 * H, H, eb));
@@ -642,29 +683,41 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     eo.bias = (const float *)lw(e, l, L_BO);
     eo.out = x;
     eo.status = status;
+    if (fold) {  // the residual feeds LN2: bf16(gamma2 * x) and the row sums
+      eo.ln_gamma = (const float *)lw(e, l, L_LN2_G);
+      eo.ln_xb = xb;
+      eo.ln_out = ln_a;
+    }
     prof_begin(e, st, &ev);
     if (bf16)
       LAUNCH(e, launch_gemm_tc_bf16(e->tm_h, e->tm_layer[4 * l + 1], N, N_dev, H, H, eo, scr, status,
                                     st));
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WO), N, H, H, eo, st));
-    prof_end(e, st, ev, ORCA_K_GEMM_O, 2.0 * N * H * H, gemm_bytes(N, H, H, 8));
-    // h = LN2(x)
-    prof_begin(e, st, &ev);
-    LAUNCH(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN2_G), (const float *)lw(e, l, L_LN2_B), h,
-                                 N_grid, N_dev, H, nullptr, nullptr, st));
-    prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
-    // u = GeLU(h W1 + b1)
+    prof_end(e, st, ev, ORCA_K_GEMM_O, 2.0 * N * H * H, gemm_bytes(N, H, H, fold ? 8 + eb : 8));
+    if (!fold) {  // h = LN2(x)
+      prof_begin(e, st, &ev);
+      LAUNCH(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN2_G), (const float *)lw(e, l, L_LN2_B), h,
+                                   N_grid, N_dev, H, nullptr, nullptr, st));
+      prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
+    }
+    // u = GeLU(LN2(x) W1 + b1)
     EpiParams e1{};
     e1.mode = kEpiGelu;
     e1.ldo = F;
-    e1.bias = (const float *)lw(e, l, L_B1);
+    e1.bias = fold ? fold_vec(e->ws, Ly, c, l, 3) : (const float *)lw(e, l, L_B1);
     e1.out = u;
     e1.status = status;
+    if (fold) {
+      e1.ln_in = ln_a;
+      e1.ln_c = fold_vec(e->ws, Ly, c, l, 2);
+      e1.ln_width = H;
+      e1.ln_zero = ln_b;  // for this layer's FC2 epilogue
+    }
     prof_begin(e, st, &ev);
     if (bf16)
-      LAUNCH(e, launch_gemm_tc_bf16(e->tm_h, e->tm_layer[4 * l + 2], N, N_dev, F, H, e1, scr, status,
-                                    st));
+      LAUNCH(e, launch_gemm_tc_bf16(fold ? e->tm_xb : e->tm_h, e->tm_layer[4 * l + 2], N, N_dev, F, H, e1, scr,
+                                    status, st));
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_W1), N, F, H, e1, st));
     prof_end(e, st, ev, ORCA_K_GEMM_FC1, 2.0 * N * F * H, gemm_bytes(N, F, H, eb));
@@ -675,13 +728,19 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     e2.bias = (const float *)lw(e, l, L_B2);
     e2.out = x;
     e2.status = status;
+    const bool feeds_ln1 = fold && l + 1 < c.n_layers;  // the next layer's LN1 (the last feeds the final LN)
+    if (feeds_ln1) {
+      e2.ln_gamma = (const float *)lw(e, l + 1, L_LN1_G);
+      e2.ln_xb = xb;
+      e2.ln_out = ln_b;
+    }
     prof_begin(e, st, &ev);
     if (bf16)
       LAUNCH(e, launch_gemm_tc_bf16(e->tm_u, e->tm_layer[4 * l + 3], N, N_dev, H, F, e2, scr, status,
                                     st));
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)u, (const float *)lw(e, l, L_W2), N, H, F, e2, st));
-    prof_end(e, st, ev, ORCA_K_GEMM_FC2, 2.0 * N * H * F, gemm_bytes(N, H, F, 8));
+    prof_end(e, st, ev, ORCA_K_GEMM_FC2, 2.0 * N * H * F, gemm_bytes(N, H, F, feeds_ln1 ? 8 + eb : 8));
   }
   // final LayerNorm on each request's last row, LM head (tied), greedy choice
   prof_begin(e, st, &ev);
@@ -839,6 +898,22 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
       if (!rc) rc = make_operand_maps(e, &e->tm_layer[4 * l + 1], lw(e, l, L_WO), H, H);
       if (!rc) rc = make_operand_maps(e, &e->tm_layer[4 * l + 2], lw(e, l, L_W1), F, H);
       if (!rc) rc = make_operand_maps(e, &e->tm_layer[4 * l + 3], lw(e, l, L_W2), H, F);
+    }
+    if (!rc) rc = make_operand_maps(e, &e->tm_xb, e->ws + L.xb, cfg->max_rows, H);
+    // c and d of every folded LayerNorm, from the weights as they are now (the
+    // caller keeps them unchanged for the engine's lifetime)
+    if (!rc) {
+      bool okf = cudaDeviceSynchronize() == cudaSuccess;
+      for (int l = 0; l < cfg->n_layers && okf; ++l)
+        okf = launch_ln_fold_vectors(lw(e, l, L_WQKV), (const float *)lw(e, l, L_LN1_G),
+                                     (const float *)lw(e, l, L_LN1_B), (const float *)lw(e, l, L_BQKV), 3 * H, H,
+                                     fold_vec(e->ws, L, *cfg, l, 0), fold_vec(e->ws, L, *cfg, l, 1),
+                                     0) == cudaSuccess &&
+              launch_ln_fold_vectors(lw(e, l, L_W1), (const float *)lw(e, l, L_LN2_G),
+                                     (const float *)lw(e, l, L_LN2_B), (const float *)lw(e, l, L_B1), F, H,
+                                     fold_vec(e->ws, L, *cfg, l, 2), fold_vec(e->ws, L, *cfg, l, 3),
+                                     0) == cudaSuccess;
+      if (!okf || cudaDeviceSynchronize() != cudaSuccess) rc = ORCA_ECUDA;
     }
     if (rc) {
       orca_engine_destroy(e);
@@ -1277,7 +1352,8 @@ int orca_iteration_wait(orca_engine *e, int32_t *n_batch, int32_t *batch_idx, in
     int32_t *status = ws_ptr<int32_t>(e, e->lay.out[k]);
     cudaMemsetAsync(status, 0, 4, S.st);
     cudaStreamSynchronize(S.st);
-    return fail(e, ORCA_EDEVICE, "device status word 0x%x (1 wait timeout, 2 bad index, 4 bad shape)", dev_status);
+    return fail(e, ORCA_EDEVICE, "device status word 0x%x (1 wait timeout, 2 bad index, 4 bad shape, 8 out of range)",
+                dev_status);
   }
   for (int32_t i = 0; i < S.n_batch; ++i) {
     const int32_t tok = argmax_key_col(S.h_out[1 + i]);
@@ -1477,6 +1553,11 @@ int orca_argmax_rows(const float *logits_dev, int32_t n_rows, int32_t vocab, int
   return launch_argmax(logits_dev, n_rows, vocab, out_dev, nullptr, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? ORCA_OK
              : ORCA_ECUDA;
+}
+
+int orca_selftest_wait_timeout(int32_t *status_dev, void *stream) {
+  if (!status_dev) return ORCA_EINVAL;
+  return launch_wait_selftest(status_dev, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ORCA_OK : ORCA_ECUDA;
 }
 
 int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const float *bias, void *out, int32_t M,

@@ -72,7 +72,21 @@ enum : int32_t {
   kStatusWaitTimeout = 1,   // an mbarrier wait gave up
   kStatusBadIndex = 2,      // a bounds check failed (access skipped)
   kStatusBadShape = 4,      // a launch got an unsupported shape
+  kStatusRange = 8,         // a value outside the range a fixed-point sum holds
 };
+
+// Row statistics of a LayerNorm input, summed across the CTAs that hold the
+// row's columns.  Each CTA's partial sums go in as integers in units of
+// kLnStatUnit: integer addition does not depend on the order the atomics
+// land in, so the sums (and every result after them) repeat bit for bit from
+// run to run.  A partial of magnitude kLnStatMax or more raises kStatusRange
+// (2^53 units per partial, at most 2^10 partials: no overflow of 63 bits).
+struct LnStats {
+  unsigned long long sum;    // sum of x, two's complement
+  unsigned long long sumsq;  // sum of x^2
+};
+constexpr float kLnStatScale = 16777216.0f;  // 1 / kLnStatUnit = 2^24
+constexpr float kLnStatMax = 536870912.0f;   // 2^29
 
 // GEMM epilogue: C[m, n] = sum_k A[m, k] W[n, k] + bias[n], then one of:
 enum EpiMode : int32_t {
@@ -95,6 +109,22 @@ struct EpiParams {
   int64_t n_slots;
   int32_t *status;        // device status word
   unsigned long long *argmax_keys;  // Logits mode: per-row packed (value, index) max, or nullptr
+  // LayerNorm folded into the Linear that consumes it (tcgen05 GEMM only).
+  // The A operand then holds bf16(gamma * x) of the un-normalised rows x, and
+  // LN(x) W + b = rstd * (A W - mean * c) + d with c = sum_k gamma_k W[n, k]
+  // and d = b + sum_k beta_k W[n, k] (d is passed as `bias`).
+  const LnStats *ln_in;   // [rows] statistics of x over ln_width columns, or nullptr (no fold)
+  const float *ln_c;      // [N] c of the fold
+  int32_t ln_width;       // LayerNorm width (hidden)
+  // Residual mode: the residual rows also feed the next LayerNorm.  The
+  // epilogue writes bf16(ln_gamma * x) to ln_xb and adds each row's partial
+  // sums of x and x^2 into ln_out (zeroed beforehand).
+  const float *ln_gamma;  // [N] gamma of the next LayerNorm, or nullptr
+  void *ln_xb;            // bf16 [rows, ldo]
+  LnStats *ln_out;        // [rows]
+  // Rows of a statistics buffer this launch clears for a later residual
+  // epilogue (by the thread that stores the row's column 0), or nullptr.
+  LnStats *ln_zero;
 };
 
 // Greedy-choice key of (value, column): larger value first, then lower
@@ -159,14 +189,26 @@ struct TcAttnArgs {
 // ---- launch wrappers (defined in the .cu files); all return cudaError_t.
 // Row counts: `n_rows` on the host, or *n_rows_dev when given (then n_rows
 // is only the capacity the fixed grid is sized for).
+// ln_g / ln_b / ln_out (optional, together): the first block's LayerNorm of
+// each embedded row, written to ln_out in the model dtype.
 cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows, const int32_t *n_rows_dev,
                          const void *tok_emb, const void *pos_emb, float *x, int H,
-                         int vocab, int max_pos, int32_t *status, cudaStream_t st);
+                         int vocab, int max_pos, int32_t *status, const float *ln_g, const float *ln_b,
+                         void *ln_out, cudaStream_t st);
+// c[n] = sum_k gamma_k W[n, k] and d[n] = bias[n] + sum_k beta_k W[n, k]
+// for a bf16 weight W [N, K] (row n = output column n): the vectors of a
+// LayerNorm folded into the Linear W.  bias may be nullptr.
+cudaError_t launch_ln_fold_vectors(const void *W, const float *gamma, const float *beta, const float *bias, int N,
+                                   int K, float *c, float *d, cudaStream_t st);
 // zero_keys (optional): per-row argmax keys set to 0 (final LayerNorm, ahead
 // of the LM head's fused greedy choice).
 cudaError_t launch_layernorm(int dtype, const float *x, const float *g, const float *b, void *out,
                              int n_rows, const int32_t *n_rows_dev, int H, const ReqInfo *gather_last_row,
                              unsigned long long *zero_keys, cudaStream_t st);
+// One CTA that waits on an mbarrier nothing completes: the bounded wait
+// expires and raises kStatusWaitTimeout in *status (the failure path of
+// every kernel's waits, exercised without a fault).
+cudaError_t launch_wait_selftest(int32_t *status, cudaStream_t st);
 // Greedy choice per row: column index to `out`, or its packed argmax_key to `keys` when given.
 cudaError_t launch_argmax(const float *logits, int n_rows, int vocab, int32_t *out, unsigned long long *keys,
                           cudaStream_t st);

@@ -395,10 +395,11 @@ def test_graph_replay_equals_eager_launches(cuda):
     for g, e in zip(*out):
         assert g.req_ids == e.req_ids and g.next_tokens == e.next_tokens
         np.testing.assert_array_equal(g.logits, e.logits)
-        # embed, final LN, LM head + per layer LN1, QKV, attention, Attn-Out,
-        # LN2, FC1, FC2, and the tensor-core prompt attention when a prompt of
-        # >= 32 rows is in the batch
-        want = 3 + nl * (7 + int(max(e.n_new) >= 32))
+        # embed (with the first LN1), final LN, LM head + per layer QKV (LN1
+        # folded in), attention, Attn-Out, FC1 (LN2 folded in), FC2, and the
+        # tensor-core prompt attention when a prompt of >= 32 rows is in the
+        # batch
+        want = 3 + nl * (5 + int(max(e.n_new) >= 32))
         assert g.launches == want and e.launches == want
 
 
