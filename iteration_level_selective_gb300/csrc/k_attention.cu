@@ -557,29 +557,30 @@ int resident_ctas() {
 }
 
 template <typename T, int D>
-cudaError_t launch_d(const AttnArgs &a, int n_work, cudaStream_t st) {
+cudaError_t launch_d(const AttnArgs &a, int n_work, cudaStream_t st, bool early) {
   const long long total = (long long)n_work * a.n_heads;
   const int cap = resident_ctas<T, D>();
   const dim3 grid(a.hdr != nullptr ? cap : (int)(total < cap ? total : cap));
-  return launch_pdl(attention_kernel<T, D>, grid, kThreads, attn_smem_bytes<T, D>(), st, a);
+  return launch_pdl_if(early, attention_kernel<T, D>, grid, kThreads, attn_smem_bytes<T, D>(), st, a);
 }
 
 template <typename T>
-cudaError_t launch_t(int head_dim, const AttnArgs &a, int n_work, cudaStream_t st) {
+cudaError_t launch_t(int head_dim, const AttnArgs &a, int n_work, cudaStream_t st, bool early) {
   switch (head_dim) {
-    case 16: return launch_d<T, 16>(a, n_work, st);
-    case 32: return launch_d<T, 32>(a, n_work, st);
-    case 64: return launch_d<T, 64>(a, n_work, st);
-    case 128: return launch_d<T, 128>(a, n_work, st);
+    case 16: return launch_d<T, 16>(a, n_work, st, early);
+    case 32: return launch_d<T, 32>(a, n_work, st, early);
+    case 64: return launch_d<T, 64>(a, n_work, st, early);
+    case 128: return launch_d<T, 128>(a, n_work, st, early);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &a, int n_work, cudaStream_t st) {
+cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &a, int n_work, cudaStream_t st, bool early) {
   if (n_work <= 0) return cudaSuccess;
-  return dtype == 1 ? launch_t<__nv_bfloat16>(head_dim, a, n_work, st) : launch_t<float>(head_dim, a, n_work, st);
+  return dtype == 1 ? launch_t<__nv_bfloat16>(head_dim, a, n_work, st, early)
+                    : launch_t<float>(head_dim, a, n_work, st, early);
 }
 
 // One-time per-device set-up of the attention kernels (shared-memory limits,

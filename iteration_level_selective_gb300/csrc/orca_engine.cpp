@@ -380,6 +380,10 @@ struct orca_engine {
   int cur_slot = 0;                          // in-flight slot of the iteration being enqueued
   // CUDA graphs of the forward, keyed by GEMM tile choices and logits pointer
   cudaStream_t cap_stream = nullptr;
+  // layers with prompt rows on the tensor cores: the decode-attention launch
+  // runs on side_stream, forked after the QKV Linear and joined before Attn-Out
+  cudaStream_t side_stream = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   struct Graph {
     cudaGraphExec_t exec;
     int32_t n_kernels;  // kernel nodes in the captured forward
@@ -656,6 +660,17 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     aa.hdr = graph ? d_hdr : nullptr;
     aa.blocks = ws_ptr<int32_t>(e, Ly.blocks[k]);
     prof_begin(e, st, &ev);
+    // With prompt rows on the tensor cores the two attention launches run side
+    // by side: the prompt launch follows the QKV Linear as a dependent launch
+    // (its CTAs take their SMs first), and the decode launch goes to the side
+    // stream as an ordinary launch after the QKV Linear has completed, so it
+    // no longer waits for the prompt launch to finish.  The streams join
+    // before Attn-Out.
+    const bool overlap = e->attn_tc && z.n_work_tc > 0;
+    if (overlap) {
+      CUDA_TRY(e, cudaEventRecord(e->ev_fork, st));
+      CUDA_TRY(e, cudaStreamWaitEvent(e->side_stream, e->ev_fork, 0));
+    }
     if (e->attn_tc && z.n_work_tc > 0) {  // prompts: tensor-core tiles; then decodes and short prompts
       TcAttnArgs ta{};
       ta.out = h;
@@ -674,7 +689,12 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
                                       z.n_work_tc, st));
       ++e->n_launch;
     }
-    LAUNCH(e, launch_attention(c.dtype, D, aa, graph ? Ly.max_work : z.n_work, st));
+    LAUNCH(e, launch_attention(c.dtype, D, aa, graph ? Ly.max_work : z.n_work, overlap ? e->side_stream : st,
+                               !overlap));
+    if (overlap) {
+      CUDA_TRY(e, cudaEventRecord(e->ev_join, e->side_stream));
+      CUDA_TRY(e, cudaStreamWaitEvent(st, e->ev_join, 0));
+    }
     prof_end(e, st, ev, ORCA_K_ATTENTION, attn_flops, attn_bytes);
     // x += a Wo + bo
     EpiParams eo{};
@@ -845,7 +865,10 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
   if (cudaGetDevice(&dev) != cudaSuccess) { delete e; return ORCA_ECUDA; }
   e->device = dev;
   const auto &L = e->lay;
-  bool ok = cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
+  bool ok = cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&e->side_stream, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&e->ev_fork, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&e->ev_join, cudaEventDisableTiming) == cudaSuccess;
   for (int k = 0; k < kMaxInflight && ok; ++k) {
     orca_engine::IterSlot &S = e->slot[k];
     ok = cudaHostAlloc(&S.h_hdr, sizeof(DevHeader) + sizeof(ReqInfo) * cfg->max_bs, cudaHostAllocDefault) ==
@@ -929,6 +952,12 @@ int orca_engine_destroy(orca_engine *e) {
   if (!e->host_only) {
     for (auto &g : e->graphs) cudaGraphExecDestroy(g.second.exec);
     if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
+    if (e->side_stream) {
+      cudaStreamSynchronize(e->side_stream);
+      cudaStreamDestroy(e->side_stream);
+    }
+    if (e->ev_fork) cudaEventDestroy(e->ev_fork);
+    if (e->ev_join) cudaEventDestroy(e->ev_join);
     for (auto &S : e->slot) {
       if (S.done) cudaEventSynchronize(S.done);
       cudaFreeHost(S.h_hdr);

@@ -263,8 +263,12 @@ cudaError_t launch_attention_tc(int head_dim, const CUtensorMap *tmQ, const CUte
                                 const CUtensorMap *tmKb, const CUtensorMap *tmVb, const TcAttnArgs &a, int n_work,
                                 cudaStream_t st);
 // Persistent over (work item, head) pairs; n_work is the host count, or
-// the capacity when args.hdr is set.
-cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &args, int n_work, cudaStream_t st);
+// the capacity when args.hdr is set.  early = false: an ordinary launch, which
+// starts only once everything before it on `st` has completed (instead of a
+// programmatic dependent launch that may start while the previous kernel
+// runs).
+cudaError_t launch_attention(int dtype, int head_dim, const AttnArgs &args, int n_work, cudaStream_t st,
+                             bool early = true);
 
 // GEMM tile shape of the tcgen05 kernel (used by the host to build TMA maps).
 constexpr int kTcBM = 128;
@@ -282,9 +286,11 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 #endif
 
+// early = true: programmatic dependent launch (the kernel may start while
+// the previous one on `st` runs; its pdl_wait() then waits for it).
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                              Args &&...args) {
+inline cudaError_t launch_pdl_if(bool early, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, Args &&...args) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -294,8 +300,14 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = early ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+  return launch_pdl_if(true, kernel, grid, block, smem, st, std::forward<Args>(args)...);
 }
 
 }  // namespace orca
