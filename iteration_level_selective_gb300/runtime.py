@@ -167,6 +167,7 @@ class IterRecord:
     logits: Optional[np.ndarray] = None
     launches: int = 0          # kernels the iteration launched on the device
     preempted: List[int] = dataclasses.field(default_factory=list)  # paged K/V: requests sent back by this Select
+    kv: Optional[tuple] = None  # (reserved, stored) K/V slots after the iteration (track_kv)
 
 
 class ServingLoop:
@@ -184,11 +185,13 @@ class ServingLoop:
 
     def __init__(self, engine: Engine, pool: RequestPool, teacher_force: bool = False, keep_logits: bool = False,
                  stream: Optional[torch.cuda.Stream] = None, keep_ids: Optional[set] = None, eager: bool = False,
-                 token_budget: Optional[int] = None, chunk: Optional[int] = None, n_workers: int = 1):
+                 token_budget: Optional[int] = None, chunk: Optional[int] = None, n_workers: int = 1,
+                 track_kv: bool = False):
         if n_workers not in (1, 2):
             raise ValueError("n_workers must be 1 or 2")
         self.eng, self.pool = engine, pool
         self.n_workers = n_workers
+        self.track_kv = track_kv
         self.flags = (C.ORCA_ITER_TEACHER_FORCE if teacher_force else 0) | (C.ORCA_ITER_EAGER if eager else 0)
         keep_logits = keep_logits or keep_ids is not None
         self.keep_logits = keep_logits
@@ -229,6 +232,8 @@ class ServingLoop:
         if done.any():
             rec.released = P.view["req_id"][idx][done].tolist()
             self.n_done += int(done.sum())
+        if self.track_kv:
+            rec.kv = C.orca_kv_usage(self.eng.handle, P.arr, self.n_arrived)
         if lg is not None:
             if self.keep_ids is None:
                 rec.logits = lg[:nb].cpu().numpy()

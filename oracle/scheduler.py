@@ -266,6 +266,8 @@ class IterRecord:
     slot_base: List[int]
     released: List[int]
     preempted: List[int] = dataclasses.field(default_factory=list)
+    # (reserved, stored) K/V slots once this iteration's results are applied
+    kv: Tuple[int, int] = (0, 0)
 
 
 def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
@@ -335,6 +337,7 @@ def run_schedule(trace, max_bs: int, n_slots: int, max_iters: int = 10_000_000,
                     slots.release(r.req_id)
                     rec.released.append(r.req_id)
             pool = [r for r in pool if r.state != FINISHED]
+            rec.kv = kv_usage(states, slots)
         elif not run:
             if pool:
                 raise RuntimeError(f"no request can be scheduled at iteration {it}")

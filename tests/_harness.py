@@ -24,7 +24,7 @@ def run_gpu(shape, host_weights, trace, max_bs, n_slots, max_rows, teacher_force
                     reserve_policy=reserve_policy)
     pool = rt.RequestPool(trace, teacher_force=teacher_force)
     loop = rt.ServingLoop(eng, pool, teacher_force=teacher_force, keep_logits=keep_all, keep_ids=keep_ids,
-                          eager=eager, token_budget=token_budget, chunk=chunk, n_workers=n_workers)
+                          eager=eager, token_budget=token_budget, chunk=chunk, n_workers=n_workers, track_kv=True)
     recs = loop.run()
     return recs, eng, pool
 
@@ -38,6 +38,8 @@ def compare_schedule(gpu_recs, trace, max_bs, n_slots, token_budget=None, chunk=
     for g, o in zip(gpu_recs, orecs):
         assert (g.it, g.req_ids, g.n_new, g.n_ctx, g.slot_base, sorted(g.released), sorted(g.preempted)) == \
                (o.it, o.req_ids, o.n_new, o.n_ctx, o.slot_base, sorted(o.released), sorted(o.preempted)), (g, o)
+        if g.kv is not None:   # reserved and stored K/V slots after the iteration
+            assert tuple(g.kv) == tuple(o.kv), (g.it, g.kv, o.kv)
     return orecs
 
 

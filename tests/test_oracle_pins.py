@@ -500,6 +500,50 @@ def test_policies_agree_when_memory_is_ample_and_stored_never_exceeds_reserved()
             assert all(r.state == scheduler.FINISHED for r in states)
 
 
+def test_kv_usage_reserved_vs_stored_by_hand():
+    """CS349D Lecture 2, section 6.1: a reservation occupies slots that are
+    not yet written ("reserved" is not "used").  Reading: after each
+    iteration, reserved = slots held by reservations, stored = sum of the
+    cached tokens of the requests that hold one.  Three requests, a 20-slot
+    pool, max_bs 3:
+        A: arrives 0, prompt 3, 4 tokens, max_tokens 10  (true length 7)
+        B: arrives 0, prompt 2, 2 tokens, max_tokens 8   (true length 4)
+        C: arrives 1, prompt 5, 3 tokens, max_tokens 12  (true length 8)
+    Max reserves max_tokens: A 10 + B 8 = 18, so C (12) waits until A and B
+    are both gone.
+        it 0: A, B prefill            -> reserved 18, stored 3 + 2
+        it 1: C does not fit (30 > 20); A 4 cached, B finishes (8 freed)
+                                      -> 10, 4
+        it 2: C still does not fit (22 > 20); A 5 cached      -> 10, 5
+        it 3: A finishes              -> 0, 0
+        it 4: C at base 0, prefill    -> 12, 5
+        it 5, 6: C decodes, then finishes -> 12, 6 and 0, 0
+    Pow2 reserves the true length rounded up to a power of two: A 8, B 4,
+    C 8; Oracle the true length: A 7, B 4, C 8.  Both admit C at it 1.
+        Pow2:   it 0 -> 12, 5; it 1 (B done, C prefills) -> 16, 4 + 5;
+                it 2 -> 16, 5 + 6; it 3 (A and C done) -> 0, 0
+        Oracle: it 0 -> 11, 5; it 1 -> 15, 9; it 2 -> 15, 11; it 3 -> 0, 0
+    A mistake that sums n_prompt or max_tokens instead of the cached tokens,
+    or that keeps a finished request's count, changes at least one pair."""
+    trace = [_R(0, 0, 3, 4, 10), _R(1, 0, 2, 2, 8), _R(2, 1, 5, 3, 12)]
+    want = {
+        scheduler.RESERVE_MAX: [(0, [0, 1], (18, 5)), (1, [0, 1], (10, 4)), (2, [0], (10, 5)),
+                                (3, [0], (0, 0)), (4, [2], (12, 5)), (5, [2], (12, 6)), (6, [2], (0, 0))],
+        scheduler.RESERVE_POW2: [(0, [0, 1], (12, 5)), (1, [0, 1, 2], (16, 9)), (2, [0, 2], (16, 11)),
+                                 (3, [0, 2], (0, 0))],
+        scheduler.RESERVE_ORACLE: [(0, [0, 1], (11, 5)), (1, [0, 1, 2], (15, 9)), (2, [0, 2], (15, 11)),
+                                   (3, [0, 2], (0, 0))],
+    }
+    for pol, rows in want.items():
+        recs = scheduler.run_schedule(trace, max_bs=3, n_slots=20, policy=pol)
+        assert [(r.it, r.req_ids, r.kv) for r in recs] == rows, pol
+    # C lands at base 0 under Max (the two freed segments merged), at 12
+    # under Pow2 (after A's 8 and B's 4) and at 11 under Oracle
+    bases = {pol: {rid: b for r in scheduler.run_schedule(trace, max_bs=3, n_slots=20, policy=pol)
+                   for rid, b in zip(r.req_ids, r.slot_base)}[2] for pol in want}
+    assert bases == {scheduler.RESERVE_MAX: 0, scheduler.RESERVE_POW2: 12, scheduler.RESERVE_ORACLE: 11}
+
+
 # ---------------------------------------------------------------- batches in flight (Algorithm 1, n_workers = 2)
 
 def test_two_workers_by_hand():
