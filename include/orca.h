@@ -381,12 +381,21 @@ int orca_attention(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_s
  * array compiled into the library, held on every device that loads it until
  * the process exits.  A batch whose scratch need (what
  * orca_attention_workspace_bytes reports) exceeds 8 MiB returns ORCA_EBATCH
- * before any launch.  The first call on a device, with that device current,
- * looks up the array's device address once; make that first call before any
- * stream capture.  All calls share the array and it keeps the last call's
- * contents; each call clears the counters it uses, and calls that overlap on
- * the GPU (unordered streams) race on it.  Nothing is allocated: no
- * cudaMalloc, cudaFree or allocating library routine is called. */
+ * before any launch.  The need grows with the number of requests (key-split
+ * partials are sized for 16 splits of every request and head), so the cap is
+ * 25 requests at 40 heads of 128, 31 at 32 heads of 128 and 164 at 12 heads
+ * of 64, whatever their rows.
+ * Set-up: the first call on a device (per CUDA context), with that device
+ * current, looks up the array's device address and keeps it.  With lazy
+ * module loading that lookup may make the driver load the library's device
+ * code and reserve the array then, so make the first call early, where the
+ * caller may still allocate, and before any stream capture.  If the device's
+ * context is replaced (cudaDeviceReset), the next call repeats the set-up.
+ * All calls share the array and it keeps the last call's contents; each call
+ * clears the counters it uses, and calls that overlap on the GPU (unordered
+ * streams) race on it.  Apart from that first-call set-up nothing is
+ * allocated: no cudaMalloc, cudaFree or allocating library routine is
+ * called. */
 int orca_attention_noalloc(int32_t dtype, int32_t n_heads, int32_t head_dim, int64_t n_slots, const void *q,
                            const void *k_layer, const void *v_layer, void *out, int32_t n_batch,
                            const int32_t *row_off, const int32_t *ctx, const int64_t *slot_base,

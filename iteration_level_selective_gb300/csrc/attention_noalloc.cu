@@ -11,13 +11,19 @@
 // their counters) in one file-scope device array of fixed size instead of a
 // caller-provided workspace.
 //
-// Set-up: the first call on a device, with that device current, looks up the
-// array's device address once (cudaGetSymbolAddress); make that first call
-// before any stream capture.  The array (kNoAllocScratchBytes) stays resident
-// on every device that loads the library until the process exits.  Every
-// call shares it and it keeps the last call's contents: each call clears the
-// counters it needs, and calls that overlap on the GPU (different streams,
-// no ordering between them) race on it.
+// Set-up: the first call on a device (per CUDA context), with that device
+// current, looks up the array's device address (cudaGetSymbolAddress) and
+// keeps it for later calls.  With lazy module loading that first lookup may
+// make the driver load this library's device code and reserve the array, so
+// make the first call early, where the caller may still allocate, and before
+// any stream capture.  When the device's context changes (after a
+// cudaDeviceReset, say) the next call repeats the set-up instead of reusing
+// an address of the old context.  The array (kNoAllocScratchBytes) stays
+// resident on every device that loads the library until the process exits.
+// Every call shares it and it keeps the last call's contents: each call
+// clears the counters it needs, and calls that overlap on the GPU (different
+// streams, no ordering between them) race on it.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -31,20 +37,47 @@ constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
 __device__ __align__(256) unsigned char g_attention_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  CUcontext ctx;  // the context the address belongs to
+  void *addr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device (looked up once).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+// cuCtxGetCurrent through the runtime's driver entry point (no libcuda link).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+// Device address of the scratch array in the current device's context
+// (looked up once per context).
 int scratch_address(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ORCA_ECUDA;
+  CtxGetCurrentFn get_ctx = ctx_get_current();
+  if (!get_ctx) return ORCA_ECUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return ORCA_ECUDA;
+  ScratchAddr &slot = g_scratch_addr[dev];
+  if (!slot.addr || !ctx || ctx != slot.ctx) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_attention_scratch) != cudaSuccess || !p) return ORCA_ECUDA;
-    g_scratch_addr[dev] = p;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return ORCA_ECUDA;  // made current by the lookup
+    slot.ctx = ctx;
+    slot.addr = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = slot.addr;
   return ORCA_OK;
 }
 

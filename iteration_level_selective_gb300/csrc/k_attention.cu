@@ -443,14 +443,20 @@ __device__ __forceinline__ void key_split(const AttnArgs &a, const AttnWork &w, 
   if (!sm.last) return;
   const int64_t s0 = (int64_t)w.req * kMaxSplits;  // the row's split partials
   if (dim < D) {
-    // online merge of the other splits' (max, sum, value) with this CTA's own
-    // (its loads are independent of one another, so they overlap)
-    float Mx = M, Lx = L, Ax = A;
+    // online merge of the splits' (max, sum, value) in split order, this
+    // CTA's own state taken from registers at its index: the result does not
+    // depend on which CTA finished last (the loads are independent of one
+    // another, so they overlap)
+    float Mx = -INFINITY, Lx = 0.f, Ax = 0.f;
 #pragma unroll 4
     for (int j = 0; j < n_splits; ++j) {
-      if (j == w.b) continue;
-      const float *pj = a.part + ((s0 + j) * a.n_heads + head) * (D + 2);
-      const float mj = __ldcg(pj + D), lj = __ldcg(pj + D + 1), aj = __ldcg(pj + dim);
+      float mj = M, lj = L, aj = A;
+      if (j != w.b) {
+        const float *pj = a.part + ((s0 + j) * a.n_heads + head) * (D + 2);
+        mj = __ldcg(pj + D);
+        lj = __ldcg(pj + D + 1);
+        aj = __ldcg(pj + dim);
+      }
       const float mn = fmaxf(Mx, mj);
       if (mn == -INFINITY) continue;
       const float c1 = exp2f(Mx - mn), c2 = exp2f(mj - mn);
