@@ -3,6 +3,7 @@
     python -m iteration_level_selective_gb300.kernel_bench linear --M 2048 --N 20480 --K 5120
     python -m iteration_level_selective_gb300.kernel_bench sweep
     python -m iteration_level_selective_gb300.kernel_bench linear-graph
+    python -m iteration_level_selective_gb300.kernel_bench linears-13b-mixed
 
 `linear` times orca_linear (the token-wise Linear of one iteration, bf16
 tcgen05) with CUDA events, after warm-up, and prints achieved TFLOP/s and
@@ -10,7 +11,11 @@ algorithmic GB/s.  `linear-graph` times the small-M Linears of GPT-2-small as
 they run in an iteration - 20 back-to-back launches captured in a CUDA graph,
 so that launch latency and programmatic dependent launch count as they do in
 the engine - next to cuBLAS (torch.nn.functional.linear) captured the same
-way.  Inputs are random on the device.
+way.  `linears-13b-mixed` runs the four token-wise Linears of one layer of
+the prefill-heavy 13B iteration (24,373 rows) and its LM head (256 rows),
+each with the epilogue the engine uses (bf16 store, fp32 residual add, GeLU),
+one warm-up and one timed launch each, for per-launch DRAM traffic captures.
+Inputs are random on the device.
 """
 from __future__ import annotations
 
@@ -21,6 +26,15 @@ import torch
 
 from . import _orca as C
 from . import build as B
+
+
+# the Linears of one layer of the prefill-heavy 13B iteration (rows of 16
+# prompts U{1024..2048} + 240 decodes) and its LM head: (name, M, N, K, mode)
+LINEARS_13B_MIXED = (("qkv", 24373, 15360, 5120, C.ORCA_LINEAR_STORE),
+                     ("attn_out", 24373, 5120, 5120, C.ORCA_LINEAR_RESID),
+                     ("fc1", 24373, 20480, 5120, C.ORCA_LINEAR_GELU),
+                     ("fc2", 24373, 5120, 20480, C.ORCA_LINEAR_RESID),
+                     ("lm_head", 256, 50257, 5120, C.ORCA_LINEAR_F32OUT))
 
 
 def time_linear(M: int, N: int, K: int, reps: int = 20, warmup: int = 3, mode: int = C.ORCA_LINEAR_STORE):
@@ -184,6 +198,7 @@ def main():
     p.add_argument("--warmup", type=int, default=3)
     sub.add_parser("sweep")
     sub.add_parser("linear-graph")
+    sub.add_parser("linears-13b-mixed")
     pa = sub.add_parser("attention")
     pa.add_argument("--case", choices=sorted(ATTN_CASES), required=True)
     pa.add_argument("--reps", type=int, default=5)
@@ -197,6 +212,12 @@ def main():
         print(json.dumps(r))
     elif a.cmd == "linear":
         print(json.dumps(time_linear(a.M, a.N, a.K, a.reps, a.warmup)))
+    elif a.cmd == "linears-13b-mixed":
+        for name, M, N, K, mode in LINEARS_13B_MIXED:
+            r = time_linear(M, N, K, reps=1, warmup=1, mode=mode)
+            r["name"] = name
+            print(json.dumps(r), flush=True)
+            torch.cuda.empty_cache()
     elif a.cmd == "linear-graph":
         # GPT-2-small's Linears (QKV, Attn-Out, FC1, FC2, LM head) at decode and prefill row counts
         for M in (8, 64, 128, 256):
