@@ -781,6 +781,281 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Large-M products: one 256 x 256 output tile per CTA pair (tcgen05 with
+// cta_group::2).  The two CTAs of a cluster of 2 share one MMA of M = 256,
+// N = 256: each holds 128 rows of the A tile and 128 rows (output columns) of
+// the W tile in its own shared memory, at the same offsets, and 128 rows x
+// 256 columns of the accumulator in its own tensor memory.  Per k-block an SM
+// then takes in 32 KB (A and W halves) for the same 128 x 256 x 64 MMA work
+// that costs a single CTA 48 KB; with the operand stream the bound of the
+// single-CTA kernel at large M (about 70% tensor-pipe activity, the ring's
+// bytes in flight over the L2 latency), this is what feeds the tensor core.
+// Roles, in both CTAs unless stated:
+//   warp 0      one lane loads its CTA's A and W halves of each stage; the
+//               copies complete on the leader CTA's (rank 0) full barrier,
+//               whose expected bytes the leader sets for both;
+//   warp 1      allocates 512 TMEM columns (cta_group::2, both CTAs); in the
+//               leader one lane issues the MMAs and commits each stage's
+//               release and each finished accumulator to both CTAs' barriers
+//               (multicast);
+//   warps 2..5  read their CTA's accumulator rows and run the epilogue, then
+//               tell the leader that the accumulator is free (its tempty
+//               barrier counts the 8 epilogue warps of the pair).
+// Two cluster barriers: barriers initialised before any copy or arrive
+// crosses CTAs; every MMA and epilogue done before either CTA frees its
+// tensor memory or leaves.  Every other wait is bounded.
+constexpr int kPairBN = 256;                             // output columns of a pair tile
+constexpr int kPairBM = 2 * BM;                          // output rows of a pair tile
+constexpr int kPairHalf = BM * BK * 2;                   // one operand half of a stage: 16 KB
+constexpr int kPairStage = 2 * kPairHalf;                // A half + W half
+constexpr int kPairStages = 7;
+constexpr int kPairSmem = kPairStages * kPairStage + 1024 + 256;
+constexpr int kPairGroupM = 4;                           // pair tiles per row group (1024 rows)
+// kind::f16, D fp32, A/B bf16 K-major, N = 256, M = 256 (the pair's rows)
+constexpr uint32_t kPairIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPairBN >> 3) << 17) |
+                                ((uint32_t)(kPairBM >> 4) << 24);
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+// Arrive on `bar` (same offset) in both CTAs of the pair once the MMAs issued
+// so far are complete.
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+// 3-D tiled load into this CTA's shared memory, completing on a barrier that
+// may be in the peer CTA (bar: shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *tm, int x, int y, int z,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait for a barrier that the peer CTA also arrives on (cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                  int32_t *status) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait_cluster(addr, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait_cluster(addr, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > 2000000000ull) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusWaitTimeout);
+      return false;
+    }
+  }
+}
+
+// Pair tiles in groups of kPairGroupM row tiles, so the pairs running at the
+// same time share their W tiles in L2.
+struct PairSched {
+  int nM, nN, KB, units;
+  __host__ __device__ void init(int M, int N, int K) {
+    nM = (M + kPairBM - 1) / kPairBM;
+    nN = (N + kPairBN - 1) / kPairBN;
+    KB = K / BK;
+    units = nM * nN;
+  }
+  __device__ __forceinline__ void unit(int u, int &m, int &n) const {
+    const int group = u / (kPairGroupM * nN);
+    const int first_m = group * kPairGroupM;
+    const int gm = min(kPairGroupM, nM - first_m);
+    const int r = u - group * kPairGroupM * nN;
+    m = first_m + r % gm;
+    n = r / gm;
+  }
+};
+
+// grid = 2 x pairs, clusters of 2; tmA / tmW: 3-D views with boxes of 128
+// rows x 1 k-block.
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, int M_arg,
+                        const int32_t *M_dev, int N, int K, EpiParams epi, int32_t *status) {
+  constexpr int ST = kPairStages;
+  extern __shared__ uint8_t smem_raw[];
+  // the same offsets in both CTAs (same kernel, same static shared memory)
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t *sA = smem_raw + pad;
+  uint8_t *sB = sA + ST * kPairHalf;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sB + ST * kPairHalf);
+  uint64_t *empty = full + ST;
+  uint64_t *tfull = empty + ST;
+  uint64_t *tempty = tfull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = M_dev != nullptr ? *M_dev : M_arg;  // M_dev: the descriptor header, written before the forward
+  const uint32_t rank = cluster_rank();             // 0: leader (issues the MMAs), 1: peer
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  PairSched sc;
+  sc.init(M, N, K);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], 8);
+    mbar_init(&tempty[1], 8);
+    *abort_flag = 0;
+    mbar_fence_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, 2 * kPairBN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();  // only once this CTA holds its tensor memory (as in the persistent kernel)
+  // both CTAs' barriers are initialised before any copy or arrive crosses over
+  cluster_arrive_release();
+  cluster_wait_acquire();
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer (both CTAs): this CTA's halves, on the leader's full barriers
+      const uint32_t full0 = map_to_rank(smem_u32(full), 0);
+      const int row_half = (int)rank * BM, col_half = (int)rank * BM;
+      int pre = 0;
+      if (pair < sc.units) {  // weights first: they do not depend on earlier kernels
+        int m, n;
+        sc.unit(pair, m, n);
+        pre = min(ST, sc.KB);
+        for (int j = 0; j < pre; ++j) {
+          if (rank == 0) mbar_expect_tx(&full[j], 2u * kPairStage);
+          tma_load_3d_pair(sB + j * kPairHalf, &tmW, 0, n * kPairBN + col_half, j, full0 + 8u * j);
+        }
+      }
+      pdl_wait();  // A (activations) comes from earlier kernels
+      int it = 0, s = 0;
+      uint32_t ph = 0;
+      for (int u = pair; u < sc.units; u += npairs) {
+        int m, n;
+        sc.unit(u, m, n);
+        for (int kb = 0; kb < sc.KB; ++kb, ++it, s = s + 1 == ST ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
+          const uint32_t bar = full0 + 8u * (uint32_t)s;
+          if (it < pre) {  // W already requested
+            tma_load_3d_pair(sA + s * kPairHalf, &tmA, 0, m * kPairBM + row_half, kb, bar);
+            continue;
+          }
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status) || *abort_flag) continue;
+          if (rank == 0) mbar_expect_tx(&full[s], 2u * kPairStage);
+          tma_load_3d_pair(sA + s * kPairHalf, &tmA, 0, m * kPairBM + row_half, kb, bar);
+          tma_load_3d_pair(sB + s * kPairHalf, &tmW, 0, n * kPairBN + col_half, kb, bar);
+        }
+      }
+      if (*abort_flag) drain_after_abort();  // copies issued before the abort land first
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {  // MMA issuer (leader)
+      int i = 0, s = 0;
+      uint32_t ph = 0;
+      for (int u = pair; u < sc.units; u += npairs, ++i) {
+        const int acc = i & 1;
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * kPairBN);
+        mbar_wait_cluster(&tempty[acc], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, status);
+        tc_fence_after();
+        for (int kb = 0; kb < sc.KB; ++kb, s = s + 1 == ST ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
+          if (mbar_wait(&full[s], ph, abort_flag, status)) {
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + s * kPairHalf);
+            const uint32_t b0 = smem_u32(sB + s * kPairHalf);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              tc_mma_pair(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), kPairIdesc,
+                          (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit_pair(&empty[s]);
+        }
+        tc_commit_pair(&tfull[acc]);
+      }
+    }
+  } else {  // epilogue warps 2..5 (both CTAs): TMEM lane quarter = warp % 4
+    const int q = warp & 3;
+    const uint32_t tempty0 = map_to_rank(smem_u32(tempty), 0);
+    int i = 0;
+    for (int u = pair; u < sc.units; u += npairs, ++i) {
+      int m, n;
+      sc.unit(u, m, n);
+      const int acc = i & 1;
+      float bl_next = n * kPairBN < N ? run_bias(epi, n * kPairBN, min(32, N - n * kPairBN)) : 0.f;
+      if (i == 0) pdl_wait();  // the epilogue reads / writes buffers of earlier kernels (x, K/V slots)
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], (uint32_t)(i >> 1) & 1u, abort_flag, status));
+      tc_fence_after();
+      const int row = m * kPairBM + (int)rank * BM + q * 32 + lane;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPairBN);
+      unsigned long long best = 0ull;
+#pragma unroll 1
+      for (int c = 0; c < kPairBN; c += 32) {
+        float v[32];
+        if (ok) tmem_ld32(tbase + (uint32_t)c, v);
+        if (c + 32 == kPairBN) {  // the accumulator is read: free it for the leader's next tile
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
+        }
+        const int col = n * kPairBN + c;
+        const float bl = bl_next;
+        if (c + 32 < kPairBN && col + 32 < N) bl_next = run_bias(epi, col + 32, min(32, N - col - 32));
+        if (ok && col < N) finish_run(epi, row, col, v, min(32, N - col), row < M, best, bl);
+      }
+      if (epi.argmax_keys != nullptr && best != 0ull) atomicMax(epi.argmax_keys + row, best);
+    }
+  }
+  // every MMA of the pair is complete (each epilogue saw its last commit) and
+  // every epilogue is done before either CTA frees its tensor memory or leaves
+  tc_fence_before();
+  __syncthreads();
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 2 * kPairBN);
+  }
+}
+
 template <int BN, int KS>
 cudaError_t set_smem_limit(int dev) {
   static uint64_t attr_mask = 0;  // one bit per device ordinal
@@ -846,6 +1121,43 @@ cudaError_t launch_bn(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, con
                     sm, a_box, epi, scr, status);
 }
 
+cudaError_t set_pair_smem_limit(int dev) {
+  static uint64_t attr_mask = 0;
+  if (dev >= 64 || !(attr_mask & (1ull << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_mask |= 1ull << dev;
+  }
+  return cudaSuccess;
+}
+
+// Persistent pairs: at most one pair per two SMs (with M_dev the grid is
+// fixed, the device decides how many units there are).
+cudaError_t launch_pair(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, const int32_t *M_dev, int N, int K,
+                        const EpiParams &epi, int32_t *status, cudaStream_t st, int sm, int dev) {
+  cudaError_t e = set_pair_smem_limit(dev);
+  if (e != cudaSuccess) return e;
+  PairSched sc;
+  sc.init(M, N, K);
+  const int pairs = M_dev != nullptr ? sm / 2 : (sc.units < sm / 2 ? sc.units : sm / 2);
+  if (pairs <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, *tmA, *tmW, M, M_dev, N, K, epi, status);
+}
+
 }  // namespace
 
 int gemm_sm_count() {
@@ -909,8 +1221,15 @@ double load_us(double bytes) { return 0.45 + bytes / 115e3; }
 // K = 768 the persistent kernel was faster for every N of GPT-2 small, with
 // K = 3072 the cluster kernel by 30-40%.)
 constexpr int kClusterMinKb = 32;
+// Products of at least this many rows take the CTA-pair kernel.
+constexpr int kPairMinRows = 512;
 GemmPlan gemm_plan(int M, int N, int K) {
   GemmPlan p{};
+  if (M >= kPairMinRows) {
+    p.pair = true;
+    p.bn = kPairBN;
+    return p;
+  }
   p.bn = gemm_tile_n(M, N);
   p.ks = gemm_ks(p.bn, K);
   const int KB = K / BK;
@@ -946,9 +1265,11 @@ GemmPlan gemm_plan(int M, int N, int K) {
 }
 
 // A small integer naming the plan, below 64: callers pack one per Linear
-// into 6 bits of their CUDA-graph keys (persistent 0..7, cluster 8..39).
+// into 6 bits of their CUDA-graph keys (persistent 0..7, cluster 8..39,
+// CTA pair 40).
 int gemm_plan_code(int M, int N, int K) {
   const GemmPlan p = gemm_plan(M, N, K);
+  if (p.pair) return 40;
   if (!p.cluster) return bn_code(p.bn) * 2 + (p.a_box == 64 ? 1 : 0);
   return 8 + bn_code(p.bn) * 8 + (p.S == 2 ? 0 : p.S == 4 ? 1 : 2) * 2 + (p.a_box == 64 ? 1 : 0);
 }
@@ -969,6 +1290,7 @@ cudaError_t gemm_prepare() {
   if (e == cudaSuccess) e = set_cluster_smem_limit<64>(dev);
   if (e == cudaSuccess) e = set_cluster_smem_limit<128>(dev);
   if (e == cudaSuccess) e = set_cluster_smem_limit<256>(dev);
+  if (e == cudaSuccess) e = set_pair_smem_limit(dev);
   gemm_sm_count();
   return e;
 }
@@ -987,6 +1309,7 @@ cudaError_t launch_gemm_tc_bf16(const OperandMaps &A, const OperandMaps &W, int 
   if (e != cudaSuccess) return e;
   const int sm = gemm_sm_count();
   const GemmPlan p = gemm_plan(M, N, K);
+  if (p.pair) return launch_pair(A.get(BM, 1), W.get(BM, 1), M, M_dev, N, K, epi, status, st, sm, dev);
   if (p.cluster) {
     switch (p.bn) {
       case 256: return launch_cluster<256>(A, W, M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);

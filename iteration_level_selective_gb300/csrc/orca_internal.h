@@ -238,6 +238,7 @@ struct OperandMaps {
 // split-K kernel with S CTAs per output tile, kbs k-blocks each, A boxes of
 // a_box rows); gemm_plan_code is a small integer unique per plan.
 struct GemmPlan {
+  bool pair = false;  // CTA-pair kernel (256 x 256 tiles, cta_group::2)
   bool cluster = false;
   int bn = 128, S = 1, kbs = 0, a_box = 128, ks = 1;
 };

@@ -34,7 +34,7 @@ _TIME = {"ns": 1e-6, "nsecond": 1e-6, "us": 1e-3, "usecond": 1e-3, "ms": 1.0, "m
 _BYTES = {"byte": 1.0, "b": 1.0, "kbyte": 1e3, "kb": 1e3, "mbyte": 1e6, "mb": 1e6, "gbyte": 1e9, "gb": 1e9}
 
 CLASSES = {
-    "gemm_tc_bf16": ("gemm_tc_bf16_kernel", "gemm_tc_cluster_kernel"),
+    "gemm_tc_bf16": ("gemm_tc_bf16_kernel", "gemm_tc_cluster_kernel", "gemm_tc_pair_kernel"),
     "attention": ("attention_kernel", "prefill_attention_tc_kernel"),
     "layernorm": ("layernorm_kernel",),
     "embed": ("embed_kernel",),
@@ -81,8 +81,9 @@ def source_hash(csrc: str = CSRC) -> str:
 
 
 def short_name(full: str) -> str:
-    """'void orca::(anonymous namespace)::gemm_tc_bf16_kernel<128>(...)' -> 'gemm_tc_bf16_kernel'."""
-    head = re.split(r"[<(]", full.replace("(anonymous namespace)", ""), maxsplit=1)[0]
+    """'void orca::(anonymous namespace)::gemm_tc_bf16_kernel<128>(...)' -> 'gemm_tc_bf16_kernel'
+    (ncu also prints the anonymous namespace as '<unnamed>')."""
+    head = re.split(r"[<(]", full.replace("(anonymous namespace)", "").replace("<unnamed>", ""), maxsplit=1)[0]
     return head.split("::")[-1].split()[-1]
 
 

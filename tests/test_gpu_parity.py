@@ -62,7 +62,12 @@ def test_argmax_forced_logits_bit_exact(cuda):
                                    (37, 300, 2048), (100, 768, 3072), (1, 1000, 4096), (128, 520, 2112),
                                    # few narrow tiles with a 1 MB weight block each: split-K over the
                                    # persistent kernel when a scratch buffer is given
-                                   (200, 520, 16384)])
+                                   (200, 520, 16384),
+                                   # CTA-pair kernel (>= 512 rows, 256 x 256 tiles over two SMs): ragged
+                                   # last pair tile (one row in the leader, none in the peer), a single
+                                   # k-block, vocab-wide ragged N, a long K, wide N and K
+                                   (513, 1000, 512), (1024, 256, 64), (777, 50257, 1024), (4100, 520, 20480),
+                                   (1500, 4096, 5120)])
 @pytest.mark.parametrize("mode", ["store", "gelu", "resid", "f32out"])
 @pytest.mark.parametrize("split", [False, True])
 def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode, split):

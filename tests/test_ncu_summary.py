@@ -61,3 +61,14 @@ def test_source_hash_ignores_comments_and_layout(tmp_path):
     (b / "k.cu").write_text('__global__ void k() { asm("mov.u32 %0, 2; // in a string"); }\n')
     assert ns.source_hash(str(a)) != ns.source_hash(str(b))
     assert ns.code_only('x = "/*"; /* c */ y = \'"\'; // d\nz') == 'x = "/*"; y = \'"\'; z'
+
+
+def test_short_name_of_the_names_ncu_prints():
+    assert ns.short_name("void orca::(anonymous namespace)::gemm_tc_bf16_kernel<128>(CUtensorMap, int)") == \
+        "gemm_tc_bf16_kernel"
+    assert ns.short_name("void orca::<unnamed>::gemm_tc_bf16_kernel<256, 1>(CUtensorMap_st, int)") == \
+        "gemm_tc_bf16_kernel"
+    assert ns.short_name("orca::<unnamed>::ln_fold_vectors_kernel(const __nv_bfloat16 *, int)") == \
+        "ln_fold_vectors_kernel"
+    assert ns.short_name("void orca::<unnamed>::gemm_tc_pair_kernel(CUtensorMap_st, CUtensorMap_st, int)") == \
+        "gemm_tc_pair_kernel"
