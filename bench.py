@@ -459,7 +459,7 @@ def build_fixed(config, dev, stream):
              "n_rows": n_rows, "n_slots": n_slots, "kv_pool_gb": round(eng.kv_bytes / 1e9, 1),
              "weights_gb": round(weights.nbytes / 1e9, 1),
              "l2": "inputs larger than L2 (weights and K/V many times L2), no flush"}
-    return shape, weights, eng, (lambda warm=False: work), workload, extra
+    return shape, weights, eng, (lambda warm=False, gen=1: work), workload, extra
 
 
 def measure(C, eng, stream, dev, make_work, steps, warmup, is_trace, world, local):
@@ -480,7 +480,7 @@ def measure(C, eng, stream, dev, make_work, steps, warmup, is_trace, world, loca
         dist.barrier()
     sampler = ClockSampler(local)
     recs, evs, step_ms, usage, xfer = [], [], [], [], []
-    runs = [make_work() for _ in range(steps)] if is_trace else [work]
+    runs = [make_work(gen=i + 1) for i in range(steps)] if is_trace else [work]
     torch.cuda.synchronize(dev)
     w0 = time.perf_counter()
     ev0 = torch.cuda.Event(enable_timing=True)
@@ -549,13 +549,17 @@ def run_config(args, config, rank, world, local, dev, stream):
         del host_w
         eng = rt.Engine(shape, weights, max_bs=max_bs, n_slots=n_slots, max_rows=max_rows, device=dev,
                         reserve_policy=rt.RESERVE_POLICIES[args.reserve])
-        gen = [0]
+        n_warm = [0]
 
-        def make_work(warm=False):
-            gen[0] += 1
-            trace = trace_fn(rank, gen[0])
-            if warm:   # a short warm-up trace: the first 32 requests at once, at most 8 tokens each
-                trace = [synth.Request(r.req_id, 0, r.prompt, min(r.out_len, 8), r.max_tokens) for r in trace[:32]]
+        def make_work(warm=False, gen=1):
+            """Timed trace number `gen` (1, 2, ...), or a short warm-up trace:
+            the first 32 requests of another stream, at once, at most 8 tokens each."""
+            if warm:
+                n_warm[0] += 1
+                trace = [synth.Request(r.req_id, 0, r.prompt, min(r.out_len, 8), r.max_tokens)
+                         for r in trace_fn(rank, 10_000 + n_warm[0])[:32]]
+            else:
+                trace = trace_fn(rank, gen)
             return TraceWorkload(eng, trace, stream, args.token_budget or None, args.chunk or None, args.workers)
         extra = {"model": f"{'gpt2-small' if shape is synth.GPT2_SMALL else '13B'}-shaped, random init N(0, 0.02)",
                  "max_bs": max_bs, "n_slots": n_slots, "kv_pool_gb": round(eng.kv_bytes / 1e9, 1),
@@ -585,24 +589,29 @@ def run_config(args, config, rank, world, local, dev, stream):
     (dev_s, wall), (rows, gen_tok, done, h2d, d2h, launches, n_it_all) = replicas.reduce_timing(
         [m["dev_s"], m["wall"]], [rows, gen_tok, done, h2d, d2h, launches, n_it], device=dev)
 
-    # profiled pass: per-launch CUDA events around every kernel, same iterations
-    C.orca_profile_enable(eng.handle, True)
-    t_prof = time.perf_counter()
-    if is_trace:
-        pw = make_work()
-        n_prof = 0
-        while not pw.done() and n_prof < n_it:
-            pw.step()
-            n_prof += 1
-    else:
-        pw = m["work"]
-        for _ in range(n_it):
-            pw.step()
-        n_prof = n_it
-    torch.cuda.synchronize(dev)
-    t_prof = time.perf_counter() - t_prof
-    agg = kernel_classes(C, eng)
-    C.orca_profile_enable(eng.handle, False)
+    def kernel_pass(mode):
+        """The timed iterations again (the first timed trace, whole), with
+        per-kernel-class timing: mode 2 = launch stamps in the graph-replayed
+        forward, mode 1 = CUDA events around eagerly launched kernels."""
+        C.orca_profile_enable(eng.handle, mode)
+        t = time.perf_counter()
+        if is_trace:
+            pw, n = make_work(gen=1), 0
+            while not pw.done():
+                pw.step()
+                n += 1
+        else:
+            pw, n = m["work"], n_it
+            for _ in range(n_it):
+                pw.step()
+        torch.cuda.synchronize(dev)
+        t = time.perf_counter() - t
+        agg = kernel_classes(C, eng)
+        C.orca_profile_enable(eng.handle, 0)
+        return agg, n, t
+
+    agg, n_prof, t_prof = kernel_pass(2)
+    agg_ev, n_ev, t_ev = kernel_pass(1)
     peaks, peak_src = load_peaks()
     total_ms = sum(a["ms"] for a in agg.values()) or 1.0
     dom = max(agg, key=lambda k: agg[k]["ms"])
@@ -628,9 +637,19 @@ def run_config(args, config, rank, world, local, dev, stream):
         "kernel_roofline": per_kernel_roofline(agg, peaks),
         "kernel_time_share": {k: round(v["ms"] / total_ms, 4) for k, v in agg.items()},
         "kernel_ms_per_step": {k: round(v["ms"] / max(1, n_prof), 4) for k, v in agg.items()},
-        "profiled_pass": {"iterations": n_prof, "ms_per_step_wall": round(1000 * t_prof / max(1, n_prof), 4),
-                          "how": "the same iterations again, launched eagerly with a CUDA event pair around every "
-                                 "kernel on the iteration stream"},
+        "kernel_timing": {
+            "how": "the timed iterations again on the same path (graph replay); every kernel raises a %globaltimer "
+                   "end stamp, a launch's share is its end minus the previous launch's end, so the classes add up "
+                   "to each iteration's device time",
+            "iterations": n_prof, "ms_per_step_wall": round(1000 * t_prof / max(1, n_prof), 4),
+            "kernel_ms_sum_per_step": round(total_ms / max(1, n_prof), 4)},
+        "event_pass": {
+            "how": "the same iterations launched eagerly with a CUDA event pair around every kernel on the "
+                   "iteration stream (no graph, no overlap between kernels)",
+            "iterations": n_ev, "ms_per_step_wall": round(1000 * t_ev / max(1, n_ev), 4),
+            "kernel_ms_per_step": {k: round(v["ms"] / max(1, n_ev), 4) for k, v in agg_ev.items()},
+            "roofline_frac": {k: v.get("frac_tensor", v.get("frac_hbm")) for k, v in
+                              per_kernel_roofline(agg_ev, load_peaks()[0]).items()}},
         "kv_usage": {"reserved_frac": round(float(np.mean([u[0] for u in usage])) / eng.cfg.n_slots, 5),
                      "stored_frac": round(float(np.mean([u[1] for u in usage])) / eng.cfg.n_slots, 5),
                      "stored_over_reserved": round(float(np.sum([u[1] for u in usage]) /
@@ -651,7 +670,7 @@ def run_config(args, config, rank, world, local, dev, stream):
     return line
 
 
-SUB_KEYS = ("value", "unit", "steps", "ms_per_step", "config", "roofline", "attention_roofline",
+SUB_KEYS = ("value", "unit", "steps", "ms_per_step", "config", "roofline", "attention_roofline", "kernel_timing",
             "iteration_roofline", "kernel_roofline", "kernel_ms_per_step", "gpu_launches", "e2e", "clocks",
             "steady_state", "overall", "completed_requests_per_s", "generated_tokens_per_s")
 

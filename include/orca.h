@@ -402,8 +402,18 @@ int orca_attention_noalloc(int32_t dtype, int32_t n_heads, int32_t head_dim, int
                            int32_t *status_dev, void *stream);
 
 /* ---------------------------------------------------------------- profiling */
-/* enable != 0: time every launch of every kernel class with CUDA events on
- * the iteration stream (adds event overhead); 0 disables.  Resets stats. */
+/* Per-kernel-class timing of the iterations that follow; resets the
+ * statistics orca_profile_read returns.  No iteration may be in flight.
+ *   0: off.
+ *   1: CUDA events around every launch; the forward then runs eagerly (no
+ *      CUDA graph) and waits for each kernel before the next starts.
+ *   2 (bf16 models): launch stamps on the path that runs anyway - every
+ *      kernel of the (graph-replayed) forward raises its end time
+ *      (%globaltimer) in device memory, and the stamps come back with the
+ *      tokens.  A launch's share is its end minus the previous launch's end
+ *      (the two attention launches of a layer count as one), so the shares
+ *      of an iteration add up to its time on the device.
+ * Each launch adds its algorithmic FLOPs and bytes to its class. */
 int orca_profile_enable(orca_engine *eng, int32_t enable);
 int orca_profile_read(const orca_engine *eng, int32_t kernel_class, orca_kernel_stats *out);
 

@@ -544,6 +544,8 @@ __global__ void __launch_bounds__(kThreads, (attn_min_ctas<T, D>())) attention_k
       a.ticket[1] = 0;
     }
   }
+  __syncthreads();
+  stamp_end(a.stamp);
 }
 
 // CTAs that fit on the GPU at once (one wave) for this instantiation; the

@@ -563,6 +563,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (*abort_flag) drain_after_abort();
   }
   __syncthreads();
+  stamp_end(a.stamp);
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");

@@ -102,10 +102,16 @@ template <typename T>
 __global__ void embed_kernel(const RowInfo *__restrict__ rows, int n_rows_arg, const int32_t *n_rows_dev,
                              const T *__restrict__ tok_emb, const T *__restrict__ pos_emb, float *__restrict__ x,
                              int H, int vocab, int max_pos, int32_t *status, const float *__restrict__ ln_g,
-                             const float *__restrict__ ln_b, T *__restrict__ ln_out) {
+                             const float *__restrict__ ln_b, T *__restrict__ ln_out,
+                             unsigned long long *stamp_start, unsigned long long *stamp) {
   pdl_trigger();
   const int n_rows = n_rows_dev ? *n_rows_dev : n_rows_arg;
   pdl_wait();
+  if (stamp_start != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    *stamp_start = t;
+  }
   for (int r = blockIdx.x; r < n_rows; r += gridDim.x) {
     const RowInfo ri = rows[r];
     if (ri.tok < 0 || ri.tok >= vocab || ri.pos < 0 || ri.pos >= max_pos) {
@@ -124,6 +130,8 @@ __global__ void embed_kernel(const RowInfo *__restrict__ rows, int n_rows_arg, c
       if (threadIdx.x < 32) layernorm_row<T, 0>(x, ln_g, ln_b, ln_out, r, r, H, threadIdx.x);
     }
   }
+  __syncthreads();
+  stamp_end(stamp);
 }
 
 // out[i] = LayerNorm(x[src_i]), one warp per output row, rows grid-strided;
@@ -133,7 +141,7 @@ template <typename T, int NV4>
 __global__ void layernorm_kernel(const float *__restrict__ x, const float *__restrict__ g,
                                  const float *__restrict__ b, T *__restrict__ out, int n_rows_arg,
                                  const int32_t *n_rows_dev, int H, const ReqInfo *__restrict__ gather,
-                                 unsigned long long *zero_keys) {
+                                 unsigned long long *zero_keys, unsigned long long *stamp) {
   pdl_trigger();
   const int n_rows = n_rows_dev ? *n_rows_dev : n_rows_arg;
   const int lane = threadIdx.x & 31;
@@ -143,6 +151,8 @@ __global__ void layernorm_kernel(const float *__restrict__ x, const float *__res
     layernorm_row<T, NV4>(x, g, b, out, row, gather ? gather[row].row_off + gather[row].n_new - 1 : row, H, lane);
     if (zero_keys != nullptr && lane == 0) zero_keys[row] = 0ull;
   }
+  __syncthreads();
+  stamp_end(stamp);
 }
 
 // (value, index) order of the greedy choice: larger value wins, equal values
@@ -222,7 +232,8 @@ __global__ void ln_fold_vectors_kernel(const __nv_bfloat16 *__restrict__ W, cons
 
 cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows, const int32_t *n_rows_dev, const void *tok_emb,
                          const void *pos_emb, float *x, int H, int vocab, int max_pos, int32_t *status,
-                         const float *ln_g, const float *ln_b, void *ln_out, cudaStream_t st) {
+                         const float *ln_g, const float *ln_b, void *ln_out, unsigned long long *stamp_start,
+                         unsigned long long *stamp, cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
   const int threads = H >= 512 ? 128 : 32;
   const int grid = n_rows < 1184 ? n_rows : 1184;
@@ -230,10 +241,10 @@ cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows, const int32
   if (dtype == 1)
     return launch_pdl(embed_kernel<__nv_bfloat16>, grid, threads, 0, st, rows, n_rows, n_rows_dev,
                       static_cast<const __nv_bfloat16 *>(tok_emb), static_cast<const __nv_bfloat16 *>(pos_emb), x, H,
-                      vocab, max_pos, status, ln_g, ln_b, static_cast<__nv_bfloat16 *>(ln_out));
+                      vocab, max_pos, status, ln_g, ln_b, static_cast<__nv_bfloat16 *>(ln_out), stamp_start, stamp);
   return launch_pdl(embed_kernel<float>, grid, threads, 0, st, rows, n_rows, n_rows_dev,
                     static_cast<const float *>(tok_emb), static_cast<const float *>(pos_emb), x, H, vocab, max_pos,
-                    status, ln_g, ln_b, static_cast<float *>(ln_out));
+                    status, ln_g, ln_b, static_cast<float *>(ln_out), stamp_start, stamp);
 }
 
 cudaError_t launch_ln_fold_vectors(const void *W, const float *gamma, const float *beta, const float *bias, int N,
@@ -248,26 +259,31 @@ cudaError_t launch_ln_fold_vectors(const void *W, const float *gamma, const floa
 template <typename T>
 static cudaError_t layernorm_t(const float *x, const float *g, const float *b, T *out, int n_rows,
                                const int32_t *n_rows_dev, int H, const ReqInfo *gather, unsigned long long *zk,
-                               cudaStream_t st) {
+                               unsigned long long *stamp, cudaStream_t st) {
   const int rows_per_cta = 8;
   int grid = (n_rows + rows_per_cta - 1) / rows_per_cta;
   if (grid > 1184) grid = 1184;
   const dim3 block(32 * rows_per_cta);
   switch (H) {
-    case 768: return launch_pdl(layernorm_kernel<T, 6>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk);
-    case 1024: return launch_pdl(layernorm_kernel<T, 8>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk);
-    case 2048: return launch_pdl(layernorm_kernel<T, 16>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk);
-    default: return launch_pdl(layernorm_kernel<T, 0>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk);
+    case 768: return launch_pdl(layernorm_kernel<T, 6>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk,
+                                  stamp);
+    case 1024: return launch_pdl(layernorm_kernel<T, 8>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk,
+                                  stamp);
+    case 2048: return launch_pdl(layernorm_kernel<T, 16>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk,
+                                  stamp);
+    default: return launch_pdl(layernorm_kernel<T, 0>, grid, block, 0, st, x, g, b, out, n_rows, n_rows_dev, H, gather, zk,
+                                  stamp);
   }
 }
 
 cudaError_t launch_layernorm(int dtype, const float *x, const float *g, const float *b, void *out, int n_rows,
                              const int32_t *n_rows_dev, int H, const ReqInfo *gather, unsigned long long *zero_keys,
-                             cudaStream_t st) {
+                             unsigned long long *stamp, cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
   if (dtype == 1)
-    return layernorm_t(x, g, b, static_cast<__nv_bfloat16 *>(out), n_rows, n_rows_dev, H, gather, zero_keys, st);
-  return layernorm_t(x, g, b, static_cast<float *>(out), n_rows, n_rows_dev, H, gather, zero_keys, st);
+    return layernorm_t(x, g, b, static_cast<__nv_bfloat16 *>(out), n_rows, n_rows_dev, H, gather, zero_keys, stamp,
+                       st);
+  return layernorm_t(x, g, b, static_cast<float *>(out), n_rows, n_rows_dev, H, gather, zero_keys, stamp, st);
 }
 
 cudaError_t launch_argmax(const float *logits, int n_rows, int vocab, int32_t *out, unsigned long long *keys,

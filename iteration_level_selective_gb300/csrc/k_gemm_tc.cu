@@ -502,6 +502,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
+  stamp_end(epi.stamp);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -775,6 +776,7 @@ __global__ void __launch_bounds__(192, 1)
   cluster_wait_acquire();
   tc_fence_before();
   __syncthreads();
+  stamp_end(epi.stamp);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -811,7 +813,7 @@ constexpr int kPairHalf = BM * BK * 2;                   // one operand half of 
 constexpr int kPairStage = 2 * kPairHalf;                // A half + W half
 constexpr int kPairStages = 7;
 constexpr int kPairSmem = kPairStages * kPairStage + 1024 + 256;
-constexpr int kPairGroupM = 4;                           // pair tiles per row group (1024 rows)
+constexpr int kPairGroupM = 16;  // pair tiles per row group (4096 rows; measured best of 4, 8, 16)
 // kind::f16, D fp32, A/B bf16 K-major, N = 256, M = 256 (the pair's rows)
 constexpr uint32_t kPairIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPairBN >> 3) << 17) |
                                 ((uint32_t)(kPairBM >> 4) << 24);
@@ -1050,6 +1052,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   cluster_arrive_release();
   cluster_wait_acquire();
+  stamp_end(epi.stamp);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, 2 * kPairBN);
@@ -1221,11 +1224,20 @@ double load_us(double bytes) { return 0.45 + bytes / 115e3; }
 // K = 768 the persistent kernel was faster for every N of GPT-2 small, with
 // K = 3072 the cluster kernel by 30-40%.)
 constexpr int kClusterMinKb = 32;
-// Products of at least this many rows take the CTA-pair kernel.
+// The CTA-pair kernel takes products of at least 512 rows whose 256 x 256
+// tiles give every pair of SMs one at least, and products of 129..511 rows
+// with at least 48 pair tiles across N (N >= 12288: the 13B QKV, FC1 and LM
+// head).  Measured on GB300 against the single-CTA kernel: at 200-256 rows
+// the pair kernel is 20-25% faster for N = 15360 and 20480 and slower for
+// N = 5120 (20 pair tiles leave most pairs idle); GPT-2-small's prompt
+// iterations (600 rows, N <= 3072) lost 4% on it.
 constexpr int kPairMinRows = 512;
+constexpr int kPairMinRowsWide = 129;
+constexpr int kPairWideN = 12288;
 GemmPlan gemm_plan(int M, int N, int K) {
   GemmPlan p{};
-  if (M >= kPairMinRows) {
+  const long long pair_tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
+  if ((M >= kPairMinRows && pair_tiles >= gemm_sm_count() / 2) || (M >= kPairMinRowsWide && N >= kPairWideN)) {
     p.pair = true;
     p.bn = kPairBN;
     return p;
@@ -1243,7 +1255,9 @@ GemmPlan gemm_plan(int M, int N, int K) {
     const int nN = (N + bn - 1) / bn;
     for (int S : {4, 8}) {
       const int kbs = (KB + S - 1) / S;
-      if (bn % (4 * S) != 0 || cluster_smem(bn, kbs, a_box) > kClusterSmemMax || nN * S > 16 * sm) continue;
+      // one wave at most: with more waves the per-wave estimate below no longer
+      // holds (measured: 64 x 15360 x 5120 took 4x its estimate)
+      if (bn % (4 * S) != 0 || cluster_smem(bn, kbs, a_box) > kClusterSmemMax || nN * S > sm) continue;
       const long long waves = ((long long)nN * S + sm - 1) / sm;
       const double t = (double)waves * (load_us((double)kbs * (a_box + bn) * 128.0) + kbs * 4 * mma_us(bn));
       if (t < best) {

@@ -196,6 +196,10 @@ int check_config(const orca_config *c, std::string *why) {
   return ORCA_OK;
 }
 
+// Launch stamps of one iteration: the start, then one end per launch (the
+// two attention launches of a layer share one).
+size_t stamp_capacity(const orca_config *c) { return 4 + 8 * (size_t)c->n_layers; }
+
 Layout make_layout(const orca_config *c) {
   Layout L{};
   const size_t e = elem_bytes(c->dtype);
@@ -211,7 +215,8 @@ Layout make_layout(const orca_config *c) {
   L.hf = take(B * H * e);
   L.logits = take(B * V * 4);
   for (int k = 0; k < kMaxInflight; ++k) {
-    L.out[k] = take((B + 1) * 8);  // [0] status word, [1..B] packed argmax keys
+    // [0] status word, [1..B] packed argmax keys, then the launch stamps
+    L.out[k] = take((B + 1 + stamp_capacity(c)) * 8);
     L.req[k] = take(sizeof(DevHeader) + B * sizeof(ReqInfo));  // header, then request records
     L.row[k] = take(R * sizeof(RowInfo));
     L.work[k] = take((size_t)L.max_work * sizeof(AttnWork));
@@ -339,6 +344,7 @@ struct orca_engine {
   std::vector<const void *> w;
   char *kv = nullptr;
   char *ws = nullptr;
+  struct Unit { int cls; double flops, bytes; };  // one launch (stamp slot) of the forward
   // one in-flight iteration: pinned host staging and what its wait needs
   struct IterSlot {
     DevHeader *h_hdr = nullptr;  // pinned: header followed by the request records
@@ -354,6 +360,7 @@ struct orca_engine {
     cudaStream_t st = nullptr;
     int32_t flags = 0, n_batch = 0;
     std::vector<int32_t> idx, L;
+    std::vector<Unit> units;  // stamps: the launches of this iteration, in stamp order
   };
   IterSlot slot[kMaxInflight];
   int q_head = 0, q_len = 0;  // submitted iterations, oldest first
@@ -371,8 +378,14 @@ struct orca_engine {
   int32_t n_launch = 0;               // kernels enqueued by the current eager forward
   int64_t last_h2d = 0, last_d2h = 0;
   std::vector<int32_t> last_row_off, last_row_pos, last_row_slot, last_last_row;
-  // profiling
+  // profiling: prof = CUDA-event pairs around eager launches; stamps = every
+  // launch of the (graph-replayed) forward raises its end stamp, read back
+  // with the tokens.  A dry enqueue (nothing launched) lists the launches'
+  // classes and algorithmic work in stamp order.
   bool prof = false;
+  bool stamps = false;
+  bool dry = false;
+  std::vector<Unit> dry_units;
   orca_kernel_stats stats[ORCA_K_COUNT]{};
   struct Pending { int slot, cls; cudaEvent_t a, b; double flops, bytes; };
   std::vector<cudaEvent_t> ev_all, ev_free;  // every event created; those not recorded for a pending launch
@@ -413,10 +426,10 @@ int fail(orca_engine *e, int code, const char *fmt, ...) {
   } while (0)
 
 // A kernel launch of the forward: checked, and counted for orca_last_launches.
-#define LAUNCH(eng, call)   \
-  do {                      \
-    CUDA_TRY(eng, call);    \
-    ++(eng)->n_launch;      \
+#define LAUNCH(eng, call)               \
+  do {                                  \
+    if (!(eng)->dry) CUDA_TRY(eng, call); \
+    ++(eng)->n_launch;                  \
   } while (0)
 
 template <typename T> T *ws_ptr(orca_engine *e, size_t off) { return reinterpret_cast<T *>(e->ws + off); }
@@ -499,11 +512,15 @@ cudaEvent_t prof_event(orca_engine *e) {
 }
 void prof_begin(orca_engine *e, cudaStream_t st, cudaEvent_t *a) {
   *a = nullptr;
-  if (!e->prof) return;
+  if (!e->prof || e->dry) return;
   *a = prof_event(e);
   if (*a) cudaEventRecord(*a, st);
 }
 void prof_end(orca_engine *e, cudaStream_t st, cudaEvent_t a, int cls, double flops, double bytes) {
+  if (e->dry) {
+    e->dry_units.push_back({cls, flops, bytes});
+    return;
+  }
   if (!e->prof || !a) return;
   cudaEvent_t b = prof_event(e);
   if (!b) {
@@ -589,12 +606,20 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
   LnStats *ln_a = ws_ptr<LnStats>(e, Ly.ln_a);  // LN2 of each layer
   LnStats *ln_b = ws_ptr<LnStats>(e, Ly.ln_b);  // LN1 of layers 1 ..
 
+  // launch stamps (stamps mode): [0] the start, then launch j's end at 1 + j
+  unsigned long long *stamps = e->stamps ? d_out + 1 + c.max_bs : nullptr;
+  int su = 0;  // launches (stamp slots) so far
+  auto stamp = [&]() { return stamps != nullptr ? stamps + 1 + su : nullptr; };
+  if (stamps != nullptr && !e->dry)
+    CUDA_TRY(e, cudaMemsetAsync(stamps, 0, stamp_capacity(&c) * sizeof(unsigned long long), st));
+
   cudaEvent_t ev;
   prof_begin(e, st, &ev);
   LAUNCH(e, launch_embed(c.dtype, d_row, N_grid, N_dev, e->w[W_TOK], e->w[W_POS], x, H, V, c.max_pos, status,
                          fold ? (const float *)lw(e, 0, L_LN1_G) : nullptr,
-                         fold ? (const float *)lw(e, 0, L_LN1_B) : nullptr, fold ? h : nullptr, st));
+                         fold ? (const float *)lw(e, 0, L_LN1_B) : nullptr, fold ? h : nullptr, stamps, stamp(), st));
   prof_end(e, st, ev, ORCA_K_EMBED, 0.0, (double)N * H * (2 * eb + 4 + (fold ? eb : 0)));
+  ++su;
 
   const size_t layer_kv = (size_t)2 * nh * c.n_slots * D * eb;
   const double attn_flops = 4.0 * D * z.attn_pairs * nh;
@@ -608,8 +633,9 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     if (!fold) {  // h = LN1(x)
       prof_begin(e, st, &ev);
       LAUNCH(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN1_G), (const float *)lw(e, l, L_LN1_B), h,
-                                   N_grid, N_dev, H, nullptr, nullptr, st));
+                                   N_grid, N_dev, H, nullptr, nullptr, stamp(), st));
       prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
+      ++su;
     }
     // QKV Linear; K/V scattered to the requests' slots (Split)
     EpiParams ep{};
@@ -630,6 +656,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     ep.head_dim = D;
     ep.n_slots = c.n_slots;
     ep.status = status;
+    ep.stamp = stamp();
     prof_begin(e, st, &ev);
     if (bf16)
       LAUNCH(e, launch_gemm_tc_bf16(fold_in ? e->tm_xb : e->tm_h, e->tm_layer[4 * l + 0], N, N_dev, 3 * H, H, ep,
@@ -637,6 +664,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WQKV), N, 3 * H, H, ep, st));
     prof_end(e, st, ev, ORCA_K_GEMM_QKV, 2.0 * N * 3 * H * H, gemm_bytes(N, 3.0 * H, H, eb));
+    ++su;
     // ragged attention -> h (rows in place: Merge)
     AttnArgs aa{};
     aa.q = q;
@@ -659,6 +687,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     aa.hdr = graph ? d_hdr : nullptr;
     aa.blocks = ws_ptr<int32_t>(e, Ly.blocks[k]);
+    aa.stamp = stamp();  // both attention launches of the layer: one stamp
     prof_begin(e, st, &ev);
     // With prompt rows on the tensor cores the two attention launches run side
     // by side: the prompt launch follows the QKV Linear as a dependent launch
@@ -667,7 +696,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     // no longer waits for the prompt launch to finish.  The streams join
     // before Attn-Out.
     const bool overlap = e->attn_tc && z.n_work_tc > 0;
-    if (overlap) {
+    if (overlap && !e->dry) {
       CUDA_TRY(e, cudaEventRecord(e->ev_fork, st));
       CUDA_TRY(e, cudaStreamWaitEvent(e->side_stream, e->ev_fork, 0));
     }
@@ -685,17 +714,20 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
       ta.blocks = aa.blocks;
       ta.n_slots = c.n_slots;
       ta.scale_log2 = aa.scale_log2;
-      CUDA_TRY(e, launch_attention_tc(D, &e->tm_q, &e->tm_k[l], &e->tm_v[l], &e->tm_kb[l], &e->tm_vb[l], ta,
-                                      z.n_work_tc, st));
+      ta.stamp = aa.stamp;
+      if (!e->dry)
+        CUDA_TRY(e, launch_attention_tc(D, &e->tm_q, &e->tm_k[l], &e->tm_v[l], &e->tm_kb[l], &e->tm_vb[l], ta,
+                                        z.n_work_tc, st));
       ++e->n_launch;
     }
     LAUNCH(e, launch_attention(c.dtype, D, aa, graph ? Ly.max_work : z.n_work, overlap ? e->side_stream : st,
                                !overlap));
-    if (overlap) {
+    if (overlap && !e->dry) {
       CUDA_TRY(e, cudaEventRecord(e->ev_join, e->side_stream));
       CUDA_TRY(e, cudaStreamWaitEvent(st, e->ev_join, 0));
     }
     prof_end(e, st, ev, ORCA_K_ATTENTION, attn_flops, attn_bytes);
+    ++su;
     // x += a Wo + bo
     EpiParams eo{};
     eo.mode = kEpiResid;
@@ -703,6 +735,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     eo.bias = (const float *)lw(e, l, L_BO);
     eo.out = x;
     eo.status = status;
+    eo.stamp = stamp();
     if (fold) {  // the residual feeds LN2: bf16(gamma2 * x) and the row sums
       eo.ln_gamma = (const float *)lw(e, l, L_LN2_G);
       eo.ln_xb = xb;
@@ -715,11 +748,13 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_WO), N, H, H, eo, st));
     prof_end(e, st, ev, ORCA_K_GEMM_O, 2.0 * N * H * H, gemm_bytes(N, H, H, fold ? 8 + eb : 8));
+    ++su;
     if (!fold) {  // h = LN2(x)
       prof_begin(e, st, &ev);
       LAUNCH(e, launch_layernorm(c.dtype, x, (const float *)lw(e, l, L_LN2_G), (const float *)lw(e, l, L_LN2_B), h,
-                                   N_grid, N_dev, H, nullptr, nullptr, st));
+                                   N_grid, N_dev, H, nullptr, nullptr, stamp(), st));
       prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)N * H * (4 + eb));
+      ++su;
     }
     // u = GeLU(LN2(x) W1 + b1)
     EpiParams e1{};
@@ -728,6 +763,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     e1.bias = fold ? fold_vec(e->ws, Ly, c, l, 3) : (const float *)lw(e, l, L_B1);
     e1.out = u;
     e1.status = status;
+    e1.stamp = stamp();
     if (fold) {
       e1.ln_in = ln_a;
       e1.ln_c = fold_vec(e->ws, Ly, c, l, 2);
@@ -741,6 +777,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)h, (const float *)lw(e, l, L_W1), N, F, H, e1, st));
     prof_end(e, st, ev, ORCA_K_GEMM_FC1, 2.0 * N * F * H, gemm_bytes(N, F, H, eb));
+    ++su;
     // x += u W2 + b2
     EpiParams e2{};
     e2.mode = kEpiResid;
@@ -748,6 +785,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     e2.bias = (const float *)lw(e, l, L_B2);
     e2.out = x;
     e2.status = status;
+    e2.stamp = stamp();
     const bool feeds_ln1 = fold && l + 1 < c.n_layers;  // the next layer's LN1 (the last feeds the final LN)
     if (feeds_ln1) {
       e2.ln_gamma = (const float *)lw(e, l + 1, L_LN1_G);
@@ -761,13 +799,15 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
     else
       LAUNCH(e, launch_gemm_simt_f32((const float *)u, (const float *)lw(e, l, L_W2), N, H, F, e2, st));
     prof_end(e, st, ev, ORCA_K_GEMM_FC2, 2.0 * N * H * F, gemm_bytes(N, H, F, feeds_ln1 ? 8 + eb : 8));
+    ++su;
   }
   // final LayerNorm on each request's last row, LM head (tied), greedy choice
   prof_begin(e, st, &ev);
   // (also zeroes the argmax keys the LM head's epilogue max-reduces into)
   LAUNCH(e, launch_layernorm(c.dtype, x, (const float *)e->w[W_LNF_G], (const float *)e->w[W_LNF_B], hf, B_grid,
-                               B_dev, H, d_req, d_keys, st));
+                               B_dev, H, d_req, d_keys, stamp(), st));
   prof_end(e, st, ev, ORCA_K_LAYERNORM, 0.0, (double)B * H * (4 + eb));
+  ++su;
   EpiParams el{};
   el.mode = kEpiLogits;
   el.ldo = V;
@@ -775,12 +815,14 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
   el.out = logits;
   el.status = status;
   el.argmax_keys = bf16 ? d_keys : nullptr;
+  el.stamp = stamp();
   prof_begin(e, st, &ev);
   if (bf16)
     LAUNCH(e, launch_gemm_tc_bf16(e->tm_hf, e->tm_emb, B, B_dev, V, H, el, scr, status, st));
   else
     LAUNCH(e, launch_gemm_simt_f32((const float *)hf, (const float *)e->w[W_TOK], B, V, H, el, st));
   prof_end(e, st, ev, ORCA_K_LM_HEAD, 2.0 * B * V * H, gemm_bytes(B, V, H, logits ? 4 : 0));
+  ++su;
   if (!bf16) {
     prof_begin(e, st, &ev);
     LAUNCH(e, launch_argmax(logits, B, V, nullptr, d_keys, st));
@@ -877,7 +919,8 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
          cudaHostAlloc(&S.h_work, sizeof(AttnWork) * L.max_work, cudaHostAllocDefault) == cudaSuccess &&
          cudaHostAlloc(&S.h_work_tc, sizeof(AttnWork) * max_tc_work(cfg->max_bs, cfg->max_rows),
                        cudaHostAllocDefault) == cudaSuccess &&
-         cudaHostAlloc(&S.h_out, sizeof(unsigned long long) * (cfg->max_bs + 1), cudaHostAllocDefault) ==
+         cudaHostAlloc(&S.h_out, sizeof(unsigned long long) * (cfg->max_bs + 1 + stamp_capacity(cfg)),
+                       cudaHostAllocDefault) ==
              cudaSuccess &&
          cudaHostAlloc(&S.h_blocks, max_table_entries(cfg) * 4, cudaHostAllocDefault) == cudaSuccess &&
          cudaEventCreateWithFlags(&S.done, cudaEventDisableTiming) == cudaSuccess &&
@@ -1264,7 +1307,6 @@ int orca_iteration_submit(orca_engine *e, orca_request *pool, const int32_t *bat
   e->last_work = n_work;
   e->last_h2d = (int64_t)sizeof(DevHeader) + (int64_t)sizeof(ReqInfo) * n_batch + (int64_t)sizeof(RowInfo) * N +
                 (int64_t)sizeof(AttnWork) * (n_work + n_work_tc) + (int64_t)sizeof(int32_t) * n_entries;
-  e->last_d2h = (int64_t)sizeof(unsigned long long) * (n_batch + 1);
   e->last_row_off.assign(n_batch + 1, 0);
   e->last_last_row.resize(n_batch);
   for (int32_t i = 0; i < n_batch; ++i) {
@@ -1307,13 +1349,22 @@ int orca_iteration_submit(orca_engine *e, orca_request *pool, const int32_t *bat
   // logits only when the caller asks for them; fp32: logits, then argmax.
   float *logits = logits_dev ? logits_dev : (bf16 ? nullptr : ws_ptr<float>(e, Ly.logits));
   const bool use_graph = bf16 && !e->prof && !(flags & ORCA_ITER_EAGER);
+  S.units.clear();
+  if (e->stamps) {  // the launches' classes and algorithmic work, in stamp order (nothing is launched)
+    e->dry = true;
+    e->dry_units.clear();
+    const int rc = enqueue_forward(e, st, z, logits, use_graph, k);
+    e->dry = false;
+    if (rc) return rc;
+    S.units = e->dry_units;
+  }
   if (use_graph) {
     // graphs differ in their GEMM plans, in whether the tensor-core prompt
     // attention runs at all, and in the in-flight slot they read
     const uint64_t key = (uint64_t)gemm_plan_code(N, 3 * H, H) | ((uint64_t)gemm_plan_code(N, H, H) << 6) |
                          ((uint64_t)gemm_plan_code(N, F, H) << 12) | ((uint64_t)gemm_plan_code(N, H, F) << 18) |
                          ((uint64_t)gemm_plan_code(n_batch, V, H) << 24) | ((uint64_t)(n_work_tc > 0) << 30) |
-                         ((uint64_t)k << 31);
+                         ((uint64_t)k << 31) | ((uint64_t)e->stamps << 32);
     const auto gk = std::make_pair(key, reinterpret_cast<uintptr_t>(logits));
     auto it = e->graphs.find(gk);
     if (it == e->graphs.end()) {
@@ -1350,7 +1401,10 @@ int orca_iteration_submit(orca_engine *e, orca_request *pool, const int32_t *bat
     if (rc) return rc;
     e->last_launches = e->n_launch;
   }
-  CUDA_TRY(e, cudaMemcpyAsync(S.h_out, d_out, sizeof(unsigned long long) * (n_batch + 1), cudaMemcpyDeviceToHost, st));
+  // the status word and the tokens (with stamps: up to the last stamp, in one copy)
+  const size_t out_words = e->stamps ? (size_t)e->cfg.max_bs + 2 + S.units.size() : (size_t)n_batch + 1;
+  CUDA_TRY(e, cudaMemcpyAsync(S.h_out, d_out, sizeof(unsigned long long) * out_words, cudaMemcpyDeviceToHost, st));
+  e->last_d2h = (int64_t)(sizeof(unsigned long long) * out_words);
   CUDA_TRY(e, cudaEventRecord(S.done, st));
   S.pool = pool;
   S.logits = logits_dev;
@@ -1376,6 +1430,20 @@ int orca_iteration_wait(orca_engine *e, int32_t *n_batch, int32_t *batch_idx, in
   if (batch_idx) std::copy(S.idx.begin(), S.idx.end(), batch_idx);
   CUDA_TRY(e, cudaEventSynchronize(S.done));
   if (e->prof) prof_collect(e, k);
+  if (e->stamps && !S.units.empty()) {  // each launch's share: its end minus the previous end
+    const unsigned long long *ts = S.h_out + 1 + e->cfg.max_bs;
+    unsigned long long prev = ts[0];
+    for (size_t j = 0; j < S.units.size(); ++j) {
+      const unsigned long long t = ts[1 + j];
+      const double ms = (prev != 0 && t > prev) ? (double)(t - prev) * 1e-6 : 0.0;
+      if (t > prev) prev = t;
+      orca_kernel_stats &ks = e->stats[S.units[j].cls];
+      ks.launches += 1;
+      ks.total_ms += ms;
+      ks.flops += S.units[j].flops;
+      ks.bytes += S.units[j].bytes;
+    }
+  }
   const int32_t dev_status = (int32_t)(S.h_out[0] & 0xFFFFFFFFull);
   if (dev_status != 0) {
     int32_t *status = ws_ptr<int32_t>(e, e->lay.out[k]);
@@ -1635,9 +1703,12 @@ int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const
 }
 
 int orca_profile_enable(orca_engine *e, int32_t enable) {
-  if (!e) return ORCA_EINVAL;
+  if (!e || enable < 0 || enable > 2) return ORCA_EINVAL;
   if (e->host_only && enable) return ORCA_ESTATE;
-  e->prof = enable != 0;
+  if (e->q_len > 0) return fail(e, ORCA_ESTATE, "iterations in flight");
+  if (enable == 2 && e->cfg.dtype != ORCA_DTYPE_BF16) return fail(e, ORCA_EINVAL, "launch stamps need a bf16 model");
+  e->prof = enable == 1;
+  e->stamps = enable == 2;
   for (auto &s : e->stats) s = orca_kernel_stats{};
   for (auto &p : e->pending) {  // launches still in flight are not counted
     e->ev_free.push_back(p.a);

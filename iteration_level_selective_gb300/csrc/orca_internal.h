@@ -125,6 +125,7 @@ struct EpiParams {
   // Rows of a statistics buffer this launch clears for a later residual
   // epilogue (by the thread that stores the row's column 0), or nullptr.
   LnStats *ln_zero;
+  unsigned long long *stamp;  // launch-end stamp (stamp_end), or nullptr
 };
 
 // Greedy-choice key of (value, column): larger value first, then lower
@@ -169,6 +170,7 @@ struct AttnArgs {
   float scale_log2;       // log2(e) / sqrt(D)
   const DevHeader *hdr;   // when set, n_rows / n_work / split come from it
   const int32_t *blocks;  // paged K/V block tables (ReqInfo::block_off >= 0)
+  unsigned long long *stamp;  // launch-end stamp (stamp_end), or nullptr
 };
 
 // Arguments of the tensor-core prefill attention (work items: kind 2,
@@ -184,6 +186,7 @@ struct TcAttnArgs {
   const int32_t *blocks;      // paged K/V block tables (ReqInfo::block_off >= 0)
   int64_t n_slots;
   float scale_log2;
+  unsigned long long *stamp;  // launch-end stamp (stamp_end), or nullptr
 };
 
 // ---- launch wrappers (defined in the .cu files); all return cudaError_t.
@@ -191,10 +194,12 @@ struct TcAttnArgs {
 // is only the capacity the fixed grid is sized for).
 // ln_g / ln_b / ln_out (optional, together): the first block's LayerNorm of
 // each embedded row, written to ln_out in the model dtype.
+// stamp_start / stamp (optional): the iteration's start (CTA 0, once the
+// kernel may read its inputs) and this launch's end (stamp_end).
 cudaError_t launch_embed(int dtype, const RowInfo *rows, int n_rows, const int32_t *n_rows_dev,
                          const void *tok_emb, const void *pos_emb, float *x, int H,
                          int vocab, int max_pos, int32_t *status, const float *ln_g, const float *ln_b,
-                         void *ln_out, cudaStream_t st);
+                         void *ln_out, unsigned long long *stamp_start, unsigned long long *stamp, cudaStream_t st);
 // c[n] = sum_k gamma_k W[n, k] and d[n] = bias[n] + sum_k beta_k W[n, k]
 // for a bf16 weight W [N, K] (row n = output column n): the vectors of a
 // LayerNorm folded into the Linear W.  bias may be nullptr.
@@ -204,7 +209,7 @@ cudaError_t launch_ln_fold_vectors(const void *W, const float *gamma, const floa
 // of the LM head's fused greedy choice).
 cudaError_t launch_layernorm(int dtype, const float *x, const float *g, const float *b, void *out,
                              int n_rows, const int32_t *n_rows_dev, int H, const ReqInfo *gather_last_row,
-                             unsigned long long *zero_keys, cudaStream_t st);
+                             unsigned long long *zero_keys, unsigned long long *stamp, cudaStream_t st);
 // One CTA that waits on an mbarrier nothing completes: the bounded wait
 // expires and raises kStatusWaitTimeout in *status (the failure path of
 // every kernel's waits, exercised without a fault).
@@ -284,6 +289,17 @@ constexpr int kTcBK = 64;
 // header copied before the forward, or set up shared / tensor memory).
 #ifdef __CUDACC__
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Launch-end stamp: thread 0 of every CTA, once the CTA's work is done, raises
+// *stamp to the current %globaltimer (ns), so that after the launch *stamp is
+// the time its last CTA finished.  The engine zeroes the stamps of an
+// iteration before its first launch and reads them after the last.
+__device__ __forceinline__ void stamp_end(unsigned long long *stamp) {
+  if (stamp != nullptr && threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    atomicMax(stamp, t);
+  }
+}
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 #endif
 

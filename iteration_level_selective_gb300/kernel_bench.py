@@ -37,7 +37,10 @@ LINEARS_13B_MIXED = (("qkv", 24373, 15360, 5120, C.ORCA_LINEAR_STORE),
                      ("lm_head", 256, 50257, 5120, C.ORCA_LINEAR_F32OUT))
 
 
-def time_linear(M: int, N: int, K: int, reps: int = 20, warmup: int = 3, mode: int = C.ORCA_LINEAR_STORE):
+def time_linear(M: int, N: int, K: int, reps: int = 20, warmup: int = 3, mode: int = C.ORCA_LINEAR_STORE,
+                scratch: bool = True):
+    """scratch: pass the split-K / balanced-schedule scratch the engine gives
+    every Linear (64 MB); without it the kernels run data-parallel."""
     dev = torch.device("cuda")
     g = torch.Generator(device=dev)
     g.manual_seed(0)
@@ -48,10 +51,12 @@ def time_linear(M: int, N: int, K: int, reps: int = 20, warmup: int = 3, mode: i
                       else torch.bfloat16)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     st = torch.cuda.current_stream()
+    scr = torch.empty(64 << 20, dtype=torch.uint8, device=dev) if scratch else None
 
     def run():
         C.orca_linear(C.ORCA_DTYPE_BF16, mode, A.data_ptr(), W.data_ptr(), bias.data_ptr(), out.data_ptr(), M, N, K,
-                      status.data_ptr(), st.cuda_stream)
+                      status.data_ptr(), st.cuda_stream, scratch_ptr=scr.data_ptr() if scratch else 0,
+                      scratch_bytes=(64 << 20) if scratch else 0)
 
     for _ in range(warmup):
         run()
@@ -94,6 +99,26 @@ def graph_us(fn, n: int = 20, trials: int = 3) -> float:
         torch.cuda.synchronize()
         best = min(best, e0.elapsed_time(e1) * 1000.0 / n)
     return best
+
+
+def time_cublas(M: int, N: int, K: int, reps: int = 20, warmup: int = 3):
+    """torch.nn.functional.linear (cuBLAS, bf16 out) on the same shapes, for reference."""
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    A = torch.randn((M, K), device=dev, generator=g).to(torch.bfloat16)
+    W = (torch.randn((N, K), device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    out = torch.empty((M, N), device=dev, dtype=torch.bfloat16)
+    for _ in range(warmup):
+        torch.nn.functional.linear(A, W, out=out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        torch.nn.functional.linear(A, W, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
 
 
 def time_linear_graph(M: int, N: int, K: int):
@@ -199,6 +224,7 @@ def main():
     sub.add_parser("sweep")
     sub.add_parser("linear-graph")
     sub.add_parser("linears-13b-mixed")
+    sub.add_parser("linear-13b")
     pa = sub.add_parser("attention")
     pa.add_argument("--case", choices=sorted(ATTN_CASES), required=True)
     pa.add_argument("--reps", type=int, default=5)
@@ -212,6 +238,18 @@ def main():
         print(json.dumps(r))
     elif a.cmd == "linear":
         print(json.dumps(time_linear(a.M, a.N, a.K, a.reps, a.warmup)))
+    elif a.cmd == "linear-13b":
+        # the 13B Linears (QKV, Attn-Out, FC1, FC2) at the row counts of decode-heavy iterations
+        for M in (1, 64, 128, 200, 256, 384, 512, 1024, 2048, 24373):
+            for (N, K) in ((15360, 5120), (5120, 5120), (20480, 5120), (5120, 20480), (50257, 5120)):
+                if M == 24373 and N == 50257:
+                    continue
+                r = time_linear(M, N, K, reps=20)
+                r["no_scratch_ms"] = time_linear(M, N, K, reps=20, scratch=False)["ms"]
+                r["cublas_ms"] = time_cublas(M, N, K)
+                r["weight_gbs"] = N * K * 2 / r["ms"] / 1e6
+                r["cublas_weight_gbs"] = N * K * 2 / r["cublas_ms"] / 1e6
+                print(json.dumps(r), flush=True)
     elif a.cmd == "linears-13b-mixed":
         for name, M, N, K, mode in LINEARS_13B_MIXED:
             r = time_linear(M, N, K, reps=1, warmup=1, mode=mode)

@@ -63,11 +63,12 @@ def test_argmax_forced_logits_bit_exact(cuda):
                                    # few narrow tiles with a 1 MB weight block each: split-K over the
                                    # persistent kernel when a scratch buffer is given
                                    (200, 520, 16384),
-                                   # CTA-pair kernel (>= 512 rows, 256 x 256 tiles over two SMs): ragged
-                                   # last pair tile (one row in the leader, none in the peer), a single
-                                   # k-block, vocab-wide ragged N, a long K, wide N and K
-                                   (513, 1000, 512), (1024, 256, 64), (777, 50257, 1024), (4100, 520, 20480),
-                                   (1500, 4096, 5120)])
+                                   # CTA-pair kernel (>= 512 rows and a tile per pair, or >= 129 rows and
+                                   # N >= 12288; 256 x 256 tiles over two SMs): ragged last pair tile (one
+                                   # row in the leader, none in the peer), a single k-block with ragged N,
+                                   # vocab-wide ragged N, a long K, wide N and K
+                                   (513, 20480, 256), (1024, 20000, 64), (777, 50257, 1024), (300, 12288, 4096),
+                                   (1500, 4096, 5120), (200, 15360, 512)])
 @pytest.mark.parametrize("mode", ["store", "gelu", "resid", "f32out"])
 @pytest.mark.parametrize("split", [False, True])
 def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode, split):
@@ -406,6 +407,45 @@ def test_graph_replay_equals_eager_launches(cuda):
         # batch
         want = 3 + nl * (5 + int(max(e.n_new) >= 32))
         assert g.launches == want and e.launches == want
+
+
+def test_launch_stamps_time_the_graph_path(cuda):
+    """Profiling mode 2 (launch stamps in the graph-replayed forward): the
+    tokens and logits are those of an unprofiled run, every launch of every
+    iteration is counted in its class, and the classes' times add up to no
+    more than the device time of the iterations (CUDA events around them)."""
+    from iteration_level_selective_gb300 import _orca as C
+    from iteration_level_selective_gb300 import runtime as rt
+    shape = SMALL_BF16
+    w = synth.make_weights(shape, seed=21, w_std=0.05, bias_std=0.02, ln_std=0.1)
+    trace = synth.make_trace(10, (1, 300), (1, 12), vocab=shape.vocab, seed=22, rate_per_iter=0.6, forced=True)
+    out = []
+    for mode in (0, 2):
+        dw = rt.DeviceWeights(shape, cuda, host=w)
+        eng = rt.Engine(shape, dw, max_bs=8, n_slots=8000, max_rows=2048, device=cuda)
+        C.orca_profile_enable(eng.handle, mode)
+        loop = rt.ServingLoop(eng, rt.RequestPool(trace, teacher_force=True), teacher_force=True, keep_logits=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(loop.stream)
+        recs = loop.run()
+        e1.record(loop.stream)
+        torch.cuda.synchronize()
+        stats = {C.KERNEL_NAMES[k]: C.orca_profile_read(eng.handle, k) for k in range(C.ORCA_K_COUNT)}
+        out.append((recs, stats, e0.elapsed_time(e1)))
+        eng.close()
+    (r0, _, _), (r2, stats, dev_ms) = out
+    for a, b in zip(r0, r2):
+        assert a.next_tokens == b.next_tokens
+        np.testing.assert_array_equal(a.logits, b.logits)
+    n_it, nl = len(r2), shape.n_layers
+    # embed, final LN, LM head; per layer QKV, attention (both launches: one stamp), Attn-Out, FC1, FC2
+    assert stats["embed"]["launches"] == n_it and stats["lm_head"]["launches"] == n_it
+    assert stats["layernorm"]["launches"] == n_it
+    for k in ("gemm_qkv", "attention", "gemm_o", "gemm_fc1", "gemm_fc2"):
+        assert stats[k]["launches"] == n_it * nl, k
+        assert stats[k]["total_ms"] > 0 and stats[k]["flops"] > 0, k
+    total = sum(s["total_ms"] for s in stats.values())
+    assert 0 < total <= dev_ms, (total, dev_ms)
 
 
 # ------------------------------------------------------------------ GPT-2-small, full size, sampled
