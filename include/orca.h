@@ -60,6 +60,12 @@ extern "C" {
                                      never write generated tokens into it   */
 #define ORCA_ITER_EAGER 2         /* launch the kernels one by one instead of
                                      replaying the engine's CUDA graph      */
+#define ORCA_ITER_SELFTEST_TIMEOUT 4 /* test hook: after the forward, one CTA
+                                     waits on a barrier that nothing
+                                     completes; its bounded wait (about 2 s)
+                                     expires and sets the iteration's status
+                                     word, so the wait returns ORCA_EDEVICE
+                                     (the failure path, without a fault)    */
 
 /* ---------------------------------------------------------------- types */
 typedef struct orca_engine orca_engine;

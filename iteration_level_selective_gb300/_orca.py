@@ -33,6 +33,7 @@ ORCA_RESERVE_MAX, ORCA_RESERVE_POW2, ORCA_RESERVE_ORACLE, ORCA_RESERVE_PAGED = 0
 ORCA_KV_BLOCK = 32
 ORCA_ITER_TEACHER_FORCE = 1
 ORCA_ITER_EAGER = 2
+ORCA_ITER_SELFTEST_TIMEOUT = 4
 (ORCA_K_EMBED, ORCA_K_LAYERNORM, ORCA_K_GEMM_QKV, ORCA_K_ATTENTION, ORCA_K_GEMM_O, ORCA_K_GEMM_FC1,
  ORCA_K_GEMM_FC2, ORCA_K_LM_HEAD, ORCA_K_ARGMAX, ORCA_K_COUNT) = range(10)
 KERNEL_NAMES = ["embed", "layernorm", "gemm_qkv", "attention", "gemm_o", "gemm_fc1", "gemm_fc2",
@@ -314,8 +315,10 @@ def argmax_key_column(key: int) -> int:
     return -1 if key == 0 else 0xFFFFFFFF - (key & 0xFFFFFFFF)
 
 
-def orca_profile_enable(eng, enable: bool) -> None:
-    _check(lib().orca_profile_enable(eng, 1 if enable else 0), eng)
+def orca_profile_enable(eng, mode: int) -> None:
+    """mode 0 off, 1 CUDA events around eager launches, 2 launch stamps in
+    the graph-replayed forward (True / False mean 1 / 0)."""
+    _check(lib().orca_profile_enable(eng, int(mode)), eng)
 
 
 def orca_profile_read(eng, kernel_class: int) -> dict:

@@ -1401,6 +1401,8 @@ int orca_iteration_submit(orca_engine *e, orca_request *pool, const int32_t *bat
     if (rc) return rc;
     e->last_launches = e->n_launch;
   }
+  if (flags & ORCA_ITER_SELFTEST_TIMEOUT)  // test hook: a bounded wait expires on the status word
+    CUDA_TRY(e, launch_wait_selftest(reinterpret_cast<int32_t *>(d_out), st));
   // the status word and the tokens (with stamps: up to the last stamp, in one copy)
   const size_t out_words = e->stamps ? (size_t)e->cfg.max_bs + 2 + S.units.size() : (size_t)n_batch + 1;
   CUDA_TRY(e, cudaMemcpyAsync(S.h_out, d_out, sizeof(unsigned long long) * out_words, cudaMemcpyDeviceToHost, st));

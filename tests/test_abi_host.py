@@ -70,6 +70,12 @@ def test_host_only_engine_reserve_release_errors(liborca):
         with pytest.raises(C.OrcaError) as ei:
             C.orca_kv_reserve(eng, 7, 0)
         assert ei.value.code == C.ORCA_EINVAL
+        # profiling modes: 0 off, 1 events, 2 launch stamps; a host-only engine profiles nothing
+        C.orca_profile_enable(eng, 0)
+        for mode, code in ((3, C.ORCA_EINVAL), (-1, C.ORCA_EINVAL), (1, C.ORCA_ESTATE), (2, C.ORCA_ESTATE)):
+            with pytest.raises(C.OrcaError) as ei:
+                C.orca_profile_enable(eng, mode)
+            assert ei.value.code == code, mode
         # orca_iteration needs a device side
         pool = (C.orca_request * 1)()
         bi = (ctypes.c_int32 * 4)()

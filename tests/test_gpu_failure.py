@@ -120,3 +120,51 @@ def test_no_kernel_writes_outside_its_buffers(cuda, policy):
                 assert hz.max_rel_err(g, o) < 2e-2
     finally:
         eng.close()
+
+
+def test_iteration_reports_an_expired_wait_and_the_engine_goes_on(cuda):
+    """An iteration whose status word a bounded wait raised (the self-test
+    hook: one CTA waits on a barrier nothing completes) returns ORCA_EDEVICE
+    after the bound; requests admitted afterwards on the same engine, and a
+    fresh engine, still match the oracle."""
+    import ctypes
+    from iteration_level_selective_gb300 import _orca as C
+    from iteration_level_selective_gb300 import runtime as rt
+    shape = SMALL_BF16
+    w = synth.make_weights(shape, seed=25, w_std=0.05, bias_std=0.02, ln_std=0.1)
+    dw = rt.DeviceWeights(shape, cuda, host=w)
+    eng = rt.Engine(shape, dw, max_bs=4, n_slots=2000, max_rows=512, device=cuda)
+    try:
+        bad = synth.make_trace(2, (40, 60), (3, 3), vocab=shape.vocab, seed=26, forced=True)
+        pool = rt.RequestPool(bad, teacher_force=True)
+        bi, nt = (ctypes.c_int32 * 4)(), (ctypes.c_int32 * 4)()
+        nb = C.orca_select_batch(eng.handle, pool.arr, pool.n, bi)
+        assert nb == 2
+        t0 = time.perf_counter()
+        with pytest.raises(C.OrcaError) as ei:
+            C.orca_iteration(eng.handle, pool.arr, bi, nb, C.ORCA_ITER_TEACHER_FORCE | C.ORCA_ITER_SELFTEST_TIMEOUT,
+                             nt)
+        assert ei.value.code == C.ORCA_EDEVICE
+        assert 1.0 < time.perf_counter() - t0 < 30.0
+        # new requests on the same engine (the failed ones keep their slots)
+        good = [synth.Request(100 + r.req_id, 0, r.prompt, r.out_len, r.max_tokens, forced=r.forced)
+                for r in synth.make_trace(3, (1, 80), (2, 5), vocab=shape.vocab, seed=27, forced=True)]
+        loop = rt.ServingLoop(eng, rt.RequestPool(good, teacher_force=True), teacher_force=True, keep_logits=True)
+        got = hz.gpu_logits_by_request(loop.run())
+        for req in good:
+            _, logits = hz.oracle_generate(shape, w, req, teacher_force=True)
+            for g, o in zip(got[req.req_id], logits):
+                assert hz.max_rel_err(g, o) < 2e-2
+    finally:
+        eng.close()
+    # and a fresh engine serves the requests that failed
+    recs, eng2, _ = hz.run_gpu(shape, w, bad, max_bs=4, n_slots=2000, max_rows=512, teacher_force=True,
+                               keep_all=True)
+    try:
+        got = hz.gpu_logits_by_request(recs)
+        for req in bad:
+            _, logits = hz.oracle_generate(shape, w, req, teacher_force=True)
+            for g, o in zip(got[req.req_id], logits):
+                assert hz.max_rel_err(g, o) < 2e-2
+    finally:
+        eng2.close()
