@@ -13,14 +13,23 @@
 //   warp 1     issues the MMAs: S = Q K^T into one of two TMEM buffers, and
 //              O += P V into a TMEM accumulator (V is the B operand as it
 //              lies in the K/V pool, head dim contiguous: MN-major);
-//   warps 2-5  one query row per thread (one TMEM lane): read the row of S,
-//              mask the keys past the row's position, keep the running max
-//              m and sum l, write P = exp2((S - m) * log2(e)/sqrt(d)) as
-//              bf16 into shared memory; O is rescaled only when m grows by
+//   warps 2-9  softmax in two groups of four warps: warp w and warp w + 4
+//              share one TMEM lane quarter, so each query row (one TMEM lane)
+//              has two threads, one per half of the tile's 128 keys.  They
+//              read their half of the row of S, mask the keys past the row's
+//              position and swap their half-row maxima through shared memory
+//              (a named barrier per lane quarter), so both keep the same
+//              running max m; each keeps the sum l of its half and writes its
+//              half of P = exp2((S - m) * log2(e)/sqrt(d)) as bf16 into
+//              tensor memory, in one of two P buffers, from where the P V
+//              MMA reads it as its A operand.  O is
+//              rescaled, half of its columns by each, only when m grows by
 //              more than a factor 2^8 (until then P may exceed 1, which fp32
-//              and bf16 hold as well); at the end O / l -> bf16 rows.
+//              and bf16 hold as well); at the end the two sums are added and
+//              each thread writes its half of the row of O / l.
 // While the softmax warps work on tile t the tensor core computes S of tile
-// t+1 and P V of tile t-1.  Keys beyond the item's causal range are masked by
+// t+1 and P V of tile t-1; with two P buffers the softmax of tile t waits only
+// for P V of tile t-2 (and, when O must be rescaled, of tile t-1).  Keys beyond the item's causal range are masked by
 // selection; their V rows are zeroed in shared memory before P V, so stale
 // slot contents never reach O.  Every mbarrier wait is bounded.
 #include <cuda.h>
@@ -35,7 +44,9 @@ namespace {
 
 constexpr int kRows = 128;       // query rows per item = TMEM lanes
 constexpr int kKeys = 128;       // keys per tile
-constexpr int kThreadsTc = 192;  // warp 0 loads, warp 1 issues MMAs, warps 2-5 softmax
+constexpr int kThreadsTc = 320;  // warp 0 loads, warp 1 issues MMAs, warps 2-9 softmax
+constexpr int kSoftmaxThreads = 256;
+constexpr int kHalf = kKeys / 2;  // keys of a tile per softmax thread
 constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
@@ -45,10 +56,12 @@ struct TcCfg {
   static constexpr int Q_BYTES = KB * kRows * 128;
   static constexpr int K_BYTES = KB * kKeys * 128;  // K-major: key rows of 128 B per block
   static constexpr int V_BYTES = KB * kKeys * 128;  // same bytes, read as an MN-major operand
-  static constexpr int P_BYTES = 2 * kRows * 128;   // 128 rows x 128 keys, K-major
-  static constexpr int SMEM = Q_BYTES + NS * (K_BYTES + V_BYTES) + P_BYTES + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;        // S0 [0,128), S1 [128,256), O [256, 256+D)
+  static constexpr int SMEM = Q_BYTES + NS * (K_BYTES + V_BYTES) + 1024;
+  // S0 [0,128), S1 [128,256), O [256, 256+D), P0 [384,448), P1 [448,512):
+  // P as bf16 pairs, 64 columns per 128-key tile
+  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 256;
+  static constexpr uint32_t P_COL = 384;
   // kind::f16: D fp32 (bit 4), A bf16 (bits 7-9), B bf16 (bits 10-12),
   // B MN-major (bit 16) for P V, N >> 3 (bits 17-22), M >> 4 (bits 24-28)
   static constexpr uint32_t IDESC_S =
@@ -84,6 +97,18 @@ __device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// D (+)= A B with A (M x K) in tensor memory: lane = row, K packed two bf16
+// to a column.
+__device__ __forceinline__ void tc_mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -107,43 +132,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 128 consecutive TMEM columns of this thread's lane in one load (warp-collective).
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float *v) {
-  uint32_t r[128];
+// 64 consecutive TMEM columns of this thread's lane (warp-collective).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float *v) {
+  uint32_t r[64];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {"
-      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
-      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, "
-      "%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
-      "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, "
-      "%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, "
-      "%112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127"
-      "}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63"
+      "}, [%64];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
-        "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
-        "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
-        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
-        "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
-        "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]),
-        "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]),
-        "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]),
-        "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]),
-        "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr)
       : "memory");
 #pragma unroll
-  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// Named barrier of the two softmax warps that share a TMEM lane quarter.
+__device__ __forceinline__ void pair_barrier(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
   asm volatile(
@@ -172,13 +178,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Byte offset of element (row, k) in a K-major, 128-byte-swizzled operand
-// tile of `rows` rows (64-element K-blocks stacked, 8-row atoms of 1024 B).
-__device__ __forceinline__ uint32_t sw128_offset(int row, int k, int rows) {
-  const int kb = k >> 6, kk = k & 63;
-  return (uint32_t)(kb * rows * 128 + row * 128 + ((((kk >> 3) ^ (row & 7)) << 4) | ((kk & 7) << 1)));
-}
-
 // One claimed work item, decoded by the loader for the other roles.
 struct TcItem {
   int head, r0, nq, p0;  // query rows r0 .. r0+nq-1 at positions p0 ..
@@ -193,9 +192,11 @@ struct TcShared {
   uint64_t q_full, q_empty;
   uint64_t k_full[NS], v_full[NS], kv_empty[NS];
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, o_done;
+  uint64_t p_full[2], o_done[2];  // per P buffer: P written; P V with it done
   uint64_t it_full[2], it_empty[2];
   TcItem it[2];
+  float half_max[2][2][kRows];  // [tile parity][key half][row]: the softmax halves' maxima
+  float half_sum[2][kRows];     // [key half][row]: each half's sum at the end of an item
   uint32_t tmem;
   int abort;
 };
@@ -221,7 +222,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint8_t *sQ = smem_raw + pad;
   uint8_t *sK = sQ + C::Q_BYTES;       // NS stages of K
   uint8_t *sV = sK + NS * C::K_BYTES;  // NS stages of V
-  uint8_t *sP = sV + NS * C::V_BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
@@ -233,12 +233,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.s_full[b], 1);
-      mbar_init(&sh.s_empty[b], 128);
+      mbar_init(&sh.s_empty[b], kSoftmaxThreads);
       mbar_init(&sh.it_full[b], 1);
-      mbar_init(&sh.it_empty[b], 1 + 4);  // the MMA warp and the four softmax warps
+      mbar_init(&sh.it_empty[b], 1 + 8);  // the MMA warp and the eight softmax warps
     }
-    mbar_init(&sh.p_full, 128);
-    mbar_init(&sh.o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.p_full[b], kSoftmaxThreads);
+      mbar_init(&sh.o_done[b], 1);
+    }
     sh.abort = 0;
     mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     uint32_t n_item = 0, g = 0;
-    const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV), pa = smem_u32(sP);
+    const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
     while (true) {
       const uint32_t slot = n_item & 1;
       if (!warp_wait(&sh.it_full[slot], (n_item >> 1) & 1, abort_flag, a.status)) break;
@@ -400,8 +402,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         if (tile >= 1) {  // O += P(tile-1) V(tile-1)
           const int tp = tile - 1;
-          const uint32_t gp = g + tp, s = gp % NS;
-          if (!warp_wait(&sh.p_full, gp & 1, abort_flag, a.status) ||
+          const uint32_t gp = g + tp, s = gp % NS, pb = gp & 1;
+          if (!warp_wait(&sh.p_full[pb], (gp >> 1) & 1, abort_flag, a.status) ||
               !warp_wait(&sh.v_full[s], (gp / NS) & 1, abort_flag, a.status)) {
             ok = false;
             break;
@@ -420,12 +422,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           __syncwarp();
           if (lane == 0) {
             tc_fence_after();
-            for (int kk = 0; kk < kKeys / 16; ++kk)
-              tc_mma(tmem + C::O_COL, sw128_desc(pa + (kk >> 2) * kRows * 128 + (kk & 3) * 32),
-                     sw128_mn_desc(va + s * C::V_BYTES + kk * 2048, kKeys * 128, 1024), C::IDESC_O,
-                     (tp | kk) ? 1u : 0u);
+            for (int kk = 0; kk < kKeys / 16; ++kk)  // 16 keys = 8 columns of the P buffer
+              tc_mma_ts(tmem + C::O_COL, tmem + C::P_COL + pb * 64 + kk * 8,
+                        sw128_mn_desc(va + s * C::V_BYTES + kk * 2048, kKeys * 128, 1024), C::IDESC_O,
+                        (tp | kk) ? 1u : 0u);
             tc_commit(&sh.kv_empty[s]);
-            tc_commit(&sh.o_done);
+            tc_commit(&sh.o_done[pb]);
           }
           __syncwarp();
         }
@@ -438,16 +440,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else {
     // ------------------------------------------------------------ softmax
     const int quad = warp & 3;         // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // keys [half * 64, half * 64 + 64) of every tile
     const int row = quad * 32 + lane;  // query row of this thread
+    const int bar_id = 1 + quad;       // the two warps of this lane quarter
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-    uint32_t n_item = 0, g = 0, o_cnt = 0;
+    constexpr int DH = D / 2;          // output columns of this thread's half
+    uint32_t n_item = 0, g = 0;
+    // P V of global tile j has completed once phase j >> 1 of o_done[j & 1] has
+    auto pv_done = [&](uint32_t j) {
+      return warp_wait(&sh.o_done[j & 1], (j >> 1) & 1, abort_flag, a.status);
+    };
     while (true) {
       const uint32_t slot = n_item & 1;
       if (!warp_wait(&sh.it_full[slot], (n_item >> 1) & 1, abort_flag, a.status)) break;
       const TcItem it = sh.it[slot];
       if (it.n_tiles < 0) break;
       const int my_pos = row < it.nq ? it.p0 + row : -1;  // -1: no key is visible to this row
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f;  // l: the sum over this thread's half of the keys
       bool ok = true;
       for (int tile = 0; tile < it.n_tiles; ++tile) {
         const uint32_t gt = g + tile, b = gt & 1;
@@ -456,23 +465,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           break;
         }
         tc_fence_after();
-        float v[kKeys];
-        tmem_ld128(tl + b * 128, v);
+        float v[kHalf];
+        tmem_ld64(tl + b * 128 + half * kHalf, v);
         tc_fence_before();
         mbar_arrive(&sh.s_empty[b]);
-        const int k0 = tile * kKeys;
-        if (k0 + kKeys - 1 > my_pos) {
+        const int k0 = tile * kKeys + half * kHalf;
+        if (k0 + kHalf - 1 > my_pos) {
 #pragma unroll
-          for (int i = 0; i < kKeys; ++i)
+          for (int i = 0; i < kHalf; ++i)
             if (k0 + i > my_pos) v[i] = -INFINITY;
         }
         float mx[8];  // eight independent chains, then a tree
 #pragma unroll
         for (int j = 0; j < 8; ++j) mx[j] = v[j];
 #pragma unroll
-        for (int i = 8; i < kKeys; ++i) mx[i & 7] = fmaxf(mx[i & 7], v[i]);
-        const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+        for (int i = 8; i < kHalf; ++i) mx[i & 7] = fmaxf(mx[i & 7], v[i]);
+        const float hmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        // both threads of the row take the maximum of the two halves, so they
+        // keep the same running max and rescale decision
+        sh.half_max[b][half][row] = hmax;
+        pair_barrier(bar_id);
+        const float tmax = fmaxf(hmax, sh.half_max[b][half ^ 1][row]);
         const float m_new = fmaxf(m, tmax);
         const bool need = (m_new - m) * a.scale_log2 > kRescaleLog2;  // false while both are -inf
         float alpha = 1.f;
@@ -482,10 +496,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           m = m_new;
         }
         const float ms = m == -INFINITY ? 0.f : m * a.scale_log2;
-        uint32_t pk[kKeys / 2];
+        uint32_t pk[kHalf / 2];
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < kKeys; i += 2) {
+        for (int i = 0; i < kHalf; i += 2) {
           const float p0 = ex2(fmaf(v[i], a.scale_log2, -ms));
           const float p1 = ex2(fmaf(v[i + 1], a.scale_log2, -ms));
           const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
@@ -493,41 +507,39 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           pk[i / 2] = *reinterpret_cast<const uint32_t *>(&b2);
         }
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-        if (tile > 0) {  // P buffer and O are free once P V of the previous tile is done
-          if (!warp_wait(&sh.o_done, o_cnt & 1, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          ++o_cnt;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, need)) {
+        // P buffer gt & 1 is free once P V of tile gt - 2 is done; O may be
+        // rescaled only once P V of the previous tile (the last to add to it) is
+        if ((gt >= 2 && !pv_done(gt - 2)) || (tile > 0 && __any_sync(0xffffffffu, need) && !pv_done(gt - 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (tile > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-              float o[32];
-              tmem_ld32(tl + C::O_COL + c, o);
+          for (int c = half * DH; c < half * DH + DH; c += 32) {
+            float o[32];
+            tmem_ld32(tl + C::O_COL + c, o);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= alpha;
-              tmem_st32(tl + C::O_COL + c, o);
-            }
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tl + C::O_COL + c, o);
           }
         }
-#pragma unroll
-        for (int q = 0; q < kKeys / 8; ++q)
-          *reinterpret_cast<uint4 *>(sP + sw128_offset(row, q * 8, kRows)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        fence_proxy_async();  // P (generic stores) becomes visible to the tensor core
+        // this half's 64 keys: 32 columns of bf16 pairs in P buffer gt & 1
+        tmem_st32(tl + C::P_COL + (gt & 1) * 64 + half * 32, reinterpret_cast<const float *>(pk));
         tc_fence_before();
-        mbar_arrive(&sh.p_full);
+        mbar_arrive(&sh.p_full[gt & 1]);
       }
       if (!ok) break;
-      // ---- O / l -> output rows
-      if (!warp_wait(&sh.o_done, o_cnt & 1, abort_flag, a.status)) break;
-      ++o_cnt;
+      // ---- O / l -> output rows (l = the two halves' sums)
+      if (!pv_done(g + it.n_tiles - 1)) break;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      sh.half_sum[half][row] = l;
+      pair_barrier(bar_id);
+      const float lt = l + sh.half_sum[half ^ 1][row];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) + (int64_t)(it.r0 + row) * a.hidden + it.head * D;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = half * DH; c < half * DH + DH; c += 32) {
         float o[32];
         tmem_ld32(tl + C::O_COL + c, o);
         if (row < it.nq) {

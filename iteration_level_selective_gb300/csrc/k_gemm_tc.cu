@@ -448,7 +448,9 @@ __global__ void __launch_bounds__(192, 1)
           if (ok && col < N) finish_run(epi, row, col, v, min(32, N - col), row < M, best, bl);
         }
       } else {
-        float *part = scr.partials + ((size_t)(tile * sc.S + split) * BM + q * 32 + lane) * BN;
+        // partial tiles are column-major [BN columns][BM rows]: the 32 lanes of a
+        // warp (32 consecutive rows) store and load 128 contiguous bytes
+        float *part = scr.partials + (size_t)(tile * sc.S + split) * BM * BN + q * 32 + lane;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
@@ -460,8 +462,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           if (ok && row < M) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4 *>(part + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            for (int j = 0; j < 32; ++j) __stcg(part + (size_t)(c + j) * BM, v[j]);
           }
         }
         __threadfence();
@@ -472,7 +473,7 @@ __global__ void __launch_bounds__(192, 1)
           __threadfence();
           if (threadIdx.x == 64) scr.counters[tile] = 0;
           if (ok) {
-            const float *p0 = scr.partials + ((size_t)tile * sc.S * BM + q * 32 + lane) * BN;
+            const float *p0 = scr.partials + (size_t)tile * sc.S * BM * BN + q * 32 + lane;
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
               const int col = n * BN + c;
@@ -480,16 +481,23 @@ __global__ void __launch_bounds__(192, 1)
               float v[32];
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = 0.f;
+              // the splits in order, two at a time: all 64 loads in flight together
 #pragma unroll 1
-              for (int s = 0; s < sc.S && row < M; ++s) {
-                const float4 *ps = reinterpret_cast<const float4 *>(p0 + (size_t)s * BM * BN + c);
+              for (int s = 0; s < sc.S && row < M; s += 2) {
+                const float *ps = p0 + (size_t)s * BM * BN + (size_t)c * BM;
+                float t0[32], t1[32];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float4 t = __ldcg(ps + j);
-                  v[4 * j] += t.x;
-                  v[4 * j + 1] += t.y;
-                  v[4 * j + 2] += t.z;
-                  v[4 * j + 3] += t.w;
+                for (int j = 0; j < 32; ++j) t0[j] = __ldcg(ps + (size_t)j * BM);
+                const bool two = s + 1 < sc.S;
+                if (two) {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) t1[j] = __ldcg(ps + (size_t)BM * BN + (size_t)j * BM);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += t0[j];
+                if (two) {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) v[j] += t1[j];
                 }
               }
               finish_run(epi, row, col, v, min(32, N - col), row < M, best, run_bias(epi, col, min(32, N - col)));
@@ -1174,13 +1182,25 @@ int gemm_sm_count() {
   return n;
 }
 
+// Products of at least this many rows may take the CTA-pair kernel (gemm_plan).
+constexpr int kPairMinRows = 512;
+// Weight streams at least this large, at a few hundred rows, take 256-wide
+// tiles split along K.  Measured on GB300 at 200-256 rows: the 13B FC2 (210 MB)
+// 17% faster than on 128-wide unsplit tiles, the Attn-Out (52 MB) 25% slower
+// (its reduction of 3 partial tiles costs more than its shorter K saves).
+constexpr double kSplitMinWeightBytes = 128.0 * (1 << 20);
+
 // Output-tile width of the persistent kernel: 256 when those tiles fill the
 // GPU, else the widest of 128 / 64 / 32 whose tiles occupy at least half the
 // SMs (narrower tiles spread a small-M product's weight stream over more SMs).
-int gemm_tile_n(int M, int N) {
+int gemm_tile_n(int M, int N, int K) {
   const long long nM = (M + BM - 1) / BM;
   const int sm = gemm_sm_count();
   if (nM * ((N + 255) / 256) >= sm) return 256;
+  // a large weight stream (tens of MB) at a few hundred rows: 256-wide tiles
+  // few enough to be split along K over the SMs (persistent split-K)
+  if (M > BM && M < kPairMinRows && 2.0 * N * K >= kSplitMinWeightBytes && nM * ((N + 255) / 256) * 2 <= sm)
+    return 256;
   if (nM * ((N + 127) / 128) * 2 >= sm) return 128;
   if (nM * ((N + 63) / 64) * 2 >= sm) return 64;
   return 32;
@@ -1231,7 +1251,6 @@ constexpr int kClusterMinKb = 32;
 // the pair kernel is 20-25% faster for N = 15360 and 20480 and slower for
 // N = 5120 (20 pair tiles leave most pairs idle); GPT-2-small's prompt
 // iterations (600 rows, N <= 3072) lost 4% on it.
-constexpr int kPairMinRows = 512;
 constexpr int kPairMinRowsWide = 129;
 constexpr int kPairWideN = 12288;
 GemmPlan gemm_plan(int M, int N, int K) {
@@ -1242,7 +1261,7 @@ GemmPlan gemm_plan(int M, int N, int K) {
     p.bn = kPairBN;
     return p;
   }
-  p.bn = gemm_tile_n(M, N);
+  p.bn = gemm_tile_n(M, N, K);
   p.ks = gemm_ks(p.bn, K);
   const int KB = K / BK;
   if (M > BM || M <= 0) return p;
@@ -1272,7 +1291,7 @@ GemmPlan gemm_plan(int M, int N, int K) {
     }
   }
   if (!p.cluster) {
-    p.bn = gemm_tile_n(M, N);
+    p.bn = gemm_tile_n(M, N, K);
     p.ks = gemm_ks(p.bn, K);
   }
   return p;

@@ -254,7 +254,7 @@ cudaError_t launch_gemm_tc_bf16(const OperandMaps &A, const OperandMaps &W, int 
                                 cudaStream_t st);
 int gemm_sm_count();
 // Output-tile width (128 or 256) the tcgen05 GEMM uses for an M x N product.
-int gemm_tile_n(int M, int N);
+int gemm_tile_n(int M, int N, int K);
 // Per-device one-time set-up of the GEMM kernels (shared-memory limits);
 // call before any stream capture.
 cudaError_t gemm_prepare();

@@ -203,6 +203,8 @@ ATTN_CASES = {
     # 16 prompts U{1024..2048} + 240 decodes with contexts U{128..2048}, 13B-shaped heads
     "c5": lambda rng: ([(int(L), 0) for L in rng.integers(1024, 2049, 16)] +
                        [(1, int(c)) for c in rng.integers(128, 2049, 240)], 40, 128),
+    # four prompts of 4096 tokens, 13B-shaped heads: items with 16 key tiles on average
+    "long_prompts": lambda rng: ([(4096, 0)] * 4, 40, 128),
     # the 16 prompts of c5 alone (tensor-core prefill kernel only)
     "c5_prefill": lambda rng: ([(int(L), 0) for L in rng.integers(1024, 2049, 16)], 40, 128),
     # one GPT-2-small prefill of 512 tokens plus 63 decodes with contexts U{32..768}

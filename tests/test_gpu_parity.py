@@ -68,7 +68,10 @@ def test_argmax_forced_logits_bit_exact(cuda):
                                    # row in the leader, none in the peer), a single k-block with ragged N,
                                    # vocab-wide ragged N, a long K, wide N and K
                                    (513, 20480, 256), (1024, 20000, 64), (777, 50257, 1024), (300, 12288, 4096),
-                                   (1500, 4096, 5120), (200, 15360, 512)])
+                                   (1500, 4096, 5120), (200, 15360, 512),
+                                   # 129..511 rows and a weight stream of >= 128 MB with N < 12288: 256-wide
+                                   # tiles split along K when a scratch buffer is given (2-3 splits)
+                                   (200, 5120, 5120), (300, 4096, 16384)])
 @pytest.mark.parametrize("mode", ["store", "gelu", "resid", "f32out"])
 @pytest.mark.parametrize("split", [False, True])
 def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode, split):
