@@ -22,8 +22,10 @@ value  = processed tokens (sum L_i) per second over the timed iterations,
          CUDA events on the iteration stream around the timed region;
 e2e    = the same through the C ABI with host request buffers, wall clock
          (host scheduling, descriptor H2D and token D2H included);
-roofline = the dominant kernel class, timed per launch with CUDA events in
-         a profiled pass over the same iterations;
+roofline = the dominant kernel class, timed per launch on the same path: the
+         timed iterations replayed again with launch stamps (every kernel
+         raises a %globaltimer end stamp; a launch's share is its end minus
+         the previous launch's end), with a CUDA-event pass as a cross-check;
 iteration_roofline = max(weight + K/V bytes at the HBM peak, FLOPs at the
          tensor peak) over the measured iteration time.
 

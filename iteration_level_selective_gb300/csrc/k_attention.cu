@@ -88,17 +88,20 @@ struct TileSmem {
 // ring_stages<D>()-stage shared-memory ring, filled by 1-D bulk copies issued
 // by thread 0 (one per K/V block of the chunk: the keys of a request and head
 // are contiguous in the slot pool, or one run per block of a paged table).
-// One block per chunk and four stages: on GPT-2-small decode, larger chunks
-// or an 8-stage ring (fewer waits per key, more bytes in flight per CTA)
-// measured slower, as the bigger ring halves the CTAs resident per SM and
-// the batch's items then need two waves.
+// One block per chunk; four stages for 64-dim heads: on GPT-2-small decode,
+// larger chunks or an 8-stage ring (fewer waits per key, more bytes in flight
+// per CTA) measured slower, as the bigger ring halves the CTAs resident per SM
+// and the batch's items then need two waves.
 template <int D>
 __host__ __device__ constexpr int chunk_keys() {
   return kKvBlock;
 }
+// 128-dim heads take three stages (50 KB of shared memory): a CTA then fits
+// on an SM next to a tensor-core prompt-attention CTA (168 KB), so a layer's
+// decode rows stream while its prompts run on the tensor cores.
 template <int D>
 __host__ __device__ constexpr int ring_stages() {
-  return 4;
+  return D == 128 ? 3 : 4;
 }
 constexpr int kRingMax = 4;
 

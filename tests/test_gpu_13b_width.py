@@ -8,7 +8,9 @@ sampled requests:
   (iteration 0, ~16k rows), then two new prompts of 1024-2048 tokens run
   next to the 16 decode rows (iteration 1, the mixed shape), then decodes;
 * decode-dominated: 62 requests with 1024-4096 cached tokens and two short
-  ones decode together.
+  ones decode together;
+* a few hundred decode rows (200 short requests), where each Linear takes a
+  different GEMM plan.
 The integer record of every iteration (batch, rows, cached lengths, slots,
 releases, K/V usage) is compared in full with the oracle scheduler; the
 logits of the sampled requests (the short decodes and the shorter new
@@ -93,3 +95,17 @@ def test_13b_width_decode_dominated_iteration(cuda, model):
     recs, worst = _check(model, trace, [trace[0], trace[1]], max_bs=64, n_slots=n_slots, max_rows=sum(ctx) + 64)
     # iteration 1: every request decodes one row against its long context
     assert recs[1].n_new == [1] * 64 and recs[1].n_ctx == ctx
+
+
+def test_13b_width_few_hundred_decode_rows(cuda, model):
+    """200 requests with short prompts decode together: a 200-row iteration,
+    where the QKV and FC1 Linears take the CTA-pair kernel, Attn-Out the
+    single-CTA one and FC2 (a 210 MB weight stream) 256-wide tiles split
+    along K, each with its engine epilogue (K/V scatter, GeLU, residual and
+    the folded LayerNorm statistics)."""
+    rng = np.random.default_rng(34)
+    ctx = [17, 29] + rng.integers(8, 65, 198).tolist()
+    trace = [_req(rng, i, 0, int(c), 2) for i, c in enumerate(ctx)]
+    n_slots = sum(r.max_tokens for r in trace) + 64
+    recs, worst = _check(model, trace, [trace[0], trace[1]], max_bs=256, n_slots=n_slots, max_rows=sum(ctx) + 64)
+    assert recs[1].n_new == [1] * 200 and recs[1].n_ctx == ctx
