@@ -673,7 +673,7 @@ def run_config(args, config, rank, world, local, dev, stream):
 
 
 SUB_KEYS = ("value", "unit", "steps", "ms_per_step", "config", "roofline", "attention_roofline", "kernel_timing",
-            "iteration_roofline", "kernel_roofline", "kernel_ms_per_step", "gpu_launches", "e2e", "clocks",
+            "event_pass", "iteration_roofline", "kernel_roofline", "kernel_ms_per_step", "gpu_launches", "e2e", "clocks",
             "steady_state", "overall", "completed_requests_per_s", "generated_tokens_per_s")
 
 

@@ -820,8 +820,18 @@ constexpr int kPairBM = 2 * BM;                          // output rows of a pai
 constexpr int kPairHalf = BM * BK * 2;                   // one operand half of a stage: 16 KB
 constexpr int kPairStage = 2 * kPairHalf;                // A half + W half
 constexpr int kPairStages = 7;
-constexpr int kPairSmem = kPairStages * kPairStage + 1024 + 256;
+constexpr int kPairSmem = kPairStages * kPairStage + 1024 + 512;
+// 16 KB slots of the ring that the last pair of a shared tile loads the other
+// pieces into (one 32-column run of one piece each), once its ring is idle
+constexpr int kPairRedSlots = kPairStages * kPairStage / (BM * 32 * 4);
 constexpr int kPairGroupM = 16;  // pair tiles per row group (4096 rows; measured best of 4, 8, 16)
+// Pair tiles shared out along K (PairSched): weight streams of at least
+// 128 MB only, ranges of at least 8 k-blocks, and reading back one other
+// pair's piece (a 128 KB fp32 partial per CTA, through L2) counted as 16
+// k-blocks of MMA time.
+constexpr double kPairSplitMinBytes = 128.0 * (1 << 20);
+constexpr int kPairMinRange = 8;
+constexpr int kPairPieceKb = 16;
 // kind::f16, D fp32, A/B bf16 K-major, N = 256, M = 256 (the pair's rows)
 constexpr uint32_t kPairIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPairBN >> 3) << 17) |
                                 ((uint32_t)(kPairBM >> 4) << 24);
@@ -895,16 +905,83 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
   }
 }
 
+// One stretch of work of a pair: k-blocks [kb0, kb1) of output tile `tile`
+// (row tile m, column tile n).  pieces = how many pairs share the tile (1: the
+// pair computes it whole), mine = which of them this pair is in k order.
+struct PairSeg {
+  int m, n, tile, kb0, kb1, pieces, mine, first;
+};
+
 // Pair tiles in groups of kPairGroupM row tiles, so the pairs running at the
-// same time share their W tiles in L2.
+// same time share their W tiles in L2.  P pairs run.  A large weight stream
+// at a few hundred rows leaves most pairs idle in its last wave (the 13B FC1
+// at 200 rows: 80 tiles on 76 pairs, two waves; the FC2: 20 tiles of 320
+// k-blocks on 76 pairs), so its tiles are shared out along K in one of two
+// ways:
+//   kind 1 (split): S pairs per tile, pair p = tile * S + s taking the s-th
+//     of S equal k-ranges (tiles * S <= P);
+//   kind 2 (stream): the W = tiles * KB k-blocks in tile-major order cut into
+//     P equal ranges, pair p taking [p W / P, (p + 1) W / P), so a tile is
+//     shared by the pairs whose ranges meet it (a range's first and last
+//     tiles may be shared, those in between are whole).
+// The cost of either, in k-blocks of one pair's MMA time: its longest range
+// plus kPairPieceKb for each other piece the last pair of a tile reads back;
+// taken when it beats whole tiles by 15%.  A pair keeps a shared piece in
+// slot `unit` (split) or 2p / 2p + 1 (stream: its first / last tile); the
+// last pair to finish a tile sums its pieces in k order, so the result does
+// not depend on which pair finishes last.  Computed identically on the host
+// and by every thread of the kernel.
 struct PairSched {
-  int nM, nN, KB, units;
-  __host__ __device__ void init(int M, int N, int K) {
+  int nM, nN, KB, tiles, P, kind, S, kbs, W;
+  __host__ __device__ void init(int M, int N, int K, int pairs, bool can_split) {
     nM = (M + kPairBM - 1) / kPairBM;
     nN = (N + kPairBN - 1) / kPairBN;
     KB = K / BK;
-    units = nM * nN;
+    tiles = nM * nN;
+    P = pairs;
+    kind = 0;
+    S = 1;
+    kbs = KB;
+    W = 0;
+    if (!can_split || P <= 0 || tiles <= 0 || M <= BM || 2.0 * N * K < kPairSplitMinBytes) return;
+    long long best = (long long)((tiles + P - 1) / P) * KB * 85 / 100;
+    if (tiles * 2 <= P) {
+      int s = min(P / tiles, KB / kPairMinRange);
+      if (s >= 2) {
+        const int k = (KB + s - 1) / s;
+        s = (KB + k - 1) / k;  // no empty range
+        const long long cost = k + (long long)(s - 1) * kPairPieceKb;
+        if (cost < best) {
+          best = cost;
+          kind = 1;
+          S = s;
+          kbs = k;
+        }
+      }
+    }
+    // a stream range walks the row tiles of a column of W one after another,
+    // so W comes from HBM once per row tile: only for one row tile, or when
+    // whole tiles would leave at least 45% of the pairs idle
+    const long long w = (long long)tiles * KB, least = w / P;
+    const bool stream_ok = nM == 1 || (long long)tiles * 100 <= (long long)((tiles + P - 1) / P) * P * 55;
+    if (stream_ok && least >= kPairMinRange) {
+      const long long pieces = (KB + least - 1) / least + 1;  // the most a tile can have
+      const long long cost = (w + P - 1) / P + (pieces - 1) * kPairPieceKb;
+      if (cost < best) {
+        kind = 2;
+        S = 1;
+        kbs = KB;
+        W = (int)w;
+      }
+    }
   }
+  __host__ __device__ bool split() const { return kind != 0; }
+  // pairs that take work (the grid when split)
+  __host__ __device__ int busy() const { return kind == 1 ? tiles * S : kind == 2 ? P : min(tiles, P); }
+  __device__ __forceinline__ long long start(int p) const { return (long long)p * W / P; }
+  // the pair whose stream range holds k-block x (no range is empty: every one
+  // has at least kPairMinRange k-blocks)
+  __device__ __forceinline__ int owner(long long x) const { return (int)(((x + 1) * P + W - 1) / W) - 1; }
   __device__ __forceinline__ void unit(int u, int &m, int &n) const {
     const int group = u / (kPairGroupM * nN);
     const int first_m = group * kPairGroupM;
@@ -913,13 +990,68 @@ struct PairSched {
     m = first_m + r % gm;
     n = r / gm;
   }
+  // segment j of pair p; false past its last
+  __device__ __forceinline__ bool segment(int p, int j, PairSeg &g) const {
+    g.pieces = 1;
+    g.mine = 0;
+    g.first = p;
+    g.kb0 = 0;
+    g.kb1 = KB;
+    if (kind == 0) {
+      g.tile = p + j * P;
+      if (g.tile >= tiles) return false;
+    } else if (kind == 1) {
+      if (j > 0 || p >= tiles * S) return false;
+      g.tile = p / S;
+      g.mine = p - g.tile * S;
+      g.pieces = S;
+      g.first = g.tile * S;
+      g.kb0 = g.mine * kbs;
+      g.kb1 = min(KB, g.kb0 + kbs);
+    } else {
+      const long long b = start(p), e = start(p + 1);
+      const int t0 = (int)(b / KB);
+      const int t = t0 + j;
+      if ((long long)t * KB >= e) return false;
+      g.tile = t;
+      g.kb0 = j == 0 ? (int)(b - (long long)t0 * KB) : 0;
+      g.kb1 = (int)min((long long)KB, e - (long long)t * KB);
+      g.first = owner((long long)t * KB);
+      g.pieces = owner((long long)(t + 1) * KB - 1) - g.first + 1;
+      g.mine = p - g.first;
+    }
+    unit(g.tile, g.m, g.n);
+    return true;
+  }
+  // partial slot of piece i (k order) of a shared tile
+  __device__ __forceinline__ int piece_slot(const PairSeg &g, int i) const {
+    if (kind == 1) return g.first + i;
+    const int q = g.first + i;
+    return 2 * q + (start(q) / KB == g.tile ? 0 : 1);
+  }
+  // arrival counters of a shared tile: [0, 2P) arrivals, [2P, 4P) pieces stored
+  __device__ __forceinline__ int counter(const PairSeg &g, uint32_t rank) const {
+    return 2 * (kind == 1 ? g.tile : g.first) + (int)rank;
+  }
 };
 
+// A split needs four counters per pair (arrivals and pieces stored, per
+// rank) and four partial tiles of 128 x 256 floats per pair (two slots, two
+// ranks).
+__host__ __device__ __forceinline__ bool pair_split_ok(const GemmScratch &scr, int pairs) {
+  return scr.partials != nullptr && scr.counters != nullptr && 4 * pairs <= scr.n_counters &&
+         (size_t)4 * pairs * BM * kPairBN * sizeof(float) <= scr.partial_bytes;
+}
+
 // grid = 2 x pairs, clusters of 2; tmA / tmW: 3-D views with boxes of 128
-// rows x 1 k-block.
+// rows x 1 k-block.  kSplit: tiles may be shared out along K (PairSched);
+// scr: their partials (slot s of CTA rank r at (2 s + r) * 128 * 256 floats,
+// column-major) and arrival counters.  Without kSplit the kernel carries none
+// of that code (the large products, whole tiles only).
+template <bool kSplit>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, int M_arg,
-                        const int32_t *M_dev, int N, int K, EpiParams epi, int32_t *status) {
+                        const int32_t *M_dev, int N, int K, EpiParams epi, GemmScratch scr, int32_t *status) {
   constexpr int ST = kPairStages;
   extern __shared__ uint8_t smem_raw[];
   // the same offsets in both CTAs (same kernel, same static shared memory)
@@ -930,15 +1062,17 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t *empty = full + ST;
   uint64_t *tfull = empty + ST;
   uint64_t *tempty = tfull + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  uint64_t *red = tempty + 2;  // kPairRedSlots
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(red + kPairRedSlots);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *last_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = M_dev != nullptr ? *M_dev : M_arg;  // M_dev: the descriptor header, written before the forward
   const uint32_t rank = cluster_rank();             // 0: leader (issues the MMAs), 1: peer
   const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
   PairSched sc;
-  sc.init(M, N, K);
+  sc.init(M, N, K, npairs, kSplit && pair_split_ok(scr, npairs));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -949,7 +1083,10 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(&tfull[1], 1);
     mbar_init(&tempty[0], 8);
     mbar_init(&tempty[1], 8);
+    if (kSplit)
+      for (int r = 0; r < kPairRedSlots; ++r) mbar_init(&red[r], 1);
     *abort_flag = 0;
+    *last_flag = 0;
     mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
@@ -964,50 +1101,47 @@ __global__ void __launch_bounds__(192, 1)
   cluster_arrive_release();
   cluster_wait_acquire();
 
+  PairSeg g;
   if (warp == 0) {
     if (lane == 0) {  // TMA producer (both CTAs): this CTA's halves, on the leader's full barriers
       const uint32_t full0 = map_to_rank(smem_u32(full), 0);
       const int row_half = (int)rank * BM, col_half = (int)rank * BM;
       int pre = 0;
-      if (pair < sc.units) {  // weights first: they do not depend on earlier kernels
-        int m, n;
-        sc.unit(pair, m, n);
-        pre = min(ST, sc.KB);
+      if (sc.segment(pair, 0, g)) {  // weights first: they do not depend on earlier kernels
+        pre = min(ST, g.kb1 - g.kb0);
         for (int j = 0; j < pre; ++j) {
           if (rank == 0) mbar_expect_tx(&full[j], 2u * kPairStage);
-          tma_load_3d_pair(sB + j * kPairHalf, &tmW, 0, n * kPairBN + col_half, j, full0 + 8u * j);
+          tma_load_3d_pair(sB + j * kPairHalf, &tmW, 0, g.n * kPairBN + col_half, g.kb0 + j, full0 + 8u * j);
         }
       }
       pdl_wait();  // A (activations) comes from earlier kernels
       int it = 0, s = 0;
       uint32_t ph = 0;
-      for (int u = pair; u < sc.units; u += npairs) {
-        int m, n;
-        sc.unit(u, m, n);
-        for (int kb = 0; kb < sc.KB; ++kb, ++it, s = s + 1 == ST ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
+      for (int j = 0; sc.segment(pair, j, g); ++j) {
+        for (int kb = g.kb0; kb < g.kb1; ++kb, ++it, s = s + 1 == ST ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
           const uint32_t bar = full0 + 8u * (uint32_t)s;
           if (it < pre) {  // W already requested
-            tma_load_3d_pair(sA + s * kPairHalf, &tmA, 0, m * kPairBM + row_half, kb, bar);
+            tma_load_3d_pair(sA + s * kPairHalf, &tmA, 0, g.m * kPairBM + row_half, kb, bar);
             continue;
           }
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status) || *abort_flag) continue;
           if (rank == 0) mbar_expect_tx(&full[s], 2u * kPairStage);
-          tma_load_3d_pair(sA + s * kPairHalf, &tmA, 0, m * kPairBM + row_half, kb, bar);
-          tma_load_3d_pair(sB + s * kPairHalf, &tmW, 0, n * kPairBN + col_half, kb, bar);
+          tma_load_3d_pair(sA + s * kPairHalf, &tmA, 0, g.m * kPairBM + row_half, kb, bar);
+          tma_load_3d_pair(sB + s * kPairHalf, &tmW, 0, g.n * kPairBN + col_half, kb, bar);
         }
       }
       if (*abort_flag) drain_after_abort();  // copies issued before the abort land first
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {  // MMA issuer (leader)
-      int i = 0, s = 0;
+      int s = 0;
       uint32_t ph = 0;
-      for (int u = pair; u < sc.units; u += npairs, ++i) {
+      for (int i = 0; sc.segment(pair, i, g); ++i) {
         const int acc = i & 1;
         const uint32_t d_tmem = tmem + (uint32_t)(acc * kPairBN);
         mbar_wait_cluster(&tempty[acc], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, status);
         tc_fence_after();
-        for (int kb = 0; kb < sc.KB; ++kb, s = s + 1 == ST ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
+        for (int kb = g.kb0; kb < g.kb1; ++kb, s = s + 1 == ST ? 0 : s + 1, ph ^= s == 0 ? 1u : 0u) {
           if (mbar_wait(&full[s], ph, abort_flag, status)) {
             tc_fence_after();
             const uint32_t a0 = smem_u32(sA + s * kPairHalf);
@@ -1015,7 +1149,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
               tc_mma_pair(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), kPairIdesc,
-                          (kb > 0 || k > 0) ? 1u : 0u);
+                          (kb > g.kb0 || k > 0) ? 1u : 0u);
           }
           tc_commit_pair(&empty[s]);
         }
@@ -1025,31 +1159,186 @@ __global__ void __launch_bounds__(192, 1)
   } else {  // epilogue warps 2..5 (both CTAs): TMEM lane quarter = warp % 4
     const int q = warp & 3;
     const uint32_t tempty0 = map_to_rank(smem_u32(tempty), 0);
-    int i = 0;
-    for (int u = pair; u < sc.units; u += npairs, ++i) {
-      int m, n;
-      sc.unit(u, m, n);
+    for (int i = 0; sc.segment(pair, i, g); ++i) {
       const int acc = i & 1;
-      float bl_next = n * kPairBN < N ? run_bias(epi, n * kPairBN, min(32, N - n * kPairBN)) : 0.f;
+      float bl_next = g.n * kPairBN < N ? run_bias(epi, g.n * kPairBN, min(32, N - g.n * kPairBN)) : 0.f;
       if (i == 0) pdl_wait();  // the epilogue reads / writes buffers of earlier kernels (x, K/V slots)
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], (uint32_t)(i >> 1) & 1u, abort_flag, status));
       tc_fence_after();
-      const int row = m * kPairBM + (int)rank * BM + q * 32 + lane;
+      const int row = g.m * kPairBM + (int)rank * BM + q * 32 + lane;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPairBN);
       unsigned long long best = 0ull;
+      if (g.pieces == 1) {
 #pragma unroll 1
-      for (int c = 0; c < kPairBN; c += 32) {
-        float v[32];
-        if (ok) tmem_ld32(tbase + (uint32_t)c, v);
-        if (c + 32 == kPairBN) {  // the accumulator is read: free it for the leader's next tile
+        for (int c = 0; c < kPairBN; c += 32) {
+          float v[32];
+          if (ok) tmem_ld32(tbase + (uint32_t)c, v);
+          if (c + 32 == kPairBN) {  // the accumulator is read: free it for the leader's next tile
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
+          }
+          const int col = g.n * kPairBN + c;
+          const float bl = bl_next;
+          if (c + 32 < kPairBN && col + 32 < N) bl_next = run_bias(epi, col + 32, min(32, N - col - 32));
+          if (ok && col < N) finish_run(epi, row, col, v, min(32, N - col), row < M, best, bl);
+        }
+      } else if constexpr (kSplit) {
+        // a tile shared by g.pieces pairs.  Each counts itself in once its
+        // accumulator is ready; all but the last to do so store their piece
+        // (column-major: a warp's 32 rows are 128 contiguous bytes) and count
+        // it stored; the last waits for those stores - their pairs are
+        // already running, nothing they do waits - and sums the pieces in
+        // k order, its own straight from tensor memory.
+        int32_t *arrived = scr.counters + sc.counter(g, rank);
+        int32_t *stored = arrived + 2 * sc.P;
+        epi_barrier();
+        if (threadIdx.x == 64) *last_flag = atomicAdd(arrived, 1) == g.pieces - 1;
+        epi_barrier();
+        const bool last = *last_flag != 0;
+        if (!last) {
+          float *part = scr.partials + (size_t)(2 * sc.piece_slot(g, g.mine) + (int)rank) * BM * kPairBN + q * 32 + lane;
+#pragma unroll 1
+          for (int c = 0; c < kPairBN; c += 32) {
+            float v[32];
+            if (ok) tmem_ld32(tbase + (uint32_t)c, v);
+            if (ok && row < M) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) __stcg(part + (size_t)(c + j) * BM, v[j]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
+          __threadfence();
+          epi_barrier();
+          if (threadIdx.x == 64) atomicAdd(stored, 1);
+        } else {
+          if (threadIdx.x == 64) {
+            bool got = true;
+            const uint64_t t0 = global_ns();
+            while (*reinterpret_cast<volatile int32_t *>(stored) < g.pieces - 1) {
+              if (*abort_flag || global_ns() - t0 > 2000000000ull) {
+                *abort_flag = 1;
+                atomicOr(status, kStatusWaitTimeout);
+                got = false;
+                break;
+              }
+            }
+            *last_flag = got ? 1 : 2;
+          }
+          epi_barrier();
+          const bool all_in = *last_flag == 1;  // the same in every epilogue warp
+          const bool sum_ok = ok && all_in;
+          __threadfence();  // the stored pieces, counted before, are read below
+          if (threadIdx.x == 64) {
+            *arrived = 0;
+            *stored = 0;
+          }
+          PairSeg nx;
+          if (all_in && !sc.segment(pair, i + 1, nx)) {
+            // this pair's last segment: its MMAs are done, so the ring is idle.
+            // The other pieces come in by bulk copies, R runs of 32 columns at
+            // a time (one 16 KB slot per run and piece), all in flight together
+            const int others = g.pieces - 1;
+            const int R = min(kPairBN / 32, kPairRedSlots / others);
+            for (int c0 = 0, round = 0; c0 < kPairBN / 32; c0 += R, ++round) {
+              const int nc = min(R, kPairBN / 32 - c0);
+              if (round > 0) {
+                epi_barrier();  // the previous round's slots are read
+                if (threadIdx.x == 64) fence_proxy_async_cta();
+              }
+              if (threadIdx.x == 64) {
+                for (int cc = 0; cc < nc; ++cc)
+                  for (int o = 0; o < others; ++o) {
+                    const int pc = o < g.mine ? o : o + 1;
+                    const int slot = cc * others + o;
+                    mbar_expect_tx(&red[slot], BM * 32 * 4);
+                    bulk_load(sA + (size_t)slot * (BM * 32 * 4),
+                              scr.partials + (size_t)(2 * sc.piece_slot(g, pc) + (int)rank) * BM * kPairBN +
+                                  (size_t)(c0 + cc) * 32 * BM,
+                              BM * 32 * 4, &red[slot]);
+                  }
+              }
+#pragma unroll 1
+              for (int cc = 0; cc < nc; ++cc) {
+                const int c = (c0 + cc) * 32;
+                const int col = g.n * kPairBN + c;
+                bool in = true;
+                for (int o = 0; o < others; ++o) in = mbar_wait(&red[cc * others + o], (uint32_t)round & 1u, abort_flag, status) && in;
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+#pragma unroll 1
+                for (int pc = 0; pc < g.pieces; ++pc) {
+                  float t[32];
+                  if (pc == g.mine) {
+                    if (ok) tmem_ld32(tbase + (uint32_t)c, t);
+                    else {
+#pragma unroll
+                      for (int j = 0; j < 32; ++j) t[j] = 0.f;
+                    }
+                  } else {
+                    const float *src = reinterpret_cast<const float *>(
+                                           sA + (size_t)(cc * others + (pc < g.mine ? pc : pc - 1)) * (BM * 32 * 4)) +
+                                       q * 32 + lane;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) t[j] = src[j * BM];
+                  }
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) v[j] += t[j];
+                }
+                if (sum_ok && in && col < N)
+                  finish_run(epi, row, col, v, min(32, N - col), row < M, best, run_bias(epi, col, min(32, N - col)));
+              }
+            }
+          } else {
+#pragma unroll 1
+          for (int c = 0; c < kPairBN; c += 32) {
+            const int col = g.n * kPairBN + c;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            // the pieces in k order, two at a time (up to 64 loads in flight)
+#pragma unroll 1
+            for (int pc = 0; pc < g.pieces; pc += 2) {
+              const bool two = pc + 1 < g.pieces;
+              float t0[32], t1[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) t0[j] = t1[j] = 0.f;
+              if (pc == g.mine) {
+                if (ok) tmem_ld32(tbase + (uint32_t)c, t0);
+              } else if (sum_ok && row < M) {
+                const float *src = scr.partials + (size_t)(2 * sc.piece_slot(g, pc) + (int)rank) * BM * kPairBN +
+                                   (size_t)c * BM + q * 32 + lane;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) t0[j] = __ldcg(src + (size_t)j * BM);
+              }
+              if (two) {
+                if (pc + 1 == g.mine) {
+                  if (ok) tmem_ld32(tbase + (uint32_t)c, t1);
+                } else if (sum_ok && row < M) {
+                  const float *src = scr.partials + (size_t)(2 * sc.piece_slot(g, pc + 1) + (int)rank) * BM * kPairBN +
+                                     (size_t)c * BM + q * 32 + lane;
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) t1[j] = __ldcg(src + (size_t)j * BM);
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] += t0[j];
+              if (two) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += t1[j];
+              }
+            }
+            if (sum_ok && col < N)
+              finish_run(epi, row, col, v, min(32, N - col), row < M, best, run_bias(epi, col, min(32, N - col)));
+          }
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
         }
-        const int col = n * kPairBN + c;
-        const float bl = bl_next;
-        if (c + 32 < kPairBN && col + 32 < N) bl_next = run_bias(epi, col + 32, min(32, N - col - 32));
-        if (ok && col < N) finish_run(epi, row, col, v, min(32, N - col), row < M, best, bl);
       }
       if (epi.argmax_keys != nullptr && best != 0ull) atomicMax(epi.argmax_keys + row, best);
     }
@@ -1135,22 +1424,28 @@ cudaError_t launch_bn(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, con
 cudaError_t set_pair_smem_limit(int dev) {
   static uint64_t attr_mask = 0;
   if (dev >= 64 || !(attr_mask & (1ull << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tc_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_mask |= 1ull << dev;
   }
   return cudaSuccess;
 }
 
-// Persistent pairs: at most one pair per two SMs (with M_dev the grid is
-// fixed, the device decides how many units there are).
+// Persistent pairs: at most one pair per two SMs; every pair when the tiles
+// are split (with M_dev the grid is fixed, the device decides the work: a
+// grid of fewer pairs than tiles would decide the same on the device).
+// split: the plan shares tiles out along K at this M (the kernel that can).
 cudaError_t launch_pair(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, const int32_t *M_dev, int N, int K,
-                        const EpiParams &epi, int32_t *status, cudaStream_t st, int sm, int dev) {
+                        const EpiParams &epi, const GemmScratch &scr, bool split, int32_t *status, cudaStream_t st,
+                        int sm, int dev) {
   cudaError_t e = set_pair_smem_limit(dev);
   if (e != cudaSuccess) return e;
   PairSched sc;
-  sc.init(M, N, K);
-  const int pairs = M_dev != nullptr ? sm / 2 : (sc.units < sm / 2 ? sc.units : sm / 2);
+  sc.init(M, N, K, sm / 2, split && pair_split_ok(scr, sm / 2));
+  const int pairs = M_dev != nullptr || sc.split() ? sm / 2 : sc.busy();
   if (pairs <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * pairs);
@@ -1166,7 +1461,8 @@ cudaError_t launch_pair(const CUtensorMap *tmA, const CUtensorMap *tmW, int M, c
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, *tmA, *tmW, M, M_dev, N, K, epi, status);
+  return cudaLaunchKernelEx(&cfg, split ? gemm_tc_pair_kernel<true> : gemm_tc_pair_kernel<false>, *tmA, *tmW, M,
+                            M_dev, N, K, epi, scr, status);
 }
 
 }  // namespace
@@ -1182,7 +1478,8 @@ int gemm_sm_count() {
   return n;
 }
 
-// Products of at least this many rows may take the CTA-pair kernel (gemm_plan).
+// Below this many rows a large weight stream may take 256-wide single-CTA
+// tiles split along K (gemm_tile_n).
 constexpr int kPairMinRows = 512;
 // Weight streams at least this large, at a few hundred rows, take 256-wide
 // tiles split along K.  Measured on GB300 at 200-256 rows: the 13B FC2 (210 MB)
@@ -1244,20 +1541,35 @@ double load_us(double bytes) { return 0.45 + bytes / 115e3; }
 // K = 768 the persistent kernel was faster for every N of GPT-2 small, with
 // K = 3072 the cluster kernel by 30-40%.)
 constexpr int kClusterMinKb = 32;
-// The CTA-pair kernel takes products of at least 512 rows whose 256 x 256
-// tiles give every pair of SMs one at least, and products of 129..511 rows
-// with at least 48 pair tiles across N (N >= 12288: the 13B QKV, FC1 and LM
-// head).  Measured on GB300 against the single-CTA kernel: at 200-256 rows
-// the pair kernel is 20-25% faster for N = 15360 and 20480 and slower for
-// N = 5120 (20 pair tiles leave most pairs idle); GPT-2-small's prompt
-// iterations (600 rows, N <= 3072) lost 4% on it.
-constexpr int kPairMinRowsWide = 129;
-constexpr int kPairWideN = 12288;
-GemmPlan gemm_plan(int M, int N, int K) {
+// Products of more than one row tile take the CTA-pair kernel when its tiles
+// are shared out along K (PairSched), else the kernel with the lower estimate
+// of its whole waves: waves x K-blocks x the time of one k-block of a tile,
+// for a pair's 256 x 256 tile 1, for the single CTA's 128 x bn tile
+// kSingleKb x (its operand bytes per k-block, A 16 KB + W bn x 128 B) / 48 KB
+// - at bn = 256 the single CTA reaches 71% tensor-pipe activity against the
+// pair's 84% (both operand-bound).  Measured on GB300 over the 13B Linears at
+// 200-3000 rows (all 52 shapes) this picks the faster of the two every time:
+// e.g. the Attn-Out at 512-768 rows 15-19% and the FC2 36% faster on pairs (one
+// wave of 60 pair tiles against two of single-CTA tiles), the FC1 at 300-384
+// and the QKV at 600 rows 10% faster on single CTAs (2 waves against 3).
+constexpr double kSingleKb = 1.18;
+static double single_waves_cost(int M, int N, int K) {
+  const int bn = gemm_tile_n(M, N, K);
+  const long long tiles = (long long)((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  const long long waves = (tiles + gemm_sm_count() - 1) / gemm_sm_count();
+  return (double)waves * (K / BK) * kSingleKb * (16.0 + bn / 8.0) / 48.0;
+}
+GemmPlan gemm_plan(int M, int N, int K, bool split_scratch) {
   GemmPlan p{};
   const long long pair_tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
-  if ((M >= kPairMinRows && pair_tiles >= gemm_sm_count() / 2) || (M >= kPairMinRowsWide && N >= kPairWideN)) {
-    p.pair = true;
+  if (M > BM && K % BK == 0) {
+    PairSched ps;
+    ps.init(M, N, K, gemm_sm_count() / 2, split_scratch);
+    const long long pair_waves = (pair_tiles + gemm_sm_count() / 2 - 1) / (gemm_sm_count() / 2);
+    p.split = ps.split();
+    p.pair = p.split || (double)pair_waves * (K / BK) < single_waves_cost(M, N, K);
+  }
+  if (p.pair) {
     p.bn = kPairBN;
     return p;
   }
@@ -1299,10 +1611,10 @@ GemmPlan gemm_plan(int M, int N, int K) {
 
 // A small integer naming the plan, below 64: callers pack one per Linear
 // into 6 bits of their CUDA-graph keys (persistent 0..7, cluster 8..39,
-// CTA pair 40).
+// CTA pair 40, CTA pair with tiles shared out along K 41).
 int gemm_plan_code(int M, int N, int K) {
-  const GemmPlan p = gemm_plan(M, N, K);
-  if (p.pair) return 40;
+  const GemmPlan p = gemm_plan(M, N, K, true);
+  if (p.pair) return p.split ? 41 : 40;
   if (!p.cluster) return bn_code(p.bn) * 2 + (p.a_box == 64 ? 1 : 0);
   return 8 + bn_code(p.bn) * 8 + (p.S == 2 ? 0 : p.S == 4 ? 1 : 2) * 2 + (p.a_box == 64 ? 1 : 0);
 }
@@ -1341,8 +1653,8 @@ cudaError_t launch_gemm_tc_bf16(const OperandMaps &A, const OperandMaps &W, int 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const int sm = gemm_sm_count();
-  const GemmPlan p = gemm_plan(M, N, K);
-  if (p.pair) return launch_pair(A.get(BM, 1), W.get(BM, 1), M, M_dev, N, K, epi, status, st, sm, dev);
+  const GemmPlan p = gemm_plan(M, N, K, pair_split_ok(scr, sm / 2));
+  if (p.pair) return launch_pair(A.get(BM, 1), W.get(BM, 1), M, M_dev, N, K, epi, scr, p.split, status, st, sm, dev);
   if (p.cluster) {
     switch (p.bn) {
       case 256: return launch_cluster<256>(A, W, M, M_dev, N, K, p.S, p.kbs, p.a_box, epi, status, st, dev);

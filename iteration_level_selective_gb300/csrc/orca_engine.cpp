@@ -35,8 +35,12 @@ using namespace orca;
 namespace {
 
 constexpr int kMinSplit = 256;   // keys per decode split, at least
-constexpr int kGemmMaxSms = 192;  // split-K GEMM: counters (and partial tiles up to one per SM)
-constexpr size_t kGemmPartialBytes = (size_t)kGemmMaxSms * 128 * 256 * 4;
+// split-K GEMM: counters (one per split tile of the single-CTA kernel, two
+// per CTA of the CTA-pair kernel) and fp32 partial tiles of 128 x 256 - up to
+// one per SM for the single-CTA kernel, two per SM for the CTA-pair kernel
+constexpr int kGemmMaxSms = 192;
+constexpr int kGemmCounters = 4 * kGemmMaxSms;
+constexpr size_t kGemmPartialBytes = (size_t)2 * kGemmMaxSms * 128 * 256 * 4;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -225,7 +229,7 @@ Layout make_layout(const orca_config *c) {
   }
   L.part = take((size_t)B * kMaxSplits * c->n_heads * (d + 2) * 4);
   L.counters = take((B * c->n_heads + 4) * 4);  // split arrivals, then two work tickets
-  L.gemm_cnt = take(kGemmMaxSms * 4);
+  L.gemm_cnt = take(kGemmCounters * 4);
   L.gemm_part = take(kGemmPartialBytes);
   const bool fold = c->dtype == ORCA_DTYPE_BF16;
   L.xb = take(fold ? R * H * 2 : 0);
@@ -585,7 +589,7 @@ int enqueue_forward(orca_engine *e, cudaStream_t st, const FwdSizes &z, float *l
   int32_t *status = reinterpret_cast<int32_t *>(d_out);
   unsigned long long *d_keys = d_out + 1;
   GemmScratch scr{ws_ptr<float>(e, Ly.gemm_part), kGemmPartialBytes, ws_ptr<int32_t>(e, Ly.gemm_cnt),
-                  std::min(kGemmMaxSms, gemm_sm_count())};
+                  4 * std::min(kGemmMaxSms, gemm_sm_count())};
   float *x = ws_ptr<float>(e, Ly.x);
   void *h = e->ws + Ly.h;
   void *q = e->ws + Ly.q;
@@ -928,7 +932,7 @@ int orca_engine_create(const orca_config *cfg, const void *const *weights, int32
     if (ok) S.h_req = reinterpret_cast<ReqInfo *>(S.h_hdr + 1);
   }
   ok = ok && cudaMemset(e->ws + L.counters, 0, ((size_t)cfg->max_bs * cfg->n_heads + 4) * 4) == cudaSuccess &&
-       cudaMemset(e->ws + L.gemm_cnt, 0, kGemmMaxSms * 4) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
+       cudaMemset(e->ws + L.gemm_cnt, 0, kGemmCounters * 4) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
   if (ok)
     ok = gemm_prepare() == cudaSuccess && attention_prepare() == cudaSuccess && attention_tc_prepare() == cudaSuccess;
   if (!ok) {
@@ -1690,13 +1694,13 @@ int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const
   }
   if (K % kTcBK) return ORCA_EINVAL;
   GemmScratch scr{nullptr, 0, nullptr, 0};
-  const size_t cnt_bytes = align_up(kGemmMaxSms * 4, 256);
+  const size_t cnt_bytes = align_up(kGemmCounters * 4, 256);
   if (scratch && scratch_bytes > cnt_bytes && !(reinterpret_cast<uintptr_t>(scratch) & 255)) {
     scr.counters = static_cast<int32_t *>(scratch);
-    scr.n_counters = std::min(kGemmMaxSms, gemm_sm_count());
+    scr.n_counters = 4 * std::min(kGemmMaxSms, gemm_sm_count());
     scr.partials = reinterpret_cast<float *>(static_cast<char *>(scratch) + cnt_bytes);
     scr.partial_bytes = scratch_bytes - cnt_bytes;
-    if (cudaMemsetAsync(scratch, 0, kGemmMaxSms * 4, st) != cudaSuccess) return ORCA_ECUDA;
+    if (cudaMemsetAsync(scratch, 0, kGemmCounters * 4, st) != cudaSuccess) return ORCA_ECUDA;
   }
   if (argmax_keys_dev && cudaMemsetAsync(argmax_keys_dev, 0, (size_t)M * 8, st) != cudaSuccess) return ORCA_ECUDA;
   OperandMaps ta, tw;

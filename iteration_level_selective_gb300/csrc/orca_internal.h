@@ -243,11 +243,15 @@ struct OperandMaps {
 // split-K kernel with S CTAs per output tile, kbs k-blocks each, A boxes of
 // a_box rows); gemm_plan_code is a small integer unique per plan.
 struct GemmPlan {
-  bool pair = false;  // CTA-pair kernel (256 x 256 tiles, cta_group::2)
+  bool pair = false;   // CTA-pair kernel (256 x 256 tiles, cta_group::2)
+  bool split = false;  // ... with its tiles shared out along K
   bool cluster = false;
   int bn = 128, S = 1, kbs = 0, a_box = 128, ks = 1;
 };
-GemmPlan gemm_plan(int M, int N, int K);
+// split_scratch: the launch will have scratch enough for the CTA-pair
+// kernel's split tiles (the engine's always has).
+GemmPlan gemm_plan(int M, int N, int K, bool split_scratch);
+// The plan as a small integer (CUDA-graph keys), for launches with scratch.
 int gemm_plan_code(int M, int N, int K);
 cudaError_t launch_gemm_tc_bf16(const OperandMaps &A, const OperandMaps &W, int M, const int32_t *M_dev, int N,
                                 int K, const EpiParams &epi, const GemmScratch &scratch, int32_t *status,

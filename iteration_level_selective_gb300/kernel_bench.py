@@ -242,7 +242,7 @@ def main():
         print(json.dumps(time_linear(a.M, a.N, a.K, a.reps, a.warmup)))
     elif a.cmd == "linear-13b":
         # the 13B Linears (QKV, Attn-Out, FC1, FC2) at the row counts of decode-heavy iterations
-        for M in (1, 64, 128, 200, 256, 384, 512, 1024, 2048, 24373):
+        for M in (1, 64, 128, 200, 256, 300, 384, 512, 700, 1024, 2048, 24373):
             for (N, K) in ((15360, 5120), (5120, 5120), (20480, 5120), (5120, 20480), (50257, 5120)):
                 if M == 24373 and N == 50257:
                     continue

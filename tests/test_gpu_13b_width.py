@@ -99,13 +99,28 @@ def test_13b_width_decode_dominated_iteration(cuda, model):
 
 def test_13b_width_few_hundred_decode_rows(cuda, model):
     """200 requests with short prompts decode together: a 200-row iteration,
-    where the QKV and FC1 Linears take the CTA-pair kernel, Attn-Out the
-    single-CTA one and FC2 (a 210 MB weight stream) 256-wide tiles split
-    along K, each with its engine epilogue (K/V scatter, GeLU, residual and
-    the folded LayerNorm statistics)."""
+    where the QKV Linear takes whole CTA-pair tiles, Attn-Out the single-CTA
+    kernel, FC1 pair tiles in stream ranges along K and FC2 (K = 20480)
+    three equal k-ranges per pair tile, each with its engine epilogue (K/V
+    scatter, GeLU, residual and the folded LayerNorm statistics)."""
     rng = np.random.default_rng(34)
     ctx = [17, 29] + rng.integers(8, 65, 198).tolist()
     trace = [_req(rng, i, 0, int(c), 2) for i, c in enumerate(ctx)]
     n_slots = sum(r.max_tokens for r in trace) + 64
     recs, worst = _check(model, trace, [trace[0], trace[1]], max_bs=256, n_slots=n_slots, max_rows=sum(ctx) + 64)
     assert recs[1].n_new == [1] * 200 and recs[1].n_ctx == ctx
+
+
+def test_13b_width_decodes_beside_a_prompt(cuda, model):
+    """250 decode rows and a 600-token prompt in one iteration (850 rows):
+    the FC2 Linear (K = 20480) takes CTA-pair tiles in stream ranges along K
+    (the residual with the folded LayerNorm statistics on summed pieces),
+    the other Linears whole pair tiles."""
+    rng = np.random.default_rng(35)
+    ctx = [21, 33] + rng.integers(8, 49, 248).tolist()
+    trace = [_req(rng, i, 0, int(c), 2) for i, c in enumerate(ctx)]
+    trace.append(_req(rng, 250, 1, 600, 2))
+    n_slots = sum(r.max_tokens for r in trace) + 64
+    recs, worst = _check(model, trace, [trace[0], trace[1], trace[250]], max_bs=256, n_slots=n_slots,
+                         max_rows=sum(ctx) + 64)
+    assert sorted(recs[1].n_new) == [1] * 250 + [600]

@@ -63,15 +63,19 @@ def test_argmax_forced_logits_bit_exact(cuda):
                                    # few narrow tiles with a 1 MB weight block each: split-K over the
                                    # persistent kernel when a scratch buffer is given
                                    (200, 520, 16384),
-                                   # CTA-pair kernel (>= 512 rows and a tile per pair, or >= 129 rows and
-                                   # N >= 12288; 256 x 256 tiles over two SMs): ragged last pair tile (one
-                                   # row in the leader, none in the peer), a single k-block with ragged N,
-                                   # vocab-wide ragged N, a long K, wide N and K
-                                   (513, 20480, 256), (1024, 20000, 64), (777, 50257, 1024), (300, 12288, 4096),
+                                   # CTA-pair kernel (256 x 256 tiles over two SMs, when its waves beat the
+                                   # single CTA's): ragged last pair tile (one row in the leader, none in the
+                                   # peer), a single k-block with ragged N, vocab-wide ragged N, a long K;
+                                   # wide N and K on single CTAs (two waves against three)
+                                   (513, 5120, 512), (1024, 20000, 64), (777, 50257, 1024), (300, 12288, 4096),
                                    (1500, 4096, 5120), (200, 15360, 512),
-                                   # 129..511 rows and a weight stream of >= 128 MB with N < 12288: 256-wide
-                                   # tiles split along K when a scratch buffer is given (2-3 splits)
-                                   (200, 5120, 5120), (300, 4096, 16384)])
+                                   # a weight stream of >= 128 MB at a few hundred rows: CTA-pair tiles
+                                   # shared out along K when a scratch buffer is given (without one: whole
+                                   # pair tiles, or 256-wide single-CTA tiles) - 2 and 3 equal k-ranges per
+                                   # tile (ragged N and K), stream ranges over 79 tiles with 2 pieces a tile
+                                   # (ragged N), over 40 tiles in two ragged rows with up to 3 pieces
+                                   (200, 5120, 5120), (300, 4096, 16384), (200, 5000, 13440), (250, 20000, 4096),
+                                   (300, 5000, 13440)])
 @pytest.mark.parametrize("mode", ["store", "gelu", "resid", "f32out"])
 @pytest.mark.parametrize("split", [False, True])
 def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode, split):
@@ -111,7 +115,9 @@ def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode, split):
     assert err < tol, err
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 50257, 768), (64, 50257, 768), (200, 1000, 256), (7, 300, 64)])
+@pytest.mark.parametrize("M,N,K", [(1, 50257, 768), (64, 50257, 768), (200, 1000, 256), (7, 300, 64),
+                                   # CTA-pair tiles shared out along K in stream ranges
+                                   (250, 20000, 4096)])
 def test_fused_argmax_matches_argmax_of_stored_logits(cuda, M, N, K):
     """The LM head's fused greedy choice equals the argmax of the same
     call's fp32 logits, bit for bit (lowest index on ties)."""

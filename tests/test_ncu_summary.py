@@ -72,3 +72,5 @@ def test_short_name_of_the_names_ncu_prints():
         "ln_fold_vectors_kernel"
     assert ns.short_name("void orca::<unnamed>::gemm_tc_pair_kernel(CUtensorMap_st, CUtensorMap_st, int)") == \
         "gemm_tc_pair_kernel"
+    assert ns.short_name("void orca::<unnamed>::gemm_tc_pair_kernel<true>(CUtensorMap_st, CUtensorMap_st, int)") == \
+        "gemm_tc_pair_kernel"
