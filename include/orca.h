@@ -356,6 +356,42 @@ int orca_linear(int32_t dtype, int32_t mode, const void *A, const void *W, const
                 int32_t M, int32_t N, int32_t K, void *scratch, size_t scratch_bytes, void *argmax_keys_dev,
                 int32_t *status_dev, void *stream);
 
+/* How a bf16 token-wise Linear (orca_linear, and every Linear of an
+ * iteration) is planned on a GPU of n_sms SMs, computed on the host by the
+ * planner the launches use; no device is touched.  The pages have no
+ * counterpart: this is a view of the library's own GEMM planning (which
+ * kernel, which tiles, whether tiles are shared out along K) for tests and
+ * tools.  with_scratch: the launch has the split scratch the engine gives
+ * every Linear (orca_linear: a scratch buffer of at least 3 KB + n_sms / 2 x
+ * 512 KB, about 40 MB on 152 SMs).
+ * M, N, K > 0, K % 64 == 0, 2 <= n_sms <= 4096, out != NULL, else
+ * ORCA_EINVAL. */
+typedef struct {
+  int32_t kernel;  /* 0 persistent single-CTA tiles, 1 cluster split-K, 2 CTA pairs */
+  int32_t tile_m, tile_n; /* output tile: 128 x tile_n, or 256 x 256 for CTA pairs */
+  int32_t tiles;   /* output tiles */
+  int32_t k_split; /* CTA pairs: 0 whole tiles, 1 equal k-ranges per tile, 2 stream ranges */
+  int32_t ranges;  /* k-ranges per tile (cluster S; pairs kind 1: S), or the pairs the
+                      stream is cut among (kind 2); else 1 */
+  int32_t workers; /* CTAs (kernels 0, 1) or CTA pairs (kernel 2) that take work */
+  int32_t code;    /* the plan's small integer (below 64; engine CUDA-graph keys) */
+} orca_gemm_plan_info;
+int orca_gemm_plan_query(int32_t M, int32_t N, int32_t K, int32_t n_sms, int32_t with_scratch,
+                         orca_gemm_plan_info *out);
+
+/* The work of CTA pair `pair` of n_pairs in the CTA-pair GEMM of an M x N x K
+ * product, in the order the pair runs it (with_split: tiles may be shared out
+ * along K, as with the engine's scratch).  Writes up to max_seg rows of 9
+ * int32 into seg (caller-owned): {tile, row tile, column tile, first k-block,
+ * end k-block, pairs sharing the tile, this pair's place among them in k
+ * order, the shared tile's counter pair (-1 when whole), this piece's partial
+ * slot (-1 when whole)}, and returns the number of segments (which may exceed
+ * max_seg), or ORCA_EINVAL for M, N, K <= 0, K % 64 != 0, n_pairs <= 0, pair
+ * outside [0, n_pairs), max_seg < 0, or seg == NULL with max_seg > 0.  The
+ * pages have no counterpart (as orca_gemm_plan_query). */
+int orca_gemm_pair_segments(int32_t M, int32_t N, int32_t K, int32_t n_pairs, int32_t with_split, int32_t pair,
+                            int32_t *seg, int32_t max_seg);
+
 /* Ragged attention of one layer on its own (Figure 5: each request's
  * queries against its own K/V slots, rows split and merged in place).
  * Batch on the host: request i owns rows row_off[i] .. row_off[i+1]-1

@@ -66,13 +66,19 @@ class orca_kernel_stats(ctypes.Structure):
                 ("bytes", ctypes.c_double)]
 
 
+class orca_gemm_plan_info(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("tiles", ctypes.c_int32), ("k_split", ctypes.c_int32), ("ranges", ctypes.c_int32),
+                ("workers", ctypes.c_int32), ("code", ctypes.c_int32)]
+
+
 EXPORTS = ("orca_kv_pool_bytes", "orca_workspace_bytes", "orca_weight_count", "orca_engine_create",
            "orca_engine_destroy", "orca_kv_reserve", "orca_kv_release", "orca_kv_stats", "orca_select_batch",
            "orca_iteration", "orca_last_descriptor", "orca_argmax_rows", "orca_profile_enable",
            "orca_profile_read", "orca_last_error", "orca_linear", "orca_last_transfer",
            "orca_attention_workspace_bytes", "orca_attention", "orca_attention_noalloc", "orca_last_launches",
            "orca_select_batch_budget", "orca_kv_usage", "orca_iteration_submit", "orca_iteration_wait",
-           "orca_selftest_wait_timeout")
+           "orca_selftest_wait_timeout", "orca_gemm_plan_query", "orca_gemm_pair_segments")
 
 _lib = None
 
@@ -116,6 +122,8 @@ def lib() -> ctypes.CDLL:
             "orca_attention": [c_i32, c_i32, c_i32, c_i64, P, P, P, P, c_i32, i32p, i32p, i64p, P, c_sz, P, P],
             "orca_attention_noalloc": [c_i32, c_i32, c_i32, c_i64, P, P, P, P, c_i32, i32p, i32p, i64p, P, P],
             "orca_selftest_wait_timeout": [P, P],
+            "orca_gemm_plan_query": [c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(orca_gemm_plan_info)],
+            "orca_gemm_pair_segments": [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, i32p, c_i32],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -313,6 +321,28 @@ def argmax_key_column(key: int) -> int:
     """Column of a packed greedy-choice key (see orca_linear), -1 for none."""
     key = int(key) & 0xFFFFFFFFFFFFFFFF
     return -1 if key == 0 else 0xFFFFFFFF - (key & 0xFFFFFFFF)
+
+
+def orca_gemm_plan_query(M: int, N: int, K: int, n_sms: int, with_scratch: bool = True) -> dict:
+    """How the library plans a bf16 M x N x K Linear on a GPU of n_sms SMs
+    (host only; see orca.h)."""
+    r = orca_gemm_plan_info()
+    _check(lib().orca_gemm_plan_query(M, N, K, n_sms, int(bool(with_scratch)), ctypes.byref(r)))
+    return {k: getattr(r, k) for k, _ in orca_gemm_plan_info._fields_}
+
+
+def orca_gemm_pair_segments(M: int, N: int, K: int, n_pairs: int, with_split: bool, pair: int) -> list:
+    """The CTA-pair GEMM's work for one pair, in order: rows of (tile, row tile,
+    column tile, k-block begin, end, pairs sharing the tile, place in k order,
+    counter pair or -1, partial slot or -1) (host only; see orca.h)."""
+    n = lib().orca_gemm_pair_segments(M, N, K, n_pairs, int(bool(with_split)), pair, None, 0)
+    if n < 0:
+        _check(n)
+    buf = (ctypes.c_int32 * (9 * max(1, n)))()
+    m = lib().orca_gemm_pair_segments(M, N, K, n_pairs, int(bool(with_split)), pair, buf, n)
+    if m != n:
+        raise OrcaError(ORCA_EINVAL, f"orca_gemm_pair_segments: {m} segments, expected {n}")
+    return [tuple(buf[9 * i:9 * i + 9]) for i in range(n)]
 
 
 def orca_profile_enable(eng, mode: int) -> None:

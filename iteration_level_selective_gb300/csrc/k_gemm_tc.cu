@@ -39,6 +39,7 @@
 
 #include "async_copy.cuh"
 #include "epilogue.cuh"
+#include "orca.h"
 #include "orca_internal.h"
 
 namespace orca {
@@ -978,20 +979,20 @@ struct PairSched {
   __host__ __device__ bool split() const { return kind != 0; }
   // pairs that take work (the grid when split)
   __host__ __device__ int busy() const { return kind == 1 ? tiles * S : kind == 2 ? P : min(tiles, P); }
-  __device__ __forceinline__ long long start(int p) const { return (long long)p * W / P; }
+  __host__ __device__ __forceinline__ long long start(int p) const { return (long long)p * W / P; }
   // the pair whose stream range holds k-block x (no range is empty: every one
   // has at least kPairMinRange k-blocks)
-  __device__ __forceinline__ int owner(long long x) const { return (int)(((x + 1) * P + W - 1) / W) - 1; }
-  __device__ __forceinline__ void unit(int u, int &m, int &n) const {
+  __host__ __device__ __forceinline__ int owner(long long x) const { return (int)(((x + 1) * P + W - 1) / W) - 1; }
+  __host__ __device__ __forceinline__ void unit(int u, int &m, int &n) const {
     const int group = u / (kPairGroupM * nN);
     const int first_m = group * kPairGroupM;
-    const int gm = min(kPairGroupM, nM - first_m);
+    const int gm = kPairGroupM < nM - first_m ? kPairGroupM : nM - first_m;
     const int r = u - group * kPairGroupM * nN;
     m = first_m + r % gm;
     n = r / gm;
   }
   // segment j of pair p; false past its last
-  __device__ __forceinline__ bool segment(int p, int j, PairSeg &g) const {
+  __host__ __device__ __forceinline__ bool segment(int p, int j, PairSeg &g) const {
     g.pieces = 1;
     g.mine = 0;
     g.first = p;
@@ -1007,7 +1008,7 @@ struct PairSched {
       g.pieces = S;
       g.first = g.tile * S;
       g.kb0 = g.mine * kbs;
-      g.kb1 = min(KB, g.kb0 + kbs);
+      g.kb1 = g.kb0 + kbs < KB ? g.kb0 + kbs : KB;
     } else {
       const long long b = start(p), e = start(p + 1);
       const int t0 = (int)(b / KB);
@@ -1015,7 +1016,7 @@ struct PairSched {
       if ((long long)t * KB >= e) return false;
       g.tile = t;
       g.kb0 = j == 0 ? (int)(b - (long long)t0 * KB) : 0;
-      g.kb1 = (int)min((long long)KB, e - (long long)t * KB);
+      g.kb1 = (int)(e - (long long)t * KB < KB ? e - (long long)t * KB : KB);
       g.first = owner((long long)t * KB);
       g.pieces = owner((long long)(t + 1) * KB - 1) - g.first + 1;
       g.mine = p - g.first;
@@ -1024,13 +1025,13 @@ struct PairSched {
     return true;
   }
   // partial slot of piece i (k order) of a shared tile
-  __device__ __forceinline__ int piece_slot(const PairSeg &g, int i) const {
+  __host__ __device__ __forceinline__ int piece_slot(const PairSeg &g, int i) const {
     if (kind == 1) return g.first + i;
     const int q = g.first + i;
     return 2 * q + (start(q) / KB == g.tile ? 0 : 1);
   }
   // arrival counters of a shared tile: [0, 2P) arrivals, [2P, 4P) pieces stored
-  __device__ __forceinline__ int counter(const PairSeg &g, uint32_t rank) const {
+  __host__ __device__ __forceinline__ int counter(const PairSeg &g, uint32_t rank) const {
     return 2 * (kind == 1 ? g.tile : g.first) + (int)rank;
   }
 };
@@ -1490,9 +1491,8 @@ constexpr double kSplitMinWeightBytes = 128.0 * (1 << 20);
 // Output-tile width of the persistent kernel: 256 when those tiles fill the
 // GPU, else the widest of 128 / 64 / 32 whose tiles occupy at least half the
 // SMs (narrower tiles spread a small-M product's weight stream over more SMs).
-int gemm_tile_n(int M, int N, int K) {
+static int gemm_tile_n_sm(int M, int N, int K, int sm) {
   const long long nM = (M + BM - 1) / BM;
-  const int sm = gemm_sm_count();
   if (nM * ((N + 255) / 256) >= sm) return 256;
   // a large weight stream (tens of MB) at a few hundred rows: 256-wide tiles
   // few enough to be split along K over the SMs (persistent split-K)
@@ -1502,6 +1502,7 @@ int gemm_tile_n(int M, int N, int K) {
   if (nM * ((N + 63) / 64) * 2 >= sm) return 64;
   return 32;
 }
+int gemm_tile_n(int M, int N, int K) { return gemm_tile_n_sm(M, N, K, gemm_sm_count()); }
 
 namespace {
 
@@ -1553,34 +1554,34 @@ constexpr int kClusterMinKb = 32;
 // wave of 60 pair tiles against two of single-CTA tiles), the FC1 at 300-384
 // and the QKV at 600 rows 10% faster on single CTAs (2 waves against 3).
 constexpr double kSingleKb = 1.18;
-static double single_waves_cost(int M, int N, int K) {
-  const int bn = gemm_tile_n(M, N, K);
+static double single_waves_cost(int M, int N, int K, int sm) {
+  const int bn = gemm_tile_n_sm(M, N, K, sm);
   const long long tiles = (long long)((M + BM - 1) / BM) * ((N + bn - 1) / bn);
-  const long long waves = (tiles + gemm_sm_count() - 1) / gemm_sm_count();
+  const long long waves = (tiles + sm - 1) / sm;
   return (double)waves * (K / BK) * kSingleKb * (16.0 + bn / 8.0) / 48.0;
 }
-GemmPlan gemm_plan(int M, int N, int K, bool split_scratch) {
+// The plan for a GPU of `sm` SMs (gemm_plan: this device's).
+static GemmPlan gemm_plan_sm(int M, int N, int K, bool split_scratch, int sm) {
   GemmPlan p{};
   const long long pair_tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
-  if (M > BM && K % BK == 0) {
+  if (M > BM && K % BK == 0 && sm >= 2) {
     PairSched ps;
-    ps.init(M, N, K, gemm_sm_count() / 2, split_scratch);
-    const long long pair_waves = (pair_tiles + gemm_sm_count() / 2 - 1) / (gemm_sm_count() / 2);
+    ps.init(M, N, K, sm / 2, split_scratch);
+    const long long pair_waves = (pair_tiles + sm / 2 - 1) / (sm / 2);
     p.split = ps.split();
-    p.pair = p.split || (double)pair_waves * (K / BK) < single_waves_cost(M, N, K);
+    p.pair = p.split || (double)pair_waves * (K / BK) < single_waves_cost(M, N, K, sm);
   }
   if (p.pair) {
     p.bn = kPairBN;
     return p;
   }
-  p.bn = gemm_tile_n(M, N, K);
+  p.bn = gemm_tile_n_sm(M, N, K, sm);
   p.ks = gemm_ks(p.bn, K);
   const int KB = K / BK;
   if (M > BM || M <= 0) return p;
   const int a_box = M <= 64 ? 64 : 128;  // products of <= 64 rows load 64-row A boxes
   p.a_box = a_box;
   if (KB < kClusterMinKb) return p;
-  const int sm = gemm_sm_count();
   double best = 1e30;
   for (int bn : {64, 128}) {
     const int nN = (N + bn - 1) / bn;
@@ -1603,21 +1604,24 @@ GemmPlan gemm_plan(int M, int N, int K, bool split_scratch) {
     }
   }
   if (!p.cluster) {
-    p.bn = gemm_tile_n(M, N, K);
+    p.bn = gemm_tile_n_sm(M, N, K, sm);
     p.ks = gemm_ks(p.bn, K);
   }
   return p;
+}
+GemmPlan gemm_plan(int M, int N, int K, bool split_scratch) {
+  return gemm_plan_sm(M, N, K, split_scratch, gemm_sm_count());
 }
 
 // A small integer naming the plan, below 64: callers pack one per Linear
 // into 6 bits of their CUDA-graph keys (persistent 0..7, cluster 8..39,
 // CTA pair 40, CTA pair with tiles shared out along K 41).
-int gemm_plan_code(int M, int N, int K) {
-  const GemmPlan p = gemm_plan(M, N, K, true);
+static int plan_code_of(const GemmPlan &p) {
   if (p.pair) return p.split ? 41 : 40;
   if (!p.cluster) return bn_code(p.bn) * 2 + (p.a_box == 64 ? 1 : 0);
   return 8 + bn_code(p.bn) * 8 + (p.S == 2 ? 0 : p.S == 4 ? 1 : 2) * 2 + (p.a_box == 64 ? 1 : 0);
 }
+int gemm_plan_code(int M, int N, int K) { return plan_code_of(gemm_plan(M, N, K, true)); }
 
 cudaError_t gemm_prepare() {
   int dev = 0;
@@ -1683,3 +1687,66 @@ cudaError_t launch_gemm_tc_bf16(const OperandMaps &A, const OperandMaps &W, int 
 }
 
 }  // namespace orca
+
+// Host-side views of the planning above (orca.h): no device is touched.
+extern "C" int orca_gemm_plan_query(int32_t M, int32_t N, int32_t K, int32_t n_sms, int32_t with_scratch,
+                                    orca_gemm_plan_info *out) {
+  using namespace orca;
+  if (out == nullptr || M <= 0 || N <= 0 || K <= 0 || K % BK != 0 || n_sms < 2 || n_sms > 4096) return ORCA_EINVAL;
+  const GemmPlan p = gemm_plan_sm(M, N, K, with_scratch != 0, n_sms);
+  orca_gemm_plan_info r{};
+  r.code = plan_code_of(p);
+  if (p.pair) {
+    PairSched sc;
+    sc.init(M, N, K, n_sms / 2, with_scratch != 0);
+    r.kernel = 2;
+    r.tile_m = kPairBM;
+    r.tile_n = kPairBN;
+    r.tiles = sc.tiles;
+    r.k_split = sc.kind;
+    r.ranges = sc.kind == 1 ? sc.S : sc.kind == 2 ? sc.P : 1;
+    r.workers = sc.busy();
+  } else if (p.cluster) {
+    r.kernel = 1;
+    r.tile_m = BM;
+    r.tile_n = p.bn;
+    r.tiles = (N + p.bn - 1) / p.bn;
+    r.ranges = p.S;
+    r.workers = r.tiles * p.S;
+  } else {
+    r.kernel = 0;
+    r.tile_m = BM;
+    r.tile_n = p.bn;
+    r.tiles = ((M + BM - 1) / BM) * ((N + p.bn - 1) / p.bn);
+    r.ranges = 1;
+    r.workers = r.tiles < n_sms ? r.tiles : n_sms;
+  }
+  *out = r;
+  return ORCA_OK;
+}
+
+extern "C" int orca_gemm_pair_segments(int32_t M, int32_t N, int32_t K, int32_t n_pairs, int32_t with_split,
+                                       int32_t pair, int32_t *seg, int32_t max_seg) {
+  using namespace orca;
+  if (M <= 0 || N <= 0 || K <= 0 || K % BK != 0 || n_pairs <= 0 || pair < 0 || pair >= n_pairs || max_seg < 0 ||
+      (max_seg > 0 && seg == nullptr))
+    return ORCA_EINVAL;
+  PairSched sc;
+  sc.init(M, N, K, n_pairs, with_split != 0);
+  PairSeg g;
+  int n = 0;
+  for (int j = 0; sc.segment(pair, j, g); ++j, ++n) {
+    if (n >= max_seg) continue;  // counted, not written
+    int32_t *r = seg + 9 * n;
+    r[0] = g.tile;
+    r[1] = g.m;
+    r[2] = g.n;
+    r[3] = g.kb0;
+    r[4] = g.kb1;
+    r[5] = g.pieces;
+    r[6] = g.mine;
+    r[7] = g.pieces > 1 ? sc.counter(g, 0u) / 2 : -1;
+    r[8] = g.pieces > 1 ? sc.piece_slot(g, g.mine) : -1;
+  }
+  return n;
+}
