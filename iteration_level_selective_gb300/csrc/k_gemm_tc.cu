@@ -1235,13 +1235,16 @@ __global__ void __launch_bounds__(192, 1)
           if (threadIdx.x == 64) {
             *arrived = 0;
             *stored = 0;
+            // the pieces were written by ordinary stores and are read below by
+            // bulk copies (the async proxy)
+            asm volatile("fence.proxy.async.global;" ::: "memory");
           }
           PairSeg nx;
-          if (all_in && !sc.segment(pair, i + 1, nx)) {
+          const int others = g.pieces - 1;
+          if (all_in && others <= kPairRedSlots && !sc.segment(pair, i + 1, nx)) {
             // this pair's last segment: its MMAs are done, so the ring is idle.
-            // The other pieces come in by bulk copies, R runs of 32 columns at
-            // a time (one 16 KB slot per run and piece), all in flight together
-            const int others = g.pieces - 1;
+            // The other pieces come in by bulk copies, R >= 1 runs of 32 columns
+            // at a time (one 16 KB slot per run and piece), all in flight together
             const int R = min(kPairBN / 32, kPairRedSlots / others);
             for (int c0 = 0, round = 0; c0 < kPairBN / 32; c0 += R, ++round) {
               const int nc = min(R, kPairBN / 32 - c0);

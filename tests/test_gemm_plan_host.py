@@ -15,7 +15,7 @@ from iteration_level_selective_gb300 import _orca as C
 
 SHAPES_13B = [(15360, 5120), (5120, 5120), (20480, 5120), (5120, 20480), (50257, 5120)]
 SHAPES_OTHER = [(2304, 768), (768, 3072), (3072, 768), (520, 12288), (1000, 16384), (4000, 10240), (5000, 13440),
-                (20000, 4096), (64, 20480)]
+                (20000, 4096), (64, 20480), (520, 131072)]
 ROWS = [129, 200, 256, 257, 300, 511, 512, 513, 700, 769, 850, 1024, 1100, 2048, 4096]
 
 

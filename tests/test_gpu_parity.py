@@ -75,7 +75,10 @@ def test_argmax_forced_logits_bit_exact(cuda):
                                    # tile (ragged N and K), stream ranges over 79 tiles with 2 pieces a tile
                                    # (ragged N), over 40 tiles in two ragged rows with up to 3 pieces
                                    (200, 5120, 5120), (300, 4096, 16384), (200, 5000, 13440), (250, 20000, 4096),
-                                   (300, 5000, 13440)])
+                                   (300, 5000, 13440),
+                                   # a very long K on three tiles: 25 pieces a tile, more than the ring's slots
+                                   # (the last pair reads them back through registers)
+                                   (200, 520, 131072)])
 @pytest.mark.parametrize("mode", ["store", "gelu", "resid", "f32out"])
 @pytest.mark.parametrize("split", [False, True])
 def test_linear_bf16_tcgen05_vs_fp64(cuda, M, N, K, mode, split):
