@@ -7,7 +7,8 @@
 //   C[m, n] = sum_k A[m, k] * W[n, k]     A: [M, K] bf16, W: [N, K] bf16
 // with fp32 accumulation in tensor memory, then the fused epilogue.
 //
-// Two kernels.  The persistent one: CTAs (one per SM) walk a list of work
+// Three kernels; gemm_plan picks one per Linear.  The persistent one: CTAs
+// (one per SM) walk a list of work
 // units; a unit is one 128 x BN output tile, or one K-range of it when the
 // output has too few tiles to fill the GPU and each tile's weight block is
 // large (split-K).  Tiles are visited in groups of 8 M-tiles so the CTAs
@@ -28,7 +29,11 @@
 //               epilogue.
 // The cluster split-K kernel (further down) serves one 128-row tile with a
 // long K: the K-ranges of an output tile go to the CTAs of one cluster, which
-// exchange their fp32 partials through distributed shared memory.
+// exchange their fp32 partials through distributed shared memory.  The
+// CTA-pair kernel (further down) computes 256 x 256 tiles on the two SMs of a
+// cluster (cta_group::2); for a large weight stream at a few hundred rows
+// its tiles are shared out along K over every pair, the last pair of a tile
+// summing the pieces in k order.
 // Every mbarrier wait is bounded (about 2 s of %globaltimer).  On expiry the
 // CTA sets kStatusWaitTimeout and an abort flag that ends every other wait at
 // once; the roles then skip their work but keep their barrier sequence, and
