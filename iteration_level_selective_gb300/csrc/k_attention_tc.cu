@@ -8,8 +8,9 @@
 //
 // One pass over the key tiles (128 keys each) with an online softmax, the
 // roles of a CTA running as a pipeline:
-//   warp 0     claims items and loads Q, then K and V tiles by TMA into a
-//              ring of stages;
+//   warp 0     claims items and loads Q, then K and V tiles by TMA into two
+//              rings of stages, K one tile ahead of V: a K stage is free
+//              once S of its tile is done, a V stage once P V is;
 //   warp 1     issues the MMAs: S = Q K^T into one of two TMEM buffers, and
 //              O += P V into a TMEM accumulator (V is the B operand as it
 //              lies in the K/V pool, head dim contiguous: MN-major);
