@@ -2,6 +2,11 @@
 
     python -m iteration_level_selective_gb300.ncu_summary launches.csv \
         [--traffic profiles/traffic.json --workload gpt2-trace --scale S]
+    python -m iteration_level_selective_gb300.ncu_summary --raw capture_raw.csv
+
+The second form reads the raw page of a capture (``ncu -i X.ncu-rep --page raw
+--csv > capture_raw.csv``) and prints the figures the profile summaries quote,
+one column per captured launch.
 
 prints one markdown row per kernel (launches, total device time, share,
 average time, DRAM bytes per launch when the capture has the
@@ -149,14 +154,89 @@ def traffic_by_class(per, scale: float = 1.0):
     return res
 
 
+# (label, metric name, scale to the printed unit: None = print as captured)
+RAW_ROWS = (
+    ("duration (us)", "gpu__time_duration.sum", _TIME),
+    ("SM clock (GHz)", "sm__cycles_elapsed.avg.per_second", None),
+    ("tensor pipe active, % of elapsed", "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed", None),
+    ("XU pipe (exp), % of active", "sm__inst_executed_pipe_xu.avg.pct_of_peak_sustained_active", None),
+    ("ALU pipe, % of active", "sm__inst_executed_pipe_alu.avg.pct_of_peak_sustained_active", None),
+    ("warps active, % of peak", "sm__warps_active.avg.pct_of_peak_sustained_active", None),
+    ("SM throughput, %", "sm__throughput.avg.pct_of_peak_sustained_elapsed", None),
+    ("DRAM throughput, % of peak", "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed", None),
+    ("DRAM bytes per second", "dram__bytes.sum.per_second", None),
+    ("DRAM read (GB)", "dram__bytes_read.sum", _BYTES),
+    ("DRAM write (GB)", "dram__bytes_write.sum", _BYTES),
+    ("L2 hit rate, %", "lts__t_sector_hit_rate.pct", None),
+    ("grid", "launch__grid_size", None),
+    ("block", "launch__block_size", None),
+    ("cluster", "launch__cluster_dim_x", None),
+    ("registers / thread", "launch__registers_per_thread", None),
+    ("dynamic shared memory", "launch__shared_mem_per_block_dynamic", None),
+)
+STALL = "smsp__pcsamp_warps_issue_stalled_"
+
+
+def _num(v: str) -> float:
+    return float(v.replace(",", ""))
+
+
+def raw_summary(text: str) -> str:
+    """Markdown table of RAW_ROWS (and the three largest sampled warp-stall
+    reasons) from an ncu raw-page CSV: header row, units row, one row per
+    launch."""
+    rows = list(csv.reader(io.StringIO(text)))
+    rows = [r for r in rows if r]
+    head, units, data = rows[0], rows[1], rows[2:]
+    col = {k: i for i, k in enumerate(head)}
+    names = [short_name(r[col["Kernel Name"]]) if "Kernel Name" in col else f"launch {j}" for j, r in enumerate(data)]
+    out = ["| metric | " + " | ".join(names) + " |", "|---|" + "---|" * len(data)]
+    for label, key, conv in RAW_ROWS:
+        if key not in col:
+            continue
+        cells = []
+        for r in data:
+            v, u = r[col[key]], units[col[key]].strip()
+            try:
+                x = _num(v)
+            except ValueError:
+                cells.append(v)
+                continue
+            if conv is _TIME:
+                x *= _TIME.get(u.lower(), 1.0) * 1e3   # -> us
+            elif conv is _BYTES:
+                x *= _BYTES.get(u.lower(), 1.0) / 1e9  # -> GB
+            cells.append(f"{x:.4g}" + ("" if conv is not None or not u else f" {u}"))
+        out.append(f"| {label} | " + " | ".join(cells) + " |")
+    stalls = [k for k in head if k.startswith(STALL) and not k.endswith("_not_issued")]
+    if stalls:
+        cells = []
+        for r in data:
+            vals = []
+            for k in stalls:
+                try:
+                    vals.append((_num(r[col[k]]), k[len(STALL):]))
+                except ValueError:
+                    pass
+            top = sorted(vals, reverse=True)[:3]
+            cells.append(", ".join(f"{n} {int(c)}" for c, n in top))
+        out.append("| top sampled stall reasons | " + " | ".join(cells) + " |")
+    return "\n".join(out)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("csv")
+    ap.add_argument("--raw", action="store_true", help="the csv is a capture's raw page (ncu -i --page raw --csv)")
     ap.add_argument("--traffic", help="JSON file to record per-launch DRAM bytes in")
     ap.add_argument("--workload", default="gpt2-trace")
     ap.add_argument("--scale", type=float, default=1.0)
     ap.add_argument("--note", default="")
     args = ap.parse_args(argv)
+    if args.raw:
+        with open(args.csv) as f:
+            print(raw_summary(f.read()))
+        return 0
     per = summarise(read_launches(args.csv))
     print(markdown(per))
     if args.traffic:

@@ -74,3 +74,24 @@ def test_short_name_of_the_names_ncu_prints():
         "gemm_tc_pair_kernel"
     assert ns.short_name("void orca::<unnamed>::gemm_tc_pair_kernel<true>(CUtensorMap_st, CUtensorMap_st, int)") == \
         "gemm_tc_pair_kernel"
+
+
+RAW = """"ID","Kernel Name","gpu__time_duration.sum","sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed","dram__bytes_read.sum","launch__grid_size","smsp__pcsamp_warps_issue_stalled_wait","smsp__pcsamp_warps_issue_stalled_long_scoreboard","smsp__pcsamp_warps_issue_stalled_long_scoreboard_not_issued","smsp__pcsamp_warps_issue_stalled_barrier"
+"","","msecond","%","Mbyte","","warp","warp","warp","warp"
+"0","void orca::<unnamed>::prefill_attention_tc_kernel<128>(CUtensorMap_st, TcAttnArgs)","0.6276","31.37","788.8","152","6,699","15,273","14,000","735"
+"""
+
+
+def test_raw_page_summary():
+    """The raw-page summary converts the units the capture states and ranks
+    the sampled stall reasons (the *_not_issued subsets left out)."""
+    from iteration_level_selective_gb300 import ncu_summary as ns
+    t = ns.raw_summary(RAW)
+    lines = t.splitlines()
+    assert lines[0] == "| metric | prefill_attention_tc_kernel |"
+    row = {l.split("|")[1].strip(): l.split("|")[2].strip() for l in lines[2:]}
+    assert row["duration (us)"] == "627.6"
+    assert row["DRAM read (GB)"] == "0.7888"
+    assert row["tensor pipe active, % of elapsed"] == "31.37 %"
+    assert row["grid"] == "152"
+    assert row["top sampled stall reasons"] == "long_scoreboard 15273, wait 6699, barrier 735"
